@@ -1,0 +1,162 @@
+"""CPU oracle for the YOCO token-mixing path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline arm of
+``bench.py`` may import this package.  The CUDA library never imports, links or
+calls it, and it shares no code with the CUDA library.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64 accumulation); this module
+only marshals numpy arrays to it.  Every function widens its inputs to fp64
+exactly (bf16 bit patterns and fp32 values are representable in fp64), so the
+oracle sees the same numbers the GPU path consumes.
+
+Citations (paper: "You Only Cache Once: Decoder-Decoder Architectures for
+Language Models", arXiv:2405.05254v2):
+  * gret_recurrent  -- Section 3.1, Eq. 5; Appendix F RecurrentRetention
+  * gret_parallel   -- Section 3.1, Eq. 4
+  * gret_chunkwise  -- Eq. 6 with consistent indices (close-reading notes
+                       Section 2.3; slides backup "chunkwise recurrence with
+                       consistent indices"); Appendix F ChunkwiseRetention
+  * rmsnorm_proj    -- Section 2.2, Eq. 2 (LN = RMSNorm)
+  * kv_append_bf16  -- Section 2.2 (one cache, written once, shared by layers)
+  * cross_attn      -- Section 2.2, Eq. 3 (causal, grouped-query softmax)
+
+Parity status: every function here is pinned by tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+
+
+def lib():
+    """Load the compiled oracle, building it first if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            from . import build as _b
+            _b.build()
+        L = ctypes.CDLL(_LIB_PATH)
+        i, d, i64 = ctypes.c_int, ctypes.c_double, ctypes.c_int64
+        L.oracle_gate.argtypes = [d, d]
+        L.oracle_gate.restype = d
+        L.oracle_gret_recurrent.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, d, _dp, _dp, _dp]
+        L.oracle_gret_parallel.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, d, _dp]
+        L.oracle_gret_chunkwise.argtypes = [i, i, i, i, i, i, _dp, _dp, _dp, _dp, d, _dp, _dp, _dp]
+        L.oracle_rmsnorm_proj.argtypes = [i, i, i, _dp, _dp, d, _dp, _dp]
+        L.oracle_round_bf16.argtypes = [d]
+        L.oracle_round_bf16.restype = ctypes.c_uint16
+        L.oracle_kv_append_bf16.argtypes = [i, i, i, i, i64, i64, _dp, _u16p]
+        L.oracle_cross_attn.argtypes = [i, i, i, i, i, i64, _dp, _dp, _dp, i64, d, _dp]
+        for name in ("oracle_gret_recurrent", "oracle_gret_parallel", "oracle_gret_chunkwise",
+                     "oracle_rmsnorm_proj", "oracle_kv_append_bf16", "oracle_cross_attn"):
+            getattr(L, name).restype = None
+        _lib = L
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    """Widen to a contiguous fp64 array (exact for bf16 bits given as float32 and fp32)."""
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_dp)
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> exact fp64 values."""
+    b = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def gate(logit: float, tau: float) -> float:
+    """gamma = sigmoid(logit)^(1/tau), through logsigmoid (Section 3.1 Eq. 4; Appendix F)."""
+    return lib().oracle_gate(float(logit), float(tau))
+
+
+def gret_recurrent(q, k, v, logits, tau, S0=None):
+    """Recurrent gRet (Eq. 5).  q,k [B,N,H,dk], v [B,N,H,dv], logits [B,N,H].
+    Returns (o [B,N,H,dv], S_final [B,H,dk,dv]) in fp64."""
+    q, k, v, lg = _f64(q), _f64(k), _f64(v), _f64(logits)
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    S0 = None if S0 is None else _f64(S0)
+    o = np.zeros((B, N, H, dv))
+    S = np.zeros((B, H, dk, dv))
+    lib().oracle_gret_recurrent(B, N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(lg), float(tau),
+                                _ptr(S0), _ptr(o), _ptr(S))
+    return o, S
+
+
+def gret_parallel(q, k, v, logits, tau):
+    """Parallel gRet (Eq. 4), zero initial state.  O(N^2): small N only."""
+    q, k, v, lg = _f64(q), _f64(k), _f64(v), _f64(logits)
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, N, H, dv))
+    lib().oracle_gret_parallel(B, N, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(lg), float(tau), _ptr(o))
+    return o
+
+
+def gret_chunkwise(q, k, v, logits, tau, chunk, S0=None):
+    """Chunkwise gRet (corrected Eq. 6).  Returns (o, S_final) in fp64."""
+    q, k, v, lg = _f64(q), _f64(k), _f64(v), _f64(logits)
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    S0 = None if S0 is None else _f64(S0)
+    o = np.zeros((B, N, H, dv))
+    S = np.zeros((B, H, dk, dv))
+    lib().oracle_gret_chunkwise(B, N, H, dk, dv, int(chunk), _ptr(q), _ptr(k), _ptr(v), _ptr(lg),
+                                float(tau), _ptr(S0), _ptr(o), _ptr(S))
+    return o, S
+
+
+def rmsnorm_proj(M, W, eps, g=None):
+    """RMSNorm(M) @ W (Eq. 2).  M [..., dm], W [dm, n] -> fp64 [..., n]."""
+    M, W = _f64(M), _f64(W)
+    lead = M.shape[:-1]
+    dm = M.shape[-1]
+    n = W.shape[1]
+    R = int(np.prod(lead)) if lead else 1
+    g = None if g is None else _f64(g)
+    out = np.zeros((R, n))
+    lib().oracle_rmsnorm_proj(R, dm, n, _ptr(M.reshape(R, dm)), _ptr(g), float(eps), _ptr(W), _ptr(out))
+    return out.reshape(*lead, n)
+
+
+def round_bf16(x) -> np.ndarray:
+    """fp64 -> bf16 bits, round to nearest, ties to even (elementwise)."""
+    x = _f64(x)
+    f = lib().oracle_round_bf16
+    return np.array([f(float(t)) for t in x.ravel()], dtype=np.uint16).reshape(x.shape)
+
+
+def kv_append_bf16(cache_bits, kv_new, length):
+    """Expected cache after appending kv_new [B,T,Hkv*d] at slot `length`.
+    cache_bits [B,Hkv,cap,d] uint16 (bf16 bits) is copied, not modified."""
+    c = np.ascontiguousarray(np.array(cache_bits, dtype=np.uint16, copy=True))
+    B, Hkv, cap, d = c.shape
+    kv = _f64(kv_new)
+    T = kv.shape[1]
+    lib().oracle_kv_append_bf16(B, T, Hkv, d, cap, int(length), _ptr(kv), c.ctypes.data_as(_u16p))
+    return c
+
+
+def cross_attn(Q, Kc, Vc, p0, scale):
+    """Causal GQA softmax attention (Eq. 3).  Q [B,T,Hq,d]; Kc, Vc [B,Hkv,cap,d].
+    Row t sits at position p0 + t and reads slots 0..p0+t.  Returns fp64 O."""
+    Q, Kc, Vc = _f64(Q), _f64(Kc), _f64(Vc)
+    B, T, Hq, d = Q.shape
+    Hkv, cap = Kc.shape[1], Kc.shape[2]
+    O = np.zeros((B, T, Hq, d))
+    lib().oracle_cross_attn(B, T, Hq, Hkv, d, cap, _ptr(Q), _ptr(Kc), _ptr(Vc), int(p0), float(scale), _ptr(O))
+    return O

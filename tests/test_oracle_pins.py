@@ -1,0 +1,379 @@
+"""Pins for the CPU oracle: facts the pages or mathematics fix, checked without
+re-using the oracle's own formulas.  CPU only.
+
+Each test names what it pins and where that fact comes from.  Together they
+are meant to fail on any plausible slip in the oracle: a decayed current
+token, a transposed read-out, a wrong chunk index, a missing causal mask, a
+wrong GQA head map, a wrong scale or a wrong rounding.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------- gRet pins
+
+def test_worked_example_2x2():
+    """Blog post Section 4: S_prev = 2I, gamma = 0.5, k = [1,0], v = [3,4]
+    gives S = [[4,4],[0,1]] and q = [1,0] reads o = [4,4].  Pins the update
+    order (decay the old state, add the new outer product undecayed) and the
+    read-out o = q S (S q^T would give [4,0])."""
+    g = _load("worked_example_2x2.json")
+    # gamma = sigmoid(0)^(1/1) = 0.5
+    assert abs(oracle.gate(0.0, 1.0) - g["gamma"]) < 1e-16
+    q = np.array(g["q"]).reshape(1, 1, 1, 2)
+    k = np.array(g["k"]).reshape(1, 1, 1, 2)
+    v = np.array(g["v"]).reshape(1, 1, 1, 2)
+    S0 = np.array(g["S_prev"]).reshape(1, 1, 2, 2)
+    o, S = oracle.gret_recurrent(q, k, v, np.zeros((1, 1, 1)), 1.0, S0=S0)
+    np.testing.assert_allclose(S[0, 0], np.array(g["S_expected"]), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(o[0, 0, 0], np.array(g["o_expected"]), rtol=0, atol=1e-15)
+    # the same step through the chunkwise form (one chunk of one token)
+    o2, S2 = oracle.gret_chunkwise(q, k, v, np.zeros((1, 1, 1)), 1.0, 1, S0=S0)
+    np.testing.assert_allclose(S2[0, 0], np.array(g["S_expected"]), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(o2[0, 0, 0], np.array(g["o_expected"]), rtol=0, atol=1e-15)
+
+
+def test_second_state_from_zero():
+    """Close-reading notes Section 2.2: from S_0 = 0, S_2 = gamma_2 K_1^T V_1 +
+    K_2^T V_2 -- the first token is decayed by the second gate only, the
+    current token not at all (D_nn = 1)."""
+    k = np.array([[1.0, 2.0, 0.0], [0.0, -1.0, 3.0]]).reshape(1, 2, 1, 3)
+    v = np.array([[2.0, 1.0], [-1.0, 4.0]]).reshape(1, 2, 1, 2)
+    q = np.zeros((1, 2, 1, 3))
+    logits = np.array([1.3, -0.4]).reshape(1, 2, 1)
+    tau = 2.0
+    g2 = 1.0 / (1.0 + math.exp(0.4))  # sigmoid(-0.4)
+    g2 = g2 ** (1.0 / tau)
+    expect = np.zeros((3, 2))
+    for i in range(3):
+        for j in range(2):
+            expect[i, j] = g2 * k[0, 0, 0, i] * v[0, 0, 0, j] + k[0, 1, 0, i] * v[0, 1, 0, j]
+    _, S = oracle.gret_recurrent(q, k, v, logits, tau)
+    np.testing.assert_allclose(S[0, 0], expect, rtol=1e-14, atol=1e-14)
+
+
+def _int_qkv(rng, B, N, H, dk, dv, lo=-3, hi=4):
+    q = rng.integers(lo, hi, size=(B, N, H, dk)).astype(np.float64)
+    k = rng.integers(lo, hi, size=(B, N, H, dk)).astype(np.float64)
+    v = rng.integers(lo, hi, size=(B, N, H, dv)).astype(np.float64)
+    return q, k, v
+
+
+def test_gamma_one_is_causal_linear_attention():
+    """gamma == 1 (logit = +inf, logsigmoid = 0 exactly) removes the decay:
+    o_n = q_n sum_{m<=n} k_m^T v_m, causal linear attention.  Integer inputs,
+    so every form must be exact."""
+    rng = np.random.default_rng(1)
+    B, N, H, dk, dv = 2, 37, 3, 5, 4
+    q, k, v = _int_qkv(rng, B, N, H, dk, dv)
+    logits = np.full((B, N, H), np.inf)
+    expect = np.zeros((B, N, H, dv))
+    for b in range(B):
+        for h in range(H):
+            for n in range(N):
+                scores = k[b, : n + 1, h, :] @ q[b, n, h, :]       # (q_n . k_m), m <= n
+                expect[b, n, h] = scores @ v[b, : n + 1, h, :]
+    o_r, _ = oracle.gret_recurrent(q, k, v, logits, 16.0)
+    o_p = oracle.gret_parallel(q, k, v, logits, 16.0)
+    o_c, _ = oracle.gret_chunkwise(q, k, v, logits, 16.0, 8)
+    for o in (o_r, o_p, o_c):
+        assert np.array_equal(o, expect)
+
+
+def test_gamma_zero_keeps_only_current_token():
+    """gamma == 0 (logit = -inf) forgets everything before the current token:
+    o_n = (q_n . k_n) v_n."""
+    rng = np.random.default_rng(2)
+    B, N, H, dk, dv = 1, 19, 2, 4, 3
+    q, k, v = _int_qkv(rng, B, N, H, dk, dv)
+    logits = np.full((B, N, H), -np.inf)
+    expect = np.einsum("bnhd,bnhd->bnh", q, k)[..., None] * v
+    o_r, _ = oracle.gret_recurrent(q, k, v, logits, 16.0)
+    o_p = oracle.gret_parallel(q, k, v, logits, 16.0)
+    o_c, _ = oracle.gret_chunkwise(q, k, v, logits, 16.0, 4)
+    for o in (o_r, o_p, o_c):
+        assert np.array_equal(o, expect)
+
+
+def test_constant_gate_is_fixed_decay_retention():
+    """A constant gate gamma makes D_nm = gamma^(n-m): the fixed-decay
+    retention matrix (paper Section 3.1 builds gRet on retention).  Built
+    here with matrix powers, not gate products."""
+    rng = np.random.default_rng(3)
+    B, N, H, dk, dv = 1, 23, 1, 6, 5
+    q = rng.standard_normal((B, N, H, dk))
+    k = rng.standard_normal((B, N, H, dk))
+    v = rng.standard_normal((B, N, H, dv))
+    x, tau = 0.7, 3.0
+    gam = (1.0 / (1.0 + math.exp(-x))) ** (1.0 / tau)
+    logits = np.full((B, N, H), x)
+    n = np.arange(N)
+    D = np.where(n[:, None] >= n[None, :], gam ** (n[:, None] - n[None, :]).clip(min=0), 0.0)
+    A = q[0, :, 0, :] @ k[0, :, 0, :].T
+    expect = (A * D) @ v[0, :, 0, :]
+    o_r, _ = oracle.gret_recurrent(q, k, v, logits, tau)
+    np.testing.assert_allclose(o_r[0, :, 0, :], expect, rtol=1e-12, atol=1e-12)
+
+
+def test_unrolled_sum_brute_force():
+    """Blog post Section 4 unrolled sum: o_t = sum_i (prod_{j=i+1..t} gamma_j)
+    (q_t k_i^T) v_i, evaluated with pure-Python loops on a tiny case."""
+    rng = np.random.default_rng(4)
+    N, dk, dv = 5, 2, 3
+    q = rng.standard_normal((N, dk))
+    k = rng.standard_normal((N, dk))
+    v = rng.standard_normal((N, dv))
+    x = rng.standard_normal(N) * 2
+    tau = 1.5
+    gam = [(1.0 / (1.0 + math.exp(-xi))) ** (1.0 / tau) for xi in x]
+    expect = np.zeros((N, dv))
+    for t in range(N):
+        for i in range(t + 1):
+            w = 1.0
+            for j in range(i + 1, t + 1):
+                w *= gam[j]
+            qk = sum(q[t, a] * k[i, a] for a in range(dk))
+            for c in range(dv):
+                expect[t, c] += w * qk * v[i, c]
+    sh = lambda a: a.reshape(1, N, 1, -1)
+    lg = x.reshape(1, N, 1)
+    for o in (oracle.gret_recurrent(sh(q), sh(k), sh(v), lg, tau)[0],
+              oracle.gret_parallel(sh(q), sh(k), sh(v), lg, tau),
+              oracle.gret_chunkwise(sh(q), sh(k), sh(v), lg, tau, 2)[0]):
+        np.testing.assert_allclose(o[0, :, 0, :], expect, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("C", [1, 2, 3, 16, 64, 256, 200])
+def test_three_forms_agree(C):
+    """Paper Section 3.1: the parallel, recurrent and chunkwise forms are
+    equivalent.  N = 200 is not a multiple of most C (ragged last chunk)."""
+    B, N, H, dk, dv = 1, 200, 2, 8, 6
+    seed = 11
+    q = synth.normal(seed, 1, (B, N, H, dk), "f32") * 0.5
+    k = synth.normal(seed, 2, (B, N, H, dk), "f32") * 0.5
+    v = synth.normal(seed, 3, (B, N, H, dv), "f32")
+    logits = synth.normal(seed, 4, (B, N, H), "f32", mean=1.0, std=2.0)
+    tau = 4.0
+    o_r, S_r = oracle.gret_recurrent(q, k, v, logits, tau)
+    o_c, S_c = oracle.gret_chunkwise(q, k, v, logits, tau, C)
+    scale = np.abs(o_r).max()
+    np.testing.assert_allclose(o_c, o_r, rtol=0, atol=1e-12 * scale)
+    np.testing.assert_allclose(S_c, S_r, rtol=0, atol=1e-12 * np.abs(S_r).max())
+    if C == 16:
+        o_p = oracle.gret_parallel(q, k, v, logits, tau)
+        np.testing.assert_allclose(o_p, o_r, rtol=0, atol=1e-12 * scale)
+
+
+def test_state_continuation_equals_one_call():
+    """Chunked prefill (blog post Section 6: the prompt is fed in pieces that
+    carry the self-decoder state): two calls with the state carried equal one
+    call, for both the recurrent and the chunkwise form."""
+    B, N, H, d = 2, 150, 2, 4
+    q = synth.normal(5, 1, (B, N, H, d), "f32")
+    k = synth.normal(5, 2, (B, N, H, d), "f32")
+    v = synth.normal(5, 3, (B, N, H, d), "f32")
+    lg = synth.normal(5, 4, (B, N, H), "f32")
+    o_full, S_full = oracle.gret_recurrent(q, k, v, lg, 16.0)
+    n1 = 61
+    o1, S1 = oracle.gret_chunkwise(q[:, :n1], k[:, :n1], v[:, :n1], lg[:, :n1], 16.0, 16)
+    o2, S2 = oracle.gret_chunkwise(q[:, n1:], k[:, n1:], v[:, n1:], lg[:, n1:], 16.0, 16, S0=S1)
+    np.testing.assert_allclose(np.concatenate([o1, o2], axis=1), o_full, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(S2, S_full, rtol=0, atol=1e-12)
+
+
+def test_gate_limits_and_value():
+    """gamma = sigmoid(x)^(1/tau): +inf -> 1, -inf -> 0, and a generic value;
+    large |x| must not overflow."""
+    assert oracle.gate(np.inf, 16.0) == 1.0
+    assert oracle.gate(-np.inf, 16.0) == 0.0
+    assert abs(oracle.gate(2.0, 16.0) - (1 / (1 + math.exp(-2.0))) ** (1 / 16)) < 1e-15
+    assert oracle.gate(800.0, 16.0) == 1.0
+    assert 0.0 <= oracle.gate(-800.0, 16.0) < 1e-20
+
+
+# ---------------------------------------------------------- rounding pins
+
+def test_round_bf16_is_nearest_even():
+    """fp64 -> bf16: the result is the nearer of the two bf16 neighbours,
+    ties go to the even pattern; checked by brute force on the neighbours
+    and against an independent implementation (the input generator's)."""
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.standard_normal(3000) * 10.0 ** rng.integers(-30, 30, 3000),
+                        [1.0, -2.5, 0.0, 3.0e38, 1e-40]])
+    bits = oracle.round_bf16(x)
+    val = synth.bf16_bits_to_f32(bits).astype(np.float64)
+    for xi, vi, bi in zip(x, val, bits):
+        bi = int(bi)
+        mag = bi & 0x7FFF
+        # neighbours of the chosen value on both sides (same sign, magnitude +-1 ulp)
+        for s in (-1, 1):
+            if 0 <= mag + s < 0x7F80:
+                n = float(synth.bf16_bits_to_f32(np.array([(bi & 0x8000) | (mag + s)], dtype=np.uint16))[0])
+                assert abs(xi - vi) <= abs(xi - n)
+                if abs(xi - vi) == abs(xi - n) and xi != vi:
+                    assert mag % 2 == 0
+    # exact ties: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 -> even (1.0)
+    assert oracle.round_bf16(np.array([1.0 + 2 ** -8]))[0] == 0x3F80
+    assert oracle.round_bf16(np.array([1.0 + 3 * 2 ** -8]))[0] == 0x3F82
+    assert np.array_equal(bits, synth.f64_to_bf16_bits(x))
+    assert oracle.round_bf16(np.array([1e39]))[0] == 0x7F80
+
+
+# ---------------------------------------------------------- shared KV pins
+
+def test_rmsnorm_closed_forms():
+    """Eq. 2 with LN = RMSNorm.  A row of +-1 has rms 1, so with eps = 0 the
+    projection is M W exactly (dyadic W keeps every sum exact); scaling a row
+    by a > 0 leaves the eps = 0 output unchanged; the gain multiplies input
+    features."""
+    dm, n = 64, 12
+    M = synth.signs(9, 1, (5, dm)).astype(np.float64)
+    W = synth.dyadic(9, 2, (dm, n)).astype(np.float64)
+    expect = np.zeros((5, n))
+    for r in range(5):
+        for c in range(n):
+            expect[r, c] = sum(M[r, i] * W[i, c] for i in range(dm))
+    out = oracle.rmsnorm_proj(M, W, 0.0)
+    assert np.array_equal(out, expect)
+    out2 = oracle.rmsnorm_proj(M * 3.75, W, 0.0)
+    assert np.array_equal(out2, expect)
+    g = np.zeros(dm)
+    g[5] = 2.0
+    out3 = oracle.rmsnorm_proj(M, W, 0.0, g=g)
+    assert np.array_equal(out3, 2.0 * M[:, 5:6] * W[5:6, :])
+    # constant row c: rms = |c| -> r = 1/sqrt(c^2 + eps)
+    c, eps = 0.5, 0.75
+    out4 = oracle.rmsnorm_proj(np.full((1, dm), c), W, eps)
+    np.testing.assert_allclose(out4[0], c / math.sqrt(c * c + eps) * W.sum(axis=0), rtol=1e-14, atol=1e-15)
+
+
+def test_kv_append_touches_only_new_slots():
+    """Section 2.2: the cache gets row t of each new token at slot len + t of
+    every kv head (head h takes columns h*d..h*d+d-1); nothing else changes."""
+    B, Hkv, cap, d, T, length = 2, 3, 10, 4, 3, 5
+    rng = np.random.default_rng(3)
+    cache = rng.integers(0, 0xFFFF, size=(B, Hkv, cap, d)).astype(np.uint16)
+    # values exactly representable in bf16 that encode (b, t, h, c)
+    kv = np.zeros((B, T, Hkv * d))
+    for b in range(B):
+        for t in range(T):
+            for h in range(Hkv):
+                for c in range(d):
+                    kv[b, t, h * d + c] = 64 * b + 16 * t + 4 * h + c
+    new = oracle.kv_append_bf16(cache, kv, length)
+    for b in range(B):
+        for h in range(Hkv):
+            for s in range(cap):
+                for c in range(d):
+                    if length <= s < length + T:
+                        val = synth.bf16_bits_to_f32(np.array([new[b, h, s, c]]))[0]
+                        assert val == 64 * b + 16 * (s - length) + 4 * h + c
+                    else:
+                        assert new[b, h, s, c] == cache[b, h, s, c]
+
+
+def test_shared_cache_bytes_teaching_numbers():
+    """Blog post Sections 2 and 7: 2*B*N*L*H_kv*d_h*b bytes; 26 per-layer
+    caches are 13 GiB at 128 Ki tokens, the one shared cache 0.5 GiB -- the
+    shared cache does not grow with the number of cross layers."""
+    g = _load("shared_cache_bytes.json")
+    per_layer = 2 * g["B"] * g["N"] * g["layers"] * g["Hkv"] * g["d"] * g["bytes_per_elem"]
+    assert per_layer == g["per_layer_cache_GiB"] * 2 ** 30
+    # the append oracle writes one K and one V slot per token regardless of layers
+    B, Hkv, d = 1, 2, 4
+    cache = np.zeros((B, Hkv, 8, d), dtype=np.uint16)
+    touched = (oracle.kv_append_bf16(cache, np.ones((B, 3, Hkv * d)), 0) != 0).sum()
+    assert touched == B * 3 * Hkv * d
+    shared = 2 * g["B"] * g["N"] * g["Hkv"] * g["d"] * g["bytes_per_elem"]
+    assert shared == g["shared_cache_GiB"] * 2 ** 30
+
+
+# ------------------------------------------------------ attention pins
+
+def test_attention_single_key_and_equal_keys():
+    """Softmax over one key returns its value; over equal scores it is the
+    mean of the values (Eq. 3)."""
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, d, cap = 1, 4, 2, 8, 6
+    K = rng.standard_normal((B, Hkv, cap, d))
+    V = rng.standard_normal((B, Hkv, cap, d))
+    Q = rng.standard_normal((B, 1, Hq, d))
+    O = oracle.cross_attn(Q, K, V, 0, 0.3)
+    for h in range(Hq):
+        assert np.array_equal(O[0, 0, h], V[0, h // 2, 0])
+    Keq = np.repeat(K[:, :, :1], cap, axis=2)
+    O2 = oracle.cross_attn(Q, Keq, V, cap - 1, 0.3)
+    for h in range(Hq):
+        np.testing.assert_allclose(O2[0, 0, h], V[0, h // 2].mean(axis=0), rtol=1e-14, atol=1e-14)
+
+
+def test_attention_two_keys_closed_form_and_gqa_map():
+    """Two keys: o = v0 + sigmoid(s1 - s0) (v1 - v0) with s = scale q.k.
+    Distinct kv heads pin the grouped map kv = h // (Hq / Hkv)."""
+    B, Hq, Hkv, d = 1, 6, 3, 4
+    rng = np.random.default_rng(6)
+    K = rng.standard_normal((B, Hkv, 2, d))
+    V = rng.standard_normal((B, Hkv, 2, d))
+    Q = rng.standard_normal((B, 1, Hq, d))
+    scale = 0.37
+    O = oracle.cross_attn(Q, K, V, 1, scale)
+    for h in range(Hq):
+        g = h // 2
+        s0 = scale * float(Q[0, 0, h] @ K[0, g, 0])
+        s1 = scale * float(Q[0, 0, h] @ K[0, g, 1])
+        w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+        np.testing.assert_allclose(O[0, 0, h], V[0, g, 0] + w1 * (V[0, g, 1] - V[0, g, 0]), rtol=1e-13, atol=1e-14)
+
+
+def test_attention_causal_mask_and_prefill_rows():
+    """Causal mask (Eq. 3; notes Section 2.1: position n reads m <= n): a key
+    after the query's position cannot change its output, and prefill row t
+    equals a single query at p0 + t."""
+    rng = np.random.default_rng(8)
+    B, Hq, Hkv, d, cap = 2, 4, 1, 8, 12
+    K = rng.standard_normal((B, Hkv, cap, d))
+    V = rng.standard_normal((B, Hkv, cap, d))
+    Q = rng.standard_normal((B, 5, Hq, d))
+    p0 = 4
+    O = oracle.cross_attn(Q, K, V, p0, 0.25)
+    K2 = K.copy()
+    V2 = V.copy()
+    K2[:, :, p0 + 5:] = 1e3
+    V2[:, :, p0 + 5:] = -7.0
+    assert np.array_equal(O, oracle.cross_attn(Q, K2, V2, p0, 0.25))
+    for t in range(5):
+        Ot = oracle.cross_attn(Q[:, t:t + 1], K, V, p0 + t, 0.25)
+        np.testing.assert_allclose(Ot[:, 0], O[:, t], rtol=1e-14, atol=1e-15)
+
+
+def test_attention_brute_force_pure_python():
+    """Naive softmax attention in pure Python (math.exp) on a tiny input."""
+    rng = np.random.default_rng(9)
+    B, Hq, Hkv, d, cap, T, p0 = 1, 2, 1, 3, 5, 2, 2
+    K = rng.standard_normal((B, Hkv, cap, d))
+    V = rng.standard_normal((B, Hkv, cap, d))
+    Q = rng.standard_normal((B, T, Hq, d))
+    scale = 0.5
+    O = oracle.cross_attn(Q, K, V, p0, scale)
+    for t in range(T):
+        for h in range(Hq):
+            pos = p0 + t
+            e = [math.exp(scale * sum(Q[0, t, h, c] * K[0, 0, m, c] for c in range(d))) for m in range(pos + 1)]
+            z = sum(e)
+            for c in range(d):
+                ref = sum(e[m] / z * V[0, 0, m, c] for m in range(pos + 1))
+                assert abs(O[0, t, h, c] - ref) < 1e-13
