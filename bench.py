@@ -1,0 +1,372 @@
+#!/usr/bin/env python
+"""Throughput of the YOCO token-mixing hot path on one GB300 (per rank).
+
+One step = one YOCO-3B-shaped request with early exit, at the 32K-token
+single-layer gRet shape (B=1, N=32768, 24 heads x 128) stacked to the model's
+13 self-decoder and 13 cross-decoder layers, plus the first generated token:
+
+  prefill  13 x chunkwise gRet over 32768 tokens (per-layer q, k, v, gate logits)
+           shared K^/V^ projection of M [32768, 3072] (RMSNorm, W_K/W_V 3072->8x128)
+           13 x cross attention for the last prompt token (24 q heads, GQA 3:1)
+  token    13 x recurrent gRet step, 1-slot append, 13 x split-KV cross decode
+
+value = prompt tokens per second over the timed steps (inputs resident in HBM),
+e2e   = the same with every step's inputs copied from pinned host memory and the
+        final outputs copied back inside the timed region.
+--impl reference times the CPU oracle on a bounded sample of the same step.
+
+Multi-GPU: replicas only (independent requests per GPU); value sums all ranks.
+"""
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "gRet prefill tok/s + shared-KV decode tok/s (1 GB300), % of TC/HBM roofline"
+SEED = 20240509
+B, N, H, D = 1, 32768, 24, 128
+L_SELF, L_CROSS = 13, 13
+DM, HKV, HQ = 3072, 8, 24
+TAU, EPS = 16.0, 1e-6
+CFG = 2  # stream-id tag of this workload's inputs
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["yoco", "reference"], default="yoco")
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--chunk", type=int, default=0)
+    return p.parse_args()
+
+
+def workload_config(chunk_used):
+    return {"workload": "yoco3b_prefill32k_early_exit_plus_1_token", "B": B, "N": N, "self_layers": L_SELF,
+            "gret_heads": H, "d": D, "chunk": chunk_used, "tau": TAU, "cross_layers": L_CROSS, "Hq": HQ,
+            "Hkv": HKV, "d_model": DM, "gate_logits": "N(2,1)", "qk": "N(0,1)/sqrt(128)", "v_M_Q": "N(0,1)",
+            "W": "N(0,0.02)", "l2": "no flush: each step reads 8.1 GB of inputs (> 129 MB L2)",
+            "parallelism": "replicas"}
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+_CPU_INPUTS = {}
+
+
+def _cpu_inputs(tokens, proj_rows, cross_keys):
+    """Seeded host inputs for the CPU sample (made once per process)."""
+    key = (tokens, proj_rows, cross_keys)
+    if key not in _CPU_INPUTS:
+        import synth
+        sid = synth.stream_id
+        f = synth.bf16_bits_to_f32
+        _CPU_INPUTS[key] = dict(
+            q=f(synth.normal(SEED, sid(CFG, 0, synth.T_Q), (1, tokens, H, D), "bf16", std=D ** -0.5)),
+            k=f(synth.normal(SEED, sid(CFG, 0, synth.T_K), (1, tokens, H, D), "bf16", std=D ** -0.5)),
+            v=f(synth.normal(SEED, sid(CFG, 0, synth.T_V), (1, tokens, H, D), "bf16")),
+            lg=synth.normal(SEED, sid(CFG, 0, synth.T_LOGIT), (1, tokens, H), "f32", mean=2.0),
+            M=f(synth.normal(SEED, sid(CFG, 0, synth.T_M), (proj_rows, DM), "bf16")),
+            W=f(synth.normal(SEED, sid(CFG, 0, synth.T_WK), (DM, 2 * HKV * D), "bf16", std=0.02)),
+            Kc=f(synth.normal(SEED, sid(CFG, 0, synth.T_CACHE_K), (1, HKV, cross_keys, D), "bf16")),
+            Vc=f(synth.normal(SEED, sid(CFG, 0, synth.T_CACHE_V), (1, HKV, cross_keys, D), "bf16")),
+            Qx=f(synth.normal(SEED, sid(CFG, 0, synth.T_QX), (1, 1, HQ, D), "bf16")))
+    return _CPU_INPUTS[key]
+
+
+def cpu_sample(tokens=1024, proj_rows=32, cross_keys=8192):
+    """Time the oracle, as it stands, on a bounded sample of one step and scale
+    it to a whole step.  Returns (seconds per step, description, cores)."""
+    import oracle
+    x = _cpu_inputs(tokens, proj_rows, cross_keys)
+    oracle.lib()
+    t0 = time.perf_counter()
+    oracle.gret_recurrent(x["q"], x["k"], x["v"], x["lg"], TAU)
+    t_gret = (time.perf_counter() - t0) / tokens           # per token, all heads, one layer
+    t0 = time.perf_counter()
+    oracle.rmsnorm_proj(x["M"], x["W"], EPS)
+    t_proj = (time.perf_counter() - t0) / proj_rows         # per row, K and V
+    t0 = time.perf_counter()
+    oracle.cross_attn(x["Qx"], x["Kc"], x["Vc"], cross_keys - 1, D ** -0.5)
+    t_cross = (time.perf_counter() - t0) * (N / cross_keys)  # one row over N keys, one layer
+    step = L_SELF * t_gret * (N + 1) + t_proj * (N + 1) + 2 * L_CROSS * t_cross
+    desc = (f"oracle timed on {tokens} tokens x 24 heads of one gRet layer, {proj_rows} projection rows and one "
+            f"cross row over {cross_keys} keys; scaled linearly to 13 gRet layers x {N + 1} tokens, projection "
+            f"of {N + 1} rows and 26 cross rows over {N} keys")
+    cores = len(os.sched_getaffinity(0))
+    return step, desc, cores
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    times = []
+    for i in range(args.warmup + args.steps):
+        step, desc, cores = cpu_sample()
+        if i >= args.warmup:
+            times.append(step)
+    t = statistics.mean(times)
+    value = N / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(None),
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- GPU arm
+
+class Clocks:
+    """nvidia-smi sampler for the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_gpu(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    import gated_retention_shared_gb300 as Y
+    import synth
+    L = Y.lib
+    dev = torch.device("cuda", local)
+    bf, f32 = torch.bfloat16, torch.float32
+    sid = synth.stream_id
+    seed = SEED + 7919 * rank  # replicas serve different requests
+
+    def normal(shape, dtype, stream, mean=0.0, std=1.0):
+        t = torch.empty(shape, dtype=dtype, device=dev)
+        return synth.fill_normal_(t, seed, stream, mean, std)
+
+    # ---- inputs (HBM resident)
+    q = [normal((B, N, H, D), bf, sid(CFG, l, synth.T_Q), std=D ** -0.5) for l in range(L_SELF)]
+    k = [normal((B, N, H, D), bf, sid(CFG, l, synth.T_K), std=D ** -0.5) for l in range(L_SELF)]
+    v = [normal((B, N, H, D), bf, sid(CFG, l, synth.T_V)) for l in range(L_SELF)]
+    lg = [normal((B, N, H), f32, sid(CFG, l, synth.T_LOGIT), mean=2.0) for l in range(L_SELF)]
+    M = normal((B, N, DM), bf, sid(CFG, 0, synth.T_M))
+    Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
+    Wv = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WV), std=0.02)
+    Qx = [normal((B, 1, HQ, D), bf, sid(CFG, l, synth.T_QX)) for l in range(L_CROSS)]
+    q1 = [normal((B, H, D), bf, sid(CFG, l, synth.T_Q, 1), std=D ** -0.5) for l in range(L_SELF)]
+    k1 = [normal((B, H, D), bf, sid(CFG, l, synth.T_K, 1), std=D ** -0.5) for l in range(L_SELF)]
+    v1 = [normal((B, H, D), bf, sid(CFG, l, synth.T_V, 1)) for l in range(L_SELF)]
+    lg1 = [normal((B, H), f32, sid(CFG, l, synth.T_LOGIT, 1), mean=2.0) for l in range(L_SELF)]
+    M1 = normal((B, 1, DM), bf, sid(CFG, 0, synth.T_M, 1))
+    Qd = [normal((B, HQ, D), bf, sid(CFG, l, synth.T_QX, 1)) for l in range(L_CROSS)]
+    # ---- outputs and state
+    o = [torch.empty(B, N, H, D, dtype=bf, device=dev) for _ in range(L_SELF)]
+    S = [torch.zeros(B, H, D, D, dtype=f32, device=dev) for _ in range(L_SELF)]
+    Ox = [torch.empty(B, 1, HQ, D, dtype=bf, device=dev) for _ in range(L_CROSS)]
+    o1 = [torch.empty(B, H, D, dtype=bf, device=dev) for _ in range(L_SELF)]
+    Od = [torch.empty(B, HQ, D, dtype=bf, device=dev) for _ in range(L_CROSS)]
+    cache = Y.KVCache(B, HKV, D, N + 16, device=dev)
+    cc = ctypes.byref(cache.c)
+    ws_g_n = L.yoco_gret_prefill_workspace_size(B, N, H, D, D, args.chunk, Y.YOCO_BF16)
+    ws_kv_n = L.yoco_shared_kv_workspace_size(B, N, DM, cc)
+    ws_a_n = L.yoco_cross_attn_workspace_size(B, HQ, 1, cc, 0)
+    ws = torch.empty(max(ws_g_n, ws_kv_n, ws_a_n, 256), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    wsp, wsn = P(ws), ws.numel()
+    stream = torch.cuda.current_stream(dev)
+    stp = ctypes.c_void_p(stream.cuda_stream)
+    ev = {}
+
+    def check(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: {L.yoco_last_error().decode()}")
+
+    def step(timed_calls=None):
+        for s in S:
+            s.zero_()
+        cache.len_dev.zero_()
+        cache.c.len_host = 0
+        for l in range(L_SELF):
+            if timed_calls is not None:
+                timed_calls[l][0].record(stream)
+            check(L.yoco_gret_prefill_chunkwise(P(q[l]), P(k[l]), P(v[l]), P(lg[l]), TAU, P(o[l]), P(S[l]), B, N,
+                                                H, D, D, args.chunk, 1, 1, wsp, wsn, stp), "gret prefill")
+            if timed_calls is not None:
+                timed_calls[l][1].record(stream)
+        check(L.yoco_shared_kv_project_append(P(M), None, EPS, P(Wk), P(Wv), N, DM, cc, wsp, wsn, stp), "kv append")
+        for l in range(L_CROSS):
+            check(L.yoco_cross_attn_prefill(P(Qx[l]), HQ, 1, N - 1, cc, D ** -0.5, P(Ox[l]), wsp, wsn, stp),
+                  "cross prefill")
+        for l in range(L_SELF):
+            check(L.yoco_gret_decode_step(P(q1[l]), P(k1[l]), P(v1[l]), P(lg1[l]), TAU, P(S[l]), P(o1[l]), B, H, D,
+                                          D, 1, 1, stp), "gret decode")
+        check(L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, cc, wsp, wsn, stp), "append 1")
+        for l in range(L_CROSS):
+            check(L.yoco_cross_attn_decode(P(Qd[l]), HQ, cc, D ** -0.5, 0, P(Od[l]), wsp, wsn, stp), "cross decode")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    launches0 = L.yoco_launch_count()
+    step()
+    launches_per_step = L.yoco_launch_count() - launches0
+    barrier()
+
+    # ---- timed region: K steps, per-call events around the gRet prefill calls
+    calls = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L_SELF)]
+             for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        barrier()
+        e0.record(stream)
+        for i in range(args.steps):
+            step(calls[i])
+        e1.record(stream)
+        barrier()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    if dist is not None:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t)
+    ms_step = elapsed / args.steps * 1e3
+    value = world * B * N * args.steps / elapsed
+    gret_ms = statistics.mean(c[0].elapsed_time(c[1]) for row in calls for c in row)
+
+    # ---- roofline of the dominant call: chunkwise gRet prefill, one layer
+    gret_bytes = 3 * B * N * H * D * 2 + B * N * H * D * 2 + B * N * H * 4 + 2 * B * H * D * D * 4
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    achieved = gret_bytes / (gret_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "yoco_gret_prefill_chunkwise (one layer: all of its launches)",
+                "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "peak_source": "MEASURED_PEAKS.json hbm_gbs (burst copy)" if "hbm_gbs" in peaks else "fallback",
+                "algorithmic_bytes_per_launch": gret_bytes, "avg_launch_ms": round(gret_ms, 4), "traffic": None}
+
+    # ---- end to end: inputs from pinned host memory, result back to host
+    e2e = e2e_measure(args, torch, stream, step, [q, k, v, lg], [M, q1, k1, v1, lg1, M1, Qx, Qd], [Ox[-1], Od[-1]])
+
+    clocks = clk.summary()
+    out = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+           "config": workload_config(args.chunk if args.chunk else "auto"),
+           "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches_per_step * args.steps),
+           "gpu_launches_per_step": int(launches_per_step), "clocks": clocks}
+    if rank == 0 and not args.no_cpu_baseline:
+        step_s, desc, cores = cpu_sample()
+        out["cpu_baseline"] = {"value": N / step_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                               "sample": desc}
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def e2e_measure(args, torch, stream, step, big_lists, small, results):
+    """Same step with host->device copies of its inputs and a device->host read of
+    its final outputs inside the timed region."""
+    if args.e2e_steps <= 0:
+        return None
+    dev_tensors = [t for lst in big_lists for t in lst]
+    for x in small:
+        dev_tensors.extend(x if isinstance(x, list) else [x])
+    host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_tensors]
+    for h, d in zip(host, dev_tensors):
+        h.copy_(d)
+    res_host = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
+    h2d = sum(t.numel() * t.element_size() for t in dev_tensors)
+    d2h = sum(r.numel() * r.element_size() for r in results)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        for h, d in zip(host, dev_tensors):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, r in zip(res_host, results):
+            h.copy_(r, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / args.e2e_steps
+    return {"value": B * N / t, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": args.e2e_steps, "ms_per_step": t * 1e3}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

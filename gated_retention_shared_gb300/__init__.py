@@ -1,0 +1,212 @@
+"""Python binding of libyoco (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of the method: it reads shapes and device pointers off torch
+tensors, passes them with the current CUDA stream through ctypes, and raises
+on a non-OK status.  All computation runs in the CUDA kernels of
+``_build/libyoco.so``; there is no fallback.  If the library is missing the
+import fails with a message saying how to build it.
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libyoco.so")
+
+YOCO_OK, YOCO_ERR_INVALID_ARG, YOCO_ERR_UNSUPPORTED, YOCO_ERR_CAPACITY, YOCO_ERR_CUDA, YOCO_ERR_TIMEOUT, \
+    YOCO_ERR_WORKSPACE = range(7)
+YOCO_F32, YOCO_BF16 = 0, 1
+
+
+class YocoError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: status {status} ({detail})")
+        self.status = status
+
+
+class _KVCacheC(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("len_dev", ctypes.c_void_p),
+                ("len_host", ctypes.c_int64), ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("capacity", ctypes.c_int64), ("dtype", ctypes.c_int)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libyoco.so not found at {LIB_PATH}; build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_int64
+    cp = ctypes.POINTER(_KVCacheC)
+    sigs = {
+        "yoco_gret_prefill_chunkwise": (i, [vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, i, i, i, vp, sz, vp]),
+        "yoco_gret_prefill_workspace_size": (sz, [i, i, i, i, i, i, i]),
+        "yoco_gret_decode_step": (i, [vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, i, vp]),
+        "yoco_shared_kv_project_append": (i, [vp, vp, f, vp, vp, i, i, cp, vp, sz, vp]),
+        "yoco_shared_kv_workspace_size": (sz, [i, i, i, cp]),
+        "yoco_cross_attn_prefill": (i, [vp, i, i, i64, cp, f, vp, vp, sz, vp]),
+        "yoco_cross_attn_decode": (i, [vp, i, cp, f, i, vp, vp, sz, vp]),
+        "yoco_cross_attn_workspace_size": (sz, [i, i, i, cp, i]),
+        "yoco_status_string": (ctypes.c_char_p, [i]),
+        "yoco_last_error": (ctypes.c_char_p, []),
+        "yoco_version": (i, []),
+        "yoco_launch_count": (ctypes.c_uint64, []),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
+lib = _load()
+EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "yoco_gret_decode_step",
+            "yoco_shared_kv_project_append", "yoco_shared_kv_workspace_size", "yoco_cross_attn_prefill",
+            "yoco_cross_attn_decode", "yoco_cross_attn_workspace_size", "yoco_status_string",
+            "yoco_last_error", "yoco_version", "yoco_launch_count")
+
+
+def _check(status: int, where: str):
+    if status != YOCO_OK:
+        detail = lib.yoco_last_error().decode() or lib.yoco_status_string(status).decode()
+        raise YocoError(status, where, detail)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return YOCO_F32
+    if t.dtype == torch.bfloat16:
+        return YOCO_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def _workspace(nbytes: int, device, workspace):
+    if nbytes == 0:
+        return workspace
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return workspace
+
+
+# ------------------------------------------------------------------ gRet
+
+def yoco_gret_prefill_workspace_size(B, N, H, dk, dv, chunk, dtype) -> int:
+    return lib.yoco_gret_prefill_workspace_size(B, N, H, dk, dv, chunk, dtype)
+
+
+def yoco_gret_prefill_chunkwise(q, k, v, gate_logits, tau, o, state, chunk=0, workspace=None, stream=None):
+    """q, k [B,N,H,dk]; v, o [B,N,H,dv]; gate_logits [B,N,H] fp32; state [B,H,dk,dv] fp32 (in/out)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (gate_logits, "gate_logits"), (o, "o"), (state, "state")):
+        _need(t, n)
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dt(q)
+    ws_n = lib.yoco_gret_prefill_workspace_size(B, N, H, dk, dv, chunk, dt)
+    ws = _workspace(ws_n, q.device, workspace)
+    st = lib.yoco_gret_prefill_chunkwise(_ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), float(tau), _ptr(o),
+                                         _ptr(state), B, N, H, dk, dv, chunk, dt, _dt(o), _ptr(ws),
+                                         0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "yoco_gret_prefill_chunkwise")
+
+
+def yoco_gret_decode_step(q, k, v, gate_logits, tau, state, o, stream=None):
+    """q, k [B,H,dk]; v, o [B,H,dv]; gate_logits [B,H] fp32; state [B,H,dk,dv] fp32 (in/out)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (gate_logits, "gate_logits"), (o, "o"), (state, "state")):
+        _need(t, n)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    st = lib.yoco_gret_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), float(tau), _ptr(state),
+                                   _ptr(o), B, H, dk, dv, _dt(q), _dt(o), _stream(stream))
+    _check(st, "yoco_gret_decode_step")
+
+
+# ------------------------------------------------------------- shared KV
+
+class KVCache:
+    """Caller-side holder of the shared K^/V^ cache: two [B, Hkv, capacity, d]
+    tensors, the device length pair and the C descriptor that points at them."""
+
+    def __init__(self, B, Hkv, d, capacity, dtype=torch.bfloat16, device="cuda", k=None, v=None):
+        self.k = k if k is not None else torch.zeros(B, Hkv, capacity, d, dtype=dtype, device=device)
+        self.v = v if v is not None else torch.zeros(B, Hkv, capacity, d, dtype=dtype, device=device)
+        self.len_dev = torch.zeros(2, dtype=torch.int32, device=self.k.device)
+        self.c = _KVCacheC(self.k.data_ptr(), self.v.data_ptr(), self.len_dev.data_ptr(), 0, B, Hkv, d,
+                           capacity, _dt(self.k))
+
+    @property
+    def length(self) -> int:
+        return int(self.c.len_host)
+
+    def set_length(self, n: int):
+        """Declare the first n slots filled (e.g. after writing k/v directly)."""
+        self.c.len_host = n
+        self.len_dev[0] = n
+
+    @staticmethod
+    def nbytes(B, Hkv, d, capacity, elem_bytes=2) -> int:
+        return 2 * B * Hkv * capacity * d * elem_bytes
+
+
+def yoco_shared_kv_project_append(M, Wk, Wv, cache: KVCache, eps=1e-6, rms_w=None, workspace=None, stream=None):
+    """M [B, T, dm]; Wk, Wv [dm, Hkv*d]; appends T slots to `cache`."""
+    for t, n in ((M, "M"), (Wk, "Wk"), (Wv, "Wv")):
+        _need(t, n)
+    B, T, dm = M.shape
+    ws_n = lib.yoco_shared_kv_workspace_size(B, T, dm, ctypes.byref(cache.c))
+    ws = _workspace(ws_n, M.device, workspace)
+    st = lib.yoco_shared_kv_project_append(_ptr(M), _ptr(rms_w), float(eps), _ptr(Wk), _ptr(Wv), T, dm,
+                                           ctypes.byref(cache.c), _ptr(ws),
+                                           0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "yoco_shared_kv_project_append")
+
+
+# -------------------------------------------------------- cross attention
+
+def yoco_cross_attn_workspace_size(B, Hq, T, cache: KVCache, num_splits=0) -> int:
+    return lib.yoco_cross_attn_workspace_size(B, Hq, T, ctypes.byref(cache.c), num_splits)
+
+
+def yoco_cross_attn_prefill(Q, cache: KVCache, p0, O, scale=None, workspace=None, stream=None):
+    """Q, O [B, T, Hq, d]; rows at positions p0..p0+T-1."""
+    _need(Q, "Q")
+    _need(O, "O")
+    B, T, Hq, d = Q.shape
+    scale = d ** -0.5 if scale is None else scale
+    ws_n = lib.yoco_cross_attn_workspace_size(B, Hq, T, ctypes.byref(cache.c), 0)
+    ws = _workspace(ws_n, Q.device, workspace)
+    st = lib.yoco_cross_attn_prefill(_ptr(Q), Hq, T, int(p0), ctypes.byref(cache.c), float(scale), _ptr(O), _ptr(ws),
+                                     0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "yoco_cross_attn_prefill")
+
+
+def yoco_cross_attn_decode(Q, cache: KVCache, O, scale=None, num_splits=0, workspace=None, stream=None):
+    """Q, O [B, Hq, d]; the query sits at position len - 1."""
+    _need(Q, "Q")
+    _need(O, "O")
+    B, Hq, d = Q.shape
+    scale = d ** -0.5 if scale is None else scale
+    ws_n = lib.yoco_cross_attn_workspace_size(B, Hq, 1, ctypes.byref(cache.c), num_splits)
+    ws = _workspace(ws_n, Q.device, workspace)
+    st = lib.yoco_cross_attn_decode(_ptr(Q), Hq, ctypes.byref(cache.c), float(scale), num_splits, _ptr(O), _ptr(ws),
+                                    0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "yoco_cross_attn_decode")

@@ -1,0 +1,219 @@
+// api.cu -- the C ABI of libyoco: host-side validation, workspace sizing and
+// dispatch to the kernels.  Every check runs before anything is enqueued, so an
+// error status means nothing was launched and nothing was written.
+#include <atomic>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace yoco_host {
+
+static thread_local char g_last_error[512] = "";
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+void set_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+}
+
+static yoco_status fail(yoco_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+static yoco_status cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) {
+        g_last_error[0] = 0;
+        return YOCO_OK;
+    }
+    set_error("%s: %s", what, cudaGetErrorString(e));
+    return YOCO_ERR_CUDA;
+}
+
+static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+static bool valid_dt(yoco_dtype d) { return d == YOCO_F32 || d == YOCO_BF16; }
+
+static yoco_status check_ws(void *ws, size_t have, size_t need) {
+    if (need == 0) return YOCO_OK;
+    if (!ws) return fail(YOCO_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL", need);
+    if (have < need) return fail(YOCO_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", have, need);
+    if (!aligned(ws, 256)) return fail(YOCO_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    return YOCO_OK;
+}
+
+static yoco_status check_cache(const yoco_kv_cache *c) {
+    if (!c) return fail(YOCO_ERR_INVALID_ARG, "cache is NULL");
+    if (!c->k || !c->v || !c->len_dev) return fail(YOCO_ERR_INVALID_ARG, "cache k, v and len_dev must be set");
+    if (!valid_dt(c->dtype)) return fail(YOCO_ERR_INVALID_ARG, "cache dtype invalid");
+    if (c->B <= 0 || c->Hkv <= 0 || c->capacity <= 0)
+        return fail(YOCO_ERR_INVALID_ARG, "cache B, Hkv and capacity must be positive");
+    if (c->d != 64 && c->d != 128) return fail(YOCO_ERR_UNSUPPORTED, "cache head size %d not in {64, 128}", c->d);
+    if (c->len_host < 0 || c->len_host > c->capacity)
+        return fail(YOCO_ERR_INVALID_ARG, "cache length %lld outside [0, capacity]", (long long)c->len_host);
+    if (!aligned(c->k, 16) || !aligned(c->v, 16)) return fail(YOCO_ERR_INVALID_ARG, "cache k/v must be 16-byte aligned");
+    if (c->capacity > (int64_t)INT32_MAX) return fail(YOCO_ERR_UNSUPPORTED, "capacity above 2^31-1");
+    return YOCO_OK;
+}
+
+}  // namespace yoco_host
+
+using namespace yoco_host;
+
+extern "C" {
+
+const char *yoco_status_string(yoco_status s) {
+    switch (s) {
+    case YOCO_OK: return "ok";
+    case YOCO_ERR_INVALID_ARG: return "invalid argument";
+    case YOCO_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case YOCO_ERR_CAPACITY: return "cache capacity exceeded";
+    case YOCO_ERR_CUDA: return "CUDA error";
+    case YOCO_ERR_TIMEOUT: return "on-device wait timed out";
+    case YOCO_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    }
+    return "unknown status";
+}
+
+const char *yoco_last_error(void) { return g_last_error; }
+
+int yoco_version(void) { return YOCO_VERSION; }
+
+uint64_t yoco_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+// ----------------------------------------------------------------------- gRet
+
+static yoco_status check_gret_shapes(int B, int N, int H, int dk, int dv, yoco_dtype in_dt, yoco_dtype out_dt) {
+    if (B <= 0 || H <= 0 || N < 0) return fail(YOCO_ERR_INVALID_ARG, "B, H must be > 0 and N >= 0");
+    if (!valid_dt(in_dt) || !valid_dt(out_dt)) return fail(YOCO_ERR_INVALID_ARG, "dtype invalid");
+    if (in_dt != out_dt) return fail(YOCO_ERR_UNSUPPORTED, "in_dt must equal out_dt");
+    if (dk != dv || (dk != 64 && dk != 128)) return fail(YOCO_ERR_UNSUPPORTED, "need dk == dv in {64, 128}");
+    if ((int64_t)B * N * H * dk > ((int64_t)1 << 40)) return fail(YOCO_ERR_UNSUPPORTED, "tensor too large");
+    return YOCO_OK;
+}
+
+size_t yoco_gret_prefill_workspace_size(int B, int N, int H, int dk, int dv, int chunk, yoco_dtype in_dt) {
+    if (check_gret_shapes(B, N, H, dk, dv, in_dt, in_dt) != YOCO_OK || N == 0) return 0;
+    bool tc = (chunk == 0 || chunk == 128) && gret_tc_eligible(B, N, H, dk, dv, in_dt);
+    return tc ? gret_tc_workspace(B, N, H, dk, dv) : gret_simt_workspace(B, N, H, dk, dv);
+}
+
+yoco_status yoco_gret_prefill_chunkwise(const void *q, const void *k, const void *v, const float *gate_logits,
+                                        float tau, void *o, float *state, int B, int N, int H, int dk, int dv,
+                                        int chunk, yoco_dtype in_dt, yoco_dtype out_dt, void *workspace,
+                                        size_t ws_bytes, void *stream) {
+    yoco_status s = check_gret_shapes(B, N, H, dk, dv, in_dt, out_dt);
+    if (s != YOCO_OK) return s;
+    if (!state) return fail(YOCO_ERR_INVALID_ARG, "state is NULL");
+    if (!(tau > 0.0f) || !isfinite(tau)) return fail(YOCO_ERR_INVALID_ARG, "tau must be finite and > 0");
+    if (chunk != 0 && chunk != 64 && chunk != 128)
+        return fail(YOCO_ERR_UNSUPPORTED, "chunk %d not in {0, 64, 128}", chunk);
+    if (N == 0) return YOCO_OK;
+    if (!q || !k || !v || !gate_logits || !o) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(state, 16))
+        return fail(YOCO_ERR_INVALID_ARG, "q, k, v, o, state must be 16-byte aligned");
+    const bool tc = (chunk == 0 || chunk == 128) && gret_tc_eligible(B, N, H, dk, dv, in_dt);
+    const size_t need = tc ? gret_tc_workspace(B, N, H, dk, dv) : gret_simt_workspace(B, N, H, dk, dv);
+    if ((s = check_ws(workspace, ws_bytes, need)) != YOCO_OK) return s;
+    GretArgs a{q, k, v, gate_logits, tau, o, state, B, N, H, dk, dv, in_dt};
+    cudaStream_t st = (cudaStream_t)stream;
+    return cuda_status(tc ? gret_prefill_tc(a, workspace, st) : gret_prefill_simt(a, workspace, st),
+                       "gret_prefill_chunkwise");
+}
+
+yoco_status yoco_gret_decode_step(const void *q, const void *k, const void *v, const float *gate_logits, float tau,
+                                  float *state, void *o, int B, int H, int dk, int dv, yoco_dtype in_dt,
+                                  yoco_dtype out_dt, void *stream) {
+    yoco_status s = check_gret_shapes(B, 1, H, dk, dv, in_dt, out_dt);
+    if (s != YOCO_OK) return s;
+    if (!q || !k || !v || !gate_logits || !state || !o) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (!(tau > 0.0f) || !isfinite(tau)) return fail(YOCO_ERR_INVALID_ARG, "tau must be finite and > 0");
+    if (!aligned(state, 16)) return fail(YOCO_ERR_INVALID_ARG, "state must be 16-byte aligned");
+    return cuda_status(gret_decode(q, k, v, gate_logits, tau, state, o, B, H, dk, dv, in_dt, (cudaStream_t)stream),
+                       "gret_decode_step");
+}
+
+// ------------------------------------------------------------------ shared KV
+
+size_t yoco_shared_kv_workspace_size(int B, int T, int dm, const yoco_kv_cache *cache) {
+    if (!cache || B <= 0 || T <= 0 || dm <= 0) return 0;
+    return kv_proj_workspace(B, T, dm, cache->Hkv, cache->d, cache->dtype);
+}
+
+yoco_status yoco_shared_kv_project_append(const void *M, const void *rms_w, float eps, const void *Wk,
+                                          const void *Wv, int T, int dm, yoco_kv_cache *cache, void *workspace,
+                                          size_t ws_bytes, void *stream) {
+    yoco_status s = check_cache(cache);
+    if (s != YOCO_OK) return s;
+    if (T <= 0 || dm <= 0) return fail(YOCO_ERR_INVALID_ARG, "T and dm must be > 0");
+    if (!M || !Wk || !Wv) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (!(eps >= 0.0f) || !isfinite(eps)) return fail(YOCO_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (cache->len_host + T > cache->capacity)
+        return fail(YOCO_ERR_CAPACITY, "append of %d tokens at length %lld exceeds capacity %lld", T,
+                    (long long)cache->len_host, (long long)cache->capacity);
+    if ((int64_t)cache->B * T > INT32_MAX) return fail(YOCO_ERR_UNSUPPORTED, "B*T too large");
+    const size_t need = kv_proj_workspace(cache->B, T, dm, cache->Hkv, cache->d, cache->dtype);
+    if ((s = check_ws(workspace, ws_bytes, need)) != YOCO_OK) return s;
+    KvProjArgs a{M, rms_w, Wk, Wv, eps, cache->B, T, dm, cache->Hkv, cache->d, cache->capacity, cache->len_host,
+                 cache->k, cache->v, cache->len_dev, cache->dtype};
+    s = cuda_status(kv_project_append(a, workspace, (cudaStream_t)stream), "shared_kv_project_append");
+    if (s == YOCO_OK) cache->len_host += T;
+    return s;
+}
+
+// ------------------------------------------------------------ cross attention
+
+size_t yoco_cross_attn_workspace_size(int B, int Hq, int T, const yoco_kv_cache *cache, int num_splits) {
+    if (!cache || B <= 0 || Hq <= 0 || T <= 0 || cache->Hkv <= 0) return 0;
+    int splits = num_splits > 0 ? num_splits : attn_auto_splits(B, cache->Hkv, cache->capacity);
+    if (T > 1 && num_splits <= 0) splits = 1;
+    return attn_workspace(B, Hq, T, cache->d, splits);
+}
+
+static yoco_status attn_common(const void *Q, int Hq, int T, int64_t p0, const yoco_kv_cache *cache, float scale,
+                               int num_splits, void *O, void *ws, size_t ws_bytes, void *stream) {
+    yoco_status s = check_cache(cache);
+    if (s != YOCO_OK) return s;
+    if (!Q || !O) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (Hq <= 0 || Hq % cache->Hkv != 0) return fail(YOCO_ERR_UNSUPPORTED, "Hq must be a positive multiple of Hkv");
+    if (Hq / cache->Hkv > 16) return fail(YOCO_ERR_UNSUPPORTED, "at most 16 query heads per kv head");
+    if (T <= 0) return fail(YOCO_ERR_INVALID_ARG, "T must be > 0");
+    if (p0 < 0 || p0 + T > cache->len_host)
+        return fail(YOCO_ERR_INVALID_ARG, "rows at positions [%lld, %lld) are not all in the cache (length %lld)",
+                    (long long)p0, (long long)(p0 + T), (long long)cache->len_host);
+    if (!isfinite(scale)) return fail(YOCO_ERR_INVALID_ARG, "scale must be finite");
+    if (!aligned(Q, 16) || !aligned(O, 16)) return fail(YOCO_ERR_INVALID_ARG, "Q/O must be 16-byte aligned");
+    if (num_splits < 0) return fail(YOCO_ERR_INVALID_ARG, "num_splits must be >= 0");
+    const int64_t keys = p0 + T;
+    int splits = num_splits > 0 ? num_splits : (T == 1 ? attn_auto_splits(cache->B, cache->Hkv, keys) : 1);
+    if (splits > 4096) return fail(YOCO_ERR_UNSUPPORTED, "num_splits above 4096");
+    const size_t need = attn_workspace(cache->B, Hq, T, cache->d, splits);
+    if ((s = check_ws(ws, ws_bytes, need)) != YOCO_OK) return s;
+    AttnArgs a{Q, O, cache->k, cache->v, cache->B, T, Hq, cache->Hkv, cache->d, cache->capacity, p0, scale,
+               cache->dtype};
+    return cuda_status(attn_run(a, splits, ws, (cudaStream_t)stream), "cross_attn");
+}
+
+yoco_status yoco_cross_attn_prefill(const void *Q, int Hq, int T, int64_t p0, const yoco_kv_cache *cache, float scale,
+                                    void *O, void *workspace, size_t ws_bytes, void *stream) {
+    return attn_common(Q, Hq, T, p0, cache, scale, T == 1 ? 0 : 1, O, workspace, ws_bytes, stream);
+}
+
+yoco_status yoco_cross_attn_decode(const void *Q, int Hq, const yoco_kv_cache *cache, float scale, int num_splits,
+                                   void *O, void *workspace, size_t ws_bytes, void *stream) {
+    yoco_status s = check_cache(cache);
+    if (s != YOCO_OK) return s;
+    if (cache->len_host < 1) return fail(YOCO_ERR_INVALID_ARG, "decode needs a non-empty cache");
+    return attn_common(Q, Hq, 1, cache->len_host - 1, cache, scale, num_splits, O, workspace, ws_bytes, stream);
+}
+
+}  // extern "C"

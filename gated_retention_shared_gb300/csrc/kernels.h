@@ -1,0 +1,60 @@
+// kernels.h -- host-side launchers behind the C ABI (internal to libyoco).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "yoco.h"
+
+namespace yoco_host {
+
+struct GretArgs {
+    const void *q, *k, *v;
+    const float *logits;
+    float tau;
+    void *o;
+    float *state;
+    int B, N, H, dk, dv;
+    yoco_dtype in_dt;
+};
+
+// gret_simt.cu
+size_t gret_simt_smem_bytes(int dk);
+size_t gret_simt_workspace(int B, int N, int H, int dk, int dv);
+cudaError_t gret_prefill_simt(const GretArgs &a, void *ws, cudaStream_t st);
+cudaError_t gret_decode(const void *q, const void *k, const void *v, const float *logits, float tau,
+                        float *state, void *o, int B, int H, int dk, int dv, yoco_dtype dt, cudaStream_t st);
+
+// gret_tc.cu (bf16, d = 128, tensor cores)
+bool gret_tc_eligible(int B, int N, int H, int dk, int dv, yoco_dtype dt);
+size_t gret_tc_workspace(int B, int N, int H, int dk, int dv);
+cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st);
+
+// kv_proj.cu
+struct KvProjArgs {
+    const void *M, *rms_w, *Wk, *Wv;
+    float eps;
+    int B, T, dm, Hkv, d;
+    int64_t cap, len;
+    void *kc, *vc;
+    int32_t *len_dev;
+    yoco_dtype dt;
+};
+size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt);
+cudaError_t kv_project_append(const KvProjArgs &a, void *ws, cudaStream_t st);
+
+// attn.cu
+struct AttnArgs {
+    const void *Q;
+    void *O;
+    const void *kc, *vc;
+    int B, T, Hq, Hkv, d;
+    int64_t cap, p0;  // row t sits at position p0 + t
+    float scale;
+    yoco_dtype dt;
+};
+int attn_auto_splits(int B, int Hkv, int64_t keys);
+size_t attn_workspace(int B, int Hq, int T, int d, int splits);
+cudaError_t attn_run(const AttnArgs &a, int splits, void *ws, cudaStream_t st);
+
+}  // namespace yoco_host

@@ -1,0 +1,195 @@
+/*
+ * yoco.h -- C ABI of libyoco, the GB300 (sm_103a) token-mixing path of YOCO
+ * ("You Only Cache Once: Decoder-Decoder Architectures for Language Models",
+ * arXiv:2405.05254v2).
+ *
+ * Two parts of the model are covered:
+ *   - gated retention (gRet), the self-decoder's token mixer
+ *     (paper Section 3.1, Eqs. 4-6; Appendix F);
+ *   - the cross-decoder's causal grouped-query softmax attention against the
+ *     ONE shared K^/V^ cache projected once from the self-decoder output
+ *     (paper Section 2.2, Eqs. 2-3).
+ * Prefill runs the chunkwise gRet form and fills the shared cache, then runs
+ * the cross layers only for the last prompt token; generation runs the
+ * recurrent gRet form and appends one cache slot per token before the cross
+ * layers read it (paper Section 2.3, Fig. 3).
+ *
+ * Conventions common to every call:
+ *   - Every tensor argument is a DEVICE pointer to caller-owned memory, dense
+ *     row-major with the last index fastest.  The library allocates nothing
+ *     on the device, keeps no global state and never frees caller memory.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work on it and return without synchronising.
+ *   - Arguments are validated on the host before anything is enqueued; on
+ *     any error nothing is launched and nothing is written.
+ *   - Status YOCO_ERR_CUDA means a launch failed; yoco_last_error() has the
+ *     CUDA error text.  It is per thread.
+ *   - bf16 tensors hold raw bfloat16 bit patterns (uint16 per element).
+ *   - Gate logits and gRet states are always fp32.
+ */
+#ifndef YOCO_H
+#define YOCO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define YOCO_VERSION 100 /* 1.0.0 */
+
+#if defined(__GNUC__)
+#define YOCO_API __attribute__((visibility("default")))
+#else
+#define YOCO_API
+#endif
+
+typedef enum {
+    YOCO_OK = 0,
+    YOCO_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad position       */
+    YOCO_ERR_UNSUPPORTED = 2, /* head size / dtype / ratio the kernels lack  */
+    YOCO_ERR_CAPACITY = 3,    /* append would pass the cache capacity        */
+    YOCO_ERR_CUDA = 4,        /* a kernel launch or CUDA call failed         */
+    YOCO_ERR_TIMEOUT = 5,     /* a bounded on-device wait gave up            */
+    YOCO_ERR_WORKSPACE = 6    /* workspace missing, too small or misaligned  */
+} yoco_status;
+
+typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1 } yoco_dtype;
+
+/*
+ * The shared K^/V^ cache (paper Section 2.2: projected once from the
+ * self-decoder output, reused by every cross-decoder layer).  One cache per
+ * batch of B sequences that all have the same length.
+ *   k, v      [B, Hkv, capacity, d] of `dtype` (caller-owned device memory)
+ *   len_dev   device int32[2]; [0] = current length, [1] = an internal
+ *             counter that must be 0 before the first append (zero both).
+ *             Appends update [0] on the device, so a captured CUDA graph
+ *             sees the new length on replay.
+ *   len_host  host copy of the length; appends advance it, attention calls
+ *             read it.  The caller keeps it equal to len_dev[0].
+ */
+typedef struct {
+    void *k;
+    void *v;
+    int32_t *len_dev;
+    int64_t len_host;
+    int32_t B;
+    int32_t Hkv;
+    int32_t d;
+    int64_t capacity;
+    yoco_dtype dtype;
+} yoco_kv_cache;
+
+/* ------------------------------------------------------------------ gRet */
+
+/*
+ * Chunkwise gated-retention prefill (paper Section 3.1, Eq. 6 with
+ * consistent indices; Appendix F ChunkwiseRetention), per head:
+ *     gamma_n = sigmoid(logit_n)^(1/tau), taken as exp(logsigmoid(logit)/tau)
+ *     S_n = gamma_n S_{n-1} + k_n^T v_n,    o_n = q_n S_n
+ * evaluated chunk by chunk (intra-chunk decay-masked Q K^T V plus the carried
+ * state).  No 1/sqrt(d) scale and no group norm are applied: o is the raw
+ * retention output.
+ *   q, k         [B, N, H, dk]  in_dt        v  [B, N, H, dv] in_dt
+ *   gate_logits  [B, N, H]      fp32         o  [B, N, H, dv] out_dt
+ *   state        [B, H, dk, dv] fp32, in: the state before token 0 (zero it
+ *                for a fresh sequence), out: the state after token N-1.
+ *   chunk        0 = the kernel's own choice, else 16, 32, 64 or 128; the
+ *                result depends on it only through rounding.
+ *   workspace    device scratch of at least yoco_gret_prefill_workspace_size
+ *                bytes, 256-byte aligned (may be NULL when that size is 0).
+ * Supported: dk = dv in {64, 128}; in_dt = out_dt; N >= 0 (N = 0 leaves
+ * state unchanged); gate logits may be +-inf.
+ * Calls that share `workspace` must be ordered on one stream.
+ */
+YOCO_API yoco_status yoco_gret_prefill_chunkwise(const void *q, const void *k, const void *v,
+                                        const float *gate_logits, float tau, void *o,
+                                        float *state, int B, int N, int H, int dk, int dv,
+                                        int chunk, yoco_dtype in_dt, yoco_dtype out_dt,
+                                        void *workspace, size_t ws_bytes, void *stream);
+
+YOCO_API size_t yoco_gret_prefill_workspace_size(int B, int N, int H, int dk, int dv, int chunk,
+                                        yoco_dtype in_dt);
+
+/*
+ * One recurrent gated-retention step (paper Section 3.1, Eq. 5; Appendix F
+ * RecurrentRetention without its group norm), per head:
+ *     S <- gamma S + k^T v,   o = q S
+ *   q, k [B, H, dk], v [B, H, dv]  in_dt;  gate_logits [B, H] fp32;
+ *   state [B, H, dk, dv] fp32 updated in place;  o [B, H, dv] out_dt.
+ * Supported: dk = dv in {64, 128}.
+ */
+YOCO_API yoco_status yoco_gret_decode_step(const void *q, const void *k, const void *v,
+                                  const float *gate_logits, float tau, float *state, void *o,
+                                  int B, int H, int dk, int dv, yoco_dtype in_dt,
+                                  yoco_dtype out_dt, void *stream);
+
+/* ------------------------------------------------------------- shared KV */
+
+/*
+ * Shared K^/V^ projection and append (paper Section 2.2, Eq. 2):
+ *     K^ = RMSNorm(M) W_K,   V^ = RMSNorm(M) W_V
+ *     RMSNorm(m) = m * g / sqrt(mean(m^2) + eps)
+ * for T new tokens of each of the B sequences, written to cache slots
+ * [len, len + T) of every kv head, after which the length is len + T.
+ *   M      [B, T, dm]       cache dtype
+ *   rms_w  [dm] gain g      cache dtype, or NULL for ones
+ *   Wk, Wv [dm, Hkv * d]    cache dtype; column h*d + c feeds head h, lane c
+ * Exactly slots [len, len + T) change; every other cache byte is untouched.
+ * Returns YOCO_ERR_CAPACITY (nothing written) if len + T > capacity.
+ *   workspace  >= yoco_shared_kv_workspace_size bytes, 256-byte aligned.
+ */
+YOCO_API yoco_status yoco_shared_kv_project_append(const void *M, const void *rms_w, float eps,
+                                          const void *Wk, const void *Wv, int T, int dm,
+                                          yoco_kv_cache *cache, void *workspace,
+                                          size_t ws_bytes, void *stream);
+
+YOCO_API size_t yoco_shared_kv_workspace_size(int B, int T, int dm, const yoco_kv_cache *cache);
+
+/* ------------------------------------------------------- cross attention */
+
+/*
+ * Cross-decoder attention, prefill form (paper Section 2.2, Eq. 3): causal
+ * grouped-query softmax attention of T query rows at positions p0 .. p0+T-1
+ * against the shared cache; row t reads slots 0 .. p0 + t.
+ *     o = sum_m softmax_m(scale * q . k_m) v_m
+ * Query head h reads kv head h / (Hq / Hkv).
+ *   Q, O [B, T, Hq, d] cache dtype.   Requires p0 >= 0, p0 + T <= len.
+ * With early exit (paper Section 2.3, Fig. 3) a prefill calls this with
+ * T = 1 at p0 = len - 1.
+ */
+YOCO_API yoco_status yoco_cross_attn_prefill(const void *Q, int Hq, int T, int64_t p0,
+                                    const yoco_kv_cache *cache, float scale, void *O,
+                                    void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Cross-decoder attention for the newest token of each sequence (position
+ * len - 1, so it reads every slot including its own, which the preceding
+ * append wrote).  Split-KV: num_splits slices of the cache are reduced in
+ * parallel and merged by log-sum-exp; 0 = automatic.
+ *   Q, O [B, Hq, d] cache dtype.   Requires len >= 1.
+ */
+YOCO_API yoco_status yoco_cross_attn_decode(const void *Q, int Hq, const yoco_kv_cache *cache,
+                                   float scale, int num_splits, void *O, void *workspace,
+                                   size_t ws_bytes, void *stream);
+
+/* Workspace bytes for a prefill (T rows) or decode (T = 1) attention call. */
+YOCO_API size_t yoco_cross_attn_workspace_size(int B, int Hq, int T, const yoco_kv_cache *cache,
+                                      int num_splits);
+
+/* ------------------------------------------------------------ utilities */
+
+YOCO_API const char *yoco_status_string(yoco_status s);
+YOCO_API const char *yoco_last_error(void);
+YOCO_API int yoco_version(void);
+
+/* Number of kernels this process has enqueued through libyoco so far
+ * (monotonic, all threads).  A diagnostic for counting launches per step. */
+YOCO_API uint64_t yoco_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* YOCO_H */

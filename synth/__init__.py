@@ -128,3 +128,44 @@ def dyadic(seed: int, stream: int, shape, start: int = 0) -> np.ndarray:
     zero = ((a >> np.uint64(20)) & np.uint64(3)) == 0
     v = np.where(zero, 0.0, sgn * np.ldexp(1.0, -e))
     return v.astype(np.float32).reshape(shape)
+
+
+# ----------------------------------------------------------- device copy
+
+_dev_lib = None
+
+
+def _device_lib():
+    global _dev_lib
+    if _dev_lib is None:
+        import ctypes
+        import os
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libsynth.so")
+        if not os.path.exists(path):
+            raise ImportError(f"{path} missing; run synth/build.py (nvcc)")
+        L = ctypes.CDLL(path)
+        for name in ("synth_normal_bf16", "synth_normal_f32"):
+            fn = getattr(L, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double,
+                           ctypes.c_double, ctypes.c_int64, ctypes.c_void_p]
+        _dev_lib = L
+    return _dev_lib
+
+
+def fill_normal_(t, seed: int, stream: int, mean: float = 0.0, std: float = 1.0, start: int = 0):
+    """Fill a contiguous CUDA tensor (bfloat16 or float32) in place with elements
+    start..start+numel-1 of the stream -- the same values normal() returns."""
+    import ctypes
+    import torch
+    assert t.is_cuda and t.is_contiguous()
+    L = _device_lib()
+    fn = L.synth_normal_bf16 if t.dtype == torch.bfloat16 else L.synth_normal_f32
+    if t.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError(t.dtype)
+    st = torch.cuda.current_stream().cuda_stream
+    rc = fn(ctypes.c_void_p(t.data_ptr()), t.numel(), seed & MASK64, stream & MASK64, float(mean), float(std),
+            int(start), ctypes.c_void_p(st))
+    if rc != 0:
+        raise RuntimeError(f"synth device generator failed with CUDA error {rc}")
+    return t

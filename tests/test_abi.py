@@ -1,0 +1,144 @@
+"""CPU checks of the C ABI: the library loads, exports every entry point the
+header declares, and rejects bad arguments on the host before any launch
+(these calls never reach the GPU, so they run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "yoco.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"YOCO_API\s+[\w\s\*]+?\b(yoco_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def Y():
+    import gated_retention_shared_gb300 as Y
+    return Y
+
+
+def test_header_declares_the_five_calls():
+    syms = declared_symbols()
+    for name in ("yoco_gret_prefill_chunkwise", "yoco_gret_decode_step", "yoco_shared_kv_project_append",
+                 "yoco_cross_attn_prefill", "yoco_cross_attn_decode"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(Y):
+    lib = ctypes.CDLL(Y.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) == set(Y.EXPORTED)
+
+
+def test_status_strings_and_version(Y):
+    assert Y.lib.yoco_version() == 100
+    for s in range(7):
+        assert Y.lib.yoco_status_string(s)
+    assert Y.lib.yoco_status_string(99) == b"unknown status"
+
+
+FAKE = ctypes.c_void_p(0x1000)  # 16-byte aligned non-null; never dereferenced: every call below fails validation
+
+
+def _prefill(Y, B=1, N=8, H=1, dk=64, dv=64, chunk=0, in_dt=1, out_dt=1, tau=16.0, state=FAKE):
+    return Y.lib.yoco_gret_prefill_chunkwise(FAKE, FAKE, FAKE, FAKE, tau, FAKE, state, B, N, H, dk, dv, chunk,
+                                             in_dt, out_dt, None, 0, None)
+
+
+def test_gret_prefill_rejects_bad_arguments(Y):
+    assert _prefill(Y, dk=96, dv=96) == Y.YOCO_ERR_UNSUPPORTED
+    assert _prefill(Y, dk=64, dv=128) == Y.YOCO_ERR_UNSUPPORTED
+    assert _prefill(Y, in_dt=0, out_dt=1) == Y.YOCO_ERR_UNSUPPORTED
+    assert _prefill(Y, in_dt=7, out_dt=7) == Y.YOCO_ERR_INVALID_ARG
+    assert _prefill(Y, B=0) == Y.YOCO_ERR_INVALID_ARG
+    assert _prefill(Y, N=-1) == Y.YOCO_ERR_INVALID_ARG
+    assert _prefill(Y, tau=0.0) == Y.YOCO_ERR_INVALID_ARG
+    assert _prefill(Y, tau=float("nan")) == Y.YOCO_ERR_INVALID_ARG
+    assert _prefill(Y, chunk=48) == Y.YOCO_ERR_UNSUPPORTED
+    assert _prefill(Y, state=None) == Y.YOCO_ERR_INVALID_ARG
+    assert b"state" in Y.lib.yoco_last_error()
+    # N = 0 is a no-op that touches nothing
+    assert _prefill(Y, N=0) == Y.YOCO_OK
+
+
+def test_gret_prefill_workspace_is_checked(Y):
+    need = Y.lib.yoco_gret_prefill_workspace_size(1, 100000, 1, 128, 128, 0, 1)
+    assert need > 0
+    st = Y.lib.yoco_gret_prefill_chunkwise(FAKE, FAKE, FAKE, FAKE, 16.0, FAKE, FAKE, 1, 100000, 1, 128, 128, 0,
+                                           1, 1, None, 0, None)
+    assert st == Y.YOCO_ERR_WORKSPACE
+    st = Y.lib.yoco_gret_prefill_chunkwise(FAKE, FAKE, FAKE, FAKE, 16.0, FAKE, FAKE, 1, 100000, 1, 128, 128, 0,
+                                           1, 1, ctypes.c_void_p(0x1010), need, None)
+    assert st == Y.YOCO_ERR_WORKSPACE  # misaligned
+    st = Y.lib.yoco_gret_prefill_chunkwise(FAKE, FAKE, FAKE, FAKE, 16.0, FAKE, FAKE, 1, 100000, 1, 128, 128, 0,
+                                           1, 1, ctypes.c_void_p(0x1000), need - 1, None)
+    assert st == Y.YOCO_ERR_WORKSPACE  # too small
+
+
+def test_gret_decode_rejects_bad_arguments(Y):
+    L = Y.lib
+    assert L.yoco_gret_decode_step(FAKE, FAKE, FAKE, FAKE, 16.0, FAKE, FAKE, 1, 1, 32, 32, 1, 1, None) == \
+        Y.YOCO_ERR_UNSUPPORTED
+    assert L.yoco_gret_decode_step(None, FAKE, FAKE, FAKE, 16.0, FAKE, FAKE, 1, 1, 64, 64, 1, 1, None) == \
+        Y.YOCO_ERR_INVALID_ARG
+    assert L.yoco_gret_decode_step(FAKE, FAKE, FAKE, FAKE, 16.0, ctypes.c_void_p(0x1004), FAKE, 1, 1, 64, 64, 1, 1,
+                                   None) == Y.YOCO_ERR_INVALID_ARG
+
+
+def _cache(Y, length=0, cap=16, d=64, Hkv=2, B=1, dtype=1):
+    return Y._KVCacheC(0x2000, 0x3000, 0x4000, length, B, Hkv, d, cap, dtype)
+
+
+def test_kv_append_capacity_and_validation(Y):
+    L = Y.lib
+    c = _cache(Y, length=14)
+    need = L.yoco_shared_kv_workspace_size(1, 3, 64, ctypes.byref(c))
+    st = L.yoco_shared_kv_project_append(FAKE, None, 1e-6, FAKE, FAKE, 3, 64, ctypes.byref(c), FAKE, need, None)
+    assert st == Y.YOCO_ERR_CAPACITY
+    assert c.len_host == 14  # unchanged
+    assert b"capacity" in L.yoco_last_error()
+    bad = _cache(Y, d=96)
+    assert L.yoco_shared_kv_project_append(FAKE, None, 1e-6, FAKE, FAKE, 1, 64, ctypes.byref(bad), FAKE, 1 << 20,
+                                           None) == Y.YOCO_ERR_UNSUPPORTED
+    assert L.yoco_shared_kv_project_append(FAKE, None, -1.0, FAKE, FAKE, 1, 64, ctypes.byref(c), FAKE, 1 << 20,
+                                           None) == Y.YOCO_ERR_INVALID_ARG
+    assert L.yoco_shared_kv_project_append(FAKE, None, 1e-6, FAKE, FAKE, 0, 64, ctypes.byref(c), FAKE, 1 << 20,
+                                           None) == Y.YOCO_ERR_INVALID_ARG
+    nolen = Y._KVCacheC(0x2000, 0x3000, 0, 0, 1, 2, 64, 16, 1)
+    assert L.yoco_shared_kv_project_append(FAKE, None, 1e-6, FAKE, FAKE, 1, 64, ctypes.byref(nolen), FAKE, 1 << 20,
+                                           None) == Y.YOCO_ERR_INVALID_ARG
+
+
+def test_cross_attn_validation(Y):
+    L = Y.lib
+    c = _cache(Y, length=10)
+    # rows past the cached length
+    assert L.yoco_cross_attn_prefill(FAKE, 4, 3, 8, ctypes.byref(c), 0.1, FAKE, FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_INVALID_ARG
+    assert L.yoco_cross_attn_prefill(FAKE, 4, 1, -1, ctypes.byref(c), 0.1, FAKE, FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_INVALID_ARG
+    # Hq not a multiple of Hkv
+    assert L.yoco_cross_attn_prefill(FAKE, 3, 1, 0, ctypes.byref(c), 0.1, FAKE, FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_UNSUPPORTED
+    empty = _cache(Y, length=0)
+    assert L.yoco_cross_attn_decode(FAKE, 4, ctypes.byref(empty), 0.1, 0, FAKE, FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_INVALID_ARG
+    assert L.yoco_cross_attn_decode(FAKE, 4, ctypes.byref(c), 0.1, -2, FAKE, FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_INVALID_ARG
+    big = _cache(Y, length=100000, cap=100000, Hkv=1)
+    need = L.yoco_cross_attn_workspace_size(1, 4, 1, ctypes.byref(big), 0)
+    assert need > 0
+    assert L.yoco_cross_attn_decode(FAKE, 4, ctypes.byref(big), 0.1, 0, FAKE, None, 0, None) == \
+        Y.YOCO_ERR_WORKSPACE
+
+
+def test_kv_cache_bytes_match_teaching_numbers(Y):
+    """Blog post Section 7: one shared K/V of 128 Ki tokens x 8 heads x 128 in
+    2-byte elements is 0.5 GiB, whatever the number of cross layers."""
+    assert Y.KVCache.nbytes(1, 8, 128, 131072, 2) == 2 ** 29

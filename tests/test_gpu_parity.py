@@ -1,0 +1,356 @@
+"""GPU parity: every libyoco call against the CPU oracle on the same seeded
+inputs, through the C ABI (the Python binding only marshals arguments).
+
+Tolerances: fp32 paths max-abs <= 1e-4; bf16-input / fp32-accumulate paths
+relative L2 <= 1e-2 per output tensor; the cache append bit-exact where the
+inputs make every sum exact.  Sizes span several chunks / tiles / splits and
+end on ragged tails.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _util import dev_bf16, dev_f32, gen, host_bits, host_f64, max_abs, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+FP32_MAX_ABS = 1e-4
+BF16_REL_L2 = 1e-2
+SEED = synth.DEFAULT_SEED
+
+
+@pytest.fixture(scope="module")
+def Y():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    import gated_retention_shared_gb300 as Y
+    return Y
+
+
+def sid(cfg, layer, tensor, step=0):
+    return synth.stream_id(cfg, layer, tensor, step)
+
+
+def gret_inputs(cfg, B, N, H, d, dtype, logit_mean=0.0, qk_std=None):
+    qk_std = d ** -0.5 if qk_std is None else qk_std
+    q, qd = gen(SEED, sid(cfg, 0, synth.T_Q), (B, N, H, d), dtype, std=qk_std)
+    k, kd = gen(SEED, sid(cfg, 0, synth.T_K), (B, N, H, d), dtype, std=qk_std)
+    v, vd = gen(SEED, sid(cfg, 0, synth.T_V), (B, N, H, d), dtype)
+    lg = synth.normal(SEED, sid(cfg, 0, synth.T_LOGIT), (B, N, H), "f32", mean=logit_mean)
+    return (q, k, v, lg.astype(np.float64)), (qd, kd, vd, dev_f32(lg))
+
+
+def run_prefill(Y, dev_in, B, N, H, d, dtype, S0=None, chunk=0):
+    import torch
+    qd, kd, vd, lgd = dev_in
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    o = torch.empty(B, N, H, d, dtype=tdt, device="cuda")
+    S = torch.zeros(B, H, d, d, dtype=torch.float32, device="cuda") if S0 is None else dev_f32(S0)
+    Y.yoco_gret_prefill_chunkwise(qd, kd, vd, lgd, 16.0, o, S, chunk=chunk)
+    torch.cuda.synchronize()
+    return host_f64(o), S.cpu().numpy().astype(np.float64)
+
+
+# --------------------------------------------------------------- gRet prefill
+
+def test_gret_prefill_fp32_tiny_config(Y):
+    """B=1, N=256, 2 heads x 64, q,k,v ~ N(0,1)/8, logits ~ N(0,1), tau 16, chunk 64."""
+    B, N, H, d = 1, 256, 2, 64
+    host, dev = gret_inputs(1, B, N, H, d, "f32", qk_std=1 / 8)
+    o, S = run_prefill(Y, dev, B, N, H, d, "f32", chunk=64)
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0)
+    assert max_abs(o, o_ref) <= FP32_MAX_ABS
+    assert max_abs(S, S_ref) <= FP32_MAX_ABS
+
+
+@pytest.mark.parametrize("N", [1, 63, 200, 2049])
+def test_gret_prefill_fp32_ragged_with_state(Y, N):
+    """Ragged lengths, B=2, d=128, a non-zero initial state; N=2049 runs the
+    sequence-split path (segment states + scan)."""
+    B, H, d = 2, 3, 128
+    host, dev = gret_inputs(10 + N % 7, B, N, H, d, "f32", logit_mean=2.0)
+    S0 = synth.normal(SEED, sid(11, 0, synth.T_S0), (B, H, d, d), "f32", std=0.1).astype(np.float64)
+    o, S = run_prefill(Y, dev, B, N, H, d, "f32", S0=S0)
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0, S0=S0)
+    assert max_abs(o, o_ref) <= FP32_MAX_ABS
+    assert max_abs(S, S_ref) <= FP32_MAX_ABS
+
+
+def test_gret_prefill_fp32_many_segments(Y):
+    """One head, long sequence: the kernel splits it into many segments."""
+    B, N, H, d = 1, 5000, 1, 64
+    host, dev = gret_inputs(12, B, N, H, d, "f32", logit_mean=3.0)
+    o, S = run_prefill(Y, dev, B, N, H, d, "f32")
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0)
+    assert max_abs(o, o_ref) <= FP32_MAX_ABS
+    assert max_abs(S, S_ref) <= FP32_MAX_ABS
+
+
+@pytest.mark.parametrize("chunk", [0, 64, 128])
+@pytest.mark.parametrize("N", [130, 1500])
+def test_gret_prefill_bf16(Y, N, chunk):
+    B, H, d = 1, 4, 128
+    host, dev = gret_inputs(2, B, N, H, d, "bf16", logit_mean=2.0)
+    o, S = run_prefill(Y, dev, B, N, H, d, "bf16", chunk=chunk)
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0)
+    assert rel_l2(o, o_ref) <= BF16_REL_L2
+    assert rel_l2(S, S_ref) <= BF16_REL_L2
+
+
+def test_gret_prefill_state_continuation(Y):
+    """Two calls with the state carried equal one oracle pass (chunked prefill)."""
+    B, N, H, d = 1, 1500, 2, 128
+    host, dev = gret_inputs(3, B, N, H, d, "bf16", logit_mean=2.0)
+    import torch
+    n1 = 700
+    parts = [tuple(t[:, :n1].contiguous() for t in dev), tuple(t[:, n1:].contiguous() for t in dev)]
+    S = torch.zeros(B, H, d, d, dtype=torch.float32, device="cuda")
+    outs = []
+    for (qd, kd, vd, lgd) in parts:
+        o = torch.empty_like(vd)
+        Y.yoco_gret_prefill_chunkwise(qd, kd, vd, lgd, 16.0, o, S)
+        outs.append(host_f64(o))
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0)
+    assert rel_l2(np.concatenate(outs, axis=1), o_ref) <= BF16_REL_L2
+    assert rel_l2(S.cpu().numpy(), S_ref) <= BF16_REL_L2
+
+
+def test_gret_prefill_gate_limits(Y):
+    """Logits of +inf (gamma = 1) and -inf (gamma = 0) mixed in."""
+    B, N, H, d = 1, 300, 2, 64
+    host, dev = gret_inputs(4, B, N, H, d, "f32")
+    lg = host[3].copy()
+    lg[:, ::7] = np.inf
+    lg[:, 3::11] = -np.inf
+    dev = dev[:3] + (dev_f32(lg),)
+    o, S = run_prefill(Y, dev, B, N, H, d, "f32")
+    o_ref, S_ref = oracle.gret_recurrent(host[0], host[1], host[2], lg, 16.0)
+    assert max_abs(o, o_ref) <= FP32_MAX_ABS
+    assert max_abs(S, S_ref) <= FP32_MAX_ABS
+
+
+def test_gret_prefill_empty_sequence(Y):
+    import torch
+    S = torch.full((1, 2, 64, 64), 0.5, device="cuda")
+    z = torch.empty(1, 0, 2, 64, device="cuda")
+    lg = torch.empty(1, 0, 2, device="cuda")
+    Y.yoco_gret_prefill_chunkwise(z, z, z, lg, 16.0, z, S)
+    torch.cuda.synchronize()
+    assert bool((S == 0.5).all())
+
+
+# ---------------------------------------------------------------- gRet decode
+
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
+def test_gret_decode_steps(Y, dtype, d):
+    """Several recurrent steps from a random state match the oracle."""
+    import torch
+    B, H, steps = 2, 3, 5
+    host, dev = gret_inputs(5, B, steps, H, d, dtype, logit_mean=1.0)
+    S0 = synth.normal(SEED, sid(5, 0, synth.T_S0), (B, H, d, d), "f32", std=0.2).astype(np.float64)
+    S = dev_f32(S0)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    outs = []
+    for t in range(steps):
+        o = torch.empty(B, H, d, dtype=tdt, device="cuda")
+        Y.yoco_gret_decode_step(*(x[:, t].contiguous() for x in dev), 16.0, S, o)
+        outs.append(host_f64(o))
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0, S0=S0)
+    o_gpu = np.stack(outs, axis=1)
+    if dtype == "f32":
+        assert max_abs(o_gpu, o_ref) <= FP32_MAX_ABS
+        assert max_abs(S.cpu().numpy(), S_ref) <= FP32_MAX_ABS
+    else:
+        assert rel_l2(o_gpu, o_ref) <= BF16_REL_L2
+        assert rel_l2(S.cpu().numpy(), S_ref) <= BF16_REL_L2
+
+
+# ------------------------------------------------------------- shared KV
+
+def test_kv_append_bit_exact(Y):
+    """+-1 rows (rms 1), eps 0 and dyadic weights make every sum exact: the
+    cache must equal the oracle's bit for bit, and only the new slots change."""
+    import torch
+    B, dm, Hkv, d, cap = 2, 256, 2, 64, 16
+    rng_bits = np.random.default_rng(0).integers(0, 0x7F7F, size=(B, Hkv, cap, d)).astype(np.uint16)
+    cache = Y.KVCache(B, Hkv, d, cap, k=dev_bf16(rng_bits), v=dev_bf16(rng_bits[::-1].copy()))
+    cache.set_length(3)
+    kref, vref = rng_bits.copy(), rng_bits[::-1].copy()
+    Wk = synth.dyadic(SEED, sid(20, 0, synth.T_WK), (dm, Hkv * d))
+    Wv = synth.dyadic(SEED, sid(20, 0, synth.T_WV), (dm, Hkv * d))
+    Wkd, Wvd = dev_bf16(synth.f64_to_bf16_bits(Wk)), dev_bf16(synth.f64_to_bf16_bits(Wv))
+    length = 3
+    for step, T in enumerate((5, 4)):
+        M = synth.signs(SEED, sid(20, 0, synth.T_M, step), (B, T, dm))
+        Y.yoco_shared_kv_project_append(dev_bf16(synth.f64_to_bf16_bits(M)), Wkd, Wvd, cache, eps=0.0)
+        kref = oracle.kv_append_bf16(kref, oracle.rmsnorm_proj(M, Wk, 0.0), length)
+        vref = oracle.kv_append_bf16(vref, oracle.rmsnorm_proj(M, Wv, 0.0), length)
+        length += T
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(cache.k), kref)
+        assert np.array_equal(host_bits(cache.v), vref)
+        assert cache.length == length and int(cache.len_dev[0]) == length and int(cache.len_dev[1]) == 0
+
+
+def test_kv_append_fp32_and_gain(Y):
+    """fp32 cache (tiny config: dm 128 -> one 64-wide head), with an RMSNorm gain."""
+    import torch
+    B, T, dm, Hkv, d = 1, 256, 128, 1, 64
+    M, Md = gen(SEED, sid(1, 0, synth.T_M), (B, T, dm), "f32")
+    Wk, Wkd = gen(SEED, sid(1, 0, synth.T_WK), (dm, Hkv * d), "f32", std=0.02)
+    Wv, Wvd = gen(SEED, sid(1, 0, synth.T_WV), (dm, Hkv * d), "f32", std=0.02)
+    g, gd = gen(SEED, sid(1, 0, synth.T_RMSW), (dm,), "f32", mean=1.0, std=0.1)
+    cache = Y.KVCache(B, Hkv, d, T + 4, dtype=torch.float32)
+    Y.yoco_shared_kv_project_append(Md, Wkd, Wvd, cache, eps=1e-6, rms_w=gd)
+    torch.cuda.synchronize()
+    kref = oracle.rmsnorm_proj(M, Wk, 1e-6, g=g).reshape(B, T, Hkv, d).transpose(0, 2, 1, 3)
+    vref = oracle.rmsnorm_proj(M, Wv, 1e-6, g=g).reshape(B, T, Hkv, d).transpose(0, 2, 1, 3)
+    assert max_abs(host_f64(cache.k)[:, :, :T], kref) <= FP32_MAX_ABS
+    assert max_abs(host_f64(cache.v)[:, :, :T], vref) <= FP32_MAX_ABS
+    assert bool((cache.k[:, :, T:] == 0).all())
+
+
+def test_kv_append_capacity_error_writes_nothing(Y):
+    import torch
+    B, dm, Hkv, d, cap = 1, 64, 1, 64, 12
+    cache = Y.KVCache(B, Hkv, d, cap)
+    cache.set_length(10)
+    before = cache.k.clone()
+    M = torch.ones(B, 3, dm, dtype=torch.bfloat16, device="cuda")
+    W = torch.ones(dm, Hkv * d, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(Y.YocoError) as e:
+        Y.yoco_shared_kv_project_append(M, W, W, cache)
+    assert e.value.status == Y.YOCO_ERR_CAPACITY
+    torch.cuda.synchronize()
+    assert torch.equal(before, cache.k) and cache.length == 10 and int(cache.len_dev[0]) == 10
+
+
+# ----------------------------------------------------------- cross attention
+
+def fill_cache(Y, B, Hkv, d, cap, length, dtype, cfg):
+    import torch
+    K, Kd = gen(SEED, sid(cfg, 0, synth.T_CACHE_K), (B, Hkv, cap, d), dtype)
+    V, Vd = gen(SEED, sid(cfg, 0, synth.T_CACHE_V), (B, Hkv, cap, d), dtype)
+    cache = Y.KVCache(B, Hkv, d, cap, dtype=Kd.dtype, k=Kd, v=Vd)
+    cache.set_length(length)
+    return K, V, cache
+
+
+def test_cross_attn_prefill_fp32_full_causal(Y):
+    """Tiny config: 256 causal rows, 2 query heads on one 64-wide kv head."""
+    import torch
+    B, Hq, Hkv, d, N = 1, 2, 1, 64, 256
+    K, V, cache = fill_cache(Y, B, Hkv, d, N, N, "f32", 1)
+    Q, Qd = gen(SEED, sid(1, 0, synth.T_QX), (B, N, Hq, d), "f32")
+    O = torch.empty_like(Qd)
+    Y.yoco_cross_attn_prefill(Qd, cache, 0, O)
+    torch.cuda.synchronize()
+    O_ref = oracle.cross_attn(Q, K, V, 0, d ** -0.5)
+    assert max_abs(host_f64(O), O_ref) <= FP32_MAX_ABS
+
+
+@pytest.mark.parametrize("T,p0", [(1, 999), (37, 100), (130, 0)])
+def test_cross_attn_prefill_bf16_gqa(Y, T, p0):
+    import torch
+    B, Hq, Hkv, d = 2, 24, 8, 128
+    length = p0 + T + 5
+    K, V, cache = fill_cache(Y, B, Hkv, d, length + 3, length, "bf16", 3)
+    Q, Qd = gen(SEED, sid(3, 1, synth.T_QX), (B, T, Hq, d), "bf16")
+    O = torch.empty_like(Qd)
+    Y.yoco_cross_attn_prefill(Qd, cache, p0, O)
+    torch.cuda.synchronize()
+    O_ref = oracle.cross_attn(Q, K, V, p0, d ** -0.5)
+    assert rel_l2(host_f64(O), O_ref) <= BF16_REL_L2
+
+
+def test_cross_attn_decode_split_invariance(Y):
+    """The decode result does not depend on the number of key splits."""
+    import torch
+    B, Hq, Hkv, d, length = 2, 24, 8, 128, 3001
+    K, V, cache = fill_cache(Y, B, Hkv, d, length, length, "bf16", 5)
+    Q, Qd = gen(SEED, sid(5, 2, synth.T_QX), (B, Hq, d), "bf16")
+    O_ref = oracle.cross_attn(Q[:, None], K, V, length - 1, d ** -0.5)[:, 0]
+    results = []
+    for splits in (1, 2, 7, 0):
+        O = torch.empty_like(Qd)
+        Y.yoco_cross_attn_decode(Qd, cache, O, num_splits=splits)
+        torch.cuda.synchronize()
+        results.append(host_f64(O))
+        assert rel_l2(results[-1], O_ref) <= BF16_REL_L2
+    for r in results[1:]:
+        assert rel_l2(r, results[0]) <= 1e-2
+
+
+def test_early_exit_matches_full_prefill_last_row(Y):
+    """Early exit (paper Fig. 3): the last prompt row computed alone equals the
+    last row of the full causal prefill."""
+    import torch
+    B, Hq, Hkv, d, N = 1, 6, 2, 64, 300
+    K, V, cache = fill_cache(Y, B, Hkv, d, N, N, "f32", 6)
+    Q, Qd = gen(SEED, sid(6, 0, synth.T_QX), (B, N, Hq, d), "f32")
+    O_full = torch.empty_like(Qd)
+    Y.yoco_cross_attn_prefill(Qd, cache, 0, O_full)
+    O_last = torch.empty(B, 1, Hq, d, device="cuda")
+    Y.yoco_cross_attn_prefill(Qd[:, -1:].contiguous(), cache, N - 1, O_last)
+    torch.cuda.synchronize()
+    assert max_abs(host_f64(O_last)[:, 0], host_f64(O_full)[:, -1]) <= FP32_MAX_ABS
+
+
+# --------------------------------------------------- tiny config end to end
+
+def test_tiny_config_pipeline_fp32(Y):
+    """The whole tiny fp32 configuration: gRet prefill (2 heads x 64, N=256),
+    shared KV from a 128-wide M, 2 cross layers x 2 query heads over all 256
+    rows, then 16 decode steps (recurrent step, append, 2 cross layers)."""
+    import torch
+    B, N, H, d, dm, Hkv, Hq, L, steps = 1, 256, 2, 64, 128, 1, 2, 2, 16
+    host, dev = gret_inputs(1, B, N, H, d, "f32", qk_std=1 / 8)
+    o, S = run_prefill(Y, dev, B, N, H, d, "f32", chunk=64)
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0)
+    assert max_abs(o, o_ref) <= FP32_MAX_ABS
+    M, Md = gen(SEED, sid(1, 0, synth.T_M), (B, N + steps, dm), "f32")
+    Wk, Wkd = gen(SEED, sid(1, 0, synth.T_WK), (dm, d), "f32", std=0.02)
+    Wv, Wvd = gen(SEED, sid(1, 0, synth.T_WV), (dm, d), "f32", std=0.02)
+    cache = Y.KVCache(B, Hkv, d, N + steps, dtype=torch.float32)
+    Y.yoco_shared_kv_project_append(Md[:, :N].contiguous(), Wkd, Wvd, cache, eps=1e-6)
+    Kall = oracle.rmsnorm_proj(M, Wk, 1e-6).reshape(B, N + steps, Hkv, d).transpose(0, 2, 1, 3)
+    Vall = oracle.rmsnorm_proj(M, Wv, 1e-6).reshape(B, N + steps, Hkv, d).transpose(0, 2, 1, 3)
+    for layer in range(L):
+        Q, Qd = gen(SEED, sid(1, layer, synth.T_QX), (B, N, Hq, d), "f32")
+        O = torch.empty_like(Qd)
+        Y.yoco_cross_attn_prefill(Qd, cache, 0, O)
+        torch.cuda.synchronize()
+        assert max_abs(host_f64(O), oracle.cross_attn(Q, Kall, Vall, 0, d ** -0.5)) <= FP32_MAX_ABS
+    Sd = dev_f32(S)
+    S_host = S_ref
+    for t in range(steps):
+        xs, xd = gret_inputs(100 + t, B, 1, H, d, "f32", qk_std=1 / 8)
+        od = torch.empty(B, H, d, device="cuda")
+        Y.yoco_gret_decode_step(*(x[:, 0].contiguous() for x in xd), 16.0, Sd, od)
+        o1, S_host = oracle.gret_recurrent(*xs, 16.0, S0=S_host)
+        Y.yoco_shared_kv_project_append(Md[:, N + t:N + t + 1].contiguous(), Wkd, Wvd, cache, eps=1e-6)
+        torch.cuda.synchronize()
+        assert max_abs(host_f64(od), o1[:, 0]) <= FP32_MAX_ABS
+        for layer in range(L):
+            Q, Qd = gen(SEED, sid(1, layer, synth.T_QX, 1 + t), (B, Hq, d), "f32")
+            O = torch.empty_like(Qd)
+            Y.yoco_cross_attn_decode(Qd, cache, O)
+            torch.cuda.synchronize()
+            O_ref = oracle.cross_attn(Q[:, None], Kall, Vall, N + t, d ** -0.5)[:, 0]
+            assert max_abs(host_f64(O), O_ref) <= FP32_MAX_ABS
+    assert max_abs(Sd.cpu().numpy(), S_host) <= FP32_MAX_ABS
+
+
+def test_device_generator_matches_host(Y):
+    """The device copy of the input generator reproduces the host one."""
+    import torch
+    t = torch.empty(100003, dtype=torch.bfloat16, device="cuda")
+    synth.fill_normal_(t, SEED, sid(2, 3, synth.T_Q), std=0.25, start=17)
+    host = synth.normal(SEED, sid(2, 3, synth.T_Q), (100003,), "bf16", std=0.25, start=17)
+    assert np.mean(host_bits(t) != host) < 1e-4
+    f = torch.empty(5000, dtype=torch.float32, device="cuda")
+    synth.fill_normal_(f, SEED, 99, mean=2.0)
+    assert np.max(np.abs(f.cpu().numpy() - synth.normal(SEED, 99, (5000,), "f32", mean=2.0))) <= 1e-6
