@@ -56,6 +56,7 @@ def _load():
         "yoco_last_error": (ctypes.c_char_p, []),
         "yoco_version": (i, []),
         "yoco_launch_count": (ctypes.c_uint64, []),
+        "yoco_workspace_status": (i, [vp, i, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -68,7 +69,8 @@ lib = _load()
 EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "yoco_gret_decode_step",
             "yoco_shared_kv_project_append", "yoco_shared_kv_workspace_size", "yoco_cross_attn_prefill",
             "yoco_cross_attn_decode", "yoco_cross_attn_workspace_size", "yoco_status_string",
-            "yoco_last_error", "yoco_version", "yoco_launch_count")
+            "yoco_last_error", "yoco_version", "yoco_launch_count",
+            "yoco_workspace_status")
 
 
 def _check(status: int, where: str):
@@ -127,6 +129,12 @@ def yoco_gret_prefill_chunkwise(q, k, v, gate_logits, tau, o, state, chunk=0, wo
                                          _ptr(state), B, N, H, dk, dv, chunk, dt, _dt(o), _ptr(ws),
                                          0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "yoco_gret_prefill_chunkwise")
+
+
+def yoco_workspace_status(workspace, clear=True, stream=None):
+    """Wait for the stream and raise YocoError(YOCO_ERR_TIMEOUT) if a kernel
+    that used `workspace` gave up a bounded on-device wait."""
+    _check(lib.yoco_workspace_status(_ptr(workspace), int(clear), _stream(stream)), "yoco_workspace_status")
 
 
 def yoco_gret_decode_step(q, k, v, gate_logits, tau, state, o, stream=None):

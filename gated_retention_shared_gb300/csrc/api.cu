@@ -88,6 +88,24 @@ const char *yoco_last_error(void) { return g_last_error; }
 
 int yoco_version(void) { return YOCO_VERSION; }
 
+yoco_status yoco_workspace_status(void *workspace, int clear, void *stream) {
+    if (!workspace) return fail(YOCO_ERR_INVALID_ARG, "workspace is NULL");
+    uint32_t word = 0;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e, "workspace_status");
+    const bool hit = (word & 0xFFFFFF00u) == yoco::kErrMagic;
+    if (clear && hit) {
+        e = cudaMemsetAsync(workspace, 0, sizeof(word), st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_status(e, "workspace_status");
+    }
+    if (hit) return fail(YOCO_ERR_TIMEOUT, "a bounded on-device wait gave up (site %u)", word & 0xFFu);
+    g_last_error[0] = 0;
+    return YOCO_OK;
+}
+
 uint64_t yoco_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 // ----------------------------------------------------------------------- gRet

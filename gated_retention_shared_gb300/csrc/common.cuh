@@ -14,6 +14,10 @@ namespace yoco {
 // for every tolerance the path is held to.
 constexpr float kLogGateMin = -30.0f;
 
+// Workspace status word written by a kernel whose bounded wait gave up:
+// kErrMagic | site code.  Anything else means no failure was recorded.
+constexpr uint32_t kErrMagic = 0x59434F00u;
+
 typedef uint16_t bf16_t;  // raw bfloat16 bits
 
 __device__ __forceinline__ float to_f32(float x) { return x; }

@@ -314,6 +314,12 @@ static cudaError_t run_simt(const GretArgs &a, int P, int seg_len, float *ws, cu
     return launch_chunk<Tin, Tout, DK, true>(a, E, nullptr, nullptr, seg_len, P, st);
 }
 
+cudaError_t gret_scan_launch(float *E, const float *G, float *state, int BH, int P, int DD, cudaStream_t st) {
+    dim3 g2((unsigned)((DD + 255) / 256), BH);
+    gret_segment_scan<<<g2, 256, 0, st>>>(E, G, state, P, DD);
+    return cudaGetLastError();
+}
+
 int gret_simt_segments(int B, int N, int H, int dv) {
     // enough CTAs to cover the GPU about once; each segment at least one chunk
     int ctas = B * H * (dv / kSimtDVB);

@@ -22,6 +22,8 @@ struct GretArgs {
 size_t gret_simt_smem_bytes(int dk);
 size_t gret_simt_workspace(int B, int N, int H, int dk, int dv);
 cudaError_t gret_prefill_simt(const GretArgs &a, void *ws, cudaStream_t st);
+// segment join shared by both paths: E[bh][p] (zero-start end states) -> initial states
+cudaError_t gret_scan_launch(float *E, const float *G, float *state, int BH, int P, int DD, cudaStream_t st);
 cudaError_t gret_decode(const void *q, const void *k, const void *v, const float *logits, float tau,
                         float *state, void *o, int B, int H, int dk, int dv, yoco_dtype dt, cudaStream_t st);
 

@@ -184,6 +184,16 @@ YOCO_API const char *yoco_status_string(yoco_status s);
 YOCO_API const char *yoco_last_error(void);
 YOCO_API int yoco_version(void);
 
+/*
+ * Status word of a workspace.  Kernels that wait on on-device signals give up
+ * after a bounded time instead of hanging; they then record the failure in
+ * the first bytes of the workspace they were given.  This call waits for
+ * `stream`, reads that word and returns YOCO_OK or YOCO_ERR_TIMEOUT (the
+ * detail is in yoco_last_error()); with clear != 0 it also resets the word.
+ * A freshly allocated workspace needs no initialisation.
+ */
+YOCO_API yoco_status yoco_workspace_status(void *workspace, int clear, void *stream);
+
 /* Number of kernels this process has enqueued through libyoco so far
  * (monotonic, all threads).  A diagnostic for counting launches per step. */
 YOCO_API uint64_t yoco_launch_count(void);

@@ -98,6 +98,43 @@ def test_gret_prefill_bf16(Y, N, chunk):
     assert rel_l2(S, S_ref) <= BF16_REL_L2
 
 
+@pytest.mark.parametrize("B,N,H,with_state", [(1, 8192 + 77, 24, True), (2, 300, 80, True), (1, 128, 3, False),
+                                              (3, 1, 2, True)])
+def test_gret_prefill_bf16_tensor_core_shapes(Y, B, N, H, with_state):
+    """Tensor-core path: many chunks per segment (N=8269 over 24 heads), one
+    segment per sequence (B*H >= 152), exactly one chunk, a single token."""
+    import torch
+    d = 128
+    host, dev = gret_inputs(7, B, N, H, d, "bf16", logit_mean=2.0)
+    S0 = None
+    if with_state:
+        S0 = synth.normal(SEED, sid(7, 1, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
+    o, S = run_prefill(Y, dev, B, N, H, d, "bf16", S0=S0)
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0, S0=S0)
+    assert rel_l2(o, o_ref) <= BF16_REL_L2
+    assert rel_l2(S, S_ref) <= BF16_REL_L2
+    ws = torch.empty(max(256, Y.yoco_gret_prefill_workspace_size(B, N, H, d, d, 0, Y.YOCO_BF16)),
+                     dtype=torch.uint8, device="cuda")
+    qd, kd, vd, lgd = dev
+    o2 = torch.empty_like(vd)
+    S2 = torch.zeros(B, H, d, d, device="cuda")
+    Y.yoco_gret_prefill_chunkwise(qd, kd, vd, lgd, 16.0, o2, S2, workspace=ws)
+    Y.yoco_workspace_status(ws)  # no bounded wait gave up
+
+
+def test_gret_prefill_bf16_strong_decay(Y):
+    """Gates near 0 inside chunks (b_C < -80) take the direct-exponent branch."""
+    B, N, H, d = 1, 1000, 4, 128
+    host, dev = gret_inputs(8, B, N, H, d, "bf16", logit_mean=-6.0)
+    lg = host[3].copy()
+    lg[:, 500:530] = -2000.0
+    dev = dev[:3] + (dev_f32(lg),)
+    o, S = run_prefill(Y, dev, B, N, H, d, "bf16")
+    o_ref, S_ref = oracle.gret_recurrent(host[0], host[1], host[2], lg, 16.0)
+    assert rel_l2(o, o_ref) <= BF16_REL_L2
+    assert rel_l2(S, S_ref) <= BF16_REL_L2
+
+
 def test_gret_prefill_state_continuation(Y):
     """Two calls with the state carried equal one oracle pass (chunked prefill)."""
     B, N, H, d = 1, 1500, 2, 128
