@@ -52,6 +52,7 @@ def _load():
         "yoco_cross_attn_prefill": (i, [vp, i, i, i64, cp, f, vp, vp, sz, vp]),
         "yoco_cross_attn_decode": (i, [vp, i, cp, f, i, vp, vp, sz, vp]),
         "yoco_cross_attn_workspace_size": (sz, [i, i, i, cp, i]),
+        "yoco_cross_attn_decode_noalloc": (i, [vp, i, cp, f, i, vp, vp]),
         "yoco_status_string": (ctypes.c_char_p, [i]),
         "yoco_last_error": (ctypes.c_char_p, []),
         "yoco_version": (i, []),
@@ -70,7 +71,7 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_shared_kv_project_append", "yoco_shared_kv_workspace_size", "yoco_cross_attn_prefill",
             "yoco_cross_attn_decode", "yoco_cross_attn_workspace_size", "yoco_status_string",
             "yoco_last_error", "yoco_version", "yoco_launch_count",
-            "yoco_workspace_status")
+            "yoco_workspace_status", "yoco_cross_attn_decode_noalloc")
 
 
 def _check(status: int, where: str):
@@ -189,6 +190,19 @@ def yoco_shared_kv_project_append(M, Wk, Wv, cache: KVCache, eps=1e-6, rms_w=Non
 
 
 # -------------------------------------------------------- cross attention
+
+def yoco_cross_attn_decode_noalloc(Q, cache: KVCache, O, scale=None, num_splits=0, stream=None):
+    """Decode attention without a workspace: the split partials go to scratch
+    built into the library, for callers that cannot allocate device memory.
+    Calls on one device share that scratch, so do not overlap them."""
+    _need(Q, "Q")
+    _need(O, "O")
+    B, Hq, d = Q.shape
+    scale = d ** -0.5 if scale is None else scale
+    st = lib.yoco_cross_attn_decode_noalloc(_ptr(Q), Hq, ctypes.byref(cache.c), float(scale), num_splits, _ptr(O),
+                                            _stream(stream))
+    _check(st, "yoco_cross_attn_decode_noalloc")
+
 
 def yoco_cross_attn_workspace_size(B, Hq, T, cache: KVCache, num_splits=0) -> int:
     return lib.yoco_cross_attn_workspace_size(B, Hq, T, ctypes.byref(cache.c), num_splits)

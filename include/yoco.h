@@ -174,6 +174,31 @@ YOCO_API yoco_status yoco_cross_attn_decode(const void *Q, int Hq, const yoco_kv
                                    float scale, int num_splits, void *O, void *workspace,
                                    size_t ws_bytes, void *stream);
 
+/*
+ * Cross-attention decode without a workspace, for callers that cannot
+ * allocate device memory when they decode (a runtime that forbids allocation
+ * after start-up, a serving loop with a fixed memory budget, a plugin handed
+ * only its input and output buffers).  The paper has no counterpart: this is
+ * a deployment variant of yoco_cross_attn_decode with the same arguments and
+ * result, minus the workspace.
+ *   - Its scratch is a 4 MiB array built into the library's device code.  The
+ *     CUDA runtime creates it on every GPU that loads libyoco; it stays there
+ *     until the process exits.  The call itself allocates nothing.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress on the current device); make that first call
+ *     before capturing any stream on that device.
+ *   - num_splits = 0 picks the usual split count, lowered until the partial
+ *     results fit in 4 MiB.  An explicit num_splits whose partials
+ *     (B * Hq * num_splits * (d + 2) * 4 bytes) do not fit returns
+ *     YOCO_ERR_UNSUPPORTED and launches nothing.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (every partial read is first written by the same call, so
+ *     nothing needs clearing).  Calls that overlap on the GPU, e.g. on two
+ *     streams at once, race on it: order them on one stream.
+ */
+YOCO_API yoco_status yoco_cross_attn_decode_noalloc(const void *Q, int Hq, const yoco_kv_cache *cache,
+                                                    float scale, int num_splits, void *O, void *stream);
+
 /* Workspace bytes for a prefill (T rows) or decode (T = 1) attention call. */
 YOCO_API size_t yoco_cross_attn_workspace_size(int B, int Hq, int T, const yoco_kv_cache *cache,
                                       int num_splits);
