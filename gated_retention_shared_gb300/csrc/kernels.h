@@ -44,6 +44,9 @@ struct KvProjArgs {
 };
 size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt);
 cudaError_t kv_project_append(const KvProjArgs &a, void *ws, cudaStream_t st);
+// kv_proj_tc.cu: bf16, no gain, Hkv*d % 256 == 0, >= 128 rows
+bool kv_proj_tc_eligible(const KvProjArgs &a);
+cudaError_t kv_project_append_tc(const KvProjArgs &a, const float *rrow, int *err, cudaStream_t st);
 
 // attn.cu
 struct AttnArgs {

@@ -9,6 +9,8 @@
 //
 // This file holds the CUDA-core path (any dtype, any T); large bf16 appends go to
 // the tensor-core GEMM in kv_proj_tc.cu.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -122,20 +124,23 @@ proj_append_simt(const T *__restrict__ M, const T *__restrict__ g, const T *__re
 namespace yoco_host {
 using namespace yoco;
 
+// workspace: [0, 256) status word of the tensor-core kernel, then one fp32 RMS factor per row
 size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt) {
     (void)dm; (void)Hkv; (void)d; (void)dt;
     size_t rows = (size_t)B * T;
-    return ((rows * sizeof(float) + 255) / 256) * 256;
+    return 256 + ((rows * sizeof(float) + 255) / 256) * 256;
 }
 
 template <typename T>
 static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
     const int R = a.B * a.T;
-    float *r = (float *)ws;
-    count_launches(2);
+    float *r = (float *)((char *)ws + 256);
+    count_launches(1);
     rms_rows_kernel<T><<<(R * 32 + 255) / 256, 256, 0, st>>>((const T *)a.M, r, R, a.dm, a.eps);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a)) return kv_project_append_tc(a, r, (int *)ws, st);
+    count_launches(1);
     dim3 grid((2 * a.Hkv * a.d + 63) / 64, (R + 63) / 64);
     proj_append_simt<T><<<grid, 256, 0, st>>>((const T *)a.M, (const T *)a.rms_w, (const T *)a.Wk, (const T *)a.Wv,
                                               r, (T *)a.kc, (T *)a.vc, R, a.T, a.dm, a.Hkv, a.d, a.cap, a.len,

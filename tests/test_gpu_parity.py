@@ -232,6 +232,45 @@ def test_kv_append_bit_exact(Y):
         assert cache.length == length and int(cache.len_dev[0]) == length and int(cache.len_dev[1]) == 0
 
 
+def test_kv_append_tensor_core_bit_exact(Y):
+    """The tensor-core projection (>= 128 rows, Hkv*d a multiple of 256): exact
+    inputs give a bit-identical cache, appended after existing slots."""
+    import torch
+    B, T, dm, Hkv, d, cap, length = 2, 150, 512, 8, 128, 170, 7
+    rng_bits = np.random.default_rng(1).integers(0, 0x7F7F, size=(B, Hkv, cap, d)).astype(np.uint16)
+    cache = Y.KVCache(B, Hkv, d, cap, k=dev_bf16(rng_bits), v=dev_bf16(rng_bits.copy()))
+    cache.set_length(length)
+    Wk = synth.dyadic(SEED, sid(21, 0, synth.T_WK), (dm, Hkv * d))
+    Wv = synth.dyadic(SEED, sid(21, 0, synth.T_WV), (dm, Hkv * d))
+    M = synth.signs(SEED, sid(21, 0, synth.T_M), (B, T, dm))
+    Y.yoco_shared_kv_project_append(dev_bf16(synth.f64_to_bf16_bits(M)), dev_bf16(synth.f64_to_bf16_bits(Wk)),
+                                    dev_bf16(synth.f64_to_bf16_bits(Wv)), cache, eps=0.0)
+    torch.cuda.synchronize()
+    kref = oracle.kv_append_bf16(rng_bits, oracle.rmsnorm_proj(M, Wk, 0.0), length)
+    vref = oracle.kv_append_bf16(rng_bits, oracle.rmsnorm_proj(M, Wv, 0.0), length)
+    assert np.array_equal(host_bits(cache.k), kref)
+    assert np.array_equal(host_bits(cache.v), vref)
+    assert cache.length == length + T and int(cache.len_dev[0]) == length + T and int(cache.len_dev[1]) == 0
+
+
+def test_kv_append_tensor_core_3b_width(Y):
+    """d_model 3072 -> 8 x 128 (the 3B shape) on random data, ragged row count."""
+    import torch
+    B, T, dm, Hkv, d = 2, 150, 3072, 8, 128
+    M, Md = gen(SEED, sid(22, 0, synth.T_M), (B, T, dm), "bf16")
+    Wk, Wkd = gen(SEED, sid(22, 0, synth.T_WK), (dm, Hkv * d), "bf16", std=0.02)
+    Wv, Wvd = gen(SEED, sid(22, 0, synth.T_WV), (dm, Hkv * d), "bf16", std=0.02)
+    cache = Y.KVCache(B, Hkv, d, T)
+    ws = torch.empty(Y.lib.yoco_shared_kv_workspace_size(B, T, dm, __import__("ctypes").byref(cache.c)),
+                     dtype=torch.uint8, device="cuda")
+    Y.yoco_shared_kv_project_append(Md, Wkd, Wvd, cache, eps=1e-6, workspace=ws)
+    Y.yoco_workspace_status(ws)
+    kref = oracle.rmsnorm_proj(M, Wk, 1e-6).reshape(B, T, Hkv, d).transpose(0, 2, 1, 3)
+    vref = oracle.rmsnorm_proj(M, Wv, 1e-6).reshape(B, T, Hkv, d).transpose(0, 2, 1, 3)
+    assert rel_l2(host_f64(cache.k), kref) <= BF16_REL_L2
+    assert rel_l2(host_f64(cache.v), vref) <= BF16_REL_L2
+
+
 def test_kv_append_fp32_and_gain(Y):
     """fp32 cache (tiny config: dm 128 -> one 64-wide head), with an RMSNorm gain."""
     import torch
