@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk", type=int, default=0)
+    p.add_argument("--only", choices=["gret", "proj", "cross_decode"], default=None,
+                   help="time one call of the step on its bench shape (for profiling)")
     return p.parse_args()
 
 
@@ -239,11 +241,15 @@ def run_gpu(args):
         if st != 0:
             raise RuntimeError(f"{what}: {L.yoco_last_error().decode()}")
 
-    def step(timed_calls=None):
+    def step(timed_calls=None, marks=None):
+        def mark(i):
+            if marks is not None:
+                marks[i].record(stream)
         for s in S:
             s.zero_()
         cache.len_dev.zero_()
         cache.c.len_host = 0
+        mark(0)
         for l in range(L_SELF):
             if timed_calls is not None:
                 timed_calls[l][0].record(stream)
@@ -251,16 +257,22 @@ def run_gpu(args):
                                                 H, D, D, args.chunk, 1, 1, wsp, wsn, stp), "gret prefill")
             if timed_calls is not None:
                 timed_calls[l][1].record(stream)
+        mark(1)
         check(L.yoco_shared_kv_project_append(P(M), None, EPS, P(Wk), P(Wv), N, DM, cc, wsp, wsn, stp), "kv append")
+        mark(2)
         for l in range(L_CROSS):
             check(L.yoco_cross_attn_prefill(P(Qx[l]), HQ, 1, N - 1, cc, D ** -0.5, P(Ox[l]), wsp, wsn, stp),
                   "cross prefill")
+        mark(3)
         for l in range(L_SELF):
             check(L.yoco_gret_decode_step(P(q1[l]), P(k1[l]), P(v1[l]), P(lg1[l]), TAU, P(S[l]), P(o1[l]), B, H, D,
                                           D, 1, 1, stp), "gret decode")
+        mark(4)
         check(L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, cc, wsp, wsn, stp), "append 1")
+        mark(5)
         for l in range(L_CROSS):
             check(L.yoco_cross_attn_decode(P(Qd[l]), HQ, cc, D ** -0.5, 0, P(Od[l]), wsp, wsn, stp), "cross decode")
+        mark(6)
 
     def barrier():
         if dist is not None:
@@ -294,6 +306,14 @@ def run_gpu(args):
     value = world * B * N * args.steps / elapsed
     gret_ms = statistics.mean(c[0].elapsed_time(c[1]) for row in calls for c in row)
 
+    # ---- per-phase split: one more (untimed) step with events between phases
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    phase_names = ["gret_prefill_x13", "kv_project_32k", "cross_last_row_x13", "gret_decode_x13",
+                   "kv_append_1", "cross_decode_x13"]
+    step(marks=marks)
+    torch.cuda.synchronize()
+    phases = {n: round(marks[i].elapsed_time(marks[i + 1]), 4) for i, n in enumerate(phase_names)}
+
     # ---- roofline of the dominant call: chunkwise gRet prefill, one layer
     gret_bytes = 3 * B * N * H * D * 2 + B * N * H * D * 2 + B * N * H * 4 + 2 * B * H * D * D * 4
     peaks = {}
@@ -318,7 +338,7 @@ def run_gpu(args):
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
            "config": workload_config(args.chunk if args.chunk else "auto"),
            "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches_per_step * args.steps),
-           "gpu_launches_per_step": int(launches_per_step), "clocks": clocks}
+           "gpu_launches_per_step": int(launches_per_step), "clocks": clocks, "phases_ms": phases}
     if rank == 0 and not args.no_cpu_baseline:
         step_s, desc, cores = cpu_sample()
         out["cpu_baseline"] = {"value": N / step_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
@@ -360,9 +380,79 @@ def e2e_measure(args, torch, stream, step, big_lists, small, results):
             "steps": args.e2e_steps, "ms_per_step": t * 1e3}
 
 
+def run_only(args):
+    """One call kind of the step, on its bench shape, for kernel profiling."""
+    import torch
+
+    import gated_retention_shared_gb300 as Y
+    import synth
+    L = Y.lib
+    dev = torch.device("cuda", 0)
+    sid = synth.stream_id
+    bf, f32 = torch.bfloat16, torch.float32
+
+    def normal(shape, dtype, stream, mean=0.0, std=1.0):
+        return synth.fill_normal_(torch.empty(shape, dtype=dtype, device=dev), SEED, stream, mean, std)
+
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    stp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if args.only == "gret":
+        q = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_Q), std=D ** -0.5)
+        k = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_K), std=D ** -0.5)
+        v = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_V))
+        lg = normal((B, N, H), f32, sid(CFG, 0, synth.T_LOGIT), mean=2.0)
+        o = torch.empty_like(v)
+        S = torch.zeros(B, H, D, D, dtype=f32, device=dev)
+        ws = torch.empty(max(256, L.yoco_gret_prefill_workspace_size(B, N, H, D, D, args.chunk, 1)), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            S.zero_()
+            return L.yoco_gret_prefill_chunkwise(P(q), P(k), P(v), P(lg), TAU, P(o), P(S), B, N, H, D, D, args.chunk,
+                                                 1, 1, P(ws), ws.numel(), stp)
+    elif args.only == "proj":
+        M = normal((B, N, DM), bf, sid(CFG, 0, synth.T_M))
+        Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
+        Wv = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WV), std=0.02)
+        cache = Y.KVCache(B, HKV, D, N, device=dev)
+        ws = torch.empty(L.yoco_shared_kv_workspace_size(B, N, DM, ctypes.byref(cache.c)), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            cache.len_dev.zero_()
+            cache.c.len_host = 0
+            return L.yoco_shared_kv_project_append(P(M), None, EPS, P(Wk), P(Wv), N, DM, ctypes.byref(cache.c), P(ws),
+                                                   ws.numel(), stp)
+    else:
+        Kc = normal((B, HKV, N, D), bf, sid(CFG, 0, synth.T_CACHE_K))
+        Vc = normal((B, HKV, N, D), bf, sid(CFG, 0, synth.T_CACHE_V))
+        cache = Y.KVCache(B, HKV, D, N, k=Kc, v=Vc)
+        cache.set_length(N)
+        Qd = normal((B, HQ, D), bf, sid(CFG, 0, synth.T_QX, 1))
+        Od = torch.empty_like(Qd)
+        ws = torch.empty(max(256, L.yoco_cross_attn_workspace_size(B, HQ, 1, ctypes.byref(cache.c), 0)),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            return L.yoco_cross_attn_decode(P(Qd), HQ, ctypes.byref(cache.c), D ** -0.5, 0, P(Od), P(ws), ws.numel(),
+                                            stp)
+    for _ in range(args.warmup):
+        assert call() == 0, L.yoco_last_error()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        assert call() == 0, L.yoco_last_error()
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"only": args.only, "ms_per_call": e0.elapsed_time(e1) / args.steps, "steps": args.steps}))
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.only:
+        run_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -175,6 +175,8 @@ yoco_status yoco_shared_kv_project_append(const void *M, const void *rms_w, floa
     if (T <= 0 || dm <= 0) return fail(YOCO_ERR_INVALID_ARG, "T and dm must be > 0");
     if (!M || !Wk || !Wv) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
     if (!(eps >= 0.0f) || !isfinite(eps)) return fail(YOCO_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (!aligned(M, 16) || !aligned(Wk, 16) || !aligned(Wv, 16) || (rms_w && !aligned(rms_w, 16)))
+        return fail(YOCO_ERR_INVALID_ARG, "M, Wk, Wv and rms_w must be 16-byte aligned");
     if (cache->len_host + T > cache->capacity)
         return fail(YOCO_ERR_CAPACITY, "append of %d tokens at length %lld exceeds capacity %lld", T,
                     (long long)cache->len_host, (long long)cache->capacity);

@@ -27,32 +27,32 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-template <typename T, int D> struct AttnCfg {
+template <typename T, int D, int NQ = kAttnMaxQ> struct AttnCfg {
     static constexpr int kRowBytes = D * (int)sizeof(T);
     static constexpr int kKPitch = kRowBytes + 16;  // padded K rows: lanes read different rows
     static constexpr int kVPitch = kRowBytes;
-    static constexpr int kStages = (sizeof(T) == 2) ? 2 : 1;
+    static constexpr int kStages = 1;  // overlap comes from 3 resident CTAs per SM
     static constexpr int kStageBytes = kAttnTile * (kKPitch + kVPitch);
     static constexpr int kEpt = D / 32;  // head-dim elements per lane
     __host__ __device__ static constexpr size_t smem_bytes() {
         size_t tiles = (size_t)kStages * kStageBytes;
-        size_t merge = (size_t)kAttnWarps * kAttnMaxQ * (D + 2) * sizeof(float);
-        return (tiles > merge ? tiles : merge) + (size_t)kAttnMaxQ * D * sizeof(float);
+        size_t merge = (size_t)kAttnWarps * NQ * (D + 2) * sizeof(float);
+        return (tiles > merge ? tiles : merge) + (size_t)NQ * D * sizeof(float);
     }
 };
 
 // grid: x = key split, y = query row block, z = b * Hkv + kv head
 // rows: t in [y * RB, min(T, (y + 1) * RB)); query vector qv = (t - t0) * G + g
-template <typename T, int D>
-__global__ void __launch_bounds__(kAttnThreads)
+template <typename T, int D, int NQ>
+__global__ void __launch_bounds__(kAttnThreads, 3)
 attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restrict__ Kc,
                   const T *__restrict__ Vc, float *__restrict__ part, int T_rows, int Hq, int Hkv,
                   int64_t cap, int64_t p0, float scale, int RB, int64_t keys_per_split, int splits) {
-    using Cfg = AttnCfg<T, D>;
+    using Cfg = AttnCfg<T, D, NQ>;
     constexpr int E = Cfg::kEpt;
     extern __shared__ float4 smem4[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(smem4);
-    float *qs = reinterpret_cast<float *>(smem + (Cfg::smem_bytes() - (size_t)kAttnMaxQ * D * sizeof(float)));
+    float *qs = reinterpret_cast<float *>(smem + (Cfg::smem_bytes() - (size_t)NQ * D * sizeof(float)));
 
     const int G = Hq / Hkv;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -75,9 +75,9 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
     const T *Kb = Kc + ((size_t)b * Hkv + hk) * (size_t)cap * D;
     const T *Vb = Vc + ((size_t)b * Hkv + hk) * (size_t)cap * D;
 
-    float m[kAttnMaxQ], l[kAttnMaxQ], acc[kAttnMaxQ][E];
+    float m[NQ], l[NQ], acc[NQ][E];
 #pragma unroll
-    for (int i = 0; i < kAttnMaxQ; ++i) {
+    for (int i = 0; i < NQ; ++i) {
         m[i] = -INFINITY;
         l[i] = 0.f;
 #pragma unroll
@@ -124,9 +124,9 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
         const bool key_ok = key < k_hi;
 
         // scores s[qv] = q_qv . k_key (q already scaled)
-        float s[kAttnMaxQ];
+        float s[NQ];
 #pragma unroll
-        for (int i = 0; i < kAttnMaxQ; ++i) s[i] = 0.f;
+        for (int i = 0; i < NQ; ++i) s[i] = 0.f;
         const T *krow = reinterpret_cast<const T *>(sk + r * Cfg::kKPitch);
         for (int c = 0; c < D; c += 4) {
             float kv[4];
@@ -141,7 +141,7 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
                 kv[0] = f.x; kv[1] = f.y; kv[2] = f.z; kv[3] = f.w;
             }
 #pragma unroll
-            for (int i = 0; i < kAttnMaxQ; ++i) {
+            for (int i = 0; i < NQ; ++i) {
                 if (i < nq) {
                     float4 qq = *reinterpret_cast<const float4 *>(&qs[i * D + c]);
                     s[i] = fmaf(qq.x, kv[0], fmaf(qq.y, kv[1], fmaf(qq.z, kv[2], fmaf(qq.w, kv[3], s[i]))));
@@ -151,7 +151,7 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
         // causal mask + online softmax per query vector (warp-wide over its 32 keys)
         const T *vbase = reinterpret_cast<const T *>(sv);
 #pragma unroll
-        for (int i = 0; i < kAttnMaxQ; ++i) {
+        for (int i = 0; i < NQ; ++i) {
             if (i >= nq) break;
             const int64_t pos = p0 + t0 + i / G;
             float si = (key_ok && key <= pos) ? s[i] : -INFINITY;
@@ -193,7 +193,7 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
                 for (int e = 0; e < E; ++e) vv[e] = vrow[e];
             }
 #pragma unroll
-            for (int i = 0; i < kAttnMaxQ; ++i) {
+            for (int i = 0; i < NQ; ++i) {
                 if (i < nq) {
                     float pj = __shfl_sync(0xffffffffu, s[i], j);
 #pragma unroll
@@ -208,7 +208,7 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
     float *mw = reinterpret_cast<float *>(smem);              // [warps][MaxQ][D + 2]
     const int pitch = D + 2;
     for (int i = 0; i < nq; ++i) {
-        float *row = mw + ((size_t)warp * kAttnMaxQ + i) * pitch;
+        float *row = mw + ((size_t)warp * NQ + i) * pitch;
 #pragma unroll
         for (int e = 0; e < E; ++e) row[lane * E + e] = acc[i][e];
         if (lane == 0) {
@@ -220,10 +220,10 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
     for (int e = threadIdx.x; e < nq * D; e += kAttnThreads) {
         const int i = e / D, c = e % D;
         float M = -INFINITY;
-        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mw[((size_t)w * kAttnMaxQ + i) * pitch + D]);
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mw[((size_t)w * NQ + i) * pitch + D]);
         float L = 0.f, A = 0.f;
         for (int w = 0; w < kAttnWarps; ++w) {
-            const float *row = mw + ((size_t)w * kAttnMaxQ + i) * pitch;
+            const float *row = mw + ((size_t)w * NQ + i) * pitch;
             float f = (row[D] == -INFINITY) ? 0.f : __expf(row[D] - M);
             L += row[D + 1] * f;
             A += row[c] * f;
@@ -243,30 +243,23 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
     }
 }
 
-// merge the splits of every query row by log-sum-exp; one warp per (row, head)
+// merge the splits of every query row by log-sum-exp: one CTA per (row, head),
+// thread c owns head dim c
 template <typename T, int D>
-__global__ void attn_combine_kernel(const float *__restrict__ part, T *__restrict__ O, int rows, int splits) {
-    const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
-    const int lane = threadIdx.x % 32;
-    if (w >= rows) return;
+__global__ void __launch_bounds__(D) attn_combine_kernel(const float *__restrict__ part, T *__restrict__ O, int splits) {
+    const int w = blockIdx.x, c = threadIdx.x;
     const float *pp = part + (size_t)w * splits * (D + 2);
     float M = -INFINITY;
-    for (int s = lane; s < splits; s += 32) M = fmaxf(M, pp[(size_t)s * (D + 2) + D]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    constexpr int E = D / 32;
-    float A[E] = {};
-    float L = 0.f;
+    for (int s = 0; s < splits; ++s) M = fmaxf(M, pp[(size_t)s * (D + 2) + D]);
+    float L = 0.f, A = 0.f;
     for (int s = 0; s < splits; ++s) {
         const float *row = pp + (size_t)s * (D + 2);
-        float ms = row[D];
-        float f = (ms == -INFINITY) ? 0.f : __expf(ms - M);
+        const float ms = row[D];
+        const float f = (ms == -INFINITY) ? 0.f : __expf(ms - M);
         L += row[D + 1] * f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) A[e] += row[lane * E + e] * f;
+        A += row[c] * f;
     }
-#pragma unroll
-    for (int e = 0; e < E; ++e) O[(size_t)w * D + lane * E + e] = from_f32<T>(A[e] / L);
+    O[(size_t)w * D + c] = from_f32<T>(A / L);
 }
 
 }  // namespace yoco
@@ -277,9 +270,9 @@ using namespace yoco;
 static int rows_per_block(int G) { return G >= kAttnMaxQ ? 1 : kAttnMaxQ / G; }
 
 int attn_auto_splits(int B, int Hkv, int64_t keys) {
-    // enough CTAs for ~4 per SM on 152 SMs, each slice at least 4 tiles
-    int64_t want = (4 * 152 + (int64_t)B * Hkv - 1) / ((int64_t)B * Hkv);
-    int64_t max_by_len = (keys + 4 * kAttnTile - 1) / (4 * kAttnTile);
+    // about one wave of CTAs on 152 SMs with three resident CTAs each; slices of >= 2 tiles
+    int64_t want = (3 * 152 + (int64_t)B * Hkv - 1) / ((int64_t)B * Hkv);
+    int64_t max_by_len = (keys + 2 * kAttnTile - 1) / (2 * kAttnTile);
     if (want > max_by_len) want = max_by_len;
     if (want < 1) want = 1;
     if (want > 1024) want = 1024;
@@ -291,6 +284,19 @@ size_t attn_workspace(int B, int Hq, int T, int d, int splits) {
     return (size_t)B * T * Hq * splits * (d + 2) * sizeof(float);
 }
 
+template <typename T, int D, int NQ>
+static cudaError_t launch_nq(const AttnArgs &a, int RB, int64_t kps, int splits, void *ws, cudaStream_t st) {
+    auto kern = attn_split_kernel<T, D, NQ>;
+    size_t smem = AttnCfg<T, D, NQ>::smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(splits, (a.T + RB - 1) / RB, a.B * a.Hkv);
+    count_launches(splits > 1 ? 2 : 1);
+    kern<<<grid, kAttnThreads, smem, st>>>((const T *)a.Q, (T *)a.O, (const T *)a.kc, (const T *)a.vc, (float *)ws,
+                                           a.T, a.Hq, a.Hkv, a.cap, a.p0, a.scale, RB, kps, splits);
+    return cudaGetLastError();
+}
+
 template <typename T, int D>
 static cudaError_t launch(const AttnArgs &a, int splits, void *ws, cudaStream_t st) {
     const int G = a.Hq / a.Hkv;
@@ -299,18 +305,15 @@ static cudaError_t launch(const AttnArgs &a, int splits, void *ws, cudaStream_t 
     int64_t kps = (keys + splits - 1) / splits;
     kps = ((kps + kAttnTile - 1) / kAttnTile) * kAttnTile;
     splits = (int)((keys + kps - 1) / kps);
-    auto kern = attn_split_kernel<T, D>;
-    size_t smem = AttnCfg<T, D>::smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int nq = (a.T < RB ? a.T : RB) * G;  // query vectors per CTA
+    cudaError_t e;
+    if (nq <= 4) e = launch_nq<T, D, 4>(a, nq <= 4 && a.T <= RB ? a.T : RB, kps, splits, ws, st);
+    else if (nq <= 8) e = launch_nq<T, D, 8>(a, RB, kps, splits, ws, st);
+    else e = launch_nq<T, D, 16>(a, RB, kps, splits, ws, st);
     if (e != cudaSuccess) return e;
-    dim3 grid(splits, (a.T + RB - 1) / RB, a.B * a.Hkv);
-    count_launches(splits > 1 ? 2 : 1);
-    kern<<<grid, kAttnThreads, smem, st>>>((const T *)a.Q, (T *)a.O, (const T *)a.kc, (const T *)a.vc,
-                                           (float *)ws, a.T, a.Hq, a.Hkv, a.cap, a.p0, a.scale, RB, kps, splits);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (splits > 1) {
-        int rows = a.B * a.T * a.Hq;
-        attn_combine_kernel<T, D><<<(rows * 32 + 255) / 256, 256, 0, st>>>((const float *)ws, (T *)a.O, rows, splits);
+        const int rows = a.B * a.T * a.Hq;
+        attn_combine_kernel<T, D><<<rows, D, 0, st>>>((const float *)ws, (T *)a.O, splits);
         e = cudaGetLastError();
     }
     return e;

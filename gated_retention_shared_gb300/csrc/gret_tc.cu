@@ -7,15 +7,17 @@
 // state S (d_k x d_v) before the chunk:
 //     o_j  = sum_{k<=j} (q_j . k_k) e^{b_j - b_k} v_k  +  e^{b_j} q_j S
 //     S'   = e^{b_C} S + sum_k e^{b_C - b_k} k_k^T v_k
-// Everything is computed transposed, so that one TMEM lane holds one d_v column
-// and the output leaves TMEM as coalesced rows:
-//     A    = Q K^T                       (lane = query j)         MMA1
-//     P_jk = A_jk e^{b_j - b_k} [k <= j] (bf16, shared memory)
-//     O^T  = V^T P^T + S^T Q'^T,  Q'_j = e^{b_j} q_j               MMA2, MMA3
-//     U^T  = V^T K',              K'_k = e^{b_C - b_k} k_k         MMA4
-//     S'^T = e^{b_C} S^T + U^T   (fp32, registers of the state warps)
-// S^T is fed back to MMA3 as a bf16 A operand in TMEM; the fp32 state never
-// leaves the registers until the segment ends.
+// On the tensor cores, per chunk (lane = TMEM lane):
+//     A    = Q K^T                               MMA1   lane = query j
+//     P_jk = A_jk e^{-b_k} [k <= j]  (bf16, written over A in TMEM)
+//     O    = P V + Q S                           MMA2 (P from TMEM), MMA3
+//     o_j  = e^{b_j} O_j                         epilogue
+//     U    = K'^T V,  K'_k = e^{b_C - b_k} k_k   MMA4   lane = d_k row i
+//     S'   = e^{b_C} S + U   (fp32, registers of the state warps; bf16 copy in
+//                             shared memory is MMA3's B operand)
+// Factoring e^{b_j - b_k} = e^{b_j} e^{-b_k} needs e^{-b_k} finite; a chunk whose
+// total log decay is below -60 instead multiplies P by e^{b_j - b_k} directly and
+// scales Q's rows by e^{b_j} in place (and the epilogue multiplies by 1).
 //
 // Sequence parallelism: the sequence of every (b, h) is cut into P segments of
 // whole chunks.  Kernel mode SEG_STATE walks a segment backwards and accumulates
@@ -25,9 +27,11 @@
 // mode OUTPUT runs the chunk recurrence above from it.  With B*H >= #SMs, P = 1
 // and only OUTPUT runs.
 //
-// Warp roles (320 threads): warps 0-3 state + output epilogue (thread = TMEM lane
-// = d_v column), warps 4-7 decay / P / in-place scaling of Q and K (thread = token
-// row of the chunk), warp 8 TMA producer, warp 9 MMA issuer.
+// Warp roles (320 threads): warps 0-3 keep the state (thread t = TMEM lane t =
+// d_k row t), warps 4-7 compute the decay, P, the in-place scaling of K (and Q)
+// and write the output rows (thread j = query row j), warp 8 issues TMA loads,
+// warp 9 issues the MMAs: per chunk MMA1, then (factored chunks) MMA3 while P is
+// being computed, then MMA4 so the state warps can start, then MMA2.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -44,25 +48,27 @@ constexpr int kTile = kC * kD * 2;          // 32 KB bf16 tile
 constexpr int kHalf = kTile / 2;            // one 64-column block
 constexpr int kStages = 2;
 constexpr int kTcThreads = 320;
+constexpr float kFactorMin = -60.f;         // chunk decay above which e^{-b_k} is used
 
-// TMEM columns
-constexpr uint32_t kColA = 0, kColO = 128, kColU = 256, kColS = 384;
+// TMEM columns: A / P, two O accumulators, U
+constexpr uint32_t kColA = 0, kColO = 128, kColU = 384;
 
 enum : int { MODE_OUTPUT = 0, MODE_SEG_STATE = 1 };
 
 struct TcSmem {
-    uint64_t full[kStages], empty[kStages], pq_ready[kStages];
-    uint64_t as_full, as_free, o_full, o_free, u_full, u_free, s_ready, drain;
+    uint64_t full[kStages], empty[kStages], pq_ready[kStages], o_free[2], bc_ready[2], o_full[2];
+    uint64_t qfree[kStages], k_ready[kStages];
+    uint64_t as_full, p_free, u_full, u_free, s_ready, drain;
     uint32_t tmem_base;
     int abort_flag;
     int go0, go1;  // per-group continue decisions (written by one thread, read by all after a barrier)
-    float bc[4];
-    float wsum[4];
-    float bsm[kC];
-    float eneg[kC];
+    float wsum1[4];
+    float bcr[4];  // chunk total log decay b_C, ring over chunks
+    float ew[kC];  // e^{-b_k} (factored chunks) or b_k (direct chunks)
+    float kw[2][kC];  // K row weights e^{b_C - b_k}, ring over chunks
 };
 
-constexpr size_t kTileBytes = (size_t)kStages * 3 * kTile + kTile;  // Q,K,V per stage + P
+constexpr size_t kTileBytes = (size_t)kStages * 3 * kTile + kTile;  // Q,K,V per stage + bf16 state
 constexpr size_t kTcSmemBytes = 232448;                            // the sm_100 per-block maximum
 
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
@@ -90,20 +96,41 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h2);
 }
 
+// Byte offset of 16-B chunk c (0..15, 8 bf16 each) of row r in a 128 x 128
+// swizzled bf16 tile ([64-column block][128 rows][128 B], chunks XOR row % 8).
+__device__ __forceinline__ uint32_t tile_chunk(int r, int c) {
+    return (uint32_t)(c >> 3) * kHalf + (uint32_t)r * 128u + (uint32_t)(((c & 7) ^ (r & 7)) * 16);
+}
+
 // Scale row r of a 128 x 128 swizzled bf16 tile in place.
 __device__ __forceinline__ void scale_row_inplace(uint8_t *tile, int r, float s) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-        uint32_t off = (uint32_t)(c >> 3) * kHalf + (uint32_t)r * 128u + (uint32_t)(((c & 7) ^ (r & 7)) * 16);
-        uint4 *p = reinterpret_cast<uint4 *>(tile + off);
+        uint4 *p = reinterpret_cast<uint4 *>(tile + tile_chunk(r, c));
         *p = scale_bf16x8(*p, s);
     }
+}
+
+// Inclusive cumsum of one value per thread over a 128-thread group (4 warps).
+__device__ __forceinline__ float group_scan(float x, float *wsum, int lane, int wq, int bar_id, float &total) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        float y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) wsum[wq] = x;
+    named_bar(bar_id, 128);
+    float pre = 0.f;
+    for (int w = 0; w < wq; ++w) pre += wsum[w];
+    total = wsum[0] + wsum[1] + wsum[2] + wsum[3];
+    return x + pre;
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ logits, float inv_tau,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const float *__restrict__ logits, float inv_tau,
                bf16_t *__restrict__ o, const float *__restrict__ S_in, float *__restrict__ S_out,
                float *__restrict__ G_out, int N, int H, int seg_len, int P, int *err) {
     extern __shared__ uint8_t smem_raw[];
@@ -121,7 +148,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int t_end = min(N, t_begin + seg_len);
     const int nchunks = (t_end - t_begin + kC - 1) / kC;
     const size_t bhp = ((size_t)b * H + h) * P + p;
-    uint8_t *Pbuf = tiles + (size_t)kStages * 3 * kTile;
+    uint8_t *Sbuf = tiles + (size_t)kStages * 3 * kTile;  // bf16 state, MMA3's B operand
     auto stage_q = [&](int s) { return tiles + (size_t)s * 3 * kTile; };
     auto stage_k = [&](int s) { return tiles + (size_t)s * 3 * kTile + kTile; };
     auto stage_v = [&](int s) { return tiles + (size_t)s * 3 * kTile + 2 * kTile; };
@@ -131,11 +158,14 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
             mbar_init(&sm.pq_ready[s], 1);
+            mbar_init(&sm.o_free[s], 1);
+            mbar_init(&sm.bc_ready[s], 1);
+            mbar_init(&sm.o_full[s], 1);
+            mbar_init(&sm.qfree[s], 1);
+            mbar_init(&sm.k_ready[s], 1);
         }
         mbar_init(&sm.as_full, 1);
-        mbar_init(&sm.as_free, 1);
-        mbar_init(&sm.o_full, 1);
-        mbar_init(&sm.o_free, 1);
+        mbar_init(&sm.p_free, 1);
         mbar_init(&sm.u_full, 1);
         mbar_init(&sm.u_free, 1);
         mbar_init(&sm.s_ready, 1);
@@ -158,6 +188,9 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         int c = (MODE == MODE_OUTPUT) ? i : (nchunks - 1 - i);
         return t_begin + c * kC;
     };
+    auto chunk_log_gate = [&](int n0, int row) {
+        return (n0 + row < N) ? log_gate(logits[((size_t)b * N + n0 + row) * H + h], inv_tau) : 0.f;
+    };
 
     if (warp == 8) {
         // ------------------------------------------------------ TMA producer
@@ -175,9 +208,17 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const int n0 = chunk_start(i);
                 mbar_arrive_expect_tx(&sm.full[s], bytes);
                 for (int half = 0; half < 2; ++half) {
-                    if (MODE == MODE_OUTPUT) tma_load_4d(stage_q(s) + half * kHalf, &tm_q, &sm.full[s], half * 64, h, n0, b);
                     tma_load_4d(stage_k(s) + half * kHalf, &tm_k, &sm.full[s], half * 64, h, n0, b);
                     tma_load_4d(stage_v(s) + half * kHalf, &tm_v, &sm.full[s], half * 64, h, n0, b);
+                }
+                if (MODE == MODE_OUTPUT) {
+                    // the Q slot doubles as the staging buffer of chunk i-2's output store
+                    if (i >= kStages && !mbar_wait(&sm.qfree[s], ((i / kStages) + 1) & 1, abort_flag)) {
+                        report(err, &sm.abort_flag, 8);
+                        break;
+                    }
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_4d(stage_q(s) + half * kHalf, &tm_q, &sm.full[s], half * 64, h, n0, b);
                 }
             }
             // leave no copy in flight: wait for the last loads of each stage
@@ -187,18 +228,18 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     } else if (warp == 9) {
         // --------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t id_qk = idesc_bf16_f32(kC, kC, false, false);   // A=Q (K-major), B=K (K-major)
-            const uint32_t id_vp = idesc_bf16_f32(kD, kC, true, false);    // A=V^T (MN-major), B=P (K-major)
-            const uint32_t id_sq = idesc_bf16_f32(kD, kC, false, false);   // A=S^T (TMEM), B=Q' (K-major)
-            const uint32_t id_vk = idesc_bf16_f32(kD, kD, true, true);     // A=V^T (MN-major), B=K' (MN-major)
+            const uint32_t id_qk = idesc_bf16_f32(kC, kC, false, false);  // A=Q (K-major),    B=K (K-major)
+            const uint32_t id_pv = idesc_bf16_f32(kC, kD, false, true);   // A=P (TMEM),       B=V (N-major)
+            const uint32_t id_qs = idesc_bf16_f32(kC, kD, false, true);   // A=Q (K-major),    B=S (N-major)
+            const uint32_t id_kv = idesc_bf16_f32(kD, kD, true, true);    // A=K'^T (M-major), B=V (N-major)
             bool ok = true;
             for (int i = 0; i < nchunks && ok; ++i) {
-                const int s = i % kStages;
+                const int s = i % kStages, ob = i & 1;
                 const uint32_t q_a = smem_u32(stage_q(s)), k_a = smem_u32(stage_k(s)), v_a = smem_u32(stage_v(s));
-                ok = mbar_wait(&sm.full[s], (i / kStages) & 1, abort_flag);
-                if (!ok) break;
+                if (!(ok = mbar_wait(&sm.full[s], (i / kStages) & 1, abort_flag))) break;
                 if (MODE == MODE_OUTPUT) {
-                    if (i > 0 && !(ok = mbar_wait(&sm.as_free, (i - 1) & 1, abort_flag))) break;
+                    // P of the previous chunk (TMEM columns of A) must have been consumed
+                    if (i > 0 && !(ok = mbar_wait(&sm.p_free, (i - 1) & 1, abort_flag))) break;
                     tc_fence_after();
                     for (int kk = 0; kk < 8; ++kk) {  // MMA1: A = Q K^T
                         const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -207,32 +248,49 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                     mma_commit(&sm.as_full);
                 }
-                if (!(ok = mbar_wait(&sm.pq_ready[s], (i / kStages) & 1, abort_flag))) break;
-                tc_fence_after();
                 if (MODE == MODE_OUTPUT) {
-                    if (i > 0 && !(ok = mbar_wait(&sm.o_free, (i - 1) & 1, abort_flag))) break;
-                    tc_fence_after();
-                    const uint32_t p_a = smem_u32(Pbuf);
-                    for (int kk = 0; kk < 8; ++kk) {  // MMA2: O^T = V^T P^T
-                        mma_ss(tmem + kColO, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024),
-                               smem_desc_sw128(p_a + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024), id_vp, kk > 0);
+                    // the decay warps publish the chunk's total decay first: it decides the order
+                    if (!(ok = mbar_wait(&sm.bc_ready[i & 1], (i / 2) & 1, abort_flag))) break;
+                    const bool factor = sm.bcr[i & 3] > kFactorMin;
+                    if (i >= 2 && !(ok = mbar_wait(&sm.o_free[ob], ((i / 2) - 1) & 1, abort_flag))) break;
+                    const uint32_t o_t = tmem + kColO + 128 * ob;
+                    const uint32_t s_a = smem_u32(Sbuf);
+                    auto mma3 = [&]() {  // O = Q S  (Q' = diag(e^b) Q in direct chunks)
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                            mma_ss(o_t, smem_desc_sw128(q_a + off, 16, 1024),
+                                   smem_desc_sw128(s_a + kk * 2048, kHalf, 1024), id_qs, kk > 0);
+                        }
+                    };
+                    if (!factor) {  // Q is rescaled in place together with P
+                        if (!(ok = mbar_wait(&sm.pq_ready[s], (i / kStages) & 1, abort_flag))) break;
                     }
+                    // the cross term needs nothing else from the decay warps: it fills the P bubble
                     if (!(ok = mbar_wait(&sm.s_ready, i & 1, abort_flag))) break;
                     tc_fence_after();
-                    for (int kk = 0; kk < 8; ++kk) {  // MMA3: O^T += S^T Q'^T
-                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        mma_ts(tmem + kColO, tmem + kColS + kk * 8, smem_desc_sw128(q_a + off, 16, 1024), id_sq, 1);
-                    }
-                    mma_commit(&sm.o_full);
+                    mma3();
+                    if (!(ok = mbar_wait(&sm.k_ready[s], (i / kStages) & 1, abort_flag))) break;
                     if (i > 0 && !(ok = mbar_wait(&sm.u_free, (i - 1) & 1, abort_flag))) break;
                     tc_fence_after();
+                    for (int kk = 0; kk < 8; ++kk)  // MMA4: U = K'^T V
+                        mma_ss(tmem + kColU, smem_desc_sw128(k_a + kk * 2048, kHalf, 1024),
+                               smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_kv, kk > 0);
+                    mma_commit(&sm.u_full);
+                    if (factor) {
+                        if (!(ok = mbar_wait(&sm.pq_ready[s], (i / kStages) & 1, abort_flag))) break;
+                        tc_fence_after();
+                    }
+                    for (int kk = 0; kk < 8; ++kk)  // MMA2: O += P V
+                        mma_ts(o_t, tmem + kColA + kk * 8, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_pv, 1);
+                    mma_commit(&sm.o_full[ob]);
+                    mma_commit(&sm.p_free);
+                } else {
+                    if (!(ok = mbar_wait(&sm.pq_ready[s], (i / kStages) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < 8; ++kk)  // E^T += V^T K''
+                        mma_ss(tmem + kColU, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024),
+                               smem_desc_sw128(k_a + kk * 2048, kHalf, 1024), id_kv, (i > 0 || kk > 0));
                 }
-                for (int kk = 0; kk < 8; ++kk) {  // MMA4: U^T (+)= V^T K'
-                    const uint32_t acc = (MODE == MODE_OUTPUT) ? (kk > 0) : (i > 0 || kk > 0);
-                    mma_ss(tmem + kColU, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024),
-                           smem_desc_sw128(k_a + kk * 2048, kHalf, 1024), id_vk, acc);
-                }
-                if (MODE == MODE_OUTPUT) mma_commit(&sm.u_full);
                 mma_commit(&sm.empty[s]);
             }
             if (!ok) report(err, &sm.abort_flag, 2);
@@ -242,122 +300,180 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_wait(&sm.drain, 0, abort_flag, 200000000ull);
         }
     } else if (warp >= 4) {
-        // ------------------------------------ decay, P and in-place scaling
-        const int j = tid - 128;  // token row of the chunk, TMEM lane j
-        const int w4 = warp - 4;
-        const uint32_t lane_base = (uint32_t)(w4 * 32) << 16;
-        float suffix = 0.f;  // SEG_STATE: log decay of the chunks already processed (after this one)
-        for (int i = 0; i < nchunks; ++i) {
-            const int s = i % kStages;
+        // ------------------ decay, P, in-place scaling of K (Q) and the output rows
+        const int j = tid - 128;  // token row of the chunk = TMEM lane
+        const int wq = warp - 4;
+        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        float suffix = 0.f;  // SEG_STATE: log decay of the chunks after this one
+        float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), j) : 0.f;
+        // output rows of chunk i: o_j = e^{b_j} O_j (factored chunks) or O_j, staged as
+        // bf16 in the chunk's Q slot (free once MMA3 is done) and written by one TMA store
+        auto epilogue = [&](int i, float sc) {
             const int n0 = chunk_start(i);
-            const int len = min(kC, N - n0);
-            // chunk-local inclusive cumsum of log gates
-            float lg = (j < len) ? log_gate(logits[((size_t)b * N + n0 + j) * H + h], inv_tau) : 0.f;
-            float x = lg;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                float y = __shfl_up_sync(0xffffffffu, x, off);
-                if (lane >= off) x += y;
-            }
-            if (lane == 31) sm.wsum[w4] = x;
-            named_bar(1, 128);
-            float pre = 0.f;
-            for (int w = 0; w < w4; ++w) pre += sm.wsum[w];
-            const float bj = x + pre;
-            const float bC = sm.wsum[0] + sm.wsum[1] + sm.wsum[2] + sm.wsum[3];
-            sm.bsm[j] = bj;
-            const bool factor = (bC > -80.f);  // e^{-b_k} stays finite: use e^{b_j} e^{-b_k}
-            sm.eneg[j] = factor ? __expf(-bj) : 0.f;
-            named_bar(1, 128);  // bsm / eneg complete; wsum may be reused next chunk
-
+            const int s = i % kStages;
             bool ok = true;
+            if (j == 0) {
+                ok = mbar_wait(&sm.o_full[i & 1], (i / 2) & 1, abort_flag);
+                if (!ok) report(err, &sm.abort_flag, 6);
+                sm.go1 = ok && !*abort_flag;
+            }
+            named_bar(1, 128);
+            if (!sm.go1) return false;
+            tc_fence_after();
+            uint8_t *stage_o = stage_q(s);
+            const uint32_t o_t = tmem + kColO + 128 * (i & 1) + lane_base;
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t r[32];
+                tmem_ld32(o_t + cb * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<uint4 *>(stage_o + tile_chunk(j, cb * 4 + q4)) = make_uint4(
+                        pack_bf16x2(__uint_as_float(r[8 * q4]) * sc, __uint_as_float(r[8 * q4 + 1]) * sc),
+                        pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * sc, __uint_as_float(r[8 * q4 + 3]) * sc),
+                        pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * sc, __uint_as_float(r[8 * q4 + 5]) * sc),
+                        pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * sc, __uint_as_float(r[8 * q4 + 7]) * sc));
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            named_bar(1, 128);
+            if (j == 0) {
+                mbar_arrive(&sm.o_free[i & 1]);
+                tma_store_4d(&tm_o, stage_o, 0, h, n0, b);
+                tma_store_4d(&tm_o, stage_o + kHalf, 64, h, n0, b);
+                bulk_commit_group();
+                bulk_wait_read_all();
+                mbar_arrive(&sm.qfree[s]);
+            }
+            return true;
+        };
+        float prev_sc = 1.f;
+        bool alive = true;
+        for (int i = 0; i < nchunks && alive; ++i) {
+            const int s = i % kStages;
+            float bC;
+            const float bj = group_scan(lg_next, sm.wsum1, lane, wq, 1, bC);
+            if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), j);  // in flight during this chunk
+            const bool factor = (bC > kFactorMin);
             if (MODE == MODE_OUTPUT) {
+                sm.ew[j] = factor ? __expf(-bj) : bj;
+                sm.kw[i & 1][j] = __expf(bC - bj);  // K'_j = e^{b_C - b_j} k_j, applied by the state warps
                 if (j == 0) {
-                    ok = mbar_wait(&sm.as_full, i & 1, abort_flag);
-                    if (ok && i > 0) ok = mbar_wait(&sm.o_full, (i - 1) & 1, abort_flag);  // MMA2(i-1) done with P
-                    if (!ok) report(err, &sm.abort_flag, 3);
-                    sm.go1 = ok && !*abort_flag;
+                    sm.bcr[i & 3] = bC;
+                    mbar_arrive(&sm.bc_ready[i & 1]);
                 }
-                named_bar(1, 128);
-                if (!sm.go1) break;
+            }
+            named_bar(1, 128);  // ew complete; wsum1 free for the next chunk
+            bool ok = true;
+            if (j == 0) {
+                ok = (MODE == MODE_OUTPUT) ? mbar_wait(&sm.as_full, i & 1, abort_flag)
+                                           : mbar_wait(&sm.full[s], (i / kStages) & 1, abort_flag);
+                if (!ok) report(err, &sm.abort_flag, 3);
+                sm.go1 = ok && !*abort_flag;
+            }
+            named_bar(1, 128);
+            if (!sm.go1) {
+                alive = false;
+                break;
+            }
+            if (MODE == MODE_OUTPUT) {
                 tc_fence_after();
-                const float ebj = __expf(bj);
+                // P row j over A row j, written in place as packed bf16 (keys 2c, 2c+1 in column c)
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t r[32];
                     tmem_ld32(tmem + kColA + lane_base + cb * 32, r);
                     tmem_wait_ld();
                     uint32_t pk[16];
+                    if (factor) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int k0 = cb * 32 + 2 * e;
-                        float v0 = 0.f, v1 = 0.f;
-                        if (k0 <= j) v0 = __uint_as_float(r[2 * e]) * (factor ? ebj * sm.eneg[k0] : __expf(bj - sm.bsm[k0]));
-                        if (k0 + 1 <= j)
-                            v1 = __uint_as_float(r[2 * e + 1]) * (factor ? ebj * sm.eneg[k0 + 1] : __expf(bj - sm.bsm[k0 + 1]));
-                        pk[e] = pack_bf16x2(v0, v1);
-                    }
-                    // keys cb*32 .. cb*32+31 -> 4 chunks of 16 B in row j of P
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const int k0 = cb * 32 + 4 * e4;
+                            const float4 w = *reinterpret_cast<const float4 *>(&sm.ew[k0]);
+                            const float v0 = (k0 <= j) ? __uint_as_float(r[4 * e4]) * w.x : 0.f;
+                            const float v1 = (k0 + 1 <= j) ? __uint_as_float(r[4 * e4 + 1]) * w.y : 0.f;
+                            const float v2 = (k0 + 2 <= j) ? __uint_as_float(r[4 * e4 + 2]) * w.z : 0.f;
+                            const float v3 = (k0 + 3 <= j) ? __uint_as_float(r[4 * e4 + 3]) * w.w : 0.f;
+                            pk[2 * e4] = pack_bf16x2(v0, v1);
+                            pk[2 * e4 + 1] = pack_bf16x2(v2, v3);
+                        }
+                    } else {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const int key = cb * 32 + q4 * 8;
-                        const uint32_t off = (uint32_t)(key >> 6) * kHalf + (uint32_t)j * 128u +
-                                             (uint32_t)((((key & 63) >> 3) ^ (j & 7)) * 16);
-                        *reinterpret_cast<uint4 *>(Pbuf + off) =
-                            make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                        for (int e = 0; e < 16; ++e) {
+                            const int k0 = cb * 32 + 2 * e;
+                            const float v0 = (k0 <= j) ? __uint_as_float(r[2 * e]) * __expf(bj - sm.ew[k0]) : 0.f;
+                            const float v1 = (k0 + 1 <= j) ? __uint_as_float(r[2 * e + 1]) * __expf(bj - sm.ew[k0 + 1]) : 0.f;
+                            pk[e] = pack_bf16x2(v0, v1);
+                        }
                     }
+                    tmem_st16(tmem + kColA + lane_base + cb * 16, pk);  // columns already read
                 }
+                tmem_wait_st();
                 tc_fence_before();
-                scale_row_inplace(stage_q(s), j, ebj);          // Q'_j = e^{b_j} q_j
-                scale_row_inplace(stage_k(s), j, __expf(bC - bj));  // K'_j = e^{b_C - b_j} k_j
+                if (!factor) scale_row_inplace(stage_q(s), j, __expf(bj));  // Q'_j = e^{b_j} q_j
             } else {
-                if (j == 0) {
-                    ok = mbar_wait(&sm.full[s], (i / kStages) & 1, abort_flag);
-                    if (!ok) report(err, &sm.abort_flag, 3);
-                    sm.go1 = ok && !*abort_flag;
-                }
-                named_bar(1, 128);
-                if (!sm.go1) break;
                 // weight of token j: decay from j to the segment end
                 scale_row_inplace(stage_k(s), j, __expf(suffix + (bC - bj)));
                 suffix += bC;
             }
             fence_proxy_async_smem();
-            if (MODE == MODE_OUTPUT && j == 0) sm.bc[i & 3] = bC;
             named_bar(1, 128);
-            if (j == 0) {
-                if (MODE == MODE_OUTPUT) mbar_arrive(&sm.as_free);
-                mbar_arrive(&sm.pq_ready[s]);
+            if (j == 0) mbar_arrive(&sm.pq_ready[s]);
+            if (MODE == MODE_OUTPUT) {
+                if (i > 0) alive = epilogue(i - 1, prev_sc);  // overlaps MMA4 / MMA2 of this chunk
+                prev_sc = factor ? __expf(bj) : 1.f;
             }
         }
+        if (MODE == MODE_OUTPUT && alive && nchunks > 0) epilogue(nchunks - 1, prev_sc);
+        if (MODE == MODE_OUTPUT && j == 0) bulk_wait_all();  // output stores complete before exit
         if (MODE == MODE_SEG_STATE && j == 0 && G_out) G_out[bhp] = suffix;
     } else {
-        // ------------------------------------------- state warps + output
-        const int c = tid;  // d_v column = TMEM lane
+        // ------------------------------------------------------- state warps
+        const int t = tid;  // TMEM lane: d_k row t of S and U
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         if (MODE == MODE_OUTPUT) {
-            float S[kD];  // S^T row c: S[i] = S[i][c]
+            float S[kD];  // row t of the state, fp32
+            if (S_in) {
+                const float4 *src = reinterpret_cast<const float4 *>(S_in + bhp * kD * kD + (size_t)t * kD);
 #pragma unroll
-            for (int i = 0; i < kD; ++i) S[i] = S_in ? S_in[bhp * kD * kD + (size_t)i * kD + c] : 0.f;
-            auto put_state = [&]() {  // bf16 S^T into TMEM columns kColS.. (A operand of MMA3)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(S[32 * q + 2 * e], S[32 * q + 2 * e + 1]);
-                    tmem_st16(tmem + kColS + lane_base + 16 * q, pk);
+                for (int c4 = 0; c4 < kD / 4; ++c4) {
+                    const float4 x = src[c4];
+                    S[4 * c4] = x.x; S[4 * c4 + 1] = x.y; S[4 * c4 + 2] = x.z; S[4 * c4 + 3] = x.w;
                 }
-                tmem_wait_st();
-                tc_fence_before();
+            } else {
+#pragma unroll
+                for (int c = 0; c < kD; ++c) S[c] = 0.f;
+            }
+            auto put_state = [&]() {  // bf16 row t of S into the N-major B tile
+#pragma unroll
+                for (int ch = 0; ch < 16; ++ch) {
+                    uint4 v = make_uint4(pack_bf16x2(S[8 * ch], S[8 * ch + 1]), pack_bf16x2(S[8 * ch + 2], S[8 * ch + 3]),
+                                         pack_bf16x2(S[8 * ch + 4], S[8 * ch + 5]), pack_bf16x2(S[8 * ch + 6], S[8 * ch + 7]));
+                    *reinterpret_cast<uint4 *>(Sbuf + tile_chunk(t, ch)) = v;
+                }
+                fence_proxy_async_smem();
             };
             put_state();
             named_bar(2, 128);
-            if (c == 0) mbar_arrive(&sm.s_ready);
+            if (t == 0) mbar_arrive(&sm.s_ready);
             for (int i = 0; i < nchunks; ++i) {
-                const int n0 = chunk_start(i);
-                const int len = min(kC, N - n0);
+                const int s = i % kStages;
                 bool ok = true;
-                if (c == 0) {
+                // K'_t = e^{b_C - b_t} k_t in place, once MMA1 has read K (in parallel with P)
+                if (t == 0) {
+                    ok = mbar_wait(&sm.bc_ready[i & 1], (i / 2) & 1, abort_flag);
+                    if (ok) ok = mbar_wait(&sm.as_full, i & 1, abort_flag);
+                    if (!ok) report(err, &sm.abort_flag, 7);
+                    sm.go0 = ok && !*abort_flag;
+                }
+                named_bar(2, 128);
+                if (!sm.go0) break;
+                scale_row_inplace(stage_k(s), t, sm.kw[i & 1][t]);
+                fence_proxy_async_smem();
+                named_bar(2, 128);
+                if (t == 0) mbar_arrive(&sm.k_ready[s]);
+                if (t == 0) {
                     ok = mbar_wait(&sm.u_full, i & 1, abort_flag);
                     if (!ok) report(err, &sm.abort_flag, 4);
                     sm.go0 = ok && !*abort_flag;
@@ -365,7 +481,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 named_bar(2, 128);
                 if (!sm.go0) break;
                 tc_fence_after();
-                const float ebC = __expf(sm.bc[i & 3]);
+                const float ebC = __expf(sm.bcr[i & 3]);  // published before MMA4 of this chunk
 #pragma unroll
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t r[32];
@@ -375,48 +491,31 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     for (int e = 0; e < 32; ++e) S[cb * 32 + e] = fmaf(ebC, S[cb * 32 + e], __uint_as_float(r[e]));
                 }
                 tc_fence_before();
+                if (i + 1 < nchunks) put_state();  // MMA3 of this chunk is done (u_full)
                 named_bar(2, 128);
-                if (c == 0) mbar_arrive(&sm.u_free);
-                if (i + 1 < nchunks) {
-                    put_state();
-                    named_bar(2, 128);
-                    if (c == 0) mbar_arrive(&sm.s_ready);
+                if (t == 0) {
+                    mbar_arrive(&sm.u_free);
+                    if (i + 1 < nchunks) mbar_arrive(&sm.s_ready);
                 }
-                // output rows of this chunk: o[n0 + j][c] = O^T[c][j]
-                tc_fence_after();
-                bf16_t *ocol = o + (((size_t)b * N + n0) * H + h) * kD + c;
-                const size_t rstride = (size_t)H * kD;
-#pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + kColO + lane_base + cb * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int jq = cb * 32 + e;
-                        if (jq < len) ocol[(size_t)jq * rstride] = from_f32<bf16_t>(__uint_as_float(r[e]));
-                    }
-                }
-                tc_fence_before();
-                named_bar(2, 128);
-                if (c == 0) mbar_arrive(&sm.o_free);
             }
             named_bar(2, 128);
-            if (c == 0) sm.go0 = !*abort_flag;
+            if (t == 0) sm.go0 = !*abort_flag;
             named_bar(2, 128);
             if (S_out && sm.go0) {
+                float4 *dst = reinterpret_cast<float4 *>(S_out + bhp * kD * kD + (size_t)t * kD);
 #pragma unroll
-                for (int i = 0; i < kD; ++i) S_out[bhp * kD * kD + (size_t)i * kD + c] = S[i];
+                for (int c4 = 0; c4 < kD / 4; ++c4) dst[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
             }
         } else {
             bool ok = true;
-            if (c == 0) {
+            if (t == 0) {
                 ok = mbar_wait(&sm.u_full, 0, abort_flag, 4000000000ull);
                 if (!ok) report(err, &sm.abort_flag, 5);
                 sm.go0 = ok && !*abort_flag;
             }
             named_bar(2, 128);
             if (sm.go0) {
+                // E^T row t (lane = d_v column t) -> E[i][t]
                 tc_fence_after();
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
@@ -425,7 +524,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        S_out[bhp * kD * kD + (size_t)(cb * 32 + e) * kD + c] = __uint_as_float(r[e]);
+                        S_out[bhp * kD * kD + (size_t)(cb * 32 + e) * kD + t] = __uint_as_float(r[e]);
                 }
             }
         }
@@ -496,8 +595,9 @@ size_t gret_tc_workspace(int B, int N, int H, int dk, int dv) {
 }
 
 cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, a.q, a.B, a.N, a.H) || !make_map(&mk, a.k, a.B, a.N, a.H) || !make_map(&mv, a.v, a.B, a.N, a.H))
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, a.q, a.B, a.N, a.H) || !make_map(&mk, a.k, a.B, a.N, a.H) || !make_map(&mv, a.v, a.B, a.N, a.H) ||
+        !make_map(&mo, a.o, a.B, a.N, a.H))
         return cudaErrorInvalidValue;
     int P = tc_segments(a.B, a.N, a.H);
     const int seg_len = tc_seg_len(a.N, P);
@@ -516,16 +616,16 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     if (P == 1) {
         count_launches(1);
         gret_tc_kernel<MODE_OUTPUT><<<grid, kTcThreads, kTcSmemBytes, st>>>(
-            mq, mk, mv, a.logits, inv_tau, (bf16_t *)a.o, a.state, a.state, nullptr, a.N, a.H, seg_len, 1, err);
+            mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, a.state, nullptr, a.N, a.H, seg_len, 1, err);
         return cudaGetLastError();
     }
     count_launches(3);
     gret_tc_kernel<MODE_SEG_STATE><<<grid, kTcThreads, kTcSmemBytes, st>>>(
-        mq, mk, mv, a.logits, inv_tau, nullptr, nullptr, E, G, a.N, a.H, seg_len, P, err);
+        mq, mk, mv, mo, a.logits, inv_tau, nullptr, nullptr, E, G, a.N, a.H, seg_len, P, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if ((e = gret_scan_launch(E, G, a.state, a.B * a.H, P, kD * kD, st)) != cudaSuccess) return e;
     gret_tc_kernel<MODE_OUTPUT><<<grid, kTcThreads, kTcSmemBytes, st>>>(
-        mq, mk, mv, a.logits, inv_tau, (bf16_t *)a.o, E, nullptr, nullptr, a.N, a.H, seg_len, P, err);
+        mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, E, nullptr, nullptr, a.N, a.H, seg_len, P, err);
     return cudaGetLastError();
 }
 

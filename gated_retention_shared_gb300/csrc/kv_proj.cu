@@ -119,16 +119,102 @@ proj_append_simt(const T *__restrict__ M, const T *__restrict__ g, const T *__re
     finish_append(len_dev, len + T_rows);
 }
 
+// Few rows (decode): split-K GEMV.  CTA (column group, K slice) of 256 threads;
+// thread = 8 consecutive output columns (one 16-byte row segment of W), looping
+// over its slice of W rows and over the input rows 4 at a time; fp32 partials
+// go to the workspace and proj_gemv_finish sums them.
+template <typename T>
+__global__ void __launch_bounds__(256)
+proj_gemv_partial(const T *__restrict__ M, const T *__restrict__ g, const T *__restrict__ Wk,
+                  const T *__restrict__ Wv, float *__restrict__ part, int R, int dm, int n, int rows_per_split) {
+    const int col = (blockIdx.x * 256 + threadIdx.x) * 8;  // in [0, 2n)
+    const int k0 = blockIdx.y * rows_per_split;
+    const int k1 = min(dm, k0 + rows_per_split);
+    extern __shared__ float msh[];  // [R][rows_per_split]
+    for (int e = threadIdx.x; e < R * rows_per_split; e += 256) {
+        int r = e / rows_per_split, kk = k0 + e % rows_per_split;
+        float x = 0.f;
+        if (kk < k1) {
+            x = to_f32(M[(size_t)r * dm + kk]);
+            if (g) x *= to_f32(g[kk]);
+        }
+        msh[e] = x;
+    }
+    __syncthreads();
+    if (col >= 2 * n) return;
+    const T *W = (col < n) ? Wk : Wv;
+    const int wc = col % n;
+    for (int r0 = 0; r0 < R; r0 += 4) {
+        float acc[4][8] = {};
+        for (int kk = k0; kk < k1; ++kk) {
+            float w[8];
+            if constexpr (sizeof(T) == 2) {
+                uint4 u = *reinterpret_cast<const uint4 *>(W + (size_t)kk * n + wc);
+                uint32_t x[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    w[2 * e] = __uint_as_float(x[e] << 16);
+                    w[2 * e + 1] = __uint_as_float(x[e] & 0xFFFF0000u);
+                }
+            } else {
+                const float4 *p = reinterpret_cast<const float4 *>(W + (size_t)kk * n + wc);
+                float4 a = p[0], b = p[1];
+                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+            }
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const float m = (r0 + rr < R) ? msh[(r0 + rr) * rows_per_split + (kk - k0)] : 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[rr][e] = fmaf(m, w[e], acc[rr][e]);
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            if (r0 + rr >= R) break;
+            float4 *dst = reinterpret_cast<float4 *>(part + ((size_t)blockIdx.y * R + r0 + rr) * 2 * n + col);
+            dst[0] = make_float4(acc[rr][0], acc[rr][1], acc[rr][2], acc[rr][3]);
+            dst[1] = make_float4(acc[rr][4], acc[rr][5], acc[rr][6], acc[rr][7]);
+        }
+    }
+}
+
+// sum the K slices, apply the RMS factor, round once, write the cache slot
+template <typename T>
+__global__ void proj_gemv_finish(const float *__restrict__ part, const float *__restrict__ r, T *__restrict__ kc,
+                                 T *__restrict__ vc, int R, int T_rows, int n, int Hkv, int d, int64_t cap,
+                                 int64_t len, int splits, int32_t *len_dev) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;  // over R * 2n
+    if (idx < R * 2 * n) {
+        const int row = idx / (2 * n), col = idx % (2 * n);
+        float acc = 0.f;
+        for (int s = 0; s < splits; ++s) acc += part[((size_t)s * R + row) * 2 * n + col];
+        const int b = row / T_rows, t = row % T_rows;
+        const int cn = col % n, h = cn / d, c = cn % d;
+        T *dst = (col < n) ? kc : vc;
+        dst[(((size_t)b * Hkv + h) * cap + len + t) * d + c] = from_f32<T>(acc * r[row]);
+    }
+    finish_append(len_dev, len + T_rows);
+}
+
 }  // namespace yoco
 
 namespace yoco_host {
 using namespace yoco;
 
-// workspace: [0, 256) status word of the tensor-core kernel, then one fp32 RMS factor per row
+constexpr int kGemvMaxRows = 16;
+constexpr int kGemvSplits = 128;
+
+static bool gemv_eligible(int R, int n) { return R <= kGemvMaxRows && n % 8 == 0; }
+
+// workspace: [0, 256) status word of the tensor-core kernel, one fp32 RMS factor
+// per row, then (few-row path) the split-K partials
 size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt) {
-    (void)dm; (void)Hkv; (void)d; (void)dt;
+    (void)dm; (void)dt;
     size_t rows = (size_t)B * T;
-    return 256 + ((rows * sizeof(float) + 255) / 256) * 256;
+    size_t ws = 256 + ((rows * sizeof(float) + 255) / 256) * 256;
+    const int n = Hkv * d;
+    if (gemv_eligible((int)rows, n)) ws += (size_t)kGemvSplits * rows * 2 * n * sizeof(float);
+    return ws;
 }
 
 template <typename T>
@@ -140,6 +226,21 @@ static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a)) return kv_project_append_tc(a, r, (int *)ws, st);
+    const int n = a.Hkv * a.d;
+    if (gemv_eligible(R, n)) {
+        float *part = r + ((size_t)R + 63) / 64 * 64;
+        const int rows_per_split = (a.dm + kGemvSplits - 1) / kGemvSplits;
+        const int splits = (a.dm + rows_per_split - 1) / rows_per_split;
+        dim3 g1((2 * n / 8 + 255) / 256, splits);
+        count_launches(2);
+        proj_gemv_partial<T><<<g1, 256, (size_t)R * rows_per_split * sizeof(float), st>>>(
+            (const T *)a.M, (const T *)a.rms_w, (const T *)a.Wk, (const T *)a.Wv, part, R, a.dm, n, rows_per_split);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        const int total = R * 2 * n;
+        proj_gemv_finish<T><<<(total + 255) / 256, 256, 0, st>>>(part, r, (T *)a.kc, (T *)a.vc, R, a.T, n, a.Hkv, a.d,
+                                                                 a.cap, a.len, splits, a.len_dev);
+        return cudaGetLastError();
+    }
     count_launches(1);
     dim3 grid((2 * a.Hkv * a.d + 63) / 64, (R + 63) / 64);
     proj_append_simt<T><<<grid, 256, 0, st>>>((const T *)a.M, (const T *)a.rms_w, (const T *)a.Wk, (const T *)a.Wv,

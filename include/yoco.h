@@ -136,6 +136,7 @@ YOCO_API yoco_status yoco_gret_decode_step(const void *q, const void *k, const v
  *   M      [B, T, dm]       cache dtype
  *   rms_w  [dm] gain g      cache dtype, or NULL for ones
  *   Wk, Wv [dm, Hkv * d]    cache dtype; column h*d + c feeds head h, lane c
+ * All four pointers 16-byte aligned.
  * Exactly slots [len, len + T) change; every other cache byte is untouched.
  * Returns YOCO_ERR_CAPACITY (nothing written) if len + T > capacity.
  *   workspace  >= yoco_shared_kv_workspace_size bytes, 256-byte aligned.
