@@ -57,7 +57,7 @@ enum : int { MODE_OUTPUT = 0, MODE_SEG_STATE = 1 };
 
 struct TcSmem {
     uint64_t full[kStages], empty[kStages], pq_ready[kStages], o_free[2], bc_ready[2], o_full[2];
-    uint64_t qfree[kStages], k_ready[kStages];
+    uint64_t full_v[kStages], vfree[kStages], k_ready[kStages];
     uint64_t as_full, p_free, u_full, u_free, s_ready, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -70,6 +70,7 @@ struct TcSmem {
 
 constexpr size_t kTileBytes = (size_t)kStages * 3 * kTile + kTile;  // Q,K,V per stage + bf16 state
 constexpr size_t kTcSmemBytes = 232448;                            // the sm_100 per-block maximum
+static_assert(kTileBytes + sizeof(TcSmem) + 1024 <= kTcSmemBytes, "tiles + control block + alignment slack must fit");
 
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
 
@@ -161,7 +162,8 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_init(&sm.o_free[s], 1);
             mbar_init(&sm.bc_ready[s], 1);
             mbar_init(&sm.o_full[s], 1);
-            mbar_init(&sm.qfree[s], 1);
+            mbar_init(&sm.full_v[s], 1);
+            mbar_init(&sm.vfree[s], 1);
             mbar_init(&sm.k_ready[s], 1);
         }
         mbar_init(&sm.as_full, 1);
@@ -198,7 +200,9 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             if (MODE == MODE_OUTPUT) tma_prefetch_desc(&tm_q);
-            const uint32_t bytes = (MODE == MODE_OUTPUT) ? 3 * kTile : 2 * kTile;
+            // OUTPUT: Q and K complete `full`, V completes `full_v` (the V slot doubles as
+            // the staging buffer of the output store two chunks back).  SEG_STATE: K and
+            // V complete `full`.
             for (int i = 0; i < nchunks; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages && !mbar_wait(&sm.empty[s], ((i / kStages) + 1) & 1, abort_flag)) {
@@ -206,24 +210,29 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     break;
                 }
                 const int n0 = chunk_start(i);
-                mbar_arrive_expect_tx(&sm.full[s], bytes);
+                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
                 for (int half = 0; half < 2; ++half) {
                     tma_load_4d(stage_k(s) + half * kHalf, &tm_k, &sm.full[s], half * 64, h, n0, b);
-                    tma_load_4d(stage_v(s) + half * kHalf, &tm_v, &sm.full[s], half * 64, h, n0, b);
+                    if (MODE == MODE_OUTPUT)
+                        tma_load_4d(stage_q(s) + half * kHalf, &tm_q, &sm.full[s], half * 64, h, n0, b);
+                    else
+                        tma_load_4d(stage_v(s) + half * kHalf, &tm_v, &sm.full[s], half * 64, h, n0, b);
                 }
                 if (MODE == MODE_OUTPUT) {
-                    // the Q slot doubles as the staging buffer of chunk i-2's output store
-                    if (i >= kStages && !mbar_wait(&sm.qfree[s], ((i / kStages) + 1) & 1, abort_flag)) {
+                    if (i >= kStages && !mbar_wait(&sm.vfree[s], ((i / kStages) + 1) & 1, abort_flag)) {
                         report(err, &sm.abort_flag, 8);
                         break;
                     }
+                    mbar_arrive_expect_tx(&sm.full_v[s], kTile);
                     for (int half = 0; half < 2; ++half)
-                        tma_load_4d(stage_q(s) + half * kHalf, &tm_q, &sm.full[s], half * 64, h, n0, b);
+                        tma_load_4d(stage_v(s) + half * kHalf, &tm_v, &sm.full_v[s], half * 64, h, n0, b);
                 }
             }
             // leave no copy in flight: wait for the last loads of each stage
-            for (int i = max(0, nchunks - kStages); i < nchunks; ++i)
+            for (int i = max(0, nchunks - kStages); i < nchunks; ++i) {
                 mbar_wait(&sm.full[i % kStages], (i / kStages) & 1, abort_flag, 200000000ull);
+                if (MODE == MODE_OUTPUT) mbar_wait(&sm.full_v[i % kStages], (i / kStages) & 1, abort_flag, 200000000ull);
+            }
         }
     } else if (warp == 9) {
         // --------------------------------------------------------- MMA issuer
@@ -270,6 +279,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tc_fence_after();
                     mma3();
                     if (!(ok = mbar_wait(&sm.k_ready[s], (i / kStages) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait(&sm.full_v[s], (i / kStages) & 1, abort_flag))) break;
                     if (i > 0 && !(ok = mbar_wait(&sm.u_free, (i - 1) & 1, abort_flag))) break;
                     tc_fence_after();
                     for (int kk = 0; kk < 8; ++kk)  // MMA4: U = K'^T V
@@ -306,49 +316,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
         float suffix = 0.f;  // SEG_STATE: log decay of the chunks after this one
         float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), j) : 0.f;
-        // output rows of chunk i: o_j = e^{b_j} O_j (factored chunks) or O_j, staged as
-        // bf16 in the chunk's Q slot (free once MMA3 is done) and written by one TMA store
-        auto epilogue = [&](int i, float sc) {
-            const int n0 = chunk_start(i);
-            const int s = i % kStages;
-            bool ok = true;
-            if (j == 0) {
-                ok = mbar_wait(&sm.o_full[i & 1], (i / 2) & 1, abort_flag);
-                if (!ok) report(err, &sm.abort_flag, 6);
-                sm.go1 = ok && !*abort_flag;
-            }
-            named_bar(1, 128);
-            if (!sm.go1) return false;
-            tc_fence_after();
-            uint8_t *stage_o = stage_q(s);
-            const uint32_t o_t = tmem + kColO + 128 * (i & 1) + lane_base;
-#pragma unroll 1
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t r[32];
-                tmem_ld32(o_t + cb * 32, r);
-                tmem_wait_ld();
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<uint4 *>(stage_o + tile_chunk(j, cb * 4 + q4)) = make_uint4(
-                        pack_bf16x2(__uint_as_float(r[8 * q4]) * sc, __uint_as_float(r[8 * q4 + 1]) * sc),
-                        pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * sc, __uint_as_float(r[8 * q4 + 3]) * sc),
-                        pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * sc, __uint_as_float(r[8 * q4 + 5]) * sc),
-                        pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * sc, __uint_as_float(r[8 * q4 + 7]) * sc));
-            }
-            tc_fence_before();
-            fence_proxy_async_smem();
-            named_bar(1, 128);
-            if (j == 0) {
-                mbar_arrive(&sm.o_free[i & 1]);
-                tma_store_4d(&tm_o, stage_o, 0, h, n0, b);
-                tma_store_4d(&tm_o, stage_o + kHalf, 64, h, n0, b);
-                bulk_commit_group();
-                bulk_wait_read_all();
-                mbar_arrive(&sm.qfree[s]);
-            }
-            return true;
-        };
-        float prev_sc = 1.f;
         bool alive = true;
         for (int i = 0; i < nchunks && alive; ++i) {
             const int s = i % kStages;
@@ -420,13 +387,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             fence_proxy_async_smem();
             named_bar(1, 128);
             if (j == 0) mbar_arrive(&sm.pq_ready[s]);
-            if (MODE == MODE_OUTPUT) {
-                if (i > 0) alive = epilogue(i - 1, prev_sc);  // overlaps MMA4 / MMA2 of this chunk
-                prev_sc = factor ? __expf(bj) : 1.f;
-            }
         }
-        if (MODE == MODE_OUTPUT && alive && nchunks > 0) epilogue(nchunks - 1, prev_sc);
-        if (MODE == MODE_OUTPUT && j == 0) bulk_wait_all();  // output stores complete before exit
         if (MODE == MODE_SEG_STATE && j == 0 && G_out) G_out[bhp] = suffix;
     } else {
         // ------------------------------------------------------- state warps
@@ -469,7 +430,8 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 named_bar(2, 128);
                 if (!sm.go0) break;
-                scale_row_inplace(stage_k(s), t, sm.kw[i & 1][t]);
+                const float kwt = sm.kw[i & 1][t];  // read now: the ring slot is reused two chunks on
+                scale_row_inplace(stage_k(s), t, kwt);
                 fence_proxy_async_smem();
                 named_bar(2, 128);
                 if (t == 0) mbar_arrive(&sm.k_ready[s]);
@@ -497,7 +459,50 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     mbar_arrive(&sm.u_free);
                     if (i + 1 < nchunks) mbar_arrive(&sm.s_ready);
                 }
+                // output rows o_t = e^{b_t} O_t (or O_t), staged as bf16 in this chunk's
+                // V slot (free once MMA2 is done) and written by two TMA stores
+                if (t == 0) {
+                    ok = mbar_wait(&sm.o_full[i & 1], (i / 2) & 1, abort_flag);
+                    if (!ok) report(err, &sm.abort_flag, 6);
+                    sm.go0 = ok && !*abort_flag;
+                }
+                named_bar(2, 128);
+                if (!sm.go0) break;
+                tc_fence_after();
+                {
+                    const int n0 = chunk_start(i);
+                    // e^{b_t} = e^{b_C} / e^{b_C - b_t}; both finite in factored chunks
+                    const float bCi = sm.bcr[i & 3];
+                    const float sc = (bCi > kFactorMin) ? __expf(bCi) / kwt : 1.f;
+                    uint8_t *stage_o = stage_v(s);
+                    const uint32_t o_t = tmem + kColO + 128 * (i & 1) + lane_base;
+#pragma unroll 1
+                    for (int cb = 0; cb < 4; ++cb) {
+                        uint32_t r[32];
+                        tmem_ld32(o_t + cb * 32, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            *reinterpret_cast<uint4 *>(stage_o + tile_chunk(t, cb * 4 + q4)) = make_uint4(
+                                pack_bf16x2(__uint_as_float(r[8 * q4]) * sc, __uint_as_float(r[8 * q4 + 1]) * sc),
+                                pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * sc, __uint_as_float(r[8 * q4 + 3]) * sc),
+                                pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * sc, __uint_as_float(r[8 * q4 + 5]) * sc),
+                                pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * sc, __uint_as_float(r[8 * q4 + 7]) * sc));
+                    }
+                    tc_fence_before();
+                    fence_proxy_async_smem();
+                    named_bar(2, 128);
+                    if (t == 0) {
+                        mbar_arrive(&sm.o_free[i & 1]);
+                        tma_store_4d(&tm_o, stage_o, 0, h, n0, b);
+                        tma_store_4d(&tm_o, stage_o + kHalf, 64, h, n0, b);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                        mbar_arrive(&sm.vfree[s]);
+                    }
+                }
             }
+            if (t == 0) bulk_wait_all();  // output stores complete before exit
             named_bar(2, 128);
             if (t == 0) sm.go0 = !*abort_flag;
             named_bar(2, 128);
