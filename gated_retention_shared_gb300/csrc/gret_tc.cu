@@ -62,10 +62,10 @@ struct TcSmem {
     uint32_t tmem_base;
     int abort_flag;
     int go0, go1;  // per-group continue decisions (written by one thread, read by all after a barrier)
-    float wsum1[4];
+    float wsum0[4], wsum1[4];
     float bcr[4];  // chunk total log decay b_C, ring over chunks
     float ew[kC];  // e^{-b_k} (factored chunks) or b_k (direct chunks)
-    float kw[2][kC];  // K row weights e^{b_C - b_k}, ring over chunks
+
 };
 
 constexpr size_t kTileBytes = (size_t)kStages * 3 * kTile + kTile;  // Q,K,V per stage + bf16 state
@@ -325,7 +325,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const bool factor = (bC > kFactorMin);
             if (MODE == MODE_OUTPUT) {
                 sm.ew[j] = factor ? __expf(-bj) : bj;
-                sm.kw[i & 1][j] = __expf(bC - bj);  // K'_j = e^{b_C - b_j} k_j, applied by the state warps
                 if (j == 0) {
                     sm.bcr[i & 3] = bC;
                     mbar_arrive(&sm.bc_ready[i & 1]);
@@ -345,6 +344,11 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 break;
             }
             if (MODE == MODE_OUTPUT) {
+                // K'_j = e^{b_C - b_j} k_j in place first: MMA4 and the state chain wait on it
+                scale_row_inplace(stage_k(s), j, __expf(bC - bj));
+                fence_proxy_async_smem();
+                named_bar(1, 128);
+                if (j == 0) mbar_arrive(&sm.k_ready[s]);
                 tc_fence_after();
                 // P row j over A row j, written in place as packed bf16 (keys 2c, 2c+1 in column c)
 #pragma unroll 1
@@ -418,23 +422,15 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             put_state();
             named_bar(2, 128);
             if (t == 0) mbar_arrive(&sm.s_ready);
+            float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), t) : 0.f;
             for (int i = 0; i < nchunks; ++i) {
                 const int s = i % kStages;
+                // the chunk's decay, computed here too (cheap) so no ring is shared with the decay warps
+                float bC;
+                const float bt = group_scan(lg_next, sm.wsum0, lane, warp, 2, bC);
+                if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), t);
+                const float sc = (bC > kFactorMin) ? __expf(bt) : 1.f;  // output row scale
                 bool ok = true;
-                // K'_t = e^{b_C - b_t} k_t in place, once MMA1 has read K (in parallel with P)
-                if (t == 0) {
-                    ok = mbar_wait(&sm.bc_ready[i & 1], (i / 2) & 1, abort_flag);
-                    if (ok) ok = mbar_wait(&sm.as_full, i & 1, abort_flag);
-                    if (!ok) report(err, &sm.abort_flag, 7);
-                    sm.go0 = ok && !*abort_flag;
-                }
-                named_bar(2, 128);
-                if (!sm.go0) break;
-                const float kwt = sm.kw[i & 1][t];  // read now: the ring slot is reused two chunks on
-                scale_row_inplace(stage_k(s), t, kwt);
-                fence_proxy_async_smem();
-                named_bar(2, 128);
-                if (t == 0) mbar_arrive(&sm.k_ready[s]);
                 if (t == 0) {
                     ok = mbar_wait(&sm.u_full, i & 1, abort_flag);
                     if (!ok) report(err, &sm.abort_flag, 4);
@@ -443,7 +439,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 named_bar(2, 128);
                 if (!sm.go0) break;
                 tc_fence_after();
-                const float ebC = __expf(sm.bcr[i & 3]);  // published before MMA4 of this chunk
+                const float ebC = __expf(bC);
 #pragma unroll
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t r[32];
@@ -471,9 +467,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc_fence_after();
                 {
                     const int n0 = chunk_start(i);
-                    // e^{b_t} = e^{b_C} / e^{b_C - b_t}; both finite in factored chunks
-                    const float bCi = sm.bcr[i & 3];
-                    const float sc = (bCi > kFactorMin) ? __expf(bCi) / kwt : 1.f;
                     uint8_t *stage_o = stage_v(s);
                     const uint32_t o_t = tmem + kColO + 128 * (i & 1) + lane_base;
 #pragma unroll 1
