@@ -23,9 +23,10 @@
 // whole chunks.  Kernel mode SEG_STATE walks a segment backwards and accumulates
 // its zero-start end state  E^T = sum_k e^{(decay after k to segment end)} v_k^T k_k
 // directly in TMEM (every weight <= 1), plus the segment's total log decay.  A
-// small scan (gret_simt.cu) turns those into each segment's initial state, and
-// mode OUTPUT runs the chunk recurrence above from it.  With B*H >= #SMs, P = 1
-// and only OUTPUT runs.
+// OUTPUT CTA then folds the earlier segments' end states into its initial state
+// (S_start(p) = e^{G_{p-1}} S_start(p-1) + E_{p-1}) and runs the chunk recurrence
+// above from it.  The last segment's end state is the call's final state, so
+// SEG_STATE runs for P-1 segments only.  With B*H >= #SMs, P = 1 and only OUTPUT runs.
 //
 // Warp roles (320 threads): warps 0-3 keep the state (thread t = TMEM lane t =
 // d_k row t), warps 4-7 compute the decay, P, the in-place scaling of K (and Q)
@@ -57,7 +58,7 @@ enum : int { MODE_OUTPUT = 0, MODE_SEG_STATE = 1 };
 
 struct TcSmem {
     uint64_t full[kStages], empty[kStages], pq_ready[kStages], o_free[2], bc_ready[2], o_full[2];
-    uint64_t full_v[kStages], vfree[kStages], k_ready[kStages];
+    uint64_t full_v[kStages], vfree[kStages], k_ready[kStages], w_ready[2];
     uint64_t as_full, p_free, u_full, u_free, s_ready, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -112,6 +113,15 @@ __device__ __forceinline__ void scale_row_inplace(uint8_t *tile, int r, float s)
     }
 }
 
+// Scale one 64-column block (chunks 8*blk .. 8*blk+7) of row r in place.
+__device__ __forceinline__ void scale_row_block(uint8_t *tile, int r, float s, int blk) {
+#pragma unroll
+    for (int c = 8 * blk; c < 8 * blk + 8; ++c) {
+        uint4 *p = reinterpret_cast<uint4 *>(tile + tile_chunk(r, c));
+        *p = scale_bf16x8(*p, s);
+    }
+}
+
 // Inclusive cumsum of one value per thread over a 128-thread group (4 warps).
 __device__ __forceinline__ float group_scan(float x, float *wsum, int lane, int wq, int bar_id, float &total) {
 #pragma unroll
@@ -132,8 +142,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const float *__restrict__ logits, float inv_tau,
-               bf16_t *__restrict__ o, const float *__restrict__ S_in, float *__restrict__ S_out,
-               float *__restrict__ G_out, int N, int H, int seg_len, int P, int *err) {
+               bf16_t *__restrict__ o, float *__restrict__ state, float *__restrict__ E, float *__restrict__ G,
+               int N, int H, int seg_len, int P, int *err) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_u32 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base_u32 & 1023u)) & 1023u;
@@ -148,7 +158,8 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int t_begin = p * seg_len;
     const int t_end = min(N, t_begin + seg_len);
     const int nchunks = (t_end - t_begin + kC - 1) / kC;
-    const size_t bhp = ((size_t)b * H + h) * P + p;
+    const size_t bh = (size_t)b * H + h;
+    const size_t bhp = bh * P + p;  // segment slot in E / G; slot P-1 of E holds the initial state
     uint8_t *Sbuf = tiles + (size_t)kStages * 3 * kTile;  // bf16 state, MMA3's B operand
     auto stage_q = [&](int s) { return tiles + (size_t)s * 3 * kTile; };
     auto stage_k = [&](int s) { return tiles + (size_t)s * 3 * kTile + kTile; };
@@ -158,12 +169,13 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
-            mbar_init(&sm.pq_ready[s], 1);
+            mbar_init(&sm.pq_ready[s], MODE == MODE_OUTPUT ? 1 : 2);  // SEG_STATE: both groups scale K
             mbar_init(&sm.o_free[s], 1);
             mbar_init(&sm.bc_ready[s], 1);
             mbar_init(&sm.o_full[s], 1);
             mbar_init(&sm.full_v[s], 1);
             mbar_init(&sm.vfree[s], 1);
+            mbar_init(&sm.w_ready[s], 1);
             mbar_init(&sm.k_ready[s], 1);
         }
         mbar_init(&sm.as_full, 1);
@@ -384,31 +396,50 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc_fence_before();
                 if (!factor) scale_row_inplace(stage_q(s), j, __expf(bj));  // Q'_j = e^{b_j} q_j
             } else {
-                // weight of token j: decay from j to the segment end
-                scale_row_inplace(stage_k(s), j, __expf(suffix + (bC - bj)));
+                // weight of token j: decay from j to the segment end; the state warps
+                // scale the second 64 columns of every row with the same weights
+                const float w = __expf(suffix + (bC - bj));
+                float *wring = reinterpret_cast<float *>(Sbuf) + (i & 1) * kC;  // Sbuf is unused here
+                wring[j] = w;
+                named_bar(1, 128);
+                if (j == 0) mbar_arrive(&sm.w_ready[i & 1]);
+                scale_row_block(stage_k(s), j, w, 0);
                 suffix += bC;
             }
             fence_proxy_async_smem();
             named_bar(1, 128);
             if (j == 0) mbar_arrive(&sm.pq_ready[s]);
         }
-        if (MODE == MODE_SEG_STATE && j == 0 && G_out) G_out[bhp] = suffix;
+        if (MODE == MODE_SEG_STATE && j == 0) G[bhp] = suffix;
     } else {
         // ------------------------------------------------------- state warps
         const int t = tid;  // TMEM lane: d_k row t of S and U
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         if (MODE == MODE_OUTPUT) {
             float S[kD];  // row t of the state, fp32
-            if (S_in) {
-                const float4 *src = reinterpret_cast<const float4 *>(S_in + bhp * kD * kD + (size_t)t * kD);
+            {
+                // initial state of this segment: the caller's state, advanced over the
+                // earlier segments with their zero-start end states E_q and decays G_q
+                const float *init = (P == 1) ? state + bh * kD * kD : E + (bh * P + P - 1) * kD * kD;
+                const float4 *src = reinterpret_cast<const float4 *>(init + (size_t)t * kD);
 #pragma unroll
                 for (int c4 = 0; c4 < kD / 4; ++c4) {
                     const float4 x = src[c4];
                     S[4 * c4] = x.x; S[4 * c4 + 1] = x.y; S[4 * c4 + 2] = x.z; S[4 * c4 + 3] = x.w;
                 }
-            } else {
+#pragma unroll 1
+                for (int q = 0; q < p; ++q) {
+                    const float g = __expf(G[bh * P + q]);
+                    const float4 *eq = reinterpret_cast<const float4 *>(E + (bh * P + q) * kD * kD + (size_t)t * kD);
 #pragma unroll
-                for (int c = 0; c < kD; ++c) S[c] = 0.f;
+                    for (int c4 = 0; c4 < kD / 4; ++c4) {
+                        const float4 x = eq[c4];
+                        S[4 * c4] = fmaf(g, S[4 * c4], x.x);
+                        S[4 * c4 + 1] = fmaf(g, S[4 * c4 + 1], x.y);
+                        S[4 * c4 + 2] = fmaf(g, S[4 * c4 + 2], x.z);
+                        S[4 * c4 + 3] = fmaf(g, S[4 * c4 + 3], x.w);
+                    }
+                }
             }
             auto put_state = [&]() {  // bf16 row t of S into the N-major B tile
 #pragma unroll
@@ -499,13 +530,34 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             named_bar(2, 128);
             if (t == 0) sm.go0 = !*abort_flag;
             named_bar(2, 128);
-            if (S_out && sm.go0) {
-                float4 *dst = reinterpret_cast<float4 *>(S_out + bhp * kD * kD + (size_t)t * kD);
+            if (p == P - 1 && sm.go0) {  // the last segment's end state is the call's final state
+                float4 *dst = reinterpret_cast<float4 *>(state + bh * kD * kD + (size_t)t * kD);
 #pragma unroll
                 for (int c4 = 0; c4 < kD / 4; ++c4) dst[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
             }
         } else {
+            if (p == 0) {  // keep the caller's initial state: the OUTPUT pass overwrites `state`
+                const float4 *src = reinterpret_cast<const float4 *>(state + bh * kD * kD + (size_t)t * kD);
+                float4 *dst = reinterpret_cast<float4 *>(E + (bh * P + P - 1) * kD * kD + (size_t)t * kD);
+#pragma unroll 4
+                for (int c4 = 0; c4 < kD / 4; ++c4) dst[c4] = src[c4];
+            }
             bool ok = true;
+            for (int i = 0; i < nchunks; ++i) {
+                const int s = i % kStages;
+                if (t == 0) {
+                    ok = mbar_wait(&sm.w_ready[i & 1], (i / 2) & 1, abort_flag);
+                    if (!ok) report(err, &sm.abort_flag, 10);
+                    sm.go0 = ok && !*abort_flag;
+                }
+                named_bar(2, 128);
+                if (!sm.go0) break;
+                const float *wring = reinterpret_cast<const float *>(Sbuf) + (i & 1) * kC;
+                scale_row_block(stage_k(s), t, wring[t], 1);
+                fence_proxy_async_smem();
+                named_bar(2, 128);
+                if (t == 0) mbar_arrive(&sm.pq_ready[s]);
+            }
             if (t == 0) {
                 ok = mbar_wait(&sm.u_full, 0, abort_flag, 4000000000ull);
                 if (!ok) report(err, &sm.abort_flag, 5);
@@ -522,7 +574,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        S_out[bhp * kD * kD + (size_t)(cb * 32 + e) * kD + t] = __uint_as_float(r[e]);
+                        E[bhp * kD * kD + (size_t)(cb * 32 + e) * kD + t] = __uint_as_float(r[e]);
                 }
             }
         }
@@ -610,20 +662,19 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     e = cudaFuncSetAttribute(gret_tc_kernel<MODE_SEG_STATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kTcSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(P, a.H, a.B);
     if (P == 1) {
         count_launches(1);
-        gret_tc_kernel<MODE_OUTPUT><<<grid, kTcThreads, kTcSmemBytes, st>>>(
-            mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, a.state, nullptr, a.N, a.H, seg_len, 1, err);
+        gret_tc_kernel<MODE_OUTPUT><<<dim3(1, a.H, a.B), kTcThreads, kTcSmemBytes, st>>>(
+            mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, a.N, a.H, seg_len, 1, err);
         return cudaGetLastError();
     }
-    count_launches(3);
-    gret_tc_kernel<MODE_SEG_STATE><<<grid, kTcThreads, kTcSmemBytes, st>>>(
-        mq, mk, mv, mo, a.logits, inv_tau, nullptr, nullptr, E, G, a.N, a.H, seg_len, P, err);
+    // end states of segments 0 .. P-2 (the last segment's is computed by the OUTPUT pass)
+    count_launches(2);
+    gret_tc_kernel<MODE_SEG_STATE><<<dim3(P - 1, a.H, a.B), kTcThreads, kTcSmemBytes, st>>>(
+        mq, mk, mv, mo, a.logits, inv_tau, nullptr, a.state, E, G, a.N, a.H, seg_len, P, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = gret_scan_launch(E, G, a.state, a.B * a.H, P, kD * kD, st)) != cudaSuccess) return e;
-    gret_tc_kernel<MODE_OUTPUT><<<grid, kTcThreads, kTcSmemBytes, st>>>(
-        mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, E, nullptr, nullptr, a.N, a.H, seg_len, P, err);
+    gret_tc_kernel<MODE_OUTPUT><<<dim3(P, a.H, a.B), kTcThreads, kTcSmemBytes, st>>>(
+        mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, a.N, a.H, seg_len, P, err);
     return cudaGetLastError();
 }
 
