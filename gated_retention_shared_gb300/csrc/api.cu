@@ -194,7 +194,9 @@ yoco_status yoco_shared_kv_project_append(const void *M, const void *rms_w, floa
 
 size_t yoco_cross_attn_workspace_size(int B, int Hq, int T, const yoco_kv_cache *cache, int num_splits) {
     if (!cache || B <= 0 || Hq <= 0 || T <= 0 || cache->Hkv <= 0) return 0;
-    int splits = num_splits > 0 ? num_splits : attn_auto_splits(B, cache->Hkv, cache->capacity);
+    int splits = num_splits > 0 ? num_splits
+                                : attn_auto_splits(B, cache->Hkv, cache->capacity,
+                                                   attn_ctas_per_sm(cache->dtype, cache->d, Hq / cache->Hkv));
     if (T > 1 && num_splits <= 0) splits = 1;
     return attn_workspace(B, Hq, T, cache->d, splits);
 }
@@ -214,7 +216,10 @@ static yoco_status attn_common(const void *Q, int Hq, int T, int64_t p0, const y
     if (!aligned(Q, 16) || !aligned(O, 16)) return fail(YOCO_ERR_INVALID_ARG, "Q/O must be 16-byte aligned");
     if (num_splits < 0) return fail(YOCO_ERR_INVALID_ARG, "num_splits must be >= 0");
     const int64_t keys = p0 + T;
-    int splits = num_splits > 0 ? num_splits : (T == 1 ? attn_auto_splits(cache->B, cache->Hkv, keys) : 1);
+    int splits = num_splits > 0 ? num_splits
+                                : (T == 1 ? attn_auto_splits(cache->B, cache->Hkv, keys,
+                                                             attn_ctas_per_sm(cache->dtype, cache->d, Hq / cache->Hkv))
+                                          : 1);
     if (splits > 4096) return fail(YOCO_ERR_UNSUPPORTED, "num_splits above 4096");
     const size_t need = attn_workspace(cache->B, Hq, T, cache->d, splits);
     if ((s = check_ws(ws, ws_bytes, need)) != YOCO_OK) return s;

@@ -8,6 +8,8 @@
 // key for the scores, lane = 4 head-dim lanes for the value sum; each warp keeps
 // its own running max / sum / accumulator and the warps are merged at the end.
 // K/V tiles are double-buffered in shared memory with cp.async.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -269,9 +271,9 @@ using namespace yoco;
 
 static int rows_per_block(int G) { return G >= kAttnMaxQ ? 1 : kAttnMaxQ / G; }
 
-int attn_auto_splits(int B, int Hkv, int64_t keys) {
-    // about one wave of CTAs on 152 SMs with three resident CTAs each; slices of >= 2 tiles
-    int64_t want = (3 * 152 + (int64_t)B * Hkv - 1) / ((int64_t)B * Hkv);
+int attn_auto_splits(int B, int Hkv, int64_t keys, int ctas_per_sm) {
+    // about one wave of CTAs on 152 SMs; slices of >= 2 tiles
+    int64_t want = ((int64_t)ctas_per_sm * 152 + (int64_t)B * Hkv - 1) / ((int64_t)B * Hkv);
     int64_t max_by_len = (keys + 2 * kAttnTile - 1) / (2 * kAttnTile);
     if (want > max_by_len) want = max_by_len;
     if (want < 1) want = 1;
@@ -279,9 +281,12 @@ int attn_auto_splits(int B, int Hkv, int64_t keys) {
     return (int)want;
 }
 
+// workspace: [0, 256) status word of the tensor-core kernel, then the split partials
+int attn_ctas_per_sm(yoco_dtype dt, int d, int group) { return (dt == YOCO_BF16 && d == 128 && group <= 16) ? 1 : 3; }
+
 size_t attn_workspace(int B, int Hq, int T, int d, int splits) {
-    if (splits <= 1) return 0;
-    return (size_t)B * T * Hq * splits * (d + 2) * sizeof(float);
+    if (splits <= 1) return 256;
+    return 256 + (size_t)B * T * Hq * splits * (d + 2) * sizeof(float);
 }
 
 template <typename T, int D, int NQ>
@@ -306,14 +311,19 @@ static cudaError_t launch(const AttnArgs &a, int splits, void *ws, cudaStream_t 
     kps = ((kps + kAttnTile - 1) / kAttnTile) * kAttnTile;
     splits = (int)((keys + kps - 1) / kps);
     const int nq = (a.T < RB ? a.T : RB) * G;  // query vectors per CTA
+    const int rb_eff = (nq <= 4 && a.T <= RB) ? a.T : RB;
+    float *part = (float *)((char *)ws + 256);
     cudaError_t e;
-    if (nq <= 4) e = launch_nq<T, D, 4>(a, nq <= 4 && a.T <= RB ? a.T : RB, kps, splits, ws, st);
-    else if (nq <= 8) e = launch_nq<T, D, 8>(a, RB, kps, splits, ws, st);
-    else e = launch_nq<T, D, 16>(a, RB, kps, splits, ws, st);
+    if (std::is_same<T, bf16_t>::value && attn_tc_eligible(a, nq)) {
+        count_launches(splits > 1 ? 2 : 1);
+        e = attn_tc_launch(a, rb_eff, nq, kps, splits, part, (int *)ws, st);
+    } else if (nq <= 4) e = launch_nq<T, D, 4>(a, rb_eff, kps, splits, part, st);
+    else if (nq <= 8) e = launch_nq<T, D, 8>(a, RB, kps, splits, part, st);
+    else e = launch_nq<T, D, 16>(a, RB, kps, splits, part, st);
     if (e != cudaSuccess) return e;
     if (splits > 1) {
         const int rows = a.B * a.T * a.Hq;
-        attn_combine_kernel<T, D><<<rows, D, 0, st>>>((const float *)ws, (T *)a.O, splits);
+        attn_combine_kernel<T, D><<<rows, D, 0, st>>>((const float *)part, (T *)a.O, splits);
         e = cudaGetLastError();
     }
     return e;

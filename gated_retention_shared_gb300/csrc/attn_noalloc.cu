@@ -81,7 +81,7 @@ extern "C" YOCO_API yoco_status yoco_cross_attn_decode_noalloc(const void *Q, in
     int splits = num_splits;
     if (splits == 0) {
         // automatic: the usual split count, reduced until the partials fit the scratch
-        splits = attn_auto_splits(cache->B, cache->Hkv, keys);
+        splits = attn_auto_splits(cache->B, cache->Hkv, keys, attn_ctas_per_sm(cache->dtype, cache->d, Hq / cache->Hkv));
         while (splits > 1 && attn_workspace(cache->B, Hq, 1, cache->d, splits) > kNoAllocScratchBytes) --splits;
     }
     const size_t need = attn_workspace(cache->B, Hq, 1, cache->d, splits);

@@ -58,8 +58,15 @@ struct AttnArgs {
     float scale;
     yoco_dtype dt;
 };
-int attn_auto_splits(int B, int Hkv, int64_t keys);
+// resident CTAs per SM of the decode kernel that will run: 1 for the tensor-core
+// kernel (bf16, d = 128, <= 16 query heads per kv head), 3 for the CUDA-core one
+int attn_ctas_per_sm(yoco_dtype dt, int d, int group);
+int attn_auto_splits(int B, int Hkv, int64_t keys, int ctas_per_sm);
 size_t attn_workspace(int B, int Hq, int T, int d, int splits);
 cudaError_t attn_run(const AttnArgs &a, int splits, void *ws, cudaStream_t st);
+// attn_tc.cu: bf16, d = 128, <= 16 query vectors per CTA
+bool attn_tc_eligible(const AttnArgs &a, int nq);
+cudaError_t attn_tc_launch(const AttnArgs &a, int RB, int nq, int64_t kps, int splits, void *part, int *err,
+                           cudaStream_t st);
 
 }  // namespace yoco_host
