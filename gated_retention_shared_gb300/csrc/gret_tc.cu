@@ -47,7 +47,8 @@ constexpr int kC = 128;                     // chunk length = MMA M/N
 constexpr int kD = 128;                     // head size
 constexpr int kTile = kC * kD * 2;          // 32 KB bf16 tile
 constexpr int kHalf = kTile / 2;            // one 64-column block
-constexpr int kStages = 2;
+constexpr int kStages = 2;                  // OUTPUT: 2 x (Q, K, V)
+constexpr int kStagesSeg = 3;               // SEG_STATE: 3 x (K, V)
 constexpr int kTcThreads = 320;
 constexpr float kFactorMin = -60.f;         // chunk decay above which e^{-b_k} is used
 
@@ -57,8 +58,8 @@ constexpr uint32_t kColA = 0, kColO = 128, kColU = 384;
 enum : int { MODE_OUTPUT = 0, MODE_SEG_STATE = 1 };
 
 struct TcSmem {
-    uint64_t full[kStages], empty[kStages], pq_ready[kStages], o_free[2], bc_ready[2], o_full[2];
-    uint64_t full_v[kStages], vfree[kStages], k_ready[kStages], w_ready[2];
+    uint64_t full[kStagesSeg], empty[kStagesSeg], pq_ready[kStagesSeg], o_free[2], bc_ready[2], o_full[2];
+    uint64_t full_v[kStages], vfree[kStages], k_ready[kStages], w_ready[kStagesSeg];
     uint64_t as_full, p_free, u_full, u_free, s_ready, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -150,6 +151,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint8_t *tiles = smem_raw + pad;
     TcSmem &sm = *reinterpret_cast<TcSmem *>(tiles + kTileBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int NS = (MODE == MODE_OUTPUT) ? kStages : kStagesSeg;
     if (pad + kTileBytes + sizeof(TcSmem) > kTcSmemBytes) {  // cannot happen with a 16-B aligned window
         if (tid == 0 && err) atomicExch(err, (int)(kErrMagic | 9u));
         return;
@@ -160,22 +162,26 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int nchunks = (t_end - t_begin + kC - 1) / kC;
     const size_t bh = (size_t)b * H + h;
     const size_t bhp = bh * P + p;  // segment slot in E / G; slot P-1 of E holds the initial state
-    uint8_t *Sbuf = tiles + (size_t)kStages * 3 * kTile;  // bf16 state, MMA3's B operand
-    auto stage_q = [&](int s) { return tiles + (size_t)s * 3 * kTile; };
-    auto stage_k = [&](int s) { return tiles + (size_t)s * 3 * kTile + kTile; };
-    auto stage_v = [&](int s) { return tiles + (size_t)s * 3 * kTile + 2 * kTile; };
+    // OUTPUT stages hold Q, K, V; SEG_STATE stages hold K, V (no Q), so it keeps 3 in flight
+    uint8_t *Sbuf = tiles + (size_t)6 * kTile;  // bf16 state, MMA3's B operand (SEG_STATE: weight ring)
+    constexpr size_t kSS = (MODE == MODE_OUTPUT ? 3 : 2) * (size_t)kTile;
+    auto stage_q = [&](int s) { return tiles + (size_t)s * kSS; };
+    auto stage_k = [&](int s) { return tiles + (size_t)s * kSS + (MODE == MODE_OUTPUT ? kTile : 0); };
+    auto stage_v = [&](int s) { return stage_k(s) + kTile; };
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NS; ++s) {  // ring barriers, one per stage
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
             mbar_init(&sm.pq_ready[s], MODE == MODE_OUTPUT ? 1 : 2);  // SEG_STATE: both groups scale K
+            mbar_init(&sm.w_ready[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {  // double-buffered per-chunk barriers
             mbar_init(&sm.o_free[s], 1);
             mbar_init(&sm.bc_ready[s], 1);
             mbar_init(&sm.o_full[s], 1);
             mbar_init(&sm.full_v[s], 1);
             mbar_init(&sm.vfree[s], 1);
-            mbar_init(&sm.w_ready[s], 1);
             mbar_init(&sm.k_ready[s], 1);
         }
         mbar_init(&sm.as_full, 1);
@@ -216,8 +222,8 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // the staging buffer of the output store two chunks back).  SEG_STATE: K and
             // V complete `full`.
             for (int i = 0; i < nchunks; ++i) {
-                const int s = i % kStages;
-                if (i >= kStages && !mbar_wait(&sm.empty[s], ((i / kStages) + 1) & 1, abort_flag)) {
+                const int s = i % NS;
+                if (i >= NS && !mbar_wait(&sm.empty[s], ((i / NS) + 1) & 1, abort_flag)) {
                     report(err, &sm.abort_flag, 1);
                     break;
                 }
@@ -231,7 +237,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tma_load_4d(stage_v(s) + half * kHalf, &tm_v, &sm.full[s], half * 64, h, n0, b);
                 }
                 if (MODE == MODE_OUTPUT) {
-                    if (i >= kStages && !mbar_wait(&sm.vfree[s], ((i / kStages) + 1) & 1, abort_flag)) {
+                    if (i >= NS && !mbar_wait(&sm.vfree[s], ((i / NS) + 1) & 1, abort_flag)) {
                         report(err, &sm.abort_flag, 8);
                         break;
                     }
@@ -241,9 +247,9 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             }
             // leave no copy in flight: wait for the last loads of each stage
-            for (int i = max(0, nchunks - kStages); i < nchunks; ++i) {
-                mbar_wait(&sm.full[i % kStages], (i / kStages) & 1, abort_flag, 200000000ull);
-                if (MODE == MODE_OUTPUT) mbar_wait(&sm.full_v[i % kStages], (i / kStages) & 1, abort_flag, 200000000ull);
+            for (int i = max(0, nchunks - NS); i < nchunks; ++i) {
+                mbar_wait(&sm.full[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
+                if (MODE == MODE_OUTPUT) mbar_wait(&sm.full_v[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
             }
         }
     } else if (warp == 9) {
@@ -255,9 +261,9 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t id_kv = idesc_bf16_f32(kD, kD, true, true);    // A=K'^T (M-major), B=V (N-major)
             bool ok = true;
             for (int i = 0; i < nchunks && ok; ++i) {
-                const int s = i % kStages, ob = i & 1;
+                const int s = i % NS, ob = i & 1;
                 const uint32_t q_a = smem_u32(stage_q(s)), k_a = smem_u32(stage_k(s)), v_a = smem_u32(stage_v(s));
-                if (!(ok = mbar_wait(&sm.full[s], (i / kStages) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sm.full[s], (i / NS) & 1, abort_flag))) break;
                 if (MODE == MODE_OUTPUT) {
                     // P of the previous chunk (TMEM columns of A) must have been consumed
                     if (i > 0 && !(ok = mbar_wait(&sm.p_free, (i - 1) & 1, abort_flag))) break;
@@ -284,14 +290,14 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         }
                     };
                     if (!factor) {  // Q is rescaled in place together with P
-                        if (!(ok = mbar_wait(&sm.pq_ready[s], (i / kStages) & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
                     }
                     // the cross term needs nothing else from the decay warps: it fills the P bubble
                     if (!(ok = mbar_wait(&sm.s_ready, i & 1, abort_flag))) break;
                     tc_fence_after();
                     mma3();
-                    if (!(ok = mbar_wait(&sm.k_ready[s], (i / kStages) & 1, abort_flag))) break;
-                    if (!(ok = mbar_wait(&sm.full_v[s], (i / kStages) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait(&sm.k_ready[s], (i / NS) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait(&sm.full_v[s], (i / NS) & 1, abort_flag))) break;
                     if (i > 0 && !(ok = mbar_wait(&sm.u_free, (i - 1) & 1, abort_flag))) break;
                     tc_fence_after();
                     for (int kk = 0; kk < 8; ++kk)  // MMA4: U = K'^T V
@@ -299,7 +305,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_kv, kk > 0);
                     mma_commit(&sm.u_full);
                     if (factor) {
-                        if (!(ok = mbar_wait(&sm.pq_ready[s], (i / kStages) & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
                         tc_fence_after();
                     }
                     for (int kk = 0; kk < 8; ++kk)  // MMA2: O += P V
@@ -307,7 +313,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     mma_commit(&sm.o_full[ob]);
                     mma_commit(&sm.p_free);
                 } else {
-                    if (!(ok = mbar_wait(&sm.pq_ready[s], (i / kStages) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
                     tc_fence_after();
                     for (int kk = 0; kk < 8; ++kk)  // E^T += V^T K''
                         mma_ss(tmem + kColU, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024),
@@ -330,7 +336,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), j) : 0.f;
         bool alive = true;
         for (int i = 0; i < nchunks && alive; ++i) {
-            const int s = i % kStages;
+            const int s = i % NS;
             float bC;
             const float bj = group_scan(lg_next, sm.wsum1, lane, wq, 1, bC);
             if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), j);  // in flight during this chunk
@@ -346,7 +352,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             bool ok = true;
             if (j == 0) {
                 ok = (MODE == MODE_OUTPUT) ? mbar_wait(&sm.as_full, i & 1, abort_flag)
-                                           : mbar_wait(&sm.full[s], (i / kStages) & 1, abort_flag);
+                                           : mbar_wait(&sm.full[s], (i / NS) & 1, abort_flag);
                 if (!ok) report(err, &sm.abort_flag, 3);
                 sm.go1 = ok && !*abort_flag;
             }
@@ -399,10 +405,10 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 // weight of token j: decay from j to the segment end; the state warps
                 // scale the second 64 columns of every row with the same weights
                 const float w = __expf(suffix + (bC - bj));
-                float *wring = reinterpret_cast<float *>(Sbuf) + (i & 1) * kC;  // Sbuf is unused here
+                float *wring = reinterpret_cast<float *>(Sbuf) + s * kC;  // Sbuf is unused here; one slot per stage
                 wring[j] = w;
                 named_bar(1, 128);
-                if (j == 0) mbar_arrive(&sm.w_ready[i & 1]);
+                if (j == 0) mbar_arrive(&sm.w_ready[s]);
                 scale_row_block(stage_k(s), j, w, 0);
                 suffix += bC;
             }
@@ -455,7 +461,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (t == 0) mbar_arrive(&sm.s_ready);
             float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), t) : 0.f;
             for (int i = 0; i < nchunks; ++i) {
-                const int s = i % kStages;
+                const int s = i % NS;
                 // the chunk's decay, computed here too (cheap) so no ring is shared with the decay warps
                 float bC;
                 const float bt = group_scan(lg_next, sm.wsum0, lane, warp, 2, bC);
@@ -544,15 +550,15 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             bool ok = true;
             for (int i = 0; i < nchunks; ++i) {
-                const int s = i % kStages;
+                const int s = i % NS;
                 if (t == 0) {
-                    ok = mbar_wait(&sm.w_ready[i & 1], (i / 2) & 1, abort_flag);
+                    ok = mbar_wait(&sm.w_ready[s], (i / NS) & 1, abort_flag);
                     if (!ok) report(err, &sm.abort_flag, 10);
                     sm.go0 = ok && !*abort_flag;
                 }
                 named_bar(2, 128);
                 if (!sm.go0) break;
-                const float *wring = reinterpret_cast<const float *>(Sbuf) + (i & 1) * kC;
+                const float *wring = reinterpret_cast<const float *>(Sbuf) + s * kC;
                 scale_row_block(stage_k(s), t, wring[t], 1);
                 fence_proxy_async_smem();
                 named_bar(2, 128);
