@@ -70,6 +70,18 @@ def _counters(seed, stream, start, count):
     return a, b
 
 
+def normal_at(seed: int, stream: int, idx, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
+    """fp64 normals of the stream at arbitrary element indices (any shape)."""
+    idx = np.asarray(idx, dtype=np.uint64)
+    key = stream_key(seed, stream)
+    with np.errstate(over="ignore"):
+        a = splitmix64(key + np.uint64(2) * idx)
+        b = splitmix64(key + np.uint64(2) * idx + np.uint64(1))
+    u1 = ((a >> np.uint64(11)) + np.uint64(1)).astype(np.float64) * (2.0 ** -53)
+    u2 = (b >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    return mean + std * (np.sqrt(-2.0 * np.log(u1)) * np.cos(TWO_PI * u2))
+
+
 def normal_f64(seed: int, stream: int, count: int, mean: float = 0.0, std: float = 1.0,
                start: int = 0) -> np.ndarray:
     """Elements start..start+count-1 of the stream as fp64 normals (before rounding)."""
