@@ -81,17 +81,12 @@ __device__ __forceinline__ void report(int *err, int *abort_flag, int code) {
     if (err) atomicExch(err, (int)(kErrMagic | (uint32_t)code));
 }
 
-// bf16x8 in a uint4 scaled by s, rounded back to bf16 (nearest even)
-__device__ __forceinline__ uint4 scale_bf16x8(uint4 u, float s) {
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// bf16x8 in a uint4 times the bf16 pair s2 (packed bf16x2 multiply, nearest even)
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 u, __nv_bfloat162 s2) {
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float lo = __uint_as_float(w[i] << 16) * s;
-        float hi = __uint_as_float(w[i] & 0xFFFF0000u) * s;
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(lo, hi);
-        w[i] = *reinterpret_cast<uint32_t *>(&h2);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < 4; ++i) h[i] = __hmul2(h[i], s2);
+    return u;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -107,19 +102,21 @@ __device__ __forceinline__ uint32_t tile_chunk(int r, int c) {
 
 // Scale row r of a 128 x 128 swizzled bf16 tile in place.
 __device__ __forceinline__ void scale_row_inplace(uint8_t *tile, int r, float s) {
+    const __nv_bfloat162 s2 = __float2bfloat162_rn(s);
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
         uint4 *p = reinterpret_cast<uint4 *>(tile + tile_chunk(r, c));
-        *p = scale_bf16x8(*p, s);
+        *p = scale_bf16x8(*p, s2);
     }
 }
 
 // Scale one 64-column block (chunks 8*blk .. 8*blk+7) of row r in place.
 __device__ __forceinline__ void scale_row_block(uint8_t *tile, int r, float s, int blk) {
+    const __nv_bfloat162 s2 = __float2bfloat162_rn(s);
 #pragma unroll
     for (int c = 8 * blk; c < 8 * blk + 8; ++c) {
         uint4 *p = reinterpret_cast<uint4 *>(tile + tile_chunk(r, c));
-        *p = scale_bf16x8(*p, s);
+        *p = scale_bf16x8(*p, s2);
     }
 }
 
@@ -202,6 +199,9 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     volatile int *abort_flag = &sm.abort_flag;
+    // SEG_STATE: the OUTPUT grid may start on idle SMs now; it waits for this grid
+    // (griddepcontrol.wait) before it reads E, G or `state`
+    if (MODE == MODE_SEG_STATE) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     // chunk order: OUTPUT forwards, SEG_STATE backwards (running suffix decay)
     auto chunk_start = [&](int i) {
@@ -423,6 +423,8 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         if (MODE == MODE_OUTPUT) {
             float S[kD];  // row t of the state, fp32
+            // inputs of this pass written by the SEG_STATE grid: wait for it (no-op without one)
+            asm volatile("griddepcontrol.wait;\n" ::: "memory");
             {
                 // initial state of this segment: the caller's state, advanced over the
                 // earlier segments with their zero-start end states E_q and decays G_q
@@ -679,9 +681,20 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     gret_tc_kernel<MODE_SEG_STATE><<<dim3(P - 1, a.H, a.B), kTcThreads, kTcSmemBytes, st>>>(
         mq, mk, mv, mo, a.logits, inv_tau, nullptr, a.state, E, G, a.N, a.H, seg_len, P, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    gret_tc_kernel<MODE_OUTPUT><<<dim3(P, a.H, a.B), kTcThreads, kTcSmemBytes, st>>>(
-        mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, a.N, a.H, seg_len, P, err);
-    return cudaGetLastError();
+    // the OUTPUT grid may begin (TMA loads, first MMAs) while SEG_STATE drains; its
+    // state warps wait for SEG_STATE before touching E, G and `state`
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P, a.H, a.B);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kTcSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gret_tc_kernel<MODE_OUTPUT>, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o,
+                              a.state, E, G, a.N, a.H, seg_len, P, err);
 }
 
 }  // namespace yoco_host
