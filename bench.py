@@ -130,6 +130,26 @@ def run_reference(args):
 
 # --------------------------------------------------------------------- GPU arm
 
+# DRAM bytes of one gRet prefill call on the bench's layer shape (32768 x 24 x 128, bf16),
+# from one ncu capture of the current kernel: dram__bytes_read.sum + dram__bytes_write.sum
+# of the SEG_STATE launch (342.4 + 4.8 MB) and the OUTPUT launch (617.0 + 173.9 MB).
+# Must be re-captured (or set to None) whenever gret_tc.cu changes.
+GRET_CALL_DRAM_BYTES = 1138.1e6
+
+
+def aggregate_over_ranks(elapsed_s, units_per_rank, dist=None, device="cpu"):
+    """Whole-job throughput of independent replicas: the units every rank
+    processed over the slowest rank's time.  Returns (units/s, max seconds)."""
+    import torch
+    world = 1
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        t = torch.tensor([float(elapsed_s)], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_s = float(t)
+    return world * units_per_rank / elapsed_s, elapsed_s
+
+
 class Clocks:
     """nvidia-smi sampler for the timed region."""
 
@@ -298,12 +318,8 @@ def run_gpu(args):
         e1.record(stream)
         barrier()
     elapsed = e0.elapsed_time(e1) / 1e3
-    if dist is not None:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t)
+    value, elapsed = aggregate_over_ranks(elapsed, B * N * args.steps, dist, dev)
     ms_step = elapsed / args.steps * 1e3
-    value = world * B * N * args.steps / elapsed
     gret_ms = statistics.mean(c[0].elapsed_time(c[1]) for row in calls for c in row)
 
     # ---- per-phase split: one more (untimed) step with events between phases
@@ -327,7 +343,8 @@ def run_gpu(args):
     roofline = {"bound": "hbm", "kernel": "yoco_gret_prefill_chunkwise (one layer: all of its launches)",
                 "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (burst copy)" if "hbm_gbs" in peaks else "fallback",
-                "algorithmic_bytes_per_launch": gret_bytes, "avg_launch_ms": round(gret_ms, 4), "traffic": None}
+                "algorithmic_bytes_per_launch": gret_bytes, "avg_launch_ms": round(gret_ms, 4),
+                "traffic": GRET_CALL_DRAM_BYTES, "traffic_unit": "bytes per call (ncu dram read + write, both passes)"}
 
     # ---- end to end: inputs from pinned host memory, result back to host
     e2e = e2e_measure(args, torch, stream, step, [q, k, v, lg], [M, q1, k1, v1, lg1, M1, Qx, Qd], [Ox[-1], Od[-1]])

@@ -58,6 +58,7 @@ def _load():
         "yoco_version": (i, []),
         "yoco_launch_count": (ctypes.c_uint64, []),
         "yoco_workspace_status": (i, [vp, i, vp]),
+        "yoco_selftest_wait_timeout": (i, [vp, ctypes.c_uint64, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -71,7 +72,7 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_shared_kv_project_append", "yoco_shared_kv_workspace_size", "yoco_cross_attn_prefill",
             "yoco_cross_attn_decode", "yoco_cross_attn_workspace_size", "yoco_status_string",
             "yoco_last_error", "yoco_version", "yoco_launch_count",
-            "yoco_workspace_status", "yoco_cross_attn_decode_noalloc")
+            "yoco_workspace_status", "yoco_cross_attn_decode_noalloc", "yoco_selftest_wait_timeout")
 
 
 def _check(status: int, where: str):

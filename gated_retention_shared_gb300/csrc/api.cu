@@ -106,6 +106,12 @@ yoco_status yoco_workspace_status(void *workspace, int clear, void *stream) {
     return YOCO_OK;
 }
 
+yoco_status yoco_selftest_wait_timeout(void *workspace, uint64_t limit_ns, void *stream) {
+    if (!workspace || !aligned(workspace, 256)) return fail(YOCO_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (limit_ns == 0 || limit_ns > 10000000000ull) return fail(YOCO_ERR_INVALID_ARG, "limit_ns must be in (0, 1e10]");
+    return cuda_status(selftest_wait(workspace, limit_ns, (cudaStream_t)stream), "selftest_wait_timeout");
+}
+
 uint64_t yoco_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 // ----------------------------------------------------------------------- gRet

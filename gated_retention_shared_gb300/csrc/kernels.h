@@ -69,4 +69,7 @@ bool attn_tc_eligible(const AttnArgs &a, int nq);
 cudaError_t attn_tc_launch(const AttnArgs &a, int RB, int nq, int64_t kps, int splits, void *part, int *err,
                            cudaStream_t st);
 
+// selftest.cu
+cudaError_t selftest_wait(void *ws, uint64_t limit_ns, cudaStream_t st);
+
 }  // namespace yoco_host

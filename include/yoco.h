@@ -220,6 +220,17 @@ YOCO_API int yoco_version(void);
  */
 YOCO_API yoco_status yoco_workspace_status(void *workspace, int clear, void *stream);
 
+/*
+ * Failure-path self-test: enqueues one kernel that waits on an on-device
+ * barrier nothing ever completes, using the same bounded wait as the
+ * tensor-core kernels; after limit_ns (<= 10 s) it gives up and records the
+ * timeout in `workspace` (>= 256 bytes, 256-byte aligned).  A following
+ * yoco_workspace_status returns YOCO_ERR_TIMEOUT and the CUDA context stays
+ * usable.  Not part of the method; it exists so tests can exercise the
+ * timeout path without faulting or hanging a GPU.
+ */
+YOCO_API yoco_status yoco_selftest_wait_timeout(void *workspace, uint64_t limit_ns, void *stream);
+
 /* Number of kernels this process has enqueued through libyoco so far
  * (monotonic, all threads).  A diagnostic for counting launches per step. */
 YOCO_API uint64_t yoco_launch_count(void);

@@ -142,3 +142,11 @@ def test_kv_cache_bytes_match_teaching_numbers(Y):
     """Blog post Section 7: one shared K/V of 128 Ki tokens x 8 heads x 128 in
     2-byte elements is 0.5 GiB, whatever the number of cross layers."""
     assert Y.KVCache.nbytes(1, 8, 128, 131072, 2) == 2 ** 29
+
+
+def test_selftest_rejects_bad_arguments(Y):
+    L = Y.lib
+    assert L.yoco_selftest_wait_timeout(ctypes.c_void_p(0x1010), 1000, None) == Y.YOCO_ERR_WORKSPACE
+    assert L.yoco_selftest_wait_timeout(None, 1000, None) == Y.YOCO_ERR_WORKSPACE
+    assert L.yoco_selftest_wait_timeout(FAKE, 0, None) == Y.YOCO_ERR_INVALID_ARG
+    assert L.yoco_selftest_wait_timeout(FAKE, 20_000_000_000, None) == Y.YOCO_ERR_INVALID_ARG

@@ -430,3 +430,29 @@ def test_device_generator_matches_host(Y):
     f = torch.empty(5000, dtype=torch.float32, device="cuda")
     synth.fill_normal_(f, SEED, 99, mean=2.0)
     assert np.max(np.abs(f.cpu().numpy() - synth.normal(SEED, 99, (5000,), "f32", mean=2.0))) <= 1e-6
+
+
+# ------------------------------------------------------------- failure path
+
+def test_bounded_wait_times_out_and_context_survives(Y):
+    """A device wait that nothing completes gives up after its limit, the
+    timeout shows up through yoco_workspace_status, and the GPU keeps
+    working (a gRet call right after matches the oracle)."""
+    import ctypes
+    import time
+    import torch
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    t0 = time.time()
+    st = Y.lib.yoco_selftest_wait_timeout(ctypes.c_void_p(ws.data_ptr()), 50_000_000,
+                                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == Y.YOCO_OK
+    with pytest.raises(Y.YocoError) as e:
+        Y.yoco_workspace_status(ws)
+    assert e.value.status == Y.YOCO_ERR_TIMEOUT
+    assert time.time() - t0 < 5.0
+    Y.yoco_workspace_status(ws)  # cleared by the previous read
+    B, N, H, d = 1, 300, 2, 128
+    host, dev = gret_inputs(30, B, N, H, d, "bf16", logit_mean=2.0)
+    o, S = run_prefill(Y, dev, B, N, H, d, "bf16")
+    o_ref, _ = oracle.gret_recurrent(*host, 16.0)
+    assert rel_l2(o, o_ref) <= BF16_REL_L2
