@@ -249,6 +249,9 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
 // thread c owns head dim c
 template <typename T, int D>
 __global__ void __launch_bounds__(D) attn_combine_kernel(const float *__restrict__ part, T *__restrict__ O, int splits) {
+    // launched as a programmatic dependent of the split kernel: wait for its partials
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int w = blockIdx.x, c = threadIdx.x;
     const float *pp = part + (size_t)w * splits * (D + 2);
     float M = -INFINITY;
@@ -323,8 +326,16 @@ static cudaError_t launch(const AttnArgs &a, int splits, void *ws, cudaStream_t 
     if (e != cudaSuccess) return e;
     if (splits > 1) {
         const int rows = a.B * a.T * a.Hq;
-        attn_combine_kernel<T, D><<<rows, D, 0, st>>>((const float *)part, (T *)a.O, splits);
-        e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(rows);
+        cfg.blockDim = dim3(D);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, attn_combine_kernel<T, D>, (const float *)part, (T *)a.O, splits);
     }
     return e;
 }

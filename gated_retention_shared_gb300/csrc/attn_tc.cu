@@ -97,6 +97,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         sm.abort_flag = 0;
         fence_mbar_init();
     }
+    // Programmatic dependent launch: the combine grid (and a following call) may
+    // start now; nothing of another kernel is read or written before the wait below,
+    // which returns once the previous kernel on the stream has completed (at once
+    // when this grid was launched without the attribute).
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     // Q rows (unscaled bf16) as the K-major B operand; rows >= nq and both P buffers zero
     for (int e = tid; e < kAN * kAD / 8; e += kAThreads) {
         const int n = e / (kAD / 8), c8 = (e % (kAD / 8)) * 8;
@@ -353,11 +359,24 @@ cudaError_t attn_tc_launch(const AttnArgs &a, int RB, int nq, int64_t kps, int s
         return cudaErrorInvalidValue;
     dim3 grid(splits, (a.T + RB - 1) / RB, a.B * a.Hkv);
     cudaError_t e;
+    // launched as a programmatic dependent of the previous kernel on the stream: its
+    // prologue (barriers, TMEM, descriptor prefetch) overlaps that kernel's tail
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kAThreads);
+    cfg.dynamicSmemBytes = kASmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
 #define YOCO_ATTN_TC(NQ_)                                                                                          \
     e = cudaFuncSetAttribute(attn_tc_kernel<NQ_>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem);       \
     if (e != cudaSuccess) return e;                                                                                \
-    attn_tc_kernel<NQ_><<<grid, kAThreads, kASmem, st>>>(mk, mv, (const bf16_t *)a.Q, (bf16_t *)a.O, (float *)ws, \
-                                                         a.T, a.Hq, a.Hkv, a.p0, a.scale, RB, kps, splits, err);
+    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<NQ_>, mk, mv, (const bf16_t *)a.Q, (bf16_t *)a.O, (float *)ws,     \
+                           a.T, a.Hq, a.Hkv, a.p0, a.scale, RB, kps, splits, err);                                 \
+    if (e != cudaSuccess) return e;
     if (nq <= 4) {
         YOCO_ATTN_TC(4)
     } else if (nq <= 8) {
