@@ -122,6 +122,22 @@ def test_gret_prefill_bf16_tensor_core_shapes(Y, B, N, H, with_state):
     Y.yoco_workspace_status(ws)  # no bounded wait gave up
 
 
+def test_gret_prefill_bf16_many_segments_state_and_strong_decay(Y):
+    """Many segments per head with an initial state and a stretch of near-zero
+    gates inside a segment (B=2, N=7600, 4 heads: 15 segments of 4
+    chunks; chunk 15 has total decay far below the factoring limit)."""
+    B, N, H, d = 2, 7600, 4, 128
+    host, dev = gret_inputs(31, B, N, H, d, "bf16", logit_mean=1.0)
+    lg = host[3].copy()
+    lg[:, 2000:2010] = -2000.0
+    dev = dev[:3] + (dev_f32(lg),)
+    S0 = synth.normal(SEED, sid(31, 1, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
+    o, S = run_prefill(Y, dev, B, N, H, d, "bf16", S0=S0)
+    o_ref, S_ref = oracle.gret_recurrent(host[0], host[1], host[2], lg, 16.0, S0=S0)
+    assert rel_l2(o, o_ref) <= BF16_REL_L2
+    assert rel_l2(S, S_ref) <= BF16_REL_L2
+
+
 def test_gret_prefill_bf16_strong_decay(Y):
     """Gates near 0 inside chunks (b_C < -80) take the direct-exponent branch."""
     B, N, H, d = 1, 1000, 4, 128
