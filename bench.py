@@ -49,6 +49,9 @@ def parse():
     p.add_argument("--chunk", type=int, default=0)
     p.add_argument("--only", choices=["gret", "proj", "cross_decode"], default=None,
                    help="time one call of the step on its bench shape (for profiling)")
+    p.add_argument("--cache-len", type=int, default=0,
+                   help="--only cross_decode: cache length (default: the step's prompt length)")
+    p.add_argument("--batch", type=int, default=0, help="--only cross_decode: sequences (default: the step's B)")
     return p.parse_args()
 
 
@@ -151,13 +154,17 @@ def aggregate_over_ranks(elapsed_s, units_per_rank, dist=None, device="cpu"):
 
 
 class Clocks:
-    """nvidia-smi sampler for the timed region."""
+    """nvidia-smi sampler (every 100 ms) running across the timed region; each line
+    is stamped on arrival so the summary keeps the samples taken inside a window."""
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.lines = []
+        self.thread = None
 
     def __enter__(self):
+        import threading
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -167,22 +174,37 @@ class Clocks:
                                          stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        if self.proc is not None:
+            def reader():
+                for line in self.proc.stdout:
+                    self.lines.append((time.monotonic(), line))
+            self.thread = threading.Thread(target=reader, daemon=True)
+            self.thread.start()
         return self
 
+    def wait_first(self, timeout=3.0):
+        t0 = time.monotonic()
+        while self.proc is not None and not self.lines and time.monotonic() - t0 < timeout:
+            time.sleep(0.01)
+
     def __exit__(self, *exc):
-        self.out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+                self.proc.wait()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
 
-    def summary(self):
+    def summary(self, t_lo=None, t_hi=None):
+        """Samples stamped in [t_lo, t_hi] (all of them without a window)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").splitlines():
+        for ts, line in self.lines:
+            if (t_lo is not None and ts < t_lo) or (t_hi is not None and ts > t_hi):
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -299,6 +321,11 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    # the clock sampler starts before the warm-up so that it is sampling when the
+    # timed region begins; the summary keeps the samples stamped inside that region
+    # (plus one interval on either side, the GPU being busy then too)
+    clk = Clocks(local).__enter__()
+    clk.wait_first()
     for _ in range(args.warmup):
         step()
     launches0 = L.yoco_launch_count()
@@ -310,13 +337,16 @@ def run_gpu(args):
     calls = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L_SELF)]
              for _ in range(args.steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
-        barrier()
-        e0.record(stream)
-        for i in range(args.steps):
-            step(calls[i])
-        e1.record(stream)
-        barrier()
+    barrier()
+    t_lo = time.monotonic()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(calls[i])
+    e1.record(stream)
+    barrier()
+    t_hi = time.monotonic()
+    time.sleep(0.12)  # let the sample that closes the region arrive
+    clk.__exit__(None, None, None)
     elapsed = e0.elapsed_time(e1) / 1e3
     value, elapsed = aggregate_over_ranks(elapsed, B * N * args.steps, dist, dev)
     ms_step = elapsed / args.steps * 1e3
@@ -346,16 +376,32 @@ def run_gpu(args):
                 "algorithmic_bytes_per_launch": gret_bytes, "avg_launch_ms": round(gret_ms, 4),
                 "traffic": GRET_CALL_DRAM_BYTES, "traffic_unit": "bytes per call (ncu dram read + write, both passes)"}
 
+    # ---- the generated token: 13 recurrent gRet steps, one append, 13 cross layers
+    dec_ms = phases["gret_decode_x13"] + phases["kv_append_1"] + phases["cross_decode_x13"]
+    cross_bytes = 2 * B * (N + 1) * HKV * D * 2
+    cross_call_ms = phases["cross_decode_x13"] / L_CROSS
+    cross_gbs = cross_bytes / (cross_call_ms / 1e3) / 1e9
+    decode = {"value": round(1e3 / dec_ms, 1), "unit": "tok/s", "context": N + 1, "B": B,
+              "ms_per_token": round(dec_ms, 4), "timed": "phase-split step (CUDA events between phases)",
+              "roofline_cross_decode": {
+                  "bound": "hbm", "kernel": "yoco_cross_attn_decode (split + combine)",
+                  "achieved": round(cross_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                  "frac": round(cross_gbs / hbm_peak, 4), "algorithmic_bytes_per_launch": cross_bytes,
+                  "avg_launch_ms": round(cross_call_ms, 4),
+                  "note": "the 134 MB cache is read by 13 layers in a row and is about the size of L2"}}
+
     # ---- end to end: inputs from pinned host memory, result back to host
     e2e = e2e_measure(args, torch, stream, step, [q, k, v, lg], [M, q1, k1, v1, lg1, M1, Qx, Qd], [Ox[-1], Od[-1]])
 
-    clocks = clk.summary()
+    clocks = clk.summary(t_lo - 0.1, t_hi + 0.1)
+    clocks["window_ms"] = round((t_hi - t_lo) * 1e3, 1)
     out = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
            "config": workload_config(args.chunk if args.chunk else "auto"),
            "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches_per_step * args.steps),
-           "gpu_launches_per_step": int(launches_per_step), "clocks": clocks, "phases_ms": phases}
+           "gpu_launches_per_step": int(launches_per_step), "clocks": clocks, "phases_ms": phases,
+           "decode": decode}
     if rank == 0 and not args.no_cpu_baseline:
         step_s, desc, cores = cpu_sample()
         out["cpu_baseline"] = {"value": N / step_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
@@ -441,13 +487,15 @@ def run_only(args):
             return L.yoco_shared_kv_project_append(P(M), None, EPS, P(Wk), P(Wv), N, DM, ctypes.byref(cache.c), P(ws),
                                                    ws.numel(), stp)
     else:
-        Kc = normal((B, HKV, N, D), bf, sid(CFG, 0, synth.T_CACHE_K))
-        Vc = normal((B, HKV, N, D), bf, sid(CFG, 0, synth.T_CACHE_V))
-        cache = Y.KVCache(B, HKV, D, N, k=Kc, v=Vc)
-        cache.set_length(N)
-        Qd = normal((B, HQ, D), bf, sid(CFG, 0, synth.T_QX, 1))
+        Bc = args.batch or B
+        Nc = args.cache_len or N
+        Kc = normal((Bc, HKV, Nc, D), bf, sid(CFG, 0, synth.T_CACHE_K))
+        Vc = normal((Bc, HKV, Nc, D), bf, sid(CFG, 0, synth.T_CACHE_V))
+        cache = Y.KVCache(Bc, HKV, D, Nc, k=Kc, v=Vc)
+        cache.set_length(Nc)
+        Qd = normal((Bc, HQ, D), bf, sid(CFG, 0, synth.T_QX, 1))
         Od = torch.empty_like(Qd)
-        ws = torch.empty(max(256, L.yoco_cross_attn_workspace_size(B, HQ, 1, ctypes.byref(cache.c), 0)),
+        ws = torch.empty(max(256, L.yoco_cross_attn_workspace_size(Bc, HQ, 1, ctypes.byref(cache.c), 0)),
                          dtype=torch.uint8, device=dev)
 
         def call():
@@ -462,7 +510,14 @@ def run_only(args):
         assert call() == 0, L.yoco_last_error()
     e1.record()
     torch.cuda.synchronize()
-    print(json.dumps({"only": args.only, "ms_per_call": e0.elapsed_time(e1) / args.steps, "steps": args.steps}))
+    ms = e0.elapsed_time(e1) / args.steps
+    line = {"only": args.only, "ms_per_call": ms, "steps": args.steps}
+    if args.only == "cross_decode":
+        # every K/V byte of every sequence is read once per call
+        nbytes = 2 * Bc * HKV * Nc * D * 2
+        line.update({"B": Bc, "cache_len": Nc, "bytes_per_call": nbytes,
+                     "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1)})
+    print(json.dumps(line))
 
 
 def main():

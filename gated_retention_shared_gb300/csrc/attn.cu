@@ -10,6 +10,8 @@
 // K/V tiles are double-buffered in shared memory with cp.async.
 #include <type_traits>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -275,13 +277,30 @@ using namespace yoco;
 static int rows_per_block(int G) { return G >= kAttnMaxQ ? 1 : kAttnMaxQ / G; }
 
 int attn_auto_splits(int B, int Hkv, int64_t keys, int ctas_per_sm) {
-    // about one wave of CTAs on 152 SMs; slices of >= 2 tiles
-    int64_t want = ((int64_t)ctas_per_sm * 152 + (int64_t)B * Hkv - 1) / ((int64_t)B * Hkv);
-    int64_t max_by_len = (keys + 2 * kAttnTile - 1) / (2 * kAttnTile);
-    if (want > max_by_len) want = max_by_len;
-    if (want < 1) want = 1;
-    if (want > 1024) want = 1024;
-    return (int)want;
+    // Split count for B*Hkv (sequence, kv head) units: at least one full wave of
+    // CTAs on the 152 SMs, then the smallest count whose last wave is >= 95 % full
+    // (so 8 units take 19 splits = 152 CTAs, 64 units 7 = 448 of 456 slots, 256
+    // units 4 = 1024 of 1064), never more than one split per two key tiles.
+    const int64_t units = (int64_t)B * Hkv;
+    const int64_t slots = (int64_t)ctas_per_sm * 152;
+    int64_t cap = (keys + 2 * kAttnTile - 1) / (2 * kAttnTile);
+    if (cap > 1024) cap = 1024;
+    if (cap < 1) cap = 1;
+    int64_t s_min = (slots + units - 1) / units;
+    if (s_min > cap) s_min = cap;
+    const int64_t s_max = std::min<int64_t>(cap, 8 * s_min);
+    int64_t best = s_min;
+    double best_eff = -1.0;
+    for (int64_t s = s_min; s <= s_max; ++s) {
+        const int64_t ctas = units * s;
+        const double eff = (double)ctas / (double)(slots * ((ctas + slots - 1) / slots));
+        if (eff >= 0.95) return (int)s;
+        if (eff > best_eff) {
+            best_eff = eff;
+            best = s;
+        }
+    }
+    return (int)best;
 }
 
 // workspace: [0, 256) status word of the tensor-core kernel, then the split partials
