@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk", type=int, default=0)
-    p.add_argument("--only", choices=["gret", "proj", "cross_decode"], default=None,
+    p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode"], default=None,
                    help="time one call of the step on its bench shape (for profiling)")
     p.add_argument("--cache-len", type=int, default=0,
                    help="--only cross_decode: cache length (default: the step's prompt length)")
@@ -494,6 +494,18 @@ def run_only(args):
             S.zero_()
             return L.yoco_gret_prefill_chunkwise(P(q), P(k), P(v), P(lg), TAU, P(o), P(S), B, N, H, D, D, args.chunk,
                                                  1, 1, P(ws), ws.numel(), stp)
+    elif args.only == "append":  # one generated token's K/V slot into a cache holding the prompt
+        M1 = normal((B, 1, DM), bf, sid(CFG, 0, synth.T_M, 1))
+        Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
+        Wv = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WV), std=0.02)
+        cache = Y.KVCache(B, HKV, D, N + 1, device=dev)
+        ws = torch.empty(max(256, L.yoco_shared_kv_workspace_size(B, 1, DM, ctypes.byref(cache.c))),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            cache.set_length(N)
+            return L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, ctypes.byref(cache.c),
+                                                   P(ws), ws.numel(), stp)
     elif args.only == "proj":
         M = normal((B, N, DM), bf, sid(CFG, 0, synth.T_M))
         Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)

@@ -9,6 +9,7 @@
 //
 // This file holds the CUDA-core path (any dtype, any T); large bf16 appends go to
 // the tensor-core GEMM in kv_proj_tc.cu.
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -119,81 +120,195 @@ proj_append_simt(const T *__restrict__ M, const T *__restrict__ g, const T *__re
     finish_append(len_dev, len + T_rows);
 }
 
-// Few rows (decode): split-K GEMV.  CTA (column group, K slice) of 256 threads;
-// thread = 8 consecutive output columns (one 16-byte row segment of W), looping
-// over its slice of W rows and over the input rows 4 at a time; fp32 partials
-// go to the workspace and proj_gemv_finish sums them.
+// Few rows (decode): one GEMV launch, split over K.  CTA (column group cg, K
+// chunk kc), 256 threads = 8 warps: lane l owns the 8 columns cg * 256 + 8 l
+// (one 16-byte W segment, so a warp reads 512 contiguous bytes of a W row), warp
+// w the rows kc * KR + w, + 8, ... of the chunk.  The CTA sums its 8 warps in
+// shared memory and writes one fp32 partial per (row, column) to the workspace;
+// the last CTA to finish (ticket in len_dev[1], no waiting) adds the KCH partials
+// in chunk order, computes each input row's RMS factor, rounds once, writes the
+// cache slots and publishes the new length.
+constexpr int kGemvU = 10;  // W rows in flight per warp
+
+// 8 consecutive W elements as raw 16-byte words (bf16: one, fp32: two)
 template <typename T>
-__global__ void __launch_bounds__(256)
-proj_gemv_partial(const T *__restrict__ M, const T *__restrict__ g, const T *__restrict__ Wk,
-                  const T *__restrict__ Wv, float *__restrict__ part, int R, int dm, int n, int rows_per_split) {
-    const int col = (blockIdx.x * 256 + threadIdx.x) * 8;  // in [0, 2n)
-    const int k0 = blockIdx.y * rows_per_split;
-    const int k1 = min(dm, k0 + rows_per_split);
-    extern __shared__ float msh[];  // [R][rows_per_split]
-    for (int e = threadIdx.x; e < R * rows_per_split; e += 256) {
-        int r = e / rows_per_split, kk = k0 + e % rows_per_split;
-        float x = 0.f;
-        if (kk < k1) {
-            x = to_f32(M[(size_t)r * dm + kk]);
-            if (g) x *= to_f32(g[kk]);
+struct W8 {
+    uint4 u[sizeof(T) / 2];
+};
+template <typename T>
+__device__ __forceinline__ W8<T> ld_w8(const T *p) {
+    W8<T> r;
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(T) / 2); ++i) r.u[i] = __ldg(reinterpret_cast<const uint4 *>(p) + i);
+    return r;
+}
+template <typename T>
+__device__ __forceinline__ void cvt_w8(const W8<T> &r, float w[8]) {
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t x[4] = {r.u[0].x, r.u[0].y, r.u[0].z, r.u[0].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            w[2 * e] = __uint_as_float(x[e] << 16);
+            w[2 * e + 1] = __uint_as_float(x[e] & 0xFFFF0000u);
         }
-        msh[e] = x;
-    }
-    __syncthreads();
-    if (col >= 2 * n) return;
-    const T *W = (col < n) ? Wk : Wv;
-    const int wc = col % n;
-    for (int r0 = 0; r0 < R; r0 += 4) {
-        float acc[4][8] = {};
-        for (int kk = k0; kk < k1; ++kk) {
-            float w[8];
-            if constexpr (sizeof(T) == 2) {
-                uint4 u = *reinterpret_cast<const uint4 *>(W + (size_t)kk * n + wc);
-                uint32_t x[4] = {u.x, u.y, u.z, u.w};
+    } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    w[2 * e] = __uint_as_float(x[e] << 16);
-                    w[2 * e + 1] = __uint_as_float(x[e] & 0xFFFF0000u);
-                }
-            } else {
-                const float4 *p = reinterpret_cast<const float4 *>(W + (size_t)kk * n + wc);
-                float4 a = p[0], b = p[1];
-                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-            }
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                const float m = (r0 + rr < R) ? msh[(r0 + rr) * rows_per_split + (kk - k0)] : 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[rr][e] = fmaf(m, w[e], acc[rr][e]);
-            }
-        }
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            if (r0 + rr >= R) break;
-            float4 *dst = reinterpret_cast<float4 *>(part + ((size_t)blockIdx.y * R + r0 + rr) * 2 * n + col);
-            dst[0] = make_float4(acc[rr][0], acc[rr][1], acc[rr][2], acc[rr][3]);
-            dst[1] = make_float4(acc[rr][4], acc[rr][5], acc[rr][6], acc[rr][7]);
+        for (int i = 0; i < 2; ++i) {
+            w[4 * i] = __uint_as_float(r.u[i].x);
+            w[4 * i + 1] = __uint_as_float(r.u[i].y);
+            w[4 * i + 2] = __uint_as_float(r.u[i].z);
+            w[4 * i + 3] = __uint_as_float(r.u[i].w);
         }
     }
 }
 
-// sum the K slices, apply the RMS factor, round once, write the cache slot
 template <typename T>
-__global__ void proj_gemv_finish(const float *__restrict__ part, const float *__restrict__ r, T *__restrict__ kc,
-                                 T *__restrict__ vc, int R, int T_rows, int n, int Hkv, int d, int64_t cap,
-                                 int64_t len, int splits, int32_t *len_dev) {
-    const int idx = blockIdx.x * blockDim.x + threadIdx.x;  // over R * 2n
-    if (idx < R * 2 * n) {
-        const int row = idx / (2 * n), col = idx % (2 * n);
-        float acc = 0.f;
-        for (int s = 0; s < splits; ++s) acc += part[((size_t)s * R + row) * 2 * n + col];
-        const int b = row / T_rows, t = row % T_rows;
-        const int cn = col % n, h = cn / d, c = cn % d;
-        T *dst = (col < n) ? kc : vc;
-        dst[(((size_t)b * Hkv + h) * cap + len + t) * d + c] = from_f32<T>(acc * r[row]);
+__device__ __forceinline__ void load_w8(const T *p, float w[8]) {
+    if constexpr (sizeof(T) == 2) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+        const uint32_t x[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            w[2 * e] = __uint_as_float(x[e] << 16);
+            w[2 * e + 1] = __uint_as_float(x[e] & 0xFFFF0000u);
+        }
+    } else {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p)), b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
     }
-    finish_append(len_dev, len + T_rows);
+}
+
+template <typename T, int kGemvRG>
+__global__ void __launch_bounds__(256)
+proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__restrict__ Wk, const T *__restrict__ Wv,
+                 float *__restrict__ part, T *__restrict__ kc, T *__restrict__ vc, int R, int T_rows, int dm, int n,
+                 int Hkv, int d, int64_t cap, int64_t len, float eps, int KR, int32_t *len_dev) {
+    extern __shared__ float msh[];  // [kGemvRG][KR]: this chunk of the input rows, times the gain
+    __shared__ float red[8][256];   // [warp][lane * 8 + e] for one input row
+    __shared__ int last;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int col = blockIdx.x * 256 + lane * 8;  // first of this lane's 8 columns, in [0, 2n)
+    const bool col_ok = col < 2 * n;
+    const T *W = (col < n) ? Wk + col : Wv + (col - n);
+    const int k0 = blockIdx.y * KR, k1 = min(dm, k0 + KR);
+    const int nkc = gridDim.y;
+    for (int r0 = 0; r0 < R; r0 += kGemvRG) {
+        const int rg = min(kGemvRG, R - r0);
+        for (int e = tid; e < rg * KR; e += 256) {
+            const int rr = e / KR, kk = k0 + e % KR;
+            float x = 0.f;
+            if (kk < k1) {
+                x = to_f32(M[(size_t)(r0 + rr) * dm + kk]);
+                if (g) x *= to_f32(g[kk]);
+            }
+            msh[e] = x;
+        }
+        __syncthreads();
+        float acc[kGemvRG][8] = {};
+        auto fma_row = [&](const W8<T> &raw, int kk) {
+            float w[8];
+            cvt_w8(raw, w);
+#pragma unroll
+            for (int rr = 0; rr < kGemvRG; ++rr) {
+                const float m = (rr < rg) ? msh[rr * KR + (kk - k0)] : 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[rr][e] = fmaf(m, w[e], acc[rr][e]);
+            }
+        };
+        if (col_ok) {
+            int kk = k0 + warp;
+            // batches of kGemvU rows: every load of a batch is issued before its FMAs
+            for (; kk + 8 * (kGemvU - 1) < k1; kk += 8 * kGemvU) {
+                W8<T> raw[kGemvU];
+#pragma unroll
+                for (int u = 0; u < kGemvU; ++u) raw[u] = ld_w8(W + (size_t)(kk + 8 * u) * n);
+#pragma unroll
+                for (int u = 0; u < kGemvU; ++u) fma_row(raw[u], kk + 8 * u);
+            }
+            for (; kk < k1; kk += 8) fma_row(ld_w8(W + (size_t)kk * n), kk);
+        }
+        for (int rr = 0; rr < rg; ++rr) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) red[warp][lane * 8 + e] = acc[rr][e];
+            __syncthreads();
+            // thread tid sums column tid of this group over the 8 warps
+            const int c = blockIdx.x * 256 + tid;
+            if (c < 2 * n) {
+                float sum = 0.f;
+#pragma unroll
+                for (int w8 = 0; w8 < 8; ++w8) sum += red[w8][tid];
+                part[((size_t)blockIdx.y * R + r0 + rr) * 2 * n + c] = sum;
+            }
+            __syncthreads();
+        }
+    }
+    // the last CTA adds the chunks' partials (fixed order) and writes the slots
+    __threadfence();  // this thread's partials are visible before the ticket is taken
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned total = gridDim.x * gridDim.y;
+        last = (atomicAdd(reinterpret_cast<unsigned *>(len_dev + 1), 1u) == total - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    for (int row = 0; row < R; ++row) {
+        // RMS factor of the raw input row (16-byte loads; dm % 8 == 0)
+        float ss = 0.f;
+        for (int kv = tid * 8; kv < dm; kv += 256 * 8) {
+            float x[8];
+            load_w8(M + (size_t)row * dm + kv, x);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) ss = fmaf(x[q], x[q], ss);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) red[0][warp] = ss;
+        __syncthreads();
+        float sq = 0.f;
+#pragma unroll
+        for (int w8 = 0; w8 < 8; ++w8) sq += red[0][w8];
+        const float r = rsqrtf(sq / (float)dm + eps);
+        const int b = row / T_rows, t = row % T_rows;
+        // 8 consecutive columns per thread (2n % 8 == 0): the chunks' partials as
+        // float4 pairs, four chunks in flight
+        for (int c = tid * 8; c < 2 * n; c += 256 * 8) {
+            float sum[8] = {};
+            const float *pc = part + (size_t)row * 2 * n + c;
+            const size_t qstride = (size_t)R * 2 * n;
+            int q = 0;
+            for (; q + 4 <= nkc; q += 4) {
+                float4 v[4][2];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    v[u][0] = __ldcg(reinterpret_cast<const float4 *>(pc + (q + u) * qstride));
+                    v[u][1] = __ldcg(reinterpret_cast<const float4 *>(pc + (q + u) * qstride) + 1);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    sum[0] += v[u][0].x; sum[1] += v[u][0].y; sum[2] += v[u][0].z; sum[3] += v[u][0].w;
+                    sum[4] += v[u][1].x; sum[5] += v[u][1].y; sum[6] += v[u][1].z; sum[7] += v[u][1].w;
+                }
+            }
+            for (; q < nkc; ++q) {
+                const float4 a = __ldcg(reinterpret_cast<const float4 *>(pc + q * qstride));
+                const float4 bb = __ldcg(reinterpret_cast<const float4 *>(pc + q * qstride) + 1);
+                sum[0] += a.x; sum[1] += a.y; sum[2] += a.z; sum[3] += a.w;
+                sum[4] += bb.x; sum[5] += bb.y; sum[6] += bb.z; sum[7] += bb.w;
+            }
+            // the 8 columns lie in one head of Wk or of Wv (n % 8 == 0, d % 8 == 0)
+            const int cn = c % n, h = cn / d, cc = cn % d;
+            T *dst = ((c < n) ? kc : vc) + (((size_t)b * Hkv + h) * cap + len + t) * d + cc;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = from_f32<T>(sum[e] * r);
+        }
+        __syncthreads();  // red[0] is rewritten for the next row
+    }
+    if (tid == 0) {
+        len_dev[0] = (int32_t)(len + T_rows);
+        __threadfence();
+        atomicExch(reinterpret_cast<unsigned *>(len_dev + 1), 0u);
+    }
 }
 
 }  // namespace yoco
@@ -202,45 +317,55 @@ namespace yoco_host {
 using namespace yoco;
 
 constexpr int kGemvMaxRows = 16;
-constexpr int kGemvSplits = 128;
 
-static bool gemv_eligible(int R, int n) { return R <= kGemvMaxRows && n % 8 == 0; }
+static bool gemv_eligible(int R, int n, int dm) { return R <= kGemvMaxRows && n % 8 == 0 && dm % 8 == 0; }
+
+// K chunks of the few-row path: about one CTA per SM over all column groups
+static int gemv_chunks(int n, int dm) {
+    const int groups = (2 * n + 255) / 256;
+    int kch = std::max(1, 152 / groups);
+    kch = std::min(kch, dm);
+    const int kr = (dm + kch - 1) / kch;
+    return (dm + kr - 1) / kr;
+}
 
 // workspace: [0, 256) status word of the tensor-core kernel, one fp32 RMS factor
-// per row, then (few-row path) the split-K partials
+// per row (tensor-core and tiled paths), then (few-row path) the K-chunk partials
 size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt) {
-    (void)dm; (void)dt;
+    (void)dt;
     size_t rows = (size_t)B * T;
     size_t ws = 256 + ((rows * sizeof(float) + 255) / 256) * 256;
     const int n = Hkv * d;
-    if (gemv_eligible((int)rows, n)) ws += (size_t)kGemvSplits * rows * 2 * n * sizeof(float);
+    if (gemv_eligible((int)rows, n, dm)) ws += (size_t)gemv_chunks(n, dm) * rows * 2 * n * sizeof(float);
     return ws;
 }
 
 template <typename T>
 static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
     const int R = a.B * a.T;
-    float *r = (float *)((char *)ws + 256);
-    count_launches(1);
-    rms_rows_kernel<T><<<(R * 32 + 255) / 256, 256, 0, st>>>((const T *)a.M, r, R, a.dm, a.eps);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    if (std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a)) return kv_project_append_tc(a, r, (int *)ws, st);
     const int n = a.Hkv * a.d;
-    if (gemv_eligible(R, n)) {
+    float *r = (float *)((char *)ws + 256);
+    cudaError_t e;
+    if (gemv_eligible(R, n, a.dm) && !(std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a))) {
+        const int kch = gemv_chunks(n, a.dm);
+        const int KR = (a.dm + kch - 1) / kch;
+        const int rg = (R == 1) ? 1 : 4;  // input rows per pass
+        const size_t smem = (size_t)rg * KR * sizeof(float);
+        auto kern = (R == 1) ? proj_gemv_splitk<T, 1> : proj_gemv_splitk<T, 4>;
+        if (smem > 48 * 1024 &&
+            (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+            return e;
         float *part = r + ((size_t)R + 63) / 64 * 64;
-        const int rows_per_split = (a.dm + kGemvSplits - 1) / kGemvSplits;
-        const int splits = (a.dm + rows_per_split - 1) / rows_per_split;
-        dim3 g1((2 * n / 8 + 255) / 256, splits);
-        count_launches(2);
-        proj_gemv_partial<T><<<g1, 256, (size_t)R * rows_per_split * sizeof(float), st>>>(
-            (const T *)a.M, (const T *)a.rms_w, (const T *)a.Wk, (const T *)a.Wv, part, R, a.dm, n, rows_per_split);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        const int total = R * 2 * n;
-        proj_gemv_finish<T><<<(total + 255) / 256, 256, 0, st>>>(part, r, (T *)a.kc, (T *)a.vc, R, a.T, n, a.Hkv, a.d,
-                                                                 a.cap, a.len, splits, a.len_dev);
+        count_launches(1);
+        kern<<<dim3((2 * n + 255) / 256, kch), 256, smem, st>>>(
+            (const T *)a.M, (const T *)a.rms_w, (const T *)a.Wk, (const T *)a.Wv, part, (T *)a.kc, (T *)a.vc, R, a.T,
+            a.dm, n, a.Hkv, a.d, a.cap, a.len, a.eps, KR, a.len_dev);
         return cudaGetLastError();
     }
+    count_launches(1);
+    rms_rows_kernel<T><<<(R * 32 + 255) / 256, 256, 0, st>>>((const T *)a.M, r, R, a.dm, a.eps);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a)) return kv_project_append_tc(a, r, (int *)ws, st);
     count_launches(1);
     dim3 grid((2 * a.Hkv * a.d + 63) / 64, (R + 63) / 64);
     proj_append_simt<T><<<grid, 256, 0, st>>>((const T *)a.M, (const T *)a.rms_w, (const T *)a.Wk, (const T *)a.Wv,
