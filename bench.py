@@ -52,6 +52,7 @@ def parse():
     p.add_argument("--cache-len", type=int, default=0,
                    help="--only cross_decode: cache length (default: the step's prompt length)")
     p.add_argument("--batch", type=int, default=0, help="--only cross_decode: sequences (default: the step's B)")
+    p.add_argument("--splits", type=int, default=0, help="--only cross_decode: key splits (default: automatic)")
     return p.parse_args()
 
 
@@ -528,12 +529,12 @@ def run_only(args):
         cache.set_length(Nc)
         Qd = normal((Bc, HQ, D), bf, sid(CFG, 0, synth.T_QX, 1))
         Od = torch.empty_like(Qd)
-        ws = torch.empty(max(256, L.yoco_cross_attn_workspace_size(Bc, HQ, 1, ctypes.byref(cache.c), 0)),
+        ws = torch.empty(max(256, L.yoco_cross_attn_workspace_size(Bc, HQ, 1, ctypes.byref(cache.c), args.splits)),
                          dtype=torch.uint8, device=dev)
 
         def call():
-            return L.yoco_cross_attn_decode(P(Qd), HQ, ctypes.byref(cache.c), D ** -0.5, 0, P(Od), P(ws), ws.numel(),
-                                            stp)
+            return L.yoco_cross_attn_decode(P(Qd), HQ, ctypes.byref(cache.c), D ** -0.5, args.splits, P(Od), P(ws),
+                                            ws.numel(), stp)
     for _ in range(args.warmup):
         assert call() == 0, L.yoco_last_error()
     torch.cuda.synchronize()

@@ -376,6 +376,26 @@ def test_cross_attn_decode_split_invariance(Y):
         assert rel_l2(r, results[0]) <= 1e-2
 
 
+def test_cross_attn_decode_garbage_workspace_twice(Y):
+    """Decode needs no clean workspace: one full of arbitrary bytes (status
+    word aside) gives the oracle's result, and so does a second call on it."""
+    import torch
+    B, Hq, Hkv, d, length = 1, 24, 8, 128, 5000
+    K, V, cache = fill_cache(Y, B, Hkv, d, length, length, "bf16", 32)
+    Q, Qd = gen(SEED, sid(32, 2, synth.T_QX), (B, Hq, d), "bf16")
+    O_ref = oracle.cross_attn(Q[:, None], K, V, length - 1, d ** -0.5)[:, 0]
+    for splits in (0, 5):
+        n = Y.yoco_cross_attn_workspace_size(B, Hq, 1, cache, splits)
+        ws = torch.full((n,), 0xA5, dtype=torch.uint8, device="cuda")
+        ws[:256] = 0  # the status word of a fresh workspace
+        for _ in range(2):
+            O = torch.empty_like(Qd)
+            Y.yoco_cross_attn_decode(Qd, cache, O, num_splits=splits, workspace=ws)
+            torch.cuda.synchronize()
+            assert rel_l2(host_f64(O), O_ref) <= BF16_REL_L2
+        Y.yoco_workspace_status(ws)
+
+
 def test_early_exit_matches_full_prefill_last_row(Y):
     """Early exit (paper Fig. 3): the last prompt row computed alone equals the
     last row of the full causal prefill."""
