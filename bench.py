@@ -61,7 +61,8 @@ def workload_config(chunk_used):
             "gret_heads": H, "d": D, "chunk": chunk_used, "tau": TAU, "cross_layers": L_CROSS, "Hq": HQ,
             "Hkv": HKV, "d_model": DM, "gate_logits": "N(2,1)", "qk": "N(0,1)/sqrt(128)", "v_M_Q": "N(0,1)",
             "W": "N(0,0.02)", "l2": "no flush: each step reads 8.1 GB of inputs (> 129 MB L2)",
-            "parallelism": "replicas"}
+            "parallelism": "replicas",
+            "cuda_graph": "the generated token's 13 recurrent gRet steps, captured once, replayed every step"}
 
 
 # ----------------------------------------------------------------- CPU oracle
@@ -284,6 +285,13 @@ def run_gpu(args):
         if st != 0:
             raise RuntimeError(f"{what}: {L.yoco_last_error().decode()}")
 
+    def gret_decode_layers(sp):
+        for l in range(L_SELF):
+            check(L.yoco_gret_decode_step(P(q1[l]), P(k1[l]), P(v1[l]), P(lg1[l]), TAU, P(S[l]), P(o1[l]), B, H, D,
+                                          D, 1, 1, sp), "gret decode")
+
+    decode_graph = []  # filled below: the 13 recurrent gRet steps as one CUDA graph
+
     def step(timed_calls=None, marks=None, wait_layer=None, wait_rest=None):
         def mark(i):
             if marks is not None:
@@ -311,9 +319,10 @@ def run_gpu(args):
             check(L.yoco_cross_attn_prefill(P(Qx[l]), HQ, 1, N - 1, cc, D ** -0.5, P(Ox[l]), wsp, wsn, stp),
                   "cross prefill")
         mark(3)
-        for l in range(L_SELF):
-            check(L.yoco_gret_decode_step(P(q1[l]), P(k1[l]), P(v1[l]), P(lg1[l]), TAU, P(S[l]), P(o1[l]), B, H, D,
-                                          D, 1, 1, stp), "gret decode")
+        if decode_graph:
+            decode_graph[0].replay()  # the 13 recurrent steps (their launches, captured once)
+        else:
+            gret_decode_layers(stp)
         mark(4)
         check(L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, cc, wsp, wsn, stp), "append 1")
         mark(5)
@@ -326,6 +335,22 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    # The generated token's 13 recurrent gRet steps do not depend on the cache
+    # length, so they are captured once as a CUDA graph (same buffers, same launches)
+    # and replayed every step: the step is then not bound by 13 host launches.
+    step()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    n0 = L.yoco_launch_count()
+    with torch.cuda.graph(g, stream=cap):
+        gret_decode_layers(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    graph_launches = L.yoco_launch_count() - n0
+    stream.wait_stream(cap)
+    torch.cuda.synchronize()
+    decode_graph.append(g)
+
     # the clock sampler starts before the warm-up so that it is sampling when the
     # timed region begins; the summary keeps the samples stamped inside that region
     # (plus one interval on either side, the GPU being busy then too)
@@ -335,7 +360,7 @@ def run_gpu(args):
         step()
     launches0 = L.yoco_launch_count()
     step()
-    launches_per_step = L.yoco_launch_count() - launches0
+    launches_per_step = L.yoco_launch_count() - launches0 + graph_launches  # replays are not counted on the host
     barrier()
 
     # ---- timed region: K steps, per-call events around the gRet prefill calls

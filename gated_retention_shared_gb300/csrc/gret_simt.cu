@@ -239,6 +239,21 @@ gret_decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, co
     const int bh = blockIdx.y;
     const int c0 = blockIdx.x * 32;
     const int tid = threadIdx.x;
+    const int cg = tid % 8;   // columns c0 + 4 cg .. +3
+    const int rg = tid / 8;   // rows rg, rg + 32, ...
+    // launched as a programmatic dependent of the previous kernel on the stream: let
+    // the next one start its launch, then wait for this one's inputs
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // this thread's state rows first (dk <= 128: at most 4 rows), so their loads
+    // and those of q, k, v are in flight together
+    float *Sb = state + (size_t)bh * dk * dv;
+    float4 srow[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = rg + 32 * u;
+        if (i < dk) srow[u] = *reinterpret_cast<const float4 *>(Sb + (size_t)i * dv + c0 + 4 * cg);
+    }
     for (int i = tid; i < dk; i += 256) {
         qs[i] = to_f32(q[(size_t)bh * dk + i]);
         ks[i] = to_f32(k[(size_t)bh * dk + i]);
@@ -246,19 +261,18 @@ gret_decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, co
     if (tid < 32) vs[tid] = to_f32(v[(size_t)bh * dv + c0 + tid]);
     const float gamma = expf(log_gate(logits[bh], inv_tau));
     __syncthreads();
-    const int cg = tid % 8;   // columns c0 + 4 cg .. +3
-    const int rg = tid / 8;   // rows rg, rg + 32, ...
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float *Sb = state + (size_t)bh * dk * dv;
-    for (int i = rg; i < dk; i += 32) {
-        float4 *p4 = reinterpret_cast<float4 *>(Sb + (size_t)i * dv + c0 + 4 * cg);
-        float4 s = *p4;
-        float ki = ks[i], qi = qs[i];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = rg + 32 * u;
+        if (i >= dk) break;
+        float4 s = srow[u];
+        const float ki = ks[i], qi = qs[i];
         s.x = fmaf(gamma, s.x, ki * vs[4 * cg + 0]);
         s.y = fmaf(gamma, s.y, ki * vs[4 * cg + 1]);
         s.z = fmaf(gamma, s.z, ki * vs[4 * cg + 2]);
         s.w = fmaf(gamma, s.w, ki * vs[4 * cg + 3]);
-        *p4 = s;
+        *reinterpret_cast<float4 *>(Sb + (size_t)i * dv + c0 + 4 * cg) = s;
         acc[0] = fmaf(qi, s.x, acc[0]);
         acc[1] = fmaf(qi, s.y, acc[1]);
         acc[2] = fmaf(qi, s.z, acc[2]);
@@ -358,17 +372,23 @@ cudaError_t gret_prefill_simt(const GretArgs &a, void *ws, cudaStream_t st) {
 
 cudaError_t gret_decode(const void *q, const void *k, const void *v, const float *logits, float tau,
                         float *state, void *o, int B, int H, int dk, int dv, yoco_dtype dt, cudaStream_t st) {
-    dim3 grid(dv / 32, B * H);
+    // a programmatic dependent of the previous kernel: in a run of layers (or a
+    // captured graph of them) each step's launch overlaps the previous step
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(dv / 32, B * H);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     count_launches(1);
     if (dt == YOCO_F32)
-        gret_decode_step_kernel<float, float><<<grid, 256, 0, st>>>((const float *)q, (const float *)k,
-                                                                    (const float *)v, logits, 1.0f / tau, state,
-                                                                    (float *)o, H, dk, dv);
-    else
-        gret_decode_step_kernel<bf16_t, bf16_t><<<grid, 256, 0, st>>>((const bf16_t *)q, (const bf16_t *)k,
-                                                                      (const bf16_t *)v, logits, 1.0f / tau,
-                                                                      state, (bf16_t *)o, H, dk, dv);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, gret_decode_step_kernel<float, float>, (const float *)q, (const float *)k,
+                                  (const float *)v, logits, 1.0f / tau, state, (float *)o, H, dk, dv);
+    return cudaLaunchKernelEx(&cfg, gret_decode_step_kernel<bf16_t, bf16_t>, (const bf16_t *)q, (const bf16_t *)k,
+                              (const bf16_t *)v, logits, 1.0f / tau, state, (bf16_t *)o, H, dk, dv);
 }
 
 }  // namespace yoco_host

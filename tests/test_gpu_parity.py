@@ -468,6 +468,46 @@ def test_device_generator_matches_host(Y):
     assert np.max(np.abs(f.cpu().numpy() - synth.normal(SEED, 99, (5000,), "f32", mean=2.0))) <= 1e-6
 
 
+# ------------------------------------------------------------- CUDA graphs
+
+def test_gret_decode_steps_replayed_from_a_cuda_graph(Y):
+    """The recurrent step launches nothing that a stream capture forbids: 13
+    layers' steps captured once and replayed three times give bit for bit what
+    three eager passes give (the state carries from replay to replay)."""
+    import torch
+    B, H, d, layers = 1, 24, 128, 13
+    ins = []
+    for l in range(layers):
+        q, qd = gen(SEED, sid(33, l, synth.T_Q), (B, H, d), "bf16", std=d ** -0.5)
+        k, kd = gen(SEED, sid(33, l, synth.T_K), (B, H, d), "bf16", std=d ** -0.5)
+        v, vd = gen(SEED, sid(33, l, synth.T_V), (B, H, d), "bf16")
+        lg = synth.normal(SEED, sid(33, l, synth.T_LOGIT), (B, H), "f32", mean=2.0)
+        ins.append((qd, kd, vd, dev_f32(lg)))
+    S0 = dev_f32(synth.normal(SEED, sid(33, 99, synth.T_S0), (layers, B, H, d, d), "f32", std=0.05))
+
+    def run(S, outs, stream=None):
+        for l in range(layers):
+            qd, kd, vd, lgd = ins[l]
+            Y.yoco_gret_decode_step(qd, kd, vd, lgd, 16.0, S[l], outs[l], stream=stream)
+
+    S_e, o_e = S0.clone(), [torch.empty_like(ins[0][2]) for _ in range(layers)]
+    for _ in range(3):
+        run(S_e, o_e)
+    S_g, o_g = S0.clone(), [torch.empty_like(ins[0][2]) for _ in range(layers)]
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side):
+        run(S_g, o_g)
+    S_g.copy_(S0)  # capture recorded the launches without running them; start from S0
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(S_g, S_e)
+    for a, b in zip(o_g, o_e):
+        assert torch.equal(a, b)
+
+
 # ------------------------------------------------------------- failure path
 
 def test_bounded_wait_times_out_and_context_survives(Y):
