@@ -47,7 +47,7 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk", type=int, default=0)
-    p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode"], default=None,
+    p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode", "cross_prefill"], default=None,
                    help="time one call of the step on its bench shape (for profiling)")
     p.add_argument("--cache-len", type=int, default=0,
                    help="--only cross_decode: cache length (default: the step's prompt length)")
@@ -532,6 +532,20 @@ def run_only(args):
             cache.set_length(N)
             return L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, ctypes.byref(cache.c),
                                                    P(ws), ws.numel(), stp)
+    elif args.only == "cross_prefill":  # every prompt row over the shared cache (no early exit)
+        Tq = args.cache_len or N
+        Kc = normal((B, HKV, Tq, D), bf, sid(CFG, 0, synth.T_CACHE_K))
+        Vc = normal((B, HKV, Tq, D), bf, sid(CFG, 0, synth.T_CACHE_V))
+        cache = Y.KVCache(B, HKV, D, Tq, k=Kc, v=Vc)
+        cache.set_length(Tq)
+        Qp = normal((B, Tq, HQ, D), bf, sid(CFG, 0, synth.T_QX))
+        Op = torch.empty_like(Qp)
+        ws = torch.empty(max(256, L.yoco_cross_attn_workspace_size(B, HQ, Tq, ctypes.byref(cache.c), 0)),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            return L.yoco_cross_attn_prefill(P(Qp), HQ, Tq, 0, ctypes.byref(cache.c), D ** -0.5, P(Op), P(ws),
+                                             ws.numel(), stp)
     elif args.only == "proj":
         M = normal((B, N, DM), bf, sid(CFG, 0, synth.T_M))
         Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
@@ -571,6 +585,10 @@ def run_only(args):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     line = {"only": args.only, "ms_per_call": ms, "steps": args.steps}
+    if args.only == "cross_prefill":
+        # causal: row t reads t + 1 keys; QK^T and PV cost 2 d flops per (row, key, head) each
+        flops = 4.0 * D * HQ * B * Tq * (Tq + 1) / 2
+        line.update({"rows": Tq, "flops_per_call": flops, "achieved_tflops": round(flops / (ms / 1e3) / 1e12, 1)})
     if args.only == "cross_decode":
         # every K/V byte of every sequence is read once per call
         nbytes = 2 * Bc * HKV * Nc * D * 2

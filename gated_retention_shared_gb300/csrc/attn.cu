@@ -274,6 +274,8 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(const float *__restrict
 namespace yoco_host {
 using namespace yoco;
 
+constexpr int kFaMinRows = 64;  // from this many query rows on, prefill uses attn_fa_kernel
+
 static int rows_per_block(int G) { return G >= kAttnMaxQ ? 1 : kAttnMaxQ / G; }
 
 int attn_auto_splits(int B, int Hkv, int64_t keys, int ctas_per_sm) {
@@ -336,6 +338,9 @@ static cudaError_t launch(const AttnArgs &a, int splits, void *ws, cudaStream_t 
     const int rb_eff = (nq <= 4 && a.T <= RB) ? a.T : RB;
     float *part = (float *)((char *)ws + 256);
     cudaError_t e;
+    // many rows (prefill): 128-row query tiles on the tensor cores, no key splits
+    if (std::is_same<T, bf16_t>::value && a.T >= kFaMinRows && attn_fa_eligible(a))
+        return attn_fa_launch(a, 0, (int *)ws, st);
     if (std::is_same<T, bf16_t>::value && attn_tc_eligible(a, nq)) {
         count_launches(splits > 1 ? 2 : 1);
         e = attn_tc_launch(a, rb_eff, nq, kps, splits, part, (int *)ws, st);

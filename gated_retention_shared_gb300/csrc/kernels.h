@@ -69,6 +69,10 @@ bool attn_tc_eligible(const AttnArgs &a, int nq);
 cudaError_t attn_tc_launch(const AttnArgs &a, int RB, int nq, int64_t kps, int splits, void *part, int *err,
                            cudaStream_t st);
 
+// attn_fa.cu: many query rows (prefill), bf16, d = 128; window > 0 adds the sliding-window mask
+bool attn_fa_eligible(const AttnArgs &a);
+cudaError_t attn_fa_launch(const AttnArgs &a, int64_t window, int *err, cudaStream_t st);
+
 // selftest.cu
 cudaError_t selftest_wait(void *ws, uint64_t limit_ns, cudaStream_t st);
 

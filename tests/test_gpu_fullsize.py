@@ -154,6 +154,34 @@ def test_decode_step_131072_cache(Y, B):
     assert cache.length == N + 1
 
 
+def test_cross_attn_full_prefill_32k(Y):
+    """Causal cross-attention prefill of all 32768 rows over a 32768-token cache
+    (24 query heads on 8 kv heads): sampled rows of two kv groups, from the
+    first and last query tiles and between, against the oracle row by row."""
+    import torch
+    B, Hkv, Hq, D, N = 1, 8, 24, 128, 32768
+    cfg = 36
+    K = dev_normal((B, Hkv, N, D), torch.bfloat16, SID(cfg, 0, synth.T_CACHE_K))
+    V = dev_normal((B, Hkv, N, D), torch.bfloat16, SID(cfg, 0, synth.T_CACHE_V))
+    cache = Y.KVCache(B, Hkv, D, N, k=K, v=V)
+    cache.set_length(N)
+    Q = dev_normal((B, N, Hq, D), torch.bfloat16, SID(cfg, 1, synth.T_QX))
+    O = torch.empty_like(Q)
+    Y.yoco_cross_attn_prefill(Q, cache, 0, O)
+    torch.cuda.synchronize()
+    G = Hq // Hkv
+    for hk in (0, Hkv - 1):
+        Kh = _host_cache_rows(cfg, synth.T_CACHE_K, B, Hkv, N, D, 0, hk, N)
+        Vh = _host_cache_rows(cfg, synth.T_CACHE_V, B, Hkv, N, D, 0, hk, N)
+        for row in (0, 127, 128, 5000, 16383, N - 1):
+            Qg = np.stack([host_head(SID(cfg, 1, synth.T_QX), B, N, Hq, D, 0, h, row, row + 1)[0]
+                           for h in range(hk * G, (hk + 1) * G)])
+            O_ref = oracle.cross_attn(Qg[None, None], Kh[None, None, :row + 1], Vh[None, None, :row + 1], row,
+                                      D ** -0.5)[0, 0]
+            got = host_f64(O[0, row, hk * G:(hk + 1) * G])
+            assert rel_l2(got, O_ref) <= BF16_REL_L2, (hk, row, rel_l2(got, O_ref))
+
+
 def test_decode_1m_cache_and_state_step(Y):
     """1M-token decode: one recurrent gRet step on 24 x 128 x 128 states and a
     cross layer over 1048576 cached tokens (kv head 0's group checked)."""

@@ -358,6 +358,43 @@ def test_cross_attn_prefill_bf16_gqa(Y, T, p0):
     assert rel_l2(host_f64(O), O_ref) <= BF16_REL_L2
 
 
+@pytest.mark.parametrize("B,T,p0", [(2, 300, 77), (1, 64, 0), (1, 2048, 0), (1, 257, 4000)])
+def test_cross_attn_prefill_many_rows(Y, B, T, p0):
+    """Many-row prefill (128-row query tiles): ragged last tile, a diagonal that
+    does not start on a tile boundary, a block of exactly 64 rows, 2048 causal
+    rows, rows far into a long cache."""
+    import torch
+    Hq, Hkv, d = 24, 8, 128
+    length = p0 + T
+    K, V, cache = fill_cache(Y, B, Hkv, d, length + 129, length, "bf16", 34)
+    Q, Qd = gen(SEED, sid(34, 1, synth.T_QX), (B, T, Hq, d), "bf16")
+    O = torch.empty_like(Qd)
+    Y.yoco_cross_attn_prefill(Qd, cache, p0, O)
+    torch.cuda.synchronize()
+    O_ref = oracle.cross_attn(Q, K, V, p0, d ** -0.5)
+    assert rel_l2(host_f64(O), O_ref) <= BF16_REL_L2
+
+
+def test_cross_attn_prefill_growing_scores(Y):
+    """Keys whose scale grows along the sequence (x1 .. x8) push each row's
+    running maximum up tile after tile, so the output is rescaled many times."""
+    import torch
+    B, T, Hq, Hkv, d = 1, 1024, 24, 8, 128
+    Kb = synth.normal_f64(SEED, sid(35, 0, synth.T_CACHE_K), B * Hkv * T * d).reshape(B, Hkv, T, d)
+    Kb *= (1.0 + 7.0 * np.arange(T) / T)[None, None, :, None]
+    kbits = synth.f64_to_bf16_bits(Kb)
+    K = synth.bf16_bits_to_f32(kbits).astype(np.float64)
+    V, Vd = gen(SEED, sid(35, 0, synth.T_CACHE_V), (B, Hkv, T, d), "bf16")
+    cache = Y.KVCache(B, Hkv, d, T, dtype=Vd.dtype, k=dev_bf16(kbits), v=Vd)
+    cache.set_length(T)
+    Q, Qd = gen(SEED, sid(35, 1, synth.T_QX), (B, T, Hq, d), "bf16", std=2.0)
+    O = torch.empty_like(Qd)
+    Y.yoco_cross_attn_prefill(Qd, cache, 0, O)
+    torch.cuda.synchronize()
+    O_ref = oracle.cross_attn(Q, K, V, 0, d ** -0.5)
+    assert rel_l2(host_f64(O), O_ref) <= BF16_REL_L2
+
+
 def test_cross_attn_decode_split_invariance(Y):
     """The decode result does not depend on the number of key splits."""
     import torch
