@@ -3,24 +3,28 @@
 // prefill; with a window it is the sliding-window attention of Section 3.2,
 // Eq. 8), bf16, head size 128, on the 5th-generation tensor cores.
 //
-// One CTA = 128 consecutive query rows of one query head.  Per 128-key tile j:
-//     S_j   = Q K_j^T                       (tcgen05, M 128 rows, N 128 keys, TMEM)
-//     P_j   = exp(scale S_j - m)  masked    (softmax warps, bf16 written over S_j)
-//     O    += P_j V_j                       (tcgen05, A = P_j from TMEM)
-// m is a per-row reference maximum that only moves when a tile's maximum passes
-// it by more than 8 (natural log units); O is then rescaled in TMEM once.  Every
-// P value stays below e^8, the exponent of the final normalisation uses the same
-// m, so the result is the plain softmax up to rounding.
+// One CTA = 256 consecutive query rows of one query head, as two sets of 128
+// (A: rows 0..127, B: rows 128..255), each with its own softmax warpgroup, so the
+// tensor cores work on one set while the other set's softmax runs.  Per 128-key
+// tile j and set X:
+//     S_X   = Q_X K_j^T                     (tcgen05, M 128 rows, N 128 keys, TMEM)
+//     P_X   = 2^(c S_X - m)  masked         (softmax warps, bf16 written over S_X)
+//     O_X  += P_X V_j                       (tcgen05, A = P_X from TMEM)
+// with c = scale * log2(e) and m a per-row reference maximum (base-2 units) that
+// only moves when a tile's maximum passes it by more than 8 / ln 2 (so by e^8);
+// O_X is then rescaled in TMEM once.  Every P value stays below e^8 and the final
+// normalisation uses the same m, so the result is the plain softmax up to rounding.
 //
 // Masks: key m is seen by the row at position p when m <= p (causal) and, with
-// a window W > 0, p - W < m.  Key tiles outside the block's range are skipped.
+// a window W > 0, p - W < m.  Only tiles that cross a row's boundary are masked
+// element by element; key tiles outside the CTA's range are skipped.
 //
-// Warps: 0 TMA producer (Q once, then K/V tiles through a 3-stage ring), 1 MMA
-// issuer (S of tile i is issued before P V of tile i-1, so the softmax of one
-// tile overlaps the tensor cores on the other), 2-5 softmax + epilogue (thread =
-// TMEM lane = query row).  TMEM: S double buffer at columns 0 / 128, O at 256.
-// The GQA group's heads are adjacent in the grid, so their K/V tiles are shared
-// through L2.
+// Warps: 0 TMA producer (Q_A, Q_B once, then K/V tiles through a 2-stage ring),
+// 1 MMA issuer, 2-5 softmax + epilogue of set A, 6-9 of set B (thread = TMEM lane
+// = query row).  Tensor-core order per tile: S_A(j), P_B V(j-1), S_B(j), P_A V(j),
+// so softmax A(j) overlaps the B-side MMAs and softmax B(j) the A-side ones.
+// TMEM: S_A 0, O_A 128, S_B 256, O_B 384.  The GQA group's heads are adjacent in
+// the grid, so their K/V tiles are shared through L2.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -31,28 +35,29 @@ namespace yoco {
 
 using namespace tc;
 
-constexpr int kFK = 128;                   // keys per tile = query rows per CTA
+constexpr int kFK = 128;                   // keys per tile = query rows per set
 constexpr int kFD = 128;                   // head size
-constexpr int kFStages = 3;
+constexpr int kFRows = 2 * kFK;            // query rows per CTA
+constexpr int kFStages = 2;
 constexpr int kFTile = kFK * kFD * 2;      // 32 KB bf16 tile
 constexpr int kFHalf = kFTile / 2;         // one 64-column block
-constexpr int kFThreads = 192;
-constexpr uint32_t kColS0 = 0, kColO = 256;
-constexpr float kRescaleGap = 8.f;         // m moves only when exceeded by more than this
+constexpr int kFThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleGap2 = 8.f * kLog2e;  // reference moves only when passed by more than e^8
 
 struct FaSmem {
     uint64_t q_full, full[kFStages], empty[kFStages];
-    uint64_t s_full[2], p_ready[2], pv_done[2];
+    uint64_t s_full[2], p_ready[2], pv_done[2];  // per set
     uint32_t tmem_base;
     int abort_flag;
-    int go;
+    int go[2];
 };
 
-constexpr size_t kFTileBytes = (size_t)kFTile + (size_t)kFStages * 2 * kFTile;  // Q + K/V ring
+constexpr size_t kFTileBytes = (size_t)2 * kFTile + (size_t)kFStages * 2 * kFTile;  // Q_A, Q_B + K/V ring
 constexpr size_t kFSmem = kFTileBytes + sizeof(FaSmem) + 1024;
 static_assert(kFSmem <= 232448, "flash-attention tiles must fit shared memory");
 
-__device__ __forceinline__ void fbar(int n) { asm volatile("bar.sync 1, %0;\n" ::"r"(n) : "memory"); }
+__device__ __forceinline__ void fbar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
 
 __device__ __forceinline__ uint32_t fa_tile_chunk(int r, int c) {  // 16-B chunk c (0..15) of row r, SW128
     return (uint32_t)(c >> 3) * kFHalf + (uint32_t)r * 128u + (uint32_t)(((c & 7) ^ (r & 7)) * 16);
@@ -63,6 +68,12 @@ __device__ __forceinline__ uint32_t fa_pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h2);
 }
 
+__device__ __forceinline__ float fa_ex2(float x) {  // 2^x, hardware approximation (exact 0 at -inf)
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __global__ void __launch_bounds__(kFThreads, 1)
 attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, int T, int Hq,
@@ -70,18 +81,18 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
-    uint8_t *sQ = tiles;                      // Q, later the output staging tile
-    uint8_t *ring = tiles + kFTile;           // stage s: K at ring + 2 s kFTile, V after it
+    uint8_t *sQ = tiles;                      // Q_A, Q_B (later the output staging tiles)
+    uint8_t *ring = tiles + 2 * kFTile;       // stage s: K at ring + 2 s kFTile, V after it
     FaSmem &sm = *reinterpret_cast<FaSmem *>(tiles + kFTileBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x % Hq;
     const int b = blockIdx.x / Hq;
     const int qb = (int)gridDim.y - 1 - (int)blockIdx.y;  // longest rows first
-    const int q0 = qb * kFK;
+    const int q0 = qb * kFRows;
     const int G = Hq / Hkv;
     const int bz = b * Hkv + h / G;  // (sequence, kv head) index of the cache view
     const int64_t pos_lo = p0 + q0;
-    const int64_t pos_hi = p0 + min(q0 + kFK, T) - 1;
+    const int64_t pos_hi = p0 + min(q0 + kFRows, T) - 1;
     const int64_t key_lo = (window > 0) ? max((int64_t)0, pos_lo - window + 1) : 0;
     const int j_lo = (int)(key_lo / kFK), j_hi = (int)(pos_hi / kFK);
     const int ntiles = j_hi - j_lo + 1;
@@ -92,10 +103,10 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&sm.s_full[s], 1);
-            mbar_init(&sm.p_ready[s], 1);
-            mbar_init(&sm.pv_done[s], 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&sm.s_full[x], 1);
+            mbar_init(&sm.p_ready[x], 1);
+            mbar_init(&sm.pv_done[x], 1);
         }
         sm.abort_flag = 0;
         fence_mbar_init();
@@ -123,9 +134,10 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(&sm.q_full, kFTile);
-            for (int half = 0; half < 2; ++half)
-                tma_load_4d(sQ + half * kFHalf, &tm_q, &sm.q_full, half * 64, h, q0, b);
+            mbar_arrive_expect_tx(&sm.q_full, 2 * kFTile);
+            for (int x = 0; x < 2; ++x)
+                for (int half = 0; half < 2; ++half)
+                    tma_load_4d(sQ + x * kFTile + half * kFHalf, &tm_q, &sm.q_full, half * 64, h, q0 + x * kFK, b);
             int i = 0;
             for (; i < ntiles; ++i) {
                 const int s = i % kFStages;
@@ -151,82 +163,107 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16_f32(kFK, kFK, false, false);  // A = Q (K-major), B = K (K-major)
             const uint32_t id_o = idesc_bf16_f32(kFK, kFD, false, true);   // A = P (TMEM),   B = V (N-major)
-            const uint32_t q_a = smem_u32(sQ);
             bool ok = mbar_wait(&sm.q_full, 0, abort_flag);
-            auto issue_pv = [&](int i) -> bool {  // O += P(i) V(i)
-                const int s = i % kFStages;
-                if (!mbar_wait(&sm.p_ready[i & 1], (i / 2) & 1, abort_flag)) return false;
+            auto issue_s = [&](int x, int i) -> bool {  // S_X = Q_X K(i)^T; S_X's TMEM held P_X(i-1)
+                if (i > 0 && !mbar_wait(&sm.pv_done[x], (i - 1) & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t v_a = smem_u32(ring + (size_t)s * 2 * kFTile + kFTile);
+                const uint32_t q_a = smem_u32(sQ + x * kFTile);
+                const uint32_t k_a = smem_u32(ring + (size_t)(i % kFStages) * 2 * kFTile);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kFHalf + (kk & 3) * 32;
+                    mma_ss(tmem + 256 * x, smem_desc_sw128(q_a + off, 16, 1024), smem_desc_sw128(k_a + off, 16, 1024),
+                           id_s, kk > 0);
+                }
+                mma_commit(&sm.s_full[x]);
+                return true;
+            };
+            auto issue_pv = [&](int x, int i) -> bool {  // O_X += P_X(i) V(i)
+                if (!mbar_wait(&sm.p_ready[x], i & 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t v_a = smem_u32(ring + (size_t)(i % kFStages) * 2 * kFTile + kFTile);
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColO, tmem + kColS0 + 128 * (i & 1) + kk * 8,
-                           smem_desc_sw128(v_a + kk * 2048, kFHalf, 1024), id_o, (i > 0 || kk > 0));
-                mma_commit(&sm.pv_done[i & 1]);
-                mma_commit(&sm.empty[s]);
+                    mma_ts(tmem + 256 * x + 128, tmem + 256 * x + kk * 8, smem_desc_sw128(v_a + kk * 2048, kFHalf, 1024),
+                           id_o, (i > 0 || kk > 0));
+                mma_commit(&sm.pv_done[x]);
                 return true;
             };
             for (int i = 0; i < ntiles && ok; ++i) {
                 const int s = i % kFStages;
                 if (!(ok = mbar_wait(&sm.full[s], (i / kFStages) & 1, abort_flag))) break;
-                // S buffer i&1 held P(i-2): P V of tile i-2 must be done with it
-                if (i >= 2 && !(ok = mbar_wait(&sm.pv_done[i & 1], ((i / 2) - 1) & 1, abort_flag))) break;
-                tc_fence_after();
-                const uint32_t k_a = smem_u32(ring + (size_t)s * 2 * kFTile);
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kFHalf + (kk & 3) * 32;
-                    mma_ss(tmem + kColS0 + 128 * (i & 1), smem_desc_sw128(q_a + off, 16, 1024),
-                           smem_desc_sw128(k_a + off, 16, 1024), id_s, kk > 0);
+                if (!(ok = issue_s(0, i))) break;
+                if (i > 0) {
+                    if (!(ok = issue_pv(1, i - 1))) break;
+                    mma_commit(&sm.empty[(i - 1) % kFStages]);  // tile i-1 fully used
                 }
-                mma_commit(&sm.s_full[i & 1]);
-                if (i > 0 && !(ok = issue_pv(i - 1))) break;
+                if (!(ok = issue_s(1, i))) break;
+                if (!(ok = issue_pv(0, i))) break;
             }
-            if (ok && ntiles > 0) ok = issue_pv(ntiles - 1);
+            if (ok && ntiles > 0) {
+                ok = issue_pv(1, ntiles - 1);
+                mma_commit(&sm.empty[(ntiles - 1) % kFStages]);
+            }
             if (!ok) fail(32);
         }
     } else {
         // ------------------------------------------ softmax, rescale, epilogue
-        const int q4 = warp & 3;       // TMEM lane quarter of this warp
-        const int r = q4 * 32 + lane;  // query row of the block = TMEM lane
+        const int x = (warp - 2) / 4;   // set: A (warps 2-5) or B (6-9)
+        const int q4 = warp & 3;        // TMEM lane quarter of this warp
+        const int r = q4 * 32 + lane;   // row of the set = TMEM lane
+        const int bar_id = 1 + x;
         const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-        const int64_t pos = p0 + q0 + r;
-        float m_ref = -INFINITY, l = 0.f;
+        const uint32_t colS = 256 * x, colO = 256 * x + 128;
+        const int64_t set_lo = p0 + q0 + x * kFK;       // position of the set's first row
+        const int64_t pos = set_lo + r;
+        const float c2 = scale * kLog2e;
+        float m_ref = -INFINITY, l = 0.f;                // base-2 units
         bool alive = true;
         for (int i = 0; i < ntiles && alive; ++i) {
             if (r == 0) {
-                const bool ok = mbar_wait(&sm.s_full[i & 1], (i / 2) & 1, abort_flag);
+                const bool ok = mbar_wait(&sm.s_full[x], i & 1, abort_flag);
                 if (!ok) fail(33);
-                sm.go = ok && !*abort_flag;
+                sm.go[x] = ok && !*abort_flag;
             }
-            fbar(128);
-            if (!sm.go) {
+            fbar(bar_id, 128);
+            if (!sm.go[x]) {
                 alive = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t s_t = tmem + kColS0 + 128 * (i & 1) + lane_base;
+            const uint32_t s_t = tmem + colS + lane_base;
             uint32_t sv[128];
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) tmem_ld32(s_t + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * cb));
             tmem_wait_ld();
             const int64_t key0 = (int64_t)(j_lo + i) * kFK;
-            // keys of this tile that row r sees: [lo_c, hi_c)
-            const int64_t first = (window > 0) ? pos - window + 1 : 0;
-            const int lo_c = (int)max((int64_t)0, min((int64_t)kFK, first - key0));
-            const int hi_c = (int)max((int64_t)0, min((int64_t)kFK, pos + 1 - key0));
+            // every row of the set sees every key of this tile: no per-element mask
+            const bool full = (key0 + kFK - 1 <= set_lo) && (window <= 0 || key0 >= set_lo + kFK - 1 - window + 1);
             float mt = -INFINITY;
+            if (full) {
 #pragma unroll
-            for (int c = 0; c < kFK; ++c) {
-                const float x = (c >= lo_c && c < hi_c) ? __uint_as_float(sv[c]) * scale : -INFINITY;
-                sv[c] = __float_as_uint(x);
-                mt = fmaxf(mt, x);
+                for (int c = 0; c < kFK; ++c) {
+                    const float v = __uint_as_float(sv[c]) * c2;
+                    sv[c] = __float_as_uint(v);
+                    mt = fmaxf(mt, v);
+                }
+            } else {
+                const int64_t first = (window > 0) ? pos - window + 1 : 0;
+                const int lo_c = (int)max((int64_t)0, min((int64_t)kFK, first - key0));
+                const int hi_c = (int)max((int64_t)0, min((int64_t)kFK, pos + 1 - key0));
+#pragma unroll
+                for (int c = 0; c < kFK; ++c) {
+                    const float v = (c >= lo_c && c < hi_c) ? __uint_as_float(sv[c]) * c2 : -INFINITY;
+                    sv[c] = __float_as_uint(v);
+                    mt = fmaxf(mt, v);
+                }
             }
             // move the reference maximum only when this tile passes it by more than the gap
             float alpha = 1.f;
-            const bool move = (mt > m_ref + kRescaleGap) || (m_ref == -INFINITY && mt > -INFINITY);
+            const bool move = (mt > m_ref + kRescaleGap2) || (m_ref == -INFINITY && mt > -INFINITY);
             if (move) {
-                alpha = (m_ref == -INFINITY) ? 0.f : __expf(m_ref - mt);
+                alpha = (m_ref == -INFINITY) ? 0.f : fa_ex2(m_ref - mt);
                 m_ref = mt;
             }
+            const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;  // a row with nothing seen yet: every p is 0
             // P as packed bf16 over the first 64 columns of S (keys 2c, 2c+1 in column c; every
             // S value is already in registers), 32 keys at a time
             float ls = 0.f;
@@ -234,28 +271,27 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t pk[16];
 #pragma unroll
-                for (int c2 = 0; c2 < 16; ++c2) {
-                    const float x0 = __uint_as_float(sv[32 * cb + 2 * c2]), x1 = __uint_as_float(sv[32 * cb + 2 * c2 + 1]);
-                    const float e0 = (x0 == -INFINITY) ? 0.f : __expf(x0 - m_ref);
-                    const float e1 = (x1 == -INFINITY) ? 0.f : __expf(x1 - m_ref);
+                for (int c2i = 0; c2i < 16; ++c2i) {
+                    const float e0 = fa_ex2(__uint_as_float(sv[32 * cb + 2 * c2i]) - mu);
+                    const float e1 = fa_ex2(__uint_as_float(sv[32 * cb + 2 * c2i + 1]) - mu);
                     ls += e0 + e1;
-                    pk[c2] = fa_pack_bf16x2(e0, e1);
+                    pk[c2i] = fa_pack_bf16x2(e0, e1);
                 }
                 tmem_st16(s_t + cb * 16, pk);
             }
             l = fmaf(l, alpha, ls);
             tmem_wait_st();
-            // O holds tiles < i; a row whose reference moved rescales it before P V of tile i
+            // O_X holds tiles < i; rows whose reference moved rescale it before P V of tile i
             // (the whole warp takes part: TMEM loads and stores are warp-wide)
             if (i > 0 && __any_sync(0xffffffffu, move)) {
                 bool ok = true;
-                if (lane == 0) ok = mbar_wait(&sm.pv_done[(i - 1) & 1], ((i - 1) / 2) & 1, abort_flag);
+                if (lane == 0) ok = mbar_wait(&sm.pv_done[x], (i - 1) & 1, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) {
                     if (lane == 0) fail(34);
                 } else {
                     tc_fence_after();
-                    const uint32_t o_t = tmem + kColO + lane_base;
+                    const uint32_t o_t = tmem + colO + lane_base;
 #pragma unroll 1
                     for (int cb = 0; cb < 8; ++cb) {
                         uint32_t ov[16];
@@ -269,21 +305,22 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             }
             tc_fence_before();
-            fbar(128);  // every row's P (and rescaled O) is in TMEM
-            if (r == 0) mbar_arrive(&sm.p_ready[i & 1]);
+            fbar(bar_id, 128);  // every row's P (and rescaled O) is in TMEM
+            if (r == 0) mbar_arrive(&sm.p_ready[x]);
         }
-        // epilogue: o = O / l as bf16, staged in the Q tile (free: every S MMA is done)
+        // epilogue: o = O / l as bf16, staged in this set's Q tile (free: every S MMA is done)
         if (alive && ntiles > 0) {
             if (r == 0) {
-                const bool ok = mbar_wait(&sm.pv_done[(ntiles - 1) & 1], ((ntiles - 1) / 2) & 1, abort_flag);
+                const bool ok = mbar_wait(&sm.pv_done[x], (ntiles - 1) & 1, abort_flag);
                 if (!ok) fail(35);
-                sm.go = ok && !*abort_flag;
+                sm.go[x] = ok && !*abort_flag;
             }
-            fbar(128);
-            if (sm.go) {
+            fbar(bar_id, 128);
+            if (sm.go[x]) {
                 tc_fence_after();
+                uint8_t *stg = sQ + x * kFTile;
                 const float inv = (l > 0.f) ? 1.f / l : 0.f;
-                const uint32_t o_t = tmem + kColO + lane_base;
+                const uint32_t o_t = tmem + colO + lane_base;
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t ov[32];
@@ -291,7 +328,7 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tmem_wait_ld();
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        *reinterpret_cast<uint4 *>(sQ + fa_tile_chunk(r, cb * 4 + q)) = make_uint4(
+                        *reinterpret_cast<uint4 *>(stg + fa_tile_chunk(r, cb * 4 + q)) = make_uint4(
                             fa_pack_bf16x2(__uint_as_float(ov[8 * q]) * inv, __uint_as_float(ov[8 * q + 1]) * inv),
                             fa_pack_bf16x2(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv),
                             fa_pack_bf16x2(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv),
@@ -299,10 +336,10 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 tc_fence_before();
                 fence_proxy_async_smem();
-                fbar(128);
-                if (r == 0) {
-                    tma_store_4d(&tm_o, sQ, 0, h, q0, b);  // rows past T are not written
-                    tma_store_4d(&tm_o, sQ + kFHalf, 64, h, q0, b);
+                fbar(bar_id, 128);
+                if (r == 0 && q0 + x * kFK < T) {  // rows past T are not written
+                    tma_store_4d(&tm_o, stg, 0, h, q0 + x * kFK, b);
+                    tma_store_4d(&tm_o, stg + kFHalf, 64, h, q0 + x * kFK, b);
                     bulk_commit_group();
                     bulk_wait_all();
                 }
@@ -366,7 +403,7 @@ cudaError_t attn_fa_launch(const AttnArgs &a, int64_t window, int *err, cudaStre
     cudaError_t e = cudaFuncSetAttribute(attn_fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.B * a.Hq), (unsigned)((a.T + kFK - 1) / kFK));
+    cfg.gridDim = dim3((unsigned)(a.B * a.Hq), (unsigned)((a.T + kFRows - 1) / kFRows));
     cfg.blockDim = dim3(kFThreads);
     cfg.dynamicSmemBytes = kFSmem;
     cfg.stream = st;
