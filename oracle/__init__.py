@@ -19,6 +19,8 @@ Language Models", arXiv:2405.05254v2):
   * rmsnorm_proj    -- Section 2.2, Eq. 2 (LN = RMSNorm)
   * kv_append_bf16  -- Section 2.2 (one cache, written once, shared by layers)
   * cross_attn      -- Section 2.2, Eq. 3 (causal, grouped-query softmax)
+  * swa_attn        -- Section 3.2, Eq. 8 (sliding-window attention, window
+                       mask n - C < m <= n)
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py.
 """
@@ -56,6 +58,7 @@ def lib():
         L.oracle_round_bf16.restype = ctypes.c_uint16
         L.oracle_kv_append_bf16.argtypes = [i, i, i, i, i64, i64, _dp, _u16p]
         L.oracle_cross_attn.argtypes = [i, i, i, i, i, i64, _dp, _dp, _dp, i64, d, _dp]
+        L.oracle_swa_attn.argtypes = [i, i, i, i, i, i64, _dp, _dp, _dp, d, _dp]
         for name in ("oracle_gret_recurrent", "oracle_gret_parallel", "oracle_gret_chunkwise",
                      "oracle_rmsnorm_proj", "oracle_kv_append_bf16", "oracle_cross_attn"):
             getattr(L, name).restype = None
@@ -159,4 +162,15 @@ def cross_attn(Q, Kc, Vc, p0, scale):
     Hkv, cap = Kc.shape[1], Kc.shape[2]
     O = np.zeros((B, T, Hq, d))
     lib().oracle_cross_attn(B, T, Hq, Hkv, d, cap, _ptr(Q), _ptr(Kc), _ptr(Vc), int(p0), float(scale), _ptr(O))
+    return O
+
+
+def swa_attn(Q, K, V, window, scale):
+    """Sliding-window attention (Section 3.2, Eq. 8): the query at position n sees
+    keys n - window < m <= n.  Q [B,N,Hq,d]; K, V [B,N,Hkv,d].  Returns fp64 O."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, N, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    O = np.zeros((B, N, Hq, d))
+    lib().oracle_swa_attn(B, N, Hq, Hkv, d, int(window), _ptr(Q), _ptr(K), _ptr(V), float(scale), _ptr(O))
     return O

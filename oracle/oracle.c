@@ -344,3 +344,57 @@ void oracle_cross_attn(int B, int T, int Hq, int Hkv, int d, int64_t cap,
         }
     }
 }
+
+/*
+ * Sliding-window attention of the self-decoder (paper Section 3.2, Eq. 8):
+ *   head_i = softmax(Q K^T + B) V,  B_nm = 0 for n - C < m <= n, -inf otherwise,
+ * i.e. the query at position n sees the C most recent keys including its own.
+ * The formula prints no scale; the score is q . k times `scale` (the caller's
+ * reading, 1 / sqrt(d) by default).  Query head h reads kv head h / (Hq / Hkv).
+ * q [B, N, Hq, d], k, v [B, N, Hkv, d], o [B, N, Hq, d] (token-major, as the
+ * projections write them).
+ */
+void oracle_swa_attn(int B, int N, int Hq, int Hkv, int d, int64_t window,
+                     const double *Q, const double *K, const double *V,
+                     double scale, double *O)
+{
+    int group = Hq / Hkv;
+    #pragma omp parallel for collapse(3) schedule(dynamic)
+    for (int b = 0; b < B; ++b) {
+        for (int n = 0; n < N; ++n) {
+            for (int h = 0; h < Hq; ++h) {
+                int hk = h / group;
+                int64_t m0 = (int64_t)n - window + 1;
+                if (m0 < 0)
+                    m0 = 0;
+                const double *qv = Q + (((size_t)b * N + n) * Hq + h) * d;
+                double *ov = O + (((size_t)b * N + n) * Hq + h) * d;
+                int64_t cnt = (int64_t)n - m0 + 1;
+                double *s = (double *)malloc(sizeof(double) * (size_t)cnt);
+                double mx = -INFINITY;
+                for (int64_t m = m0; m <= n; ++m) {
+                    const double *kv = K + (((size_t)b * N + m) * Hkv + hk) * d;
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c)
+                        acc += qv[c] * kv[c];
+                    s[m - m0] = scale * acc;
+                    if (s[m - m0] > mx)
+                        mx = s[m - m0];
+                }
+                double den = 0.0;
+                for (int64_t i = 0; i < cnt; ++i) {
+                    s[i] = exp(s[i] - mx);
+                    den += s[i];
+                }
+                for (int c = 0; c < d; ++c)
+                    ov[c] = 0.0;
+                for (int64_t m = m0; m <= n; ++m) {
+                    const double *vv = V + (((size_t)b * N + m) * Hkv + hk) * d;
+                    for (int c = 0; c < d; ++c)
+                        ov[c] += (s[m - m0] / den) * vv[c];
+                }
+                free(s);
+            }
+        }
+    }
+}

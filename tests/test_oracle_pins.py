@@ -377,3 +377,69 @@ def test_attention_brute_force_pure_python():
             for c in range(d):
                 ref = sum(e[m] / z * V[0, 0, m, c] for m in range(pos + 1))
                 assert abs(O[0, t, h, c] - ref) < 1e-13
+
+
+# ---------------------------------------------- sliding-window attention pins
+
+def test_swa_window_one_returns_own_value():
+    """Window C = 1 (Section 3.2, Eq. 8: keys n - C < m <= n): each query sees
+    only its own key, so the softmax weight is 1 and o_n = v_n exactly."""
+    rng = np.random.default_rng(21)
+    B, N, Hq, Hkv, d = 2, 7, 4, 2, 5
+    Q = rng.standard_normal((B, N, Hq, d))
+    K = rng.standard_normal((B, N, Hkv, d))
+    V = rng.standard_normal((B, N, Hkv, d))
+    O = oracle.swa_attn(Q, K, V, 1, 0.4)
+    for h in range(Hq):
+        assert np.array_equal(O[:, :, h], V[:, :, h // 2])
+
+
+def test_swa_brute_force_pure_python():
+    """The window mask written out in pure Python on a tiny input: query n
+    weighs keys max(0, n - C + 1) .. n by exp(scale q.k)."""
+    rng = np.random.default_rng(22)
+    B, N, Hq, Hkv, d, C = 1, 6, 2, 1, 3, 3
+    Q = rng.standard_normal((B, N, Hq, d))
+    K = rng.standard_normal((B, N, Hkv, d))
+    V = rng.standard_normal((B, N, Hkv, d))
+    scale = 0.7
+    O = oracle.swa_attn(Q, K, V, C, scale)
+    for n in range(N):
+        keys = [m for m in range(N) if n - C < m <= n]
+        for h in range(Hq):
+            e = {m: math.exp(scale * sum(Q[0, n, h, c] * K[0, m, 0, c] for c in range(d))) for m in keys}
+            z = sum(e.values())
+            for c in range(d):
+                ref = sum(e[m] / z * V[0, m, 0, c] for m in keys)
+                assert abs(O[0, n, h, c] - ref) < 1e-13
+
+
+def test_swa_wide_window_is_causal_attention():
+    """A window at least as long as the sequence masks nothing but the future:
+    the result equals the causal attention oracle over the same keys laid out
+    as a cache (an independent implementation of Eq. 3)."""
+    rng = np.random.default_rng(23)
+    B, N, Hq, Hkv, d = 2, 9, 6, 3, 4
+    Q = rng.standard_normal((B, N, Hq, d))
+    K = rng.standard_normal((B, N, Hkv, d))
+    V = rng.standard_normal((B, N, Hkv, d))
+    O = oracle.swa_attn(Q, K, V, N + 5, 0.3)
+    O_ref = oracle.cross_attn(Q, K.transpose(0, 2, 1, 3), V.transpose(0, 2, 1, 3), 0, 0.3)
+    np.testing.assert_allclose(O, O_ref, rtol=1e-13, atol=1e-14)
+
+
+def test_swa_keys_outside_the_window_change_nothing():
+    """Keys older than C positions cannot reach a query: changing them leaves
+    its output bit-identical, while changing an in-window key does not."""
+    rng = np.random.default_rng(24)
+    B, N, Hq, Hkv, d, C = 1, 10, 2, 2, 4, 4
+    Q = rng.standard_normal((B, N, Hq, d))
+    K = rng.standard_normal((B, N, Hkv, d))
+    V = rng.standard_normal((B, N, Hkv, d))
+    O = oracle.swa_attn(Q, K, V, C, 0.5)
+    K2, V2 = K.copy(), V.copy()
+    K2[:, :5] = 50.0
+    V2[:, :5] = -3.0
+    O2 = oracle.swa_attn(Q, K2, V2, C, 0.5)
+    assert np.array_equal(O[:, 8:], O2[:, 8:])   # rows 8, 9 see keys 5..9 only
+    assert not np.allclose(O[:, 7], O2[:, 7])    # row 7 sees key 4
