@@ -36,6 +36,11 @@ class _KVCacheC(ctypes.Structure):
                 ("d", ctypes.c_int32), ("capacity", ctypes.c_int64), ("dtype", ctypes.c_int)]
 
 
+class _SwaRingC(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("d", ctypes.c_int32), ("window", ctypes.c_int32), ("pos", ctypes.c_int64), ("dtype", ctypes.c_int)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libyoco.so not found at {LIB_PATH}; build it with "
@@ -43,6 +48,7 @@ def _load():
     L = ctypes.CDLL(LIB_PATH)
     vp, i, f, sz, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_int64
     cp = ctypes.POINTER(_KVCacheC)
+    rp = ctypes.POINTER(_SwaRingC)
     sigs = {
         "yoco_gret_prefill_chunkwise": (i, [vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, i, i, i, vp, sz, vp]),
         "yoco_gret_prefill_workspace_size": (sz, [i, i, i, i, i, i, i]),
@@ -59,6 +65,9 @@ def _load():
         "yoco_launch_count": (ctypes.c_uint64, []),
         "yoco_workspace_status": (i, [vp, i, vp]),
         "yoco_selftest_wait_timeout": (i, [vp, ctypes.c_uint64, vp]),
+        "yoco_swa_prefill": (i, [vp, vp, vp, i, i, f, vp, rp, vp, sz, vp]),
+        "yoco_swa_decode": (i, [vp, vp, vp, i, f, vp, rp, vp, sz, vp]),
+        "yoco_swa_workspace_size": (sz, [i, i, rp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -72,7 +81,8 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_shared_kv_project_append", "yoco_shared_kv_workspace_size", "yoco_cross_attn_prefill",
             "yoco_cross_attn_decode", "yoco_cross_attn_workspace_size", "yoco_status_string",
             "yoco_last_error", "yoco_version", "yoco_launch_count",
-            "yoco_workspace_status", "yoco_cross_attn_decode_noalloc", "yoco_selftest_wait_timeout")
+            "yoco_workspace_status", "yoco_cross_attn_decode_noalloc", "yoco_selftest_wait_timeout",
+            "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size")
 
 
 def _check(status: int, where: str):
@@ -233,3 +243,44 @@ def yoco_cross_attn_decode(Q, cache: KVCache, O, scale=None, num_splits=0, works
     st = lib.yoco_cross_attn_decode(_ptr(Q), Hq, ctypes.byref(cache.c), float(scale), num_splits, _ptr(O), _ptr(ws),
                                     0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "yoco_cross_attn_decode")
+
+
+# ----------------------------------------------- sliding-window self-decoder
+
+class SwaRing:
+    """Caller-side ring cache of one sliding-window layer: k, v [B, Hkv, window, d]
+    (token at position p in slot p % window) and the C descriptor; `pos` counts
+    the tokens seen."""
+
+    def __init__(self, B, Hkv, d, window, dtype=torch.bfloat16, device="cuda"):
+        self.k = torch.zeros(B, Hkv, window, d, dtype=dtype, device=device)
+        self.v = torch.zeros(B, Hkv, window, d, dtype=dtype, device=device)
+        self.c = _SwaRingC(self.k.data_ptr(), self.v.data_ptr(), B, Hkv, d, window, 0, _dt(self.k))
+
+    @property
+    def pos(self) -> int:
+        return int(self.c.pos)
+
+
+def yoco_swa_prefill(q, k, v, ring: SwaRing, o, scale=None, workspace=None, stream=None):
+    """q, o [B, N, Hq, d]; k, v [B, N, Hkv, d]; starts the sequence held in `ring`."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _need(t, n)
+    B, N, Hq, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    ws = _workspace(max(256, lib.yoco_swa_workspace_size(B, Hq, ctypes.byref(ring.c))), q.device, workspace)
+    st = lib.yoco_swa_prefill(_ptr(q), _ptr(k), _ptr(v), Hq, N, float(scale), _ptr(o), ctypes.byref(ring.c),
+                              _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "yoco_swa_prefill")
+
+
+def yoco_swa_decode(q, k, v, ring: SwaRing, o, scale=None, workspace=None, stream=None):
+    """q, o [B, Hq, d]; k, v [B, Hkv, d] of the new token."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _need(t, n)
+    B, Hq, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    ws = _workspace(max(256, lib.yoco_swa_workspace_size(B, Hq, ctypes.byref(ring.c))), q.device, workspace)
+    st = lib.yoco_swa_decode(_ptr(q), _ptr(k), _ptr(v), Hq, float(scale), _ptr(o), ctypes.byref(ring.c), _ptr(ws),
+                             ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "yoco_swa_decode")

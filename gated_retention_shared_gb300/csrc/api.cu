@@ -247,4 +247,80 @@ yoco_status yoco_cross_attn_decode(const void *Q, int Hq, const yoco_kv_cache *c
     return attn_common(Q, Hq, 1, cache->len_host - 1, cache, scale, num_splits, O, workspace, ws_bytes, stream);
 }
 
+// ------------------------------------------------ sliding-window self-decoder
+
+static yoco_status check_ring(const yoco_swa_ring *r, int Hq) {
+    if (!r) return fail(YOCO_ERR_INVALID_ARG, "ring is NULL");
+    if (!r->k || !r->v) return fail(YOCO_ERR_INVALID_ARG, "ring k and v must be set");
+    if (!valid_dt(r->dtype)) return fail(YOCO_ERR_INVALID_ARG, "ring dtype invalid");
+    if (r->B <= 0 || r->Hkv <= 0 || r->window <= 0) return fail(YOCO_ERR_INVALID_ARG, "ring B, Hkv and window must be positive");
+    if (r->d != 64 && r->d != 128) return fail(YOCO_ERR_UNSUPPORTED, "ring head size %d not in {64, 128}", r->d);
+    if (r->pos < 0) return fail(YOCO_ERR_INVALID_ARG, "ring position must be >= 0");
+    if (!aligned(r->k, 16) || !aligned(r->v, 16)) return fail(YOCO_ERR_INVALID_ARG, "ring k/v must be 16-byte aligned");
+    if (Hq <= 0 || Hq % r->Hkv != 0) return fail(YOCO_ERR_UNSUPPORTED, "Hq must be a positive multiple of Hkv");
+    if (Hq / r->Hkv > 16) return fail(YOCO_ERR_UNSUPPORTED, "at most 16 query heads per kv head");
+    return YOCO_OK;
+}
+
+size_t yoco_swa_workspace_size(int B, int Hq, const yoco_swa_ring *ring) {
+    if (!ring || B <= 0 || Hq <= 0 || ring->Hkv <= 0 || ring->window <= 0) return 0;
+    const int splits = attn_auto_splits(B, ring->Hkv, ring->window, attn_ctas_per_sm(ring->dtype, ring->d, Hq / ring->Hkv));
+    return attn_workspace(B, Hq, 1, ring->d, splits);
+}
+
+yoco_status yoco_swa_prefill(const void *q, const void *k, const void *v, int Hq, int N, float scale, void *o,
+                             yoco_swa_ring *ring, void *workspace, size_t ws_bytes, void *stream) {
+    yoco_status s = check_ring(ring, Hq);
+    if (s != YOCO_OK) return s;
+    if (!q || !k || !v || !o) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (N < 0) return fail(YOCO_ERR_INVALID_ARG, "N must be >= 0");
+    if (ring->pos != 0) return fail(YOCO_ERR_INVALID_ARG, "prefill starts a sequence: ring position must be 0");
+    if (ring->dtype != YOCO_BF16 || ring->d != 128)
+        return fail(YOCO_ERR_UNSUPPORTED, "sliding-window prefill runs in bf16 with head size 128");
+    if (!isfinite(scale)) return fail(YOCO_ERR_INVALID_ARG, "scale must be finite");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+        return fail(YOCO_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned");
+    if ((int64_t)ring->B * Hq > 0x7fffffff || N > (1 << 30)) return fail(YOCO_ERR_UNSUPPORTED, "size out of range");
+    if ((s = check_ws(workspace, ws_bytes, 256)) != YOCO_OK) return s;
+    if (N == 0) return YOCO_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = swa_fa_launch(q, k, v, o, ring->B, N, Hq, ring->Hkv, ring->window, scale, (int *)workspace, st);
+    if (e == cudaSuccess) {
+        // the ring keeps the last `window` tokens for decoding
+        const int n = N < ring->window ? N : ring->window;
+        e = swa_ring_write(k, v, ring->k, ring->v, ring->B, N, ring->Hkv, ring->d, ring->window, N - n, n, N - n,
+                           ring->dtype, st);
+    }
+    if (e != cudaSuccess) return cuda_status(e, "swa_prefill");
+    ring->pos = N;
+    return YOCO_OK;
+}
+
+yoco_status yoco_swa_decode(const void *q, const void *k, const void *v, int Hq, float scale, void *o,
+                            yoco_swa_ring *ring, void *workspace, size_t ws_bytes, void *stream) {
+    yoco_status s = check_ring(ring, Hq);
+    if (s != YOCO_OK) return s;
+    if (!q || !k || !v || !o) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (!isfinite(scale)) return fail(YOCO_ERR_INVALID_ARG, "scale must be finite");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+        return fail(YOCO_ERR_INVALID_ARG, "q, k, v, o must be 16-byte aligned");
+    // keys in the ring after this token: positions max(0, pos - window + 1) .. pos
+    const int64_t keys = ring->pos + 1 < ring->window ? ring->pos + 1 : ring->window;
+    const int splits =
+        attn_auto_splits(ring->B, ring->Hkv, keys, attn_ctas_per_sm(ring->dtype, ring->d, Hq / ring->Hkv));
+    if ((s = check_ws(workspace, ws_bytes, attn_workspace(ring->B, Hq, 1, ring->d, splits))) != YOCO_OK) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = swa_ring_write(k, v, ring->k, ring->v, ring->B, 1, ring->Hkv, ring->d, ring->window, 0, 1,
+                                   ring->pos, ring->dtype, st);
+    if (e == cudaSuccess) {
+        // the filled slots, in whatever order the ring holds them: every one is in the window
+        AttnArgs a{q, o, ring->k, ring->v, ring->B, 1, Hq, ring->Hkv, ring->d, ring->window, keys - 1, scale,
+                   ring->dtype};
+        e = attn_run(a, splits, workspace, st);
+    }
+    if (e != cudaSuccess) return cuda_status(e, "swa_decode");
+    ring->pos += 1;
+    return YOCO_OK;
+}
+
 }  // extern "C"

@@ -77,7 +77,7 @@ __device__ __forceinline__ float fa_ex2(float x) {  // 2^x, hardware approximati
 __global__ void __launch_bounds__(kFThreads, 1)
 attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, int T, int Hq,
-               int Hkv, int64_t p0, float scale, int64_t window, int *err) {
+               int Hkv, int64_t p0, float scale, int64_t window, int kv_token_major, int *err) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
@@ -90,7 +90,7 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int qb = (int)gridDim.y - 1 - (int)blockIdx.y;  // longest rows first
     const int q0 = qb * kFRows;
     const int G = Hq / Hkv;
-    const int bz = b * Hkv + h / G;  // (sequence, kv head) index of the cache view
+    const int hk = h / G;            // kv head
     const int64_t pos_lo = p0 + q0;
     const int64_t pos_hi = p0 + min(q0 + kFRows, T) - 1;
     const int64_t key_lo = (window > 0) ? max((int64_t)0, pos_lo - window + 1) : 0;
@@ -148,9 +148,11 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const int key0 = (j_lo + i) * kFK;
                 uint8_t *st = ring + (size_t)s * 2 * kFTile;
                 mbar_arrive_expect_tx(&sm.full[s], 2 * kFTile);
+                // K/V as {d, key, kv head, b} (a cache) or {d, kv head, key, b} (token-major)
+                const int c1 = kv_token_major ? hk : key0, c2 = kv_token_major ? key0 : hk;
                 for (int half = 0; half < 2; ++half) {
-                    tma_load_3d(st + half * kFHalf, &tm_k, &sm.full[s], half * 64, key0, bz);
-                    tma_load_3d(st + kFTile + half * kFHalf, &tm_v, &sm.full[s], half * 64, key0, bz);
+                    tma_load_4d(st + half * kFHalf, &tm_k, &sm.full[s], half * 64, c1, c2, b);
+                    tma_load_4d(st + kFTile + half * kFHalf, &tm_v, &sm.full[s], half * 64, c1, c2, b);
                 }
             }
             // leave no copy in flight
@@ -386,24 +388,13 @@ bool attn_fa_eligible(const AttnArgs &a) {
            a.B <= 65535 && (int64_t)a.B * a.Hq <= 0x7fffffff;
 }
 
-cudaError_t attn_fa_launch(const AttnArgs &a, int64_t window, int *err, cudaStream_t st) {
-    const int64_t keys = a.p0 + a.T;
-    CUtensorMap mq, mk, mv, mo;
-    // Q, O: [B, T, Hq, d] as {d, Hq, T, B}, box {64, 1, 128, 1}
-    const cuuint64_t qd[4] = {(cuuint64_t)kFD, (cuuint64_t)a.Hq, (cuuint64_t)a.T, (cuuint64_t)a.B};
-    const cuuint64_t qs[3] = {(cuuint64_t)kFD * 2, (cuuint64_t)a.Hq * kFD * 2, (cuuint64_t)a.T * a.Hq * kFD * 2};
-    const cuuint32_t qbox[4] = {64, 1, (cuuint32_t)kFK, 1};
-    // K, V: [B * Hkv, cap, d] viewed with `keys` rows, box {64, 128, 1}
-    const cuuint64_t kd[3] = {(cuuint64_t)kFD, (cuuint64_t)keys, (cuuint64_t)a.B * a.Hkv};
-    const cuuint64_t ks[2] = {(cuuint64_t)kFD * 2, (cuuint64_t)a.cap * kFD * 2};
-    const cuuint32_t kbox[3] = {64, (cuuint32_t)kFK, 1};
-    if (!fa_map(&mq, 4, a.Q, qd, qs, qbox) || !fa_map(&mo, 4, a.O, qd, qs, qbox) || !fa_map(&mk, 3, a.kc, kd, ks, kbox) ||
-        !fa_map(&mv, 3, a.vc, kd, ks, kbox))
-        return cudaErrorInvalidValue;
+static cudaError_t fa_run(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
+                          int B, int T, int Hq, int Hkv, int64_t p0, float scale, int64_t window, int kv_token_major,
+                          int *err, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(attn_fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(a.B * a.Hq), (unsigned)((a.T + kFRows - 1) / kFRows));
+    cfg.gridDim = dim3((unsigned)(B * Hq), (unsigned)((T + kFRows - 1) / kFRows));
     cfg.blockDim = dim3(kFThreads);
     cfg.dynamicSmemBytes = kFSmem;
     cfg.stream = st;
@@ -413,7 +404,37 @@ cudaError_t attn_fa_launch(const AttnArgs &a, int64_t window, int *err, cudaStre
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     count_launches(1);
-    return cudaLaunchKernelEx(&cfg, attn_fa_kernel, mq, mk, mv, mo, a.T, a.Hq, a.Hkv, a.p0, a.scale, window, err);
+    return cudaLaunchKernelEx(&cfg, attn_fa_kernel, mq, mk, mv, mo, T, Hq, Hkv, p0, scale, window, kv_token_major, err);
+}
+
+// [B, rows, H, 128] token-major bf16 as {d, H, rows, B}, box {64, 1, 128, 1}
+static bool fa_token_major_map(CUtensorMap *m, const void *ptr, int B, int64_t rows, int H) {
+    const cuuint64_t dims[4] = {(cuuint64_t)kFD, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)kFD * 2, (cuuint64_t)H * kFD * 2, (cuuint64_t)rows * H * kFD * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kFK, 1};
+    return fa_map(m, 4, ptr, dims, strides, box);
+}
+
+cudaError_t attn_fa_launch(const AttnArgs &a, int64_t window, int *err, cudaStream_t st) {
+    const int64_t keys = a.p0 + a.T;
+    CUtensorMap mq, mk, mv, mo;
+    // K, V: cache [B, Hkv, cap, d] viewed with `keys` rows as {d, key, kv head, b}, box {64, 128, 1, 1}
+    const cuuint64_t kd[4] = {(cuuint64_t)kFD, (cuuint64_t)keys, (cuuint64_t)a.Hkv, (cuuint64_t)a.B};
+    const cuuint64_t ks[3] = {(cuuint64_t)kFD * 2, (cuuint64_t)a.cap * kFD * 2, (cuuint64_t)a.Hkv * a.cap * kFD * 2};
+    const cuuint32_t kbox[4] = {64, (cuuint32_t)kFK, 1, 1};
+    if (!fa_token_major_map(&mq, a.Q, a.B, a.T, a.Hq) || !fa_token_major_map(&mo, a.O, a.B, a.T, a.Hq) ||
+        !fa_map(&mk, 4, a.kc, kd, ks, kbox) || !fa_map(&mv, 4, a.vc, kd, ks, kbox))
+        return cudaErrorInvalidValue;
+    return fa_run(mq, mk, mv, mo, a.B, a.T, a.Hq, a.Hkv, a.p0, a.scale, window, 0, err, st);
+}
+
+cudaError_t swa_fa_launch(const void *q, const void *k, const void *v, void *o, int B, int N, int Hq, int Hkv,
+                          int64_t window, float scale, int *err, cudaStream_t st) {
+    CUtensorMap mq, mk, mv, mo;
+    if (!fa_token_major_map(&mq, q, B, N, Hq) || !fa_token_major_map(&mo, o, B, N, Hq) ||
+        !fa_token_major_map(&mk, k, B, N, Hkv) || !fa_token_major_map(&mv, v, B, N, Hkv))
+        return cudaErrorInvalidValue;
+    return fa_run(mq, mk, mv, mo, B, N, Hq, Hkv, 0, scale, window, 1, err, st);
 }
 
 }  // namespace yoco_host

@@ -72,6 +72,12 @@ cudaError_t attn_tc_launch(const AttnArgs &a, int RB, int nq, int64_t kps, int s
 // attn_fa.cu: many query rows (prefill), bf16, d = 128; window > 0 adds the sliding-window mask
 bool attn_fa_eligible(const AttnArgs &a);
 cudaError_t attn_fa_launch(const AttnArgs &a, int64_t window, int *err, cudaStream_t st);
+// sliding-window self-attention over token-major q [B,N,Hq,128], k, v [B,N,Hkv,128] (bf16)
+cudaError_t swa_fa_launch(const void *q, const void *k, const void *v, void *o, int B, int N, int Hq, int Hkv,
+                          int64_t window, float scale, int *err, cudaStream_t st);
+// swa.cu: copy tokens [tok0, tok0 + n) of k, v [B, N, Hkv, d] to ring slots (pos0 + i) % window
+cudaError_t swa_ring_write(const void *k, const void *v, void *rk, void *rv, int B, int N, int Hkv, int d,
+                           int window, int64_t tok0, int n, int64_t pos0, yoco_dtype dt, cudaStream_t st);
 
 // selftest.cu
 cudaError_t selftest_wait(void *ws, uint64_t limit_ns, cudaStream_t st);

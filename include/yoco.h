@@ -204,6 +204,50 @@ YOCO_API yoco_status yoco_cross_attn_decode_noalloc(const void *Q, int Hq, const
 YOCO_API size_t yoco_cross_attn_workspace_size(int B, int Hq, int T, const yoco_kv_cache *cache,
                                       int num_splits);
 
+/* ------------------------------------------- sliding-window self-decoder */
+
+/*
+ * The pages' second self-decoder choice (paper Section 3.2, Eq. 8): each query
+ * attends to the C most recent keys of its own layer, itself included,
+ *     head = softmax(scale * Q K^T + B) V,  B_nm = 0 for n - C < m <= n, else -inf,
+ * so the layer's cache is a ring of C tokens whatever the sequence length.
+ * (Eq. 8 prints no scale; `scale` is the caller's, 1 / sqrt(d) in practice.)
+ *
+ * Ring cache, caller-owned: token at position p lives in slot p % window of
+ *   k, v [B, Hkv, window, d] (dtype).  `pos` is the number of tokens seen, i.e.
+ *   the next token's position; prefill and decode advance it on the host.
+ */
+typedef struct {
+    void *k, *v;
+    int B, Hkv, d;
+    int window;   /* C */
+    int64_t pos;  /* tokens seen */
+    yoco_dtype dtype;
+} yoco_swa_ring;
+
+/*
+ * Prefill of a new sequence (ring->pos must be 0): q [B, N, Hq, d], k, v
+ * [B, N, Hkv, d] token-major as the projections write them; o [B, N, Hq, d].
+ * Writes the last min(N, window) tokens' k, v into the ring and sets
+ * ring->pos = N.  bf16 with d = 128 (tensor cores), else YOCO_ERR_UNSUPPORTED.
+ * workspace: >= 256 bytes, 256-byte aligned (status word).
+ */
+YOCO_API yoco_status yoco_swa_prefill(const void *q, const void *k, const void *v, int Hq, int N, float scale,
+                                      void *o, yoco_swa_ring *ring, void *workspace, size_t ws_bytes,
+                                      void *stream);
+
+/*
+ * One generated token: q [B, Hq, d], k, v [B, Hkv, d] (the token's own), o
+ * [B, Hq, d].  Writes k, v into slot ring->pos % window, attends over the
+ * min(ring->pos + 1, window) filled slots, then increments ring->pos.
+ * bf16 or f32, d in {64, 128}.  workspace: >= yoco_swa_workspace_size bytes.
+ */
+YOCO_API yoco_status yoco_swa_decode(const void *q, const void *k, const void *v, int Hq, float scale, void *o,
+                                     yoco_swa_ring *ring, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes for yoco_swa_decode (also enough for yoco_swa_prefill). */
+YOCO_API size_t yoco_swa_workspace_size(int B, int Hq, const yoco_swa_ring *ring);
+
 /* ------------------------------------------------------------ utilities */
 
 YOCO_API const char *yoco_status_string(yoco_status s);

@@ -150,3 +150,32 @@ def test_selftest_rejects_bad_arguments(Y):
     assert L.yoco_selftest_wait_timeout(None, 1000, None) == Y.YOCO_ERR_WORKSPACE
     assert L.yoco_selftest_wait_timeout(FAKE, 0, None) == Y.YOCO_ERR_INVALID_ARG
     assert L.yoco_selftest_wait_timeout(FAKE, 20_000_000_000, None) == Y.YOCO_ERR_INVALID_ARG
+
+
+def _ring(Y, window=64, d=128, Hkv=2, B=1, dtype=1, pos=0):
+    return Y._SwaRingC(0x2000, 0x3000, B, Hkv, d, window, pos, dtype)
+
+
+def test_swa_validation(Y):
+    L = Y.lib
+    r = _ring(Y, pos=5)
+    assert L.yoco_swa_prefill(FAKE, FAKE, FAKE, 4, 10, 0.1, FAKE, ctypes.byref(r), FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_INVALID_ARG  # prefill starts a sequence
+    assert b"position" in L.yoco_last_error()
+    r = _ring(Y, dtype=0)
+    assert L.yoco_swa_prefill(FAKE, FAKE, FAKE, 4, 10, 0.1, FAKE, ctypes.byref(r), FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_UNSUPPORTED  # fp32 prefill
+    r = _ring(Y, d=96)
+    assert L.yoco_swa_decode(FAKE, FAKE, FAKE, 4, 0.1, FAKE, ctypes.byref(r), FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_UNSUPPORTED
+    r = _ring(Y)
+    assert L.yoco_swa_decode(FAKE, FAKE, FAKE, 3, 0.1, FAKE, ctypes.byref(r), FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_UNSUPPORTED  # Hq not a multiple of Hkv
+    assert L.yoco_swa_decode(FAKE, FAKE, FAKE, 4, 0.1, FAKE, ctypes.byref(r), None, 0, None) == \
+        Y.YOCO_ERR_WORKSPACE
+    r = _ring(Y, window=0)
+    assert L.yoco_swa_prefill(FAKE, FAKE, FAKE, 4, 10, 0.1, FAKE, ctypes.byref(r), FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_INVALID_ARG
+    r = _ring(Y)
+    assert L.yoco_swa_workspace_size(1, 4, ctypes.byref(r)) >= 256
+    assert r.pos == 0  # failed calls do not move the ring

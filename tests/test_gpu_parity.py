@@ -505,6 +505,80 @@ def test_device_generator_matches_host(Y):
     assert np.max(np.abs(f.cpu().numpy() - synth.normal(SEED, 99, (5000,), "f32", mean=2.0))) <= 1e-6
 
 
+# ------------------------------------------------ sliding-window self-decoder
+
+def swa_inputs(cfg, B, N, Hq, Hkv, d):
+    q, qd = gen(SEED, sid(cfg, 0, synth.T_Q), (B, N, Hq, d), "bf16")
+    k, kd = gen(SEED, sid(cfg, 0, synth.T_K), (B, N, Hkv, d), "bf16")
+    v, vd = gen(SEED, sid(cfg, 0, synth.T_V), (B, N, Hkv, d), "bf16")
+    return (q, k, v), (qd, kd, vd)
+
+
+@pytest.mark.parametrize("B,N,Hq,Hkv,window", [(1, 3000, 8, 8, 1024), (2, 777, 24, 8, 200), (1, 500, 4, 2, 4096),
+                                                (1, 130, 6, 3, 1)])
+def test_swa_prefill(Y, B, N, Hq, Hkv, window):
+    """Sliding-window prefill against the window-mask oracle: multi-head and
+    grouped heads, windows shorter than the sequence (a multiple of the key
+    tile and not), longer than it, and a window of one key."""
+    import torch
+    d = 128
+    (q, k, v), (qd, kd, vd) = swa_inputs(40, B, N, Hq, Hkv, d)
+    ring = Y.SwaRing(B, Hkv, d, window)
+    o = torch.empty_like(qd)
+    Y.yoco_swa_prefill(qd, kd, vd, ring, o)
+    torch.cuda.synchronize()
+    o_ref = oracle.swa_attn(q, k, v, window, d ** -0.5)
+    assert rel_l2(host_f64(o), o_ref) <= BF16_REL_L2
+    assert ring.pos == N
+    # the ring holds the last min(N, window) tokens at slot position % window
+    for p in range(max(0, N - window), N, max(1, min(N, window) // 7)):
+        assert np.array_equal(host_bits(ring.k[:, :, p % window]), host_bits(kd[:, p]))
+        assert np.array_equal(host_bits(ring.v[:, :, p % window]), host_bits(vd[:, p]))
+
+
+@pytest.mark.parametrize("window", [256, 100])
+def test_swa_decode_continues_prefill(Y, window):
+    """Prefill 300 tokens, then 40 decode steps through the ring (window 100
+    wraps it several times): every generated token's output equals the oracle
+    over the whole sequence with the window mask."""
+    import torch
+    B, Hq, Hkv, d, N0, steps = 2, 6, 2, 128, 300, 40
+    N = N0 + steps
+    (q, k, v), (qd, kd, vd) = swa_inputs(41, B, N, Hq, Hkv, d)
+    ring = Y.SwaRing(B, Hkv, d, window)
+    o = torch.empty_like(qd)
+    Y.yoco_swa_prefill(qd[:, :N0].contiguous(), kd[:, :N0].contiguous(), vd[:, :N0].contiguous(), ring,
+                       o[:, :N0].contiguous())
+    outs = []
+    for t in range(N0, N):
+        ot = torch.empty(B, Hq, d, dtype=qd.dtype, device="cuda")
+        Y.yoco_swa_decode(qd[:, t].contiguous(), kd[:, t].contiguous(), vd[:, t].contiguous(), ring, ot)
+        outs.append(ot)
+    torch.cuda.synchronize()
+    assert ring.pos == N
+    o_ref = oracle.swa_attn(q, k, v, window, d ** -0.5)
+    got = np.stack([host_f64(x) for x in outs], axis=1)
+    assert rel_l2(got, o_ref[:, N0:]) <= BF16_REL_L2
+
+
+def test_swa_decode_fp32_from_empty_ring(Y):
+    """fp32, head size 64: decode from the first token on (no prefill)."""
+    import torch
+    B, Hq, Hkv, d, N, window = 1, 4, 4, 64, 50, 16
+    q, qd = gen(SEED, sid(42, 0, synth.T_Q), (B, N, Hq, d), "f32")
+    k, kd = gen(SEED, sid(42, 0, synth.T_K), (B, N, Hkv, d), "f32")
+    v, vd = gen(SEED, sid(42, 0, synth.T_V), (B, N, Hkv, d), "f32")
+    ring = Y.SwaRing(B, Hkv, d, window, dtype=torch.float32)
+    outs = []
+    for t in range(N):
+        ot = torch.empty(B, Hq, d, device="cuda")
+        Y.yoco_swa_decode(qd[:, t].contiguous(), kd[:, t].contiguous(), vd[:, t].contiguous(), ring, ot)
+        outs.append(ot)
+    torch.cuda.synchronize()
+    got = np.stack([host_f64(x) for x in outs], axis=1)
+    assert max_abs(got, oracle.swa_attn(q, k, v, window, d ** -0.5)) <= FP32_MAX_ABS
+
+
 # ------------------------------------------------------------- CUDA graphs
 
 def test_gret_decode_steps_replayed_from_a_cuda_graph(Y):
