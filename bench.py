@@ -47,7 +47,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk", type=int, default=0)
-    p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode", "cross_prefill"], default=None,
+    p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode", "cross_prefill", "swa_prefill",
+                                      "swa_decode"], default=None,
                    help="time one call of the step on its bench shape (for profiling)")
     p.add_argument("--cache-len", type=int, default=0,
                    help="--only cross_decode: cache length (default: the step's prompt length)")
@@ -546,6 +547,33 @@ def run_only(args):
         def call():
             return L.yoco_cross_attn_prefill(P(Qp), HQ, Tq, 0, ctypes.byref(cache.c), D ** -0.5, P(Op), P(ws),
                                              ws.numel(), stp)
+    elif args.only in ("swa_prefill", "swa_decode"):
+        # a sliding-window self-decoder layer of the 3B shape: 24 heads x 128, window 1024
+        Ns = args.cache_len or N
+        W = 1024
+        qs = normal((B, Ns, H, D), bf, sid(CFG, 0, synth.T_Q))
+        ks = normal((B, Ns, H, D), bf, sid(CFG, 0, synth.T_K))
+        vs = normal((B, Ns, H, D), bf, sid(CFG, 0, synth.T_V))
+        os_ = torch.empty_like(qs)
+        ring = Y.SwaRing(B, H, D, W, device=dev)
+        ws = torch.empty(max(256, L.yoco_swa_workspace_size(B, H, ctypes.byref(ring.c))), dtype=torch.uint8,
+                         device=dev)
+        q1s, k1s, v1s = qs[:, 0].contiguous(), ks[:, 0].contiguous(), vs[:, 0].contiguous()
+        o1s = torch.empty_like(q1s)
+
+        if args.only == "swa_prefill":
+            def call():
+                ring.c.pos = 0
+                return L.yoco_swa_prefill(P(qs), P(ks), P(vs), H, Ns, D ** -0.5, P(os_), ctypes.byref(ring.c), P(ws),
+                                          ws.numel(), stp)
+        else:
+            ring.c.pos = 0
+            assert L.yoco_swa_prefill(P(qs), P(ks), P(vs), H, Ns, D ** -0.5, P(os_), ctypes.byref(ring.c), P(ws),
+                                      ws.numel(), stp) == 0
+
+            def call():
+                return L.yoco_swa_decode(P(q1s), P(k1s), P(v1s), H, D ** -0.5, P(o1s), ctypes.byref(ring.c), P(ws),
+                                         ws.numel(), stp)
     elif args.only == "proj":
         M = normal((B, N, DM), bf, sid(CFG, 0, synth.T_M))
         Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
@@ -585,6 +613,15 @@ def run_only(args):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     line = {"only": args.only, "ms_per_call": ms, "steps": args.steps}
+    if args.only == "swa_prefill":
+        # row n sees min(n + 1, 1024) keys; QK^T and PV cost 2 d flops per (row, key, head) each
+        seen = sum(min(n + 1, 1024) for n in range(Ns))
+        flops = 4.0 * D * H * B * seen
+        line.update({"rows": Ns, "window": 1024, "flops_per_call": flops,
+                     "achieved_tflops": round(flops / (ms / 1e3) / 1e12, 1)})
+    if args.only == "swa_decode":
+        nbytes = 2 * B * H * 1024 * D * 2  # the full ring read once (after the prefill it is full)
+        line.update({"window": 1024, "bytes_per_call": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1)})
     if args.only == "cross_prefill":
         # causal: row t reads t + 1 keys; QK^T and PV cost 2 d flops per (row, key, head) each
         flops = 4.0 * D * HQ * B * Tq * (Tq + 1) / 2
