@@ -21,6 +21,7 @@ Language Models", arXiv:2405.05254v2):
   * cross_attn      -- Section 2.2, Eq. 3 (causal, grouped-query softmax)
   * swa_attn        -- Section 3.2, Eq. 8 (sliding-window attention, window
                        mask n - C < m <= n)
+  * group_norm_gate -- Section 3.1, Eq. 7 (GroupNorm per head, swish gate)
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py.
 """
@@ -59,6 +60,7 @@ def lib():
         L.oracle_kv_append_bf16.argtypes = [i, i, i, i, i64, i64, _dp, _u16p]
         L.oracle_cross_attn.argtypes = [i, i, i, i, i, i64, _dp, _dp, _dp, i64, d, _dp]
         L.oracle_swa_attn.argtypes = [i, i, i, i, i, i64, _dp, _dp, _dp, d, _dp]
+        L.oracle_group_norm_gate.argtypes = [i, i, i, i, _dp, _dp, _dp, _dp, d, _dp]
         for name in ("oracle_gret_recurrent", "oracle_gret_parallel", "oracle_gret_chunkwise",
                      "oracle_rmsnorm_proj", "oracle_kv_append_bf16", "oracle_cross_attn"):
             getattr(L, name).restype = None
@@ -174,3 +176,16 @@ def swa_attn(Q, K, V, window, scale):
     O = np.zeros((B, N, Hq, d))
     lib().oracle_swa_attn(B, N, Hq, Hkv, d, int(window), _ptr(Q), _ptr(K), _ptr(V), float(scale), _ptr(O))
     return O
+
+
+def group_norm_gate(o, gpre, eps, w=None, b=None):
+    """Eq. 7: swish(gpre) * GroupNorm_h(o) with one group per head.  o, gpre
+    [B,N,H,d]; w, b [H*d] or None (1 and 0).  Returns fp64 z."""
+    o, gpre = _f64(o), _f64(gpre)
+    B, N, H, d = o.shape
+    z = np.zeros_like(o)
+    wp = None if w is None else _f64(np.asarray(w, dtype=np.float64).reshape(H * d))
+    bp = None if b is None else _f64(np.asarray(b, dtype=np.float64).reshape(H * d))
+    lib().oracle_group_norm_gate(B, N, H, d, _ptr(o), _ptr(gpre), None if wp is None else _ptr(wp),
+                                 None if bp is None else _ptr(bp), float(eps), _ptr(z))
+    return z

@@ -398,3 +398,43 @@ void oracle_swa_attn(int B, int N, int Hq, int Hkv, int d, int64_t window,
         }
     }
 }
+
+/*
+ * Output of multi-head gated retention (paper Section 3.1, Eq. 7):
+ *   Y = GroupNorm_h(Concat(head_1..head_H)),  out = swish(X W_G) (.) Y
+ * GroupNorm with one group per head: each token's head vector is centred and
+ * divided by sqrt(variance + eps) (variance over the head's d channels, divided
+ * by d), then scaled and shifted per channel by w, b (w = 1, b = 0 when absent).
+ * swish(x) = x * sigmoid(x).  `gpre` is X W_G (the projection itself is outside
+ * this library).  o, gpre, z [B, N, H, d].
+ */
+void oracle_group_norm_gate(int B, int N, int H, int d, const double *o, const double *gpre,
+                            const double *w, const double *bias, double eps, double *z)
+{
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int b = 0; b < B; ++b) {
+        for (int n = 0; n < N; ++n) {
+            for (int h = 0; h < H; ++h) {
+                size_t base = (((size_t)b * N + n) * H + h) * d;
+                double mean = 0.0;
+                for (int c = 0; c < d; ++c)
+                    mean += o[base + c];
+                mean /= d;
+                double var = 0.0;
+                for (int c = 0; c < d; ++c)
+                    var += (o[base + c] - mean) * (o[base + c] - mean);
+                var /= d;
+                double inv = 1.0 / sqrt(var + eps);
+                for (int c = 0; c < d; ++c) {
+                    double y = (o[base + c] - mean) * inv;
+                    if (w)
+                        y *= w[(size_t)h * d + c];
+                    if (bias)
+                        y += bias[(size_t)h * d + c];
+                    double g = gpre[base + c];
+                    z[base + c] = g / (1.0 + exp(-g)) * y;
+                }
+            }
+        }
+    }
+}

@@ -443,3 +443,55 @@ def test_swa_keys_outside_the_window_change_nothing():
     O2 = oracle.swa_attn(Q, K2, V2, C, 0.5)
     assert np.array_equal(O[:, 8:], O2[:, 8:])   # rows 8, 9 see keys 5..9 only
     assert not np.allclose(O[:, 7], O2[:, 7])    # row 7 sees key 4
+
+
+# ------------------------------------------ gated retention output (Eq. 7) pins
+
+def test_group_norm_gate_normalises_each_head():
+    """Eq. 7, GroupNorm with one group per head: with a gate of swish(g) = g
+    sigmoid(g), dividing z by the gate recovers y with mean 0 and variance
+    var / (var + eps) over each head's channels, and w, b act per channel."""
+    rng = np.random.default_rng(31)
+    B, N, H, d, eps = 2, 3, 4, 16, 1e-5
+    o = rng.standard_normal((B, N, H, d)) * 3.0 + 1.5
+    g = rng.uniform(0.5, 2.0, (B, N, H, d))
+    z = oracle.group_norm_gate(o, g, eps)
+    y = z / (g / (1.0 + np.exp(-g)))
+    var = o.var(axis=-1)
+    np.testing.assert_allclose(y.mean(axis=-1), 0.0, atol=1e-12)
+    np.testing.assert_allclose(y.var(axis=-1), var / (var + eps), rtol=1e-12)
+    w = rng.standard_normal(H * d)
+    bb = rng.standard_normal(H * d)
+    z2 = oracle.group_norm_gate(o, g, eps, w, bb)
+    np.testing.assert_allclose(z2, (y * w.reshape(H, d) + bb.reshape(H, d)) * (g / (1.0 + np.exp(-g))),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_group_norm_gate_special_values():
+    """swish(0) = 0 closes the gate; a constant head vector normalises to 0, so
+    the output is the gate times the bias."""
+    rng = np.random.default_rng(32)
+    B, N, H, d = 1, 2, 2, 8
+    o = rng.standard_normal((B, N, H, d))
+    assert np.array_equal(oracle.group_norm_gate(o, np.zeros_like(o), 1e-6), np.zeros_like(o))
+    oc = np.full((B, N, H, d), 4.25)
+    g = rng.standard_normal((B, N, H, d))
+    bb = rng.standard_normal(H * d)
+    z = oracle.group_norm_gate(oc, g, 1e-6, None, bb)
+    np.testing.assert_allclose(z, g / (1.0 + np.exp(-g)) * bb.reshape(H, d), rtol=1e-14, atol=1e-15)
+
+
+def test_group_norm_gate_brute_force():
+    """Pure Python on one head vector."""
+    rng = np.random.default_rng(33)
+    d, eps = 5, 1e-3
+    o = rng.standard_normal((1, 1, 1, d))
+    g = rng.standard_normal((1, 1, 1, d))
+    z = oracle.group_norm_gate(o, g, eps)
+    xs = [float(x) for x in o.ravel()]
+    mu = sum(xs) / d
+    var = sum((x - mu) ** 2 for x in xs) / d
+    for c in range(d):
+        gc = float(g.ravel()[c])
+        ref = (xs[c] - mu) / math.sqrt(var + eps) * gc / (1.0 + math.exp(-gc))
+        assert abs(z.ravel()[c] - ref) < 1e-13
