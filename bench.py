@@ -48,7 +48,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk", type=int, default=0)
     p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode", "cross_prefill", "swa_prefill",
-                                      "swa_decode"], default=None,
+                                      "swa_decode", "gn_gate"], default=None,
                    help="time one call of the step on its bench shape (for profiling)")
     p.add_argument("--cache-len", type=int, default=0,
                    help="--only cross_decode: cache length (default: the step's prompt length)")
@@ -574,6 +574,13 @@ def run_only(args):
             def call():
                 return L.yoco_swa_decode(P(q1s), P(k1s), P(v1s), H, D ** -0.5, P(o1s), ctypes.byref(ring.c), P(ws),
                                          ws.numel(), stp)
+    elif args.only == "gn_gate":  # GroupNorm per head + swish gate over one gRet layer's output
+        og = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_V))
+        gg = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_Q))
+        zg = torch.empty_like(og)
+
+        def call():
+            return L.yoco_gret_group_norm_gate(P(og), P(gg), None, None, 1e-5, P(zg), B, N, H, D, 1, stp)
     elif args.only == "proj":
         M = normal((B, N, DM), bf, sid(CFG, 0, synth.T_M))
         Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
@@ -613,6 +620,9 @@ def run_only(args):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     line = {"only": args.only, "ms_per_call": ms, "steps": args.steps}
+    if args.only == "gn_gate":
+        nbytes = 3 * B * N * H * D * 2  # o and gate read, z written
+        line.update({"bytes_per_call": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1)})
     if args.only == "swa_prefill":
         # row n sees min(n + 1, 1024) keys; QK^T and PV cost 2 d flops per (row, key, head) each
         seen = sum(min(n + 1, 1024) for n in range(Ns))

@@ -68,6 +68,7 @@ def _load():
         "yoco_swa_prefill": (i, [vp, vp, vp, i, i, f, vp, rp, vp, sz, vp]),
         "yoco_swa_decode": (i, [vp, vp, vp, i, f, vp, rp, vp, sz, vp]),
         "yoco_swa_workspace_size": (sz, [i, i, rp]),
+        "yoco_gret_group_norm_gate": (i, [vp, vp, vp, vp, f, vp, i, i, i, i, i, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -82,7 +83,7 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_cross_attn_decode", "yoco_cross_attn_workspace_size", "yoco_status_string",
             "yoco_last_error", "yoco_version", "yoco_launch_count",
             "yoco_workspace_status", "yoco_cross_attn_decode_noalloc", "yoco_selftest_wait_timeout",
-            "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size")
+            "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size", "yoco_gret_group_norm_gate")
 
 
 def _check(status: int, where: str):
@@ -284,3 +285,21 @@ def yoco_swa_decode(q, k, v, ring: SwaRing, o, scale=None, workspace=None, strea
     st = lib.yoco_swa_decode(_ptr(q), _ptr(k), _ptr(v), Hq, float(scale), _ptr(o), ctypes.byref(ring.c), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "yoco_swa_decode")
+
+
+def yoco_gret_group_norm_gate(o, gate, z, eps=1e-5, gn_weight=None, gn_bias=None, stream=None):
+    """z = swish(gate) * GroupNorm_h(o); o, gate, z [B, N, H, d] (or [B, H, d] for a decode step);
+    gn_weight, gn_bias fp32 [H * d] or None.  z may be o."""
+    for t, n in ((o, "o"), (gate, "gate"), (z, "z")):
+        _need(t, n)
+    if o.dim() == 3:
+        B, H, d = o.shape
+        N = 1
+    else:
+        B, N, H, d = o.shape
+    for t, n in ((gn_weight, "gn_weight"), (gn_bias, "gn_bias")):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != H * d):
+            raise ValueError(f"{n} must be fp32 with H * d elements")
+    st = lib.yoco_gret_group_norm_gate(_ptr(o), _ptr(gate), _ptr(gn_weight), _ptr(gn_bias), float(eps), _ptr(z), B, N,
+                                       H, d, _dt(o), _stream(stream))
+    _check(st, "yoco_gret_group_norm_gate")

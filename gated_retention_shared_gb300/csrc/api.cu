@@ -247,6 +247,22 @@ yoco_status yoco_cross_attn_decode(const void *Q, int Hq, const yoco_kv_cache *c
     return attn_common(Q, Hq, 1, cache->len_host - 1, cache, scale, num_splits, O, workspace, ws_bytes, stream);
 }
 
+// ---------------------------------------------- gated retention output (Eq. 7)
+
+yoco_status yoco_gret_group_norm_gate(const void *o, const void *gate, const float *gn_weight, const float *gn_bias,
+                                      float eps, void *z, int B, int N, int H, int d, yoco_dtype dt, void *stream) {
+    if (!o || !gate || !z) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (!valid_dt(dt)) return fail(YOCO_ERR_INVALID_ARG, "dtype invalid");
+    if (d != 64 && d != 128) return fail(YOCO_ERR_UNSUPPORTED, "head size %d not in {64, 128}", d);
+    if (B <= 0 || N < 0 || H <= 0) return fail(YOCO_ERR_INVALID_ARG, "B, H must be > 0 and N >= 0");
+    if (!(eps > 0.f) || !isfinite(eps)) return fail(YOCO_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (!aligned(o, 16) || !aligned(gate, 16) || !aligned(z, 16))
+        return fail(YOCO_ERR_INVALID_ARG, "o, gate, z must be 16-byte aligned");
+    return cuda_status(group_norm_gate(o, gate, gn_weight, gn_bias, eps, z, (int64_t)B * N * H, H, d, dt,
+                                       (cudaStream_t)stream),
+                       "gret_group_norm_gate");
+}
+
 // ------------------------------------------------ sliding-window self-decoder
 
 static yoco_status check_ring(const yoco_swa_ring *r, int Hq) {

@@ -79,6 +79,10 @@ cudaError_t swa_fa_launch(const void *q, const void *k, const void *v, void *o, 
 cudaError_t swa_ring_write(const void *k, const void *v, void *rk, void *rv, int B, int N, int Hkv, int d,
                            int window, int64_t tok0, int n, int64_t pos0, yoco_dtype dt, cudaStream_t st);
 
+// gn_gate.cu: z = swish(gate) * GroupNorm_h(o) over rows of d (one group per head)
+cudaError_t group_norm_gate(const void *o, const void *gate, const float *w, const float *b, float eps, void *z,
+                            int64_t rows, int H, int d, yoco_dtype dt, cudaStream_t st);
+
 // selftest.cu
 cudaError_t selftest_wait(void *ws, uint64_t limit_ns, cudaStream_t st);
 

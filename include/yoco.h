@@ -204,6 +204,21 @@ YOCO_API yoco_status yoco_cross_attn_decode_noalloc(const void *Q, int Hq, const
 YOCO_API size_t yoco_cross_attn_workspace_size(int B, int Hq, int T, const yoco_kv_cache *cache,
                                       int num_splits);
 
+/* ------------------------------------- gated retention output (Eq. 7) */
+
+/*
+ * Output of multi-head gated retention (paper Section 3.1, Eq. 7):
+ *     z = swish(gate) (.) GroupNorm_h(o),   swish(x) = x sigmoid(x),
+ * GroupNorm with one group per head: each token's head vector is centred and
+ * divided by sqrt(variance over its d channels + eps), then multiplied by
+ * gn_weight and shifted by gn_bias per channel (fp32 [H * d]; NULL = 1 / 0).
+ * o, gate, z [B, N, H, d] of dtype dt (gate = X W_G, computed by the caller);
+ * N = 1 serves a decode step.  z may be o.  d in {64, 128}; eps > 0.
+ */
+YOCO_API yoco_status yoco_gret_group_norm_gate(const void *o, const void *gate, const float *gn_weight,
+                                               const float *gn_bias, float eps, void *z, int B, int N, int H, int d,
+                                               yoco_dtype dt, void *stream);
+
 /* ------------------------------------------- sliding-window self-decoder */
 
 /*

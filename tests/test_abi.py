@@ -179,3 +179,14 @@ def test_swa_validation(Y):
     r = _ring(Y)
     assert L.yoco_swa_workspace_size(1, 4, ctypes.byref(r)) >= 256
     assert r.pos == 0  # failed calls do not move the ring
+
+
+def test_group_norm_gate_validation(Y):
+    L = Y.lib
+    assert L.yoco_gret_group_norm_gate(FAKE, FAKE, None, None, 0.0, FAKE, 1, 4, 2, 128, 1, None) == \
+        Y.YOCO_ERR_INVALID_ARG
+    assert L.yoco_gret_group_norm_gate(FAKE, FAKE, None, None, 1e-5, FAKE, 1, 4, 2, 96, 1, None) == \
+        Y.YOCO_ERR_UNSUPPORTED
+    assert L.yoco_gret_group_norm_gate(FAKE, None, None, None, 1e-5, FAKE, 1, 4, 2, 128, 1, None) == \
+        Y.YOCO_ERR_INVALID_ARG
+    assert L.yoco_gret_group_norm_gate(FAKE, FAKE, None, None, 1e-5, FAKE, 1, 0, 2, 128, 1, None) == Y.YOCO_OK

@@ -579,6 +579,46 @@ def test_swa_decode_fp32_from_empty_ring(Y):
     assert max_abs(got, oracle.swa_attn(q, k, v, window, d ** -0.5)) <= FP32_MAX_ABS
 
 
+# --------------------------------------------- gated retention output (Eq. 7)
+
+@pytest.mark.parametrize("dtype,d,affine,inplace", [("bf16", 128, True, False), ("f32", 64, False, True),
+                                                    ("bf16", 64, False, True), ("f32", 128, True, False)])
+def test_group_norm_gate(Y, dtype, d, affine, inplace):
+    """swish(gate) * GroupNorm_h(o) over 777 tokens x 6 heads: bf16 within the
+    relative-L2 bound, fp32 within the max-abs bound; with and without the
+    per-channel affine; in place (z = o)."""
+    import torch
+    B, N, H = 2, 777, 6
+    o, od = gen(SEED, sid(50, 0, synth.T_V), (B, N, H, d), dtype, mean=0.3, std=2.0)
+    g, gd = gen(SEED, sid(50, 0, synth.T_Q), (B, N, H, d), dtype)
+    w = b = wd = bd = None
+    if affine:
+        w = synth.normal(SEED, sid(50, 1, synth.T_K), (H * d,), "f32", mean=1.0, std=0.2)
+        b = synth.normal(SEED, sid(50, 2, synth.T_K), (H * d,), "f32", std=0.2)
+        wd, bd = dev_f32(w), dev_f32(b)
+    z = od if inplace else torch.empty_like(od)
+    Y.yoco_gret_group_norm_gate(od, gd, z, eps=1e-5, gn_weight=wd, gn_bias=bd)
+    torch.cuda.synchronize()
+    z_ref = oracle.group_norm_gate(o, g, 1e-5, w, b)
+    if dtype == "f32":
+        assert max_abs(host_f64(z), z_ref) <= FP32_MAX_ABS
+    else:
+        assert rel_l2(host_f64(z), z_ref) <= BF16_REL_L2
+
+
+def test_group_norm_gate_decode_row(Y):
+    """A decode step's output [B, H, d] goes through the same call (N = 1)."""
+    import torch
+    B, H, d = 3, 24, 128
+    o, od = gen(SEED, sid(51, 0, synth.T_V), (B, H, d), "bf16")
+    g, gd = gen(SEED, sid(51, 0, synth.T_Q), (B, H, d), "bf16")
+    z = torch.empty_like(od)
+    Y.yoco_gret_group_norm_gate(od, gd, z)
+    torch.cuda.synchronize()
+    z_ref = oracle.group_norm_gate(o[:, None], g[:, None], 1e-5)[:, 0]
+    assert rel_l2(host_f64(z), z_ref) <= BF16_REL_L2
+
+
 # ------------------------------------------------------------- CUDA graphs
 
 def test_gret_decode_steps_replayed_from_a_cuda_graph(Y):
