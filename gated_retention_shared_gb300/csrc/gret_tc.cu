@@ -199,9 +199,14 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     volatile int *abort_flag = &sm.abort_flag;
-    // SEG_STATE: the OUTPUT grid may start on idle SMs now; it waits for this grid
-    // (griddepcontrol.wait) before it reads E, G or `state`
-    if (MODE == MODE_SEG_STATE) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    // Programmatic dependent launch.  SEG_STATE (launched as a dependent of whatever
+    // ran before, e.g. the previous layer's OUTPUT grid) waits for it before touching
+    // global memory, and only then lets its own OUTPUT grid start: that grid's TMA
+    // producer reads q, k, v at once, which is safe because everything before this
+    // grid has completed by then.  OUTPUT lets the next kernel (the next call's
+    // SEG_STATE) start its prologue on idle SMs right away; that kernel waits too.
+    if (MODE == MODE_SEG_STATE) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     // chunk order: OUTPUT forwards, SEG_STATE backwards (running suffix decay)
     auto chunk_start = [&](int i) {
@@ -684,21 +689,24 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     }
     // end states of segments 0 .. P-2 (the last segment's is computed by the OUTPUT pass)
     count_launches(2);
-    gret_tc_kernel<MODE_SEG_STATE><<<dim3(P - 1, a.H, a.B), kTcThreads, kTcSmemBytes, st>>>(
-        mq, mk, mv, mo, a.logits, inv_tau, nullptr, a.state, E, G, a.N, a.H, seg_len, P, err);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // the OUTPUT grid may begin (TMA loads, first MMAs) while SEG_STATE drains; its
-    // state warps wait for SEG_STATE before touching E, G and `state`
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(P, a.H, a.B);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = kTcSmemBytes;
-    cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kTcSmemBytes;
+    cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // SEG_STATE: its prologue overlaps the previous kernel's tail; it waits for it
+    // before reading anything
+    cfg.gridDim = dim3(P - 1, a.H, a.B);
+    e = cudaLaunchKernelEx(&cfg, gret_tc_kernel<MODE_SEG_STATE>, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)nullptr,
+                           a.state, E, G, a.N, a.H, seg_len, P, err);
+    if (e != cudaSuccess) return e;
+    // OUTPUT may begin (TMA loads, first MMAs) while SEG_STATE drains; its state
+    // warps wait for SEG_STATE before touching E, G and `state`
+    cfg.gridDim = dim3(P, a.H, a.B);
     return cudaLaunchKernelEx(&cfg, gret_tc_kernel<MODE_OUTPUT>, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o,
                               a.state, E, G, a.N, a.H, seg_len, P, err);
 }
