@@ -17,21 +17,48 @@
 
 namespace yoco {
 
-// r_row = 1 / sqrt(mean(M_row^2) + eps), one warp per row
+// r_row = 1 / sqrt(mean(M_row^2) + eps), one warp per row (rows strided over a
+// grid of at most one wave, 16-byte loads when the rows allow).  It releases its
+// programmatic dependents at once: the tensor-core GEMM that follows streams M
+// and W while this pass runs and waits for r only in its epilogue.
 template <typename T>
 __global__ void rms_rows_kernel(const T *__restrict__ M, float *__restrict__ r, int rows, int dm, float eps) {
-    const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    constexpr int EV = 16 / sizeof(T);  // elements per 16-byte load
     const int lane = threadIdx.x % 32;
-    if (w >= rows) return;
-    const T *row = M + (size_t)w * dm;
-    float ss = 0.f;
-    for (int i = lane; i < dm; i += 32) {
-        float x = to_f32(row[i]);
-        ss = fmaf(x, x, ss);
-    }
+    const int warps = gridDim.x * (blockDim.x / 32);
+    const bool vec = (dm % EV) == 0;
+    for (int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32; w < rows; w += warps) {
+        const T *row = M + (size_t)w * dm;
+        float ss = 0.f;
+        if (vec) {
+            for (int i = lane * EV; i < dm; i += 32 * EV) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(row + i);
+                if constexpr (sizeof(T) == 2) {
+                    const uint32_t x[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if (lane == 0) r[w] = rsqrtf(ss / (float)dm + eps);
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(x[e] << 16), hi = __uint_as_float(x[e] & 0xFFFF0000u);
+                        ss = fmaf(lo, lo, ss);
+                        ss = fmaf(hi, hi, ss);
+                    }
+                } else {
+                    const float f[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                        __uint_as_float(u.w)};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) ss = fmaf(f[e], f[e], ss);
+                }
+            }
+        } else {
+            for (int i = lane; i < dm; i += 32) {
+                const float x = to_f32(row[i]);
+                ss = fmaf(x, x, ss);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (lane == 0) r[w] = rsqrtf(ss / (float)dm + eps);
+    }
 }
 
 // Marks one CTA done; the last one publishes len + T.  len_dev[1] counts CTAs and
@@ -363,7 +390,7 @@ static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
         return cudaGetLastError();
     }
     count_launches(1);
-    rms_rows_kernel<T><<<(R * 32 + 255) / 256, 256, 0, st>>>((const T *)a.M, r, R, a.dm, a.eps);
+    rms_rows_kernel<T><<<std::min((R * 32 + 255) / 256, 152 * 8), 256, 0, st>>>((const T *)a.M, r, R, a.dm, a.eps);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a)) return kv_project_append_tc(a, r, (int *)ws, st);
     count_launches(1);

@@ -144,7 +144,10 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__
             mbar_wait(&sm.drain, 0, abort_flag, 200000000ull);
         }
     } else {
-        // epilogue: warps 2..5, TMEM lane quarter = warp % 4
+        // epilogue: warps 2..5, TMEM lane quarter = warp % 4.  The RMS factors come
+        // from the kernel before this one (a programmatic dependency): wait for it here,
+        // while the producer and the MMA warp are already running
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
         const int q = warp & 3;
         const int rloc = q * 32 + lane;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -260,10 +263,21 @@ cudaError_t kv_project_append_tc(const KvProjArgs &a, const float *rrow, int *er
     if (e != cudaSuccess) return e;
     const int ntiles = ((R + kPM - 1) / kPM) * (2 * n / kPN);
     const int grid = ntiles < 152 ? ntiles : 152;
+    // a programmatic dependent of the RMS pass (M and W are read-only here; the cache
+    // slots it writes were last touched by kernels that completed before that pass)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = kPSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     count_launches(1);
-    proj_tc_kernel<<<grid, kPThreads, kPSmem, st>>>(mm, mk, mv, rrow, (bf16_t *)a.kc, (bf16_t *)a.vc, R, a.T, a.dm, n,
-                                                   a.Hkv, a.d, a.cap, a.len, a.len_dev, err);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, proj_tc_kernel, mm, mk, mv, rrow, (bf16_t *)a.kc, (bf16_t *)a.vc, R, a.T, a.dm, n,
+                              a.Hkv, a.d, a.cap, a.len, a.len_dev, err);
 }
 
 }  // namespace yoco_host
