@@ -22,6 +22,9 @@ Language Models", arXiv:2405.05254v2):
   * swa_attn        -- Section 3.2, Eq. 8 (sliding-window attention, window
                        mask n - C < m <= n)
   * group_norm_gate -- Section 3.1, Eq. 7 (GroupNorm per head, swish gate)
+  * rope            -- Section 3.1 (Q (.) Theta, K (.) conj(Theta)); the notes'
+                       cross-decoder walk-through (K^ rotated in the shared
+                       projection, each layer's Q rotated)
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py.
 """
@@ -61,6 +64,7 @@ def lib():
         L.oracle_cross_attn.argtypes = [i, i, i, i, i, i64, _dp, _dp, _dp, i64, d, _dp]
         L.oracle_swa_attn.argtypes = [i, i, i, i, i, i64, _dp, _dp, _dp, d, _dp]
         L.oracle_group_norm_gate.argtypes = [i, i, i, i, _dp, _dp, _dp, _dp, d, _dp]
+        L.oracle_rope.argtypes = [i64, i, ctypes.POINTER(ctypes.c_int64), d, _dp]
         for name in ("oracle_gret_recurrent", "oracle_gret_parallel", "oracle_gret_chunkwise",
                      "oracle_rmsnorm_proj", "oracle_kv_append_bf16", "oracle_cross_attn"):
             getattr(L, name).restype = None
@@ -189,3 +193,14 @@ def group_norm_gate(o, gpre, eps, w=None, b=None):
     lib().oracle_group_norm_gate(B, N, H, d, _ptr(o), _ptr(gpre), None if wp is None else _ptr(wp),
                                  None if bp is None else _ptr(bp), float(eps), _ptr(z))
     return z
+
+
+def rope(x, pos, base):
+    """Rotary encoding of channel pairs (2i, 2i+1) by pos * base^(-2i/d).  x [..., d]
+    (fp64 copy returned); pos broadcastable to x.shape[:-1] (integer positions)."""
+    x = np.array(_f64(x), dtype=np.float64, copy=True)
+    d = x.shape[-1]
+    p = np.ascontiguousarray(np.broadcast_to(np.asarray(pos, dtype=np.int64), x.shape[:-1]).reshape(-1))
+    flat = np.ascontiguousarray(x.reshape(-1, d))
+    lib().oracle_rope(flat.shape[0], d, p.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), float(base), _ptr(flat))
+    return flat.reshape(x.shape)

@@ -438,3 +438,29 @@ void oracle_group_norm_gate(int B, int N, int H, int d, const double *o, const d
         }
     }
 }
+
+/*
+ * Rotary position encoding (paper Section 3.1: Q = (X W_Q) (.) Theta,
+ * K = (X W_K) (.) conj(Theta), Theta_n = e^{i n theta}; the notes: the shared K^
+ * is rotated once in the cross-decoder's projection and every cross layer
+ * rotates its own Q).  Real-valued form: channel pair (2i, 2i+1) of the vector at
+ * position p is turned by the angle p * base^(-2i/d):
+ *   x'_2i   = x_2i cos a - x_2i+1 sin a,   x'_2i+1 = x_2i sin a + x_2i+1 cos a.
+ * Turning q and k each by its own position makes q'.k' depend on the positions
+ * only through their difference, which is what the complex product of Theta and
+ * conj(Theta) expresses.  x [rows, d] with row r at position pos[r]; in place.
+ */
+void oracle_rope(int64_t rows, int d, const int64_t *pos, double base, double *x)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int i = 0; i < d / 2; ++i) {
+            double theta = pow(base, -2.0 * i / d);
+            double a = (double)pos[r] * theta;
+            double c = cos(a), s = sin(a);
+            double x0 = x[r * d + 2 * i], x1 = x[r * d + 2 * i + 1];
+            x[r * d + 2 * i] = x0 * c - x1 * s;
+            x[r * d + 2 * i + 1] = x0 * s + x1 * c;
+        }
+    }
+}

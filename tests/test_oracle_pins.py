@@ -495,3 +495,41 @@ def test_group_norm_gate_brute_force():
         gc = float(g.ravel()[c])
         ref = (xs[c] - mu) / math.sqrt(var + eps) * gc / (1.0 + math.exp(-gc))
         assert abs(z.ravel()[c] - ref) < 1e-13
+
+
+# ------------------------------------------------------- rotary encoding pins
+
+def test_rope_position_zero_is_identity_and_pairs_keep_length():
+    """Angle 0 at position 0; a rotation keeps the length of every pair."""
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((3, 5, 16))
+    assert np.array_equal(oracle.rope(x, 0, 10000.0), x)
+    pos = rng.integers(0, 10 ** 6, size=(3, 5))
+    y = oracle.rope(x, pos, 10000.0)
+    np.testing.assert_allclose(np.hypot(y[..., 0::2], y[..., 1::2]), np.hypot(x[..., 0::2], x[..., 1::2]),
+                               rtol=1e-13)
+
+
+def test_rope_first_pair_turns_by_the_position():
+    """Pair 0 has frequency base^0 = 1: (1, 0) at position p becomes (cos p, sin p);
+    the last pair of d = 4 turns by p / base^(1/2)."""
+    for p in (0, 1, 7, 1000, 123456789):
+        y = oracle.rope(np.array([[1.0, 0.0, 0.0, 1.0]]), p, 100.0)
+        np.testing.assert_allclose(y[0, :2], [math.cos(p), math.sin(p)], rtol=0, atol=1e-9)
+        a = p / 10.0
+        np.testing.assert_allclose(y[0, 2:], [-math.sin(a), math.cos(a)], rtol=0, atol=1e-9)
+
+
+def test_rope_dot_product_depends_on_the_offset_only():
+    """q rotated at n and k at m: their dot product is unchanged when both
+    positions move by the same amount, and rotations compose additively."""
+    rng = np.random.default_rng(42)
+    q = rng.standard_normal((1, 32))
+    k = rng.standard_normal((1, 32))
+    base = 640000.0
+    ref = float(oracle.rope(q, 50, base)[0] @ oracle.rope(k, 20, base)[0])
+    for shift in (1, 999, 65536):
+        got = float(oracle.rope(q, 50 + shift, base)[0] @ oracle.rope(k, 20 + shift, base)[0])
+        assert abs(got - ref) < 1e-9 * max(1.0, abs(ref))
+    np.testing.assert_allclose(oracle.rope(oracle.rope(q, 300, base), 45, base), oracle.rope(q, 345, base),
+                               rtol=1e-12, atol=1e-12)
