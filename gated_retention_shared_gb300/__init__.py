@@ -33,7 +33,8 @@ class YocoError(RuntimeError):
 class _KVCacheC(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("len_dev", ctypes.c_void_p),
                 ("len_host", ctypes.c_int64), ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32),
-                ("d", ctypes.c_int32), ("capacity", ctypes.c_int64), ("dtype", ctypes.c_int)]
+                ("d", ctypes.c_int32), ("capacity", ctypes.c_int64), ("dtype", ctypes.c_int),
+                ("rope_base", ctypes.c_float)]
 
 
 class _SwaRingC(ctypes.Structure):
@@ -69,6 +70,7 @@ def _load():
         "yoco_swa_decode": (i, [vp, vp, vp, i, f, vp, rp, vp, sz, vp]),
         "yoco_swa_workspace_size": (sz, [i, i, rp]),
         "yoco_gret_group_norm_gate": (i, [vp, vp, vp, vp, f, vp, i, i, i, i, i, vp]),
+        "yoco_rope_apply": (i, [vp, i, i, i, i, i64, f, i, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -83,7 +85,8 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_cross_attn_decode", "yoco_cross_attn_workspace_size", "yoco_status_string",
             "yoco_last_error", "yoco_version", "yoco_launch_count",
             "yoco_workspace_status", "yoco_cross_attn_decode_noalloc", "yoco_selftest_wait_timeout",
-            "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size", "yoco_gret_group_norm_gate")
+            "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size", "yoco_gret_group_norm_gate",
+            "yoco_rope_apply")
 
 
 def _check(status: int, where: str):
@@ -167,12 +170,12 @@ class KVCache:
     """Caller-side holder of the shared K^/V^ cache: two [B, Hkv, capacity, d]
     tensors, the device length pair and the C descriptor that points at them."""
 
-    def __init__(self, B, Hkv, d, capacity, dtype=torch.bfloat16, device="cuda", k=None, v=None):
+    def __init__(self, B, Hkv, d, capacity, dtype=torch.bfloat16, device="cuda", k=None, v=None, rope_base=0.0):
         self.k = k if k is not None else torch.zeros(B, Hkv, capacity, d, dtype=dtype, device=device)
         self.v = v if v is not None else torch.zeros(B, Hkv, capacity, d, dtype=dtype, device=device)
         self.len_dev = torch.zeros(2, dtype=torch.int32, device=self.k.device)
         self.c = _KVCacheC(self.k.data_ptr(), self.v.data_ptr(), self.len_dev.data_ptr(), 0, B, Hkv, d,
-                           capacity, _dt(self.k))
+                           capacity, _dt(self.k), float(rope_base))
 
     @property
     def length(self) -> int:
@@ -303,3 +306,13 @@ def yoco_gret_group_norm_gate(o, gate, z, eps=1e-5, gn_weight=None, gn_bias=None
     st = lib.yoco_gret_group_norm_gate(_ptr(o), _ptr(gate), _ptr(gn_weight), _ptr(gn_bias), float(eps), _ptr(z), B, N,
                                        H, d, _dt(o), _stream(stream))
     _check(st, "yoco_gret_group_norm_gate")
+
+
+# ------------------------------------------------- rotary position encoding
+
+def yoco_rope_apply(x, base, pos0=0, stream=None):
+    """Rotary encoding of x [B, N, H, d] (token-major q or k) in place: row n at position pos0 + n."""
+    _need(x, "x")
+    B, N, H, d = x.shape
+    st = lib.yoco_rope_apply(_ptr(x), B, N, H, d, int(pos0), float(base), _dt(x), _stream(stream))
+    _check(st, "yoco_rope_apply")

@@ -62,6 +62,8 @@ static yoco_status check_cache(const yoco_kv_cache *c) {
         return fail(YOCO_ERR_INVALID_ARG, "cache length %lld outside [0, capacity]", (long long)c->len_host);
     if (!aligned(c->k, 16) || !aligned(c->v, 16)) return fail(YOCO_ERR_INVALID_ARG, "cache k/v must be 16-byte aligned");
     if (c->capacity > (int64_t)INT32_MAX) return fail(YOCO_ERR_UNSUPPORTED, "capacity above 2^31-1");
+    if (!(c->rope_base == 0.0f || (c->rope_base > 1.0f && isfinite(c->rope_base))))
+        return fail(YOCO_ERR_INVALID_ARG, "rope_base must be 0 (off) or a finite base > 1");
     return YOCO_OK;
 }
 
@@ -190,7 +192,7 @@ yoco_status yoco_shared_kv_project_append(const void *M, const void *rms_w, floa
     const size_t need = kv_proj_workspace(cache->B, T, dm, cache->Hkv, cache->d, cache->dtype);
     if ((s = check_ws(workspace, ws_bytes, need)) != YOCO_OK) return s;
     KvProjArgs a{M, rms_w, Wk, Wv, eps, cache->B, T, dm, cache->Hkv, cache->d, cache->capacity, cache->len_host,
-                 cache->k, cache->v, cache->len_dev, cache->dtype};
+                 cache->k, cache->v, cache->len_dev, cache->dtype, cache->rope_base};
     s = cuda_status(kv_project_append(a, workspace, (cudaStream_t)stream), "shared_kv_project_append");
     if (s == YOCO_OK) cache->len_host += T;
     return s;
@@ -230,7 +232,7 @@ static yoco_status attn_common(const void *Q, int Hq, int T, int64_t p0, const y
     const size_t need = attn_workspace(cache->B, Hq, T, cache->d, splits);
     if ((s = check_ws(ws, ws_bytes, need)) != YOCO_OK) return s;
     AttnArgs a{Q, O, cache->k, cache->v, cache->B, T, Hq, cache->Hkv, cache->d, cache->capacity, p0, scale,
-               cache->dtype};
+               cache->dtype, cache->rope_base};
     return cuda_status(attn_run(a, splits, ws, (cudaStream_t)stream), "cross_attn");
 }
 
@@ -261,6 +263,20 @@ yoco_status yoco_gret_group_norm_gate(const void *o, const void *gate, const flo
     return cuda_status(group_norm_gate(o, gate, gn_weight, gn_bias, eps, z, (int64_t)B * N * H, H, d, dt,
                                        (cudaStream_t)stream),
                        "gret_group_norm_gate");
+}
+
+// -------------------------------------------------- rotary position encoding
+
+yoco_status yoco_rope_apply(void *x, int B, int N, int H, int d, int64_t pos0, float base, yoco_dtype dt,
+                            void *stream) {
+    if (!x) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (!valid_dt(dt)) return fail(YOCO_ERR_INVALID_ARG, "dtype invalid");
+    if (d != 64 && d != 128) return fail(YOCO_ERR_UNSUPPORTED, "head size %d not in {64, 128}", d);
+    if (B <= 0 || N < 0 || H <= 0 || B > 65535) return fail(YOCO_ERR_INVALID_ARG, "B in [1, 65535], H > 0, N >= 0");
+    if (pos0 < 0) return fail(YOCO_ERR_INVALID_ARG, "pos0 must be >= 0");
+    if (!(base > 1.0f) || !isfinite(base)) return fail(YOCO_ERR_INVALID_ARG, "base must be finite and > 1");
+    if (!aligned(x, 16)) return fail(YOCO_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    return cuda_status(rope_apply(x, B, N, H, d, pos0, base, dt, (cudaStream_t)stream), "rope_apply");
 }
 
 // ------------------------------------------------ sliding-window self-decoder
@@ -331,7 +347,7 @@ yoco_status yoco_swa_decode(const void *q, const void *k, const void *v, int Hq,
     if (e == cudaSuccess) {
         // the filled slots, in whatever order the ring holds them: every one is in the window
         AttnArgs a{q, o, ring->k, ring->v, ring->B, 1, Hq, ring->Hkv, ring->d, ring->window, keys - 1, scale,
-                   ring->dtype};
+                   ring->dtype, 0.0f};
         e = attn_run(a, splits, workspace, st);
     }
     if (e != cudaSuccess) return cuda_status(e, "swa_decode");

@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rope.cuh"
 
 namespace yoco {
 
@@ -51,7 +52,8 @@ template <typename T, int D, int NQ>
 __global__ void __launch_bounds__(kAttnThreads, 3)
 attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restrict__ Kc,
                   const T *__restrict__ Vc, float *__restrict__ part, int T_rows, int Hq, int Hkv,
-                  int64_t cap, int64_t p0, float scale, int RB, int64_t keys_per_split, int splits) {
+                  int64_t cap, int64_t p0, float scale, int RB, int64_t keys_per_split, int splits,
+                  float rope_base) {
     using Cfg = AttnCfg<T, D, NQ>;
     constexpr int E = Cfg::kEpt;
     extern __shared__ float4 smem4[];
@@ -72,6 +74,16 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
         int qv = e / D, c = e % D;
         int t = t0 + qv / G, h = hk * G + qv % G;
         qs[e] = scale * to_f32(Q[(((size_t)b * T_rows + t) * Hq + h) * D + c]);
+    }
+    if (rope_base > 0.f) {  // rotary encoding: turn each query row by its position
+        __syncthreads();
+        for (int e = threadIdx.x; e < nq * (D / 2); e += kAttnThreads) {
+            const int qv = e / (D / 2), i = e % (D / 2);
+            float c, s;
+            rope_cs_exact(p0 + t0 + qv / G, rope_theta(i, D, rope_base), c, s);
+            rope_turn(qs[qv * D + 2 * i], qs[qv * D + 2 * i + 1], c, s);
+        }
+        __syncthreads();
     }
 
     const int64_t k_lo = (int64_t)split * keys_per_split;
@@ -322,7 +334,7 @@ static cudaError_t launch_nq(const AttnArgs &a, int RB, int64_t kps, int splits,
     dim3 grid(splits, (a.T + RB - 1) / RB, a.B * a.Hkv);
     count_launches(splits > 1 ? 2 : 1);
     kern<<<grid, kAttnThreads, smem, st>>>((const T *)a.Q, (T *)a.O, (const T *)a.kc, (const T *)a.vc, (float *)ws,
-                                           a.T, a.Hq, a.Hkv, a.cap, a.p0, a.scale, RB, kps, splits);
+                                           a.T, a.Hq, a.Hkv, a.cap, a.p0, a.scale, RB, kps, splits, a.rope_base);
     return cudaGetLastError();
 }
 

@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rope.cuh"
 #include "tc.cuh"
 
 namespace yoco {
@@ -48,6 +49,8 @@ constexpr float kRescaleGap2 = 8.f * kLog2e;  // reference moves only when passe
 struct FaSmem {
     uint64_t q_full, full[kFStages], empty[kFStages];
     uint64_t s_full[2], p_ready[2], pv_done[2];  // per set
+    uint64_t q_rot[2];                           // per set: Q tile turned (rotary encoding) or as loaded
+    float rope_c[2][64], rope_s[2][64], rope_th[2][64];
     uint32_t tmem_base;
     int abort_flag;
     int go[2];
@@ -77,7 +80,7 @@ __device__ __forceinline__ float fa_ex2(float x) {  // 2^x, hardware approximati
 __global__ void __launch_bounds__(kFThreads, 1)
 attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, int T, int Hq,
-               int Hkv, int64_t p0, float scale, int64_t window, int kv_token_major, int *err) {
+               int Hkv, int64_t p0, float scale, int64_t window, int kv_token_major, int *err, float rope_base) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
@@ -107,6 +110,7 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_init(&sm.s_full[x], 1);
             mbar_init(&sm.p_ready[x], 1);
             mbar_init(&sm.pv_done[x], 1);
+            mbar_init(&sm.q_rot[x], 1);
         }
         sm.abort_flag = 0;
         fence_mbar_init();
@@ -168,6 +172,7 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             bool ok = mbar_wait(&sm.q_full, 0, abort_flag);
             auto issue_s = [&](int x, int i) -> bool {  // S_X = Q_X K(i)^T; S_X's TMEM held P_X(i-1)
                 if (i > 0 && !mbar_wait(&sm.pv_done[x], (i - 1) & 1, abort_flag)) return false;
+                if (i == 0 && !mbar_wait(&sm.q_rot[x], 0, abort_flag)) return false;  // Q_X as the MMA reads it
                 tc_fence_after();
                 const uint32_t q_a = smem_u32(sQ + x * kFTile);
                 const uint32_t k_a = smem_u32(ring + (size_t)(i % kFStages) * 2 * kFTile);
@@ -219,6 +224,45 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const float c2 = scale * kLog2e;
         float m_ref = -INFINITY, l = 0.f;                // base-2 units
         bool alive = true;
+        if (rope_base > 0.f) {
+            // rotary encoding of this set's Q rows in place: row r at position set_lo + r
+            // turns pair i by (set_lo + r) theta_i = base angle (fp64, once per pair) + r theta_i
+            if (r == 0) {
+                const bool ok = mbar_wait(&sm.q_full, 0, abort_flag);
+                if (!ok) fail(36);
+                sm.go[x] = ok && !*abort_flag;
+            }
+            if (r < kFD / 2) {
+                const double th = rope_theta(r, kFD, rope_base);
+                rope_cs_exact(set_lo, th, sm.rope_c[x][r], sm.rope_s[x][r]);
+                sm.rope_th[x][r] = (float)th;
+            }
+            fbar(bar_id, 128);
+            alive = sm.go[x];
+            if (alive) {
+                uint8_t *qt = sQ + x * kFTile;
+#pragma unroll 1
+                for (int ch = 0; ch < kFD / 8; ++ch) {  // 16-byte chunk = 4 pairs
+                    uint4 *p = reinterpret_cast<uint4 *>(qt + fa_tile_chunk(r, ch));
+                    uint4 u = *p;
+                    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int i = ch * 4 + q;
+                        float x0 = __uint_as_float(w[q] << 16), x1 = __uint_as_float(w[q] & 0xFFFF0000u);
+                        float cj, sj, c, s;
+                        rope_cs_offset(r, sm.rope_th[x][i], cj, sj);
+                        rope_cs_add(sm.rope_c[x][i], sm.rope_s[x][i], cj, sj, c, s);
+                        rope_turn(x0, x1, c, s);
+                        w[q] = fa_pack_bf16x2(x0, x1);
+                    }
+                    *p = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                fence_proxy_async_smem();
+            }
+            fbar(bar_id, 128);
+        }
+        if (r == 0) mbar_arrive(&sm.q_rot[x]);
         for (int i = 0; i < ntiles && alive; ++i) {
             if (r == 0) {
                 const bool ok = mbar_wait(&sm.s_full[x], i & 1, abort_flag);
@@ -390,7 +434,7 @@ bool attn_fa_eligible(const AttnArgs &a) {
 
 static cudaError_t fa_run(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv, const CUtensorMap &mo,
                           int B, int T, int Hq, int Hkv, int64_t p0, float scale, int64_t window, int kv_token_major,
-                          int *err, cudaStream_t st) {
+                          int *err, float rope_base, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(attn_fa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -404,7 +448,8 @@ static cudaError_t fa_run(const CUtensorMap &mq, const CUtensorMap &mk, const CU
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     count_launches(1);
-    return cudaLaunchKernelEx(&cfg, attn_fa_kernel, mq, mk, mv, mo, T, Hq, Hkv, p0, scale, window, kv_token_major, err);
+    return cudaLaunchKernelEx(&cfg, attn_fa_kernel, mq, mk, mv, mo, T, Hq, Hkv, p0, scale, window, kv_token_major, err,
+                              rope_base);
 }
 
 // [B, rows, H, 128] token-major bf16 as {d, H, rows, B}, box {64, 1, 128, 1}
@@ -425,7 +470,7 @@ cudaError_t attn_fa_launch(const AttnArgs &a, int64_t window, int *err, cudaStre
     if (!fa_token_major_map(&mq, a.Q, a.B, a.T, a.Hq) || !fa_token_major_map(&mo, a.O, a.B, a.T, a.Hq) ||
         !fa_map(&mk, 4, a.kc, kd, ks, kbox) || !fa_map(&mv, 4, a.vc, kd, ks, kbox))
         return cudaErrorInvalidValue;
-    return fa_run(mq, mk, mv, mo, a.B, a.T, a.Hq, a.Hkv, a.p0, a.scale, window, 0, err, st);
+    return fa_run(mq, mk, mv, mo, a.B, a.T, a.Hq, a.Hkv, a.p0, a.scale, window, 0, err, a.rope_base, st);
 }
 
 cudaError_t swa_fa_launch(const void *q, const void *k, const void *v, void *o, int B, int N, int Hq, int Hkv,
@@ -434,7 +479,7 @@ cudaError_t swa_fa_launch(const void *q, const void *k, const void *v, void *o, 
     if (!fa_token_major_map(&mq, q, B, N, Hq) || !fa_token_major_map(&mo, o, B, N, Hq) ||
         !fa_token_major_map(&mk, k, B, N, Hkv) || !fa_token_major_map(&mv, v, B, N, Hkv))
         return cudaErrorInvalidValue;
-    return fa_run(mq, mk, mv, mo, B, N, Hq, Hkv, 0, scale, window, 1, err, st);
+    return fa_run(mq, mk, mv, mo, B, N, Hq, Hkv, 0, scale, window, 1, err, 0.0f, st);
 }
 
 }  // namespace yoco_host

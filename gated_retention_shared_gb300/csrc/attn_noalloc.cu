@@ -68,6 +68,8 @@ extern "C" YOCO_API yoco_status yoco_cross_attn_decode_noalloc(const void *Q, in
     if (cache->B <= 0 || cache->Hkv <= 0 || cache->capacity <= 0 || cache->capacity > (int64_t)INT32_MAX)
         return reject(YOCO_ERR_INVALID_ARG, "cache B, Hkv or capacity out of range");
     if (cache->d != 64 && cache->d != 128) return reject(YOCO_ERR_UNSUPPORTED, "cache head size %lld not in {64, 128}", cache->d);
+    if (!(cache->rope_base == 0.0f || (cache->rope_base > 1.0f && isfinite(cache->rope_base))))
+        return reject(YOCO_ERR_INVALID_ARG, "rope_base must be 0 (off) or a finite base > 1");
     if (cache->len_host < 1 || cache->len_host > cache->capacity)
         return reject(YOCO_ERR_INVALID_ARG, "decode needs 1 <= length (%lld) <= capacity", cache->len_host);
     if (Hq <= 0 || Hq % cache->Hkv != 0 || Hq / cache->Hkv > 16)
@@ -98,7 +100,7 @@ extern "C" YOCO_API yoco_status yoco_cross_attn_decode_noalloc(const void *Q, in
         return YOCO_ERR_CUDA;
     }
     AttnArgs a{Q, O, cache->k, cache->v, cache->B, 1, Hq, cache->Hkv, cache->d, cache->capacity, keys - 1, scale,
-               cache->dtype};
+               cache->dtype, cache->rope_base};
     e = attn_run(a, splits, scratch, (cudaStream_t)stream);
     if (e != cudaSuccess) {
         set_error("cross_attn_decode_noalloc: %s", cudaGetErrorString(e));

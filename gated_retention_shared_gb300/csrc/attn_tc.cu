@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rope.cuh"
 #include "tc.cuh"
 
 namespace yoco {
@@ -62,7 +63,8 @@ template <int NQ>
 __global__ void __launch_bounds__(kAThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const bf16_t *__restrict__ Q, bf16_t *__restrict__ O, float *__restrict__ part, int T_rows, int Hq,
-               int Hkv, int64_t p0, float scale, int RB, int64_t keys_per_split, int splits, int *err) {
+               int Hkv, int64_t p0, float scale, int RB, int64_t keys_per_split, int splits, int *err,
+               float rope_base) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
@@ -110,6 +112,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         if (n < nq) {
             const int t = t0 + n / G, h = hk * G + n % G;
             v = *reinterpret_cast<const uint4 *>(Q + (((size_t)b * T_rows + t) * Hq + h) * kAD + c8);
+            if (rope_base > 0.f) {  // rotary encoding: turn the row's pairs by its position
+                uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float x0 = __uint_as_float(w[q] << 16), x1 = __uint_as_float(w[q] & 0xFFFF0000u);
+                    float c, s;
+                    rope_cs_exact(p0 + t, rope_theta(c8 / 2 + q, kAD, rope_base), c, s);
+                    rope_turn(x0, x1, c, s);
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+                    w[q] = *reinterpret_cast<uint32_t *>(&h2);
+                }
+                v = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
         *reinterpret_cast<uint4 *>(sQ + sw_off(n, c8, kAN)) = v;
     }
@@ -375,7 +390,7 @@ cudaError_t attn_tc_launch(const AttnArgs &a, int RB, int nq, int64_t kps, int s
     e = cudaFuncSetAttribute(attn_tc_kernel<NQ_>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem);       \
     if (e != cudaSuccess) return e;                                                                                \
     e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<NQ_>, mk, mv, (const bf16_t *)a.Q, (bf16_t *)a.O, (float *)ws,     \
-                           a.T, a.Hq, a.Hkv, a.p0, a.scale, RB, kps, splits, err);                                 \
+                           a.T, a.Hq, a.Hkv, a.p0, a.scale, RB, kps, splits, err, a.rope_base);                   \
     if (e != cudaSuccess) return e;
     if (nq <= 4) {
         YOCO_ATTN_TC(4)

@@ -41,6 +41,7 @@ struct KvProjArgs {
     void *kc, *vc;
     int32_t *len_dev;
     yoco_dtype dt;
+    float rope_base;  // 0: K^ is not rotated
 };
 size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt);
 cudaError_t kv_project_append(const KvProjArgs &a, void *ws, cudaStream_t st);
@@ -57,6 +58,7 @@ struct AttnArgs {
     int64_t cap, p0;  // row t sits at position p0 + t
     float scale;
     yoco_dtype dt;
+    float rope_base;  // 0: queries are not rotated
 };
 // resident CTAs per SM of the decode kernel that will run: 1 for the tensor-core
 // kernel (bf16, d = 128, <= 16 query heads per kv head), 3 for the CUDA-core one
@@ -82,6 +84,9 @@ cudaError_t swa_ring_write(const void *k, const void *v, void *rk, void *rv, int
 // gn_gate.cu: z = swish(gate) * GroupNorm_h(o) over rows of d (one group per head)
 cudaError_t group_norm_gate(const void *o, const void *gate, const float *w, const float *b, float eps, void *z,
                             int64_t rows, int H, int d, yoco_dtype dt, cudaStream_t st);
+
+// rope.cu: rotary encoding of token-major x [B, N, H, d] in place, row n at position pos0 + n
+cudaError_t rope_apply(void *x, int B, int N, int H, int d, int64_t pos0, float base, yoco_dtype dt, cudaStream_t st);
 
 // selftest.cu
 cudaError_t selftest_wait(void *ws, uint64_t limit_ns, cudaStream_t st);

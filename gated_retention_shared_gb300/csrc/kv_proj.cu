@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rope.cuh"
 
 namespace yoco {
 
@@ -83,7 +84,8 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 proj_append_simt(const T *__restrict__ M, const T *__restrict__ g, const T *__restrict__ Wk,
                  const T *__restrict__ Wv, const float *__restrict__ r, T *__restrict__ kc, T *__restrict__ vc,
-                 int R, int T_rows, int dm, int Hkv, int d, int64_t cap, int64_t len, int32_t *len_dev) {
+                 int R, int T_rows, int dm, int Hkv, int d, int64_t cap, int64_t len, int32_t *len_dev,
+                 float rope_base) {
     constexpr int BM = 64, BN = 64, BK = 16;
     __shared__ float As[BK][BM + 4];
     __shared__ float Bs[BK][BN + 4];
@@ -135,13 +137,26 @@ proj_append_simt(const T *__restrict__ M, const T *__restrict__ g, const T *__re
         if (row >= R) continue;
         int b = row / T_rows, t = row % T_rows;
         float rs = r[row];
+        float val[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) val[j] = acc[i][j] * rs;
+        // the thread's 4 columns lie in one head of Wk or Wv (d, n multiples of 64)
+        const int col4 = col0 + tc * 4;
+        if (rope_base > 0.f && col4 < n) {  // rotary encoding of K^ at slot position len + t
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                float cs, sn;
+                rope_cs_exact(len + t, rope_theta((col4 % d) / 2 + q, d, rope_base), cs, sn);
+                rope_turn(val[2 * q], val[2 * q + 1], cs, sn);
+            }
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            int col = col0 + tc * 4 + j;
+            int col = col4 + j;
             if (col >= 2 * n) continue;
             int cn = col % n, h = cn / d, c = cn % d;
             T *dst = (col < n) ? kc : vc;
-            dst[(((size_t)b * Hkv + h) * cap + len + t) * d + c] = from_f32<T>(acc[i][j] * rs);
+            dst[(((size_t)b * Hkv + h) * cap + len + t) * d + c] = from_f32<T>(val[j]);
         }
     }
     finish_append(len_dev, len + T_rows);
@@ -209,7 +224,7 @@ template <typename T, int kGemvRG>
 __global__ void __launch_bounds__(256)
 proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__restrict__ Wk, const T *__restrict__ Wv,
                  float *__restrict__ part, T *__restrict__ kc, T *__restrict__ vc, int R, int T_rows, int dm, int n,
-                 int Hkv, int d, int64_t cap, int64_t len, float eps, int KR, int32_t *len_dev) {
+                 int Hkv, int d, int64_t cap, int64_t len, float eps, int KR, int32_t *len_dev, float rope_base) {
     extern __shared__ float msh[];  // [kGemvRG][KR]: this chunk of the input rows, times the gain
     __shared__ float red[8][256];   // [warp][lane * 8 + e] for one input row
     __shared__ int last;
@@ -327,7 +342,17 @@ proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__re
             const int cn = c % n, h = cn / d, cc = cn % d;
             T *dst = ((c < n) ? kc : vc) + (((size_t)b * Hkv + h) * cap + len + t) * d + cc;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) dst[e] = from_f32<T>(sum[e] * r);
+            for (int e = 0; e < 8; ++e) sum[e] *= r;
+            if (rope_base > 0.f && c < n) {  // rotary encoding of K^ at slot position len + t
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float cs, sn;
+                    rope_cs_exact(len + t, rope_theta(cc / 2 + q, d, rope_base), cs, sn);
+                    rope_turn(sum[2 * q], sum[2 * q + 1], cs, sn);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dst[e] = from_f32<T>(sum[e]);
         }
         __syncthreads();  // red[0] is rewritten for the next row
     }
@@ -386,7 +411,7 @@ static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
         count_launches(1);
         kern<<<dim3((2 * n + 255) / 256, kch), 256, smem, st>>>(
             (const T *)a.M, (const T *)a.rms_w, (const T *)a.Wk, (const T *)a.Wv, part, (T *)a.kc, (T *)a.vc, R, a.T,
-            a.dm, n, a.Hkv, a.d, a.cap, a.len, a.eps, KR, a.len_dev);
+            a.dm, n, a.Hkv, a.d, a.cap, a.len, a.eps, KR, a.len_dev, a.rope_base);
         return cudaGetLastError();
     }
     count_launches(1);
@@ -397,7 +422,7 @@ static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
     dim3 grid((2 * a.Hkv * a.d + 63) / 64, (R + 63) / 64);
     proj_append_simt<T><<<grid, 256, 0, st>>>((const T *)a.M, (const T *)a.rms_w, (const T *)a.Wk, (const T *)a.Wv,
                                               r, (T *)a.kc, (T *)a.vc, R, a.T, a.dm, a.Hkv, a.d, a.cap, a.len,
-                                              a.len_dev);
+                                              a.len_dev, a.rope_base);
     return cudaGetLastError();
 }
 

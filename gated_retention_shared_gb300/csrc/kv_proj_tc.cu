@@ -16,6 +16,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "rope.cuh"
 #include "tc.cuh"
 
 namespace yoco {
@@ -27,7 +28,6 @@ constexpr int kPAtile = kPM * kPK * 2;          // 16 KB
 constexpr int kPBtile = kPK * kPN * 2;          // 32 KB (4 blocks of 64 columns)
 constexpr int kPStage = kPAtile + kPBtile;      // 48 KB
 constexpr int kPThreads = 192;
-constexpr size_t kPSmem = (size_t)kPStages * kPStage + 1024 + 256;
 
 struct ProjSmem {
     uint64_t full[kPStages], empty[kPStages];
@@ -35,13 +35,17 @@ struct ProjSmem {
     uint32_t tmem_base;
     int abort_flag;
     int go;  // epilogue continue decision (one writer, read after a barrier)
+    double rope_theta[64];  // rotary frequencies of the K^ channel pairs (d <= 128)
 };
+
+constexpr size_t kPSmem = (size_t)kPStages * kPStage + 1024 + sizeof(ProjSmem);
+static_assert(kPSmem <= 232448, "projection tiles and control block must fit shared memory");
 
 __global__ void __launch_bounds__(kPThreads, 1)
 proj_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_wk,
                const __grid_constant__ CUtensorMap tm_wv, const float *__restrict__ rrow, bf16_t *__restrict__ kc,
                bf16_t *__restrict__ vc, int R, int T_rows, int dm, int n, int Hkv, int d, int64_t cap, int64_t len,
-               int32_t *len_dev, int *err) {
+               int32_t *len_dev, int *err, float rope_base) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
@@ -150,6 +154,10 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__
         asm volatile("griddepcontrol.wait;\n" ::: "memory");
         const int q = warp & 3;
         const int rloc = q * 32 + lane;
+        if (rope_base > 0.f) {
+            if (rloc < d / 2) sm.rope_theta[rloc] = rope_theta(rloc, d, rope_base);
+            asm volatile("bar.sync 1, 128;\n" ::: "memory");
+        }
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
@@ -177,6 +185,18 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__
                     const int cg = col0 + cb * 32;  // 32 columns inside one head (d is a multiple of 32)
                     bf16_t *dst = (cg < n) ? kc : vc;
                     const int cn = cg % n, h = cn / d, c = cn % d;
+                    if (rope_base > 0.f && cg < n) {
+                        // rotary encoding of K^ at slot position len + t (V is not rotated)
+#pragma unroll
+                        for (int e2 = 0; e2 < 16; ++e2) {
+                            float x0 = __uint_as_float(r[2 * e2]), x1 = __uint_as_float(r[2 * e2 + 1]);
+                            float cs, sn;
+                            rope_cs_exact(len + t, sm.rope_theta[c / 2 + e2], cs, sn);
+                            rope_turn(x0, x1, cs, sn);
+                            r[2 * e2] = __float_as_uint(x0);
+                            r[2 * e2 + 1] = __float_as_uint(x1);
+                        }
+                    }
                     uint4 *p = reinterpret_cast<uint4 *>(dst + (((size_t)bb * Hkv + h) * cap + len + t) * d + c);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
@@ -277,7 +297,7 @@ cudaError_t kv_project_append_tc(const KvProjArgs &a, const float *rrow, int *er
     cfg.numAttrs = 1;
     count_launches(1);
     return cudaLaunchKernelEx(&cfg, proj_tc_kernel, mm, mk, mv, rrow, (bf16_t *)a.kc, (bf16_t *)a.vc, R, a.T, a.dm, n,
-                              a.Hkv, a.d, a.cap, a.len, a.len_dev, err);
+                              a.Hkv, a.d, a.cap, a.len, a.len_dev, err, a.rope_base);
 }
 
 }  // namespace yoco_host

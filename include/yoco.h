@@ -68,6 +68,13 @@ typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1 } yoco_dtype;
  *             sees the new length on replay.
  *   len_host  host copy of the length; appends advance it, attention calls
  *             read it.  The caller keeps it equal to len_dev[0].
+ *   rope_base 0: no rotary encoding.  > 1: rotary position encoding (paper
+ *             Section 3.1, Q (.) Theta / K (.) conj(Theta); the shared K^ is
+ *             rotated once when projected, each cross layer rotates its Q):
+ *             appends turn channel pair (2i, 2i+1) of K^ at slot p by
+ *             p * rope_base^(-2i/d) before rounding, and attention calls turn
+ *             each query row's pairs by its position the same way.  V is never
+ *             rotated.
  */
 typedef struct {
     void *k;
@@ -79,6 +86,7 @@ typedef struct {
     int32_t d;
     int64_t capacity;
     yoco_dtype dtype;
+    float rope_base;
 } yoco_kv_cache;
 
 /* ------------------------------------------------------------------ gRet */
@@ -218,6 +226,20 @@ YOCO_API size_t yoco_cross_attn_workspace_size(int B, int Hq, int T, const yoco_
 YOCO_API yoco_status yoco_gret_group_norm_gate(const void *o, const void *gate, const float *gn_weight,
                                                const float *gn_bias, float eps, void *z, int B, int N, int H, int d,
                                                yoco_dtype dt, void *stream);
+
+/* ----------------------------------------------- rotary position encoding */
+
+/*
+ * Rotary position encoding in place (paper Section 3.1: Q (.) Theta,
+ * K (.) conj(Theta), Theta_n = e^{i n theta}), for the q and k a self-decoder
+ * layer (gated retention or sliding-window attention) mixes: channel pair
+ * (2i, 2i+1) of row n turns by (pos0 + n) * base^(-2i/d).  The shared K^ and
+ * the cross layers' queries are rotated inside the append and attention calls
+ * instead (yoco_kv_cache.rope_base).
+ *   x [B, N, H, d] token-major, dtype dt; d in {64, 128}; base > 1; pos0 >= 0.
+ */
+YOCO_API yoco_status yoco_rope_apply(void *x, int B, int N, int H, int d, int64_t pos0, float base, yoco_dtype dt,
+                                     void *stream);
 
 /* ------------------------------------------- sliding-window self-decoder */
 

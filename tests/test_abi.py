@@ -190,3 +190,16 @@ def test_group_norm_gate_validation(Y):
     assert L.yoco_gret_group_norm_gate(FAKE, None, None, None, 1e-5, FAKE, 1, 4, 2, 128, 1, None) == \
         Y.YOCO_ERR_INVALID_ARG
     assert L.yoco_gret_group_norm_gate(FAKE, FAKE, None, None, 1e-5, FAKE, 1, 0, 2, 128, 1, None) == Y.YOCO_OK
+
+
+def test_rope_validation(Y):
+    L = Y.lib
+    assert L.yoco_rope_apply(FAKE, 1, 4, 2, 128, 0, 1.0, 1, None) == Y.YOCO_ERR_INVALID_ARG  # base must exceed 1
+    assert L.yoco_rope_apply(FAKE, 1, 4, 2, 96, 0, 1e4, 1, None) == Y.YOCO_ERR_UNSUPPORTED
+    assert L.yoco_rope_apply(FAKE, 1, 4, 2, 128, -1, 1e4, 1, None) == Y.YOCO_ERR_INVALID_ARG
+    assert L.yoco_rope_apply(FAKE, 1, 0, 2, 128, 0, 1e4, 1, None) == Y.YOCO_OK  # nothing to do
+    c = _cache(Y, length=10)
+    c.rope_base = -5.0
+    assert L.yoco_cross_attn_decode(FAKE, 4, ctypes.byref(c), 0.1, 0, FAKE, FAKE, 1 << 20, None) == \
+        Y.YOCO_ERR_INVALID_ARG
+    assert b"rope_base" in L.yoco_last_error()

@@ -619,6 +619,110 @@ def test_group_norm_gate_decode_row(Y):
     assert rel_l2(host_f64(z), z_ref) <= BF16_REL_L2
 
 
+# ------------------------------------------------- rotary position encoding
+
+@pytest.mark.parametrize("dtype,d,pos0,base", [("bf16", 128, 0, 10000.0), ("bf16", 128, 1000000, 8e7),
+                                               ("f32", 64, 77, 10000.0), ("f32", 128, 262000, 5e6)])
+def test_rope_apply(Y, dtype, d, pos0, base):
+    """In-place rotation of token-major q/k against the oracle, at positions up
+    to one million with the 1M-context base: bf16 within the relative-L2 bound,
+    fp32 within the max-abs bound."""
+    import torch
+    B, N, H = 2, 300, 3
+    x, xd = gen(SEED, sid(60, 0, synth.T_Q), (B, N, H, d), dtype)
+    Y.yoco_rope_apply(xd, base, pos0=pos0)
+    torch.cuda.synchronize()
+    ref = oracle.rope(x, (pos0 + np.arange(N))[None, :, None], base)
+    if dtype == "f32":
+        assert max_abs(host_f64(xd), ref) <= FP32_MAX_ABS
+    else:
+        assert rel_l2(host_f64(xd), ref) <= BF16_REL_L2
+
+
+@pytest.mark.parametrize("T,dtype,d,Hkv", [(1, "bf16", 128, 8), (256, "bf16", 128, 8), (20, "f32", 64, 2)])
+def test_kv_append_rotates_keys(Y, T, dtype, d, Hkv):
+    """With rope_base set, the append turns K^ at its slot positions (GEMV for a
+    decode token, tensor-core GEMM for 256 rows, CUDA cores for fp32) and leaves
+    V as without it."""
+    import torch
+    B, dm, length, base = 1, 256, 4000, 640000.0
+    M, Md = gen(SEED, sid(61, 0, synth.T_M), (B, T, dm), dtype)
+    Wk, Wkd = gen(SEED, sid(61, 0, synth.T_WK), (dm, Hkv * d), dtype, std=0.05)
+    Wv, Wvd = gen(SEED, sid(61, 0, synth.T_WV), (dm, Hkv * d), dtype, std=0.05)
+    cache = Y.KVCache(B, Hkv, d, length + T + 3, dtype=Md.dtype, rope_base=base)
+    cache.set_length(length)
+    Y.yoco_shared_kv_project_append(Md, Wkd, Wvd, cache, eps=1e-6)
+    torch.cuda.synchronize()
+    kref = oracle.rmsnorm_proj(M, Wk, 1e-6).reshape(B, T, Hkv, d)
+    vref = oracle.rmsnorm_proj(M, Wv, 1e-6).reshape(B, T, Hkv, d)
+    kref = oracle.rope(kref, (length + np.arange(T))[None, :, None], base)
+    kgot = host_f64(cache.k[:, :, length:length + T]).transpose(0, 2, 1, 3)
+    vgot = host_f64(cache.v[:, :, length:length + T]).transpose(0, 2, 1, 3)
+    if dtype == "f32":
+        assert max_abs(kgot, kref) <= FP32_MAX_ABS and max_abs(vgot, vref) <= FP32_MAX_ABS
+    else:
+        assert rel_l2(kgot, kref) <= BF16_REL_L2 and rel_l2(vgot, vref) <= BF16_REL_L2
+
+
+def rope_cache(Y, B, Hkv, d, length, dtype, cfg, base):
+    """A cache whose keys are already rotated at their slots (as appends leave
+    them), built from oracle values only."""
+    import torch
+    K = synth.normal_f64(SEED, sid(cfg, 0, synth.T_CACHE_K), B * Hkv * length * d).reshape(B, Hkv, length, d)
+    Krot = oracle.rope(K, np.arange(length)[None, None, :], base)
+    if dtype == "bf16":
+        bits = synth.f64_to_bf16_bits(Krot)
+        Kh, Kd = synth.bf16_bits_to_f32(bits).astype(np.float64), dev_bf16(bits)
+    else:
+        Kh = Krot.astype(np.float32).astype(np.float64)
+        Kd = dev_f32(Kh)
+    V, Vd = gen(SEED, sid(cfg, 0, synth.T_CACHE_V), (B, Hkv, length, d), dtype)
+    cache = Y.KVCache(B, Hkv, d, length, dtype=Vd.dtype, k=Kd, v=Vd, rope_base=base)
+    cache.set_length(length)
+    return Kh, V, cache
+
+
+@pytest.mark.parametrize("kind", ["decode", "early_exit", "many_rows", "noalloc"])
+def test_cross_attn_rotates_queries(Y, kind):
+    """With rope_base set every attention path turns each query row by its
+    position before the scores: decode (tensor cores), the early-exit row,
+    many prefill rows (128-row tiles) and decode without a workspace."""
+    import torch
+    B, Hq, Hkv, d, length, base = 1, 24, 8, 128, 3000, 5e6
+    K, V, cache = rope_cache(Y, B, Hkv, d, length, "bf16", 62, base)
+    T, p0 = {"decode": (1, length - 1), "early_exit": (1, length - 1), "many_rows": (300, 1500),
+             "noalloc": (1, length - 1)}[kind]
+    Q, Qd = gen(SEED, sid(62, 1, synth.T_QX), (B, T, Hq, d), "bf16")
+    if kind in ("decode", "noalloc"):
+        O = torch.empty(B, Hq, d, dtype=Qd.dtype, device="cuda")
+        if kind == "decode":
+            Y.yoco_cross_attn_decode(Qd[:, 0].contiguous(), cache, O)
+        else:
+            Y.yoco_cross_attn_decode_noalloc(Qd[:, 0].contiguous(), cache, O)
+        O = O[:, None]
+    else:
+        O = torch.empty_like(Qd)
+        Y.yoco_cross_attn_prefill(Qd, cache, p0, O)
+    torch.cuda.synchronize()
+    Qrot = oracle.rope(Q, (p0 + np.arange(T))[None, :, None], base)
+    O_ref = oracle.cross_attn(Qrot, K, V, p0, d ** -0.5)
+    assert rel_l2(host_f64(O), O_ref) <= BF16_REL_L2
+
+
+def test_cross_attn_rotates_queries_fp32(Y):
+    """The CUDA-core path (fp32, head size 64) turns its query rows too."""
+    import torch
+    B, Hq, Hkv, d, length, base = 1, 4, 2, 64, 400, 10000.0
+    K, V, cache = rope_cache(Y, B, Hkv, d, length, "f32", 63, base)
+    T, p0 = 40, 300
+    Q, Qd = gen(SEED, sid(63, 1, synth.T_QX), (B, T, Hq, d), "f32")
+    O = torch.empty_like(Qd)
+    Y.yoco_cross_attn_prefill(Qd, cache, p0, O)
+    torch.cuda.synchronize()
+    Qrot = oracle.rope(Q, (p0 + np.arange(T))[None, :, None], base)
+    assert max_abs(host_f64(O), oracle.cross_attn(Qrot, K, V, p0, d ** -0.5)) <= FP32_MAX_ABS
+
+
 # ------------------------------------------------------------- CUDA graphs
 
 def test_gret_decode_steps_replayed_from_a_cuda_graph(Y):
