@@ -48,12 +48,14 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk", type=int, default=0)
     p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode", "cross_prefill", "swa_prefill",
-                                      "swa_decode", "gn_gate"], default=None,
+                                      "swa_decode", "gn_gate", "rope"], default=None,
                    help="time one call of the step on its bench shape (for profiling)")
     p.add_argument("--cache-len", type=int, default=0,
                    help="--only cross_decode: cache length (default: the step's prompt length)")
     p.add_argument("--batch", type=int, default=0, help="--only cross_decode: sequences (default: the step's B)")
     p.add_argument("--splits", type=int, default=0, help="--only cross_decode: key splits (default: automatic)")
+    p.add_argument("--rope-base", type=float, default=0.0,
+                   help="--only proj/cross_decode/cross_prefill: rotary encoding base of the cache (0: off)")
     return p.parse_args()
 
 
@@ -538,7 +540,7 @@ def run_only(args):
         Tq = args.cache_len or N
         Kc = normal((B, HKV, Tq, D), bf, sid(CFG, 0, synth.T_CACHE_K))
         Vc = normal((B, HKV, Tq, D), bf, sid(CFG, 0, synth.T_CACHE_V))
-        cache = Y.KVCache(B, HKV, D, Tq, k=Kc, v=Vc)
+        cache = Y.KVCache(B, HKV, D, Tq, k=Kc, v=Vc, rope_base=args.rope_base)
         cache.set_length(Tq)
         Qp = normal((B, Tq, HQ, D), bf, sid(CFG, 0, synth.T_QX))
         Op = torch.empty_like(Qp)
@@ -575,6 +577,11 @@ def run_only(args):
             def call():
                 return L.yoco_swa_decode(P(q1s), P(k1s), P(v1s), H, D ** -0.5, P(o1s), ctypes.byref(ring.c), P(ws),
                                          ws.numel(), stp)
+    elif args.only == "rope":  # rotary encoding of one gRet layer's q in place
+        qr = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_Q))
+
+        def call():
+            return L.yoco_rope_apply(P(qr), B, N, H, D, 0, args.rope_base or 8e7, 1, stp)
     elif args.only == "gn_gate":  # GroupNorm per head + swish gate over one gRet layer's output
         og = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_V))
         gg = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_Q))
@@ -586,7 +593,7 @@ def run_only(args):
         M = normal((B, N, DM), bf, sid(CFG, 0, synth.T_M))
         Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
         Wv = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WV), std=0.02)
-        cache = Y.KVCache(B, HKV, D, N, device=dev)
+        cache = Y.KVCache(B, HKV, D, N, device=dev, rope_base=args.rope_base)
         ws = torch.empty(L.yoco_shared_kv_workspace_size(B, N, DM, ctypes.byref(cache.c)), dtype=torch.uint8,
                          device=dev)
 
@@ -600,7 +607,7 @@ def run_only(args):
         Nc = args.cache_len or N
         Kc = normal((Bc, HKV, Nc, D), bf, sid(CFG, 0, synth.T_CACHE_K))
         Vc = normal((Bc, HKV, Nc, D), bf, sid(CFG, 0, synth.T_CACHE_V))
-        cache = Y.KVCache(Bc, HKV, D, Nc, k=Kc, v=Vc)
+        cache = Y.KVCache(Bc, HKV, D, Nc, k=Kc, v=Vc, rope_base=args.rope_base)
         cache.set_length(Nc)
         Qd = normal((Bc, HQ, D), bf, sid(CFG, 0, synth.T_QX, 1))
         Od = torch.empty_like(Qd)
@@ -621,6 +628,9 @@ def run_only(args):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     line = {"only": args.only, "ms_per_call": ms, "steps": args.steps}
+    if args.only == "rope":
+        nbytes = 2 * B * N * H * D * 2  # read and written once
+        line.update({"bytes_per_call": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1)})
     if args.only == "gn_gate":
         nbytes = 3 * B * N * H * D * 2  # o and gate read, z written
         line.update({"bytes_per_call": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1)})

@@ -172,7 +172,7 @@ yoco_status yoco_gret_decode_step(const void *q, const void *k, const void *v, c
 
 size_t yoco_shared_kv_workspace_size(int B, int T, int dm, const yoco_kv_cache *cache) {
     if (!cache || B <= 0 || T <= 0 || dm <= 0) return 0;
-    return kv_proj_workspace(B, T, dm, cache->Hkv, cache->d, cache->dtype);
+    return kv_proj_workspace(B, T, dm, cache->Hkv, cache->d, cache->dtype, cache->rope_base);
 }
 
 yoco_status yoco_shared_kv_project_append(const void *M, const void *rms_w, float eps, const void *Wk,
@@ -189,7 +189,7 @@ yoco_status yoco_shared_kv_project_append(const void *M, const void *rms_w, floa
         return fail(YOCO_ERR_CAPACITY, "append of %d tokens at length %lld exceeds capacity %lld", T,
                     (long long)cache->len_host, (long long)cache->capacity);
     if ((int64_t)cache->B * T > INT32_MAX) return fail(YOCO_ERR_UNSUPPORTED, "B*T too large");
-    const size_t need = kv_proj_workspace(cache->B, T, dm, cache->Hkv, cache->d, cache->dtype);
+    const size_t need = kv_proj_workspace(cache->B, T, dm, cache->Hkv, cache->d, cache->dtype, cache->rope_base);
     if ((s = check_ws(workspace, ws_bytes, need)) != YOCO_OK) return s;
     KvProjArgs a{M, rms_w, Wk, Wv, eps, cache->B, T, dm, cache->Hkv, cache->d, cache->capacity, cache->len_host,
                  cache->k, cache->v, cache->len_dev, cache->dtype, cache->rope_base};

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kAttnThreads, 3)
 attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restrict__ Kc,
                   const T *__restrict__ Vc, float *__restrict__ part, int T_rows, int Hq, int Hkv,
                   int64_t cap, int64_t p0, float scale, int RB, int64_t keys_per_split, int splits,
-                  float rope_base) {
+                  float rope_base, const RopeFreq rf) {
     using Cfg = AttnCfg<T, D, NQ>;
     constexpr int E = Cfg::kEpt;
     extern __shared__ float4 smem4[];
@@ -80,7 +80,7 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
         for (int e = threadIdx.x; e < nq * (D / 2); e += kAttnThreads) {
             const int qv = e / (D / 2), i = e % (D / 2);
             float c, s;
-            rope_cs_exact(p0 + t0 + qv / G, rope_theta(i, D, rope_base), c, s);
+            rope_cs_exact(p0 + t0 + qv / G, rf.theta[i], c, s);
             rope_turn(qs[qv * D + 2 * i], qs[qv * D + 2 * i + 1], c, s);
         }
         __syncthreads();
@@ -334,7 +334,7 @@ static cudaError_t launch_nq(const AttnArgs &a, int RB, int64_t kps, int splits,
     dim3 grid(splits, (a.T + RB - 1) / RB, a.B * a.Hkv);
     count_launches(splits > 1 ? 2 : 1);
     kern<<<grid, kAttnThreads, smem, st>>>((const T *)a.Q, (T *)a.O, (const T *)a.kc, (const T *)a.vc, (float *)ws,
-                                           a.T, a.Hq, a.Hkv, a.cap, a.p0, a.scale, RB, kps, splits, a.rope_base);
+                                           a.T, a.Hq, a.Hkv, a.cap, a.p0, a.scale, RB, kps, splits, a.rope_base, make_rope_freq(a.rope_base, D));
     return cudaGetLastError();
 }
 

@@ -80,7 +80,8 @@ __device__ __forceinline__ float fa_ex2(float x) {  // 2^x, hardware approximati
 __global__ void __launch_bounds__(kFThreads, 1)
 attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, int T, int Hq,
-               int Hkv, int64_t p0, float scale, int64_t window, int kv_token_major, int *err, float rope_base) {
+               int Hkv, int64_t p0, float scale, int64_t window, int kv_token_major, int *err, float rope_base,
+               const RopeFreq rf) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
@@ -233,7 +234,7 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 sm.go[x] = ok && !*abort_flag;
             }
             if (r < kFD / 2) {
-                const double th = rope_theta(r, kFD, rope_base);
+                const double th = rf.theta[r];
                 rope_cs_exact(set_lo, th, sm.rope_c[x][r], sm.rope_s[x][r]);
                 sm.rope_th[x][r] = (float)th;
             }
@@ -449,7 +450,7 @@ static cudaError_t fa_run(const CUtensorMap &mq, const CUtensorMap &mk, const CU
     cfg.numAttrs = 1;
     count_launches(1);
     return cudaLaunchKernelEx(&cfg, attn_fa_kernel, mq, mk, mv, mo, T, Hq, Hkv, p0, scale, window, kv_token_major, err,
-                              rope_base);
+                              rope_base, make_rope_freq(rope_base, kFD));
 }
 
 // [B, rows, H, 128] token-major bf16 as {d, H, rows, B}, box {64, 1, 128, 1}

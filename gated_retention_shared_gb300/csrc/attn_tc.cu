@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kAThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                const bf16_t *__restrict__ Q, bf16_t *__restrict__ O, float *__restrict__ part, int T_rows, int Hq,
                int Hkv, int64_t p0, float scale, int RB, int64_t keys_per_split, int splits, int *err,
-               float rope_base) {
+               float rope_base, const RopeFreq rf) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
@@ -118,7 +118,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 for (int q = 0; q < 4; ++q) {
                     float x0 = __uint_as_float(w[q] << 16), x1 = __uint_as_float(w[q] & 0xFFFF0000u);
                     float c, s;
-                    rope_cs_exact(p0 + t, rope_theta(c8 / 2 + q, kAD, rope_base), c, s);
+                    rope_cs_exact(p0 + t, rf.theta[c8 / 2 + q], c, s);
                     rope_turn(x0, x1, c, s);
                     __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
                     w[q] = *reinterpret_cast<uint32_t *>(&h2);
@@ -373,6 +373,7 @@ cudaError_t attn_tc_launch(const AttnArgs &a, int RB, int nq, int64_t kps, int s
     if (!cache_map(&mk, a.kc, (int64_t)a.B * a.Hkv, a.cap, keys) || !cache_map(&mv, a.vc, (int64_t)a.B * a.Hkv, a.cap, keys))
         return cudaErrorInvalidValue;
     dim3 grid(splits, (a.T + RB - 1) / RB, a.B * a.Hkv);
+    const RopeFreq rf = make_rope_freq(a.rope_base, kAD);
     cudaError_t e;
     // launched as a programmatic dependent of the previous kernel on the stream: its
     // prologue (barriers, TMEM, descriptor prefetch) overlaps that kernel's tail
@@ -390,7 +391,7 @@ cudaError_t attn_tc_launch(const AttnArgs &a, int RB, int nq, int64_t kps, int s
     e = cudaFuncSetAttribute(attn_tc_kernel<NQ_>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem);       \
     if (e != cudaSuccess) return e;                                                                                \
     e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<NQ_>, mk, mv, (const bf16_t *)a.Q, (bf16_t *)a.O, (float *)ws,     \
-                           a.T, a.Hq, a.Hkv, a.p0, a.scale, RB, kps, splits, err, a.rope_base);                   \
+                           a.T, a.Hq, a.Hkv, a.p0, a.scale, RB, kps, splits, err, a.rope_base, rf);               \
     if (e != cudaSuccess) return e;
     if (nq <= 4) {
         YOCO_ATTN_TC(4)

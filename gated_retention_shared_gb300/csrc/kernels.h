@@ -43,11 +43,12 @@ struct KvProjArgs {
     yoco_dtype dt;
     float rope_base;  // 0: K^ is not rotated
 };
-size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt);
+size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt, float rope_base);
 cudaError_t kv_project_append(const KvProjArgs &a, void *ws, cudaStream_t st);
 // kv_proj_tc.cu: bf16, no gain, Hkv*d % 256 == 0, >= 128 rows
 bool kv_proj_tc_eligible(const KvProjArgs &a);
-cudaError_t kv_project_append_tc(const KvProjArgs &a, const float *rrow, int *err, cudaStream_t st);
+cudaError_t kv_project_append_tc(const KvProjArgs &a, const float *rrow, const float2 *rope_cs, int *err,
+                                 cudaStream_t st);
 
 // attn.cu
 struct AttnArgs {
@@ -87,6 +88,8 @@ cudaError_t group_norm_gate(const void *o, const void *gate, const float *w, con
 
 // rope.cu: rotary encoding of token-major x [B, N, H, d] in place, row n at position pos0 + n
 cudaError_t rope_apply(void *x, int B, int N, int H, int d, int64_t pos0, float base, yoco_dtype dt, cudaStream_t st);
+// (cos, sin) of (pos0 + t) theta_i into tab [T][d/2] (float2)
+cudaError_t rope_table(float2 *tab, int64_t pos0, int T, int d, float base, cudaStream_t st);
 
 // selftest.cu
 cudaError_t selftest_wait(void *ws, uint64_t limit_ns, cudaStream_t st);

@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(256)
 proj_append_simt(const T *__restrict__ M, const T *__restrict__ g, const T *__restrict__ Wk,
                  const T *__restrict__ Wv, const float *__restrict__ r, T *__restrict__ kc, T *__restrict__ vc,
                  int R, int T_rows, int dm, int Hkv, int d, int64_t cap, int64_t len, int32_t *len_dev,
-                 float rope_base) {
+                 float rope_base, const RopeFreq rf) {
     constexpr int BM = 64, BN = 64, BK = 16;
     __shared__ float As[BK][BM + 4];
     __shared__ float Bs[BK][BN + 4];
@@ -146,7 +146,7 @@ proj_append_simt(const T *__restrict__ M, const T *__restrict__ g, const T *__re
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 float cs, sn;
-                rope_cs_exact(len + t, rope_theta((col4 % d) / 2 + q, d, rope_base), cs, sn);
+                rope_cs_exact(len + t, rf.theta[(col4 % d) / 2 + q], cs, sn);
                 rope_turn(val[2 * q], val[2 * q + 1], cs, sn);
             }
         }
@@ -224,7 +224,8 @@ template <typename T, int kGemvRG>
 __global__ void __launch_bounds__(256)
 proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__restrict__ Wk, const T *__restrict__ Wv,
                  float *__restrict__ part, T *__restrict__ kc, T *__restrict__ vc, int R, int T_rows, int dm, int n,
-                 int Hkv, int d, int64_t cap, int64_t len, float eps, int KR, int32_t *len_dev, float rope_base) {
+                 int Hkv, int d, int64_t cap, int64_t len, float eps, int KR, int32_t *len_dev, float rope_base,
+                 const RopeFreq rf) {
     extern __shared__ float msh[];  // [kGemvRG][KR]: this chunk of the input rows, times the gain
     __shared__ float red[8][256];   // [warp][lane * 8 + e] for one input row
     __shared__ int last;
@@ -347,7 +348,7 @@ proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__re
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float cs, sn;
-                    rope_cs_exact(len + t, rope_theta(cc / 2 + q, d, rope_base), cs, sn);
+                    rope_cs_exact(len + t, rf.theta[cc / 2 + q], cs, sn);
                     rope_turn(sum[2 * q], sum[2 * q + 1], cs, sn);
                 }
             }
@@ -383,13 +384,18 @@ static int gemv_chunks(int n, int dm) {
 
 // workspace: [0, 256) status word of the tensor-core kernel, one fp32 RMS factor
 // per row (tensor-core and tiled paths), then (few-row path) the K-chunk partials
-size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt) {
+// workspace: [0, 256) status word, one fp32 RMS factor per row (padded to 256 B), then
+// either the few-row path's K-chunk partials or, with rotary encoding on the other
+// paths, the (cos, sin) table of the T positions [T][d/2] (the paths never meet)
+size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt, float rope_base) {
     (void)dt;
     size_t rows = (size_t)B * T;
     size_t ws = 256 + ((rows * sizeof(float) + 255) / 256) * 256;
     const int n = Hkv * d;
-    if (gemv_eligible((int)rows, n, dm)) ws += (size_t)gemv_chunks(n, dm) * rows * 2 * n * sizeof(float);
-    return ws;
+    size_t extra = 0;
+    if (gemv_eligible((int)rows, n, dm)) extra = (size_t)gemv_chunks(n, dm) * rows * 2 * n * sizeof(float);
+    else if (rope_base > 0.f) extra = (size_t)T * (d / 2) * sizeof(float2);
+    return ws + extra;
 }
 
 template <typename T>
@@ -411,18 +417,26 @@ static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
         count_launches(1);
         kern<<<dim3((2 * n + 255) / 256, kch), 256, smem, st>>>(
             (const T *)a.M, (const T *)a.rms_w, (const T *)a.Wk, (const T *)a.Wv, part, (T *)a.kc, (T *)a.vc, R, a.T,
-            a.dm, n, a.Hkv, a.d, a.cap, a.len, a.eps, KR, a.len_dev, a.rope_base);
+            a.dm, n, a.Hkv, a.d, a.cap, a.len, a.eps, KR, a.len_dev, a.rope_base, make_rope_freq(a.rope_base, a.d));
         return cudaGetLastError();
+    }
+    const bool tc = std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a);
+    float2 *rope_cs = nullptr;
+    if (tc && a.rope_base > 0.f) {
+        // the positions' (cos, sin) table for the GEMM epilogue, filled before the RMS pass
+        // (that pass releases the GEMM early, and the GEMM waits for it only)
+        rope_cs = reinterpret_cast<float2 *>(r + ((size_t)R + 63) / 64 * 64);
+        if ((e = rope_table(rope_cs, a.len, a.T, a.d, a.rope_base, st)) != cudaSuccess) return e;
     }
     count_launches(1);
     rms_rows_kernel<T><<<std::min((R * 32 + 255) / 256, 152 * 8), 256, 0, st>>>((const T *)a.M, r, R, a.dm, a.eps);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a)) return kv_project_append_tc(a, r, (int *)ws, st);
+    if (tc) return kv_project_append_tc(a, r, rope_cs, (int *)ws, st);
     count_launches(1);
     dim3 grid((2 * a.Hkv * a.d + 63) / 64, (R + 63) / 64);
     proj_append_simt<T><<<grid, 256, 0, st>>>((const T *)a.M, (const T *)a.rms_w, (const T *)a.Wk, (const T *)a.Wv,
                                               r, (T *)a.kc, (T *)a.vc, R, a.T, a.dm, a.Hkv, a.d, a.cap, a.len,
-                                              a.len_dev, a.rope_base);
+                                              a.len_dev, a.rope_base, make_rope_freq(a.rope_base, a.d));
     return cudaGetLastError();
 }
 

@@ -35,7 +35,6 @@ struct ProjSmem {
     uint32_t tmem_base;
     int abort_flag;
     int go;  // epilogue continue decision (one writer, read after a barrier)
-    double rope_theta[64];  // rotary frequencies of the K^ channel pairs (d <= 128)
 };
 
 constexpr size_t kPSmem = (size_t)kPStages * kPStage + 1024 + sizeof(ProjSmem);
@@ -45,7 +44,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 proj_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__ CUtensorMap tm_wk,
                const __grid_constant__ CUtensorMap tm_wv, const float *__restrict__ rrow, bf16_t *__restrict__ kc,
                bf16_t *__restrict__ vc, int R, int T_rows, int dm, int n, int Hkv, int d, int64_t cap, int64_t len,
-               int32_t *len_dev, int *err, float rope_base) {
+               int32_t *len_dev, int *err, const float2 *__restrict__ rope_cs) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
@@ -154,10 +153,7 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__
         asm volatile("griddepcontrol.wait;\n" ::: "memory");
         const int q = warp & 3;
         const int rloc = q * 32 + lane;
-        if (rope_base > 0.f) {
-            if (rloc < d / 2) sm.rope_theta[rloc] = rope_theta(rloc, d, rope_base);
-            asm volatile("bar.sync 1, 128;\n" ::: "memory");
-        }
+
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         uint32_t local = 0;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
@@ -185,14 +181,15 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__
                     const int cg = col0 + cb * 32;  // 32 columns inside one head (d is a multiple of 32)
                     bf16_t *dst = (cg < n) ? kc : vc;
                     const int cn = cg % n, h = cn / d, c = cn % d;
-                    if (rope_base > 0.f && cg < n) {
-                        // rotary encoding of K^ at slot position len + t (V is not rotated)
+                    if (rope_cs && cg < n) {
+                        // rotary encoding of K^ at slot position len + t (V is not rotated); the
+                        // (cos, sin) table of the call's positions was filled before the GEMM
+                        const float2 *cst = rope_cs + (size_t)t * (d / 2) + c / 2;
 #pragma unroll
                         for (int e2 = 0; e2 < 16; ++e2) {
                             float x0 = __uint_as_float(r[2 * e2]), x1 = __uint_as_float(r[2 * e2 + 1]);
-                            float cs, sn;
-                            rope_cs_exact(len + t, sm.rope_theta[c / 2 + e2], cs, sn);
-                            rope_turn(x0, x1, cs, sn);
+                            const float2 cs = cst[e2];
+                            rope_turn(x0, x1, cs.x, cs.y);
                             r[2 * e2] = __float_as_uint(x0);
                             r[2 * e2 + 1] = __float_as_uint(x1);
                         }
@@ -273,7 +270,8 @@ bool kv_proj_tc_eligible(const KvProjArgs &a) {
            (int64_t)a.B * a.T >= kPM && (al % 16) == 0;
 }
 
-cudaError_t kv_project_append_tc(const KvProjArgs &a, const float *rrow, int *err, cudaStream_t st) {
+cudaError_t kv_project_append_tc(const KvProjArgs &a, const float *rrow, const float2 *rope_cs, int *err,
+                                 cudaStream_t st) {
     const int R = a.B * a.T, n = a.Hkv * a.d;
     CUtensorMap mm, mk, mv;
     if (!map_2d(&mm, a.M, (uint64_t)R, (uint64_t)a.dm, kPM) || !map_2d(&mk, a.Wk, (uint64_t)a.dm, (uint64_t)n, kPK) ||
@@ -297,7 +295,7 @@ cudaError_t kv_project_append_tc(const KvProjArgs &a, const float *rrow, int *er
     cfg.numAttrs = 1;
     count_launches(1);
     return cudaLaunchKernelEx(&cfg, proj_tc_kernel, mm, mk, mv, rrow, (bf16_t *)a.kc, (bf16_t *)a.vc, R, a.T, a.dm, n,
-                              a.Hkv, a.d, a.cap, a.len, a.len_dev, err, a.rope_base);
+                              a.Hkv, a.d, a.cap, a.len, a.len_dev, err, rope_cs);
 }
 
 }  // namespace yoco_host

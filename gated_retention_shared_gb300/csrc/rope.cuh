@@ -13,24 +13,33 @@
 //     Elementary Functions", 1980) to [-pi, pi] and handed to __sincosf;
 // a position P0 + j combines the two by the angle-addition formulas.
 #pragma once
+#include <cmath>
 #include <cstdint>
 
 namespace yoco {
+
+// theta_i = base^(-2i/d) for the d/2 <= 64 channel pairs, computed once on the host
+// in fp64 and passed by value (kernels never evaluate the power)
+struct RopeFreq {
+    double theta[64];
+};
+
+inline RopeFreq make_rope_freq(float base, int d) {
+    RopeFreq f{};
+    if (base > 0.f)
+        for (int i = 0; i < d / 2 && i < 64; ++i) f.theta[i] = std::exp2(-2.0 * i / d * std::log2((double)base));
+    return f;
+}
 
 constexpr double kRopeTwoPi = 6.283185307179586476925286766559;
 constexpr float kRopeInvTwoPiF = 0.15915494309189533577f;
 constexpr float kRopeTwoPiHi = 6.28318548202514648438f;   // 2 pi rounded to float
 constexpr float kRopeTwoPiLo = -1.7484555314695172e-07f;  // 2 pi - kRopeTwoPiHi
 
-// theta_i = base^(-2i/d)
-__device__ __forceinline__ double rope_theta(int i, int d, float base) {
-    return exp2(-2.0 * (double)i / (double)d * log2((double)base));
-}
-
-// (cos, sin) of pos * theta, reduced in fp64
+// (cos, sin) of pos * theta, reduced in fp64 (the reduced angle lies in [0, 2 pi))
 __device__ __forceinline__ void rope_cs_exact(int64_t pos, double theta, float &c, float &s) {
     double a = (double)pos * theta;
-    a -= kRopeTwoPi * floor(a / kRopeTwoPi);
+    a = fma(-kRopeTwoPi, floor(a * (1.0 / kRopeTwoPi)), a);
     sincosf((float)a, &s, &c);
 }
 
