@@ -71,6 +71,8 @@ def _load():
         "yoco_swa_workspace_size": (sz, [i, i, rp]),
         "yoco_gret_group_norm_gate": (i, [vp, vp, vp, vp, f, vp, i, i, i, i, i, vp]),
         "yoco_rope_apply": (i, [vp, i, i, i, i, i64, f, i, vp]),
+        "yoco_gret_qkvg_project": (i, [vp, vp, i, i, i, i, i, i64, f, vp, vp, vp, vp, vp, sz, vp]),
+        "yoco_gret_qkvg_workspace_size": (sz, [i, i, i, i, f]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -86,7 +88,7 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_last_error", "yoco_version", "yoco_launch_count",
             "yoco_workspace_status", "yoco_cross_attn_decode_noalloc", "yoco_selftest_wait_timeout",
             "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size", "yoco_gret_group_norm_gate",
-            "yoco_rope_apply")
+            "yoco_rope_apply", "yoco_gret_qkvg_project", "yoco_gret_qkvg_workspace_size")
 
 
 def _check(status: int, where: str):
@@ -316,3 +318,18 @@ def yoco_rope_apply(x, base, pos0=0, stream=None):
     B, N, H, d = x.shape
     st = lib.yoco_rope_apply(_ptr(x), B, N, H, d, int(pos0), float(base), _dt(x), _stream(stream))
     _check(st, "yoco_rope_apply")
+
+
+def yoco_gret_qkvg_project(X, W, H, q, k, v, gate_logits, rope_base=0.0, pos0=0, workspace=None, stream=None):
+    """X [B, N, dm] bf16; W [dm, 3 H d + H] bf16 (W_Q | W_K | W_V | W_gamma); writes q, k, v
+    [B, N, H, d] bf16 and gate_logits [B, N, H] fp32."""
+    for t, n in ((X, "X"), (W, "W"), (q, "q"), (k, "k"), (v, "v"), (gate_logits, "gate_logits")):
+        _need(t, n)
+    B, N, dm = X.shape
+    d = q.shape[-1]
+    ws_n = lib.yoco_gret_qkvg_workspace_size(B, N, H, d, float(rope_base))
+    ws = _workspace(ws_n, X.device, workspace)
+    st = lib.yoco_gret_qkvg_project(_ptr(X), _ptr(W), B, N, dm, H, d, int(pos0), float(rope_base), _ptr(q), _ptr(k),
+                                    _ptr(v), _ptr(gate_logits), _ptr(ws), ws.numel() * ws.element_size(),
+                                    _stream(stream))
+    _check(st, "yoco_gret_qkvg_project")

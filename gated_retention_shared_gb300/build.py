@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libyoco.so")
-SOURCES = ["api.cu", "gret_simt.cu", "gret_tc.cu", "kv_proj.cu", "attn.cu", "attn_noalloc.cu", "kv_proj_tc.cu", "attn_tc.cu", "attn_fa.cu", "swa.cu", "gn_gate.cu", "rope.cu", "selftest.cu"]
+SOURCES = ["api.cu", "gret_simt.cu", "gret_tc.cu", "kv_proj.cu", "attn.cu", "attn_noalloc.cu", "kv_proj_tc.cu", "attn_tc.cu", "attn_fa.cu", "swa.cu", "gn_gate.cu", "rope.cu", "qkvg_tc.cu", "selftest.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -265,6 +265,43 @@ yoco_status yoco_gret_group_norm_gate(const void *o, const void *gate, const flo
                        "gret_group_norm_gate");
 }
 
+// ------------------------------------ gated-retention input projections (one GEMM)
+
+size_t yoco_gret_qkvg_workspace_size(int B, int N, int H, int d, float rope_base) {
+    (void)B; (void)H;
+    if (N <= 0 || d <= 0) return 256;
+    return 256 + (rope_base > 0.f ? (size_t)N * (d / 2) * sizeof(float2) : 0);
+}
+
+yoco_status yoco_gret_qkvg_project(const void *X, const void *W, int B, int N, int dm, int H, int d, int64_t pos0,
+                                   float rope_base, void *q, void *k, void *v, float *gate_logits, void *workspace,
+                                   size_t ws_bytes, void *stream) {
+    if (!X || !W || !q || !k || !v || !gate_logits) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (B <= 0 || N < 0 || dm <= 0 || H <= 0) return fail(YOCO_ERR_INVALID_ARG, "B, dm, H must be > 0 and N >= 0");
+    if (d != 64 && d != 128) return fail(YOCO_ERR_UNSUPPORTED, "head size %d not in {64, 128}", d);
+    if (dm % 8 != 0 || H % 8 != 0)
+        return fail(YOCO_ERR_UNSUPPORTED, "dm and H must be multiples of 8 (16-byte rows of X and W)");
+    if ((int64_t)B * N > INT32_MAX / 2 || (int64_t)H * d * 3 + H > INT32_MAX / 2)
+        return fail(YOCO_ERR_UNSUPPORTED, "size out of range");
+    if (pos0 < 0) return fail(YOCO_ERR_INVALID_ARG, "pos0 must be >= 0");
+    if (!(rope_base == 0.0f || (rope_base > 1.0f && isfinite(rope_base))))
+        return fail(YOCO_ERR_INVALID_ARG, "rope_base must be 0 (off) or a finite base > 1");
+    if (!aligned(X, 16) || !aligned(W, 16) || !aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16))
+        return fail(YOCO_ERR_INVALID_ARG, "X, W, q, k, v must be 16-byte aligned");
+    yoco_status s = check_ws(workspace, ws_bytes, yoco_gret_qkvg_workspace_size(B, N, H, d, rope_base));
+    if (s != YOCO_OK) return s;
+    if (N == 0) return YOCO_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    float2 *rope_cs = nullptr;
+    cudaError_t e = cudaSuccess;
+    if (rope_base > 0.f) {
+        rope_cs = reinterpret_cast<float2 *>((char *)workspace + 256);
+        e = rope_table(rope_cs, pos0, N, d, rope_base, st);
+    }
+    if (e == cudaSuccess) e = qkvg_project(X, W, B, N, dm, H, d, q, k, v, gate_logits, rope_cs, (int *)workspace, st);
+    return cuda_status(e, "gret_qkvg_project");
+}
+
 // -------------------------------------------------- rotary position encoding
 
 yoco_status yoco_rope_apply(void *x, int B, int N, int H, int d, int64_t pos0, float base, yoco_dtype dt,

@@ -91,6 +91,10 @@ cudaError_t rope_apply(void *x, int B, int N, int H, int d, int64_t pos0, float 
 // (cos, sin) of (pos0 + t) theta_i into tab [T][d/2] (float2)
 cudaError_t rope_table(float2 *tab, int64_t pos0, int T, int d, float base, cudaStream_t st);
 
+// qkvg_tc.cu: [q | k | v | logits] = X [W_Q | W_K | W_V | W_gamma], bf16, tensor cores
+cudaError_t qkvg_project(const void *X, const void *W, int B, int N, int dm, int H, int d, void *q, void *k, void *v,
+                         float *logits, const float2 *rope_cs, int *err, cudaStream_t st);
+
 // selftest.cu
 cudaError_t selftest_wait(void *ws, uint64_t limit_ns, cudaStream_t st);
 

@@ -227,6 +227,27 @@ YOCO_API yoco_status yoco_gret_group_norm_gate(const void *o, const void *gate, 
                                                const float *gn_bias, float eps, void *z, int B, int N, int H, int d,
                                                yoco_dtype dt, void *stream);
 
+/* ------------------------- gated-retention input projections in one GEMM */
+
+/*
+ * The gated-retention layer's input projections (paper Section 3.1:
+ * Q = (X W_Q) (.) Theta, K = (X W_K) (.) conj(Theta), V = X W_V,
+ * gamma = sigmoid(X W_gamma)^(1/tau)) as one GEMM that reads X once:
+ *     [q | k | v | gate_logits] = X [W_Q | W_K | W_V | W_gamma]
+ *   X [B, N, dm] bf16 (the layer's normalised input);
+ *   W [dm, 3 H d + H] bf16, columns W_Q | W_K | W_V | W_gamma;
+ *   q, k, v [B, N, H, d] bf16 token-major, as yoco_gret_prefill_chunkwise reads them;
+ *   gate_logits [B, N, H] fp32 = X W_gamma (the chunk and recurrent kernels apply
+ *   logsigmoid / tau).
+ * rope_base > 1 turns q and k by position pos0 + n (channel pairs (2i, 2i+1),
+ * base^(-2i/d)); 0 leaves them.  bf16 on the tensor cores; d in {64, 128};
+ * dm and H multiples of 8.  workspace: yoco_gret_qkvg_workspace_size bytes.
+ */
+YOCO_API yoco_status yoco_gret_qkvg_project(const void *X, const void *W, int B, int N, int dm, int H, int d,
+                                            int64_t pos0, float rope_base, void *q, void *k, void *v,
+                                            float *gate_logits, void *workspace, size_t ws_bytes, void *stream);
+YOCO_API size_t yoco_gret_qkvg_workspace_size(int B, int N, int H, int d, float rope_base);
+
 /* ----------------------------------------------- rotary position encoding */
 
 /*

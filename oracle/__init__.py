@@ -25,6 +25,9 @@ Language Models", arXiv:2405.05254v2):
   * rope            -- Section 3.1 (Q (.) Theta, K (.) conj(Theta)); the notes'
                        cross-decoder walk-through (K^ rotated in the shared
                        projection, each layer's Q rotated)
+  * qkvg_project    -- Section 3.1 (Q = X W_Q (.) Theta, K = X W_K (.) conj(Theta),
+                       V = X W_V, gamma from X W_gamma): one product with the
+                       four weight matrices side by side
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py.
 """
@@ -204,3 +207,22 @@ def rope(x, pos, base):
     flat = np.ascontiguousarray(x.reshape(-1, d))
     lib().oracle_rope(flat.shape[0], d, p.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), float(base), _ptr(flat))
     return flat.reshape(x.shape)
+
+
+def qkvg_project(X, W, H, d, pos0=0, rope_base=0.0):
+    """Section 3.1's projections of a gRet layer: Y = X W with W = [W_Q | W_K | W_V | W_gamma]
+    (an fp64 matrix product), split into q, k, v [B, N, H, d] and the gate logits
+    [B, N, H]; with rope_base > 0, q and k turned by position pos0 + n."""
+    X, W = _f64(X), _f64(W)
+    B, N, dm = X.shape
+    Hd = H * d
+    Y = X.reshape(B * N, dm) @ W
+    q = Y[:, :Hd].reshape(B, N, H, d)
+    k = Y[:, Hd:2 * Hd].reshape(B, N, H, d)
+    v = Y[:, 2 * Hd:3 * Hd].reshape(B, N, H, d)
+    logits = Y[:, 3 * Hd:3 * Hd + H].reshape(B, N, H)
+    if rope_base > 0:
+        pos = (pos0 + np.arange(N))[None, :, None]
+        q = rope(q, pos, rope_base)
+        k = rope(k, pos, rope_base)
+    return q, k, v, logits

@@ -533,3 +533,32 @@ def test_rope_dot_product_depends_on_the_offset_only():
         assert abs(got - ref) < 1e-9 * max(1.0, abs(ref))
     np.testing.assert_allclose(oracle.rope(oracle.rope(q, 300, base), 45, base), oracle.rope(q, 345, base),
                                rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------ gRet input projection pins
+
+def test_qkvg_project_columns_and_brute_force():
+    """The four projections side by side: with W holding unit columns that pick
+    input channels, q, k, v and the logits are those channels; and the product
+    itself against explicit Python sums on a tiny case."""
+    B, N, dm, H, d = 1, 3, 8, 2, 2
+    rng = np.random.default_rng(51)
+    X = rng.standard_normal((B, N, dm))
+    W = np.zeros((dm, 3 * H * d + H))
+    for col in range(W.shape[1]):
+        W[col % dm, col] = 1.0
+    q, k, v, lg = oracle.qkvg_project(X, W, H, d)
+    cols = [c % dm for c in range(W.shape[1])]
+    np.testing.assert_array_equal(q.reshape(B, N, H * d), X[..., cols[0:4]])
+    np.testing.assert_array_equal(k.reshape(B, N, H * d), X[..., cols[4:8]])
+    np.testing.assert_array_equal(v.reshape(B, N, H * d), X[..., cols[8:12]])
+    np.testing.assert_array_equal(lg, X[..., cols[12:14]])
+    W2 = rng.standard_normal(W.shape)
+    q2, _, _, lg2 = oracle.qkvg_project(X, W2, H, d)
+    for n in range(N):
+        for j in range(H * d):
+            ref = sum(X[0, n, c] * W2[c, j] for c in range(dm))
+            assert abs(q2.reshape(B, N, H * d)[0, n, j] - ref) < 1e-12
+        for g in range(H):
+            ref = sum(X[0, n, c] * W2[c, 3 * H * d + g] for c in range(dm))
+            assert abs(lg2[0, n, g] - ref) < 1e-12
