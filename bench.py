@@ -48,7 +48,7 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk", type=int, default=0)
     p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode", "cross_prefill", "swa_prefill",
-                                      "swa_decode", "gn_gate", "rope"], default=None,
+                                      "swa_decode", "gn_gate", "rope", "qkvg"], default=None,
                    help="time one call of the step on its bench shape (for profiling)")
     p.add_argument("--cache-len", type=int, default=0,
                    help="--only cross_decode: cache length (default: the step's prompt length)")
@@ -577,6 +577,17 @@ def run_only(args):
             def call():
                 return L.yoco_swa_decode(P(q1s), P(k1s), P(v1s), H, D ** -0.5, P(o1s), ctypes.byref(ring.c), P(ws),
                                          ws.numel(), stp)
+    elif args.only == "qkvg":  # a gRet layer's four input projections in one GEMM
+        Xg = normal((B, N, DM), bf, sid(CFG, 0, synth.T_M))
+        Wg = normal((DM, 3 * H * D + H), bf, sid(CFG, 0, synth.T_WK), std=DM ** -0.5)
+        qg = torch.empty(B, N, H, D, dtype=bf, device=dev)
+        kg, vg = torch.empty_like(qg), torch.empty_like(qg)
+        lgg = torch.empty(B, N, H, dtype=f32, device=dev)
+        ws = torch.empty(L.yoco_gret_qkvg_workspace_size(B, N, H, D, args.rope_base), dtype=torch.uint8, device=dev)
+
+        def call():
+            return L.yoco_gret_qkvg_project(P(Xg), P(Wg), B, N, DM, H, D, 0, args.rope_base, P(qg), P(kg), P(vg),
+                                            P(lgg), P(ws), ws.numel(), stp)
     elif args.only == "rope":  # rotary encoding of one gRet layer's q in place
         qr = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_Q))
 
@@ -628,6 +639,9 @@ def run_only(args):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     line = {"only": args.only, "ms_per_call": ms, "steps": args.steps}
+    if args.only == "qkvg":
+        flops = 2.0 * B * N * DM * (3 * H * D + H)
+        line.update({"flops_per_call": flops, "achieved_tflops": round(flops / (ms / 1e3) / 1e12, 1)})
     if args.only == "rope":
         nbytes = 2 * B * N * H * D * 2  # read and written once
         line.update({"bytes_per_call": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1)})

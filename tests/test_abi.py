@@ -203,3 +203,14 @@ def test_rope_validation(Y):
     assert L.yoco_cross_attn_decode(FAKE, 4, ctypes.byref(c), 0.1, 0, FAKE, FAKE, 1 << 20, None) == \
         Y.YOCO_ERR_INVALID_ARG
     assert b"rope_base" in L.yoco_last_error()
+
+
+def test_qkvg_validation(Y):
+    L = Y.lib
+    args = lambda H, d, rb=0.0, ws=FAKE, n=1 << 20: (FAKE, FAKE, 1, 64, 256, H, d, 0, rb, FAKE, FAKE, FAKE, FAKE,  # noqa: E731
+                                                    ws, n, None)
+    assert L.yoco_gret_qkvg_project(*args(12, 128)) == Y.YOCO_ERR_UNSUPPORTED  # H not a multiple of 8
+    assert L.yoco_gret_qkvg_project(*args(8, 96)) == Y.YOCO_ERR_UNSUPPORTED
+    assert L.yoco_gret_qkvg_project(*args(8, 128, rb=-1.0)) == Y.YOCO_ERR_INVALID_ARG
+    assert L.yoco_gret_qkvg_project(*args(8, 128, rb=1e4, ws=None, n=0)) == Y.YOCO_ERR_WORKSPACE
+    assert L.yoco_gret_qkvg_workspace_size(1, 64, 8, 128, 1e4) == 256 + 64 * 64 * 8

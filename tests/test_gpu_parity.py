@@ -723,6 +723,67 @@ def test_cross_attn_rotates_queries_fp32(Y):
     assert max_abs(host_f64(O), oracle.cross_attn(Qrot, K, V, p0, d ** -0.5)) <= FP32_MAX_ABS
 
 
+# ------------------------------------------- gRet input projections (one GEMM)
+
+def qkvg_run(Y, cfg, B, N, dm, H, d, pos0=0, rope_base=0.0):
+    import torch
+    X, Xd = gen(SEED, sid(cfg, 0, synth.T_M), (B, N, dm), "bf16")
+    W, Wd = gen(SEED, sid(cfg, 0, synth.T_WK), (dm, 3 * H * d + H), "bf16", std=dm ** -0.5)
+    q = torch.empty(B, N, H, d, dtype=torch.bfloat16, device="cuda")
+    k, v = torch.empty_like(q), torch.empty_like(q)
+    lg = torch.empty(B, N, H, device="cuda")
+    Y.yoco_gret_qkvg_project(Xd, Wd, H, q, k, v, lg, rope_base=rope_base, pos0=pos0)
+    torch.cuda.synchronize()
+    return (X, W), (q, k, v, lg)
+
+
+@pytest.mark.parametrize("B,N,dm,H,d,pos0,rope_base", [(2, 300, 256, 8, 128, 0, 0.0), (2, 300, 256, 8, 128, 1000, 5e6),
+                                                       (1, 200, 128, 16, 64, 7, 10000.0)])
+def test_qkvg_project(Y, B, N, dm, H, d, pos0, rope_base):
+    """q, k, v (bf16, [B, N, H, d]) and the fp32 gate logits of one GEMM over
+    [W_Q | W_K | W_V | W_gamma], with and without rotary encoding; ragged rows
+    and a last column tile that is mostly past the matrix."""
+    (X, W), (q, k, v, lg) = qkvg_run(Y, 70, B, N, dm, H, d, pos0, rope_base)
+    rq, rk, rv, rlg = oracle.qkvg_project(X, W, H, d, pos0, rope_base)
+    for got, ref in ((q, rq), (k, rk), (v, rv)):
+        assert rel_l2(host_f64(got), ref) <= BF16_REL_L2
+    assert rel_l2(host_f64(lg), rlg) <= 1e-4
+
+
+def test_qkvg_project_3b_width_sampled_rows(Y):
+    """The 3B layer's width (d_model 3072, 24 heads x 128: 9240 columns) over
+    4096 tokens; 64 sampled rows against the oracle."""
+    B, N, dm, H, d = 1, 4096, 3072, 24, 128
+    (X, W), (q, k, v, lg) = qkvg_run(Y, 71, B, N, dm, H, d, 0, 8e7)
+    rows = np.linspace(0, N - 1, 64).astype(int)
+    # the oracle on the sampled rows only (positions kept: rotate by the row's own position)
+    Yr = X[0, rows] @ W
+    Hd = H * d
+    rq = oracle.rope(Yr[:, :Hd].reshape(-1, H, d), rows[:, None], 8e7)
+    rk = oracle.rope(Yr[:, Hd:2 * Hd].reshape(-1, H, d), rows[:, None], 8e7)
+    assert rel_l2(host_f64(q[0, rows]), rq) <= BF16_REL_L2
+    assert rel_l2(host_f64(k[0, rows]), rk) <= BF16_REL_L2
+    assert rel_l2(host_f64(v[0, rows]), Yr[:, 2 * Hd:3 * Hd].reshape(-1, H, d)) <= BF16_REL_L2
+    assert rel_l2(host_f64(lg[0, rows]), Yr[:, 3 * Hd:]) <= 1e-4
+
+
+def test_qkvg_feeds_the_chunk_kernel(Y):
+    """The projections' outputs go straight into the chunkwise gRet call: the
+    layer (projections + retention) matches the oracle's projections followed
+    by the recurrent form on their bf16-rounded values."""
+    import torch
+    B, N, dm, H, d = 1, 600, 256, 8, 128
+    (X, W), (q, k, v, lg) = qkvg_run(Y, 72, B, N, dm, H, d)
+    o = torch.empty_like(v)
+    S = torch.zeros(B, H, d, d, device="cuda")
+    Y.yoco_gret_prefill_chunkwise(q, k, v, lg, 16.0, o, S)
+    torch.cuda.synchronize()
+    rq, rk, rv, rlg = oracle.qkvg_project(X, W, H, d)
+    rnd = lambda a: synth.bf16_bits_to_f32(synth.f64_to_bf16_bits(a)).astype(np.float64)  # noqa: E731
+    o_ref, _ = oracle.gret_recurrent(rnd(rq), rnd(rk), rnd(rv), rlg.astype(np.float32).astype(np.float64), 16.0)
+    assert rel_l2(host_f64(o), o_ref) <= BF16_REL_L2
+
+
 # ------------------------------------------------------------- CUDA graphs
 
 def test_gret_decode_steps_replayed_from_a_cuda_graph(Y):
