@@ -738,10 +738,12 @@ def qkvg_run(Y, cfg, B, N, dm, H, d, pos0=0, rope_base=0.0):
 
 
 @pytest.mark.parametrize("B,N,dm,H,d,pos0,rope_base", [(2, 300, 256, 8, 128, 0, 0.0), (2, 300, 256, 8, 128, 1000, 5e6),
-                                                       (1, 200, 128, 16, 64, 7, 10000.0)])
+                                                       (1, 200, 128, 16, 64, 7, 10000.0),
+                                                       (1, 100, 192, 8, 64, 0, 0.0)])
 def test_qkvg_project(Y, B, N, dm, H, d, pos0, rope_base):
     """q, k, v (bf16, [B, N, H, d]) and the fp32 gate logits of one GEMM over
     [W_Q | W_K | W_V | W_gamma], with and without rotary encoding; ragged rows
+    (at 100 rows the second 128-row half of the 256-row tile lies wholly past X)
     and a last column tile that is mostly past the matrix."""
     (X, W), (q, k, v, lg) = qkvg_run(Y, 70, B, N, dm, H, d, pos0, rope_base)
     rq, rk, rv, rlg = oracle.qkvg_project(X, W, H, d, pos0, rope_base)
