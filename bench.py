@@ -422,7 +422,10 @@ def run_gpu(args):
                   "achieved": round(cross_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                   "frac": round(cross_gbs / hbm_peak, 4), "algorithmic_bytes_per_launch": cross_bytes,
                   "avg_launch_ms": round(cross_call_ms, 4),
-                  "note": "the 134 MB cache is read by 13 layers in a row and is about the size of L2"}}
+                  "note": ("algorithmic bytes: the whole 134 MB cache per call; the 13 layers read the same "
+                           "cache, and the first keys of each head (half the L2, 64 MB) are loaded with normal "
+                           "L2 priority and the rest evict-first, so about half of each call's bytes come from "
+                           "L2 rather than HBM")}}
 
     # ---- end to end: inputs from pinned host memory, result back to host
     e2e = e2e_measure(args, torch, stream, step, [q, k, v, lg], [M, q1, k1, v1, lg1, M1, Qx, Qd], [Ox[-1], Od[-1]])
