@@ -260,24 +260,53 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
 }
 
 // merge the splits of every query row by log-sum-exp: one CTA per (row, head),
-// thread c owns head dim c
+// thread c owns head dim c.  Every load is independent of the others: the split
+// maxima and sums are read one split per thread, and the weighted sum over splits
+// is unrolled, so the kernel costs a few L2 round trips rather than one per split.
+constexpr int kCombineMaxSplits = 4096;
+
 template <typename T, int D>
 __global__ void __launch_bounds__(D) attn_combine_kernel(const float *__restrict__ part, T *__restrict__ O, int splits) {
+    __shared__ float fs[kCombineMaxSplits];  // m_s, then e^{m_s - M}
+    __shared__ float ls[kCombineMaxSplits];  // l_s
+    __shared__ float red[D / 32];
     // launched as a programmatic dependent of the split kernel: wait for its partials
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    const int w = blockIdx.x, c = threadIdx.x;
+    const int w = blockIdx.x, c = threadIdx.x, lane = c & 31, wid = c >> 5;
     const float *pp = part + (size_t)w * splits * (D + 2);
-    float M = -INFINITY;
-    for (int s = 0; s < splits; ++s) M = fmaxf(M, pp[(size_t)s * (D + 2) + D]);
-    float L = 0.f, A = 0.f;
-    for (int s = 0; s < splits; ++s) {
-        const float *row = pp + (size_t)s * (D + 2);
-        const float ms = row[D];
-        const float f = (ms == -INFINITY) ? 0.f : __expf(ms - M);
-        L += row[D + 1] * f;
-        A += row[c] * f;
+    float mloc = -INFINITY;
+    for (int s = c; s < splits; s += D) {
+        const float m = pp[(size_t)s * (D + 2) + D];
+        fs[s] = m;
+        ls[s] = pp[(size_t)s * (D + 2) + D + 1];
+        mloc = fmaxf(mloc, m);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    if (lane == 0) red[wid] = mloc;
+    __syncthreads();
+    float M = red[0];
+#pragma unroll
+    for (int i = 1; i < D / 32; ++i) M = fmaxf(M, red[i]);
+    __syncthreads();
+    float lloc = 0.f;
+    for (int s = c; s < splits; s += D) {
+        const float ms = fs[s];
+        const float f = (ms == -INFINITY) ? 0.f : __expf(ms - M);
+        fs[s] = f;
+        lloc += ls[s] * f;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
+    if (lane == 0) red[wid] = lloc;
+    __syncthreads();
+    float L = 0.f;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) L += red[i];
+    float A = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < splits; ++s) A += pp[(size_t)s * (D + 2) + c] * fs[s];
     O[(size_t)w * D + c] = from_f32<T>(A / L);
 }
 
@@ -346,6 +375,7 @@ static cudaError_t launch(const AttnArgs &a, int splits, void *ws, cudaStream_t 
     int64_t kps = (keys + splits - 1) / splits;
     kps = ((kps + kAttnTile - 1) / kAttnTile) * kAttnTile;
     splits = (int)((keys + kps - 1) / kps);
+    if (splits > kCombineMaxSplits) return cudaErrorInvalidValue;  // the merge holds one factor per split
     const int nq = (a.T < RB ? a.T : RB) * G;  // query vectors per CTA
     const int rb_eff = (nq <= 4 && a.T <= RB) ? a.T : RB;
     float *part = (float *)((char *)ws + 256);

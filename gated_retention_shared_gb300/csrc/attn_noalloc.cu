@@ -78,6 +78,7 @@ extern "C" YOCO_API yoco_status yoco_cross_attn_decode_noalloc(const void *Q, in
         return reject(YOCO_ERR_INVALID_ARG, "Q, O and cache k/v must be 16-byte aligned");
     if (!isfinite(scale)) return reject(YOCO_ERR_INVALID_ARG, "scale must be finite");
     if (num_splits < 0) return reject(YOCO_ERR_INVALID_ARG, "num_splits must be >= 0");
+    if (num_splits > 4096) return reject(YOCO_ERR_UNSUPPORTED, "num_splits above 4096");
 
     const int64_t keys = cache->len_host;
     int splits = num_splits;

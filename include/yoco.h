@@ -176,7 +176,8 @@ YOCO_API yoco_status yoco_cross_attn_prefill(const void *Q, int Hq, int T, int64
  * Cross-decoder attention for the newest token of each sequence (position
  * len - 1, so it reads every slot including its own, which the preceding
  * append wrote).  Split-KV: num_splits slices of the cache are reduced in
- * parallel and merged by log-sum-exp; 0 = automatic.
+ * parallel and merged by log-sum-exp; 0 = automatic, at most 4096 (more
+ * returns YOCO_ERR_UNSUPPORTED).
  *   Q, O [B, Hq, d] cache dtype.   Requires len >= 1.
  */
 YOCO_API yoco_status yoco_cross_attn_decode(const void *Q, int Hq, const yoco_kv_cache *cache,
@@ -198,8 +199,8 @@ YOCO_API yoco_status yoco_cross_attn_decode(const void *Q, int Hq, const yoco_kv
  *     before capturing any stream on that device.
  *   - num_splits = 0 picks the usual split count, lowered until the partial
  *     results fit in 4 MiB.  An explicit num_splits whose partials
- *     (B * Hq * num_splits * (d + 2) * 4 bytes) do not fit returns
- *     YOCO_ERR_UNSUPPORTED and launches nothing.
+ *     (B * Hq * num_splits * (d + 2) * 4 bytes) do not fit, or above 4096,
+ *     returns YOCO_ERR_UNSUPPORTED and launches nothing.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents (every partial read is first written by the same call, so
  *     nothing needs clearing).  Calls that overlap on the GPU, e.g. on two

@@ -413,6 +413,25 @@ def test_cross_attn_decode_split_invariance(Y):
         assert rel_l2(r, results[0]) <= 1e-2
 
 
+@pytest.mark.parametrize("dtype,d,length,splits", [("bf16", 128, 40000, 300), ("f32", 64, 9000, 100)])
+def test_cross_attn_decode_more_splits_than_merge_threads(Y, dtype, d, length, splits):
+    """The log-sum-exp merge runs d threads per query row; with more splits than
+    threads each thread gathers several splits' maxima and sums (tensor-core and
+    CUDA-core split kernels)."""
+    import torch
+    B, Hq, Hkv = 1, 6, 2
+    K, V, cache = fill_cache(Y, B, Hkv, d, length, length, dtype, 36)
+    Q, Qd = gen(SEED, sid(36, 2, synth.T_QX), (B, Hq, d), dtype)
+    O_ref = oracle.cross_attn(Q[:, None], K, V, length - 1, d ** -0.5)[:, 0]
+    O = torch.empty_like(Qd)
+    Y.yoco_cross_attn_decode(Qd, cache, O, num_splits=splits)
+    torch.cuda.synchronize()
+    if dtype == "bf16":
+        assert rel_l2(host_f64(O), O_ref) <= BF16_REL_L2
+    else:
+        assert max_abs(host_f64(O), O_ref) <= FP32_MAX_ABS
+
+
 def test_cross_attn_decode_garbage_workspace_twice(Y):
     """Decode needs no clean workspace: one full of arbitrary bytes (status
     word aside) gives the oracle's result, and so does a second call on it."""

@@ -68,3 +68,19 @@ def test_noalloc_decode_refuses_oversized_split_count(Y):
     assert b"scratch" in Y.lib.yoco_last_error()
     torch.cuda.synchronize()
     assert bool((O == 0).all())
+
+
+def test_noalloc_decode_refuses_more_than_4096_splits(Y):
+    """The merge holds one factor per split, at most 4096; a count above that
+    is refused even when its partials would fit the scratch."""
+    import torch
+    B, Hq, Hkv, d, length = 1, 1, 1, 64, 3001
+    cache = _cache(Y, B, Hkv, d, length)
+    Qd = torch.zeros(B, Hq, d, dtype=torch.bfloat16, device="cuda")
+    O = torch.zeros_like(Qd)
+    st = Y.lib.yoco_cross_attn_decode_noalloc(ctypes.c_void_p(Qd.data_ptr()), Hq, ctypes.byref(cache.c), 0.1,
+                                              5000, ctypes.c_void_p(O.data_ptr()), None)
+    assert st == Y.YOCO_ERR_UNSUPPORTED
+    assert b"4096" in Y.lib.yoco_last_error()
+    torch.cuda.synchronize()
+    assert bool((O == 0).all())
