@@ -141,7 +141,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const float *__restrict__ logits, float inv_tau,
                bf16_t *__restrict__ o, float *__restrict__ state, float *__restrict__ E, float *__restrict__ G,
-               int N, int H, int seg_len, int P, int *err) {
+               int *__restrict__ seg0_read, int N, int H, int seg_len, int P, int *err) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_u32 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base_u32 & 1023u)) & 1023u;
@@ -153,7 +153,19 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (tid == 0 && err) atomicExch(err, (int)(kErrMagic | 9u));
         return;
     }
-    const int p = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // OUTPUT: segment-major linear grid (the segment-0 CTAs, which need nothing from
+    // the SEG_STATE grid, are dispatched first); SEG_STATE: (segment, head, sequence)
+    int p, h, b;
+    if (MODE == MODE_OUTPUT) {
+        const int BH = (int)gridDim.x / P, r = (int)blockIdx.x % BH;
+        p = (int)blockIdx.x / BH;
+        h = r % H;
+        b = r / H;
+    } else {
+        p = blockIdx.x;
+        h = blockIdx.y;
+        b = blockIdx.z;
+    }
     const int t_begin = p * seg_len;
     const int t_end = min(N, t_begin + seg_len);
     const int nchunks = (t_end - t_begin + kC - 1) / kC;
@@ -205,7 +217,17 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // producer reads q, k, v at once, which is safe because everything before this
     // grid has completed by then.  OUTPUT lets the next kernel (the next call's
     // SEG_STATE) start its prologue on idle SMs right away; that kernel waits too.
-    if (MODE == MODE_SEG_STATE) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (MODE == MODE_SEG_STATE) {
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        // this call's "segment 0 holds the initial state" flag starts cleared; the
+        // OUTPUT grid, which sets and reads it, starts only after every CTA here has
+        // passed this point
+        if (p == 0 && tid == 0) {
+            *reinterpret_cast<volatile int *>(seg0_read + bh) = 0;
+            __threadfence();
+        }
+        __syncthreads();
+    }
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     // chunk order: OUTPUT forwards, SEG_STATE backwards (running suffix decay)
@@ -433,16 +455,18 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         if (MODE == MODE_OUTPUT) {
             float S[kD];  // row t of the state, fp32
-            // inputs of this pass written by the SEG_STATE grid: wait for it (no-op without one)
-            asm volatile("griddepcontrol.wait;\n" ::: "memory");
+            // Segment 0 starts from the caller's state and reads it directly, so it runs
+            // alongside the SEG_STATE grid; later segments need that grid's end states
+            // (and its copy of the caller's state): they wait for it
+            if (p > 0) asm volatile("griddepcontrol.wait;\n" ::: "memory");
             {
                 // initial state of this segment: the caller's state, advanced over the
                 // earlier segments with their zero-start end states E_q and decays G_q
-                const float *init = (P == 1) ? state + bh * kD * kD : E + (bh * P + P - 1) * kD * kD;
+                const float *init = (p == 0) ? state + bh * kD * kD : E + (bh * P + P - 1) * kD * kD;
                 const float4 *src = reinterpret_cast<const float4 *>(init + (size_t)t * kD);
 #pragma unroll
                 for (int c4 = 0; c4 < kD / 4; ++c4) {
-                    const float4 x = src[c4];
+                    const float4 x = __ldcg(src + c4);
                     S[4 * c4] = x.x; S[4 * c4 + 1] = x.y; S[4 * c4 + 2] = x.z; S[4 * c4 + 3] = x.w;
                 }
 #pragma unroll 1
@@ -470,7 +494,14 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             };
             put_state();
             named_bar(2, 128);
-            if (t == 0) mbar_arrive(&sm.s_ready);
+            if (t == 0) {
+                mbar_arrive(&sm.s_ready);
+                // the caller's state is in registers now: the last segment may overwrite it
+                if (p == 0 && P > 1) {
+                    __threadfence();
+                    atomicExch(seg0_read + bh, 1);
+                }
+            }
             float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), t) : 0.f;
             for (int i = 0; i < nchunks; ++i) {
                 const int s = i % NS;
@@ -549,6 +580,26 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             named_bar(2, 128);
             if (t == 0) sm.go0 = !*abort_flag;
             named_bar(2, 128);
+            if (p == P - 1 && sm.go0 && P > 1) {
+                // segment 0 of this (b, h) must have read the caller's state first
+                if (t == 0) {
+                    bool seen = false;
+                    uint64_t t0;
+                    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+                    for (uint32_t it = 0; !seen; ++it) {
+                        seen = *reinterpret_cast<volatile int *>(seg0_read + bh) == 1;
+                        if (!seen && (it & 63) == 63) {
+                            uint64_t tn;
+                            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tn));
+                            if (*abort_flag || tn - t0 > 2000000000ull) break;
+                        }
+                    }
+                    if (!seen) report(err, &sm.abort_flag, 11);
+                    __threadfence();
+                    sm.go0 = seen;
+                }
+                named_bar(2, 128);
+            }
             if (p == P - 1 && sm.go0) {  // the last segment's end state is the call's final state
                 float4 *dst = reinterpret_cast<float4 *>(state + bh * kD * kD + (size_t)t * kD);
 #pragma unroll
@@ -659,7 +710,7 @@ size_t gret_tc_workspace(int B, int N, int H, int dk, int dv) {
     (void)dk; (void)dv;
     int P = tc_segments(B, N, H);
     size_t ws = 256;  // status word
-    if (P > 1) ws += ((size_t)B * H * P * kD * kD + (size_t)B * H * P) * sizeof(float);
+    if (P > 1) ws += ((size_t)B * H * P * kD * kD + (size_t)B * H * P) * sizeof(float) + (size_t)B * H * sizeof(int);
     return ws;
 }
 
@@ -674,6 +725,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     int *err = (int *)ws;
     float *E = (float *)((char *)ws + 256);
     float *G = E + (size_t)a.B * a.H * P * kD * kD;
+    int *seg0_read = reinterpret_cast<int *>(G + (size_t)a.B * a.H * P);
     const float inv_tau = 1.0f / a.tau;
     cudaError_t e;
     e = cudaFuncSetAttribute(gret_tc_kernel<MODE_OUTPUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
@@ -683,8 +735,8 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (P == 1) {
         count_launches(1);
-        gret_tc_kernel<MODE_OUTPUT><<<dim3(1, a.H, a.B), kTcThreads, kTcSmemBytes, st>>>(
-            mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, a.N, a.H, seg_len, 1, err);
+        gret_tc_kernel<MODE_OUTPUT><<<dim3(a.B * a.H), kTcThreads, kTcSmemBytes, st>>>(
+            mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err);
         return cudaGetLastError();
     }
     // end states of segments 0 .. P-2 (the last segment's is computed by the OUTPUT pass)
@@ -702,13 +754,14 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     // before reading anything
     cfg.gridDim = dim3(P - 1, a.H, a.B);
     e = cudaLaunchKernelEx(&cfg, gret_tc_kernel<MODE_SEG_STATE>, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)nullptr,
-                           a.state, E, G, a.N, a.H, seg_len, P, err);
+                           a.state, E, G, seg0_read, a.N, a.H, seg_len, P, err);
     if (e != cudaSuccess) return e;
-    // OUTPUT may begin (TMA loads, first MMAs) while SEG_STATE drains; its state
-    // warps wait for SEG_STATE before touching E, G and `state`
-    cfg.gridDim = dim3(P, a.H, a.B);
+    // OUTPUT starts on the SMs SEG_STATE leaves free: its segment-0 CTAs (first in
+    // the grid) run the whole segment meanwhile; the others begin loading and wait
+    // for SEG_STATE before touching E, G and `state`
+    cfg.gridDim = dim3(P * a.B * a.H);
     return cudaLaunchKernelEx(&cfg, gret_tc_kernel<MODE_OUTPUT>, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o,
-                              a.state, E, G, a.N, a.H, seg_len, P, err);
+                              a.state, E, G, seg0_read, a.N, a.H, seg_len, P, err);
 }
 
 }  // namespace yoco_host

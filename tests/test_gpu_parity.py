@@ -170,6 +170,34 @@ def test_gret_prefill_state_continuation(Y):
     assert rel_l2(S.cpu().numpy(), S_ref) <= BF16_REL_L2
 
 
+def test_gret_prefill_two_calls_on_one_dirty_workspace(Y):
+    """Two chained calls (the second continues the first's final state) on one
+    workspace that starts as int32 ones (status word aside): segment 0 of each
+    (b, h) starts from the caller's state while the first pass runs, and the last
+    segment overwrites that state only after segment 0 has read it (16 segments
+    per head here, with a nonzero initial state)."""
+    import torch
+    B, N, H, d = 1, 4000, 8, 128
+    host, dev = gret_inputs(37, B, N, H, d, "bf16", logit_mean=2.0)
+    S0 = synth.normal(SEED, sid(37, 1, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
+    n1 = 2048
+    nbytes = max(256, Y.yoco_gret_prefill_workspace_size(B, max(n1, N - n1), H, d, d, 0, Y.YOCO_BF16))
+    ws = torch.ones((nbytes + 3) // 4, dtype=torch.int32, device="cuda").view(torch.uint8)[:nbytes]
+    ws[:256] = 0
+    S = dev_f32(S0)
+    outs = []
+    for sl in (slice(0, n1), slice(n1, N)):
+        qd, kd, vd, lgd = (t[:, sl].contiguous() for t in dev)
+        o = torch.empty_like(vd)
+        Y.yoco_gret_prefill_chunkwise(qd, kd, vd, lgd, 16.0, o, S, workspace=ws)
+        outs.append(o)
+    torch.cuda.synchronize()
+    Y.yoco_workspace_status(ws)
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0, S0=S0)
+    assert rel_l2(np.concatenate([host_f64(o) for o in outs], axis=1), o_ref) <= BF16_REL_L2
+    assert rel_l2(S.cpu().numpy().astype(np.float64), S_ref) <= BF16_REL_L2
+
+
 def test_gret_prefill_gate_limits(Y):
     """Logits of +inf (gamma = 1) and -inf (gamma = 0) mixed in."""
     B, N, H, d = 1, 300, 2, 64
