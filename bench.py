@@ -54,6 +54,10 @@ def parse():
                    help="--only cross_decode: cache length (default: the step's prompt length)")
     p.add_argument("--batch", type=int, default=0, help="--only cross_decode: sequences (default: the step's B)")
     p.add_argument("--splits", type=int, default=0, help="--only cross_decode: key splits (default: automatic)")
+    p.add_argument("--workload", choices=list(LONG_WORKLOADS), default=None,
+                   help="time one of the long-context workloads at the pages' sizes instead of the bench step "
+                        "(one JSON line per workload and batch; not the driver's line)")
+    p.add_argument("--batches", default="1,8,32", help="--workload decode128k: batch sizes")
     p.add_argument("--rope-base", type=float, default=0.0,
                    help="--only proj/cross_decode/cross_prefill: rotary encoding base of the cache (0: off)")
     return p.parse_args()
@@ -672,9 +676,208 @@ def run_only(args):
     print(json.dumps(line))
 
 
+# ------------------------------------------------- long-context workloads
+
+LONG_WORKLOADS = {
+    # 13 gRet layers over a 512K-token prompt, the shared-K/V projection, and the
+    # cross layers for the last prompt row only (early exit)
+    "prefill512k_early_exit": 4,
+    # 13 cross layers per generated token over a 128K-token shared cache, one
+    # append per token, B sequences with their own caches
+    "decode128k": 3,
+    # 1M-token context: 13 recurrent gRet steps, one append, 13 cross layers per token
+    "decode1m": 5,
+}
+
+
+def run_workload(args):
+    """Time a long-context workload; prints one JSON line per workload (and batch).
+
+    Roofline time of a step: the bytes every memory-bound call must move at the
+    measured HBM copy rate plus the projection's flops at the measured bf16 rate;
+    `frac_of_roofline` = that time / the measured step time."""
+    import torch
+
+    import gated_retention_shared_gb300 as Y
+    import synth
+    L = Y.lib
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    bf, f32 = torch.bfloat16, torch.float32
+    sid = synth.stream_id
+    cfg = LONG_WORKLOADS[args.workload]
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    stream = torch.cuda.current_stream(dev)
+    stp = ctypes.c_void_p(stream.cuda_stream)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        peaks = {}
+    hbm = peaks.get("hbm_gbs", 6800.0) * 1e9
+    tc = peaks.get("bf16_tflops", 1900.0) * 1e12
+
+    def normal(shape, dtype, stream_tag, mean=0.0, std=1.0):
+        return synth.fill_normal_(torch.empty(shape, dtype=dtype, device=dev), SEED, stream_tag, mean, std)
+
+    def check(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: {L.yoco_last_error().decode()}")
+
+    def timed(step, steps, warmup):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        clk = Clocks(0).__enter__()
+        clk.wait_first()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_lo = time.monotonic()
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_hi = time.monotonic()
+        time.sleep(0.12)
+        clk.__exit__(None, None, None)
+        c = clk.summary(t_lo - 0.1, t_hi + 0.1)
+        c["window_ms"] = round((t_hi - t_lo) * 1e3, 1)
+        return e0.elapsed_time(e1) / steps, c
+
+    lines = []
+    cache_bytes_per_key = HKV * D * 2 * 2  # K^ and V^ of one position, bf16
+    if args.workload == "prefill512k_early_exit":
+        Nl = 524288
+        q = [normal((1, Nl, H, D), bf, sid(cfg, l, synth.T_Q), std=D ** -0.5) for l in range(L_SELF)]
+        k = [normal((1, Nl, H, D), bf, sid(cfg, l, synth.T_K), std=D ** -0.5) for l in range(L_SELF)]
+        v = [normal((1, Nl, H, D), bf, sid(cfg, l, synth.T_V)) for l in range(L_SELF)]
+        lg = [normal((1, Nl, H), f32, sid(cfg, l, synth.T_LOGIT), mean=2.0) for l in range(L_SELF)]
+        M = normal((1, Nl, DM), bf, sid(cfg, 0, synth.T_M))
+        Wk = normal((DM, HKV * D), bf, sid(cfg, 0, synth.T_WK), std=0.02)
+        Wv = normal((DM, HKV * D), bf, sid(cfg, 0, synth.T_WV), std=0.02)
+        Qx = [normal((1, 1, HQ, D), bf, sid(cfg, l, synth.T_QX)) for l in range(L_CROSS)]
+        o = torch.empty(1, Nl, H, D, dtype=bf, device=dev)  # each layer's output, consumed before the next
+        S = [torch.zeros(1, H, D, D, dtype=f32, device=dev) for _ in range(L_SELF)]
+        Ox = [torch.empty(1, 1, HQ, D, dtype=bf, device=dev) for _ in range(L_CROSS)]
+        cache = Y.KVCache(1, HKV, D, Nl + 16, device=dev)
+        cc = ctypes.byref(cache.c)
+        ws = torch.empty(max(L.yoco_gret_prefill_workspace_size(1, Nl, H, D, D, 0, Y.YOCO_BF16),
+                             L.yoco_shared_kv_workspace_size(1, Nl, DM, cc),
+                             L.yoco_cross_attn_workspace_size(1, HQ, 1, cc, 0), 256), dtype=torch.uint8, device=dev)
+        wsp, wsn = P(ws), ws.numel()
+        gret_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+        def step():
+            for s_ in S:
+                s_.zero_()
+            cache.len_dev.zero_()
+            cache.c.len_host = 0
+            gret_ev[0].record(stream)
+            for l in range(L_SELF):
+                check(L.yoco_gret_prefill_chunkwise(P(q[l]), P(k[l]), P(v[l]), P(lg[l]), TAU, P(o), P(S[l]), 1, Nl,
+                                                    H, D, D, 0, 1, 1, wsp, wsn, stp), "gret prefill")
+            gret_ev[1].record(stream)
+            check(L.yoco_shared_kv_project_append(P(M), None, EPS, P(Wk), P(Wv), Nl, DM, cc, wsp, wsn, stp), "kv")
+            for l in range(L_CROSS):
+                check(L.yoco_cross_attn_prefill(P(Qx[l]), HQ, 1, Nl - 1, cc, D ** -0.5, P(Ox[l]), wsp, wsn, stp),
+                      "cross prefill")
+
+        ms, clocks = timed(step, args.steps, args.warmup)
+        gret_ms = gret_ev[0].elapsed_time(gret_ev[1]) / L_SELF  # the last timed step's 13 calls
+        gret_bytes = 4 * Nl * H * D * 2 + Nl * H * 4 + 2 * H * D * D * 4
+        proj_flops = 2.0 * Nl * DM * 2 * HKV * D
+        cross_bytes = Nl * cache_bytes_per_key
+        roof_ms = (L_SELF * gret_bytes / hbm + proj_flops / tc + L_CROSS * cross_bytes / hbm) * 1e3
+        lines.append({
+            "workload": "yoco3b_prefill512k_early_exit", "metric": "prompt tok/s", "value": Nl / (ms / 1e3),
+            "unit": "tok/s", "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
+            "data": "synthetic", "config": {"B": 1, "N": Nl, "self_layers": L_SELF, "gret_heads": H, "d": D,
+                                            "d_model": DM, "Hq": HQ, "Hkv": HKV, "cross_rows": 1},
+            "roofline_ms": round(roof_ms, 3), "frac_of_roofline": round(roof_ms / ms, 4),
+            "roofline_gret": {"bound": "hbm", "achieved": round(gret_bytes / (gret_ms / 1e3) / 1e9, 1),
+                              "peak": hbm / 1e9, "unit": "GB/s", "frac": round(gret_bytes / (gret_ms / 1e3) / hbm, 4),
+                              "algorithmic_bytes_per_launch": gret_bytes, "avg_launch_ms": round(gret_ms, 4)},
+            "clocks": clocks})
+    else:
+        one_m = args.workload == "decode1m"
+        Nc = 1048576 if one_m else 131072
+        extra = 256 if one_m else 1024
+        batches = [1] if one_m else [int(x) for x in args.batches.split(",")]
+        assert args.warmup + args.steps <= extra, "the cache holds the prompt plus this many generated tokens"
+        Wk = normal((DM, HKV * D), bf, sid(cfg, 0, synth.T_WK), std=0.02)
+        Wv = normal((DM, HKV * D), bf, sid(cfg, 0, synth.T_WV), std=0.02)
+        for Bc in batches:
+            Kc = normal((Bc, HKV, Nc + extra, D), bf, sid(cfg, 0, synth.T_CACHE_K))
+            Vc = normal((Bc, HKV, Nc + extra, D), bf, sid(cfg, 0, synth.T_CACHE_V))
+            cache = Y.KVCache(Bc, HKV, D, Nc + extra, k=Kc, v=Vc)
+            cache.set_length(Nc)
+            cc = ctypes.byref(cache.c)
+            M1 = normal((Bc, 1, DM), bf, sid(cfg, 0, synth.T_M, 1))
+            Qd = [normal((Bc, HQ, D), bf, sid(cfg, l, synth.T_QX, 1)) for l in range(L_CROSS)]
+            Od = [torch.empty(Bc, HQ, D, dtype=bf, device=dev) for _ in range(L_CROSS)]
+            ws = torch.empty(max(L.yoco_shared_kv_workspace_size(Bc, 1, DM, cc),
+                                 L.yoco_cross_attn_workspace_size(Bc, HQ, 1, cc, 0), 256), dtype=torch.uint8,
+                             device=dev)
+            wsp, wsn = P(ws), ws.numel()
+            graph = None
+            if one_m:
+                q1 = [normal((Bc, H, D), bf, sid(cfg, l, synth.T_Q, 1), std=D ** -0.5) for l in range(L_SELF)]
+                k1 = [normal((Bc, H, D), bf, sid(cfg, l, synth.T_K, 1), std=D ** -0.5) for l in range(L_SELF)]
+                v1 = [normal((Bc, H, D), bf, sid(cfg, l, synth.T_V, 1)) for l in range(L_SELF)]
+                lg1 = [normal((Bc, H), f32, sid(cfg, l, synth.T_LOGIT, 1), mean=2.0) for l in range(L_SELF)]
+                S1 = [normal((Bc, H, D, D), f32, sid(cfg, l, synth.T_S0), std=0.05) for l in range(L_SELF)]
+                o1 = [torch.empty(Bc, H, D, dtype=bf, device=dev) for _ in range(L_SELF)]
+
+                def gret_layers(sp):
+                    for l in range(L_SELF):
+                        check(L.yoco_gret_decode_step(P(q1[l]), P(k1[l]), P(v1[l]), P(lg1[l]), TAU, P(S1[l]),
+                                                      P(o1[l]), Bc, H, D, D, 1, 1, sp), "gret decode")
+                gret_layers(stp)
+                torch.cuda.synchronize()
+                cap = torch.cuda.Stream(dev)
+                cap.wait_stream(stream)
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=cap):
+                    gret_layers(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+                stream.wait_stream(cap)
+                torch.cuda.synchronize()
+
+            def step():
+                if graph is not None:
+                    graph.replay()  # the 13 recurrent gRet steps
+                check(L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, cc, wsp, wsn, stp),
+                      "append")
+                for l in range(L_CROSS):
+                    check(L.yoco_cross_attn_decode(P(Qd[l]), HQ, cc, D ** -0.5, 0, P(Od[l]), wsp, wsn, stp),
+                          "cross decode")
+
+            ms, clocks = timed(step, args.steps, args.warmup)
+            ctx = Nc + args.warmup + args.steps / 2  # mean cache length over the timed tokens
+            step_bytes = L_CROSS * Bc * ctx * cache_bytes_per_key + 2 * DM * HKV * D * 2
+            if one_m:
+                step_bytes += L_SELF * Bc * H * D * D * 4 * 2
+            roof_ms = step_bytes / hbm * 1e3
+            lines.append({
+                "workload": ("yoco3b_decode1m" if one_m else f"shared_kv_decode128k_b{Bc}"),
+                "metric": "generated tok/s", "value": Bc / (ms / 1e3), "unit": "tok/s", "ms_per_step": ms,
+                "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+                "config": {"B": Bc, "context": Nc, "cross_layers": L_CROSS, "Hq": HQ, "Hkv": HKV, "d": D,
+                           "self_layers": L_SELF if one_m else 0},
+                "roofline": {"bound": "hbm", "achieved": round(step_bytes / (ms / 1e3) / 1e9, 1),
+                             "peak": hbm / 1e9, "unit": "GB/s", "frac": round(step_bytes / (ms / 1e3) / hbm, 4),
+                             "algorithmic_bytes_per_step": int(step_bytes)},
+                "roofline_ms": round(roof_ms, 4), "frac_of_roofline": round(roof_ms / ms, 4), "clocks": clocks})
+            del Kc, Vc, cache
+            torch.cuda.empty_cache()
+    for line in lines:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
-    if args.only:
+    if args.workload:
+        run_workload(args)
+    elif args.only:
         run_only(args)
     elif args.impl == "reference":
         run_reference(args)
