@@ -59,7 +59,7 @@ enum : int { MODE_OUTPUT = 0, MODE_SEG_STATE = 1 };
 
 struct TcSmem {
     uint64_t full[kStagesSeg], empty[kStagesSeg], pq_ready[kStagesSeg], o_free[2], bc_ready[2], o_full[2];
-    uint64_t full_v[kStages], vfree[kStages], k_ready[kStages], w_ready[kStagesSeg];
+    uint64_t full_v[kStages], o_staged[kStages], k_ready[kStages], w_ready[kStagesSeg];
     uint64_t as_full, p_free, u_full, u_free, s_ready, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -190,7 +190,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             mbar_init(&sm.bc_ready[s], 1);
             mbar_init(&sm.o_full[s], 1);
             mbar_init(&sm.full_v[s], 1);
-            mbar_init(&sm.vfree[s], 1);
+            mbar_init(&sm.o_staged[s], 1);
             mbar_init(&sm.k_ready[s], 1);
         }
         mbar_init(&sm.as_full, 1);
@@ -244,15 +244,32 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane == 0) {
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            if (MODE == MODE_OUTPUT) tma_prefetch_desc(&tm_q);
+            if (MODE == MODE_OUTPUT) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_o);
+            }
             // every q, k, v line is read once per pass and every o line written once:
             // all of them are marked first to leave L2 (measured: 0.235 -> 0.221 ms per
             // 32K x 24 x 128 layer; keeping the SEG_STATE tiles for the OUTPUT pass with
             // evict-last was slower at every fraction of L2 tried)
             const uint64_t pol = l2_policy_evict_first();
-            // OUTPUT: Q and K complete `full`, V completes `full_v` (the V slot doubles as
-            // the staging buffer of the output store two chunks back).  SEG_STATE: K and
-            // V complete `full`.
+            // OUTPUT: Q and K complete `full`, V completes `full_v`.  The V slot doubles as
+            // the staging buffer of the output rows of the chunk NS back: this thread
+            // stores them (TMA) and waits for the store to read the slot before it loads
+            // the next V there, so the state warps never wait on a store.  SEG_STATE: K
+            // and V complete `full`.
+            auto store_out = [&](int c) {  // chunk c's staged output rows -> o
+                const int sc_ = c % NS;
+                if (!mbar_wait(&sm.o_staged[sc_], (c / NS) & 1, abort_flag)) {
+                    report(err, &sm.abort_flag, 8);
+                    return false;
+                }
+                const int nc = chunk_start(c);
+                tma_store_4d_hint(&tm_o, stage_v(sc_), 0, h, nc, b, pol);
+                tma_store_4d_hint(&tm_o, stage_v(sc_) + kHalf, 64, h, nc, b, pol);
+                bulk_commit_group();
+                return true;
+            };
             for (int i = 0; i < nchunks; ++i) {
                 const int s = i % NS;
                 if (i >= NS && !mbar_wait(&sm.empty[s], ((i / NS) + 1) & 1, abort_flag)) {
@@ -269,9 +286,9 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tma_load_4d_hint(stage_v(s) + half * kHalf, &tm_v, &sm.full[s], half * 64, h, n0, b, pol);
                 }
                 if (MODE == MODE_OUTPUT) {
-                    if (i >= NS && !mbar_wait(&sm.vfree[s], ((i / NS) + 1) & 1, abort_flag)) {
-                        report(err, &sm.abort_flag, 8);
-                        break;
+                    if (i >= NS) {
+                        if (!store_out(i - NS)) break;
+                        bulk_wait_read_all();  // the slot has been read: V(i) may land in it
                     }
                     mbar_arrive_expect_tx(&sm.full_v[s], kTile);
                     for (int half = 0; half < 2; ++half)
@@ -282,6 +299,12 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int i = max(0, nchunks - NS); i < nchunks; ++i) {
                 mbar_wait(&sm.full[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
                 if (MODE == MODE_OUTPUT) mbar_wait(&sm.full_v[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
+            }
+            if (MODE == MODE_OUTPUT) {
+                // the output rows of the last NS chunks, then every store complete before exit
+                for (int c = max(0, nchunks - NS); c < nchunks && !*abort_flag; ++c)
+                    if (!store_out(c)) break;
+                bulk_wait_all();
             }
         }
     } else if (warp == 9) {
@@ -536,7 +559,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (i + 1 < nchunks) mbar_arrive(&sm.s_ready);
                 }
                 // output rows o_t = e^{b_t} O_t (or O_t), staged as bf16 in this chunk's
-                // V slot (free once MMA2 is done) and written by two TMA stores
+                // V slot (free once MMA2 is done); the TMA producer thread stores them
                 if (t == 0) {
                     ok = mbar_wait(&sm.o_full[i & 1], (i / 2) & 1, abort_flag);
                     if (!ok) report(err, &sm.abort_flag, 6);
@@ -546,7 +569,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (!sm.go0) break;
                 tc_fence_after();
                 {
-                    const int n0 = chunk_start(i);
                     uint8_t *stage_o = stage_v(s);
                     const uint32_t o_t = tmem + kColO + 128 * (i & 1) + lane_base;
 #pragma unroll 1
@@ -567,16 +589,10 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     named_bar(2, 128);
                     if (t == 0) {
                         mbar_arrive(&sm.o_free[i & 1]);
-                        const uint64_t pol_o = l2_policy_evict_first();
-                        tma_store_4d_hint(&tm_o, stage_o, 0, h, n0, b, pol_o);
-                        tma_store_4d_hint(&tm_o, stage_o + kHalf, 64, h, n0, b, pol_o);
-                        bulk_commit_group();
-                        bulk_wait_read_all();
-                        mbar_arrive(&sm.vfree[s]);
+                        mbar_arrive(&sm.o_staged[s]);  // the TMA producer stores the rows
                     }
                 }
             }
-            if (t == 0) bulk_wait_all();  // output stores complete before exit
             named_bar(2, 128);
             if (t == 0) sm.go0 = !*abort_flag;
             named_bar(2, 128);
