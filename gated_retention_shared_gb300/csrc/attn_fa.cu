@@ -77,6 +77,32 @@ __device__ __forceinline__ float fa_ex2(float x) {  // 2^x, hardware approximati
     return y;
 }
 
+// Two fp32 values in one 64-bit register, for the packed f32x2 arithmetic of sm_100+
+// (one instruction for two lanes' worth of work: the softmax loop is issue-bound).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __global__ void __launch_bounds__(kFThreads, 1)
 attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o, int T, int Hq,
@@ -284,25 +310,24 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const int64_t key0 = (int64_t)(j_lo + i) * kFK;
             // every row of the set sees every key of this tile: no per-element mask
             const bool full = (key0 + kFK - 1 <= set_lo) && (window <= 0 || key0 >= set_lo + kFK - 1 - window + 1);
+            // maximum of the raw scores (the scale is positive: it is applied once, to the
+            // maximum, and folded into each exponent's argument below)
             float mt = -INFINITY;
             if (full) {
 #pragma unroll
-                for (int c = 0; c < kFK; ++c) {
-                    const float v = __uint_as_float(sv[c]) * c2;
-                    sv[c] = __float_as_uint(v);
-                    mt = fmaxf(mt, v);
-                }
+                for (int c = 0; c < kFK; c += 2) mt = fmax3(mt, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
             } else {
                 const int64_t first = (window > 0) ? pos - window + 1 : 0;
                 const int lo_c = (int)max((int64_t)0, min((int64_t)kFK, first - key0));
                 const int hi_c = (int)max((int64_t)0, min((int64_t)kFK, pos + 1 - key0));
 #pragma unroll
                 for (int c = 0; c < kFK; ++c) {
-                    const float v = (c >= lo_c && c < hi_c) ? __uint_as_float(sv[c]) * c2 : -INFINITY;
+                    const float v = (c >= lo_c && c < hi_c) ? __uint_as_float(sv[c]) : -INFINITY;
                     sv[c] = __float_as_uint(v);
                     mt = fmaxf(mt, v);
                 }
             }
+            mt *= c2;  // -inf stays -inf
             // move the reference maximum only when this tile passes it by more than the gap
             float alpha = 1.f;
             const bool move = (mt > m_ref + kRescaleGap2) || (m_ref == -INFINITY && mt > -INFINITY);
@@ -313,19 +338,27 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;  // a row with nothing seen yet: every p is 0
             // P as packed bf16 over the first 64 columns of S (keys 2c, 2c+1 in column c; every
             // S value is already in registers), 32 keys at a time
-            float ls = 0.f;
+            // per key pair: both exponent arguments s c2 - mu in one packed FMA, the row sum
+            // in a packed accumulator (masked scores are -inf and give exactly 0)
+            const uint64_t c2x2 = f2_pack(c2, c2), nmu2 = f2_pack(-mu, -mu);
+            uint64_t acc2 = f2_pack(0.f, 0.f);
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int c2i = 0; c2i < 16; ++c2i) {
-                    const float e0 = fa_ex2(__uint_as_float(sv[32 * cb + 2 * c2i]) - mu);
-                    const float e1 = fa_ex2(__uint_as_float(sv[32 * cb + 2 * c2i + 1]) - mu);
-                    ls += e0 + e1;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[32 * cb + 2 * c2i]),
+                                             __uint_as_float(sv[32 * cb + 2 * c2i + 1])), c2x2, nmu2), x0, x1);
+                    const float e0 = fa_ex2(x0), e1 = fa_ex2(x1);
+                    acc2 = f2_add(acc2, f2_pack(e0, e1));
                     pk[c2i] = fa_pack_bf16x2(e0, e1);
                 }
                 tmem_st16(s_t + cb * 16, pk);
             }
+            float ls0, ls1;
+            f2_unpack(acc2, ls0, ls1);
+            const float ls = ls0 + ls1;
             l = fmaf(l, alpha, ls);
             tmem_wait_st();
             // O_X holds tiles < i; rows whose reference moved rescale it before P V of tile i
