@@ -423,32 +423,51 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 named_bar(1, 128);
                 if (j == 0) mbar_arrive(&sm.k_ready[s]);
                 tc_fence_after();
-                // P row j over A row j, written in place as packed bf16 (keys 2c, 2c+1 in column c)
+                // P row j over A row j, written in place as packed bf16 (keys 2c, 2c+1 in column c).
+                // The 32 rows of warp wq end in key block wq: blocks before it need no mask,
+                // blocks after it are zero and are not loaded.
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + kColA + lane_base + cb * 32, r);
-                    tmem_wait_ld();
                     uint32_t pk[16];
-                    if (factor) {
+                    if (cb > wq) {
 #pragma unroll
-                        for (int e4 = 0; e4 < 8; ++e4) {
-                            const int k0 = cb * 32 + 4 * e4;
-                            const float4 w = *reinterpret_cast<const float4 *>(&sm.ew[k0]);
-                            const float v0 = (k0 <= j) ? __uint_as_float(r[4 * e4]) * w.x : 0.f;
-                            const float v1 = (k0 + 1 <= j) ? __uint_as_float(r[4 * e4 + 1]) * w.y : 0.f;
-                            const float v2 = (k0 + 2 <= j) ? __uint_as_float(r[4 * e4 + 2]) * w.z : 0.f;
-                            const float v3 = (k0 + 3 <= j) ? __uint_as_float(r[4 * e4 + 3]) * w.w : 0.f;
-                            pk[2 * e4] = pack_bf16x2(v0, v1);
-                            pk[2 * e4 + 1] = pack_bf16x2(v2, v3);
-                        }
+                        for (int e = 0; e < 16; ++e) pk[e] = 0u;
                     } else {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + kColA + lane_base + cb * 32, r);
+                        tmem_wait_ld();
+                        if (factor && cb < wq) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int k0 = cb * 32 + 2 * e;
-                            const float v0 = (k0 <= j) ? __uint_as_float(r[2 * e]) * __expf(bj - sm.ew[k0]) : 0.f;
-                            const float v1 = (k0 + 1 <= j) ? __uint_as_float(r[2 * e + 1]) * __expf(bj - sm.ew[k0 + 1]) : 0.f;
-                            pk[e] = pack_bf16x2(v0, v1);
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const float4 w = *reinterpret_cast<const float4 *>(&sm.ew[cb * 32 + 4 * e4]);
+                                float v0, v1, v2, v3;
+                                f2_unpack(f2_mul(f2_pack(__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1])),
+                                                 f2_pack(w.x, w.y)), v0, v1);
+                                f2_unpack(f2_mul(f2_pack(__uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3])),
+                                                 f2_pack(w.z, w.w)), v2, v3);
+                                pk[2 * e4] = pack_bf16x2(v0, v1);
+                                pk[2 * e4 + 1] = pack_bf16x2(v2, v3);
+                            }
+                        } else if (factor) {
+#pragma unroll
+                            for (int e4 = 0; e4 < 8; ++e4) {
+                                const int k0 = cb * 32 + 4 * e4;
+                                const float4 w = *reinterpret_cast<const float4 *>(&sm.ew[k0]);
+                                const float v0 = (k0 <= j) ? __uint_as_float(r[4 * e4]) * w.x : 0.f;
+                                const float v1 = (k0 + 1 <= j) ? __uint_as_float(r[4 * e4 + 1]) * w.y : 0.f;
+                                const float v2 = (k0 + 2 <= j) ? __uint_as_float(r[4 * e4 + 2]) * w.z : 0.f;
+                                const float v3 = (k0 + 3 <= j) ? __uint_as_float(r[4 * e4 + 3]) * w.w : 0.f;
+                                pk[2 * e4] = pack_bf16x2(v0, v1);
+                                pk[2 * e4 + 1] = pack_bf16x2(v2, v3);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int k0 = cb * 32 + 2 * e;
+                                const float v0 = (k0 <= j) ? __uint_as_float(r[2 * e]) * __expf(bj - sm.ew[k0]) : 0.f;
+                                const float v1 = (k0 + 1 <= j) ? __uint_as_float(r[2 * e + 1]) * __expf(bj - sm.ew[k0 + 1]) : 0.f;
+                                pk[e] = pack_bf16x2(v0, v1);
+                            }
                         }
                     }
                     tmem_st16(tmem + kColA + lane_base + cb * 16, pk);  // columns already read
