@@ -552,6 +552,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const float bt = group_scan(lg_next, sm.wsum0, lane, warp, 2, bC);
                 if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), t);
                 const float sc = (bC > kFactorMin) ? __expf(bt) : 1.f;  // output row scale
+                const uint64_t sc2 = f2_pack(sc, sc);
                 bool ok = true;
                 if (t == 0) {
                     ok = mbar_wait(&sm.u_full, i & 1, abort_flag);
@@ -562,13 +563,17 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (!sm.go0) break;
                 tc_fence_after();
                 const float ebC = __expf(bC);
+                const uint64_t ebC2 = f2_pack(ebC, ebC);
 #pragma unroll
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t r[32];
                     tmem_ld32(tmem + kColU + lane_base + cb * 32, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) S[cb * 32 + e] = fmaf(ebC, S[cb * 32 + e], __uint_as_float(r[e]));
+                    for (int e = 0; e < 32; e += 2)  // S <- e^{b_C} S + U, two columns per packed FMA
+                        f2_unpack(f2_fma(ebC2, f2_pack(S[cb * 32 + e], S[cb * 32 + e + 1]),
+                                         f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1]))),
+                                  S[cb * 32 + e], S[cb * 32 + e + 1]);
                 }
                 tc_fence_before();
                 if (i + 1 < nchunks) put_state();  // MMA3 of this chunk is done (u_full)
@@ -596,12 +601,18 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tmem_ld32(o_t + cb * 32, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4)
-                            *reinterpret_cast<uint4 *>(stage_o + tile_chunk(t, cb * 4 + q4)) = make_uint4(
-                                pack_bf16x2(__uint_as_float(r[8 * q4]) * sc, __uint_as_float(r[8 * q4 + 1]) * sc),
-                                pack_bf16x2(__uint_as_float(r[8 * q4 + 2]) * sc, __uint_as_float(r[8 * q4 + 3]) * sc),
-                                pack_bf16x2(__uint_as_float(r[8 * q4 + 4]) * sc, __uint_as_float(r[8 * q4 + 5]) * sc),
-                                pack_bf16x2(__uint_as_float(r[8 * q4 + 6]) * sc, __uint_as_float(r[8 * q4 + 7]) * sc));
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {  // two columns per packed multiply
+                                float y0, y1;
+                                f2_unpack(f2_mul(f2_pack(__uint_as_float(r[8 * q4 + 2 * e]),
+                                                         __uint_as_float(r[8 * q4 + 2 * e + 1])), sc2), y0, y1);
+                                w[e] = pack_bf16x2(y0, y1);
+                            }
+                            *reinterpret_cast<uint4 *>(stage_o + tile_chunk(t, cb * 4 + q4)) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
                     }
                     tc_fence_before();
                     fence_proxy_async_smem();
