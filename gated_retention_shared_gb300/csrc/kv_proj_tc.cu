@@ -134,6 +134,10 @@ cudaError_t kv_project_append_tc(const KvProjArgs &a, const float *rrow, const f
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     pair_gemm_config(cfg, attr, ntiles, pairs, st);
+    // the shared-memory opt-in is set on every launch (it belongs to the current device)
+    cudaError_t e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)pairgemm::kSmemBytes);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaLaunchKernelEx(&cfg, proj_tc_kernel, mm, mk, mv, rrow, (bf16_t *)a.kc, (bf16_t *)a.vc, R, a.T, a.dm, n,
                               a.Hkv, a.d, a.cap, a.len, a.len_dev, err, rope_cs);

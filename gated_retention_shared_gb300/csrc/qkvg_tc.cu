@@ -125,6 +125,10 @@ cudaError_t qkvg_project(const void *X, const void *W, int B, int N, int dm, int
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     pair_gemm_config(cfg, attr, ntiles, pairs, st);
+    // the shared-memory opt-in is set on every launch (it belongs to the current device)
+    cudaError_t e = cudaFuncSetAttribute(qkvg_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)pairgemm::kSmemBytes);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaLaunchKernelEx(&cfg, qkvg_tc_kernel, mx, mw, R, N, dm, H, d, (bf16_t *)q, (bf16_t *)k, (bf16_t *)v,
                               logits, rope_cs, err);
