@@ -108,6 +108,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // when this grid was launched without the attribute).
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // The producer (thread 0, which initialised the barriers) starts the first K/V
+    // tiles now: they do not depend on Q, so their loads overlap the prologue below.
+    // L2 priority: the first keep_keys keys of every head stay cached from one call
+    // to the next (every cross layer reads this same cache); the rest stream through
+    // and are evicted first.
+    uint64_t pol_keep = 0, pol_stream = 0;
+    int issued = 0;
+    auto issue_kv = [&](int i) {  // tile i into stage i % kAStages, whose previous tile is done
+        const int s = i % kAStages;
+        const int key0 = (int)(k_lo + (int64_t)i * kAK);
+        uint8_t *st = tiles + (size_t)s * 2 * kATile;
+        const uint64_t pol = key0 < keep_keys ? pol_keep : pol_stream;
+        mbar_arrive_expect_tx(&sm.full[s], 2 * kATile);
+        for (int half = 0; half < 2; ++half) {
+            tma_load_3d_hint(st + half * kAHalf, &tm_k, &sm.full[s], half * 64, key0, bz, pol);
+            tma_load_3d_hint(st + kATile + half * kAHalf, &tm_v, &sm.full[s], half * 64, key0, bz, pol);
+        }
+    };
+    if (tid == 0 && ntiles > 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        pol_keep = l2_policy_evict_normal();
+        pol_stream = l2_policy_evict_first();
+        for (; issued < ntiles && issued < kAStages; ++issued) issue_kv(issued);
+    }
     // Q rows (unscaled bf16) as the K-major B operand; rows >= nq and both P buffers zero
     for (int e = tid; e < kAN * kAD / 8; e += kAThreads) {
         const int n = e / (kAD / 8), c8 = (e % (kAD / 8)) * 8;
@@ -150,27 +175,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (warp == 0) {
         // -------------------------------------------------------------- TMA
         if (lane == 0 && ntiles > 0) {
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            // L2 priority: the first keep_keys keys of every head stay cached from one
-            // call to the next (every cross layer reads this same cache); the rest
-            // stream through and are evicted first
-            const uint64_t pol_keep = l2_policy_evict_normal(), pol_stream = l2_policy_evict_first();
-            int i = 0;
+            int i = issued;  // the first stages went out before the prologue
             for (; i < ntiles; ++i) {
                 const int s = i % kAStages;
                 if (i >= kAStages && !mbar_wait(&sm.empty[s], ((i / kAStages) + 1) & 1, abort_flag)) {
                     fail(21);
                     break;
                 }
-                const int key0 = (int)(k_lo + (int64_t)i * kAK);
-                uint8_t *st = tiles + (size_t)s * 2 * kATile;
-                const uint64_t pol = key0 < keep_keys ? pol_keep : pol_stream;
-                mbar_arrive_expect_tx(&sm.full[s], 2 * kATile);
-                for (int half = 0; half < 2; ++half) {
-                    tma_load_3d_hint(st + half * kAHalf, &tm_k, &sm.full[s], half * 64, key0, bz, pol);
-                    tma_load_3d_hint(st + kATile + half * kAHalf, &tm_v, &sm.full[s], half * 64, key0, bz, pol);
-                }
+                issue_kv(i);
             }
             for (int k = max(0, i - kAStages); k < i; ++k)
                 mbar_wait(&sm.full[k % kAStages], (k / kAStages) & 1, abort_flag, 200000000ull);
