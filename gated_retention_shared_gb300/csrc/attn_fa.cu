@@ -49,6 +49,7 @@ constexpr float kRescaleGap2 = 8.f * kLog2e;  // reference moves only when passe
 struct FaSmem {
     uint64_t q_full, full[kFStages], empty[kFStages];
     uint64_t s_full[2], p_ready[2], pv_done[2];  // per set
+    int walive[2][4];                              // per set and softmax warp, after the tile loop
     uint64_t q_rot[2];                           // per set: Q tile turned (rotary encoding) or as loaded
     float rope_c[2][64], rope_s[2][64], rope_th[2][64];
     uint32_t tmem_base;
@@ -109,7 +110,7 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&sm.s_full[x], 1);
-            mbar_init(&sm.p_ready[x], 1);
+            mbar_init(&sm.p_ready[x], 4);  // one arrival per softmax warp of the set
             mbar_init(&sm.pv_done[x], 1);
             mbar_init(&sm.q_rot[x], 1);
         }
@@ -264,14 +265,16 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             fbar(bar_id, 128);
         }
         if (r == 0) mbar_arrive(&sm.q_rot[x]);
+        // Per tile, each warp waits for S and announces its rows' P on its own (no
+        // named barrier across the set: every thread owns its row)
         for (int i = 0; i < ntiles && alive; ++i) {
-            if (r == 0) {
-                const bool ok = mbar_wait(&sm.s_full[x], i & 1, abort_flag);
-                if (!ok) fail(33);
-                sm.go[x] = ok && !*abort_flag;
+            bool okw = true;
+            if (lane == 0) {
+                okw = mbar_wait(&sm.s_full[x], i & 1, abort_flag);
+                if (!okw) fail(33);
+                okw = okw && !*abort_flag;
             }
-            fbar(bar_id, 128);
-            if (!sm.go[x]) {
+            if (__shfl_sync(0xffffffffu, okw ? 1 : 0, 0) == 0) {
                 alive = false;
                 break;
             }
@@ -359,9 +362,13 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             }
             tc_fence_before();
-            fbar(bar_id, 128);  // every row's P (and rescaled O) is in TMEM
-            if (r == 0) mbar_arrive(&sm.p_ready[x]);
+            __syncwarp();  // this warp's rows of P (and rescaled O) are in TMEM
+            if (lane == 0) mbar_arrive(&sm.p_ready[x]);
         }
+        // the set agrees on going on: a warp that gave up stops the epilogue for all four
+        if (lane == 0) sm.walive[x][q4] = alive ? 1 : 0;
+        fbar(bar_id, 128);
+        alive = sm.walive[x][0] && sm.walive[x][1] && sm.walive[x][2] && sm.walive[x][3];
         // epilogue: o = O / l as bf16, staged in this set's Q tile (free: every S MMA is done)
         if (alive && ntiles > 0) {
             if (r == 0) {
