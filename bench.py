@@ -48,7 +48,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk", type=int, default=0)
     p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode", "cross_prefill", "swa_prefill",
-                                      "swa_decode", "gn_gate", "rope", "qkvg"], default=None,
+                                      "swa_decode", "gn_gate", "rope", "qkvg", "gret_decode_unfused",
+                                      "gret_decode_gn"], default=None,
                    help="time one call of the step on its bench shape (for profiling)")
     p.add_argument("--cache-len", type=int, default=0,
                    help="--only cross_decode: cache length (default: the step's prompt length)")
@@ -595,6 +596,26 @@ def run_only(args):
         def call():
             return L.yoco_gret_qkvg_project(P(Xg), P(Wg), B, N, DM, H, D, 0, args.rope_base, P(qg), P(kg), P(vg),
                                             P(lgg), P(ws), ws.numel(), stp)
+    elif args.only in ("gret_decode_unfused", "gret_decode_gn"):
+        # one generated token through a gRet layer's recurrent step and Eq. 7's output:
+        # the step then the separate GroupNorm + gate call, or the fused call
+        q1 = normal((B, H, D), bf, sid(CFG, 0, synth.T_Q, 1), std=D ** -0.5)
+        k1 = normal((B, H, D), bf, sid(CFG, 0, synth.T_K, 1), std=D ** -0.5)
+        v1 = normal((B, H, D), bf, sid(CFG, 0, synth.T_V, 1))
+        lg1 = normal((B, H), f32, sid(CFG, 0, synth.T_LOGIT, 1), mean=2.0)
+        g1 = normal((B, H, D), bf, sid(CFG, 0, synth.T_QX, 1))
+        S1 = normal((B, H, D, D), f32, sid(CFG, 0, synth.T_S0), std=0.05)
+        o1 = torch.empty(B, H, D, dtype=bf, device=dev)
+        z1 = torch.empty_like(o1)
+
+        if args.only == "gret_decode_unfused":
+            def call():
+                st_ = L.yoco_gret_decode_step(P(q1), P(k1), P(v1), P(lg1), TAU, P(S1), P(o1), B, H, D, D, 1, 1, stp)
+                return st_ or L.yoco_gret_group_norm_gate(P(o1), P(g1), None, None, 1e-5, P(z1), B, 1, H, D, 1, stp)
+        else:
+            def call():
+                return L.yoco_gret_decode_step_gn_gate(P(q1), P(k1), P(v1), P(lg1), TAU, P(S1), P(g1), None, None,
+                                                       1e-5, P(z1), B, H, D, D, 1, stp)
     elif args.only == "rope":  # rotary encoding of one gRet layer's q in place
         qr = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_Q))
 

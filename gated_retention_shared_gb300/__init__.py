@@ -70,6 +70,7 @@ def _load():
         "yoco_swa_decode": (i, [vp, vp, vp, i, f, vp, rp, vp, sz, vp]),
         "yoco_swa_workspace_size": (sz, [i, i, rp]),
         "yoco_gret_group_norm_gate": (i, [vp, vp, vp, vp, f, vp, i, i, i, i, i, vp]),
+        "yoco_gret_decode_step_gn_gate": (i, [vp, vp, vp, vp, f, vp, vp, vp, vp, f, vp, i, i, i, i, i, vp]),
         "yoco_rope_apply": (i, [vp, i, i, i, i, i64, f, i, vp]),
         "yoco_gret_qkvg_project": (i, [vp, vp, i, i, i, i, i, i64, f, vp, vp, vp, vp, vp, sz, vp]),
         "yoco_gret_qkvg_workspace_size": (sz, [i, i, i, i, f]),
@@ -88,7 +89,8 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_last_error", "yoco_version", "yoco_launch_count",
             "yoco_workspace_status", "yoco_cross_attn_decode_noalloc", "yoco_selftest_wait_timeout",
             "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size", "yoco_gret_group_norm_gate",
-            "yoco_rope_apply", "yoco_gret_qkvg_project", "yoco_gret_qkvg_workspace_size")
+            "yoco_rope_apply", "yoco_gret_qkvg_project", "yoco_gret_qkvg_workspace_size",
+            "yoco_gret_decode_step_gn_gate")
 
 
 def _check(status: int, where: str):
@@ -164,6 +166,25 @@ def yoco_gret_decode_step(q, k, v, gate_logits, tau, state, o, stream=None):
     st = lib.yoco_gret_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), float(tau), _ptr(state),
                                    _ptr(o), B, H, dk, dv, _dt(q), _dt(o), _stream(stream))
     _check(st, "yoco_gret_decode_step")
+
+
+def yoco_gret_decode_step_gn_gate(q, k, v, gate_logits, tau, state, gate, z, eps=1e-5, gn_weight=None, gn_bias=None,
+                                  stream=None):
+    """One recurrent step and, fused, z = swish(gate) * GroupNorm_h(o) for that token.
+    q, k [B,H,dk]; v, gate, z [B,H,dv] (one dtype); gate_logits [B,H] fp32; state
+    [B,H,dk,dv] fp32 (in/out); gn_weight, gn_bias fp32 [H * dv] or None."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (gate_logits, "gate_logits"), (state, "state"), (gate, "gate"),
+                 (z, "z")):
+        _need(t, n)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    for t, n in ((gn_weight, "gn_weight"), (gn_bias, "gn_bias")):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != H * dv):
+            raise ValueError(f"{n} must be fp32 with H * dv elements")
+    st = lib.yoco_gret_decode_step_gn_gate(_ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), float(tau), _ptr(state),
+                                           _ptr(gate), _ptr(gn_weight), _ptr(gn_bias), float(eps), _ptr(z), B, H, dk,
+                                           dv, _dt(q), _stream(stream))
+    _check(st, "yoco_gret_decode_step_gn_gate")
 
 
 # ------------------------------------------------------------- shared KV

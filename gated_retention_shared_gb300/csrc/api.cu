@@ -251,6 +251,22 @@ yoco_status yoco_cross_attn_decode(const void *Q, int Hq, const yoco_kv_cache *c
 
 // ---------------------------------------------- gated retention output (Eq. 7)
 
+yoco_status yoco_gret_decode_step_gn_gate(const void *q, const void *k, const void *v, const float *gate_logits,
+                                          float tau, float *state, const void *gate, const float *gn_weight,
+                                          const float *gn_bias, float eps, void *z, int B, int H, int dk, int dv,
+                                          yoco_dtype dt, void *stream) {
+    yoco_status s = check_gret_shapes(B, 1, H, dk, dv, dt, dt);
+    if (s != YOCO_OK) return s;
+    if (!q || !k || !v || !gate_logits || !state || !gate || !z) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (dv != 64 && dv != 128) return fail(YOCO_ERR_UNSUPPORTED, "dv %d not in {64, 128}", dv);
+    if (!(tau > 0.0f) || !isfinite(tau)) return fail(YOCO_ERR_INVALID_ARG, "tau must be finite and > 0");
+    if (!(eps > 0.f) || !isfinite(eps)) return fail(YOCO_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (!aligned(state, 16)) return fail(YOCO_ERR_INVALID_ARG, "state must be 16-byte aligned");
+    return cuda_status(gret_decode_gn(q, k, v, gate_logits, tau, state, gate, gn_weight, gn_bias, eps, z, B, H, dk, dv,
+                                      dt, (cudaStream_t)stream),
+                       "gret_decode_step_gn_gate");
+}
+
 yoco_status yoco_gret_group_norm_gate(const void *o, const void *gate, const float *gn_weight, const float *gn_bias,
                                       float eps, void *z, int B, int N, int H, int d, yoco_dtype dt, void *stream) {
     if (!o || !gate || !z) return fail(YOCO_ERR_INVALID_ARG, "null tensor");

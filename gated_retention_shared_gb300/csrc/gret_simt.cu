@@ -14,6 +14,7 @@
 // take, and as the sequence-parallel scan shared with the tensor-core path.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace yoco {
 
@@ -288,6 +289,100 @@ gret_decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, co
     }
 }
 
+
+// The recurrent step followed by the output of multi-head gated retention (paper
+// Section 3.1, Eq. 7): z = swish(gate) (.) GroupNorm_h(o), one group per head.  The
+// dv/32 CTAs of one head form a cluster: each computes its 32 columns of o as the
+// plain step does, pushes the sum and the sum of squares of its columns into every
+// peer's shared memory, passes one cluster barrier, and normalises and gates its
+// own columns from the head totals (variance E[o^2] - E[o]^2, biased, in fp32).
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256)
+gret_decode_step_gn_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
+                           const float *__restrict__ logits, float inv_tau, float *__restrict__ state,
+                           const Tin *__restrict__ gate, const float *__restrict__ gn_w,
+                           const float *__restrict__ gn_b, float eps, Tout *__restrict__ z, int H, int dk, int dv) {
+    __shared__ float qs[128], ks[128], vs[32];
+    __shared__ float part[32][33];
+    __shared__ __align__(8) float red[4][2];  // (sum, sum of squares) of each CTA of the cluster, by rank
+    const int bh = blockIdx.y;
+    const int c0 = blockIdx.x * 32;
+    const int tid = threadIdx.x;
+    const int cg = tid % 8;
+    const int rg = tid / 8;
+    const uint32_t rank = tc::cluster_ctarank();
+    const uint32_t nrank = (uint32_t)(dv / 32);
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    float *Sb = state + (size_t)bh * dk * dv;
+    float4 srow[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = rg + 32 * u;
+        if (i < dk) srow[u] = *reinterpret_cast<const float4 *>(Sb + (size_t)i * dv + c0 + 4 * cg);
+    }
+    for (int i = tid; i < dk; i += 256) {
+        qs[i] = to_f32(q[(size_t)bh * dk + i]);
+        ks[i] = to_f32(k[(size_t)bh * dk + i]);
+    }
+    if (tid < 32) vs[tid] = to_f32(v[(size_t)bh * dv + c0 + tid]);
+    const float g_in = (tid < 32) ? to_f32(gate[(size_t)bh * dv + c0 + tid]) : 0.f;
+    const float gamma = expf(log_gate(logits[bh], inv_tau));
+    __syncthreads();
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = rg + 32 * u;
+        if (i >= dk) break;
+        float4 s = srow[u];
+        const float ki = ks[i], qi = qs[i];
+        s.x = fmaf(gamma, s.x, ki * vs[4 * cg + 0]);
+        s.y = fmaf(gamma, s.y, ki * vs[4 * cg + 1]);
+        s.z = fmaf(gamma, s.z, ki * vs[4 * cg + 2]);
+        s.w = fmaf(gamma, s.w, ki * vs[4 * cg + 3]);
+        *reinterpret_cast<float4 *>(Sb + (size_t)i * dv + c0 + 4 * cg) = s;
+        acc[0] = fmaf(qi, s.x, acc[0]);
+        acc[1] = fmaf(qi, s.y, acc[1]);
+        acc[2] = fmaf(qi, s.z, acc[2]);
+        acc[3] = fmaf(qi, s.w, acc[3]);
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) part[rg][4 * cg + s] = acc[s];
+    __syncthreads();
+    if (tid < 32) {
+        float ov = 0.f;
+        for (int r = 0; r < 32; ++r) ov += part[r][tid];
+        float s1 = ov, s2 = ov * ov;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+            s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+        }
+        if (tid < (int)nrank) {  // lane p writes this CTA's sums into CTA p's table
+            const uint32_t dst = tc::mapa_shared(&red[rank][0], (uint32_t)tid);
+            asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(dst), "f"(s1), "f"(s2) : "memory");
+        }
+        part[0][tid] = ov;  // kept for the normalisation below (row 0 is read above only by this thread)
+    }
+    tc::cluster_sync();  // every CTA's sums are in every CTA's table
+    if (tid < 32) {
+        float t1 = 0.f, t2 = 0.f;
+        for (uint32_t r = 0; r < nrank; ++r) {
+            t1 += red[r][0];
+            t2 += red[r][1];
+        }
+        const float mean = t1 / (float)dv;
+        const float var = fmaxf(t2 / (float)dv - mean * mean, 0.f);
+        const float inv = rsqrtf(var + eps);
+        const int h = bh % H, c = c0 + tid;
+        float y = (part[0][tid] - mean) * inv;
+        if (gn_w) y *= gn_w[(size_t)h * dv + c];
+        if (gn_b) y += gn_b[(size_t)h * dv + c];
+        const float sw = g_in / (1.f + __expf(-g_in));  // swish(g) = g sigmoid(g)
+        z[(size_t)bh * dv + c] = from_f32<Tout>(sw * y);
+    }
+}
+
 }  // namespace yoco
 
 // ------------------------------------------------------------------ host side
@@ -368,6 +463,34 @@ cudaError_t gret_prefill_simt(const GretArgs &a, void *ws, cudaStream_t st) {
         if (a.dk == 64) return run_simt<bf16_t, bf16_t, 64>(a, P, seg_len, w, st);
         return run_simt<bf16_t, bf16_t, 128>(a, P, seg_len, w, st);
     }
+}
+
+cudaError_t gret_decode_gn(const void *q, const void *k, const void *v, const float *logits, float tau,
+                           float *state, const void *gate, const float *gn_w, const float *gn_b, float eps, void *z,
+                           int B, int H, int dk, int dv, yoco_dtype dt, cudaStream_t st) {
+    // the dv/32 column slices of one head form a cluster; a programmatic dependent
+    // of the previous kernel like the plain step
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(dv / 32, B * H);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = dv / 32;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    count_launches(1);
+    if (dt == YOCO_F32)
+        return cudaLaunchKernelEx(&cfg, gret_decode_step_gn_kernel<float, float>, (const float *)q, (const float *)k,
+                                  (const float *)v, logits, 1.0f / tau, state, (const float *)gate, gn_w, gn_b, eps,
+                                  (float *)z, H, dk, dv);
+    return cudaLaunchKernelEx(&cfg, gret_decode_step_gn_kernel<bf16_t, bf16_t>, (const bf16_t *)q,
+                              (const bf16_t *)k, (const bf16_t *)v, logits, 1.0f / tau, state, (const bf16_t *)gate,
+                              gn_w, gn_b, eps, (bf16_t *)z, H, dk, dv);
 }
 
 cudaError_t gret_decode(const void *q, const void *k, const void *v, const float *logits, float tau,

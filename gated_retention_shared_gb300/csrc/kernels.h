@@ -26,6 +26,10 @@ cudaError_t gret_prefill_simt(const GretArgs &a, void *ws, cudaStream_t st);
 cudaError_t gret_scan_launch(float *E, const float *G, float *state, int BH, int P, int DD, cudaStream_t st);
 cudaError_t gret_decode(const void *q, const void *k, const void *v, const float *logits, float tau,
                         float *state, void *o, int B, int H, int dk, int dv, yoco_dtype dt, cudaStream_t st);
+// the recurrent step followed by GroupNorm_h + swish gate (one cluster per head)
+cudaError_t gret_decode_gn(const void *q, const void *k, const void *v, const float *logits, float tau,
+                           float *state, const void *gate, const float *gn_w, const float *gn_b, float eps, void *z,
+                           int B, int H, int dk, int dv, yoco_dtype dt, cudaStream_t st);
 
 // gret_tc.cu (bf16, d = 128, tensor cores)
 bool gret_tc_eligible(int B, int N, int H, int dk, int dv, yoco_dtype dt);

@@ -228,6 +228,23 @@ YOCO_API yoco_status yoco_gret_group_norm_gate(const void *o, const void *gate, 
                                                const float *gn_bias, float eps, void *z, int B, int N, int H, int d,
                                                yoco_dtype dt, void *stream);
 
+/*
+ * One recurrent step (as yoco_gret_decode_step) followed by Eq. 7's output for
+ * that token, fused: z = swish(gate) (.) GroupNorm_h(o) with o the step's
+ * fp32 output, never rounded or stored.  GroupNorm as in
+ * yoco_gret_group_norm_gate (one group per head, biased variance over the dv
+ * channels, eps > 0, gn_weight / gn_bias fp32 [H * dv] or NULL), except that
+ * the variance is formed as E[o^2] - E[o]^2 in fp32.
+ *   q, k [B, H, dk], v, gate, z [B, H, dv] of dtype dt; gate_logits [B, H]
+ *   fp32; state [B, H, dk, dv] fp32 in/out.  dk = dv in {64, 128}.
+ * The dv/32 CTAs of each head run as one thread-block cluster.
+ */
+YOCO_API yoco_status yoco_gret_decode_step_gn_gate(const void *q, const void *k, const void *v,
+                                                   const float *gate_logits, float tau, float *state,
+                                                   const void *gate, const float *gn_weight, const float *gn_bias,
+                                                   float eps, void *z, int B, int H, int dk, int dv, yoco_dtype dt,
+                                                   void *stream);
+
 /* ------------------------- gated-retention input projections in one GEMM */
 
 /*

@@ -192,6 +192,22 @@ def test_group_norm_gate_validation(Y):
     assert L.yoco_gret_group_norm_gate(FAKE, FAKE, None, None, 1e-5, FAKE, 1, 0, 2, 128, 1, None) == Y.YOCO_OK
 
 
+def test_decode_step_gn_gate_validation(Y):
+    L = Y.lib
+    odd = ctypes.c_void_p(0x1004)  # 4-byte aligned only
+    call = L.yoco_gret_decode_step_gn_gate
+    assert call(FAKE, FAKE, FAKE, FAKE, 16.0, FAKE, FAKE, None, None, 0.0, FAKE, 1, 2, 128, 128, 1, None) == \
+        Y.YOCO_ERR_INVALID_ARG  # eps
+    assert call(FAKE, FAKE, FAKE, FAKE, 0.0, FAKE, FAKE, None, None, 1e-5, FAKE, 1, 2, 128, 128, 1, None) == \
+        Y.YOCO_ERR_INVALID_ARG  # tau
+    assert call(FAKE, FAKE, FAKE, FAKE, 16.0, FAKE, None, None, None, 1e-5, FAKE, 1, 2, 128, 128, 1, None) == \
+        Y.YOCO_ERR_INVALID_ARG  # gate
+    assert call(FAKE, FAKE, FAKE, FAKE, 16.0, FAKE, FAKE, None, None, 1e-5, FAKE, 1, 2, 96, 96, 1, None) == \
+        Y.YOCO_ERR_UNSUPPORTED
+    assert call(FAKE, FAKE, FAKE, FAKE, 16.0, odd, FAKE, None, None, 1e-5, FAKE, 1, 2, 128, 128, 1, None) == \
+        Y.YOCO_ERR_INVALID_ARG  # state alignment
+
+
 def test_rope_validation(Y):
     L = Y.lib
     assert L.yoco_rope_apply(FAKE, 1, 4, 2, 128, 0, 1.0, 1, None) == Y.YOCO_ERR_INVALID_ARG  # base must exceed 1

@@ -666,6 +666,63 @@ def test_group_norm_gate_decode_row(Y):
     assert rel_l2(host_f64(z), z_ref) <= BF16_REL_L2
 
 
+@pytest.mark.parametrize("dtype,d,affine", [("bf16", 128, False), ("bf16", 128, True), ("f32", 64, True),
+                                            ("f32", 128, False)])
+def test_gret_decode_step_gn_gate_fused(Y, dtype, d, affine):
+    """Three recurrent steps with GroupNorm_h + swish gate fused (the dv/32 CTAs of a
+    head as one cluster): each step's z equals the oracle's step output passed
+    through the oracle's group_norm_gate, and the carried state the oracle's."""
+    import torch
+    B, H, steps = 2, 24, 3
+    host, dev = gret_inputs(52, B, steps, H, d, dtype, logit_mean=1.0)
+    S0 = synth.normal(SEED, sid(52, 0, synth.T_S0), (B, H, d, d), "f32", std=0.2).astype(np.float64)
+    S = dev_f32(S0)
+    g, gd = gen(SEED, sid(52, 1, synth.T_Q), (B, steps, H, d), dtype)
+    w = b = wd = bd = None
+    if affine:
+        w = synth.normal(SEED, sid(52, 1, synth.T_K), (H * d,), "f32", mean=1.0, std=0.2)
+        b = synth.normal(SEED, sid(52, 2, synth.T_K), (H * d,), "f32", std=0.2)
+        wd, bd = dev_f32(w), dev_f32(b)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    zs = []
+    for t in range(steps):
+        z = torch.empty(B, H, d, dtype=tdt, device="cuda")
+        Y.yoco_gret_decode_step_gn_gate(*(x[:, t].contiguous() for x in dev), 16.0, S, gd[:, t].contiguous(), z,
+                                        eps=1e-5, gn_weight=wd, gn_bias=bd)
+        zs.append(host_f64(z))
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0, S0=S0)
+    z_ref = oracle.group_norm_gate(o_ref, g, 1e-5, w, b)
+    z_gpu = np.stack(zs, axis=1)
+    if dtype == "f32":
+        assert max_abs(z_gpu, z_ref) <= FP32_MAX_ABS
+        assert max_abs(S.cpu().numpy(), S_ref) <= FP32_MAX_ABS
+    else:
+        assert rel_l2(z_gpu, z_ref) <= BF16_REL_L2
+        assert rel_l2(S.cpu().numpy(), S_ref) <= BF16_REL_L2
+
+
+def test_gret_decode_step_gn_gate_matches_the_two_calls(Y):
+    """The fused call equals the plain step followed by yoco_gret_group_norm_gate
+    on its fp32 output (fp32 throughout, so only the variance formula differs)."""
+    import torch
+    B, H, d = 1, 8, 128
+    host, dev = gret_inputs(53, B, 1, H, d, "f32", logit_mean=1.0)
+    S0 = synth.normal(SEED, sid(53, 0, synth.T_S0), (B, H, d, d), "f32", std=0.2)
+    g, gd = gen(SEED, sid(53, 1, synth.T_Q), (B, H, d), "f32")
+    q, k, v, lg = (x[:, 0].contiguous() for x in dev)
+    S1, S2 = dev_f32(S0), dev_f32(S0)
+    z1 = torch.empty(B, H, d, device="cuda")
+    Y.yoco_gret_decode_step_gn_gate(q, k, v, lg, 16.0, S1, gd, z1)
+    o = torch.empty(B, H, d, device="cuda")
+    Y.yoco_gret_decode_step(q, k, v, lg, 16.0, S2, o)
+    z2 = torch.empty_like(o)
+    Y.yoco_gret_group_norm_gate(o, gd, z2)
+    torch.cuda.synchronize()
+    assert torch.equal(S1, S2)
+    assert max_abs(host_f64(z1), host_f64(z2)) <= FP32_MAX_ABS
+
+
 # ------------------------------------------------- rotary position encoding
 
 @pytest.mark.parametrize("dtype,d,pos0,base", [("bf16", 128, 0, 10000.0), ("bf16", 128, 1000000, 8e7),
