@@ -9,8 +9,11 @@
 //     p   = exp(scale s - m)            one thread per key, online max per vector
 //     O^T = V^T P^T      M = 128 dims,  N = 16,                K = 128 keys (TMEM)
 //     o   = o * e^{m_old - m_new} + O^T one thread per head dim, fp32 registers
-// K/V tiles stream through a 3-stage TMA ring; the tensor map's key extent is the
-// number of keys the call may read, so slots past it arrive as zeros.  Every
+// K and V tiles stream through TMA rings of their own (3 slots each).  A K slot
+// is refilled as soon as its S^T MMA completes and a V slot once its O^T MMA
+// does, so the next keys' load overlaps the softmax instead of waiting for the
+// whole tile to be consumed.  The tensor map's key extent is the number of keys
+// the call may read, so slots past it arrive as zeros.  Every
 // cross-decoder layer reads the same shared cache, so the loads of each head's
 // first keys (half the L2 over all heads) carry normal L2 priority and stay
 // cached for the next layer's call, and the rest are marked evict-first.
@@ -40,7 +43,7 @@ constexpr int kAPBytes = kAN * kAK * 2;       // 4 KB: P^T (N rows of keys, K-ma
 constexpr uint32_t kColS = 0, kColOt = 32;    // S^T[2] at 0,16; O^T tiles[2] at 32,48
 
 struct AttnSmem {
-    uint64_t full[kAStages], empty[kAStages];
+    uint64_t full_k[kAStages], full_v[kAStages], empty_k[kAStages], empty_v[kAStages];
     uint64_t s_full[2], s_free[2], p_ready[2], o_full[2], o_free[2], drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -88,8 +91,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
 
     if (tid == 0) {
         for (int s = 0; s < kAStages; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 1);
+            mbar_init(&sm.full_k[s], 1);
+            mbar_init(&sm.full_v[s], 1);
+            mbar_init(&sm.empty_k[s], 1);
+            mbar_init(&sm.empty_v[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sm.s_full[s], 1);
@@ -115,23 +120,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // and are evicted first.
     uint64_t pol_keep = 0, pol_stream = 0;
     int issued = 0;
-    auto issue_kv = [&](int i) {  // tile i into stage i % kAStages, whose previous tile is done
+    // tile i of K (or V) into slot i % kAStages of its ring, whose previous tile is done
+    auto issue_tile = [&](int i, bool is_v) {
         const int s = i % kAStages;
         const int key0 = (int)(k_lo + (int64_t)i * kAK);
-        uint8_t *st = tiles + (size_t)s * 2 * kATile;
+        uint8_t *dst = tiles + (size_t)s * 2 * kATile + (is_v ? kATile : 0);
+        uint64_t *bar = is_v ? &sm.full_v[s] : &sm.full_k[s];
         const uint64_t pol = key0 < keep_keys ? pol_keep : pol_stream;
-        mbar_arrive_expect_tx(&sm.full[s], 2 * kATile);
-        for (int half = 0; half < 2; ++half) {
-            tma_load_3d_hint(st + half * kAHalf, &tm_k, &sm.full[s], half * 64, key0, bz, pol);
-            tma_load_3d_hint(st + kATile + half * kAHalf, &tm_v, &sm.full[s], half * 64, key0, bz, pol);
-        }
+        mbar_arrive_expect_tx(bar, kATile);
+        for (int half = 0; half < 2; ++half)
+            tma_load_3d_hint(dst + half * kAHalf, is_v ? &tm_v : &tm_k, bar, half * 64, key0, bz, pol);
     };
     if (tid == 0 && ntiles > 0) {
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         pol_keep = l2_policy_evict_normal();
         pol_stream = l2_policy_evict_first();
-        for (; issued < ntiles && issued < kAStages; ++issued) issue_kv(issued);
+        for (; issued < ntiles && issued < kAStages; ++issued) {
+            issue_tile(issued, false);
+            issue_tile(issued, true);
+        }
     }
     // Q rows (unscaled bf16) as the K-major B operand; rows >= nq and both P buffers zero
     for (int e = tid; e < kAN * kAD / 8; e += kAThreads) {
@@ -175,17 +183,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     if (warp == 0) {
         // -------------------------------------------------------------- TMA
         if (lane == 0 && ntiles > 0) {
-            int i = issued;  // the first stages went out before the prologue
+            // The first slots went out before the prologue.  K tile i waits for the
+            // S^T MMA of tile i - kAStages, V tile i for its O^T MMA, which the MMA
+            // issuer runs after the S^T MMA of the next tile: so K runs ahead.
+            volatile int no_abort = 0;
+            int i = issued;
             for (; i < ntiles; ++i) {
                 const int s = i % kAStages;
-                if (i >= kAStages && !mbar_wait(&sm.empty[s], ((i / kAStages) + 1) & 1, abort_flag)) {
+                const uint32_t par = ((i / kAStages) + 1) & 1;
+                if (i >= kAStages && !mbar_wait(&sm.empty_k[s], par, abort_flag)) {
                     fail(21);
                     break;
                 }
-                issue_kv(i);
+                issue_tile(i, false);
+                if (i >= kAStages && !mbar_wait(&sm.empty_v[s], par, abort_flag)) {
+                    fail(21);
+                    mbar_wait(&sm.full_k[s], (i / kAStages) & 1, &no_abort, 200000000ull);
+                    break;
+                }
+                issue_tile(i, true);
             }
-            for (int k = max(0, i - kAStages); k < i; ++k)
-                mbar_wait(&sm.full[k % kAStages], (k / kAStages) & 1, abort_flag, 200000000ull);
+            // leave no copy in flight (bounded by time only: an abort must still wait)
+            for (int k = max(0, i - kAStages); k < i; ++k) {
+                mbar_wait(&sm.full_k[k % kAStages], (k / kAStages) & 1, &no_abort, 200000000ull);
+                mbar_wait(&sm.full_v[k % kAStages], (k / kAStages) & 1, &no_abort, 200000000ull);
+            }
         }
     } else if (warp == 1) {
         // -------------------------------------------------------------- MMA
@@ -195,7 +217,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             const uint32_t q_a = smem_u32(sQ);
             auto issue_s = [&](int i) -> bool {
                 const int s = i % kAStages;
-                if (!mbar_wait(&sm.full[s], (i / kAStages) & 1, abort_flag)) return false;
+                if (!mbar_wait(&sm.full_k[s], (i / kAStages) & 1, abort_flag)) return false;
                 if (i >= 2 && !mbar_wait(&sm.s_free[i & 1], ((i / 2) - 1) & 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t k_a = smem_u32(tiles + (size_t)s * 2 * kATile);
@@ -206,6 +228,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                            smem_desc_sw128(q_a + qoff, 16, 1024), id_s, kk > 0);
                 }
                 mma_commit(&sm.s_full[i & 1]);
+                mma_commit(&sm.empty_k[s]);  // the K slot may be refilled
                 return true;
             };
             bool ok = issue_s(0);
@@ -214,6 +237,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                 const int s = i % kAStages;
                 if (!(ok = mbar_wait(&sm.p_ready[i & 1], (i / 2) & 1, abort_flag))) break;
                 if (i >= 2 && !(ok = mbar_wait(&sm.o_free[i & 1], ((i / 2) - 1) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sm.full_v[s], (i / kAStages) & 1, abort_flag))) break;
                 tc_fence_after();
                 const uint32_t v_a = smem_u32(tiles + (size_t)s * 2 * kATile + kATile);
                 const uint32_t p_a = smem_u32(sP + (i & 1) * kAPBytes);
@@ -223,7 +247,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
                            smem_desc_sw128(p_a + poff, 16, 1024), id_o, kk > 0);
                 }
                 mma_commit(&sm.o_full[i & 1]);
-                mma_commit(&sm.empty[s]);
+                mma_commit(&sm.empty_v[s]);
             }
             if (!ok) fail(22);
             mma_commit(&sm.drain);
