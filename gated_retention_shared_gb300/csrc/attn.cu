@@ -260,53 +260,54 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
 }
 
 // merge the splits of every query row by log-sum-exp: one CTA per (row, head),
-// thread c owns head dim c.  Every load is independent of the others: the split
-// maxima and sums are read one split per thread, and the weighted sum over splits
-// is unrolled, so the kernel costs a few L2 round trips rather than one per split.
+// thread c owns head dim c.  Splits are taken kCombineBatch at a time; every
+// thread issues all of a batch's loads at once (each split's maximum and sum,
+// the same addresses across the CTA, and its own column of the partial
+// outputs), so a batch costs one L2 round trip, and the batches are folded
+// online (running maximum, rescaled sum and output).  Partials are read past
+// L1 (the split kernel wrote them from other SMs).
 constexpr int kCombineMaxSplits = 4096;
+constexpr int kCombineBatch = 32;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(D) attn_combine_kernel(const float *__restrict__ part, T *__restrict__ O, int splits) {
-    __shared__ float fs[kCombineMaxSplits];  // m_s, then e^{m_s - M}
-    __shared__ float ls[kCombineMaxSplits];  // l_s
-    __shared__ float red[D / 32];
     // launched as a programmatic dependent of the split kernel: wait for its partials
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    const int w = blockIdx.x, c = threadIdx.x, lane = c & 31, wid = c >> 5;
+    const int w = blockIdx.x, c = threadIdx.x;
     const float *pp = part + (size_t)w * splits * (D + 2);
-    float mloc = -INFINITY;
-    for (int s = c; s < splits; s += D) {
-        const float m = pp[(size_t)s * (D + 2) + D];
-        fs[s] = m;
-        ls[s] = pp[(size_t)s * (D + 2) + D + 1];
-        mloc = fmaxf(mloc, m);
+    float M = -INFINITY, L = 0.f, A = 0.f;
+    for (int s0 = 0; s0 < splits; s0 += kCombineBatch) {
+        const int n = min(kCombineBatch, splits - s0);
+        float ms[kCombineBatch], ls[kCombineBatch], os[kCombineBatch];
+#pragma unroll
+        for (int j = 0; j < kCombineBatch; ++j) {
+            if (j < n) {
+                const float *q = pp + (size_t)(s0 + j) * (D + 2);
+                ms[j] = __ldcg(q + D);
+                ls[j] = __ldcg(q + D + 1);
+                os[j] = __ldcg(q + c);
+            } else {
+                ms[j] = -INFINITY;
+                ls[j] = 0.f;
+                os[j] = 0.f;
+            }
+        }
+        float mb = M;
+#pragma unroll
+        for (int j = 0; j < kCombineBatch; ++j) mb = fmaxf(mb, ms[j]);
+        if (mb == -INFINITY) continue;  // nothing valid so far
+        const float r = (M == -INFINITY) ? 0.f : __expf(M - mb);
+        L *= r;
+        A *= r;
+#pragma unroll
+        for (int j = 0; j < kCombineBatch; ++j) {
+            const float f = (ms[j] == -INFINITY) ? 0.f : __expf(ms[j] - mb);
+            L = fmaf(ls[j], f, L);
+            A = fmaf(os[j], f, A);
+        }
+        M = mb;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-    if (lane == 0) red[wid] = mloc;
-    __syncthreads();
-    float M = red[0];
-#pragma unroll
-    for (int i = 1; i < D / 32; ++i) M = fmaxf(M, red[i]);
-    __syncthreads();
-    float lloc = 0.f;
-    for (int s = c; s < splits; s += D) {
-        const float ms = fs[s];
-        const float f = (ms == -INFINITY) ? 0.f : __expf(ms - M);
-        fs[s] = f;
-        lloc += ls[s] * f;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
-    if (lane == 0) red[wid] = lloc;
-    __syncthreads();
-    float L = 0.f;
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) L += red[i];
-    float A = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < splits; ++s) A += pp[(size_t)s * (D + 2) + c] * fs[s];
     O[(size_t)w * D + c] = from_f32<T>(A / L);
 }
 

@@ -107,14 +107,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         sm.abort_flag = 0;
         fence_mbar_init();
     }
-    // Programmatic dependent launch: the combine grid (and a following call) may
-    // start now; nothing of another kernel is read or written before the wait below,
-    // which returns once the previous kernel on the stream has completed (at once
-    // when this grid was launched without the attribute).
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     // The producer (thread 0, which initialised the barriers) starts the first K/V
-    // tiles now: they do not depend on Q, so their loads overlap the prologue below.
+    // tiles at once, before the programmatic-dependency wait below: the cache is
+    // written only by appends, which never release their dependents early, so
+    // every append before this call on the stream has completed by the time this
+    // grid runs, and the loads overlap the previous kernel's tail.  Q (which the
+    // previous kernel may produce) and the workspace (which the previous call's
+    // merge may still be reading) are touched only after the wait.
     // L2 priority: the first keep_keys keys of every head stay cached from one call
     // to the next (every cross layer reads this same cache); the rest stream through
     // and are evicted first.
@@ -141,6 +140,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             issue_tile(issued, true);
         }
     }
+    // Programmatic dependent launch: the combine grid (and a following call) may
+    // start now; apart from the cache tiles above, nothing of another kernel is
+    // read or written before the wait, which returns once the previous kernel on
+    // the stream has completed (at once when this grid was launched without the
+    // attribute).
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     // Q rows (unscaled bf16) as the K-major B operand; rows >= nq and both P buffers zero
     for (int e = tid; e < kAN * kAD / 8; e += kAThreads) {
         const int n = e / (kAD / 8), c8 = (e % (kAD / 8)) * 8;

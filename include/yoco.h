@@ -68,6 +68,11 @@ typedef enum { YOCO_F32 = 0, YOCO_BF16 = 1 } yoco_dtype;
  *             sees the new length on replay.
  *   len_host  host copy of the length; appends advance it, attention calls
  *             read it.  The caller keeps it equal to len_dev[0].
+ *   Attention calls may start loading k and v while the kernel before them
+ *   on the stream is still finishing (programmatic dependent launch).  An
+ *   append never lets a following kernel start early, so appends are always
+ *   complete; a caller that writes k or v with a kernel of its own must not
+ *   have that kernel release its dependents early either.
  *   rope_base 0: no rotary encoding.  > 1: rotary position encoding (paper
  *             Section 3.1, Q (.) Theta / K (.) conj(Theta); the shared K^ is
  *             rotated once when projected, each cross layer rotates its Q):
