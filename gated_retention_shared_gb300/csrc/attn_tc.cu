@@ -140,14 +140,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             issue_tile(issued, true);
         }
     }
+    // The rest of the prologue that touches nothing of another kernel: both P
+    // buffers zero, the TMEM columns, and an L2 prefetch of this CTA's query rows
+    // (a prefetch only warms L2, which a later write by the kernel that produces Q
+    // updates in place, so the read after the wait still sees that write).
+    for (int e = tid; e < 2 * kAPBytes / 16; e += kAThreads) reinterpret_cast<uint4 *>(sP)[e] = make_uint4(0, 0, 0, 0);
+    if (tid < 2 * nq) {
+        const int n = tid >> 1, t = t0 + n / G, h = hk * G + n % G;
+        const bf16_t *row = Q + (((size_t)b * T_rows + t) * Hq + h) * kAD + (tid & 1) * 64;
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row));
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem_base, 64);
+        tmem_relinquish();
+    }
     // Programmatic dependent launch: the combine grid (and a following call) may
-    // start now; apart from the cache tiles above, nothing of another kernel is
-    // read or written before the wait, which returns once the previous kernel on
-    // the stream has completed (at once when this grid was launched without the
-    // attribute).
+    // start now; apart from the cache tiles and the prefetch above, nothing of
+    // another kernel is read or written before the wait, which returns once the
+    // previous kernel on the stream has completed (at once when this grid was
+    // launched without the attribute).
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    // Q rows (unscaled bf16) as the K-major B operand; rows >= nq and both P buffers zero
+    // Q rows (unscaled bf16) as the K-major B operand; rows >= nq zero
     for (int e = tid; e < kAN * kAD / 8; e += kAThreads) {
         const int n = e / (kAD / 8), c8 = (e % (kAD / 8)) * 8;
         uint4 v = make_uint4(0, 0, 0, 0);
@@ -170,12 +184,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
         *reinterpret_cast<uint4 *>(sQ + sw_off(n, c8, kAN)) = v;
     }
-    for (int e = tid; e < 2 * kAPBytes / 16; e += kAThreads) reinterpret_cast<uint4 *>(sP)[e] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
-    if (warp == 0) {
-        tmem_alloc(&sm.tmem_base, 64);
-        tmem_relinquish();
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

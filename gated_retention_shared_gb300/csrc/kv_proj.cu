@@ -170,7 +170,8 @@ proj_append_simt(const T *__restrict__ M, const T *__restrict__ g, const T *__re
 // the last CTA to finish (ticket in len_dev[1], no waiting) adds the KCH partials
 // in chunk order, computes each input row's RMS factor, rounds once, writes the
 // cache slots and publishes the new length.
-constexpr int kGemvU = 10;  // W rows in flight per warp
+constexpr int kGemvU = 10;      // W rows in flight per warp (fp32 W; bf16 W: twice as many)
+constexpr int kTailBatch = 10;  // K-chunk partials in flight per thread in the last CTA
 
 // 8 consecutive W elements as raw 16-byte words (bf16: one, fp32: two)
 template <typename T>
@@ -260,13 +261,14 @@ proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__re
         };
         if (col_ok) {
             int kk = k0 + warp;
-            // batches of kGemvU rows: every load of a batch is issued before its FMAs
-            for (; kk + 8 * (kGemvU - 1) < k1; kk += 8 * kGemvU) {
-                W8<T> raw[kGemvU];
+            // batches of U rows: every load of a batch is issued before its FMAs
+            constexpr int U = (sizeof(T) == 2) ? 2 * kGemvU : kGemvU;
+            for (; kk + 8 * (U - 1) < k1; kk += 8 * U) {
+                W8<T> raw[U];
 #pragma unroll
-                for (int u = 0; u < kGemvU; ++u) raw[u] = ld_w8(W + (size_t)(kk + 8 * u) * n);
+                for (int u = 0; u < U; ++u) raw[u] = ld_w8(W + (size_t)(kk + 8 * u) * n);
 #pragma unroll
-                for (int u = 0; u < kGemvU; ++u) fma_row(raw[u], kk + 8 * u);
+                for (int u = 0; u < U; ++u) fma_row(raw[u], kk + 8 * u);
             }
             for (; kk < k1; kk += 8) fma_row(ld_w8(W + (size_t)kk * n), kk);
         }
@@ -295,55 +297,80 @@ proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__re
     __syncthreads();
     if (!last) return;
     __threadfence();
+    // Per row: the RMS factor of the raw input row and the sum of the K chunks'
+    // partials for this thread's 8 columns.  Loads are issued in batches
+    // (kTailBatch chunks at a time, the first batch together with the row's RMS
+    // loads) so the tail costs a few L2 round trips, not one per chunk.
+    const size_t qstride = (size_t)R * 2 * n;
     for (int row = 0; row < R; ++row) {
-        // RMS factor of the raw input row (16-byte loads; dm % 8 == 0)
-        float ss = 0.f;
-        for (int kv = tid * 8; kv < dm; kv += 256 * 8) {
-            float x[8];
-            load_w8(M + (size_t)row * dm + kv, x);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) ss = fmaf(x[q], x[q], ss);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        if (lane == 0) red[0][warp] = ss;
-        __syncthreads();
-        float sq = 0.f;
-#pragma unroll
-        for (int w8 = 0; w8 < 8; ++w8) sq += red[0][w8];
-        const float r = rsqrtf(sq / (float)dm + eps);
         const int b = row / T_rows, t = row % T_rows;
-        // 8 consecutive columns per thread (2n % 8 == 0): the chunks' partials as
-        // float4 pairs, four chunks in flight
-        for (int c = tid * 8; c < 2 * n; c += 256 * 8) {
+        float rms_r = 0.f;
+        for (int c = tid * 8, first = 1; c < 2 * n || first; c += 256 * 8, first = 0) {
+            const bool has_c = c < 2 * n;
+            const float *pc = part + (size_t)row * 2 * n + (has_c ? c : 0);
             float sum[8] = {};
-            const float *pc = part + (size_t)row * 2 * n + c;
-            const size_t qstride = (size_t)R * 2 * n;
-            int q = 0;
-            for (; q + 4 <= nkc; q += 4) {
-                float4 v[4][2];
+            auto add_batch = [&](int q0) {
+                float4 v[kTailBatch][2];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    v[u][0] = __ldcg(reinterpret_cast<const float4 *>(pc + (q + u) * qstride));
-                    v[u][1] = __ldcg(reinterpret_cast<const float4 *>(pc + (q + u) * qstride) + 1);
+                for (int u = 0; u < kTailBatch; ++u) {
+                    if (q0 + u < nkc) {
+                        v[u][0] = __ldcg(reinterpret_cast<const float4 *>(pc + (q0 + u) * qstride));
+                        v[u][1] = __ldcg(reinterpret_cast<const float4 *>(pc + (q0 + u) * qstride) + 1);
+                    } else {
+                        v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < kTailBatch; ++u) {
                     sum[0] += v[u][0].x; sum[1] += v[u][0].y; sum[2] += v[u][0].z; sum[3] += v[u][0].w;
                     sum[4] += v[u][1].x; sum[5] += v[u][1].y; sum[6] += v[u][1].z; sum[7] += v[u][1].w;
                 }
+            };
+            if (first) {
+                // the first batch of partials and the row's RMS loads in flight together
+                float4 v0[kTailBatch][2];
+                if (has_c) {
+#pragma unroll
+                    for (int u = 0; u < kTailBatch; ++u) {
+                        if (u < nkc) {
+                            v0[u][0] = __ldcg(reinterpret_cast<const float4 *>(pc + u * qstride));
+                            v0[u][1] = __ldcg(reinterpret_cast<const float4 *>(pc + u * qstride) + 1);
+                        } else {
+                            v0[u][0] = v0[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                }
+                float ss = 0.f;
+#pragma unroll 4
+                for (int kv = tid * 8; kv < dm; kv += 256 * 8) {
+                    float x[8];
+                    load_w8(M + (size_t)row * dm + kv, x);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) ss = fmaf(x[q], x[q], ss);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                if (lane == 0) red[0][warp] = ss;
+                __syncthreads();
+                float sq = 0.f;
+#pragma unroll
+                for (int w8 = 0; w8 < 8; ++w8) sq += red[0][w8];
+                rms_r = rsqrtf(sq / (float)dm + eps);
+                if (has_c) {
+#pragma unroll
+                    for (int u = 0; u < kTailBatch; ++u) {
+                        sum[0] += v0[u][0].x; sum[1] += v0[u][0].y; sum[2] += v0[u][0].z; sum[3] += v0[u][0].w;
+                        sum[4] += v0[u][1].x; sum[5] += v0[u][1].y; sum[6] += v0[u][1].z; sum[7] += v0[u][1].w;
+                    }
+                }
             }
-            for (; q < nkc; ++q) {
-                const float4 a = __ldcg(reinterpret_cast<const float4 *>(pc + q * qstride));
-                const float4 bb = __ldcg(reinterpret_cast<const float4 *>(pc + q * qstride) + 1);
-                sum[0] += a.x; sum[1] += a.y; sum[2] += a.z; sum[3] += a.w;
-                sum[4] += bb.x; sum[5] += bb.y; sum[6] += bb.z; sum[7] += bb.w;
-            }
+            if (!has_c) continue;
+            for (int q0 = first ? kTailBatch : 0; q0 < nkc; q0 += kTailBatch) add_batch(q0);
             // the 8 columns lie in one head of Wk or of Wv (n % 8 == 0, d % 8 == 0)
             const int cn = c % n, h = cn / d, cc = cn % d;
             T *dst = ((c < n) ? kc : vc) + (((size_t)b * Hkv + h) * cap + len + t) * d + cc;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sum[e] *= r;
+            for (int e = 0; e < 8; ++e) sum[e] *= rms_r;
             if (rope_base > 0.f && c < n) {  // rotary encoding of K^ at slot position len + t
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
