@@ -414,6 +414,21 @@ def run_gpu(args):
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (burst copy)" if "hbm_gbs" in peaks else "fallback",
                 "algorithmic_bytes_per_launch": gret_bytes, "avg_launch_ms": round(gret_ms, 4),
                 "traffic": GRET_CALL_DRAM_BYTES, "traffic_unit": "bytes per call (ncu dram read + write, both passes)"}
+    # the same call against the tensor cores: per token and head, the causal half of the
+    # chunk's QK^T and PV (2 d (C + 1)) plus the cross-chunk q S and the state update (4 d^2),
+    # at the chunk the tensor-core kernel runs (128); attainable = min(TC, AI x HBM)
+    chunk_tc = args.chunk if args.chunk else 128
+    gret_flops = B * N * H * (2 * D * (chunk_tc + 1) + 4 * D * D)
+    # timed inside a seconds-long step: the sustained bf16 figure
+    tc_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)) * 1e12
+    tflops = gret_flops / (gret_ms / 1e3)
+    attainable = min(tc_peak, gret_flops / gret_bytes * hbm_peak * 1e9)
+    roofline.update({"flops_per_launch": gret_flops, "chunk": chunk_tc, "tc_achieved_tflops": round(tflops / 1e12, 1),
+                     "tc_peak_tflops": round(tc_peak / 1e12, 1), "tc_frac": round(tflops / tc_peak, 4),
+                     "tc_peak_source": ("MEASURED_PEAKS.json bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks
+                                        else "fallback"),
+                     "arithmetic_intensity": round(gret_flops / gret_bytes, 1),
+                     "attainable_frac": round(tflops / attainable, 4)})
 
     # ---- the generated token: 13 recurrent gRet steps, one append, 13 cross layers
     dec_ms = phases["gret_decode_x13"] + phases["kv_append_1"] + phases["cross_decode_x13"]
@@ -536,12 +551,13 @@ def run_only(args):
         M1 = normal((B, 1, DM), bf, sid(CFG, 0, synth.T_M, 1))
         Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
         Wv = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WV), std=0.02)
-        cache = Y.KVCache(B, HKV, D, N + 1, device=dev)
+        # every call appends one more slot (no length reset, so no host write inside the timed loop)
+        cache = Y.KVCache(B, HKV, D, N + args.warmup + args.steps, device=dev)
+        cache.set_length(N)
         ws = torch.empty(max(256, L.yoco_shared_kv_workspace_size(B, 1, DM, ctypes.byref(cache.c))),
                          dtype=torch.uint8, device=dev)
 
         def call():
-            cache.set_length(N)
             return L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, ctypes.byref(cache.c),
                                                    P(ws), ws.numel(), stp)
     elif args.only == "cross_prefill":  # every prompt row over the shared cache (no early exit)
