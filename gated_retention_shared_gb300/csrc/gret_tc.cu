@@ -20,13 +20,15 @@
 // scales Q's rows by e^{b_j} in place (and the epilogue multiplies by 1).
 //
 // Sequence parallelism: the sequence of every (b, h) is cut into P segments of
-// whole chunks.  Kernel mode SEG_STATE walks a segment backwards and accumulates
-// its zero-start end state  E^T = sum_k e^{(decay after k to segment end)} v_k^T k_k
-// directly in TMEM (every weight <= 1), plus the segment's total log decay.  A
-// OUTPUT CTA then folds the earlier segments' end states into its initial state
+// whole chunks.  The segment-state kernel (gret_seg_kernel) walks a segment
+// backwards and accumulates its zero-start end state
+// E^T = sum_k e^{(decay after k to segment end)} v_k^T k_k directly in TMEM (every
+// weight <= 1), plus the segment's total log decay.  An output CTA (gret_tc_kernel)
+// then folds the earlier segments' end states into its initial state
 // (S_start(p) = e^{G_{p-1}} S_start(p-1) + E_{p-1}) and runs the chunk recurrence
-// above from it.  The last segment's end state is the call's final state, so
-// SEG_STATE runs for P-1 segments only.  With B*H >= #SMs, P = 1 and only OUTPUT runs.
+// above from it.  The last segment's end state is the call's final state, so the
+// segment-state grid covers P-1 segments only.  With B*H >= #SMs, P = 1 and only the
+// output kernel runs.
 //
 // Warp roles (320 threads): warps 0-3 keep the state (thread t = TMEM lane t =
 // d_k row t), warps 4-7 compute the decay, P, the in-place scaling of K (and Q)
@@ -48,18 +50,16 @@ constexpr int kD = 128;                     // head size
 constexpr int kTile = kC * kD * 2;          // 32 KB bf16 tile
 constexpr int kHalf = kTile / 2;            // one 64-column block
 constexpr int kStages = 2;                  // OUTPUT: 2 x (Q, K, V)
-constexpr int kStagesSeg = 3;               // SEG_STATE: 3 x (K, V)
 constexpr int kTcThreads = 320;
 constexpr float kFactorMin = -60.f;         // chunk decay above which e^{-b_k} is used
 
 // TMEM columns: A / P, two O accumulators, U
 constexpr uint32_t kColA = 0, kColO = 128, kColU = 384;
 
-enum : int { MODE_OUTPUT = 0, MODE_SEG_STATE = 1 };
 
 struct TcSmem {
-    uint64_t full[kStagesSeg], empty[kStagesSeg], pq_ready[kStagesSeg], o_free[2], bc_ready[2], o_full[2];
-    uint64_t full_v[kStages], o_staged[kStages], k_ready[kStages], w_ready[kStagesSeg];
+    uint64_t full[kStages], empty[kStages], pq_ready[kStages], o_free[2], bc_ready[2], o_full[2];
+    uint64_t full_v[kStages], o_staged[kStages], k_ready[kStages];
     uint64_t as_full, p_free, u_full, u_free, s_ready, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -110,16 +110,6 @@ __device__ __forceinline__ void scale_row_inplace(uint8_t *tile, int r, float s)
     }
 }
 
-// Scale one 64-column block (chunks 8*blk .. 8*blk+7) of row r in place.
-__device__ __forceinline__ void scale_row_block(uint8_t *tile, int r, float s, int blk) {
-    const __nv_bfloat162 s2 = __float2bfloat162_rn(s);
-#pragma unroll
-    for (int c = 8 * blk; c < 8 * blk + 8; ++c) {
-        uint4 *p = reinterpret_cast<uint4 *>(tile + tile_chunk(r, c));
-        *p = scale_bf16x8(*p, s2);
-    }
-}
-
 // Inclusive cumsum of one value per thread over a 128-thread group (4 warps).
 __device__ __forceinline__ float group_scan(float x, float *wsum, int lane, int wq, int bar_id, float &total) {
 #pragma unroll
@@ -135,7 +125,6 @@ __device__ __forceinline__ float group_scan(float x, float *wsum, int lane, int 
     return x + pre;
 }
 
-template <int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -148,42 +137,31 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint8_t *tiles = smem_raw + pad;
     TcSmem &sm = *reinterpret_cast<TcSmem *>(tiles + kTileBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    constexpr int NS = (MODE == MODE_OUTPUT) ? kStages : kStagesSeg;
+    constexpr int NS = kStages;
     if (pad + kTileBytes + sizeof(TcSmem) > kTcSmemBytes) {  // cannot happen with a 16-B aligned window
         if (tid == 0 && err) atomicExch(err, (int)(kErrMagic | 9u));
         return;
     }
-    // OUTPUT: segment-major linear grid (the segment-0 CTAs, which need nothing from
-    // the SEG_STATE grid, are dispatched first); SEG_STATE: (segment, head, sequence)
-    int p, h, b;
-    if (MODE == MODE_OUTPUT) {
-        const int BH = (int)gridDim.x / P, r = (int)blockIdx.x % BH;
-        p = (int)blockIdx.x / BH;
-        h = r % H;
-        b = r / H;
-    } else {
-        p = blockIdx.x;
-        h = blockIdx.y;
-        b = blockIdx.z;
-    }
+    // segment-major linear grid: the segment-0 CTAs, which need nothing from the
+    // segment-state grid, are dispatched first
+    const int BH = (int)gridDim.x / P, r_bh = (int)blockIdx.x % BH;
+    const int p = (int)blockIdx.x / BH, h = r_bh % H, b = r_bh / H;
     const int t_begin = p * seg_len;
     const int t_end = min(N, t_begin + seg_len);
     const int nchunks = (t_end - t_begin + kC - 1) / kC;
-    const size_t bh = (size_t)b * H + h;
-    const size_t bhp = bh * P + p;  // segment slot in E / G; slot P-1 of E holds the initial state
-    // OUTPUT stages hold Q, K, V; SEG_STATE stages hold K, V (no Q), so it keeps 3 in flight
-    uint8_t *Sbuf = tiles + (size_t)6 * kTile;  // bf16 state, MMA3's B operand (SEG_STATE: weight ring)
-    constexpr size_t kSS = (MODE == MODE_OUTPUT ? 3 : 2) * (size_t)kTile;
+    const size_t bh = (size_t)b * H + h;  // E / G slots: bh * P + q; slot P-1 of E holds the initial state
+    // each stage holds Q, K, V of one chunk
+    uint8_t *Sbuf = tiles + (size_t)6 * kTile;  // bf16 state, MMA3's B operand
+    constexpr size_t kSS = 3 * (size_t)kTile;
     auto stage_q = [&](int s) { return tiles + (size_t)s * kSS; };
-    auto stage_k = [&](int s) { return tiles + (size_t)s * kSS + (MODE == MODE_OUTPUT ? kTile : 0); };
+    auto stage_k = [&](int s) { return tiles + (size_t)s * kSS + kTile; };
     auto stage_v = [&](int s) { return stage_k(s) + kTile; };
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {  // ring barriers, one per stage
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
-            mbar_init(&sm.pq_ready[s], MODE == MODE_OUTPUT ? 1 : 2);  // SEG_STATE: both groups scale K
-            mbar_init(&sm.w_ready[s], 1);
+            mbar_init(&sm.pq_ready[s], 1);
         }
         for (int s = 0; s < 2; ++s) {  // double-buffered per-chunk barriers
             mbar_init(&sm.o_free[s], 1);
@@ -211,30 +189,15 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     volatile int *abort_flag = &sm.abort_flag;
-    // Programmatic dependent launch.  SEG_STATE (launched as a dependent of whatever
-    // ran before, e.g. the previous layer's OUTPUT grid) waits for it before touching
-    // global memory, and only then lets its own OUTPUT grid start: that grid's TMA
-    // producer reads q, k, v at once, which is safe because everything before this
-    // grid has completed by then.  OUTPUT lets the next kernel (the next call's
-    // SEG_STATE) start its prologue on idle SMs right away; that kernel waits too.
-    if (MODE == MODE_SEG_STATE) {
-        asm volatile("griddepcontrol.wait;\n" ::: "memory");
-        // this call's "segment 0 holds the initial state" flag starts cleared; the
-        // OUTPUT grid, which sets and reads it, starts only after every CTA here has
-        // passed this point
-        if (p == 0 && tid == 0) {
-            *reinterpret_cast<volatile int *>(seg0_read + bh) = 0;
-            __threadfence();
-        }
-        __syncthreads();
-    }
+    // Programmatic dependent launch.  With P > 1 this grid is a dependent of the
+    // segment-state grid, which waited for whatever ran before it before letting this
+    // grid start: so the TMA producer reads q, k, v at once, and only E, G and the
+    // state wait (state warps, segments p > 0).  This grid lets the next kernel (the
+    // next call's segment-state grid) start its prologue on idle SMs right away; that
+    // kernel waits too.
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
-    // chunk order: OUTPUT forwards, SEG_STATE backwards (running suffix decay)
-    auto chunk_start = [&](int i) {
-        int c = (MODE == MODE_OUTPUT) ? i : (nchunks - 1 - i);
-        return t_begin + c * kC;
-    };
+    auto chunk_start = [&](int i) { return t_begin + i * kC; };
     auto chunk_log_gate = [&](int n0, int row) {
         return (n0 + row < N) ? log_gate(logits[((size_t)b * N + n0 + row) * H + h], inv_tau) : 0.f;
     };
@@ -244,20 +207,17 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (lane == 0) {
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            if (MODE == MODE_OUTPUT) {
-                tma_prefetch_desc(&tm_q);
-                tma_prefetch_desc(&tm_o);
-            }
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_o);
             // every q, k, v line is read once per pass and every o line written once:
             // all of them are marked first to leave L2 (measured: 0.235 -> 0.221 ms per
-            // 32K x 24 x 128 layer; keeping the SEG_STATE tiles for the OUTPUT pass with
-            // evict-last was slower at every fraction of L2 tried)
+            // 32K x 24 x 128 layer; keeping the segment-state pass's k, v tiles for this
+            // pass with evict-last was slower at every fraction of L2 tried)
             const uint64_t pol = l2_policy_evict_first();
-            // OUTPUT: Q and K complete `full`, V completes `full_v`.  The V slot doubles as
-            // the staging buffer of the output rows of the chunk NS back: this thread
-            // stores them (TMA) and waits for the store to read the slot before it loads
-            // the next V there, so the state warps never wait on a store.  SEG_STATE: K
-            // and V complete `full`.
+            // Q and K complete `full`, V completes `full_v`.  The V slot doubles as the
+            // staging buffer of the output rows of the chunk NS back: this thread stores
+            // them (TMA) and waits for the store to read the slot before it loads the next
+            // V there, so the state warps never wait on a store.
             auto store_out = [&](int c) {  // chunk c's staged output rows -> o
                 const int sc_ = c % NS;
                 if (!mbar_wait(&sm.o_staged[sc_], (c / NS) & 1, abort_flag)) {
@@ -280,32 +240,25 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
                 for (int half = 0; half < 2; ++half) {
                     tma_load_4d_hint(stage_k(s) + half * kHalf, &tm_k, &sm.full[s], half * 64, h, n0, b, pol);
-                    if (MODE == MODE_OUTPUT)
-                        tma_load_4d_hint(stage_q(s) + half * kHalf, &tm_q, &sm.full[s], half * 64, h, n0, b, pol);
-                    else
-                        tma_load_4d_hint(stage_v(s) + half * kHalf, &tm_v, &sm.full[s], half * 64, h, n0, b, pol);
+                    tma_load_4d_hint(stage_q(s) + half * kHalf, &tm_q, &sm.full[s], half * 64, h, n0, b, pol);
                 }
-                if (MODE == MODE_OUTPUT) {
-                    if (i >= NS) {
-                        if (!store_out(i - NS)) break;
-                        bulk_wait_read_all();  // the slot has been read: V(i) may land in it
-                    }
-                    mbar_arrive_expect_tx(&sm.full_v[s], kTile);
-                    for (int half = 0; half < 2; ++half)
-                        tma_load_4d_hint(stage_v(s) + half * kHalf, &tm_v, &sm.full_v[s], half * 64, h, n0, b, pol);
+                if (i >= NS) {
+                    if (!store_out(i - NS)) break;
+                    bulk_wait_read_all();  // the slot has been read: V(i) may land in it
                 }
+                mbar_arrive_expect_tx(&sm.full_v[s], kTile);
+                for (int half = 0; half < 2; ++half)
+                    tma_load_4d_hint(stage_v(s) + half * kHalf, &tm_v, &sm.full_v[s], half * 64, h, n0, b, pol);
             }
             // leave no copy in flight: wait for the last loads of each stage
             for (int i = max(0, nchunks - NS); i < nchunks; ++i) {
                 mbar_wait(&sm.full[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
-                if (MODE == MODE_OUTPUT) mbar_wait(&sm.full_v[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
+                mbar_wait(&sm.full_v[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
             }
-            if (MODE == MODE_OUTPUT) {
-                // the output rows of the last NS chunks, then every store complete before exit
-                for (int c = max(0, nchunks - NS); c < nchunks && !*abort_flag; ++c)
-                    if (!store_out(c)) break;
-                bulk_wait_all();
-            }
+            // the output rows of the last NS chunks, then every store complete before exit
+            for (int c = max(0, nchunks - NS); c < nchunks && !*abort_flag; ++c)
+                if (!store_out(c)) break;
+            bulk_wait_all();
         }
     } else if (warp == 9) {
         // --------------------------------------------------------- MMA issuer
@@ -319,65 +272,54 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const int s = i % NS, ob = i & 1;
                 const uint32_t q_a = smem_u32(stage_q(s)), k_a = smem_u32(stage_k(s)), v_a = smem_u32(stage_v(s));
                 if (!(ok = mbar_wait(&sm.full[s], (i / NS) & 1, abort_flag))) break;
-                if (MODE == MODE_OUTPUT) {
-                    // P of the previous chunk (TMEM columns of A) must have been consumed
-                    if (i > 0 && !(ok = mbar_wait(&sm.p_free, (i - 1) & 1, abort_flag))) break;
-                    tc_fence_after();
-                    for (int kk = 0; kk < 8; ++kk) {  // MMA1: A = Q K^T
-                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        mma_ss(tmem + kColA, smem_desc_sw128(q_a + off, 16, 1024), smem_desc_sw128(k_a + off, 16, 1024),
-                               id_qk, kk > 0);
-                    }
-                    mma_commit(&sm.as_full);
+                // P of the previous chunk (TMEM columns of A) must have been consumed
+                if (i > 0 && !(ok = mbar_wait(&sm.p_free, (i - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk) {  // MMA1: A = Q K^T
+                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    mma_ss(tmem + kColA, smem_desc_sw128(q_a + off, 16, 1024), smem_desc_sw128(k_a + off, 16, 1024),
+                           id_qk, kk > 0);
                 }
-                if (MODE == MODE_OUTPUT) {
-                    // the decay warps publish the chunk's total decay first: it decides the order
-                    if (!(ok = mbar_wait(&sm.bc_ready[i & 1], (i / 2) & 1, abort_flag))) break;
-                    const bool factor = sm.bcr[i & 3] > kFactorMin;
-                    if (i >= 2 && !(ok = mbar_wait(&sm.o_free[ob], ((i / 2) - 1) & 1, abort_flag))) break;
-                    const uint32_t o_t = tmem + kColO + 128 * ob;
-                    const uint32_t s_a = smem_u32(Sbuf);
-                    auto mma3 = [&]() {  // O = Q S  (Q' = diag(e^b) Q in direct chunks)
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                            mma_ss(o_t, smem_desc_sw128(q_a + off, 16, 1024),
-                                   smem_desc_sw128(s_a + kk * 2048, kHalf, 1024), id_qs, kk > 0);
-                        }
-                    };
-                    if (!factor) {  // Q is rescaled in place together with P
-                        if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
+                mma_commit(&sm.as_full);
+                // the decay warps publish the chunk's total decay first: it decides the order
+                if (!(ok = mbar_wait(&sm.bc_ready[i & 1], (i / 2) & 1, abort_flag))) break;
+                const bool factor = sm.bcr[i & 3] > kFactorMin;
+                if (i >= 2 && !(ok = mbar_wait(&sm.o_free[ob], ((i / 2) - 1) & 1, abort_flag))) break;
+                const uint32_t o_t = tmem + kColO + 128 * ob;
+                const uint32_t s_a = smem_u32(Sbuf);
+                auto mma3 = [&]() {  // O = Q S  (Q' = diag(e^b) Q in direct chunks)
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        mma_ss(o_t, smem_desc_sw128(q_a + off, 16, 1024),
+                               smem_desc_sw128(s_a + kk * 2048, kHalf, 1024), id_qs, kk > 0);
                     }
-                    // the cross term needs nothing else from the decay warps: it fills the P bubble
-                    if (!(ok = mbar_wait(&sm.s_ready, i & 1, abort_flag))) break;
-                    tc_fence_after();
-                    mma3();
-                    if (!(ok = mbar_wait(&sm.k_ready[s], (i / NS) & 1, abort_flag))) break;
-                    if (!(ok = mbar_wait(&sm.full_v[s], (i / NS) & 1, abort_flag))) break;
-                    if (i > 0 && !(ok = mbar_wait(&sm.u_free, (i - 1) & 1, abort_flag))) break;
-                    tc_fence_after();
-                    for (int kk = 0; kk < 8; ++kk)  // MMA4: U = K'^T V
-                        mma_ss(tmem + kColU, smem_desc_sw128(k_a + kk * 2048, kHalf, 1024),
-                               smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_kv, kk > 0);
-                    mma_commit(&sm.u_full);
-                    if (factor) {
-                        if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
-                        tc_fence_after();
-                    }
-                    for (int kk = 0; kk < 8; ++kk)  // MMA2: O += P V
-                        mma_ts(o_t, tmem + kColA + kk * 8, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_pv, 1);
-                    mma_commit(&sm.o_full[ob]);
-                    mma_commit(&sm.p_free);
-                } else {
+                };
+                if (!factor) {  // Q is rescaled in place together with P
+                    if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
+                }
+                // the cross term needs nothing else from the decay warps: it fills the P bubble
+                if (!(ok = mbar_wait(&sm.s_ready, i & 1, abort_flag))) break;
+                tc_fence_after();
+                mma3();
+                if (!(ok = mbar_wait(&sm.k_ready[s], (i / NS) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sm.full_v[s], (i / NS) & 1, abort_flag))) break;
+                if (i > 0 && !(ok = mbar_wait(&sm.u_free, (i - 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)  // MMA4: U = K'^T V
+                    mma_ss(tmem + kColU, smem_desc_sw128(k_a + kk * 2048, kHalf, 1024),
+                           smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_kv, kk > 0);
+                mma_commit(&sm.u_full);
+                if (factor) {
                     if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
                     tc_fence_after();
-                    for (int kk = 0; kk < 8; ++kk)  // E^T += V^T K''
-                        mma_ss(tmem + kColU, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024),
-                               smem_desc_sw128(k_a + kk * 2048, kHalf, 1024), id_kv, (i > 0 || kk > 0));
                 }
+                for (int kk = 0; kk < 8; ++kk)  // MMA2: O += P V
+                    mma_ts(o_t, tmem + kColA + kk * 8, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_pv, 1);
+                mma_commit(&sm.o_full[ob]);
+                mma_commit(&sm.p_free);
                 mma_commit(&sm.empty[s]);
             }
             if (!ok) report(err, &sm.abort_flag, 2);
-            if (MODE == MODE_SEG_STATE) mma_commit(&sm.u_full);
             // drain: nothing of ours may still run when TMEM is released
             mma_commit(&sm.drain);
             mbar_wait(&sm.drain, 0, abort_flag, 200000000ull);
@@ -387,7 +329,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int j = tid - 128;  // token row of the chunk = TMEM lane
         const int wq = warp - 4;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-        float suffix = 0.f;  // SEG_STATE: log decay of the chunks after this one
         float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), j) : 0.f;
         bool alive = true;
         for (int i = 0; i < nchunks && alive; ++i) {
@@ -396,18 +337,15 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const float bj = group_scan(lg_next, sm.wsum1, lane, wq, 1, bC);
             if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), j);  // in flight during this chunk
             const bool factor = (bC > kFactorMin);
-            if (MODE == MODE_OUTPUT) {
-                sm.ew[j] = factor ? __expf(-bj) : bj;
-                if (j == 0) {
-                    sm.bcr[i & 3] = bC;
-                    mbar_arrive(&sm.bc_ready[i & 1]);
-                }
+            sm.ew[j] = factor ? __expf(-bj) : bj;
+            if (j == 0) {
+                sm.bcr[i & 3] = bC;
+                mbar_arrive(&sm.bc_ready[i & 1]);
             }
             named_bar(1, 128);  // ew complete; wsum1 free for the next chunk
             bool ok = true;
             if (j == 0) {
-                ok = (MODE == MODE_OUTPUT) ? mbar_wait(&sm.as_full, i & 1, abort_flag)
-                                           : mbar_wait(&sm.full[s], (i / NS) & 1, abort_flag);
+                ok = mbar_wait(&sm.as_full, i & 1, abort_flag);
                 if (!ok) report(err, &sm.abort_flag, 3);
                 sm.go1 = ok && !*abort_flag;
             }
@@ -416,283 +354,226 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 alive = false;
                 break;
             }
-            if (MODE == MODE_OUTPUT) {
-                // K'_j = e^{b_C - b_j} k_j in place first: MMA4 and the state chain wait on it
-                scale_row_inplace(stage_k(s), j, __expf(bC - bj));
-                fence_proxy_async_smem();
-                named_bar(1, 128);
-                if (j == 0) mbar_arrive(&sm.k_ready[s]);
-                tc_fence_after();
-                // P row j over A row j, written in place as packed bf16 (keys 2c, 2c+1 in column c).
-                // The 32 rows of warp wq end in key block wq: blocks before it need no mask,
-                // blocks after it are zero and are not loaded.
+            // K'_j = e^{b_C - b_j} k_j in place first: MMA4 and the state chain wait on it
+            scale_row_inplace(stage_k(s), j, __expf(bC - bj));
+            fence_proxy_async_smem();
+            named_bar(1, 128);
+            if (j == 0) mbar_arrive(&sm.k_ready[s]);
+            tc_fence_after();
+            // P row j over A row j, written in place as packed bf16 (keys 2c, 2c+1 in column c).
+            // The 32 rows of warp wq end in key block wq: blocks before it need no mask,
+            // blocks after it are zero and are not loaded.
 #pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t pk[16];
-                    if (cb > wq) {
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t pk[16];
+                if (cb > wq) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                    for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                } else {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + kColA + lane_base + cb * 32, r);
+                    tmem_wait_ld();
+                    if (factor && cb < wq) {
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 w = *reinterpret_cast<const float4 *>(&sm.ew[cb * 32 + 4 * e4]);
+                            float v0, v1, v2, v3;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1])),
+                                             f2_pack(w.x, w.y)), v0, v1);
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3])),
+                                             f2_pack(w.z, w.w)), v2, v3);
+                            pk[2 * e4] = pack_bf16x2(v0, v1);
+                            pk[2 * e4 + 1] = pack_bf16x2(v2, v3);
+                        }
+                    } else if (factor) {
+#pragma unroll
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const int k0 = cb * 32 + 4 * e4;
+                            const float4 w = *reinterpret_cast<const float4 *>(&sm.ew[k0]);
+                            const float v0 = (k0 <= j) ? __uint_as_float(r[4 * e4]) * w.x : 0.f;
+                            const float v1 = (k0 + 1 <= j) ? __uint_as_float(r[4 * e4 + 1]) * w.y : 0.f;
+                            const float v2 = (k0 + 2 <= j) ? __uint_as_float(r[4 * e4 + 2]) * w.z : 0.f;
+                            const float v3 = (k0 + 3 <= j) ? __uint_as_float(r[4 * e4 + 3]) * w.w : 0.f;
+                            pk[2 * e4] = pack_bf16x2(v0, v1);
+                            pk[2 * e4 + 1] = pack_bf16x2(v2, v3);
+                        }
                     } else {
-                        uint32_t r[32];
-                        tmem_ld32(tmem + kColA + lane_base + cb * 32, r);
-                        tmem_wait_ld();
-                        if (factor && cb < wq) {
 #pragma unroll
-                            for (int e4 = 0; e4 < 8; ++e4) {
-                                const float4 w = *reinterpret_cast<const float4 *>(&sm.ew[cb * 32 + 4 * e4]);
-                                float v0, v1, v2, v3;
-                                f2_unpack(f2_mul(f2_pack(__uint_as_float(r[4 * e4]), __uint_as_float(r[4 * e4 + 1])),
-                                                 f2_pack(w.x, w.y)), v0, v1);
-                                f2_unpack(f2_mul(f2_pack(__uint_as_float(r[4 * e4 + 2]), __uint_as_float(r[4 * e4 + 3])),
-                                                 f2_pack(w.z, w.w)), v2, v3);
-                                pk[2 * e4] = pack_bf16x2(v0, v1);
-                                pk[2 * e4 + 1] = pack_bf16x2(v2, v3);
-                            }
-                        } else if (factor) {
-#pragma unroll
-                            for (int e4 = 0; e4 < 8; ++e4) {
-                                const int k0 = cb * 32 + 4 * e4;
-                                const float4 w = *reinterpret_cast<const float4 *>(&sm.ew[k0]);
-                                const float v0 = (k0 <= j) ? __uint_as_float(r[4 * e4]) * w.x : 0.f;
-                                const float v1 = (k0 + 1 <= j) ? __uint_as_float(r[4 * e4 + 1]) * w.y : 0.f;
-                                const float v2 = (k0 + 2 <= j) ? __uint_as_float(r[4 * e4 + 2]) * w.z : 0.f;
-                                const float v3 = (k0 + 3 <= j) ? __uint_as_float(r[4 * e4 + 3]) * w.w : 0.f;
-                                pk[2 * e4] = pack_bf16x2(v0, v1);
-                                pk[2 * e4 + 1] = pack_bf16x2(v2, v3);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int k0 = cb * 32 + 2 * e;
-                                const float v0 = (k0 <= j) ? __uint_as_float(r[2 * e]) * __expf(bj - sm.ew[k0]) : 0.f;
-                                const float v1 = (k0 + 1 <= j) ? __uint_as_float(r[2 * e + 1]) * __expf(bj - sm.ew[k0 + 1]) : 0.f;
-                                pk[e] = pack_bf16x2(v0, v1);
-                            }
+                        for (int e = 0; e < 16; ++e) {
+                            const int k0 = cb * 32 + 2 * e;
+                            const float v0 = (k0 <= j) ? __uint_as_float(r[2 * e]) * __expf(bj - sm.ew[k0]) : 0.f;
+                            const float v1 = (k0 + 1 <= j) ? __uint_as_float(r[2 * e + 1]) * __expf(bj - sm.ew[k0 + 1]) : 0.f;
+                            pk[e] = pack_bf16x2(v0, v1);
                         }
                     }
-                    tmem_st16(tmem + kColA + lane_base + cb * 16, pk);  // columns already read
                 }
-                tmem_wait_st();
-                tc_fence_before();
-                if (!factor) scale_row_inplace(stage_q(s), j, __expf(bj));  // Q'_j = e^{b_j} q_j
-            } else {
-                // weight of token j: decay from j to the segment end; the state warps
-                // scale the second 64 columns of every row with the same weights
-                const float w = __expf(suffix + (bC - bj));
-                float *wring = reinterpret_cast<float *>(Sbuf) + s * kC;  // Sbuf is unused here; one slot per stage
-                wring[j] = w;
-                named_bar(1, 128);
-                if (j == 0) mbar_arrive(&sm.w_ready[s]);
-                scale_row_block(stage_k(s), j, w, 0);
-                suffix += bC;
+                tmem_st16(tmem + kColA + lane_base + cb * 16, pk);  // columns already read
             }
+            tmem_wait_st();
+            tc_fence_before();
+            if (!factor) scale_row_inplace(stage_q(s), j, __expf(bj));  // Q'_j = e^{b_j} q_j
             fence_proxy_async_smem();
             named_bar(1, 128);
             if (j == 0) mbar_arrive(&sm.pq_ready[s]);
         }
-        if (MODE == MODE_SEG_STATE && j == 0) G[bhp] = suffix;
     } else {
         // ------------------------------------------------------- state warps
         const int t = tid;  // TMEM lane: d_k row t of S and U
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        if (MODE == MODE_OUTPUT) {
-            float S[kD];  // row t of the state, fp32
-            // Segment 0 starts from the caller's state and reads it directly, so it runs
-            // alongside the SEG_STATE grid; later segments need that grid's end states
-            // (and its copy of the caller's state): they wait for it
-            if (p > 0) asm volatile("griddepcontrol.wait;\n" ::: "memory");
-            {
-                // initial state of this segment: the caller's state, advanced over the
-                // earlier segments with their zero-start end states E_q and decays G_q
-                const float *init = (p == 0) ? state + bh * kD * kD : E + (bh * P + P - 1) * kD * kD;
-                const float4 *src = reinterpret_cast<const float4 *>(init + (size_t)t * kD);
+        float S[kD];  // row t of the state, fp32
+        // Segment 0 starts from the caller's state and reads it directly, so it runs
+        // alongside the segment-state grid; later segments need that grid's end states
+        // (and its copy of the caller's state): they wait for it
+        if (p > 0) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        {
+            // initial state of this segment: the caller's state, advanced over the
+            // earlier segments with their zero-start end states E_q and decays G_q
+            const float *init = (p == 0) ? state + bh * kD * kD : E + (bh * P + P - 1) * kD * kD;
+            const float4 *src = reinterpret_cast<const float4 *>(init + (size_t)t * kD);
+#pragma unroll
+            for (int c4 = 0; c4 < kD / 4; ++c4) {
+                const float4 x = __ldcg(src + c4);
+                S[4 * c4] = x.x; S[4 * c4 + 1] = x.y; S[4 * c4 + 2] = x.z; S[4 * c4 + 3] = x.w;
+            }
+#pragma unroll 1
+            for (int q = 0; q < p; ++q) {
+                const float g = __expf(G[bh * P + q]);
+                const float4 *eq = reinterpret_cast<const float4 *>(E + (bh * P + q) * kD * kD + (size_t)t * kD);
 #pragma unroll
                 for (int c4 = 0; c4 < kD / 4; ++c4) {
-                    const float4 x = __ldcg(src + c4);
-                    S[4 * c4] = x.x; S[4 * c4 + 1] = x.y; S[4 * c4 + 2] = x.z; S[4 * c4 + 3] = x.w;
-                }
-#pragma unroll 1
-                for (int q = 0; q < p; ++q) {
-                    const float g = __expf(G[bh * P + q]);
-                    const float4 *eq = reinterpret_cast<const float4 *>(E + (bh * P + q) * kD * kD + (size_t)t * kD);
-#pragma unroll
-                    for (int c4 = 0; c4 < kD / 4; ++c4) {
-                        const float4 x = eq[c4];
-                        S[4 * c4] = fmaf(g, S[4 * c4], x.x);
-                        S[4 * c4 + 1] = fmaf(g, S[4 * c4 + 1], x.y);
-                        S[4 * c4 + 2] = fmaf(g, S[4 * c4 + 2], x.z);
-                        S[4 * c4 + 3] = fmaf(g, S[4 * c4 + 3], x.w);
-                    }
+                    const float4 x = eq[c4];
+                    S[4 * c4] = fmaf(g, S[4 * c4], x.x);
+                    S[4 * c4 + 1] = fmaf(g, S[4 * c4 + 1], x.y);
+                    S[4 * c4 + 2] = fmaf(g, S[4 * c4 + 2], x.z);
+                    S[4 * c4 + 3] = fmaf(g, S[4 * c4 + 3], x.w);
                 }
             }
-            auto put_state = [&]() {  // bf16 row t of S into the N-major B tile
+        }
+        auto put_state = [&]() {  // bf16 row t of S into the N-major B tile
 #pragma unroll
-                for (int ch = 0; ch < 16; ++ch) {
-                    uint4 v = make_uint4(pack_bf16x2(S[8 * ch], S[8 * ch + 1]), pack_bf16x2(S[8 * ch + 2], S[8 * ch + 3]),
-                                         pack_bf16x2(S[8 * ch + 4], S[8 * ch + 5]), pack_bf16x2(S[8 * ch + 6], S[8 * ch + 7]));
-                    *reinterpret_cast<uint4 *>(Sbuf + tile_chunk(t, ch)) = v;
-                }
-                fence_proxy_async_smem();
-            };
-            put_state();
-            named_bar(2, 128);
-            if (t == 0) {
-                mbar_arrive(&sm.s_ready);
-                // the caller's state is in registers now: the last segment may overwrite it
-                if (p == 0 && P > 1) {
-                    __threadfence();
-                    atomicExch(seg0_read + bh, 1);
-                }
+            for (int ch = 0; ch < 16; ++ch) {
+                uint4 v = make_uint4(pack_bf16x2(S[8 * ch], S[8 * ch + 1]), pack_bf16x2(S[8 * ch + 2], S[8 * ch + 3]),
+                                     pack_bf16x2(S[8 * ch + 4], S[8 * ch + 5]), pack_bf16x2(S[8 * ch + 6], S[8 * ch + 7]));
+                *reinterpret_cast<uint4 *>(Sbuf + tile_chunk(t, ch)) = v;
             }
-            float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), t) : 0.f;
-            for (int i = 0; i < nchunks; ++i) {
-                const int s = i % NS;
-                // the chunk's decay, computed here too (cheap) so no ring is shared with the decay warps
-                float bC;
-                const float bt = group_scan(lg_next, sm.wsum0, lane, warp, 2, bC);
-                if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), t);
-                const float sc = (bC > kFactorMin) ? __expf(bt) : 1.f;  // output row scale
-                const uint64_t sc2 = f2_pack(sc, sc);
-                bool ok = true;
-                if (t == 0) {
-                    ok = mbar_wait(&sm.u_full, i & 1, abort_flag);
-                    if (!ok) report(err, &sm.abort_flag, 4);
-                    sm.go0 = ok && !*abort_flag;
-                }
-                named_bar(2, 128);
-                if (!sm.go0) break;
-                tc_fence_after();
-                const float ebC = __expf(bC);
-                const uint64_t ebC2 = f2_pack(ebC, ebC);
-#pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + kColU + lane_base + cb * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2)  // S <- e^{b_C} S + U, two columns per packed FMA
-                        f2_unpack(f2_fma(ebC2, f2_pack(S[cb * 32 + e], S[cb * 32 + e + 1]),
-                                         f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1]))),
-                                  S[cb * 32 + e], S[cb * 32 + e + 1]);
-                }
-                tc_fence_before();
-                if (i + 1 < nchunks) put_state();  // MMA3 of this chunk is done (u_full)
-                named_bar(2, 128);
-                if (t == 0) {
-                    mbar_arrive(&sm.u_free);
-                    if (i + 1 < nchunks) mbar_arrive(&sm.s_ready);
-                }
-                // output rows o_t = e^{b_t} O_t (or O_t), staged as bf16 in this chunk's
-                // V slot (free once MMA2 is done); the TMA producer thread stores them
-                if (t == 0) {
-                    ok = mbar_wait(&sm.o_full[i & 1], (i / 2) & 1, abort_flag);
-                    if (!ok) report(err, &sm.abort_flag, 6);
-                    sm.go0 = ok && !*abort_flag;
-                }
-                named_bar(2, 128);
-                if (!sm.go0) break;
-                tc_fence_after();
-                {
-                    uint8_t *stage_o = stage_v(s);
-                    const uint32_t o_t = tmem + kColO + 128 * (i & 1) + lane_base;
-#pragma unroll 1
-                    for (int cb = 0; cb < 4; ++cb) {
-                        uint32_t r[32];
-                        tmem_ld32(o_t + cb * 32, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {  // two columns per packed multiply
-                                float y0, y1;
-                                f2_unpack(f2_mul(f2_pack(__uint_as_float(r[8 * q4 + 2 * e]),
-                                                         __uint_as_float(r[8 * q4 + 2 * e + 1])), sc2), y0, y1);
-                                w[e] = pack_bf16x2(y0, y1);
-                            }
-                            *reinterpret_cast<uint4 *>(stage_o + tile_chunk(t, cb * 4 + q4)) =
-                                make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    }
-                    tc_fence_before();
-                    fence_proxy_async_smem();
-                    named_bar(2, 128);
-                    if (t == 0) {
-                        mbar_arrive(&sm.o_free[i & 1]);
-                        mbar_arrive(&sm.o_staged[s]);  // the TMA producer stores the rows
-                    }
-                }
+            fence_proxy_async_smem();
+        };
+        put_state();
+        named_bar(2, 128);
+        if (t == 0) {
+            mbar_arrive(&sm.s_ready);
+            // the caller's state is in registers now: the last segment may overwrite it
+            if (p == 0 && P > 1) {
+                __threadfence();
+                atomicExch(seg0_read + bh, 1);
             }
-            named_bar(2, 128);
-            if (t == 0) sm.go0 = !*abort_flag;
-            named_bar(2, 128);
-            if (p == P - 1 && sm.go0 && P > 1) {
-                // segment 0 of this (b, h) must have read the caller's state first
-                if (t == 0) {
-                    bool seen = false;
-                    uint64_t t0;
-                    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-                    for (uint32_t it = 0; !seen; ++it) {
-                        seen = *reinterpret_cast<volatile int *>(seg0_read + bh) == 1;
-                        if (!seen && (it & 63) == 63) {
-                            uint64_t tn;
-                            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tn));
-                            if (*abort_flag || tn - t0 > 2000000000ull) break;
-                        }
-                    }
-                    if (!seen) report(err, &sm.abort_flag, 11);
-                    __threadfence();
-                    sm.go0 = seen;
-                }
-                named_bar(2, 128);
-            }
-            if (p == P - 1 && sm.go0) {  // the last segment's end state is the call's final state
-                float4 *dst = reinterpret_cast<float4 *>(state + bh * kD * kD + (size_t)t * kD);
-#pragma unroll
-                for (int c4 = 0; c4 < kD / 4; ++c4) dst[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
-            }
-        } else {
-            if (p == 0) {  // keep the caller's initial state: the OUTPUT pass overwrites `state`
-                const float4 *src = reinterpret_cast<const float4 *>(state + bh * kD * kD + (size_t)t * kD);
-                float4 *dst = reinterpret_cast<float4 *>(E + (bh * P + P - 1) * kD * kD + (size_t)t * kD);
-#pragma unroll 4
-                for (int c4 = 0; c4 < kD / 4; ++c4) dst[c4] = src[c4];
-            }
+        }
+        float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), t) : 0.f;
+        for (int i = 0; i < nchunks; ++i) {
+            const int s = i % NS;
+            // the chunk's decay, computed here too (cheap) so no ring is shared with the decay warps
+            float bC;
+            const float bt = group_scan(lg_next, sm.wsum0, lane, warp, 2, bC);
+            if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), t);
+            const float sc = (bC > kFactorMin) ? __expf(bt) : 1.f;  // output row scale
+            const uint64_t sc2 = f2_pack(sc, sc);
             bool ok = true;
-            for (int i = 0; i < nchunks; ++i) {
-                const int s = i % NS;
-                if (t == 0) {
-                    ok = mbar_wait(&sm.w_ready[s], (i / NS) & 1, abort_flag);
-                    if (!ok) report(err, &sm.abort_flag, 10);
-                    sm.go0 = ok && !*abort_flag;
-                }
-                named_bar(2, 128);
-                if (!sm.go0) break;
-                const float *wring = reinterpret_cast<const float *>(Sbuf) + s * kC;
-                scale_row_block(stage_k(s), t, wring[t], 1);
-                fence_proxy_async_smem();
-                named_bar(2, 128);
-                if (t == 0) mbar_arrive(&sm.pq_ready[s]);
-            }
             if (t == 0) {
-                ok = mbar_wait(&sm.u_full, 0, abort_flag, 4000000000ull);
-                if (!ok) report(err, &sm.abort_flag, 5);
+                ok = mbar_wait(&sm.u_full, i & 1, abort_flag);
+                if (!ok) report(err, &sm.abort_flag, 4);
                 sm.go0 = ok && !*abort_flag;
             }
             named_bar(2, 128);
-            if (sm.go0) {
-                // E^T row t (lane = d_v column t) -> E[i][t]
-                tc_fence_after();
+            if (!sm.go0) break;
+            tc_fence_after();
+            const float ebC = __expf(bC);
+            const uint64_t ebC2 = f2_pack(ebC, ebC);
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t r[32];
+                tmem_ld32(tmem + kColU + lane_base + cb * 32, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; e += 2)  // S <- e^{b_C} S + U, two columns per packed FMA
+                    f2_unpack(f2_fma(ebC2, f2_pack(S[cb * 32 + e], S[cb * 32 + e + 1]),
+                                     f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1]))),
+                              S[cb * 32 + e], S[cb * 32 + e + 1]);
+            }
+            tc_fence_before();
+            if (i + 1 < nchunks) put_state();  // MMA3 of this chunk is done (u_full)
+            named_bar(2, 128);
+            if (t == 0) {
+                mbar_arrive(&sm.u_free);
+                if (i + 1 < nchunks) mbar_arrive(&sm.s_ready);
+            }
+            // output rows o_t = e^{b_t} O_t (or O_t), staged as bf16 in this chunk's
+            // V slot (free once MMA2 is done); the TMA producer thread stores them
+            if (t == 0) {
+                ok = mbar_wait(&sm.o_full[i & 1], (i / 2) & 1, abort_flag);
+                if (!ok) report(err, &sm.abort_flag, 6);
+                sm.go0 = ok && !*abort_flag;
+            }
+            named_bar(2, 128);
+            if (!sm.go0) break;
+            tc_fence_after();
+            {
+                uint8_t *stage_o = stage_v(s);
+                const uint32_t o_t = tmem + kColO + 128 * (i & 1) + lane_base;
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t r[32];
-                    tmem_ld32(tmem + kColU + lane_base + cb * 32, r);
+                    tmem_ld32(o_t + cb * 32, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        E[bhp * kD * kD + (size_t)(cb * 32 + e) * kD + t] = __uint_as_float(r[e]);
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {  // two columns per packed multiply
+                            float y0, y1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[8 * q4 + 2 * e]),
+                                                     __uint_as_float(r[8 * q4 + 2 * e + 1])), sc2), y0, y1);
+                            w[e] = pack_bf16x2(y0, y1);
+                        }
+                        *reinterpret_cast<uint4 *>(stage_o + tile_chunk(t, cb * 4 + q4)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+                tc_fence_before();
+                fence_proxy_async_smem();
+                named_bar(2, 128);
+                if (t == 0) {
+                    mbar_arrive(&sm.o_free[i & 1]);
+                    mbar_arrive(&sm.o_staged[s]);  // the TMA producer stores the rows
                 }
             }
+        }
+        named_bar(2, 128);
+        if (t == 0) sm.go0 = !*abort_flag;
+        named_bar(2, 128);
+        if (p == P - 1 && sm.go0 && P > 1) {
+            // segment 0 of this (b, h) must have read the caller's state first
+            if (t == 0) {
+                bool seen = false;
+                uint64_t t0;
+                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+                for (uint32_t it = 0; !seen; ++it) {
+                    seen = *reinterpret_cast<volatile int *>(seg0_read + bh) == 1;
+                    if (!seen && (it & 63) == 63) {
+                        uint64_t tn;
+                        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tn));
+                        if (*abort_flag || tn - t0 > 2000000000ull) break;
+                    }
+                }
+                if (!seen) report(err, &sm.abort_flag, 11);
+                __threadfence();
+                sm.go0 = seen;
+            }
+            named_bar(2, 128);
+        }
+        if (p == P - 1 && sm.go0) {  // the last segment's end state is the call's final state
+            float4 *dst = reinterpret_cast<float4 *>(state + bh * kD * kD + (size_t)t * kD);
+#pragma unroll
+            for (int c4 = 0; c4 < kD / 4; ++c4) dst[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
         }
     }
 
@@ -700,6 +581,211 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------
+// Segment end states, read-only over k and v: for segment p of (b, h),
+//     E_p = sum_j (prod_{m > j, m in segment} gamma_m) k_j^T v_j,   G_p = sum_j log gamma_j,
+// walking the segment's 128-token chunks backwards (the running suffix decay
+// weights each token).  The pass streams k and v and does little per byte, so a
+// ring slot should be held for as few hand-offs as possible: every token's weight
+// is computed from the gate logits before its chunk lands, and the moment it lands
+// the eight scale warps rescale K in place (thread = one row-half) and announce it;
+// the MMA E^T += V^T (w . K) into TMEM (lane = d_v) then frees the slot.
+constexpr int kSegStages = 3;
+constexpr int kSegThreads = 320;              // warps 0-7 scale, 8 TMA, 9 MMA
+constexpr int kSegScale = 256;
+
+struct SegSmem {
+    uint64_t full[kSegStages], empty[kSegStages], scaled[kSegStages], e_full;
+    uint32_t tmem_base;
+    int abort_flag;
+    int go;
+    float wsum[2][8];
+};
+
+constexpr size_t kSegSmemBytes = (size_t)kSegStages * 2 * kTile + sizeof(SegSmem) + 1024;
+static_assert(kSegSmemBytes <= kTcSmemBytes, "segment-state ring + control block must fit");
+
+__global__ void __launch_bounds__(kSegThreads, 1)
+gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const float *__restrict__ logits, float inv_tau, const float *__restrict__ state,
+                float *__restrict__ E, float *__restrict__ G, int *__restrict__ seg0_read, int N, int H, int seg_len,
+                int P, int *err) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t *tiles = smem_raw + pad;
+    SegSmem &sm = *reinterpret_cast<SegSmem *>(tiles + (size_t)kSegStages * 2 * kTile);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int p = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int t_begin = p * seg_len;
+    const int nch = (min(N, t_begin + seg_len) - t_begin + kC - 1) / kC;
+    const size_t bh = (size_t)b * H + h;
+    const size_t bhp = bh * P + p;
+    auto stage_k = [&](int s) { return tiles + (size_t)s * 2 * kTile; };
+    auto stage_v = [&](int s) { return tiles + (size_t)s * 2 * kTile + kTile; };
+    auto chunk_at = [&](int i) { return t_begin + (nch - 1 - i) * kC; };  // backwards
+
+    if (tid == 0) {
+        for (int s = 0; s < kSegStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+            mbar_init(&sm.scaled[s], 1);
+        }
+        mbar_init(&sm.e_full, 1);
+        sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&sm.tmem_base, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    volatile int *abort_flag = &sm.abort_flag;
+    // Programmatic dependent launch: wait for the previous kernel before any global
+    // access; clear this call's "segment 0 has read the caller's state" flag, then let
+    // the OUTPUT grid (which sets and reads it) start.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (p == 0 && tid == 0) {
+        *reinterpret_cast<volatile int *>(seg0_read + bh) = 0;
+        __threadfence();
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
+    if (warp == 8) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            const uint64_t pol = l2_policy_evict_first();
+            int i = 0;
+            for (; i < nch; ++i) {
+                const int s = i % kSegStages;
+                if (i >= kSegStages && !mbar_wait(&sm.empty[s], ((i / kSegStages) + 1) & 1, abort_flag)) {
+                    report(err, &sm.abort_flag, 31);
+                    break;
+                }
+                const int n0 = chunk_at(i);
+                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
+                for (int half = 0; half < 2; ++half) {
+                    tma_load_4d_hint(stage_k(s) + half * kHalf, &tm_k, &sm.full[s], half * 64, h, n0, b, pol);
+                    tma_load_4d_hint(stage_v(s) + half * kHalf, &tm_v, &sm.full[s], half * 64, h, n0, b, pol);
+                }
+            }
+            // leave no copy in flight (bounded by time only: an abort must still wait)
+            volatile int no_abort = 0;
+            for (int k = max(0, i - kSegStages); k < i; ++k)
+                mbar_wait(&sm.full[k % kSegStages], (k / kSegStages) & 1, &no_abort, 200000000ull);
+        }
+    } else if (warp == 9) {
+        // -------------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t id_kv = idesc_bf16_f32(kD, kD, true, true);  // A = V^T (M-major), B = K'' (N-major)
+            bool ok = true;
+            for (int i = 0; i < nch; ++i) {
+                const int s = i % kSegStages;
+                if (!(ok = mbar_wait(&sm.scaled[s], (i / kSegStages) & 1, abort_flag))) break;
+                tc_fence_after();
+                const uint32_t k_a = smem_u32(stage_k(s)), v_a = smem_u32(stage_v(s));
+                for (int kk = 0; kk < 8; ++kk)  // E^T += V^T K'', 16 tokens per MMA
+                    mma_ss(tmem, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024),
+                           smem_desc_sw128(k_a + kk * 2048, kHalf, 1024), id_kv, (i > 0 || kk > 0));
+                mma_commit(&sm.empty[s]);
+            }
+            if (!ok) report(err, &sm.abort_flag, 32);
+            mma_commit(&sm.e_full);  // also: nothing of ours runs once it completes
+        }
+    } else {
+        // --------------------------------------------- scale warps (0-7)
+        // thread u: row r = u % 128 of the chunk, column half u / 128 of K; warp w scans
+        // rows 32 (w % 4) .. 32 (w % 4) + 31
+        const int r = tid & (kC - 1), hf = tid >> 7, wr = warp & 3;
+        auto log_gate_at = [&](int n0) {
+            const int n = n0 + r;
+            return (n < N) ? log_gate(logits[((size_t)b * N + n) * H + h], inv_tau) : 0.f;
+        };
+        float suffix = 0.f;  // log decay of the chunks after this one
+        float lg_next = (nch > 0) ? log_gate_at(chunk_at(0)) : 0.f;
+        bool alive = true;
+        for (int i = 0; i < nch && alive; ++i) {
+            const int s = i % kSegStages;
+            float x = lg_next;
+            if (i + 1 < nch) lg_next = log_gate_at(chunk_at(i + 1));  // in flight during this chunk
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            if (lane == 31) sm.wsum[i & 1][warp] = x;
+            named_bar(1, kSegScale);
+            float pre = 0.f, bC = 0.f;
+#pragma unroll
+            for (int w4 = 0; w4 < 4; ++w4) {
+                const float t = sm.wsum[i & 1][w4];
+                bC += t;
+                if (w4 < wr) pre += t;
+            }
+            // weight of token r: decay from r (exclusive) to the segment end
+            const float w = __expf(suffix + (bC - (x + pre)));
+            suffix += bC;
+            if (tid == 0) {
+                const bool ok = mbar_wait(&sm.full[s], (i / kSegStages) & 1, abort_flag);
+                if (!ok) report(err, &sm.abort_flag, 33);
+                sm.go = ok && !*abort_flag;
+            }
+            named_bar(1, kSegScale);
+            if (!sm.go) {
+                alive = false;
+                break;
+            }
+            {  // row r, columns 64 hf .. 64 hf + 63 of K, in place (128-byte swizzle)
+                const __nv_bfloat162 w2 = __float2bfloat162_rn(w);
+                uint8_t *row = stage_k(s) + hf * kHalf + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 *q = reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) * 16));
+                    *q = scale_bf16x8(*q, w2);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar(1, kSegScale);
+            if (tid == 0) mbar_arrive(&sm.scaled[s]);
+        }
+        if (tid == 0) G[bhp] = suffix;
+        if (p == 0 && tid < kD) {  // keep the caller's initial state: the OUTPUT pass overwrites `state`
+            const float4 *src = reinterpret_cast<const float4 *>(state + bh * kD * kD + (size_t)tid * kD);
+            float4 *dst = reinterpret_cast<float4 *>(E + (bh * P + P - 1) * kD * kD + (size_t)tid * kD);
+#pragma unroll 4
+            for (int c4 = 0; c4 < kD / 4; ++c4) dst[c4] = src[c4];
+        }
+        if (tid == 0) {
+            const bool ok = mbar_wait(&sm.e_full, 0, abort_flag, 4000000000ull);
+            if (!ok) report(err, &sm.abort_flag, 34);
+            sm.go = ok && !*abort_flag;
+        }
+        named_bar(1, kSegScale);
+        if (sm.go && alive && tid < kD) {
+            // E^T row tid (lane = d_v column tid) -> E[d_k][d_v]
+            tc_fence_after();
+            const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + cb * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) E[bhp * kD * kD + (size_t)(cb * 32 + e) * kD + tid] = __uint_as_float(v[e]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 }  // namespace yoco
@@ -774,14 +860,13 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     int *seg0_read = reinterpret_cast<int *>(G + (size_t)a.B * a.H * P);
     const float inv_tau = 1.0f / a.tau;
     cudaError_t e;
-    e = cudaFuncSetAttribute(gret_tc_kernel<MODE_OUTPUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
+    e = cudaFuncSetAttribute(gret_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gret_tc_kernel<MODE_SEG_STATE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kTcSmemBytes);
+    e = cudaFuncSetAttribute(gret_seg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSegSmemBytes);
     if (e != cudaSuccess) return e;
     if (P == 1) {
         count_launches(1);
-        gret_tc_kernel<MODE_OUTPUT><<<dim3(a.B * a.H), kTcThreads, kTcSmemBytes, st>>>(
+        gret_tc_kernel<<<dim3(a.B * a.H), kTcThreads, kTcSmemBytes, st>>>(
             mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err);
         return cudaGetLastError();
     }
@@ -796,17 +881,19 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // SEG_STATE: its prologue overlaps the previous kernel's tail; it waits for it
+    // segment states: the prologue overlaps the previous kernel's tail; it waits for it
     // before reading anything
     cfg.gridDim = dim3(P - 1, a.H, a.B);
-    e = cudaLaunchKernelEx(&cfg, gret_tc_kernel<MODE_SEG_STATE>, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)nullptr,
-                           a.state, E, G, seg0_read, a.N, a.H, seg_len, P, err);
+    cfg.dynamicSmemBytes = kSegSmemBytes;
+    e = cudaLaunchKernelEx(&cfg, gret_seg_kernel, mk, mv, a.logits, inv_tau, (const float *)a.state, E, G, seg0_read,
+                           a.N, a.H, seg_len, P, err);
     if (e != cudaSuccess) return e;
-    // OUTPUT starts on the SMs SEG_STATE leaves free: its segment-0 CTAs (first in
+    cfg.dynamicSmemBytes = kTcSmemBytes;
+    // the output grid starts on the SMs the segment-state grid leaves free: its segment-0 CTAs (first in
     // the grid) run the whole segment meanwhile; the others begin loading and wait
-    // for SEG_STATE before touching E, G and `state`
+    // for the segment states before touching E, G and `state`
     cfg.gridDim = dim3(P * a.B * a.H);
-    return cudaLaunchKernelEx(&cfg, gret_tc_kernel<MODE_OUTPUT>, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o,
+    return cudaLaunchKernelEx(&cfg, gret_tc_kernel, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o,
                               a.state, E, G, seg0_read, a.N, a.H, seg_len, P, err);
 }
 
