@@ -66,10 +66,12 @@ struct TcSmem {
     int go0, go1;  // per-group continue decisions (written by one thread, read by all after a barrier)
     float wsum0[4], wsum1[4];
     float bcr[4];  // chunk total log decay b_C, ring over chunks
-    float ew[kC];  // e^{-b_k} (factored chunks) or b_k (direct chunks)
+    alignas(16) float ew[kC];  // e^{-b_k} (factored chunks) or b_k (direct chunks); read as float4
+    int pref_ok;   // the head's prefix states are complete (segments p > 0)
 
 };
 
+static_assert(offsetof(TcSmem, ew) % 16 == 0, "ew is read as float4");
 constexpr size_t kTileBytes = (size_t)kStages * 3 * kTile + kTile;  // Q,K,V per stage + bf16 state
 constexpr size_t kTcSmemBytes = 232448;                            // the sm_100 per-block maximum
 static_assert(kTileBytes + sizeof(TcSmem) + 1024 <= kTcSmemBytes, "tiles + control block + alignment slack must fit");
@@ -125,12 +127,71 @@ __device__ __forceinline__ float group_scan(float x, float *wsum, int lane, int 
     return x + pre;
 }
 
+// Prefix states of the segments of one (b, h): S_in(0) = the caller's state (kept in
+// slot P-1 of E), S_in(q) = e^{G_{q-1}} S_in(q-1) + E_{q-1} for q = 1 .. P-1, written over
+// slot q-1.  The output CTAs of segments 1 .. P-1 compute them together, CTA p taking
+// rows [r0, r1) of every S_in, so each reads about two states' worth instead of folding
+// p + 1 whole states; every element is read and written by one thread only.  u is this
+// thread's index among the n threads of the CTA that take part.  The arithmetic is the
+// fold each segment would do on its own (fmaf(e^{G_q}, S, E_q) in order of q).
+constexpr int kPrefItems = 4, kPrefQ = 6;
+
+__device__ __forceinline__ void seg_prefix_rows(float *E, const float *G, size_t bh, int P, int p, int u, int n) {
+    constexpr size_t F4 = (size_t)kD * kD / 4;
+    const int r0 = (p - 1) * kD / (P - 1), r1 = p * kD / (P - 1);
+    const int items = (r1 - r0) * (kD / 4);
+    float4 *base = reinterpret_cast<float4 *>(E) + bh * P * F4 + (size_t)r0 * (kD / 4);
+    const float *g_bh = G + bh * P;
+    for (int i0 = u; i0 < items; i0 += n * kPrefItems) {
+        float4 sv[kPrefItems];
+#pragma unroll
+        for (int k = 0; k < kPrefItems; ++k) {
+            const int it = i0 + k * n;
+            sv[k] = (it < items) ? __ldcg(base + (size_t)(P - 1) * F4 + it) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int q0 = 0; q0 < P - 1; q0 += kPrefQ) {
+            float4 x[kPrefItems][kPrefQ];
+            float g[kPrefQ];
+#pragma unroll
+            for (int qb = 0; qb < kPrefQ; ++qb) {
+                const int q = q0 + qb;
+                g[qb] = (q < P - 1) ? __ldcg(g_bh + q) : 0.f;
+#pragma unroll
+                for (int k = 0; k < kPrefItems; ++k) {
+                    const int it = i0 + k * n;
+                    x[k][qb] = (q < P - 1 && it < items) ? __ldcg(base + (size_t)q * F4 + it)
+                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int qb = 0; qb < kPrefQ; ++qb) {
+                const int q = q0 + qb;
+                if (q < P - 1) {
+                    const float gq = __expf(g[qb]);
+#pragma unroll
+                    for (int k = 0; k < kPrefItems; ++k) {
+                        const int it = i0 + k * n;
+                        if (it < items) {
+                            sv[k].x = fmaf(gq, sv[k].x, x[k][qb].x);
+                            sv[k].y = fmaf(gq, sv[k].y, x[k][qb].y);
+                            sv[k].z = fmaf(gq, sv[k].z, x[k][qb].z);
+                            sv[k].w = fmaf(gq, sv[k].w, x[k][qb].w);
+                            base[(size_t)q * F4 + it] = sv[k];
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
 gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const float *__restrict__ logits, float inv_tau,
                bf16_t *__restrict__ o, float *__restrict__ state, float *__restrict__ E, float *__restrict__ G,
-               int *__restrict__ seg0_read, int N, int H, int seg_len, int P, int *err) {
+               int *__restrict__ seg0_read, int *__restrict__ scan_count, int N, int H, int seg_len, int P,
+               int *err) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_u32 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base_u32 & 1023u)) & 1023u;
@@ -200,6 +261,34 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto chunk_start = [&](int i) { return t_begin + i * kC; };
     auto chunk_log_gate = [&](int n0, int row) {
         return (n0 + row < N) ? log_gate(logits[((size_t)b * N + n0 + row) * H + h], inv_tau) : 0.f;
+    };
+    // Segments p > 0: after the segment-state grid, the state and decay warps (256 threads)
+    // compute this CTA's rows of the head's prefix states, then wait until the head's
+    // other P - 2 output CTAs have too.  `scan_count` is cleared by the segment-state grid
+    // before it lets this grid start; the wait is bounded (error 12).
+    auto segment_prefix = [&](int u) {
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        seg_prefix_rows(E, G, bh, P, p, u, 256);
+        __threadfence();  // this thread's rows are visible to the head's other CTAs
+        named_bar(3, 256);
+        if (tid == 0) {
+            atomicAdd(scan_count + bh, 1);
+            bool seen = false;
+            uint64_t t0;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+            for (uint32_t it = 0; !seen; ++it) {
+                seen = *reinterpret_cast<volatile int *>(scan_count + bh) >= P - 1;
+                if (!seen && (it & 63) == 63) {
+                    uint64_t tn;
+                    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tn));
+                    if (*abort_flag || tn - t0 > 2000000000ull) break;
+                }
+            }
+            if (!seen) report(err, &sm.abort_flag, 12);
+            __threadfence();
+            sm.pref_ok = seen;
+        }
+        named_bar(3, 256);
     };
 
     if (warp == 8) {
@@ -329,6 +418,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int j = tid - 128;  // token row of the chunk = TMEM lane
         const int wq = warp - 4;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        if (p > 0) segment_prefix(128 + j);  // chunk 0 needs the folded state first anyway
         float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), j) : 0.f;
         bool alive = true;
         for (int i = 0; i < nchunks && alive; ++i) {
@@ -422,31 +512,19 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         float S[kD];  // row t of the state, fp32
         // Segment 0 starts from the caller's state and reads it directly, so it runs
-        // alongside the segment-state grid; later segments need that grid's end states
-        // (and its copy of the caller's state): they wait for it
-        if (p > 0) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        // alongside the segment-state grid; later segments need that grid's end states:
+        // they wait for it, fold their rows of the head's prefix states with the decay
+        // warps and the head's other output CTAs, then read their own
+        if (p > 0) segment_prefix(t);
         {
-            // initial state of this segment: the caller's state, advanced over the
-            // earlier segments with their zero-start end states E_q and decays G_q
-            const float *init = (p == 0) ? state + bh * kD * kD : E + (bh * P + P - 1) * kD * kD;
+            // initial state of this segment: the caller's state (p = 0), or the caller's
+            // state advanced over the earlier segments (prefix state p, in slot p - 1)
+            const float *init = (p == 0) ? state + bh * kD * kD : E + (bh * P + p - 1) * kD * kD;
             const float4 *src = reinterpret_cast<const float4 *>(init + (size_t)t * kD);
 #pragma unroll
             for (int c4 = 0; c4 < kD / 4; ++c4) {
                 const float4 x = __ldcg(src + c4);
                 S[4 * c4] = x.x; S[4 * c4 + 1] = x.y; S[4 * c4 + 2] = x.z; S[4 * c4 + 3] = x.w;
-            }
-#pragma unroll 1
-            for (int q = 0; q < p; ++q) {
-                const float g = __expf(G[bh * P + q]);
-                const float4 *eq = reinterpret_cast<const float4 *>(E + (bh * P + q) * kD * kD + (size_t)t * kD);
-#pragma unroll
-                for (int c4 = 0; c4 < kD / 4; ++c4) {
-                    const float4 x = eq[c4];
-                    S[4 * c4] = fmaf(g, S[4 * c4], x.x);
-                    S[4 * c4 + 1] = fmaf(g, S[4 * c4 + 1], x.y);
-                    S[4 * c4 + 2] = fmaf(g, S[4 * c4 + 2], x.z);
-                    S[4 * c4 + 3] = fmaf(g, S[4 * c4 + 3], x.w);
-                }
             }
         }
         auto put_state = [&]() {  // bf16 row t of S into the N-major B tile
@@ -610,8 +688,8 @@ static_assert(kSegSmemBytes <= kTcSmemBytes, "segment-state ring + control block
 __global__ void __launch_bounds__(kSegThreads, 1)
 gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const float *__restrict__ logits, float inv_tau, const float *__restrict__ state,
-                float *__restrict__ E, float *__restrict__ G, int *__restrict__ seg0_read, int N, int H, int seg_len,
-                int P, int *err) {
+                float *__restrict__ E, float *__restrict__ G, int *__restrict__ seg0_read,
+                int *__restrict__ scan_count, int N, int H, int seg_len, int P, int *err) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
@@ -646,11 +724,13 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const uint32_t tmem = sm.tmem_base;
     volatile int *abort_flag = &sm.abort_flag;
     // Programmatic dependent launch: wait for the previous kernel before any global
-    // access; clear this call's "segment 0 has read the caller's state" flag, then let
-    // the OUTPUT grid (which sets and reads it) start.
+    // access; clear this call's "segment 0 has read the caller's state" flag and the
+    // head's prefix-state arrival count, then let the output grid (which sets and reads
+    // them) start.
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     if (p == 0 && tid == 0) {
         *reinterpret_cast<volatile int *>(seg0_read + bh) = 0;
+        *reinterpret_cast<volatile int *>(scan_count + bh) = 0;
         __threadfence();
     }
     __syncthreads();
@@ -842,7 +922,7 @@ size_t gret_tc_workspace(int B, int N, int H, int dk, int dv) {
     (void)dk; (void)dv;
     int P = tc_segments(B, N, H);
     size_t ws = 256;  // status word
-    if (P > 1) ws += ((size_t)B * H * P * kD * kD + (size_t)B * H * P) * sizeof(float) + (size_t)B * H * sizeof(int);
+    if (P > 1) ws += ((size_t)B * H * P * kD * kD + (size_t)B * H * P) * sizeof(float) + 2 * (size_t)B * H * sizeof(int);
     return ws;
 }
 
@@ -858,6 +938,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     float *E = (float *)((char *)ws + 256);
     float *G = E + (size_t)a.B * a.H * P * kD * kD;
     int *seg0_read = reinterpret_cast<int *>(G + (size_t)a.B * a.H * P);
+    int *scan_count = seg0_read + (size_t)a.B * a.H;
     const float inv_tau = 1.0f / a.tau;
     cudaError_t e;
     e = cudaFuncSetAttribute(gret_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
@@ -867,7 +948,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     if (P == 1) {
         count_launches(1);
         gret_tc_kernel<<<dim3(a.B * a.H), kTcThreads, kTcSmemBytes, st>>>(
-            mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err);
+            mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, nullptr, nullptr, a.N, a.H, seg_len, 1, err);
         return cudaGetLastError();
     }
     // end states of segments 0 .. P-2 (the last segment's is computed by the OUTPUT pass)
@@ -885,7 +966,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     // before reading anything
     cfg.gridDim = dim3(P - 1, a.H, a.B);
     cfg.dynamicSmemBytes = kSegSmemBytes;
-    e = cudaLaunchKernelEx(&cfg, gret_seg_kernel, mk, mv, a.logits, inv_tau, (const float *)a.state, E, G, seg0_read,
+    e = cudaLaunchKernelEx(&cfg, gret_seg_kernel, mk, mv, a.logits, inv_tau, (const float *)a.state, E, G, seg0_read, scan_count,
                            a.N, a.H, seg_len, P, err);
     if (e != cudaSuccess) return e;
     cfg.dynamicSmemBytes = kTcSmemBytes;
@@ -894,7 +975,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     // for the segment states before touching E, G and `state`
     cfg.gridDim = dim3(P * a.B * a.H);
     return cudaLaunchKernelEx(&cfg, gret_tc_kernel, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o,
-                              a.state, E, G, seg0_read, a.N, a.H, seg_len, P, err);
+                              a.state, E, G, seg0_read, scan_count, a.N, a.H, seg_len, P, err);
 }
 
 }  // namespace yoco_host
