@@ -145,9 +145,9 @@ def run_reference(args):
 
 # DRAM bytes of one gRet prefill call on the bench's layer shape (32768 x 24 x 128, bf16),
 # from one ncu capture of the current kernels: dram__bytes_read.sum + dram__bytes_write.sum
-# of the segment-state launch (342.4 + 3.1 MB) and the output launch (618.3 + 147.5 MB).
+# of the segment-state launch (342.4 + 2.8 MB) and the output launch (618.2 + 155.9 MB).
 # Must be re-captured (or set to None) whenever gret_tc.cu changes.
-GRET_CALL_DRAM_BYTES = 1111.4e6
+GRET_CALL_DRAM_BYTES = 1119.3e6
 
 
 def aggregate_over_ranks(elapsed_s, units_per_rank, dist=None, device="cpu"):
