@@ -67,7 +67,6 @@ struct TcSmem {
     float wsum0[4], wsum1[4];
     float bcr[4];  // chunk total log decay b_C, ring over chunks
     alignas(16) float ew[kC];  // e^{-b_k} (factored chunks) or b_k (direct chunks); read as float4
-    int pref_ok;   // the head's prefix states are complete (segments p > 0)
 
 };
 
@@ -284,9 +283,8 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (*abort_flag || tn - t0 > 2000000000ull) break;
                 }
             }
-            if (!seen) report(err, &sm.abort_flag, 12);
+            if (!seen) report(err, &sm.abort_flag, 12);  // the chunk loops then stop at once
             __threadfence();
-            sm.pref_ok = seen;
         }
         named_bar(3, 256);
     };
