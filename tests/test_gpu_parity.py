@@ -122,6 +122,21 @@ def test_gret_prefill_bf16_tensor_core_shapes(Y, B, N, H, with_state):
     Y.yoco_workspace_status(ws)  # no bounded wait gave up
 
 
+@pytest.mark.parametrize("B,N,H", [(1, 128 * 100 + 33, 1), (2, 300, 38)])
+def test_gret_prefill_bf16_segment_prefix_extremes(Y, B, N, H):
+    """The output CTAs of a head fold the segment states together, each taking a
+    slice of the state's rows: one head over 101 chunks (101 one-chunk segments,
+    so each CTA folds one or two rows across 100 states) and 76 heads (two
+    segments, so one CTA folds all 128 rows), both from an initial state."""
+    d = 128
+    host, dev = gret_inputs(37, B, N, H, d, "bf16", logit_mean=2.0)
+    S0 = synth.normal(SEED, sid(37, 1, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
+    o, S = run_prefill(Y, dev, B, N, H, d, "bf16", S0=S0)
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0, S0=S0)
+    assert rel_l2(o, o_ref) <= BF16_REL_L2
+    assert rel_l2(S, S_ref) <= BF16_REL_L2
+
+
 def test_gret_prefill_bf16_many_segments_state_and_strong_decay(Y):
     """Many segments per head with an initial state and a stretch of near-zero
     gates inside a segment (B=2, N=7600, 4 heads: 15 segments of 4
