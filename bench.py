@@ -1,18 +1,18 @@
 #!/usr/bin/env python
 """Throughput of the YOCO token-mixing hot path on one GB300 (per rank).
 
-One step = one YOCO-3B-shaped request with early exit, at the 32K-token
-single-layer gRet shape (B=1, N=32768, 24 heads x 128) stacked to the model's
-13 self-decoder and 13 cross-decoder layers, plus the first generated token:
+One step = one YOCO-3B-shaped 512K-token prompt with early exit (the paper's
+Section 2.3, Fig. 3: the cross-decoder runs only for the last prompt token):
 
-  prefill  13 x chunkwise gRet over 32768 tokens (per-layer q, k, v, gate logits)
-           shared K^/V^ projection of M [32768, 3072] (RMSNorm, W_K/W_V 3072->8x128)
-           13 x cross attention for the last prompt token (24 q heads, GQA 3:1)
-  token    13 x recurrent gRet step, 1-slot append, 13 x split-KV cross decode
+  13 x chunkwise gRet over 524288 tokens (24 heads x 128; per-layer q, k, v, logits)
+  shared K^/V^ projection of M [524288, 3072] (RMSNorm, W_K/W_V 3072 -> 8 x 128)
+  13 x cross attention for the last prompt token (24 q heads, GQA 3:1)
 
-value = prompt tokens per second over the timed steps (inputs resident in HBM),
-e2e   = the same with every step's inputs copied from pinned host memory and the
-        final outputs copied back inside the timed region.
+value  = prompt tokens per second over the timed steps (inputs resident in HBM);
+e2e    = the same with the step's inputs copied from pinned host memory and the
+         cross layers' outputs copied back, inside the timed region;
+decode = generated tokens per second at a 1M-token context: 13 recurrent gRet
+         steps, a one-slot append and 13 split-KV cross layers per token.
 --impl reference times the CPU oracle on a bounded sample of the same step.
 
 Multi-GPU: replicas only (independent requests per GPU); value sums all ranks.
@@ -31,11 +31,20 @@ sys.path.insert(0, ROOT)
 
 METRIC = "gRet prefill tok/s + shared-KV decode tok/s (1 GB300), % of TC/HBM roofline"
 SEED = 20240509
-B, N, H, D = 1, 32768, 24, 128
+B, N, H, D = 1, 524288, 24, 128            # the 512K prompt, one sequence
 L_SELF, L_CROSS = 13, 13
 DM, HKV, HQ = 3072, 8, 24
 TAU, EPS = 16.0, 1e-6
-CFG = 2  # stream-id tag of this workload's inputs
+CFG = 4                                     # stream-id tag of the 512K prompt's inputs
+N_DEC, CFG_DEC = 1048576, 5                 # the 1M-token decode context
+N_LAYER = 32768                             # --only: the single 32K-token gRet layer shape
+CFG_LAYER = 2
+
+# DRAM bytes of one gRet prefill call on the 512K layer (524288 x 24 x 128, bf16):
+# dram__bytes_read.sum + dram__bytes_write.sum of both launches of one call, from
+# the capture summarised in profiles/gret_tc_kernel_512k_x24_layer.md (the command
+# is given there).  None until a capture of the current kernels exists.
+GRET_CALL_DRAM_BYTES = None
 
 
 def parse():
@@ -45,18 +54,22 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["yoco", "reference"], default="yoco")
     p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--decode-tokens", type=int, default=20, help="timed tokens of the 1M-context decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk", type=int, default=0)
     p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode", "cross_prefill", "swa_prefill",
                                       "swa_decode", "gn_gate", "rope", "qkvg", "gret_decode_unfused",
                                       "gret_decode_gn"], default=None,
-                   help="time one call of the step on its bench shape (for profiling)")
+                   help="time one call kind on its own (for profiling)")
+    p.add_argument("--n", type=int, default=0, help="--only gret: tokens (default 32768)")
+    p.add_argument("--no-decay", action="store_true",
+                   help="--only gret: logits +inf (gamma = 1), the case where nothing is left out")
     p.add_argument("--cache-len", type=int, default=0,
-                   help="--only cross_decode: cache length (default: the step's prompt length)")
-    p.add_argument("--batch", type=int, default=0, help="--only cross_decode: sequences (default: the step's B)")
+                   help="--only cross_decode: cache length (default 32768)")
+    p.add_argument("--batch", type=int, default=0, help="--only cross_decode: sequences (default 1)")
     p.add_argument("--splits", type=int, default=0, help="--only cross_decode: key splits (default: automatic)")
     p.add_argument("--workload", choices=list(LONG_WORKLOADS), default=None,
-                   help="time one of the long-context workloads at the pages' sizes instead of the bench step "
+                   help="time one of the decode workloads at the pages' sizes instead of the bench step "
                         "(one JSON line per workload and batch; not the driver's line)")
     p.add_argument("--batches", default="1,8,32", help="--workload decode128k: batch sizes")
     p.add_argument("--rope-base", type=float, default=0.0,
@@ -65,90 +78,110 @@ def parse():
 
 
 def workload_config(chunk_used):
-    return {"workload": "yoco3b_prefill32k_early_exit_plus_1_token", "B": B, "N": N, "self_layers": L_SELF,
-            "gret_heads": H, "d": D, "chunk": chunk_used, "tau": TAU, "cross_layers": L_CROSS, "Hq": HQ,
-            "Hkv": HKV, "d_model": DM, "gate_logits": "N(2,1)", "qk": "N(0,1)/sqrt(128)", "v_M_Q": "N(0,1)",
-            "W": "N(0,0.02)", "l2": "no flush: each step reads 8.1 GB of inputs (> 129 MB L2)",
-            "parallelism": "replicas",
-            "cuda_graph": "the generated token's 13 recurrent gRet steps, captured once, replayed every step"}
+    return {"workload": "yoco3b_prefill512k_early_exit", "B": B, "N": N, "self_layers": L_SELF,
+            "gret_heads": H, "d": D, "chunk": chunk_used, "tau": TAU, "cross_layers": L_CROSS,
+            "cross_rows": 1, "Hq": HQ, "Hkv": HKV, "d_model": DM, "gate_logits": "N(2,1)",
+            "qk": "N(0,1)/sqrt(128)", "v_M_Q": "N(0,1)", "W": "N(0,0.02)",
+            "l2": "no flush: each step reads 129 GB of inputs (> 129 MB L2)", "parallelism": "replicas"}
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
 
 
 # ----------------------------------------------------------------- CPU oracle
 
-_CPU_INPUTS = {}
+SAMPLE_TOKENS, SAMPLE_ROWS, SAMPLE_KEYS = 4096, 64, 16384
 
 
 def _cpu_inputs(tokens, proj_rows, cross_keys):
-    """Seeded host inputs for the CPU sample (made once per process)."""
-    key = (tokens, proj_rows, cross_keys)
-    if key not in _CPU_INPUTS:
-        import synth
-        sid = synth.stream_id
-        f = synth.bf16_bits_to_f32
-        _CPU_INPUTS[key] = dict(
-            q=f(synth.normal(SEED, sid(CFG, 0, synth.T_Q), (1, tokens, H, D), "bf16", std=D ** -0.5)),
-            k=f(synth.normal(SEED, sid(CFG, 0, synth.T_K), (1, tokens, H, D), "bf16", std=D ** -0.5)),
-            v=f(synth.normal(SEED, sid(CFG, 0, synth.T_V), (1, tokens, H, D), "bf16")),
-            lg=synth.normal(SEED, sid(CFG, 0, synth.T_LOGIT), (1, tokens, H), "f32", mean=2.0),
-            M=f(synth.normal(SEED, sid(CFG, 0, synth.T_M), (proj_rows, DM), "bf16")),
-            W=f(synth.normal(SEED, sid(CFG, 0, synth.T_WK), (DM, 2 * HKV * D), "bf16", std=0.02)),
-            Kc=f(synth.normal(SEED, sid(CFG, 0, synth.T_CACHE_K), (1, HKV, cross_keys, D), "bf16")),
-            Vc=f(synth.normal(SEED, sid(CFG, 0, synth.T_CACHE_V), (1, HKV, cross_keys, D), "bf16")),
-            Qx=f(synth.normal(SEED, sid(CFG, 0, synth.T_QX), (1, 1, HQ, D), "bf16")))
-    return _CPU_INPUTS[key]
+    """Seeded host inputs of the CPU sample, drawn like the step's (same streams)."""
+    import synth
+    sid = synth.stream_id
+    f = synth.bf16_bits_to_f32
+    return dict(
+        q=f(synth.normal(SEED, sid(CFG, 0, synth.T_Q), (1, tokens, H, D), "bf16", std=D ** -0.5)),
+        k=f(synth.normal(SEED, sid(CFG, 0, synth.T_K), (1, tokens, H, D), "bf16", std=D ** -0.5)),
+        v=f(synth.normal(SEED, sid(CFG, 0, synth.T_V), (1, tokens, H, D), "bf16")),
+        lg=synth.normal(SEED, sid(CFG, 0, synth.T_LOGIT), (1, tokens, H), "f32", mean=2.0),
+        M=f(synth.normal(SEED, sid(CFG, 0, synth.T_M), (proj_rows, DM), "bf16")),
+        W=f(synth.normal(SEED, sid(CFG, 0, synth.T_WK), (DM, 2 * HKV * D), "bf16", std=0.02)),
+        Kc=f(synth.normal(SEED, sid(CFG, 0, synth.T_CACHE_K), (1, HKV, cross_keys, D), "bf16")),
+        Vc=f(synth.normal(SEED, sid(CFG, 0, synth.T_CACHE_V), (1, HKV, cross_keys, D), "bf16")),
+        Qx=f(synth.normal(SEED, sid(CFG, 0, synth.T_QX), (1, 1, HQ, D), "bf16")))
 
 
-def cpu_sample(tokens=1024, proj_rows=32, cross_keys=8192):
-    """Time the oracle, as it stands, on a bounded sample of one step and scale
-    it to a whole step.  Returns (seconds per step, description, cores)."""
+def cpu_sample(x, threads=0):
+    """Time the oracle, as it stands, on the bounded sample `x` (one gRet layer's
+    first SAMPLE_TOKENS tokens x 24 heads, SAMPLE_ROWS projection rows, one cross
+    row over SAMPLE_KEYS keys) and scale each part linearly to the whole step.
+    threads = 0: all the host cores the process may use.  Returns (seconds per
+    step, seconds the sample took, cores used)."""
     import oracle
-    x = _cpu_inputs(tokens, proj_rows, cross_keys)
-    oracle.lib()
+    cores = threads or len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
     t0 = time.perf_counter()
     oracle.gret_recurrent(x["q"], x["k"], x["v"], x["lg"], TAU)
-    t_gret = (time.perf_counter() - t0) / tokens           # per token, all heads, one layer
+    t_gret = time.perf_counter() - t0
     t0 = time.perf_counter()
     oracle.rmsnorm_proj(x["M"], x["W"], EPS)
-    t_proj = (time.perf_counter() - t0) / proj_rows         # per row, K and V
+    t_proj = time.perf_counter() - t0
     t0 = time.perf_counter()
-    oracle.cross_attn(x["Qx"], x["Kc"], x["Vc"], cross_keys - 1, D ** -0.5)
-    t_cross = (time.perf_counter() - t0) * (N / cross_keys)  # one row over N keys, one layer
-    step = L_SELF * t_gret * (N + 1) + t_proj * (N + 1) + 2 * L_CROSS * t_cross
-    desc = (f"oracle timed on {tokens} tokens x 24 heads of one gRet layer, {proj_rows} projection rows and one "
-            f"cross row over {cross_keys} keys; scaled linearly to 13 gRet layers x {N + 1} tokens, projection "
-            f"of {N + 1} rows and 26 cross rows over {N} keys")
-    cores = len(os.sched_getaffinity(0))
-    return step, desc, cores
+    oracle.cross_attn(x["Qx"], x["Kc"], x["Vc"], SAMPLE_KEYS - 1, D ** -0.5)
+    t_cross = time.perf_counter() - t0
+    step = (L_SELF * t_gret * (N / SAMPLE_TOKENS) + t_proj * (N / SAMPLE_ROWS)
+            + L_CROSS * t_cross * (N / SAMPLE_KEYS))
+    return step, t_gret + t_proj + t_cross, cores
+
+
+SAMPLE_DESC = (f"oracle timed on {SAMPLE_TOKENS} tokens x 24 heads of one gRet layer, {SAMPLE_ROWS} projection "
+               f"rows and one cross row over {SAMPLE_KEYS} keys; each part scaled linearly to the step "
+               f"(13 gRet layers x {N} tokens, {N} projection rows, 13 cross rows over {N} keys)")
+
+
+def cpu_baseline_block():
+    """The oracle on all host cores and on one core, each on the bounded sample."""
+    x = _cpu_inputs(SAMPLE_TOKENS, SAMPLE_ROWS, SAMPLE_KEYS)
+    step_all, sample_all, cores = cpu_sample(x)
+    step_one, sample_one, _ = cpu_sample(x, threads=1)
+    return {"value": N / step_all, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": SAMPLE_DESC,
+            "sample_s": round(sample_all, 3), "extrapolated_ms_per_step": round(step_all * 1e3, 1),
+            "single_thread": {"value": N / step_one, "unit": "tok/s", "cores": 1, "sample_s": round(sample_one, 3),
+                              "extrapolated_ms_per_step": round(step_one * 1e3, 1)}}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    times = []
+    x = _cpu_inputs(SAMPLE_TOKENS, SAMPLE_ROWS, SAMPLE_KEYS)
+    times, samples, cores = [], [], 1
     for i in range(args.warmup + args.steps):
-        step, desc, cores = cpu_sample()
+        step, sample, cores = cpu_sample(x)
         if i >= args.warmup:
             times.append(step)
+            samples.append(sample)
     t = statistics.mean(times)
     value = N / t
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(None),
-            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "config": workload_config("auto"),
+            "timing": (f"each step times the oracle on a bounded sample ({statistics.mean(samples):.2f} s of CPU "
+                       "work measured per step) and scales it to the whole step; ms_per_step is that "
+                       "extrapolation"),
+            "sample_s_per_step": round(statistics.mean(samples), 3),
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                             "sample": SAMPLE_DESC},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # --------------------------------------------------------------------- GPU arm
-
-# DRAM bytes of one gRet prefill call on the bench's layer shape (32768 x 24 x 128, bf16),
-# from one ncu capture of the current kernels: dram__bytes_read.sum + dram__bytes_write.sum
-# of the segment-state launch (342.4 + 2.8 MB) and the output launch (618.2 + 155.9 MB).
-# Must be re-captured (or set to None) whenever gret_tc.cu changes.
-GRET_CALL_DRAM_BYTES = 1119.3e6
-
 
 def aggregate_over_ranks(elapsed_s, units_per_rank, dist=None, device="cpu"):
     """Whole-job throughput of independent replicas: the units every rank
@@ -254,7 +287,7 @@ def run_gpu(args):
         t = torch.empty(shape, dtype=dtype, device=dev)
         return synth.fill_normal_(t, seed, stream, mean, std)
 
-    # ---- inputs (HBM resident)
+    # ---- the prompt's inputs (HBM resident): 13 layers of q, k, v, logits, M, W, queries
     q = [normal((B, N, H, D), bf, sid(CFG, l, synth.T_Q), std=D ** -0.5) for l in range(L_SELF)]
     k = [normal((B, N, H, D), bf, sid(CFG, l, synth.T_K), std=D ** -0.5) for l in range(L_SELF)]
     v = [normal((B, N, H, D), bf, sid(CFG, l, synth.T_V)) for l in range(L_SELF)]
@@ -263,44 +296,27 @@ def run_gpu(args):
     Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
     Wv = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WV), std=0.02)
     Qx = [normal((B, 1, HQ, D), bf, sid(CFG, l, synth.T_QX)) for l in range(L_CROSS)]
-    q1 = [normal((B, H, D), bf, sid(CFG, l, synth.T_Q, 1), std=D ** -0.5) for l in range(L_SELF)]
-    k1 = [normal((B, H, D), bf, sid(CFG, l, synth.T_K, 1), std=D ** -0.5) for l in range(L_SELF)]
-    v1 = [normal((B, H, D), bf, sid(CFG, l, synth.T_V, 1)) for l in range(L_SELF)]
-    lg1 = [normal((B, H), f32, sid(CFG, l, synth.T_LOGIT, 1), mean=2.0) for l in range(L_SELF)]
-    M1 = normal((B, 1, DM), bf, sid(CFG, 0, synth.T_M, 1))
-    Qd = [normal((B, HQ, D), bf, sid(CFG, l, synth.T_QX, 1)) for l in range(L_CROSS)]
-    # ---- outputs and state
-    o = [torch.empty(B, N, H, D, dtype=bf, device=dev) for _ in range(L_SELF)]
+    # ---- outputs and state: each layer's o is consumed before the next layer runs
+    o = torch.empty(B, N, H, D, dtype=bf, device=dev)
     S = [torch.zeros(B, H, D, D, dtype=f32, device=dev) for _ in range(L_SELF)]
     Ox = [torch.empty(B, 1, HQ, D, dtype=bf, device=dev) for _ in range(L_CROSS)]
-    o1 = [torch.empty(B, H, D, dtype=bf, device=dev) for _ in range(L_SELF)]
-    Od = [torch.empty(B, HQ, D, dtype=bf, device=dev) for _ in range(L_CROSS)]
     cache = Y.KVCache(B, HKV, D, N + 16, device=dev)
     cc = ctypes.byref(cache.c)
-    ws_g_n = L.yoco_gret_prefill_workspace_size(B, N, H, D, D, args.chunk, Y.YOCO_BF16)
-    ws_kv_n = L.yoco_shared_kv_workspace_size(B, N, DM, cc)
-    ws_a_n = L.yoco_cross_attn_workspace_size(B, HQ, 1, cc, 0)
-    ws = torch.empty(max(ws_g_n, ws_kv_n, ws_a_n, 256), dtype=torch.uint8, device=dev)
+    ws_n = max(L.yoco_gret_prefill_workspace_size(B, N, H, D, D, args.chunk, Y.YOCO_BF16),
+               L.yoco_shared_kv_workspace_size(B, N, DM, cc), L.yoco_cross_attn_workspace_size(B, HQ, 1, cc, 0), 256)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
     P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
     wsp, wsn = P(ws), ws.numel()
     stream = torch.cuda.current_stream(dev)
     stp = ctypes.c_void_p(stream.cuda_stream)
-    ev = {}
 
     def check(st, what):
         if st != 0:
             raise RuntimeError(f"{what}: {L.yoco_last_error().decode()}")
 
-    def gret_decode_layers(sp):
-        for l in range(L_SELF):
-            check(L.yoco_gret_decode_step(P(q1[l]), P(k1[l]), P(v1[l]), P(lg1[l]), TAU, P(S[l]), P(o1[l]), B, H, D,
-                                          D, 1, 1, sp), "gret decode")
-
-    decode_graph = []  # filled below: the 13 recurrent gRet steps as one CUDA graph
-
-    def step(timed_calls=None, marks=None, wait_layer=None, wait_rest=None):
+    def step(gret_events=None, marks=None, wait_layer=None, wait_rest=None):
         def mark(i):
             if marks is not None:
                 marks[i].record(stream)
@@ -309,15 +325,15 @@ def run_gpu(args):
         cache.len_dev.zero_()
         cache.c.len_host = 0
         mark(0)
-        if timed_calls is not None:
-            timed_calls[0].record(stream)  # the gRet phase as a whole: no event between its launches
+        if gret_events is not None:
+            gret_events[0].record(stream)  # the gRet phase as a whole: no event between its launches
         for l in range(L_SELF):
             if wait_layer is not None:
                 wait_layer(l)  # end to end: this layer's inputs have arrived
-            check(L.yoco_gret_prefill_chunkwise(P(q[l]), P(k[l]), P(v[l]), P(lg[l]), TAU, P(o[l]), P(S[l]), B, N,
-                                                H, D, D, args.chunk, 1, 1, wsp, wsn, stp), "gret prefill")
-        if timed_calls is not None:
-            timed_calls[1].record(stream)
+            check(L.yoco_gret_prefill_chunkwise(P(q[l]), P(k[l]), P(v[l]), P(lg[l]), TAU, P(o), P(S[l]), B, N, H, D,
+                                                D, args.chunk, 1, 1, wsp, wsn, stp), "gret prefill")
+        if gret_events is not None:
+            gret_events[1].record(stream)
         mark(1)
         if wait_rest is not None:
             wait_rest()
@@ -327,37 +343,11 @@ def run_gpu(args):
             check(L.yoco_cross_attn_prefill(P(Qx[l]), HQ, 1, N - 1, cc, D ** -0.5, P(Ox[l]), wsp, wsn, stp),
                   "cross prefill")
         mark(3)
-        if decode_graph:
-            decode_graph[0].replay()  # the 13 recurrent steps (their launches, captured once)
-        else:
-            gret_decode_layers(stp)
-        mark(4)
-        check(L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, cc, wsp, wsn, stp), "append 1")
-        mark(5)
-        for l in range(L_CROSS):
-            check(L.yoco_cross_attn_decode(P(Qd[l]), HQ, cc, D ** -0.5, 0, P(Od[l]), wsp, wsn, stp), "cross decode")
-        mark(6)
 
     def barrier():
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
-
-    # The generated token's 13 recurrent gRet steps do not depend on the cache
-    # length, so they are captured once as a CUDA graph (same buffers, same launches)
-    # and replayed every step: the step is then not bound by 13 host launches.
-    step()
-    torch.cuda.synchronize()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    g = torch.cuda.CUDAGraph()
-    n0 = L.yoco_launch_count()
-    with torch.cuda.graph(g, stream=cap):
-        gret_decode_layers(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
-    graph_launches = L.yoco_launch_count() - n0
-    stream.wait_stream(cap)
-    torch.cuda.synchronize()
-    decode_graph.append(g)
 
     # the clock sampler starts before the warm-up so that it is sampling when the
     # timed region begins; the summary keeps the samples stamped inside that region
@@ -368,17 +358,17 @@ def run_gpu(args):
         step()
     launches0 = L.yoco_launch_count()
     step()
-    launches_per_step = L.yoco_launch_count() - launches0 + graph_launches  # replays are not counted on the host
+    launches_per_step = L.yoco_launch_count() - launches0
     barrier()
 
     # ---- timed region: K steps, events around each step's gRet phase (13 calls back to back)
-    calls = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(args.steps)]
+    gret_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(args.steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     t_lo = time.monotonic()
     e0.record(stream)
     for i in range(args.steps):
-        step(calls[i])
+        step(gret_ev[i])
     e1.record(stream)
     barrier()
     t_hi = time.monotonic()
@@ -388,67 +378,59 @@ def run_gpu(args):
     value, elapsed = aggregate_over_ranks(elapsed, B * N * args.steps, dist, dev)
     ms_step = elapsed / args.steps * 1e3
     # average gRet call: each timed step's 13 back-to-back calls over 13 (events only around the phase)
-    gret_ms = statistics.mean(c[0].elapsed_time(c[1]) / L_SELF for c in calls)
+    gret_ms = statistics.mean(c[0].elapsed_time(c[1]) / L_SELF for c in gret_ev)
 
     # ---- per-phase split: one more (untimed) step with events between phases
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
-    phase_names = ["gret_prefill_x13", "kv_project_32k", "cross_last_row_x13", "gret_decode_x13",
-                   "kv_append_1", "cross_decode_x13"]
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    phase_names = ["gret_prefill_x13", "kv_project_512k", "cross_last_row_x13"]
     step(marks=marks)
     torch.cuda.synchronize()
     phases = {n: round(marks[i].elapsed_time(marks[i + 1]), 4) for i, n in enumerate(phase_names)}
 
     # ---- roofline of the dominant call: chunkwise gRet prefill, one layer
-    gret_bytes = 3 * B * N * H * D * 2 + B * N * H * D * 2 + B * N * H * 4 + 2 * B * H * D * D * 4
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except OSError:
-        pass
+    peaks = load_peaks()
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    # algorithmic bytes of one call: q, k, v read and o written (bf16), the gate
+    # logits (fp32), the state read and written (fp32)
+    gret_bytes = 3 * B * N * H * D * 2 + B * N * H * D * 2 + B * N * H * 4 + 2 * B * H * D * D * 4
     achieved = gret_bytes / (gret_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "yoco_gret_prefill_chunkwise (one layer: all of its launches; "
-                "average over the 13 back-to-back calls of each timed step)",
+    roofline = {"bound": "hbm", "kernel": "yoco_gret_prefill_chunkwise (one 524288 x 24 x 128 layer: all of its "
+                "launches; average over the 13 back-to-back calls of each timed step)",
                 "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                "peak_source": "MEASURED_PEAKS.json hbm_gbs (burst copy)" if "hbm_gbs" in peaks else "fallback",
+                "peak_source": ("MEASURED_PEAKS.json hbm_gbs (burst copy; of measured)" if "hbm_gbs" in peaks
+                                else "fallback 6.8 TB/s (of fallback)"),
                 "algorithmic_bytes_per_launch": gret_bytes, "avg_launch_ms": round(gret_ms, 4),
-                "traffic": GRET_CALL_DRAM_BYTES, "traffic_unit": "bytes per call (ncu dram read + write, both passes)"}
-    # the same call against the tensor cores: per token and head, the causal half of the
-    # chunk's QK^T and PV (2 d (C + 1)) plus the cross-chunk q S and the state update (4 d^2),
-    # at the chunk the tensor-core kernel runs (128); attainable = min(TC, AI x HBM)
-    chunk_tc = args.chunk if args.chunk else 128
-    gret_flops = B * N * H * (2 * D * (chunk_tc + 1) + 4 * D * D)
-    # timed inside a seconds-long step: the sustained bf16 figure
-    tc_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)) * 1e12
+                "traffic": GRET_CALL_DRAM_BYTES,
+                "traffic_unit": "bytes per call (ncu dram read + write, both launches)"}
+    # the same call against the tensor cores, on the algorithmic flops at the method's
+    # chunk of 64: per token and head the causal half of the chunk's QK^T and PV,
+    # 2 d (C + 1), plus the cross-chunk q S and the state update, 4 d^2
+    gret_flops = B * N * H * (2 * D * (64 + 1) + 4 * D * D)
+    kernel_flops = B * N * H * (2 * D * (128 + 1) + 4 * D * D)  # what the kernel issues at its 128-token chunks
+    tc_peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)) * 1e12  # inside a long step
     tflops = gret_flops / (gret_ms / 1e3)
     attainable = min(tc_peak, gret_flops / gret_bytes * hbm_peak * 1e9)
-    roofline.update({"flops_per_launch": gret_flops, "chunk": chunk_tc, "tc_achieved_tflops": round(tflops / 1e12, 1),
-                     "tc_peak_tflops": round(tc_peak / 1e12, 1), "tc_frac": round(tflops / tc_peak, 4),
-                     "tc_peak_source": ("MEASURED_PEAKS.json bf16_tflops_sustained" if "bf16_tflops_sustained" in peaks
-                                        else "fallback"),
+    roofline.update({"flops_per_launch": gret_flops, "flops_chunk": 64,
+                     "tc_achieved_tflops": round(tflops / 1e12, 1), "tc_peak_tflops": round(tc_peak / 1e12, 1),
+                     "tc_frac": round(tflops / tc_peak, 4),
+                     "tc_peak_source": ("MEASURED_PEAKS.json bf16_tflops_sustained (of measured)"
+                                        if "bf16_tflops_sustained" in peaks else "fallback"),
+                     "kernel_flops_per_launch_chunk128": kernel_flops,
+                     "kernel_tc_frac_chunk128": round(kernel_flops / (gret_ms / 1e3) / tc_peak, 4),
                      "arithmetic_intensity": round(gret_flops / gret_bytes, 1),
                      "attainable_frac": round(tflops / attainable, 4)})
+    proj_flops = 2.0 * N * DM * 2 * HKV * D
+    cross_bytes = N * HKV * D * 2 * 2
+    roof_step_ms = (L_SELF * gret_bytes / (hbm_peak * 1e9) + proj_flops / (peaks.get("bf16_tflops", 1900.0) * 1e12)
+                    + L_CROSS * cross_bytes / (hbm_peak * 1e9)) * 1e3
 
-    # ---- the generated token: 13 recurrent gRet steps, one append, 13 cross layers
-    dec_ms = phases["gret_decode_x13"] + phases["kv_append_1"] + phases["cross_decode_x13"]
-    cross_bytes = 2 * B * (N + 1) * HKV * D * 2
-    cross_call_ms = phases["cross_decode_x13"] / L_CROSS
-    cross_gbs = cross_bytes / (cross_call_ms / 1e3) / 1e9
-    decode = {"value": round(1e3 / dec_ms, 1), "unit": "tok/s", "context": N + 1, "B": B,
-              "ms_per_token": round(dec_ms, 4), "timed": "phase-split step (CUDA events between phases)",
-              "roofline_cross_decode": {
-                  "bound": "hbm", "kernel": "yoco_cross_attn_decode (split + combine)",
-                  "achieved": round(cross_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                  "frac": round(cross_gbs / hbm_peak, 4), "algorithmic_bytes_per_launch": cross_bytes,
-                  "avg_launch_ms": round(cross_call_ms, 4),
-                  "note": ("algorithmic bytes: the whole 134 MB cache per call; the 13 layers read the same "
-                           "cache, and the first keys of each head (half the L2, 64 MB) are loaded with normal "
-                           "L2 priority and the rest evict-first, so about half of each call's bytes come from "
-                           "L2 rather than HBM")}}
+    # ---- end to end: inputs from pinned host memory, results back to host
+    e2e = e2e_measure(args, torch, stream, step, q, k, v, lg, [M] + Qx, Ox)
+    del q, k, v, lg, M, o
+    torch.cuda.empty_cache()
 
-    # ---- end to end: inputs from pinned host memory, result back to host
-    e2e = e2e_measure(args, torch, stream, step, [q, k, v, lg], [M, q1, k1, v1, lg1, M1, Qx, Qd], [Ox[-1], Od[-1]])
+    # ---- generation at a 1M-token context
+    decode = decode_1m(args, torch, Y, dev, seed, hbm_peak)
 
     clocks = clk.summary(t_lo - 0.1, t_hi + 0.1)
     clocks["window_ms"] = round((t_hi - t_lo) * 1e3, 1)
@@ -456,13 +438,12 @@ def run_gpu(args):
            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
            "config": workload_config(args.chunk if args.chunk else "auto"),
-           "roofline": roofline, "e2e": e2e, "gpu_launches": int(launches_per_step * args.steps),
-           "gpu_launches_per_step": int(launches_per_step), "clocks": clocks, "phases_ms": phases,
-           "decode": decode}
+           "roofline": roofline, "step_roofline_ms": round(roof_step_ms, 3),
+           "step_frac_of_roofline": round(roof_step_ms / ms_step, 4), "e2e": e2e,
+           "gpu_launches": int(launches_per_step * args.steps), "gpu_launches_per_step": int(launches_per_step),
+           "clocks": clocks, "phases_ms": phases, "decode": decode}
     if rank == 0 and not args.no_cpu_baseline:
-        step_s, desc, cores = cpu_sample()
-        out["cpu_baseline"] = {"value": N / step_s, "unit": "tok/s", "cores": cores, "kind": "oracle",
-                               "sample": desc}
+        out["cpu_baseline"] = cpu_baseline_block()
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -470,25 +451,26 @@ def run_gpu(args):
         print(json.dumps(out), flush=True)
 
 
-def e2e_measure(args, torch, stream, step, big_lists, small, results):
-    """Same step with host->device copies of its inputs and a device->host read of
-    its final outputs inside the timed region.  The inputs stream in on a second
-    stream in the order the step uses them (the gRet layers' q, k, v, logits one
-    layer at a time, then the rest); the step waits for each layer's inputs
-    before that layer's call, so the copies of later layers overlap the compute
-    of earlier ones."""
+def e2e_measure(args, torch, stream, step, q, k, v, lg, rest, results):
+    """The step with a host->device copy of its inputs and a device->host read of
+    its results inside the timed region.  Host memory holds one gRet layer's q, k,
+    v and logits (pinned, 9.7 GB) and every layer's device inputs are copied from
+    it, so the bytes copied per step are the step's whole input (129 GB) without
+    holding 13 layers on the host.  The copies run on a second stream in the order
+    the step uses them and each layer's call waits for its own inputs only, so
+    later layers' copies overlap earlier layers' compute."""
     if args.e2e_steps <= 0:
         return None
-    per_layer = [[lst[l] for lst in big_lists] for l in range(len(big_lists[0]))]
-    rest = []
-    for x in small:
-        rest.extend(x if isinstance(x, list) else [x])
-    dev_tensors = [t for grp in per_layer for t in grp] + rest
-    host = {id(t): torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_tensors}
-    for t in dev_tensors:
-        host[id(t)].copy_(t)
+    host_layer = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q[0], k[0], v[0], lg[0])]
+    for h, t in zip(host_layer, (q[0], k[0], v[0], lg[0])):
+        h.copy_(t)
+    host_rest = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in rest]
+    for h, t in zip(host_rest, rest):
+        h.copy_(t)
     res_host = [torch.empty(r.shape, dtype=r.dtype, pin_memory=True) for r in results]
-    h2d = sum(t.numel() * t.element_size() for t in dev_tensors)
+    per_layer = [(q[l], k[l], v[l], lg[l]) for l in range(len(q))]
+    h2d = (sum(t.numel() * t.element_size() for grp in per_layer for t in grp)
+           + sum(t.numel() * t.element_size() for t in rest))
     d2h = sum(r.numel() * r.element_size() for r in results)
     copy_stream = torch.cuda.Stream()
     ev_layer = [torch.cuda.Event() for _ in per_layer]
@@ -500,11 +482,11 @@ def e2e_measure(args, torch, stream, step, big_lists, small, results):
         copy_stream.wait_stream(stream)  # the previous step has finished reading its inputs
         with torch.cuda.stream(copy_stream):
             for grp, ev in zip(per_layer, ev_layer):
-                for t in grp:
-                    t.copy_(host[id(t)], non_blocking=True)
+                for t, h in zip(grp, host_layer):
+                    t.copy_(h, non_blocking=True)
                 ev.record(copy_stream)
-            for t in rest:
-                t.copy_(host[id(t)], non_blocking=True)
+            for t, h in zip(rest, host_rest):
+                t.copy_(h, non_blocking=True)
             ev_rest.record(copy_stream)
         step(wait_layer=lambda l: stream.wait_event(ev_layer[l]), wait_rest=lambda: stream.wait_event(ev_rest))
         for h, r in zip(res_host, results):
@@ -514,7 +496,118 @@ def e2e_measure(args, torch, stream, step, big_lists, small, results):
     t = e0.elapsed_time(e1) / 1e3 / args.e2e_steps
     return {"value": B * N / t, "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": args.e2e_steps, "ms_per_step": t * 1e3,
-            "h2d": "pinned host memory, one copy per tensor on a second stream, layer by layer ahead of use"}
+            "h2d": ("pinned host memory (one gRet layer's q, k, v, logits copied into every layer's device "
+                    "inputs, plus M and the cross queries), one copy per tensor on a second stream, layer by "
+                    "layer ahead of use"),
+            "d2h": "the 13 cross layers' last-row outputs"}
+
+
+def decode_1m(args, torch, Y, dev, seed, hbm_peak):
+    """Generated tokens at a 1M-token context, B = 1: per token 13 recurrent gRet
+    steps (captured once as a CUDA graph and replayed), a one-slot append of the
+    new token's K^/V^, and 13 split-KV cross layers over the whole cache.  The
+    cache (4.3 GB) is far larger than L2, so every layer's read comes from HBM."""
+    if args.decode_tokens <= 0:
+        return None
+    import synth
+    L = Y.lib
+    bf, f32 = torch.bfloat16, torch.float32
+    sid = synth.stream_id
+    stream = torch.cuda.current_stream(dev)
+    stp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+
+    def normal(shape, dtype, stream_tag, mean=0.0, std=1.0):
+        return synth.fill_normal_(torch.empty(shape, dtype=dtype, device=dev), seed, stream_tag, mean, std)
+
+    def check(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: {L.yoco_last_error().decode()}")
+
+    extra = args.warmup + args.decode_tokens + 1
+    Kc = normal((1, HKV, N_DEC + extra, D), bf, sid(CFG_DEC, 0, synth.T_CACHE_K))
+    Vc = normal((1, HKV, N_DEC + extra, D), bf, sid(CFG_DEC, 0, synth.T_CACHE_V))
+    cache = Y.KVCache(1, HKV, D, N_DEC + extra, k=Kc, v=Vc)
+    cache.set_length(N_DEC)
+    cc = ctypes.byref(cache.c)
+    Wk = normal((DM, HKV * D), bf, sid(CFG_DEC, 0, synth.T_WK), std=0.02)
+    Wv = normal((DM, HKV * D), bf, sid(CFG_DEC, 0, synth.T_WV), std=0.02)
+    M1 = normal((1, 1, DM), bf, sid(CFG_DEC, 0, synth.T_M, 1))
+    Qd = [normal((1, HQ, D), bf, sid(CFG_DEC, l, synth.T_QX, 1)) for l in range(L_CROSS)]
+    Od = [torch.empty(1, HQ, D, dtype=bf, device=dev) for _ in range(L_CROSS)]
+    q1 = [normal((1, H, D), bf, sid(CFG_DEC, l, synth.T_Q, 1), std=D ** -0.5) for l in range(L_SELF)]
+    k1 = [normal((1, H, D), bf, sid(CFG_DEC, l, synth.T_K, 1), std=D ** -0.5) for l in range(L_SELF)]
+    v1 = [normal((1, H, D), bf, sid(CFG_DEC, l, synth.T_V, 1)) for l in range(L_SELF)]
+    lg1 = [normal((1, H), f32, sid(CFG_DEC, l, synth.T_LOGIT, 1), mean=2.0) for l in range(L_SELF)]
+    S1 = [normal((1, H, D, D), f32, sid(CFG_DEC, l, synth.T_S0), std=0.05) for l in range(L_SELF)]
+    o1 = [torch.empty(1, H, D, dtype=bf, device=dev) for _ in range(L_SELF)]
+    ws = torch.empty(max(L.yoco_shared_kv_workspace_size(1, 1, DM, cc),
+                         L.yoco_cross_attn_workspace_size(1, HQ, 1, cc, 0), 256), dtype=torch.uint8, device=dev)
+    wsp, wsn = P(ws), ws.numel()
+
+    def gret_layers(sp):
+        for l in range(L_SELF):
+            check(L.yoco_gret_decode_step(P(q1[l]), P(k1[l]), P(v1[l]), P(lg1[l]), TAU, P(S1[l]), P(o1[l]), 1, H, D,
+                                          D, 1, 1, sp), "gret decode")
+
+    gret_layers(stp)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    n0 = L.yoco_launch_count()
+    with torch.cuda.graph(graph, stream=cap):
+        gret_layers(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    graph_launches = L.yoco_launch_count() - n0
+    stream.wait_stream(cap)
+    torch.cuda.synchronize()
+
+    def token(ev=None):
+        graph.replay()  # the 13 recurrent gRet steps
+        check(L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, cc, wsp, wsn, stp), "append")
+        if ev is not None:
+            ev[0].record(stream)
+        for l in range(L_CROSS):
+            check(L.yoco_cross_attn_decode(P(Qd[l]), HQ, cc, D ** -0.5, 0, P(Od[l]), wsp, wsn, stp), "cross decode")
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        token()
+    torch.cuda.synchronize()
+    len0 = cache.length
+    n0 = L.yoco_launch_count()
+    cross_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+                for _ in range(args.decode_tokens)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.decode_tokens):
+        token(cross_ev[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = L.yoco_launch_count() - n0 + graph_launches * args.decode_tokens
+    ms = e0.elapsed_time(e1) / args.decode_tokens
+    cross_ms = statistics.mean(c[0].elapsed_time(c[1]) / L_CROSS for c in cross_ev)
+    ctx = len0 + (args.decode_tokens + 1) / 2  # mean cache length the timed tokens read
+    key_bytes = HKV * D * 2 * 2  # K^ and V^ of one position
+    tok_bytes = L_CROSS * ctx * key_bytes + 2 * DM * HKV * D * 2 + L_SELF * H * D * D * 4 * 2
+    cross_bytes = ctx * key_bytes
+    out = {"value": round(1e3 / ms, 2), "unit": "tok/s", "context": N_DEC, "B": 1, "ms_per_token": round(ms, 4),
+           "tokens": args.decode_tokens, "gpu_launches_per_token": round(launches / args.decode_tokens, 1),
+           "roofline": {"bound": "hbm", "achieved": round(tok_bytes / (ms / 1e3) / 1e9, 1), "peak": hbm_peak,
+                        "unit": "GB/s", "frac": round(tok_bytes / (ms / 1e3) / 1e9 / hbm_peak, 4),
+                        "algorithmic_bytes_per_token": int(tok_bytes),
+                        "note": ("13 cross layers each read the whole shared cache (4.3 GB, far above the "
+                                 "129 MB L2, so these bytes come from HBM), the projection weights and the 13 "
+                                 "layers' fp32 states in and out")},
+           "roofline_cross_decode": {"bound": "hbm", "kernel": "yoco_cross_attn_decode (split + combine)",
+                                     "achieved": round(cross_bytes / (cross_ms / 1e3) / 1e9, 1), "peak": hbm_peak,
+                                     "unit": "GB/s", "frac": round(cross_bytes / (cross_ms / 1e3) / 1e9 / hbm_peak, 4),
+                                     "algorithmic_bytes_per_launch": int(cross_bytes),
+                                     "avg_launch_ms": round(cross_ms, 4)}}
+    del Kc, Vc, cache
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_only(args):
@@ -533,11 +626,15 @@ def run_only(args):
 
     P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
     stp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    N = args.n or N_LAYER      # tokens of the call's shape (the single 32K-token gRet layer by default)
+    CFG = CFG_LAYER if N == N_LAYER else 4
     if args.only == "gret":
         q = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_Q), std=D ** -0.5)
         k = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_K), std=D ** -0.5)
         v = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_V))
         lg = normal((B, N, H), f32, sid(CFG, 0, synth.T_LOGIT), mean=2.0)
+        if args.no_decay:
+            lg.fill_(float("inf"))
         o = torch.empty_like(v)
         S = torch.zeros(B, H, D, D, dtype=f32, device=dev)
         ws = torch.empty(max(256, L.yoco_gret_prefill_workspace_size(B, N, H, D, D, args.chunk, 1)), dtype=torch.uint8,
@@ -682,7 +779,11 @@ def run_only(args):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    line = {"only": args.only, "ms_per_call": ms, "steps": args.steps}
+    line = {"only": args.only, "ms_per_call": ms, "steps": args.steps, "N": N}
+    if args.only == "gret":
+        nbytes = 4 * B * N * H * D * 2 + B * N * H * 4 + 2 * B * H * D * D * 4
+        line.update({"bytes_per_call": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+                     "no_decay": bool(args.no_decay)})
     if args.only == "qkvg":
         flops = 2.0 * B * N * DM * (3 * H * D + H)
         line.update({"flops_per_call": flops, "achieved_tflops": round(flops / (ms / 1e3) / 1e12, 1)})
@@ -716,9 +817,6 @@ def run_only(args):
 # ------------------------------------------------- long-context workloads
 
 LONG_WORKLOADS = {
-    # 13 gRet layers over a 512K-token prompt, the shared-K/V projection, and the
-    # cross layers for the last prompt row only (early exit)
-    "prefill512k_early_exit": 4,
     # 13 cross layers per generated token over a 128K-token shared cache, one
     # append per token, B sequences with their own caches
     "decode128k": 3,
@@ -752,7 +850,6 @@ def run_workload(args):
     except OSError:
         peaks = {}
     hbm = peaks.get("hbm_gbs", 6800.0) * 1e9
-    tc = peaks.get("bf16_tflops", 1900.0) * 1e12
 
     def normal(shape, dtype, stream_tag, mean=0.0, std=1.0):
         return synth.fill_normal_(torch.empty(shape, dtype=dtype, device=dev), SEED, stream_tag, mean, std)
@@ -783,129 +880,76 @@ def run_workload(args):
 
     lines = []
     cache_bytes_per_key = HKV * D * 2 * 2  # K^ and V^ of one position, bf16
-    if args.workload == "prefill512k_early_exit":
-        Nl = 524288
-        q = [normal((1, Nl, H, D), bf, sid(cfg, l, synth.T_Q), std=D ** -0.5) for l in range(L_SELF)]
-        k = [normal((1, Nl, H, D), bf, sid(cfg, l, synth.T_K), std=D ** -0.5) for l in range(L_SELF)]
-        v = [normal((1, Nl, H, D), bf, sid(cfg, l, synth.T_V)) for l in range(L_SELF)]
-        lg = [normal((1, Nl, H), f32, sid(cfg, l, synth.T_LOGIT), mean=2.0) for l in range(L_SELF)]
-        M = normal((1, Nl, DM), bf, sid(cfg, 0, synth.T_M))
-        Wk = normal((DM, HKV * D), bf, sid(cfg, 0, synth.T_WK), std=0.02)
-        Wv = normal((DM, HKV * D), bf, sid(cfg, 0, synth.T_WV), std=0.02)
-        Qx = [normal((1, 1, HQ, D), bf, sid(cfg, l, synth.T_QX)) for l in range(L_CROSS)]
-        o = torch.empty(1, Nl, H, D, dtype=bf, device=dev)  # each layer's output, consumed before the next
-        S = [torch.zeros(1, H, D, D, dtype=f32, device=dev) for _ in range(L_SELF)]
-        Ox = [torch.empty(1, 1, HQ, D, dtype=bf, device=dev) for _ in range(L_CROSS)]
-        cache = Y.KVCache(1, HKV, D, Nl + 16, device=dev)
+    one_m = args.workload == "decode1m"
+    Nc = 1048576 if one_m else 131072
+    extra = 256 if one_m else 1024
+    batches = [1] if one_m else [int(x) for x in args.batches.split(",")]
+    assert args.warmup + args.steps <= extra, "the cache holds the prompt plus this many generated tokens"
+    Wk = normal((DM, HKV * D), bf, sid(cfg, 0, synth.T_WK), std=0.02)
+    Wv = normal((DM, HKV * D), bf, sid(cfg, 0, synth.T_WV), std=0.02)
+    for Bc in batches:
+        Kc = normal((Bc, HKV, Nc + extra, D), bf, sid(cfg, 0, synth.T_CACHE_K))
+        Vc = normal((Bc, HKV, Nc + extra, D), bf, sid(cfg, 0, synth.T_CACHE_V))
+        cache = Y.KVCache(Bc, HKV, D, Nc + extra, k=Kc, v=Vc)
+        cache.set_length(Nc)
         cc = ctypes.byref(cache.c)
-        ws = torch.empty(max(L.yoco_gret_prefill_workspace_size(1, Nl, H, D, D, 0, Y.YOCO_BF16),
-                             L.yoco_shared_kv_workspace_size(1, Nl, DM, cc),
-                             L.yoco_cross_attn_workspace_size(1, HQ, 1, cc, 0), 256), dtype=torch.uint8, device=dev)
+        M1 = normal((Bc, 1, DM), bf, sid(cfg, 0, synth.T_M, 1))
+        Qd = [normal((Bc, HQ, D), bf, sid(cfg, l, synth.T_QX, 1)) for l in range(L_CROSS)]
+        Od = [torch.empty(Bc, HQ, D, dtype=bf, device=dev) for _ in range(L_CROSS)]
+        ws = torch.empty(max(L.yoco_shared_kv_workspace_size(Bc, 1, DM, cc),
+                             L.yoco_cross_attn_workspace_size(Bc, HQ, 1, cc, 0), 256), dtype=torch.uint8,
+                         device=dev)
         wsp, wsn = P(ws), ws.numel()
-        gret_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        graph = None
+        if one_m:
+            q1 = [normal((Bc, H, D), bf, sid(cfg, l, synth.T_Q, 1), std=D ** -0.5) for l in range(L_SELF)]
+            k1 = [normal((Bc, H, D), bf, sid(cfg, l, synth.T_K, 1), std=D ** -0.5) for l in range(L_SELF)]
+            v1 = [normal((Bc, H, D), bf, sid(cfg, l, synth.T_V, 1)) for l in range(L_SELF)]
+            lg1 = [normal((Bc, H), f32, sid(cfg, l, synth.T_LOGIT, 1), mean=2.0) for l in range(L_SELF)]
+            S1 = [normal((Bc, H, D, D), f32, sid(cfg, l, synth.T_S0), std=0.05) for l in range(L_SELF)]
+            o1 = [torch.empty(Bc, H, D, dtype=bf, device=dev) for _ in range(L_SELF)]
+
+            def gret_layers(sp):
+                for l in range(L_SELF):
+                    check(L.yoco_gret_decode_step(P(q1[l]), P(k1[l]), P(v1[l]), P(lg1[l]), TAU, P(S1[l]),
+                                                  P(o1[l]), Bc, H, D, D, 1, 1, sp), "gret decode")
+            gret_layers(stp)
+            torch.cuda.synchronize()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=cap):
+                gret_layers(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+            stream.wait_stream(cap)
+            torch.cuda.synchronize()
 
         def step():
-            for s_ in S:
-                s_.zero_()
-            cache.len_dev.zero_()
-            cache.c.len_host = 0
-            gret_ev[0].record(stream)
-            for l in range(L_SELF):
-                check(L.yoco_gret_prefill_chunkwise(P(q[l]), P(k[l]), P(v[l]), P(lg[l]), TAU, P(o), P(S[l]), 1, Nl,
-                                                    H, D, D, 0, 1, 1, wsp, wsn, stp), "gret prefill")
-            gret_ev[1].record(stream)
-            check(L.yoco_shared_kv_project_append(P(M), None, EPS, P(Wk), P(Wv), Nl, DM, cc, wsp, wsn, stp), "kv")
+            if graph is not None:
+                graph.replay()  # the 13 recurrent gRet steps
+            check(L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, cc, wsp, wsn, stp),
+                  "append")
             for l in range(L_CROSS):
-                check(L.yoco_cross_attn_prefill(P(Qx[l]), HQ, 1, Nl - 1, cc, D ** -0.5, P(Ox[l]), wsp, wsn, stp),
-                      "cross prefill")
+                check(L.yoco_cross_attn_decode(P(Qd[l]), HQ, cc, D ** -0.5, 0, P(Od[l]), wsp, wsn, stp),
+                      "cross decode")
 
         ms, clocks = timed(step, args.steps, args.warmup)
-        gret_ms = gret_ev[0].elapsed_time(gret_ev[1]) / L_SELF  # the last timed step's 13 calls
-        gret_bytes = 4 * Nl * H * D * 2 + Nl * H * 4 + 2 * H * D * D * 4
-        proj_flops = 2.0 * Nl * DM * 2 * HKV * D
-        cross_bytes = Nl * cache_bytes_per_key
-        roof_ms = (L_SELF * gret_bytes / hbm + proj_flops / tc + L_CROSS * cross_bytes / hbm) * 1e3
+        ctx = Nc + args.warmup + args.steps / 2  # mean cache length over the timed tokens
+        step_bytes = L_CROSS * Bc * ctx * cache_bytes_per_key + 2 * DM * HKV * D * 2
+        if one_m:
+            step_bytes += L_SELF * Bc * H * D * D * 4 * 2
+        roof_ms = step_bytes / hbm * 1e3
         lines.append({
-            "workload": "yoco3b_prefill512k_early_exit", "metric": "prompt tok/s", "value": Nl / (ms / 1e3),
-            "unit": "tok/s", "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
-            "data": "synthetic", "config": {"B": 1, "N": Nl, "self_layers": L_SELF, "gret_heads": H, "d": D,
-                                            "d_model": DM, "Hq": HQ, "Hkv": HKV, "cross_rows": 1},
-            "roofline_ms": round(roof_ms, 3), "frac_of_roofline": round(roof_ms / ms, 4),
-            "roofline_gret": {"bound": "hbm", "achieved": round(gret_bytes / (gret_ms / 1e3) / 1e9, 1),
-                              "peak": hbm / 1e9, "unit": "GB/s", "frac": round(gret_bytes / (gret_ms / 1e3) / hbm, 4),
-                              "algorithmic_bytes_per_launch": gret_bytes, "avg_launch_ms": round(gret_ms, 4)},
-            "clocks": clocks})
-    else:
-        one_m = args.workload == "decode1m"
-        Nc = 1048576 if one_m else 131072
-        extra = 256 if one_m else 1024
-        batches = [1] if one_m else [int(x) for x in args.batches.split(",")]
-        assert args.warmup + args.steps <= extra, "the cache holds the prompt plus this many generated tokens"
-        Wk = normal((DM, HKV * D), bf, sid(cfg, 0, synth.T_WK), std=0.02)
-        Wv = normal((DM, HKV * D), bf, sid(cfg, 0, synth.T_WV), std=0.02)
-        for Bc in batches:
-            Kc = normal((Bc, HKV, Nc + extra, D), bf, sid(cfg, 0, synth.T_CACHE_K))
-            Vc = normal((Bc, HKV, Nc + extra, D), bf, sid(cfg, 0, synth.T_CACHE_V))
-            cache = Y.KVCache(Bc, HKV, D, Nc + extra, k=Kc, v=Vc)
-            cache.set_length(Nc)
-            cc = ctypes.byref(cache.c)
-            M1 = normal((Bc, 1, DM), bf, sid(cfg, 0, synth.T_M, 1))
-            Qd = [normal((Bc, HQ, D), bf, sid(cfg, l, synth.T_QX, 1)) for l in range(L_CROSS)]
-            Od = [torch.empty(Bc, HQ, D, dtype=bf, device=dev) for _ in range(L_CROSS)]
-            ws = torch.empty(max(L.yoco_shared_kv_workspace_size(Bc, 1, DM, cc),
-                                 L.yoco_cross_attn_workspace_size(Bc, HQ, 1, cc, 0), 256), dtype=torch.uint8,
-                             device=dev)
-            wsp, wsn = P(ws), ws.numel()
-            graph = None
-            if one_m:
-                q1 = [normal((Bc, H, D), bf, sid(cfg, l, synth.T_Q, 1), std=D ** -0.5) for l in range(L_SELF)]
-                k1 = [normal((Bc, H, D), bf, sid(cfg, l, synth.T_K, 1), std=D ** -0.5) for l in range(L_SELF)]
-                v1 = [normal((Bc, H, D), bf, sid(cfg, l, synth.T_V, 1)) for l in range(L_SELF)]
-                lg1 = [normal((Bc, H), f32, sid(cfg, l, synth.T_LOGIT, 1), mean=2.0) for l in range(L_SELF)]
-                S1 = [normal((Bc, H, D, D), f32, sid(cfg, l, synth.T_S0), std=0.05) for l in range(L_SELF)]
-                o1 = [torch.empty(Bc, H, D, dtype=bf, device=dev) for _ in range(L_SELF)]
-
-                def gret_layers(sp):
-                    for l in range(L_SELF):
-                        check(L.yoco_gret_decode_step(P(q1[l]), P(k1[l]), P(v1[l]), P(lg1[l]), TAU, P(S1[l]),
-                                                      P(o1[l]), Bc, H, D, D, 1, 1, sp), "gret decode")
-                gret_layers(stp)
-                torch.cuda.synchronize()
-                cap = torch.cuda.Stream(dev)
-                cap.wait_stream(stream)
-                graph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(graph, stream=cap):
-                    gret_layers(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
-                stream.wait_stream(cap)
-                torch.cuda.synchronize()
-
-            def step():
-                if graph is not None:
-                    graph.replay()  # the 13 recurrent gRet steps
-                check(L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, cc, wsp, wsn, stp),
-                      "append")
-                for l in range(L_CROSS):
-                    check(L.yoco_cross_attn_decode(P(Qd[l]), HQ, cc, D ** -0.5, 0, P(Od[l]), wsp, wsn, stp),
-                          "cross decode")
-
-            ms, clocks = timed(step, args.steps, args.warmup)
-            ctx = Nc + args.warmup + args.steps / 2  # mean cache length over the timed tokens
-            step_bytes = L_CROSS * Bc * ctx * cache_bytes_per_key + 2 * DM * HKV * D * 2
-            if one_m:
-                step_bytes += L_SELF * Bc * H * D * D * 4 * 2
-            roof_ms = step_bytes / hbm * 1e3
-            lines.append({
-                "workload": ("yoco3b_decode1m" if one_m else f"shared_kv_decode128k_b{Bc}"),
-                "metric": "generated tok/s", "value": Bc / (ms / 1e3), "unit": "tok/s", "ms_per_step": ms,
-                "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
-                "config": {"B": Bc, "context": Nc, "cross_layers": L_CROSS, "Hq": HQ, "Hkv": HKV, "d": D,
-                           "self_layers": L_SELF if one_m else 0},
-                "roofline": {"bound": "hbm", "achieved": round(step_bytes / (ms / 1e3) / 1e9, 1),
-                             "peak": hbm / 1e9, "unit": "GB/s", "frac": round(step_bytes / (ms / 1e3) / hbm, 4),
-                             "algorithmic_bytes_per_step": int(step_bytes)},
-                "roofline_ms": round(roof_ms, 4), "frac_of_roofline": round(roof_ms / ms, 4), "clocks": clocks})
-            del Kc, Vc, cache
-            torch.cuda.empty_cache()
+            "workload": ("yoco3b_decode1m" if one_m else f"shared_kv_decode128k_b{Bc}"),
+            "metric": "generated tok/s", "value": Bc / (ms / 1e3), "unit": "tok/s", "ms_per_step": ms,
+            "steps": args.steps, "warmup": args.warmup, "dtype": "bf16", "data": "synthetic",
+            "config": {"B": Bc, "context": Nc, "cross_layers": L_CROSS, "Hq": HQ, "Hkv": HKV, "d": D,
+                       "self_layers": L_SELF if one_m else 0},
+            "roofline": {"bound": "hbm", "achieved": round(step_bytes / (ms / 1e3) / 1e9, 1),
+                         "peak": hbm / 1e9, "unit": "GB/s", "frac": round(step_bytes / (ms / 1e3) / hbm, 4),
+                         "algorithmic_bytes_per_step": int(step_bytes)},
+            "roofline_ms": round(roof_ms, 4), "frac_of_roofline": round(roof_ms / ms, 4), "clocks": clocks})
+        del Kc, Vc, cache
+        torch.cuda.empty_cache()
     for line in lines:
         print(json.dumps(line), flush=True)
 

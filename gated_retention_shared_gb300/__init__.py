@@ -74,6 +74,8 @@ def _load():
         "yoco_rope_apply": (i, [vp, i, i, i, i, i64, f, i, vp]),
         "yoco_gret_qkvg_project": (i, [vp, vp, i, i, i, i, i, i64, f, vp, vp, vp, vp, vp, sz, vp]),
         "yoco_gret_qkvg_workspace_size": (sz, [i, i, i, i, f]),
+        "yoco_cross_attn_decode_noalloc_status": (i, [i, vp]),
+        "yoco_test_hook": (i, [i, i64]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -90,7 +92,8 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_workspace_status", "yoco_cross_attn_decode_noalloc", "yoco_selftest_wait_timeout",
             "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size", "yoco_gret_group_norm_gate",
             "yoco_rope_apply", "yoco_gret_qkvg_project", "yoco_gret_qkvg_workspace_size",
-            "yoco_gret_decode_step_gn_gate")
+            "yoco_gret_decode_step_gn_gate", "yoco_cross_attn_decode_noalloc_status", "yoco_test_hook")
+YOCO_HOOK_FAIL_NEXT_CALLS, YOCO_HOOK_GRET_SEG0_DELAY_NS = 1, 2
 
 
 def _check(status: int, where: str):

@@ -16,6 +16,37 @@ static std::atomic<uint64_t> g_launches{0};
 
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+static std::atomic<int64_t> g_hooks[kHookCount];
+
+int64_t test_hook_value(int hook) {
+    return (hook > 0 && hook < kHookCount) ? g_hooks[hook].load(std::memory_order_relaxed) : 0;
+}
+
+bool take_injected_failure() {
+    int64_t n = g_hooks[kHookFailNextCalls].load(std::memory_order_relaxed);
+    while (n > 0)
+        if (g_hooks[kHookFailNextCalls].compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) return true;
+    return false;
+}
+
+int device_sm_count() {
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cached[kMaxDev];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+        (void)cudaGetLastError();
+        return kDefaultSmCount;
+    }
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return kDefaultSmCount;
+    }
+    cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 void set_error(const char *fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -39,6 +70,13 @@ static yoco_status cuda_status(cudaError_t e, const char *what) {
     set_error("%s: %s", what, cudaGetErrorString(e));
     return YOCO_ERR_CUDA;
 }
+
+// A pending injected failure (yoco_test_hook) stands in for a failed launch at the
+// point where the call would enqueue its first kernel: nothing is launched or written.
+#define YOCO_INJECTED_FAILURE(what)                                                     \
+    do {                                                                                \
+        if (take_injected_failure()) return cuda_status(cudaErrorLaunchFailure, what);  \
+    } while (0)
 
 static bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 static bool valid_dt(yoco_dtype d) { return d == YOCO_F32 || d == YOCO_BF16; }
@@ -116,6 +154,19 @@ yoco_status yoco_selftest_wait_timeout(void *workspace, uint64_t limit_ns, void 
 
 uint64_t yoco_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+yoco_status yoco_test_hook(int hook, int64_t value) {
+    if (hook == YOCO_HOOK_FAIL_NEXT_CALLS) {
+        if (value < 0 || value > 1000000) return fail(YOCO_ERR_INVALID_ARG, "failure count must be in [0, 1e6]");
+    } else if (hook == YOCO_HOOK_GRET_SEG0_DELAY_NS) {
+        if (value < 0 || value > 1000000000) return fail(YOCO_ERR_INVALID_ARG, "delay must be in [0, 1e9] ns");
+    } else {
+        return fail(YOCO_ERR_INVALID_ARG, "unknown test hook %d", hook);
+    }
+    g_hooks[hook].store(value, std::memory_order_relaxed);
+    g_last_error[0] = 0;
+    return YOCO_OK;
+}
+
 // ----------------------------------------------------------------------- gRet
 
 static yoco_status check_gret_shapes(int B, int N, int H, int dk, int dv, yoco_dtype in_dt, yoco_dtype out_dt) {
@@ -150,6 +201,7 @@ yoco_status yoco_gret_prefill_chunkwise(const void *q, const void *k, const void
     const bool tc = (chunk == 0 || chunk == 128) && gret_tc_eligible(B, N, H, dk, dv, in_dt);
     const size_t need = tc ? gret_tc_workspace(B, N, H, dk, dv) : gret_simt_workspace(B, N, H, dk, dv);
     if ((s = check_ws(workspace, ws_bytes, need)) != YOCO_OK) return s;
+    YOCO_INJECTED_FAILURE("gret_prefill_chunkwise");
     GretArgs a{q, k, v, gate_logits, tau, o, state, B, N, H, dk, dv, in_dt};
     cudaStream_t st = (cudaStream_t)stream;
     return cuda_status(tc ? gret_prefill_tc(a, workspace, st) : gret_prefill_simt(a, workspace, st),
@@ -164,6 +216,7 @@ yoco_status yoco_gret_decode_step(const void *q, const void *k, const void *v, c
     if (!q || !k || !v || !gate_logits || !state || !o) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
     if (!(tau > 0.0f) || !isfinite(tau)) return fail(YOCO_ERR_INVALID_ARG, "tau must be finite and > 0");
     if (!aligned(state, 16)) return fail(YOCO_ERR_INVALID_ARG, "state must be 16-byte aligned");
+    YOCO_INJECTED_FAILURE("gret_decode_step");
     return cuda_status(gret_decode(q, k, v, gate_logits, tau, state, o, B, H, dk, dv, in_dt, (cudaStream_t)stream),
                        "gret_decode_step");
 }
@@ -191,6 +244,7 @@ yoco_status yoco_shared_kv_project_append(const void *M, const void *rms_w, floa
     if ((int64_t)cache->B * T > INT32_MAX) return fail(YOCO_ERR_UNSUPPORTED, "B*T too large");
     const size_t need = kv_proj_workspace(cache->B, T, dm, cache->Hkv, cache->d, cache->dtype, cache->rope_base);
     if ((s = check_ws(workspace, ws_bytes, need)) != YOCO_OK) return s;
+    YOCO_INJECTED_FAILURE("shared_kv_project_append");
     KvProjArgs a{M, rms_w, Wk, Wv, eps, cache->B, T, dm, cache->Hkv, cache->d, cache->capacity, cache->len_host,
                  cache->k, cache->v, cache->len_dev, cache->dtype, cache->rope_base};
     s = cuda_status(kv_project_append(a, workspace, (cudaStream_t)stream), "shared_kv_project_append");
@@ -231,6 +285,7 @@ static yoco_status attn_common(const void *Q, int Hq, int T, int64_t p0, const y
     if (splits > 4096) return fail(YOCO_ERR_UNSUPPORTED, "num_splits above 4096");
     const size_t need = attn_workspace(cache->B, Hq, T, cache->d, splits);
     if ((s = check_ws(ws, ws_bytes, need)) != YOCO_OK) return s;
+    YOCO_INJECTED_FAILURE("cross_attn");
     AttnArgs a{Q, O, cache->k, cache->v, cache->B, T, Hq, cache->Hkv, cache->d, cache->capacity, p0, scale,
                cache->dtype, cache->rope_base};
     return cuda_status(attn_run(a, splits, ws, (cudaStream_t)stream), "cross_attn");
@@ -262,6 +317,7 @@ yoco_status yoco_gret_decode_step_gn_gate(const void *q, const void *k, const vo
     if (!(tau > 0.0f) || !isfinite(tau)) return fail(YOCO_ERR_INVALID_ARG, "tau must be finite and > 0");
     if (!(eps > 0.f) || !isfinite(eps)) return fail(YOCO_ERR_INVALID_ARG, "eps must be finite and > 0");
     if (!aligned(state, 16)) return fail(YOCO_ERR_INVALID_ARG, "state must be 16-byte aligned");
+    YOCO_INJECTED_FAILURE("gret_decode_step_gn_gate");
     return cuda_status(gret_decode_gn(q, k, v, gate_logits, tau, state, gate, gn_weight, gn_bias, eps, z, B, H, dk, dv,
                                       dt, (cudaStream_t)stream),
                        "gret_decode_step_gn_gate");
@@ -276,6 +332,7 @@ yoco_status yoco_gret_group_norm_gate(const void *o, const void *gate, const flo
     if (!(eps > 0.f) || !isfinite(eps)) return fail(YOCO_ERR_INVALID_ARG, "eps must be finite and > 0");
     if (!aligned(o, 16) || !aligned(gate, 16) || !aligned(z, 16))
         return fail(YOCO_ERR_INVALID_ARG, "o, gate, z must be 16-byte aligned");
+    YOCO_INJECTED_FAILURE("gret_group_norm_gate");
     return cuda_status(group_norm_gate(o, gate, gn_weight, gn_bias, eps, z, (int64_t)B * N * H, H, d, dt,
                                        (cudaStream_t)stream),
                        "gret_group_norm_gate");
@@ -307,6 +364,7 @@ yoco_status yoco_gret_qkvg_project(const void *X, const void *W, int B, int N, i
     yoco_status s = check_ws(workspace, ws_bytes, yoco_gret_qkvg_workspace_size(B, N, H, d, rope_base));
     if (s != YOCO_OK) return s;
     if (N == 0) return YOCO_OK;
+    YOCO_INJECTED_FAILURE("gret_qkvg_project");
     cudaStream_t st = (cudaStream_t)stream;
     float2 *rope_cs = nullptr;
     cudaError_t e = cudaSuccess;
@@ -329,6 +387,7 @@ yoco_status yoco_rope_apply(void *x, int B, int N, int H, int d, int64_t pos0, f
     if (pos0 < 0) return fail(YOCO_ERR_INVALID_ARG, "pos0 must be >= 0");
     if (!(base > 1.0f) || !isfinite(base)) return fail(YOCO_ERR_INVALID_ARG, "base must be finite and > 1");
     if (!aligned(x, 16)) return fail(YOCO_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    YOCO_INJECTED_FAILURE("rope_apply");
     return cuda_status(rope_apply(x, B, N, H, d, pos0, base, dt, (cudaStream_t)stream), "rope_apply");
 }
 
@@ -368,6 +427,7 @@ yoco_status yoco_swa_prefill(const void *q, const void *k, const void *v, int Hq
     if ((int64_t)ring->B * Hq > 0x7fffffff || N > (1 << 30)) return fail(YOCO_ERR_UNSUPPORTED, "size out of range");
     if ((s = check_ws(workspace, ws_bytes, 256)) != YOCO_OK) return s;
     if (N == 0) return YOCO_OK;
+    YOCO_INJECTED_FAILURE("swa_prefill");
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = swa_fa_launch(q, k, v, o, ring->B, N, Hq, ring->Hkv, ring->window, scale, (int *)workspace, st);
     if (e == cudaSuccess) {
@@ -394,6 +454,7 @@ yoco_status yoco_swa_decode(const void *q, const void *k, const void *v, int Hq,
     const int splits =
         attn_auto_splits(ring->B, ring->Hkv, keys, attn_ctas_per_sm(ring->dtype, ring->d, Hq / ring->Hkv));
     if ((s = check_ws(workspace, ws_bytes, attn_workspace(ring->B, Hq, 1, ring->d, splits))) != YOCO_OK) return s;
+    YOCO_INJECTED_FAILURE("swa_decode");
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = swa_ring_write(k, v, ring->k, ring->v, ring->B, 1, ring->Hkv, ring->d, ring->window, 0, 1,
                                    ring->pos, ring->dtype, st);

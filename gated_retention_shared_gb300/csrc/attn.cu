@@ -322,11 +322,11 @@ static int rows_per_block(int G) { return G >= kAttnMaxQ ? 1 : kAttnMaxQ / G; }
 
 int attn_auto_splits(int B, int Hkv, int64_t keys, int ctas_per_sm) {
     // Split count for B*Hkv (sequence, kv head) units: at least one full wave of
-    // CTAs on the 152 SMs, then the smallest count whose last wave is >= 95 % full
-    // (so 8 units take 19 splits = 152 CTAs, 64 units 7 = 448 of 456 slots, 256
-    // units 4 = 1024 of 1064), never more than one split per two key tiles.
+    // CTAs on the device's SMs, then the smallest count whose last wave is >= 95 % full
+    // (on 152 SMs: 8 units take 19 splits = 152 CTAs, 64 units 7 = 448 of 456 slots,
+    // 256 units 4 = 1024 of 1064), never more than one split per two key tiles.
     const int64_t units = (int64_t)B * Hkv;
-    const int64_t slots = (int64_t)ctas_per_sm * 152;
+    const int64_t slots = (int64_t)ctas_per_sm * device_sm_count();
     int64_t cap = (keys + 2 * kAttnTile - 1) / (2 * kAttnTile);
     if (cap > 1024) cap = 1024;
     if (cap < 1) cap = 1;

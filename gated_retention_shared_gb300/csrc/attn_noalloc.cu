@@ -14,7 +14,6 @@
 // device share it and it keeps whatever the previous call wrote; this kernel
 // writes every partial it later reads, so nothing has to be cleared.  Two calls
 // that run at the same time on one device (different streams) race on it.
-#include <mutex>
 #include <stdio.h>
 
 #include "common.cuh"
@@ -29,26 +28,17 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 4u << 20;  // 4 MiB = 1,048,576 fp32 partials
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once per
-// device.  In host code `g_noalloc_scratch` is only a host-side stand-in; the
-// kernel must be given the address the runtime reports.
+// Device address of the scratch array on the current device.  In host code
+// `g_noalloc_scratch` is only a host-side stand-in; the kernel must be given the
+// address the runtime reports.  Looked up on every call (no allocation, no stream
+// work), so a context that was torn down and re-created gets its own address.  The
+// first lookup on a device may load the library's device code there, which is why
+// that first call should come before any stream capture on the device.
 cudaError_t scratch_for_current_device(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -94,6 +84,10 @@ extern "C" YOCO_API yoco_status yoco_cross_attn_decode_noalloc(const void *Q, in
                       "(use fewer splits or yoco_cross_attn_decode with a workspace)",
                       (long long)need, (long long)kNoAllocScratchBytes);
 
+    if (take_injected_failure()) {
+        set_error("cross_attn_decode_noalloc: %s", cudaGetErrorString(cudaErrorLaunchFailure));
+        return YOCO_ERR_CUDA;
+    }
     void *scratch = nullptr;
     cudaError_t e = scratch_for_current_device(&scratch);
     if (e != cudaSuccess) {
@@ -108,4 +102,16 @@ extern "C" YOCO_API yoco_status yoco_cross_attn_decode_noalloc(const void *Q, in
         return YOCO_ERR_CUDA;
     }
     return YOCO_OK;
+}
+
+extern "C" YOCO_API yoco_status yoco_cross_attn_decode_noalloc_status(int clear, void *stream) {
+    using namespace yoco_host;
+    void *scratch = nullptr;
+    cudaError_t e = scratch_for_current_device(&scratch);
+    if (e != cudaSuccess) {
+        set_error("cross_attn_decode_noalloc_status: scratch lookup failed: %s", cudaGetErrorString(e));
+        return YOCO_ERR_CUDA;
+    }
+    // the status word sits where a workspace keeps it: the scratch's first bytes
+    return yoco_workspace_status(scratch, clear, stream);
 }

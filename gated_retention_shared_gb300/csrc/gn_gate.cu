@@ -102,7 +102,7 @@ using namespace yoco;
 cudaError_t group_norm_gate(const void *o, const void *gate, const float *w, const float *b, float eps, void *z,
                             int64_t rows, int H, int d, yoco_dtype dt, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    const int blocks = (int)std::min<int64_t>((rows + 7) / 8, 152 * 16);
+    const int blocks = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)device_sm_count() * 16);
     count_launches(1);
 #define YOCO_GN(T_, D_)                                                                                             \
     group_norm_gate_kernel<T_, D_><<<blocks, 256, 0, st>>>((const T_ *)o, (const T_ *)gate, w, b, eps, (T_ *)z,    \

@@ -433,7 +433,8 @@ int gret_simt_segments(int B, int N, int H, int dv) {
     // enough CTAs to cover the GPU about once; each segment at least one chunk
     int ctas = B * H * (dv / kSimtDVB);
     int chunks = (N + kSimtC - 1) / kSimtC;
-    int P = (ctas >= 152) ? 1 : (152 + ctas - 1) / ctas;
+    const int sms = device_sm_count();
+    int P = (ctas >= sms) ? 1 : (sms + ctas - 1) / ctas;
     if (P > chunks) P = chunks;
     if (P < 1) P = 1;
     return P;

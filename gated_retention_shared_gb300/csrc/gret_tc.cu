@@ -30,6 +30,17 @@
 // segment-state grid covers P-1 segments only.  With B*H >= #SMs, P = 1 and only the
 // output kernel runs.
 //
+// Negligible weights are dropped (kDropLog): the backward walk of a segment stops at
+// the first chunk whose newest token already carries a weight below e^-40 in the
+// segment's end state (every older token's weight is smaller still), and the fold
+// leaves out every earlier segment whose decay up to this segment's start is below
+// e^-40.  What is left out is bounded by e^-40 ~ 4e-18 times the dropped terms'
+// magnitudes.  With no decay (gamma = 1) nothing is dropped and the walk and the fold
+// cover everything.  No CTA ever waits for another one: each output CTA folds the
+// states it needs on its own, and the final state reaches `state` through a
+// two-party hand-off (whichever of segment 0 and the last segment comes second
+// writes it).
+//
 // Warp roles (320 threads): warps 0-3 keep the state (thread t = TMEM lane t =
 // d_k row t), warps 4-7 compute the decay, P, the in-place scaling of K (and Q)
 // and write the output rows (thread j = query row j), warp 8 issues TMA loads,
@@ -52,6 +63,11 @@ constexpr int kHalf = kTile / 2;            // one 64-column block
 constexpr int kStages = 2;                  // OUTPUT: 2 x (Q, K, V)
 constexpr int kTcThreads = 320;
 constexpr float kFactorMin = -60.f;         // chunk decay above which e^{-b_k} is used
+constexpr float kDropLog = 40.f;            // state contributions weighted below e^-40 are left out
+
+// Hand-off word per (b, h) for the final state (cleared by the segment-state grid):
+constexpr int kHandInitRead = 1;            // segment 0 holds the caller's initial state
+constexpr int kHandParked = 2;              // the last segment parked the final state in slot P
 
 // TMEM columns: A / P, two O accumulators, U
 constexpr uint32_t kColA = 0, kColO = 128, kColU = 384;
@@ -64,6 +80,7 @@ struct TcSmem {
     uint32_t tmem_base;
     int abort_flag;
     int go0, go1;  // per-group continue decisions (written by one thread, read by all after a barrier)
+    int hand_old;  // the final-state hand-off word as one thread saw it
     float wsum0[4], wsum1[4];
     float bcr[4];  // chunk total log decay b_C, ring over chunks
     alignas(16) float ew[kC];  // e^{-b_k} (factored chunks) or b_k (direct chunks); read as float4
@@ -80,6 +97,12 @@ __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.syn
 __device__ __forceinline__ void report(int *err, int *abort_flag, int code) {
     *(volatile int *)abort_flag = 1;
     if (err) atomicExch(err, (int)(kErrMagic | (uint32_t)code));
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // bf16x8 in a uint4 times the bf16 pair s2 (packed bf16x2 multiply, nearest even)
@@ -126,59 +149,52 @@ __device__ __forceinline__ float group_scan(float x, float *wsum, int lane, int 
     return x + pre;
 }
 
-// Prefix states of the segments of one (b, h): S_in(0) = the caller's state (kept in
-// slot P-1 of E), S_in(q) = e^{G_{q-1}} S_in(q-1) + E_{q-1} for q = 1 .. P-1, written over
-// slot q-1.  The output CTAs of segments 1 .. P-1 compute them together, CTA p taking
-// rows [r0, r1) of every S_in, so each reads about two states' worth instead of folding
-// p + 1 whole states; every element is read and written by one thread only.  u is this
-// thread's index among the n threads of the CTA that take part.  The arithmetic is the
-// fold each segment would do on its own (fmaf(e^{G_q}, S, E_q) in order of q).
-constexpr int kPrefItems = 4, kPrefQ = 6;
-
-__device__ __forceinline__ void seg_prefix_rows(float *E, const float *G, size_t bh, int P, int p, int u, int n) {
-    constexpr size_t F4 = (size_t)kD * kD / 4;
-    const int r0 = (p - 1) * kD / (P - 1), r1 = p * kD / (P - 1);
-    const int items = (r1 - r0) * (kD / 4);
-    float4 *base = reinterpret_cast<float4 *>(E) + bh * P * F4 + (size_t)r0 * (kD / 4);
+// Initial state of segment p >= 1 of one (b, h), row t (into S):
+//     S_start(p) = sum_{q<p} e^{dec(q)} E_q + e^{dec(-1)} S_init,  dec(q) = sum_{q<r<p} G_r,
+// evaluated as the fold S <- e^{G_q} S + E_q in order of q, starting at the earliest
+// segment q0 whose decay up to segment p is still >= e^-kDropLog (from S_init when
+// even the caller's state is that close, else from zero).  E slots per (b, h):
+// 0 .. P-2 the segments' end states, P-1 a copy of the caller's state.  Every thread
+// of the calling group reads the same G values, so the loop bounds are uniform.
+__device__ __forceinline__ void seg_initial_row(float (&S)[kD], const float *E, const float *G, size_t bh, int P,
+                                                int p, int t) {
     const float *g_bh = G + bh * P;
-    for (int i0 = u; i0 < items; i0 += n * kPrefItems) {
-        float4 sv[kPrefItems];
+    float dec = 0.f;  // dec(q0)
+    int q0 = p - 1;
+    while (q0 > 0) {
+        const float nd = dec + __ldcg(g_bh + q0);
+        if (nd < -kDropLog) break;
+        dec = nd;
+        --q0;
+    }
+    const bool with_init = (q0 == 0) && (dec + __ldcg(g_bh) >= -kDropLog);
+    const size_t slot0 = bh * (size_t)(P + 1);
+    if (with_init) {
+        const float4 *src = reinterpret_cast<const float4 *>(E + (slot0 + P - 1) * kD * kD + (size_t)t * kD);
 #pragma unroll
-        for (int k = 0; k < kPrefItems; ++k) {
-            const int it = i0 + k * n;
-            sv[k] = (it < items) ? __ldcg(base + (size_t)(P - 1) * F4 + it) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c4 = 0; c4 < kD / 4; ++c4) {
+            const float4 x = __ldcg(src + c4);
+            S[4 * c4] = x.x; S[4 * c4 + 1] = x.y; S[4 * c4 + 2] = x.z; S[4 * c4 + 3] = x.w;
         }
-        for (int q0 = 0; q0 < P - 1; q0 += kPrefQ) {
-            float4 x[kPrefItems][kPrefQ];
-            float g[kPrefQ];
+    } else {
 #pragma unroll
-            for (int qb = 0; qb < kPrefQ; ++qb) {
-                const int q = q0 + qb;
-                g[qb] = (q < P - 1) ? __ldcg(g_bh + q) : 0.f;
+        for (int c = 0; c < kD; ++c) S[c] = 0.f;
+    }
+    for (int q = q0; q < p; ++q) {
+        const float gq = __expf(__ldcg(g_bh + q));
+        const float4 *src = reinterpret_cast<const float4 *>(E + (slot0 + q) * kD * kD + (size_t)t * kD);
 #pragma unroll
-                for (int k = 0; k < kPrefItems; ++k) {
-                    const int it = i0 + k * n;
-                    x[k][qb] = (q < P - 1 && it < items) ? __ldcg(base + (size_t)q * F4 + it)
-                                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
+        for (int cb = 0; cb < 8; ++cb) {  // 16 columns at a time: 4 loads in flight
+            float4 x[4];
 #pragma unroll
-            for (int qb = 0; qb < kPrefQ; ++qb) {
-                const int q = q0 + qb;
-                if (q < P - 1) {
-                    const float gq = __expf(g[qb]);
+            for (int u = 0; u < 4; ++u) x[u] = __ldcg(src + cb * 4 + u);
 #pragma unroll
-                    for (int k = 0; k < kPrefItems; ++k) {
-                        const int it = i0 + k * n;
-                        if (it < items) {
-                            sv[k].x = fmaf(gq, sv[k].x, x[k][qb].x);
-                            sv[k].y = fmaf(gq, sv[k].y, x[k][qb].y);
-                            sv[k].z = fmaf(gq, sv[k].z, x[k][qb].z);
-                            sv[k].w = fmaf(gq, sv[k].w, x[k][qb].w);
-                            base[(size_t)q * F4 + it] = sv[k];
-                        }
-                    }
-                }
+            for (int u = 0; u < 4; ++u) {
+                float *s4 = &S[cb * 16 + 4 * u];
+                s4[0] = fmaf(gq, s4[0], x[u].x);
+                s4[1] = fmaf(gq, s4[1], x[u].y);
+                s4[2] = fmaf(gq, s4[2], x[u].z);
+                s4[3] = fmaf(gq, s4[3], x[u].w);
             }
         }
     }
@@ -189,8 +205,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const float *__restrict__ logits, float inv_tau,
                bf16_t *__restrict__ o, float *__restrict__ state, float *__restrict__ E, float *__restrict__ G,
-               int *__restrict__ seg0_read, int *__restrict__ scan_count, int N, int H, int seg_len, int P,
-               int *err) {
+               int *__restrict__ hand, int N, int H, int seg_len, int P, int *err, uint64_t seg0_delay_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_u32 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base_u32 & 1023u)) & 1023u;
@@ -209,7 +224,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int t_begin = p * seg_len;
     const int t_end = min(N, t_begin + seg_len);
     const int nchunks = (t_end - t_begin + kC - 1) / kC;
-    const size_t bh = (size_t)b * H + h;  // E / G slots: bh * P + q; slot P-1 of E holds the initial state
+    const size_t bh = (size_t)b * H + h;  // E slots: bh * (P + 1) + q; G: bh * P + q
     // each stage holds Q, K, V of one chunk
     uint8_t *Sbuf = tiles + (size_t)6 * kTile;  // bf16 state, MMA3's B operand
     constexpr size_t kSS = 3 * (size_t)kTile;
@@ -261,34 +276,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto chunk_log_gate = [&](int n0, int row) {
         return (n0 + row < N) ? log_gate(logits[((size_t)b * N + n0 + row) * H + h], inv_tau) : 0.f;
     };
-    // Segments p > 0: after the segment-state grid, the state and decay warps (256 threads)
-    // compute this CTA's rows of the head's prefix states, then wait until the head's
-    // other P - 2 output CTAs have too.  `scan_count` is cleared by the segment-state grid
-    // before it lets this grid start; the wait is bounded (error 12).
-    auto segment_prefix = [&](int u) {
-        asm volatile("griddepcontrol.wait;\n" ::: "memory");
-        seg_prefix_rows(E, G, bh, P, p, u, 256);
-        __threadfence();  // this thread's rows are visible to the head's other CTAs
-        named_bar(3, 256);
-        if (tid == 0) {
-            atomicAdd(scan_count + bh, 1);
-            bool seen = false;
-            uint64_t t0;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-            for (uint32_t it = 0; !seen; ++it) {
-                seen = *reinterpret_cast<volatile int *>(scan_count + bh) >= P - 1;
-                if (!seen && (it & 63) == 63) {
-                    uint64_t tn;
-                    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tn));
-                    if (*abort_flag || tn - t0 > 2000000000ull) break;
-                }
-            }
-            if (!seen) report(err, &sm.abort_flag, 12);  // the chunk loops then stop at once
-            __threadfence();
-        }
-        named_bar(3, 256);
-    };
-
     if (warp == 8) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -416,7 +403,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int j = tid - 128;  // token row of the chunk = TMEM lane
         const int wq = warp - 4;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-        if (p > 0) segment_prefix(128 + j);  // chunk 0 needs the folded state first anyway
         float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), j) : 0.f;
         bool alive = true;
         for (int i = 0; i < nchunks && alive; ++i) {
@@ -510,20 +496,26 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         float S[kD];  // row t of the state, fp32
         // Segment 0 starts from the caller's state and reads it directly, so it runs
-        // alongside the segment-state grid; later segments need that grid's end states:
-        // they wait for it, fold their rows of the head's prefix states with the decay
-        // warps and the head's other output CTAs, then read their own
-        if (p > 0) segment_prefix(t);
-        {
-            // initial state of this segment: the caller's state (p = 0), or the caller's
-            // state advanced over the earlier segments (prefix state p, in slot p - 1)
-            const float *init = (p == 0) ? state + bh * kD * kD : E + (bh * P + p - 1) * kD * kD;
-            const float4 *src = reinterpret_cast<const float4 *>(init + (size_t)t * kD);
+        // alongside the segment-state grid; later segments wait for that grid and fold
+        // the end states they need into their own initial state (row t each)
+        if (p == 0) {
+            if (seg0_delay_ns) {  // test hook: take the caller's state late (bounded by the host)
+                uint64_t t0, tn;
+                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+                do {
+                    __nanosleep(1000);
+                    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tn));
+                } while (tn - t0 < seg0_delay_ns);
+            }
+            const float4 *src = reinterpret_cast<const float4 *>(state + bh * kD * kD + (size_t)t * kD);
 #pragma unroll
             for (int c4 = 0; c4 < kD / 4; ++c4) {
                 const float4 x = __ldcg(src + c4);
                 S[4 * c4] = x.x; S[4 * c4 + 1] = x.y; S[4 * c4 + 2] = x.z; S[4 * c4 + 3] = x.w;
             }
+        } else {
+            asm volatile("griddepcontrol.wait;\n" ::: "memory");
+            seg_initial_row(S, E, G, bh, P, p, t);
         }
         auto put_state = [&]() {  // bf16 row t of S into the N-major B tile
 #pragma unroll
@@ -536,12 +528,21 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         };
         put_state();
         named_bar(2, 128);
-        if (t == 0) {
-            mbar_arrive(&sm.s_ready);
-            // the caller's state is in registers now: the last segment may overwrite it
-            if (p == 0 && P > 1) {
+        if (t == 0) mbar_arrive(&sm.s_ready);
+        if (p == 0 && P > 1) {
+            // the caller's state is in registers now, so the last segment may overwrite
+            // it; if that segment has already parked the final state, copy it over
+            if (t == 0) {
                 __threadfence();
-                atomicExch(seg0_read + bh, 1);
+                sm.hand_old = atomicOr(hand + bh, kHandInitRead);
+                __threadfence();
+            }
+            named_bar(2, 128);
+            if (sm.hand_old & kHandParked) {
+                const float4 *src = reinterpret_cast<const float4 *>(E + (bh * (P + 1) + P) * kD * kD + (size_t)t * kD);
+                float4 *dst = reinterpret_cast<float4 *>(state + bh * kD * kD + (size_t)t * kD);
+#pragma unroll 8
+                for (int c4 = 0; c4 < kD / 4; ++c4) dst[c4] = __ldcg(src + c4);
             }
         }
         float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), t) : 0.f;
@@ -626,30 +627,27 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         named_bar(2, 128);
         if (t == 0) sm.go0 = !*abort_flag;
         named_bar(2, 128);
-        if (p == P - 1 && sm.go0 && P > 1) {
-            // segment 0 of this (b, h) must have read the caller's state first
-            if (t == 0) {
-                bool seen = false;
-                uint64_t t0;
-                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-                for (uint32_t it = 0; !seen; ++it) {
-                    seen = *reinterpret_cast<volatile int *>(seg0_read + bh) == 1;
-                    if (!seen && (it & 63) == 63) {
-                        uint64_t tn;
-                        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tn));
-                        if (*abort_flag || tn - t0 > 2000000000ull) break;
-                    }
-                }
-                if (!seen) report(err, &sm.abort_flag, 11);
-                __threadfence();
-                sm.go0 = seen;
-            }
-            named_bar(2, 128);
-        }
         if (p == P - 1 && sm.go0) {  // the last segment's end state is the call's final state
-            float4 *dst = reinterpret_cast<float4 *>(state + bh * kD * kD + (size_t)t * kD);
+            // With P > 1, segment 0 reads the caller's state from `state`: overwrite it
+            // only once segment 0 has its copy, else park the final state in slot P for
+            // segment 0 to copy (if segment 0 takes its copy in between, write it here too)
+            if (P > 1 && t == 0) sm.hand_old = ld_acquire_gpu(hand + bh);
+            named_bar(2, 128);
+            const bool parked = P > 1 && !(sm.hand_old & kHandInitRead);
+            float *row = parked ? E + (bh * (P + 1) + P) * kD * kD : state + bh * kD * kD;
+            for (int pass = 0; pass < 2; ++pass) {
+                float4 *dst = reinterpret_cast<float4 *>(row + (size_t)t * kD);
 #pragma unroll
-            for (int c4 = 0; c4 < kD / 4; ++c4) dst[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
+                for (int c4 = 0; c4 < kD / 4; ++c4)
+                    dst[c4] = make_float4(S[4 * c4], S[4 * c4 + 1], S[4 * c4 + 2], S[4 * c4 + 3]);
+                if (!parked || pass == 1) break;
+                __threadfence();
+                named_bar(2, 128);
+                if (t == 0) sm.hand_old = atomicOr(hand + bh, kHandParked);
+                named_bar(2, 128);
+                if (!(sm.hand_old & kHandInitRead)) break;  // segment 0 will copy the parked state
+                row = state + bh * kD * kD;
+            }
         }
     }
 
@@ -668,16 +666,21 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // is computed from the gate logits before its chunk lands, and the moment it lands
 // the eight scale warps rescale K in place (thread = one row-half) and announce it;
 // the MMA E^T += V^T (w . K) into TMEM (lane = d_v) then frees the slot.
+// The walk stops at the first chunk whose newest token weighs below e^-kDropLog
+// (found from the gate logits in a short prologue, 16 chunks per round), and
+// G_p is then the decay of the walked chunks, itself below e^-kDropLog.
 constexpr int kSegStages = 3;
 constexpr int kSegThreads = 320;              // warps 0-7 scale, 8 TMA, 9 MMA
 constexpr int kSegScale = 256;
 
 struct SegSmem {
-    uint64_t full[kSegStages], empty[kSegStages], scaled[kSegStages], e_full;
+    uint64_t full[kSegStages], empty[kSegStages], scaled[kSegStages], e_full, decided;
     uint32_t tmem_base;
     int abort_flag;
     int go;
+    int nuse;         // chunks the walk takes (decided by the scale warps' prologue)
     float wsum[2][8];
+    float csum[16];   // prologue: total log decay of 16 chunks
 };
 
 constexpr size_t kSegSmemBytes = (size_t)kSegStages * 2 * kTile + sizeof(SegSmem) + 1024;
@@ -686,8 +689,8 @@ static_assert(kSegSmemBytes <= kTcSmemBytes, "segment-state ring + control block
 __global__ void __launch_bounds__(kSegThreads, 1)
 gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const float *__restrict__ logits, float inv_tau, const float *__restrict__ state,
-                float *__restrict__ E, float *__restrict__ G, int *__restrict__ seg0_read,
-                int *__restrict__ scan_count, int N, int H, int seg_len, int P, int *err) {
+                float *__restrict__ E, float *__restrict__ G, int *__restrict__ hand, int N, int H, int seg_len,
+                int P, int *err) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
@@ -697,7 +700,8 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const int t_begin = p * seg_len;
     const int nch = (min(N, t_begin + seg_len) - t_begin + kC - 1) / kC;
     const size_t bh = (size_t)b * H + h;
-    const size_t bhp = bh * P + p;
+    const size_t bhp = bh * P + p;                 // G slot
+    const size_t e_slot = bh * (size_t)(P + 1) + p;  // E slot
     auto stage_k = [&](int s) { return tiles + (size_t)s * 2 * kTile; };
     auto stage_v = [&](int s) { return tiles + (size_t)s * 2 * kTile + kTile; };
     auto chunk_at = [&](int i) { return t_begin + (nch - 1 - i) * kC; };  // backwards
@@ -709,6 +713,7 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             mbar_init(&sm.scaled[s], 1);
         }
         mbar_init(&sm.e_full, 1);
+        mbar_init(&sm.decided, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -722,13 +727,11 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const uint32_t tmem = sm.tmem_base;
     volatile int *abort_flag = &sm.abort_flag;
     // Programmatic dependent launch: wait for the previous kernel before any global
-    // access; clear this call's "segment 0 has read the caller's state" flag and the
-    // head's prefix-state arrival count, then let the output grid (which sets and reads
-    // them) start.
+    // access; clear this call's final-state hand-off word, then let the output grid
+    // (which sets and reads it) start.
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     if (p == 0 && tid == 0) {
-        *reinterpret_cast<volatile int *>(seg0_read + bh) = 0;
-        *reinterpret_cast<volatile int *>(scan_count + bh) = 0;
+        *reinterpret_cast<volatile int *>(hand + bh) = 0;
         __threadfence();
     }
     __syncthreads();
@@ -740,8 +743,20 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             const uint64_t pol = l2_policy_evict_first();
+            // the first kSegStages chunks are requested before the walk length is known
+            // (the newest chunk is always walked); the rest only if the walk takes them
+            const int spec = min(nch, kSegStages);
+            int lim = spec;
             int i = 0;
-            for (; i < nch; ++i) {
+            for (;; ++i) {
+                if (i == spec) {
+                    if (!mbar_wait(&sm.decided, 0, abort_flag)) {
+                        report(err, &sm.abort_flag, 35);
+                        break;
+                    }
+                    lim = max(spec, sm.nuse);
+                }
+                if (i >= lim) break;
                 const int s = i % kSegStages;
                 if (i >= kSegStages && !mbar_wait(&sm.empty[s], ((i / kSegStages) + 1) & 1, abort_flag)) {
                     report(err, &sm.abort_flag, 31);
@@ -754,7 +769,7 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                     tma_load_4d_hint(stage_v(s) + half * kHalf, &tm_v, &sm.full[s], half * 64, h, n0, b, pol);
                 }
             }
-            // leave no copy in flight (bounded by time only: an abort must still wait)
+            // leave no copy in flight, walked or not (bounded by time only: an abort must still wait)
             volatile int no_abort = 0;
             for (int k = max(0, i - kSegStages); k < i; ++k)
                 mbar_wait(&sm.full[k % kSegStages], (k / kSegStages) & 1, &no_abort, 200000000ull);
@@ -763,8 +778,9 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         // -------------------------------------------------------------- MMA
         if (lane == 0) {
             const uint32_t id_kv = idesc_bf16_f32(kD, kD, true, true);  // A = V^T (M-major), B = K'' (N-major)
-            bool ok = true;
-            for (int i = 0; i < nch; ++i) {
+            bool ok = mbar_wait(&sm.decided, 0, abort_flag);
+            const int nuse = ok ? sm.nuse : 0;
+            for (int i = 0; i < nuse; ++i) {
                 const int s = i % kSegStages;
                 if (!(ok = mbar_wait(&sm.scaled[s], (i / kSegStages) & 1, abort_flag))) break;
                 tc_fence_after();
@@ -786,13 +802,61 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             const int n = n0 + r;
             return (n < N) ? log_gate(logits[((size_t)b * N + n) * H + h], inv_tau) : 0.f;
         };
+        // prologue: how many chunks, walking back from the segment end, to take.  Round
+        // by round, warp w sums the log decay of chunks c0 + 2w and c0 + 2w + 1 (eight
+        // logits in flight per lane); every thread then scans the 16 totals the same way
+        // and stops before the first chunk that starts below e^-kDropLog.
+        int nuse = nch;
+        {
+            float run = 0.f;  // log decay of the chunks already taken
+            for (int c0 = 0; c0 < nch; c0 += 16) {
+                float part[2] = {0.f, 0.f};
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int c = c0 + 2 * wr + 8 * hf + k2;  // warp (hf, wr) = warp 4 hf + wr
+                    if (c < nch) {
+                        const int n0 = chunk_at(c);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const int n = n0 + lane + 32 * m;
+                            if (n < N) part[k2] += log_gate(__ldg(logits + ((size_t)b * N + n) * H + h), inv_tau);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) part[k2] += __shfl_xor_sync(0xffffffffu, part[k2], off);
+                }
+                if (lane == 0) {
+                    sm.csum[2 * wr + 8 * hf] = part[0];
+                    sm.csum[2 * wr + 8 * hf + 1] = part[1];
+                }
+                named_bar(1, kSegScale);
+                bool stop = false;
+                for (int k2 = 0; k2 < 16 && c0 + k2 < nch; ++k2) {
+                    if (run < -kDropLog) {
+                        nuse = c0 + k2;
+                        stop = true;
+                        break;
+                    }
+                    run += sm.csum[k2];
+                }
+                named_bar(1, kSegScale);  // csum is rewritten by the next round
+                if (stop) break;
+            }
+            if (tid == 0) {
+                sm.nuse = nuse;
+                mbar_arrive(&sm.decided);
+            }
+        }
         float suffix = 0.f;  // log decay of the chunks after this one
-        float lg_next = (nch > 0) ? log_gate_at(chunk_at(0)) : 0.f;
+        float lg_next = (nuse > 0) ? log_gate_at(chunk_at(0)) : 0.f;
         bool alive = true;
-        for (int i = 0; i < nch && alive; ++i) {
+        for (int i = 0; i < nuse && alive; ++i) {
             const int s = i % kSegStages;
             float x = lg_next;
-            if (i + 1 < nch) lg_next = log_gate_at(chunk_at(i + 1));  // in flight during this chunk
+            if (i + 1 < nuse) lg_next = log_gate_at(chunk_at(i + 1));  // in flight during this chunk
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -836,7 +900,7 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
         if (tid == 0) G[bhp] = suffix;
         if (p == 0 && tid < kD) {  // keep the caller's initial state: the OUTPUT pass overwrites `state`
             const float4 *src = reinterpret_cast<const float4 *>(state + bh * kD * kD + (size_t)tid * kD);
-            float4 *dst = reinterpret_cast<float4 *>(E + (bh * P + P - 1) * kD * kD + (size_t)tid * kD);
+            float4 *dst = reinterpret_cast<float4 *>(E + (bh * (P + 1) + P - 1) * kD * kD + (size_t)tid * kD);
 #pragma unroll 4
             for (int c4 = 0; c4 < kD / 4; ++c4) dst[c4] = src[c4];
         }
@@ -856,7 +920,7 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
                 tmem_ld32(tmem + lane_base + cb * 32, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) E[bhp * kD * kD + (size_t)(cb * 32 + e) * kD + tid] = __uint_as_float(v[e]);
+                for (int e = 0; e < 32; ++e) E[e_slot * kD * kD + (size_t)(cb * 32 + e) * kD + tid] = __uint_as_float(v[e]);
             }
         }
     }
@@ -903,9 +967,11 @@ bool gret_tc_eligible(int B, int N, int H, int dk, int dv, yoco_dtype dt) {
     return dt == YOCO_BF16 && dk == kD && dv == kD && N >= 1 && B >= 1 && H >= 1 && B <= 65535 && H <= 65535;
 }
 
+// Segments per head: the output kernel runs one CTA per SM (its shared memory), so
+// about one CTA per SM of the device over the B*H heads.
 static int tc_segments(int B, int N, int H) {
     const int chunks = (N + kC - 1) / kC;
-    int P = 152 / (B * H);
+    int P = device_sm_count() / (B * H);
     if (P < 1) P = 1;
     if (P > chunks) P = chunks;
     return P;
@@ -920,7 +986,9 @@ size_t gret_tc_workspace(int B, int N, int H, int dk, int dv) {
     (void)dk; (void)dv;
     int P = tc_segments(B, N, H);
     size_t ws = 256;  // status word
-    if (P > 1) ws += ((size_t)B * H * P * kD * kD + (size_t)B * H * P) * sizeof(float) + 2 * (size_t)B * H * sizeof(int);
+    // per (b, h): P + 1 states (end states of segments 0 .. P-2, the caller's initial
+    // state, the parked final state), P segment decays and the hand-off word
+    if (P > 1) ws += ((size_t)B * H * (P + 1) * kD * kD + (size_t)B * H * P) * sizeof(float) + (size_t)B * H * sizeof(int);
     return ws;
 }
 
@@ -934,9 +1002,8 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     P = (a.N + seg_len - 1) / seg_len;
     int *err = (int *)ws;
     float *E = (float *)((char *)ws + 256);
-    float *G = E + (size_t)a.B * a.H * P * kD * kD;
-    int *seg0_read = reinterpret_cast<int *>(G + (size_t)a.B * a.H * P);
-    int *scan_count = seg0_read + (size_t)a.B * a.H;
+    float *G = E + (size_t)a.B * a.H * (P + 1) * kD * kD;
+    int *hand = reinterpret_cast<int *>(G + (size_t)a.B * a.H * P);
     const float inv_tau = 1.0f / a.tau;
     cudaError_t e;
     e = cudaFuncSetAttribute(gret_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
@@ -946,7 +1013,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     if (P == 1) {
         count_launches(1);
         gret_tc_kernel<<<dim3(a.B * a.H), kTcThreads, kTcSmemBytes, st>>>(
-            mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, nullptr, nullptr, a.N, a.H, seg_len, 1, err);
+            mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err, (uint64_t)0);
         return cudaGetLastError();
     }
     // end states of segments 0 .. P-2 (the last segment's is computed by the OUTPUT pass)
@@ -964,7 +1031,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     // before reading anything
     cfg.gridDim = dim3(P - 1, a.H, a.B);
     cfg.dynamicSmemBytes = kSegSmemBytes;
-    e = cudaLaunchKernelEx(&cfg, gret_seg_kernel, mk, mv, a.logits, inv_tau, (const float *)a.state, E, G, seg0_read, scan_count,
+    e = cudaLaunchKernelEx(&cfg, gret_seg_kernel, mk, mv, a.logits, inv_tau, (const float *)a.state, E, G, hand,
                            a.N, a.H, seg_len, P, err);
     if (e != cudaSuccess) return e;
     cfg.dynamicSmemBytes = kTcSmemBytes;
@@ -973,7 +1040,8 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     // for the segment states before touching E, G and `state`
     cfg.gridDim = dim3(P * a.B * a.H);
     return cudaLaunchKernelEx(&cfg, gret_tc_kernel, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o,
-                              a.state, E, G, seg0_read, scan_count, a.N, a.H, seg_len, P, err);
+                              a.state, E, G, hand, a.N, a.H, seg_len, P, err,
+                              (uint64_t)test_hook_value(kHookGretSeg0DelayNs));
 }
 
 }  // namespace yoco_host

@@ -3,10 +3,25 @@
 
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdint.h>
 
 #include "yoco.h"
 
 namespace yoco_host {
+
+// Streaming multiprocessors of the current device (queried once per device).  Grids
+// are sized from it; kDefaultSmCount (a GB300's 152) stands in only where no device
+// can be queried (workspace-size queries on a machine without a GPU).
+constexpr int kDefaultSmCount = 152;
+int device_sm_count();
+
+// Test hooks (yoco_test_hook): process-wide values that tests set to reach paths
+// ordinary inputs cannot force; all are 0 (off) unless a test sets them.
+enum { kHookFailNextCalls = 1, kHookGretSeg0DelayNs = 2, kHookCount = 3 };
+int64_t test_hook_value(int hook);
+// true (and the call must return YOCO_ERR_CUDA before launching anything) while an
+// injected launch failure is pending; consumes one
+bool take_injected_failure();
 
 struct GretArgs {
     const void *q, *k, *v;

@@ -403,7 +403,7 @@ static bool gemv_eligible(int R, int n, int dm) { return R <= kGemvMaxRows && n 
 // K chunks of the few-row path: about one CTA per SM over all column groups
 static int gemv_chunks(int n, int dm) {
     const int groups = (2 * n + 255) / 256;
-    int kch = std::max(1, 152 / groups);
+    int kch = std::max(1, device_sm_count() / groups);
     kch = std::min(kch, dm);
     const int kr = (dm + kch - 1) / kch;
     return (dm + kr - 1) / kr;
@@ -456,7 +456,7 @@ static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
         if ((e = rope_table(rope_cs, a.len, a.T, a.d, a.rope_base, st)) != cudaSuccess) return e;
     }
     count_launches(1);
-    rms_rows_kernel<T><<<std::min((R * 32 + 255) / 256, 152 * 8), 256, 0, st>>>((const T *)a.M, r, R, a.dm, a.eps);
+    rms_rows_kernel<T><<<std::min((R * 32 + 255) / 256, device_sm_count() * 8), 256, 0, st>>>((const T *)a.M, r, R, a.dm, a.eps);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (tc) return kv_project_append_tc(a, r, rope_cs, (int *)ws, st);
     count_launches(1);

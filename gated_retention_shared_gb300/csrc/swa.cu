@@ -44,7 +44,7 @@ cudaError_t swa_ring_write(const void *k, const void *v, void *rk, void *rv, int
     if (n <= 0) return cudaSuccess;
     const int row_bytes = d * (dt == YOCO_BF16 ? 2 : 4);
     const int64_t total = (int64_t)2 * n * B * Hkv * (row_bytes / 16);
-    const int blocks = (int)std::min<int64_t>((total + 255) / 256, 152 * 8);
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)device_sm_count() * 8);
     count_launches(1);
     swa_ring_write_kernel<<<blocks, 256, 0, st>>>((const uint8_t *)k, (const uint8_t *)v, (uint8_t *)rk,
                                                   (uint8_t *)rv, B, N, Hkv, row_bytes, window, tok0, n, pos0);

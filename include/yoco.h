@@ -17,7 +17,11 @@
  * Conventions common to every call:
  *   - Every tensor argument is a DEVICE pointer to caller-owned memory, dense
  *     row-major with the last index fastest.  The library allocates nothing
- *     on the device, keeps no global state and never frees caller memory.
+ *     on the device and never frees caller memory.  Its only state is
+ *     process-wide bookkeeping: the per-thread error text, a launch counter,
+ *     each device's SM count (queried once), the test hooks below, and the
+ *     no-workspace decode's built-in scratch array (see
+ *     yoco_cross_attn_decode_noalloc).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
  *     enqueue work on it and return without synchronising.
  *   - Arguments are validated on the host before anything is enqueued; on
@@ -108,8 +112,13 @@ typedef struct {
  *   gate_logits  [B, N, H]      fp32         o  [B, N, H, dv] out_dt
  *   state        [B, H, dk, dv] fp32, in: the state before token 0 (zero it
  *                for a fresh sequence), out: the state after token N-1.
- *   chunk        0 = the kernel's own choice, else 16, 32, 64 or 128; the
- *                result depends on it only through rounding.
+ *   chunk        0, 64 or 128 (anything else: YOCO_ERR_UNSUPPORTED); the
+ *                result depends on it only through rounding.  0 and 128 run
+ *                the tensor-core kernel (128-token chunks) when in_dt is bf16
+ *                and dk = dv = 128, else the CUDA-core kernel (64-token
+ *                chunks, fp32 arithmetic); 64 always runs the CUDA-core kernel.
+ *                With bf16 and d = 128 the tensor-core kernel leaves out state
+ *                contributions whose decay weight is below e^-40 (~4e-18).
  *   workspace    device scratch of at least yoco_gret_prefill_workspace_size
  *                bytes, 256-byte aligned (may be NULL when that size is 0).
  * Supported: dk = dv in {64, 128}; in_dt = out_dt; N >= 0 (N = 0 leaves
@@ -210,9 +219,21 @@ YOCO_API yoco_status yoco_cross_attn_decode(const void *Q, int Hq, const yoco_kv
  *     contents (every partial read is first written by the same call, so
  *     nothing needs clearing).  Calls that overlap on the GPU, e.g. on two
  *     streams at once, race on it: order them on one stream.
+ *   - The array's first 256 bytes are the status word a workspace would hold
+ *     (see yoco_workspace_status): read it with
+ *     yoco_cross_attn_decode_noalloc_status.
  */
 YOCO_API yoco_status yoco_cross_attn_decode_noalloc(const void *Q, int Hq, const yoco_kv_cache *cache,
                                                     float scale, int num_splits, void *O, void *stream);
+
+/*
+ * Status word of the no-workspace decode's built-in scratch on the current
+ * device, as yoco_workspace_status reports it for a workspace: waits for
+ * `stream`, returns YOCO_OK or YOCO_ERR_TIMEOUT (a bounded on-device wait of an
+ * earlier no-workspace call gave up; detail in yoco_last_error()), and with
+ * clear != 0 resets the word.  Allocates nothing.
+ */
+YOCO_API yoco_status yoco_cross_attn_decode_noalloc_status(int clear, void *stream);
 
 /* Workspace bytes for a prefill (T rows) or decode (T = 1) attention call. */
 YOCO_API size_t yoco_cross_attn_workspace_size(int B, int Hq, int T, const yoco_kv_cache *cache,
@@ -359,6 +380,26 @@ YOCO_API yoco_status yoco_selftest_wait_timeout(void *workspace, uint64_t limit_
 /* Number of kernels this process has enqueued through libyoco so far
  * (monotonic, all threads).  A diagnostic for counting launches per step. */
 YOCO_API uint64_t yoco_launch_count(void);
+
+/*
+ * Test hooks: process-wide switches that let tests reach failure and ordering
+ * paths that ordinary inputs cannot force.  Not part of the method; all are 0
+ * (off) at load.  Returns YOCO_ERR_INVALID_ARG for an unknown hook or a value
+ * out of range.
+ *   YOCO_HOOK_FAIL_NEXT_CALLS     the next `value` (<= 1e6) calls that would
+ *       launch a kernel instead return YOCO_ERR_CUDA ("unspecified launch
+ *       failure" in yoco_last_error()) after their argument checks and before
+ *       enqueuing anything, so nothing is written: a stand-in for a failed
+ *       launch that faults no GPU.
+ *   YOCO_HOOK_GRET_SEG0_DELAY_NS  with the tensor-core gRet prefill split into
+ *       segments, segment 0 of every head takes the caller's initial state
+ *       `value` ns (<= 1e9) late, so the last segment finishes first and its
+ *       final state goes through the hand-off's parked path.  Results are
+ *       unchanged; only timing moves.
+ */
+#define YOCO_HOOK_FAIL_NEXT_CALLS 1
+#define YOCO_HOOK_GRET_SEG0_DELAY_NS 2
+YOCO_API yoco_status yoco_test_hook(int hook, int64_t value);
 
 #ifdef __cplusplus
 }

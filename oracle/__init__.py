@@ -55,6 +55,8 @@ def lib():
             _b.build()
         L = ctypes.CDLL(_LIB_PATH)
         i, d, i64 = ctypes.c_int, ctypes.c_double, ctypes.c_int64
+        L.oracle_set_threads.argtypes = [i]
+        L.oracle_set_threads.restype = None
         L.oracle_gate.argtypes = [d, d]
         L.oracle_gate.restype = d
         L.oracle_gret_recurrent.argtypes = [i, i, i, i, i, _dp, _dp, _dp, _dp, d, _dp, _dp, _dp]
@@ -74,6 +76,11 @@ def lib():
         _lib = L
     return _lib
 
+
+
+def set_threads(n):
+    """Threads the oracle's OpenMP loops use from now on (n > 0)."""
+    lib().oracle_set_threads(int(n))
 
 def _f64(a) -> np.ndarray:
     """Widen to a contiguous fp64 array (exact for bf16 bits given as float32 and fp32)."""

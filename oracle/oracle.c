@@ -19,6 +19,9 @@
  *   Q, O      [B, T, Hq, d]      cache K, V [B, Hkv, cap, d]
  */
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -35,6 +38,17 @@ static double log_sigmoid(double x)
     if (x >= 0.0)
         return -log1p(exp(-x));
     return x - log1p(exp(x));
+}
+
+/* Threads the OpenMP loops below may use (n > 0); the checker's own knob, used to
+ * time it on one core as well as on all of them.  Without OpenMP it does nothing. */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
 }
 
 double oracle_gate(double logit, double tau)

@@ -29,6 +29,18 @@ def rel_l2(x, ref):
     return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
 
 
+def worst_block_rel_l2(x, ref, block):
+    """Largest relative L2 error over consecutive blocks of `block` rows (axis 0):
+    a single wrong chunk or segment boundary shows here even where the
+    whole-tensor figure would absorb it."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    worst = 0.0
+    for r0 in range(0, x.shape[0], block):
+        worst = max(worst, rel_l2(x[r0:r0 + block], ref[r0:r0 + block]))
+    return worst
+
+
 def max_abs(x, ref):
     return float(np.max(np.abs(np.asarray(x, np.float64) - np.asarray(ref, np.float64))))
 

@@ -230,3 +230,33 @@ def test_qkvg_validation(Y):
     assert L.yoco_gret_qkvg_project(*args(8, 128, rb=-1.0)) == Y.YOCO_ERR_INVALID_ARG
     assert L.yoco_gret_qkvg_project(*args(8, 128, rb=1e4, ws=None, n=0)) == Y.YOCO_ERR_WORKSPACE
     assert L.yoco_gret_qkvg_workspace_size(1, 64, 8, 128, 1e4) == 256 + 64 * 64 * 8
+
+
+def test_test_hook_rejects_unknown_hooks_and_ranges(Y):
+    assert Y.lib.yoco_test_hook(0, 1) == Y.YOCO_ERR_INVALID_ARG
+    assert Y.lib.yoco_test_hook(99, 1) == Y.YOCO_ERR_INVALID_ARG
+    assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_FAIL_NEXT_CALLS, -1) == Y.YOCO_ERR_INVALID_ARG
+    assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_FAIL_NEXT_CALLS, 10 ** 7) == Y.YOCO_ERR_INVALID_ARG
+    assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_GRET_SEG0_DELAY_NS, 2 * 10 ** 9) == Y.YOCO_ERR_INVALID_ARG
+    assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_GRET_SEG0_DELAY_NS, 0) == Y.YOCO_OK
+
+
+def test_injected_launch_failure_comes_after_argument_checks(Y):
+    """An injected failure is returned as YOCO_ERR_CUDA by calls whose arguments
+    pass, one per call, before anything is enqueued; a call that fails its
+    argument checks reports that instead and leaves the injection pending."""
+    def decode_step(B=1):
+        return Y.lib.yoco_gret_decode_step(FAKE, FAKE, FAKE, FAKE, 16.0, FAKE, FAKE, B, 2, 64, 64, 0, 0, None)
+
+    n0 = Y.lib.yoco_launch_count()
+    assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_FAIL_NEXT_CALLS, 2) == Y.YOCO_OK
+    try:
+        assert decode_step() == Y.YOCO_ERR_CUDA
+        assert b"launch failure" in Y.lib.yoco_last_error()
+        assert decode_step(B=0) == Y.YOCO_ERR_INVALID_ARG  # argument error first; injection still pending
+        assert Y.lib.yoco_gret_prefill_chunkwise(FAKE, FAKE, FAKE, FAKE, 16.0, FAKE, FAKE, 1, 8, 1, 64, 64, 0, 0, 0,
+                                                 FAKE, 1 << 20, None) == Y.YOCO_ERR_CUDA
+        assert b"launch failure" in Y.lib.yoco_last_error()
+        assert Y.lib.yoco_launch_count() == n0  # nothing was enqueued
+    finally:
+        assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_FAIL_NEXT_CALLS, 0) == Y.YOCO_OK

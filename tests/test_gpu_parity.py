@@ -6,17 +6,20 @@ relative L2 <= 1e-2 per output tensor; the cache append bit-exact where the
 inputs make every sum exact.  Sizes span several chunks / tiles / splits and
 end on ragged tails.
 """
+import ctypes
+
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from _util import dev_bf16, dev_f32, gen, host_bits, host_f64, max_abs, rel_l2
+from _util import dev_bf16, dev_f32, gen, host_bits, host_f64, max_abs, rel_l2, worst_block_rel_l2
 
 pytestmark = pytest.mark.gpu
 
 FP32_MAX_ABS = 1e-4
 BF16_REL_L2 = 1e-2
+BLOCK_REL_L2 = 3e-2  # worst 128-row block: bf16 rounding of one block, with room (a wrong block is ~1)
 SEED = synth.DEFAULT_SEED
 
 
@@ -124,10 +127,11 @@ def test_gret_prefill_bf16_tensor_core_shapes(Y, B, N, H, with_state):
 
 @pytest.mark.parametrize("B,N,H", [(1, 128 * 100 + 33, 1), (2, 300, 38)])
 def test_gret_prefill_bf16_segment_prefix_extremes(Y, B, N, H):
-    """The output CTAs of a head fold the segment states together, each taking a
-    slice of the state's rows: one head over 101 chunks (101 one-chunk segments,
-    so each CTA folds one or two rows across 100 states) and 76 heads (two
-    segments, so one CTA folds all 128 rows), both from an initial state."""
+    """Each output CTA folds the earlier segments' end states into its own
+    initial state: one head over 101 chunks (101 one-chunk segments; a chunk
+    decays by about e^-1.4 here, so the later CTAs fold the last ~28 states and
+    leave the older ones out) and 76 heads (two segments), both from an initial
+    state."""
     d = 128
     host, dev = gret_inputs(37, B, N, H, d, "bf16", logit_mean=2.0)
     S0 = synth.normal(SEED, sid(37, 1, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
@@ -151,6 +155,114 @@ def test_gret_prefill_bf16_many_segments_state_and_strong_decay(Y):
     o_ref, S_ref = oracle.gret_recurrent(host[0], host[1], host[2], lg, 16.0, S0=S0)
     assert rel_l2(o, o_ref) <= BF16_REL_L2
     assert rel_l2(S, S_ref) <= BF16_REL_L2
+
+
+def test_gret_prefill_bf16_no_decay_many_segments(Y):
+    """gamma = 1 everywhere (logits +inf): no state contribution is small, so the
+    segment-state walk covers every chunk and every output CTA folds all earlier
+    segments and the initial state (41 one-chunk segments of one head)."""
+    B, N, H, d = 1, 128 * 40 + 17, 2, 128
+    host, dev = gret_inputs(41, B, N, H, d, "bf16")
+    lg = np.full_like(host[3], np.inf)
+    dev = dev[:3] + (dev_f32(lg),)
+    S0 = synth.normal(SEED, sid(41, 1, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
+    o, S = run_prefill(Y, dev, B, N, H, d, "bf16", S0=S0)
+    o_ref, S_ref = oracle.gret_recurrent(host[0], host[1], host[2], lg, 16.0, S0=S0)
+    assert rel_l2(o, o_ref) <= BF16_REL_L2
+    assert rel_l2(S, S_ref) <= BF16_REL_L2
+
+
+def test_gret_prefill_bf16_mixed_decay_across_segments(Y):
+    """Segments that decay strongly (the backward walk stops after a couple of
+    chunks and later segments leave the older states out) next to segments
+    with no decay at all (the walk and the fold reach back through them), from
+    an initial state: 24 heads, 6 segments of 11 chunks."""
+    B, N, H, d = 1, 128 * 60 + 50, 24, 128
+    host, dev = gret_inputs(42, B, N, H, d, "bf16", logit_mean=2.0)
+    lg = host[3].copy()
+    seg = 11 * 128
+    lg[:, 0:seg] = np.inf                    # segment 0: gamma = 1
+    lg[:, seg:2 * seg] -= 5.0                # segment 1: about e^-0.3 per token
+    lg[:, 2 * seg:3 * seg] = np.inf          # segment 2: gamma = 1
+    lg[:, 4 * seg + 300:4 * seg + 420] = -8  # a strongly decaying stretch inside segment 4
+    lg[:, :, ::2] = np.inf                   # every other head never decays
+    dev = dev[:3] + (dev_f32(lg),)
+    S0 = synth.normal(SEED, sid(42, 1, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
+    o, S = run_prefill(Y, dev, B, N, H, d, "bf16", S0=S0)
+    o_ref, S_ref = oracle.gret_recurrent(host[0], host[1], host[2], lg, 16.0, S0=S0)
+    for h in range(H):
+        assert rel_l2(o[:, :, h], o_ref[:, :, h]) <= BF16_REL_L2, h
+        assert worst_block_rel_l2(o[0, :, h], o_ref[0, :, h], 128) <= BLOCK_REL_L2, h
+        assert rel_l2(S[:, h], S_ref[:, h]) <= BF16_REL_L2, h
+
+
+def test_gret_prefill_final_state_parked_hand_off(Y):
+    """With segment 0 made to take the caller's state 20 ms late (test hook), the
+    last segment of every head finishes first, parks the final state in the
+    workspace, and segment 0 copies it to `state` after reading the initial one.
+    Two calls in a row on one workspace; results as without the delay."""
+    import torch
+    B, N, H, d = 1, 4000, 8, 128
+    host, dev = gret_inputs(43, B, N, H, d, "bf16", logit_mean=2.0)
+    S0 = synth.normal(SEED, sid(43, 1, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
+    ws = torch.empty(max(256, Y.yoco_gret_prefill_workspace_size(B, N, H, d, d, 0, Y.YOCO_BF16)),
+                     dtype=torch.uint8, device="cuda")
+    assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_GRET_SEG0_DELAY_NS, 20_000_000) == Y.YOCO_OK
+    try:
+        qd, kd, vd, lgd = dev
+        for _ in range(2):
+            S = dev_f32(S0)
+            o = torch.empty_like(vd)
+            Y.yoco_gret_prefill_chunkwise(qd, kd, vd, lgd, 16.0, o, S, workspace=ws)
+            torch.cuda.synchronize()
+            Y.yoco_workspace_status(ws)
+            o_ref, S_ref = oracle.gret_recurrent(*host, 16.0, S0=S0)
+            assert rel_l2(host_f64(o), o_ref) <= BF16_REL_L2
+            assert rel_l2(S.cpu().numpy().astype(np.float64), S_ref) <= BF16_REL_L2
+    finally:
+        assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_GRET_SEG0_DELAY_NS, 0) == Y.YOCO_OK
+
+
+def test_injected_launch_failure_writes_nothing(Y):
+    """A launch failure injected in the status layer (test hook): the gRet
+    prefill and the decode attention return YOCO_ERR_CUDA with the outputs and
+    the state untouched, and the next calls run normally."""
+    import torch
+    B, N, H, d = 1, 300, 2, 128
+    host, dev = gret_inputs(44, B, N, H, d, "bf16", logit_mean=2.0)
+    qd, kd, vd, lgd = dev
+    o = torch.full_like(vd, 7.0)
+    S = torch.full((B, H, d, d), 3.0, device="cuda")
+    ws = torch.empty(max(256, Y.yoco_gret_prefill_workspace_size(B, N, H, d, d, 0, Y.YOCO_BF16)),
+                     dtype=torch.uint8, device="cuda")
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_FAIL_NEXT_CALLS, 2) == Y.YOCO_OK
+    n0 = Y.lib.yoco_launch_count()
+    st = Y.lib.yoco_gret_prefill_chunkwise(P(qd), P(kd), P(vd), P(lgd), 16.0, P(o), P(S), B, N, H, d, d, 0, 1, 1,
+                                           P(ws), ws.numel(), stream)
+    assert st == Y.YOCO_ERR_CUDA and b"launch failure" in Y.lib.yoco_last_error()
+    Kc, Vc = torch.randn(1, 2, 64, d, device="cuda").bfloat16(), torch.randn(1, 2, 64, d, device="cuda").bfloat16()
+    cache = Y.KVCache(1, 2, d, 64, k=Kc, v=Vc)
+    cache.set_length(64)
+    Qd = torch.randn(1, 6, d, device="cuda").bfloat16()
+    Od = torch.full_like(Qd, 5.0)
+    wsa = torch.empty(max(256, Y.lib.yoco_cross_attn_workspace_size(1, 6, 1, ctypes.byref(cache.c), 0)),
+                      dtype=torch.uint8, device="cuda")
+    st = Y.lib.yoco_cross_attn_decode(P(Qd), 6, ctypes.byref(cache.c), 0.1, 0, P(Od), P(wsa), wsa.numel(), stream)
+    assert st == Y.YOCO_ERR_CUDA
+    assert Y.lib.yoco_launch_count() == n0  # nothing was enqueued
+    torch.cuda.synchronize()
+    assert bool((o == 7.0).all()) and bool((S == 3.0).all()) and bool((Od == 5.0).all())
+    # the hook is spent: the same calls now run and match the oracle
+    S.zero_()
+    Y.yoco_gret_prefill_chunkwise(qd, kd, vd, lgd, 16.0, o, S, workspace=ws)
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0)
+    assert rel_l2(host_f64(o), o_ref) <= BF16_REL_L2
+    Y.yoco_cross_attn_decode(Qd, cache, Od)
+    torch.cuda.synchronize()
+    assert np.isfinite(host_f64(Od)).all()
 
 
 def test_gret_prefill_bf16_strong_decay(Y):
@@ -188,9 +300,10 @@ def test_gret_prefill_state_continuation(Y):
 def test_gret_prefill_two_calls_on_one_dirty_workspace(Y):
     """Two chained calls (the second continues the first's final state) on one
     workspace that starts as int32 ones (status word aside): segment 0 of each
-    (b, h) starts from the caller's state while the first pass runs, and the last
-    segment overwrites that state only after segment 0 has read it (16 segments
-    per head here, with a nonzero initial state)."""
+    (b, h) starts from the caller's state while the first pass runs, and the
+    final state replaces it only after segment 0 has its copy (the hand-off word
+    is cleared by each call; 16 segments per head here, with a nonzero initial
+    state)."""
     import torch
     B, N, H, d = 1, 4000, 8, 128
     host, dev = gret_inputs(37, B, N, H, d, "bf16", logit_mean=2.0)
