@@ -95,7 +95,7 @@ def load_peaks():
 
 # ----------------------------------------------------------------- CPU oracle
 
-SAMPLE_TOKENS, SAMPLE_ROWS, SAMPLE_KEYS = 4096, 64, 16384
+SAMPLE_TOKENS, SAMPLE_ROWS, SAMPLE_KEYS = 12288, 64, 16384
 
 
 def _cpu_inputs(tokens, proj_rows, cross_keys):

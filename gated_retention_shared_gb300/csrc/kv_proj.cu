@@ -391,6 +391,117 @@ proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__re
     }
 }
 
+// Few rows, bf16 (decode): column strips.  CTA = 16 output columns of [W_K | W_V]
+// over the whole of d_model, 512 threads: thread t holds rows t, t + 512, ... of the
+// strip (32 bytes = one sector of W each), so every W byte is read once, by one
+// CTA, in one round of loads issued before the wait on the previous kernel (the
+// weights are not written by it; the input rows M may be).  The products, and each
+// input row's sum of squares for the RMS factor, are reduced inside the CTA by warp
+// shuffles and one pass through shared memory: no partial sums leave the CTA and
+// no CTA waits for another.  The last CTA (ticket) publishes the new length.
+constexpr int kStripThreads = 512;
+constexpr int kStripCols = 16;
+
+template <int KR, int RG>
+__global__ void __launch_bounds__(kStripThreads, 1)
+proj_gemv_strip(const bf16_t *__restrict__ M, const bf16_t *__restrict__ g, const bf16_t *__restrict__ Wk,
+                const bf16_t *__restrict__ Wv, bf16_t *__restrict__ kc, bf16_t *__restrict__ vc, int R, int T_rows,
+                int dm, int n, int Hkv, int d, int64_t cap, int64_t len, float eps, int32_t *len_dev,
+                float rope_base, const RopeFreq rf) {
+    __shared__ float red[kStripThreads / 32][RG][kStripCols + 1];  // per warp: 16 column sums, sum of squares
+    __shared__ float fin[RG][kStripCols + 1];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c0 = blockIdx.x * kStripCols;               // first column of the strip in [0, 2n)
+    const bf16_t *W = (c0 < n) ? Wk + c0 : Wv + (c0 - n);  // n % 16 == 0: a strip lies in W_K or in W_V
+    uint4 wr[KR][2];
+#pragma unroll
+    for (int i = 0; i < KR; ++i) {
+        const int k = tid + i * kStripThreads;
+        if (k < dm) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(W + (size_t)k * n);
+            wr[i][0] = __ldg(src);
+            wr[i][1] = __ldg(src + 1);
+        } else {
+            wr[i][0] = wr[i][1] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");  // M (and the cache) after the previous kernel
+    for (int r0 = 0; r0 < R; r0 += RG) {
+        float acc[RG][kStripCols], ss[RG];
+#pragma unroll
+        for (int rr = 0; rr < RG; ++rr) {
+            ss[rr] = 0.f;
+#pragma unroll
+            for (int e = 0; e < kStripCols; ++e) acc[rr][e] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < KR; ++i) {
+            const int k = tid + i * kStripThreads;
+            if (k >= dm) continue;
+            float w[kStripCols];
+            const uint32_t x[8] = {wr[i][0].x, wr[i][0].y, wr[i][0].z, wr[i][0].w,
+                                   wr[i][1].x, wr[i][1].y, wr[i][1].z, wr[i][1].w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                w[2 * e] = __uint_as_float(x[e] << 16);
+                w[2 * e + 1] = __uint_as_float(x[e] & 0xFFFF0000u);
+            }
+            const float gk = g ? to_f32(g[k]) : 1.f;
+#pragma unroll
+            for (int rr = 0; rr < RG; ++rr) {
+                if (r0 + rr >= R) break;
+                const float m = to_f32(M[(size_t)(r0 + rr) * dm + k]);
+                ss[rr] = fmaf(m, m, ss[rr]);
+                const float mg = m * gk;
+#pragma unroll
+                for (int e = 0; e < kStripCols; ++e) acc[rr][e] = fmaf(mg, w[e], acc[rr][e]);
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < RG; ++rr) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+                for (int e = 0; e < kStripCols; ++e) acc[rr][e] += __shfl_xor_sync(0xffffffffu, acc[rr][e], off);
+                ss[rr] += __shfl_xor_sync(0xffffffffu, ss[rr], off);
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int e = 0; e < kStripCols; ++e) red[warp][rr][e] = acc[rr][e];
+                red[warp][rr][kStripCols] = ss[rr];
+            }
+        }
+        __syncthreads();
+        if (tid < RG * (kStripCols + 1)) {  // (row, column or sum of squares): add the 16 warps in order
+            const int rr = tid / (kStripCols + 1), e = tid % (kStripCols + 1);
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kStripThreads / 32; ++w) sum += red[w][rr][e];
+            fin[rr][e] = sum;
+        }
+        __syncthreads();
+        if (tid < RG * (kStripCols / 2)) {  // one channel pair of one row: scale, rotate (K^), round, store
+            const int rr = tid / (kStripCols / 2), j = tid % (kStripCols / 2), row = r0 + rr;
+            if (row < R) {
+                const int b = row / T_rows, t = row % T_rows;
+                const float rms = rsqrtf(fin[rr][kStripCols] / (float)dm + eps);
+                float x0 = fin[rr][2 * j] * rms, x1 = fin[rr][2 * j + 1] * rms;
+                const int c = c0 + 2 * j, cn = c % n, h = cn / d, cc = cn % d;
+                if (rope_base > 0.f && c < n) {  // rotary encoding of K^ at slot position len + t
+                    float cs, sn;
+                    rope_cs_exact(len + t, rf.theta[cc / 2], cs, sn);
+                    rope_turn(x0, x1, cs, sn);
+                }
+                bf16_t *dst = ((c < n) ? kc : vc) + (((size_t)b * Hkv + h) * cap + len + t) * d + cc;
+                dst[0] = from_f32<bf16_t>(x0);
+                dst[1] = from_f32<bf16_t>(x1);
+            }
+        }
+        __syncthreads();  // red and fin are rewritten by the next rows
+    }
+    finish_append(len_dev, len + T_rows);
+}
+
 }  // namespace yoco
 
 namespace yoco_host {
@@ -409,20 +520,48 @@ static int gemv_chunks(int n, int dm) {
     return (dm + kr - 1) / kr;
 }
 
+constexpr int kStripMaxRows = 4;
+
+static bool strip_eligible(int R, int n, int dm, yoco_dtype dt) {
+    return dt == YOCO_BF16 && R <= kStripMaxRows && n % kStripCols == 0 && dm % 8 == 0 && dm <= 6 * kStripThreads;
+}
+
 // workspace: [0, 256) status word of the tensor-core kernel, one fp32 RMS factor
 // per row (tensor-core and tiled paths), then (few-row path) the K-chunk partials
 // workspace: [0, 256) status word, one fp32 RMS factor per row (padded to 256 B), then
 // either the few-row path's K-chunk partials or, with rotary encoding on the other
 // paths, the (cos, sin) table of the T positions [T][d/2] (the paths never meet)
 size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt, float rope_base) {
-    (void)dt;
     size_t rows = (size_t)B * T;
     size_t ws = 256 + ((rows * sizeof(float) + 255) / 256) * 256;
     const int n = Hkv * d;
     size_t extra = 0;
-    if (gemv_eligible((int)rows, n, dm)) extra = (size_t)gemv_chunks(n, dm) * rows * 2 * n * sizeof(float);
+    if (strip_eligible((int)rows, n, dm, dt)) extra = 0;
+    else if (gemv_eligible((int)rows, n, dm)) extra = (size_t)gemv_chunks(n, dm) * rows * 2 * n * sizeof(float);
     else if (rope_base > 0.f) extra = (size_t)T * (d / 2) * sizeof(float2);
     return ws + extra;
+}
+
+template <int KR>
+static cudaError_t launch_strip(const KvProjArgs &a, int R, int n, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * n / kStripCols);
+    cfg.blockDim = dim3(kStripThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    count_launches(1);
+    const RopeFreq rf = make_rope_freq(a.rope_base, a.d);
+    if (R == 1)
+        return cudaLaunchKernelEx(&cfg, proj_gemv_strip<KR, 1>, (const bf16_t *)a.M, (const bf16_t *)a.rms_w,
+                                  (const bf16_t *)a.Wk, (const bf16_t *)a.Wv, (bf16_t *)a.kc, (bf16_t *)a.vc, R, a.T,
+                                  a.dm, n, a.Hkv, a.d, a.cap, a.len, a.eps, a.len_dev, a.rope_base, rf);
+    return cudaLaunchKernelEx(&cfg, proj_gemv_strip<KR, 2>, (const bf16_t *)a.M, (const bf16_t *)a.rms_w,
+                              (const bf16_t *)a.Wk, (const bf16_t *)a.Wv, (bf16_t *)a.kc, (bf16_t *)a.vc, R, a.T, a.dm,
+                              n, a.Hkv, a.d, a.cap, a.len, a.eps, a.len_dev, a.rope_base, rf);
 }
 
 template <typename T>
@@ -431,6 +570,12 @@ static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
     const int n = a.Hkv * a.d;
     float *r = (float *)((char *)ws + 256);
     cudaError_t e;
+    if (strip_eligible(R, n, a.dm, a.dt)) {
+        const int kr = (a.dm + kStripThreads - 1) / kStripThreads;  // W rows per thread
+        if (kr <= 2) return launch_strip<2>(a, R, n, st);
+        if (kr <= 4) return launch_strip<4>(a, R, n, st);
+        return launch_strip<6>(a, R, n, st);
+    }
     if (gemv_eligible(R, n, a.dm) && !(std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a))) {
         const int kch = gemv_chunks(n, a.dm);
         const int KR = (a.dm + kch - 1) / kch;

@@ -160,6 +160,10 @@ YOCO_API yoco_status yoco_gret_decode_step(const void *q, const void *k, const v
  *   Wk, Wv [dm, Hkv * d]    cache dtype; column h*d + c feeds head h, lane c
  * All four pointers 16-byte aligned.
  * Exactly slots [len, len + T) change; every other cache byte is untouched.
+ * The weights (Wk, Wv, rms_w) may be read while the kernel before the call on
+ * the stream is still finishing (programmatic dependent launch); a caller that
+ * writes them with a kernel of its own just before the append must not let that
+ * kernel release its dependents early.  M is read only after it has finished.
  * Returns YOCO_ERR_CAPACITY (nothing written) if len + T > capacity.
  *   workspace  >= yoco_shared_kv_workspace_size bytes, 256-byte aligned.
  */

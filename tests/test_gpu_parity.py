@@ -404,6 +404,40 @@ def test_kv_append_bit_exact(Y):
         assert cache.length == length and int(cache.len_dev[0]) == length and int(cache.len_dev[1]) == 0
 
 
+@pytest.mark.parametrize("B,T,dm,Hkv,d,gain", [(1, 1, 3072, 8, 128, False), (2, 2, 3072, 8, 128, True),
+                                                (1, 3, 256, 1, 64, False), (4, 1, 1000, 2, 128, True)])
+def test_kv_append_decode_rows_bit_exact(Y, B, T, dm, Hkv, d, gain):
+    """The few-row (decode) projection: at most four input rows, each CTA one
+    16-column strip of [W_K | W_V] over all of d_model.  +-1 rows, eps 0, dyadic
+    weights (and a gain of powers of two) make every sum exact, so the slots
+    must equal the oracle's bit for bit, twice in a row, and nothing else in the
+    cache may change."""
+    import torch
+    cap = 2 * T + 3
+    rng_bits = np.random.default_rng(1).integers(0, 0x7F7F, size=(B, Hkv, cap, d)).astype(np.uint16)
+    cache = Y.KVCache(B, Hkv, d, cap, k=dev_bf16(rng_bits), v=dev_bf16(rng_bits[::-1].copy()))
+    cache.set_length(1)
+    kref, vref = rng_bits.copy(), rng_bits[::-1].copy()
+    Wk = synth.dyadic(SEED, sid(21, 0, synth.T_WK), (dm, Hkv * d))
+    Wv = synth.dyadic(SEED, sid(21, 0, synth.T_WV), (dm, Hkv * d))
+    Wkd, Wvd = dev_bf16(synth.f64_to_bf16_bits(Wk)), dev_bf16(synth.f64_to_bf16_bits(Wv))
+    g = None
+    if gain:
+        g = 2.0 ** (np.arange(dm) % 3 - 1)  # 0.5, 1, 2, ...
+    length = 1
+    for step in range(2):
+        M = synth.signs(SEED, sid(21, 0, synth.T_M, step), (B, T, dm))
+        gd = None if g is None else dev_bf16(synth.f64_to_bf16_bits(g))
+        Y.yoco_shared_kv_project_append(dev_bf16(synth.f64_to_bf16_bits(M)), Wkd, Wvd, cache, eps=0.0, rms_w=gd)
+        kref = oracle.kv_append_bf16(kref, oracle.rmsnorm_proj(M, Wk, 0.0, g=g), length)
+        vref = oracle.kv_append_bf16(vref, oracle.rmsnorm_proj(M, Wv, 0.0, g=g), length)
+        length += T
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(cache.k), kref)
+        assert np.array_equal(host_bits(cache.v), vref)
+        assert cache.length == length and int(cache.len_dev[0]) == length and int(cache.len_dev[1]) == 0
+
+
 def test_kv_append_tensor_core_bit_exact(Y):
     """The tensor-core projection (>= 128 rows, Hkv*d a multiple of 256): exact
     inputs give a bit-identical cache, appended after existing slots."""
