@@ -76,6 +76,7 @@ def _load():
         "yoco_gret_qkvg_workspace_size": (sz, [i, i, i, i, f]),
         "yoco_cross_attn_decode_noalloc_status": (i, [i, vp]),
         "yoco_test_hook": (i, [i, i64]),
+        "yoco_selftest_occupy_sms": (i, [i, ctypes.c_uint64, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -92,7 +93,8 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_workspace_status", "yoco_cross_attn_decode_noalloc", "yoco_selftest_wait_timeout",
             "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size", "yoco_gret_group_norm_gate",
             "yoco_rope_apply", "yoco_gret_qkvg_project", "yoco_gret_qkvg_workspace_size",
-            "yoco_gret_decode_step_gn_gate", "yoco_cross_attn_decode_noalloc_status", "yoco_test_hook")
+            "yoco_gret_decode_step_gn_gate", "yoco_cross_attn_decode_noalloc_status", "yoco_test_hook",
+            "yoco_selftest_occupy_sms")
 YOCO_HOOK_FAIL_NEXT_CALLS, YOCO_HOOK_GRET_SEG0_DELAY_NS = 1, 2
 
 

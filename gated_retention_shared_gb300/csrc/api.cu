@@ -152,6 +152,12 @@ yoco_status yoco_selftest_wait_timeout(void *workspace, uint64_t limit_ns, void 
     return cuda_status(selftest_wait(workspace, limit_ns, (cudaStream_t)stream), "selftest_wait_timeout");
 }
 
+yoco_status yoco_selftest_occupy_sms(int ctas, uint64_t ns, void *stream) {
+    if (ctas <= 0 || ctas > 4 * device_sm_count()) return fail(YOCO_ERR_INVALID_ARG, "ctas must be in [1, 4 * SMs]");
+    if (ns == 0 || ns > 1000000000ull) return fail(YOCO_ERR_INVALID_ARG, "ns must be in (0, 1e9]");
+    return cuda_status(selftest_occupy(ctas, ns, (cudaStream_t)stream), "selftest_occupy_sms");
+}
+
 uint64_t yoco_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 yoco_status yoco_test_hook(int hook, int64_t value) {

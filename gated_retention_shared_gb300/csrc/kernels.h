@@ -116,5 +116,6 @@ cudaError_t qkvg_project(const void *X, const void *W, int B, int N, int dm, int
 
 // selftest.cu
 cudaError_t selftest_wait(void *ws, uint64_t limit_ns, cudaStream_t st);
+cudaError_t selftest_occupy(int ctas, uint64_t ns, cudaStream_t st);
 
 }  // namespace yoco_host

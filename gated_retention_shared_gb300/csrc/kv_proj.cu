@@ -398,7 +398,7 @@ proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__re
 // weights are not written by it; the input rows M may be).  The products, and each
 // input row's sum of squares for the RMS factor, are reduced inside the CTA by warp
 // shuffles and one pass through shared memory: no partial sums leave the CTA and
-// no CTA waits for another.  The last CTA (ticket) publishes the new length.
+// no CTA waits for another.
 constexpr int kStripThreads = 512;
 constexpr int kStripCols = 16;
 
@@ -499,7 +499,10 @@ proj_gemv_strip(const bf16_t *__restrict__ M, const bf16_t *__restrict__ g, cons
         }
         __syncthreads();  // red and fin are rewritten by the next rows
     }
-    finish_append(len_dev, len + T_rows);
+    // No kernel reads the length on the device, and this grid releases no dependent
+    // early, so whatever runs next on the stream sees every slot and the new length:
+    // one thread publishes it, no ticket needed.
+    if (blockIdx.x == 0 && tid == 0) len_dev[0] = (int32_t)(len + T_rows);
 }
 
 }  // namespace yoco

@@ -381,6 +381,16 @@ YOCO_API yoco_status yoco_workspace_status(void *workspace, int clear, void *str
  */
 YOCO_API yoco_status yoco_selftest_wait_timeout(void *workspace, uint64_t limit_ns, void *stream);
 
+/*
+ * Self-test for a shared device: enqueues `ctas` (<= 4 x the SM count) CTAs that
+ * each claim 200 KB of shared memory, so that nothing needing much shared memory
+ * fits beside them on their SM, and sleep for `ns` (<= 1 s) of wall time.  They
+ * touch no global memory.  Tests run libyoco's calls on another stream meanwhile
+ * to check that they make progress with part of the SMs taken.  Not part of the
+ * method.
+ */
+YOCO_API yoco_status yoco_selftest_occupy_sms(int ctas, uint64_t ns, void *stream);
+
 /* Number of kernels this process has enqueued through libyoco so far
  * (monotonic, all threads).  A diagnostic for counting launches per step. */
 YOCO_API uint64_t yoco_launch_count(void);

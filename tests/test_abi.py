@@ -260,3 +260,30 @@ def test_injected_launch_failure_comes_after_argument_checks(Y):
         assert Y.lib.yoco_launch_count() == n0  # nothing was enqueued
     finally:
         assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_FAIL_NEXT_CALLS, 0) == Y.YOCO_OK
+
+
+def test_every_documented_chunk_value_is_accepted(Y):
+    """The header documents chunk in {0, 64, 128}: those pass the argument checks
+    (the call then asks for its workspace or, needing none, tries to launch,
+    which fails without a GPU), every other value is refused."""
+    header = open(HEADER).read()
+    assert "chunk        0, 64 or 128" in header
+    # an accepted call must not reach a launch with these fake pointers, even where
+    # a GPU is present: injected failures stand in for every launch meanwhile
+    assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_FAIL_NEXT_CALLS, 1000) == Y.YOCO_OK
+    try:
+        for dt, d in ((1, 128), (1, 64), (0, 64)):
+            for chunk in (0, 64, 128):
+                st = _prefill(Y, dk=d, dv=d, in_dt=dt, out_dt=dt, chunk=chunk)
+                assert st in (Y.YOCO_ERR_WORKSPACE, Y.YOCO_ERR_CUDA), (dt, d, chunk, st)
+            for chunk in (1, 16, 32, 96, 256):
+                st = _prefill(Y, dk=d, dv=d, in_dt=dt, out_dt=dt, chunk=chunk)
+                assert st == Y.YOCO_ERR_UNSUPPORTED, (dt, d, chunk)
+    finally:
+        assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_FAIL_NEXT_CALLS, 0) == Y.YOCO_OK
+
+
+def test_selftest_occupy_rejects_bad_arguments(Y):
+    assert Y.lib.yoco_selftest_occupy_sms(0, 1000, None) == Y.YOCO_ERR_INVALID_ARG
+    assert Y.lib.yoco_selftest_occupy_sms(10, 0, None) == Y.YOCO_ERR_INVALID_ARG
+    assert Y.lib.yoco_selftest_occupy_sms(10, 2 * 10 ** 9, None) == Y.YOCO_ERR_INVALID_ARG

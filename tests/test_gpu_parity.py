@@ -1116,3 +1116,47 @@ def test_bounded_wait_times_out_and_context_survives(Y):
     o, S = run_prefill(Y, dev, B, N, H, d, "bf16")
     o_ref, _ = oracle.gret_recurrent(*host, 16.0)
     assert rel_l2(o, o_ref) <= BF16_REL_L2
+
+
+def test_calls_make_progress_with_most_sms_taken(Y):
+    """A self-test kernel holds all but 40 SMs (one CTA on each, most of its shared
+    memory) for 300 ms on another stream.  Meanwhile a segmented gRet prefill
+    (24 heads x 6 segments: 264 CTAs of its two kernels, one per SM, far more than
+    the free SMs hold at once) and a split-KV decode run on this stream: both
+    finish while the other kernel still runs, record no timeout, and match the
+    oracle."""
+    import torch
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    B, N, H, d = 1, 8192 + 77, 24, 128
+    host, dev = gret_inputs(45, B, N, H, d, "bf16", logit_mean=2.0)
+    S0 = synth.normal(SEED, sid(45, 1, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
+    qd, kd, vd, lgd = dev
+    o = torch.empty_like(vd)
+    S = dev_f32(S0)
+    ws = torch.zeros(max(256, Y.yoco_gret_prefill_workspace_size(B, N, H, d, d, 0, Y.YOCO_BF16)),
+                     dtype=torch.uint8, device="cuda")
+    Kh, Kd = gen(SEED, sid(45, 2, synth.T_CACHE_K), (1, 2, 5000, d), "bf16")
+    Vh, Vd = gen(SEED, sid(45, 2, synth.T_CACHE_V), (1, 2, 5000, d), "bf16")
+    cache = Y.KVCache(1, 2, d, 5000, k=Kd, v=Vd)
+    cache.set_length(5000)
+    Qh, Qd = gen(SEED, sid(45, 3, synth.T_QX), (1, 6, d), "bf16")
+    Od = torch.empty_like(Qd)
+    wsa = torch.zeros(max(256, Y.lib.yoco_cross_attn_workspace_size(1, 6, 1, ctypes.byref(cache.c), 0)),
+                      dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    other = torch.cuda.Stream()
+    assert Y.lib.yoco_selftest_occupy_sms(n_sm - 40, 300_000_000, ctypes.c_void_p(other.cuda_stream)) == Y.YOCO_OK
+    Y.yoco_gret_prefill_chunkwise(qd, kd, vd, lgd, 16.0, o, S, workspace=ws)
+    Y.yoco_cross_attn_decode(Qd, cache, Od, workspace=wsa)
+    done = torch.cuda.Event()
+    done.record()
+    done.synchronize()
+    assert not other.query(), "the occupying kernel ended before the calls did"
+    torch.cuda.synchronize()
+    Y.yoco_workspace_status(ws)
+    Y.yoco_workspace_status(wsa)
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0, S0=S0)
+    assert rel_l2(host_f64(o), o_ref) <= BF16_REL_L2
+    assert rel_l2(S.cpu().numpy().astype(np.float64), S_ref) <= BF16_REL_L2
+    O_ref = oracle.cross_attn(Qh[:, None], Kh, Vh, 4999, d ** -0.5)[:, 0]
+    assert rel_l2(host_f64(Od), O_ref) <= BF16_REL_L2
