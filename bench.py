@@ -57,7 +57,7 @@ def parse():
     p.add_argument("--decode-tokens", type=int, default=20, help="timed tokens of the 1M-context decode")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--chunk", type=int, default=0)
-    p.add_argument("--only", choices=["gret", "proj", "append", "cross_decode", "cross_prefill", "swa_prefill",
+    p.add_argument("--only", choices=["gret", "gret_gn", "gret_gn_unfused", "proj", "append", "cross_decode", "cross_prefill", "swa_prefill",
                                       "swa_decode", "gn_gate", "rope", "qkvg", "gret_decode_unfused",
                                       "gret_decode_gn"], default=None,
                    help="time one call kind on its own (for profiling)")
@@ -628,7 +628,7 @@ def run_only(args):
     stp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     N = args.n or N_LAYER      # tokens of the call's shape (the single 32K-token gRet layer by default)
     CFG = CFG_LAYER if N == N_LAYER else 4
-    if args.only == "gret":
+    if args.only in ("gret", "gret_gn", "gret_gn_unfused"):
         q = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_Q), std=D ** -0.5)
         k = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_K), std=D ** -0.5)
         v = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_V))
@@ -640,10 +640,25 @@ def run_only(args):
         ws = torch.empty(max(256, L.yoco_gret_prefill_workspace_size(B, N, H, D, D, args.chunk, 1)), dtype=torch.uint8,
                          device=dev)
 
-        def call():
-            S.zero_()
-            return L.yoco_gret_prefill_chunkwise(P(q), P(k), P(v), P(lg), TAU, P(o), P(S), B, N, H, D, D, args.chunk,
-                                                 1, 1, P(ws), ws.numel(), stp)
+        g = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_QX)) if args.only != "gret" else None
+        z = torch.empty_like(v) if args.only != "gret" else None
+
+        if args.only == "gret":
+            def call():
+                S.zero_()
+                return L.yoco_gret_prefill_chunkwise(P(q), P(k), P(v), P(lg), TAU, P(o), P(S), B, N, H, D, D,
+                                                     args.chunk, 1, 1, P(ws), ws.numel(), stp)
+        elif args.only == "gret_gn":  # with Eq. 7's GroupNorm and swish gate fused
+            def call():
+                S.zero_()
+                return L.yoco_gret_prefill_chunkwise_gn_gate(P(q), P(k), P(v), P(lg), TAU, P(g), None, None, 1e-5,
+                                                             P(z), P(S), B, N, H, D, D, 1, P(ws), ws.numel(), stp)
+        else:  # the prefill, then the separate GroupNorm + gate pass
+            def call():
+                S.zero_()
+                st_ = L.yoco_gret_prefill_chunkwise(P(q), P(k), P(v), P(lg), TAU, P(o), P(S), B, N, H, D, D,
+                                                    args.chunk, 1, 1, P(ws), ws.numel(), stp)
+                return st_ or L.yoco_gret_group_norm_gate(P(o), P(g), None, None, 1e-5, P(z), B, N, H, D, 1, stp)
     elif args.only == "append":  # one generated token's K/V slot into a cache holding the prompt
         M1 = normal((B, 1, DM), bf, sid(CFG, 0, synth.T_M, 1))
         Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
@@ -780,8 +795,9 @@ def run_only(args):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
     line = {"only": args.only, "ms_per_call": ms, "steps": args.steps, "N": N}
-    if args.only == "gret":
-        nbytes = 4 * B * N * H * D * 2 + B * N * H * 4 + 2 * B * H * D * D * 4
+    if args.only in ("gret", "gret_gn"):
+        # the fused call also reads the gate (bf16, the size of q)
+        nbytes = (4 + (args.only == "gret_gn")) * B * N * H * D * 2 + B * N * H * 4 + 2 * B * H * D * D * 4
         line.update({"bytes_per_call": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
                      "no_decay": bool(args.no_decay)})
     if args.only == "qkvg":

@@ -76,6 +76,8 @@ def _load():
         "yoco_gret_qkvg_workspace_size": (sz, [i, i, i, i, f]),
         "yoco_cross_attn_decode_noalloc_status": (i, [i, vp]),
         "yoco_test_hook": (i, [i, i64]),
+        "yoco_gret_prefill_chunkwise_gn_gate": (i, [vp, vp, vp, vp, f, vp, vp, vp, f, vp, vp, i, i, i, i, i, i, vp, sz,
+                                                    vp]),
         "yoco_selftest_occupy_sms": (i, [i, ctypes.c_uint64, vp]),
     }
     for name, (res, args) in sigs.items():
@@ -94,7 +96,7 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size", "yoco_gret_group_norm_gate",
             "yoco_rope_apply", "yoco_gret_qkvg_project", "yoco_gret_qkvg_workspace_size",
             "yoco_gret_decode_step_gn_gate", "yoco_cross_attn_decode_noalloc_status", "yoco_test_hook",
-            "yoco_selftest_occupy_sms")
+            "yoco_selftest_occupy_sms", "yoco_gret_prefill_chunkwise_gn_gate")
 YOCO_HOOK_FAIL_NEXT_CALLS, YOCO_HOOK_GRET_SEG0_DELAY_NS = 1, 2
 
 
@@ -154,6 +156,28 @@ def yoco_gret_prefill_chunkwise(q, k, v, gate_logits, tau, o, state, chunk=0, wo
                                          _ptr(state), B, N, H, dk, dv, chunk, dt, _dt(o), _ptr(ws),
                                          0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "yoco_gret_prefill_chunkwise")
+
+
+def yoco_gret_prefill_chunkwise_gn_gate(q, k, v, gate_logits, tau, gate, z, state, eps=1e-5, gn_weight=None,
+                                        gn_bias=None, workspace=None, stream=None):
+    """z = swish(gate) * GroupNorm_h(chunkwise gRet output); q, k, v, gate, z [B,N,H,d];
+    gate_logits [B,N,H] fp32; state [B,H,d,d] fp32 (in/out); gn_weight, gn_bias fp32 [H*d] or None."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (gate_logits, "gate_logits"), (gate, "gate"), (z, "z"),
+                 (state, "state")):
+        _need(t, n)
+    B, N, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dt(q)
+    for t, n in ((gn_weight, "gn_weight"), (gn_bias, "gn_bias")):
+        if t is not None and (t.dtype != torch.float32 or t.numel() != H * dv):
+            raise ValueError(f"{n} must be fp32 with H * d elements")
+    ws_n = lib.yoco_gret_prefill_workspace_size(B, N, H, dk, dv, 0, dt)
+    ws = _workspace(ws_n, q.device, workspace)
+    st = lib.yoco_gret_prefill_chunkwise_gn_gate(_ptr(q), _ptr(k), _ptr(v), _ptr(gate_logits), float(tau), _ptr(gate),
+                                                 _ptr(gn_weight), _ptr(gn_bias), float(eps), _ptr(z), _ptr(state), B, N,
+                                                 H, dk, dv, dt, _ptr(ws),
+                                                 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "yoco_gret_prefill_chunkwise_gn_gate")
 
 
 def yoco_workspace_status(workspace, clear=True, stream=None):

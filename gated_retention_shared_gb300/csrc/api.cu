@@ -210,8 +210,41 @@ yoco_status yoco_gret_prefill_chunkwise(const void *q, const void *k, const void
     YOCO_INJECTED_FAILURE("gret_prefill_chunkwise");
     GretArgs a{q, k, v, gate_logits, tau, o, state, B, N, H, dk, dv, in_dt};
     cudaStream_t st = (cudaStream_t)stream;
-    return cuda_status(tc ? gret_prefill_tc(a, workspace, st) : gret_prefill_simt(a, workspace, st),
+    return cuda_status(tc ? gret_prefill_tc(a, nullptr, workspace, st) : gret_prefill_simt(a, workspace, st),
                        "gret_prefill_chunkwise");
+}
+
+yoco_status yoco_gret_prefill_chunkwise_gn_gate(const void *q, const void *k, const void *v, const float *gate_logits,
+                                                float tau, const void *gate, const float *gn_weight,
+                                                const float *gn_bias, float eps, void *z, float *state, int B, int N,
+                                                int H, int dk, int dv, yoco_dtype dt, void *workspace,
+                                                size_t ws_bytes, void *stream) {
+    yoco_status s = check_gret_shapes(B, N, H, dk, dv, dt, dt);
+    if (s != YOCO_OK) return s;
+    if (!state) return fail(YOCO_ERR_INVALID_ARG, "state is NULL");
+    if (!(tau > 0.0f) || !isfinite(tau)) return fail(YOCO_ERR_INVALID_ARG, "tau must be finite and > 0");
+    if (!(eps > 0.f) || !isfinite(eps)) return fail(YOCO_ERR_INVALID_ARG, "eps must be finite and > 0");
+    if (N == 0) return YOCO_OK;
+    if (!q || !k || !v || !gate_logits || !gate || !z) return fail(YOCO_ERR_INVALID_ARG, "null tensor");
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(z, 16) || !aligned(gate, 16) ||
+        !aligned(state, 16))
+        return fail(YOCO_ERR_INVALID_ARG, "q, k, v, gate, z, state must be 16-byte aligned");
+    const bool tc = gret_tc_eligible(B, N, H, dk, dv, dt);
+    const size_t need = tc ? gret_tc_workspace(B, N, H, dk, dv) : gret_simt_workspace(B, N, H, dk, dv);
+    if ((s = check_ws(workspace, ws_bytes, need)) != YOCO_OK) return s;
+    YOCO_INJECTED_FAILURE("gret_prefill_chunkwise_gn_gate");
+    GretArgs a{q, k, v, gate_logits, tau, z, state, B, N, H, dk, dv, dt};
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e;
+    if (tc) {
+        const GnArgs gn{gate, gn_weight, gn_bias, eps};
+        e = gret_prefill_tc(a, &gn, workspace, st);
+    } else {
+        // the CUDA-core kernel writes the retention output into z, then Eq. 7 in place
+        e = gret_prefill_simt(a, workspace, st);
+        if (e == cudaSuccess) e = group_norm_gate(z, gate, gn_weight, gn_bias, eps, z, (int64_t)B * N * H, H, dv, dt, st);
+    }
+    return cuda_status(e, "gret_prefill_chunkwise_gn_gate");
 }
 
 yoco_status yoco_gret_decode_step(const void *q, const void *k, const void *v, const float *gate_logits, float tau,

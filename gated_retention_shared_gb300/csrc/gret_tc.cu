@@ -61,7 +61,7 @@ constexpr int kD = 128;                     // head size
 constexpr int kTile = kC * kD * 2;          // 32 KB bf16 tile
 constexpr int kHalf = kTile / 2;            // one 64-column block
 constexpr int kStages = 2;                  // OUTPUT: 2 x (Q, K, V)
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 512;                 // 4 warpgroups: state, decay, TMA + MMA, epilogue
 constexpr float kFactorMin = -60.f;         // chunk decay above which e^{-b_k} is used
 constexpr float kDropLog = 40.f;            // state contributions weighted below e^-40 are left out
 
@@ -79,9 +79,10 @@ struct TcSmem {
     uint64_t as_full, p_free, u_full, u_free, s_ready, drain;
     uint32_t tmem_base;
     int abort_flag;
-    int go0, go1;  // per-group continue decisions (written by one thread, read by all after a barrier)
+    int go0, go1, go2;  // per-group continue decisions (written by one thread, read by all after a barrier)
     int hand_old;  // the final-state hand-off word as one thread saw it
-    float wsum0[4], wsum1[4];
+    float wsum0[4], wsum1[4], wsum2[4];
+    float gnw[kD], gnb[kD];  // GroupNorm affine of this head (output with Eq. 7 only)
     float bcr[4];  // chunk total log decay b_C, ring over chunks
     alignas(16) float ew[kC];  // e^{-b_k} (factored chunks) or b_k (direct chunks); read as float4
 
@@ -200,12 +201,26 @@ __device__ __forceinline__ void seg_initial_row(float (&S)[kD], const float *E, 
     }
 }
 
+template <int R>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R)); }
+template <int R>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R)); }
+// Registers per thread by warpgroup (launched with 128 each, 512 threads = the whole
+// register file): state 216, decay 120, TMA + MMA 48, epilogue 128; 216 + 120 + 48 +
+// 128 = 4 x 128, so the state warpgroup's increase is exactly what the others free.
+constexpr int kRegsState = 216, kRegsDecay = 120, kRegsIssue = 48;
+
+// kGN: the epilogue applies the paper's Eq. 7 output (GroupNorm per head, then the
+// swish gate) and writes z instead of the raw retention output o.
+template <bool kGN>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const float *__restrict__ logits, float inv_tau,
-               bf16_t *__restrict__ o, float *__restrict__ state, float *__restrict__ E, float *__restrict__ G,
-               int *__restrict__ hand, int N, int H, int seg_len, int P, int *err, uint64_t seg0_delay_ns) {
+               float *__restrict__ state, float *__restrict__ E, float *__restrict__ G,
+               int *__restrict__ hand, int N, int H, int seg_len, int P, int *err, uint64_t seg0_delay_ns,
+               const bf16_t *__restrict__ gate, const float *__restrict__ gn_w, const float *__restrict__ gn_b,
+               float gn_eps) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base_u32 = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (base_u32 & 1023u)) & 1023u;
@@ -276,130 +291,255 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto chunk_log_gate = [&](int n0, int row) {
         return (n0 + row < N) ? log_gate(logits[((size_t)b * N + n0 + row) * H + h], inv_tau) : 0.f;
     };
-    if (warp == 8) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_o);
-            // every q, k, v line is read once per pass and every o line written once:
-            // all of them are marked first to leave L2 (measured: 0.235 -> 0.221 ms per
-            // 32K x 24 x 128 layer; keeping the segment-state pass's k, v tiles for this
-            // pass with evict-last was slower at every fraction of L2 tried)
-            const uint64_t pol = l2_policy_evict_first();
-            // Q and K complete `full`, V completes `full_v`.  The V slot doubles as the
-            // staging buffer of the output rows of the chunk NS back: this thread stores
-            // them (TMA) and waits for the store to read the slot before it loads the next
-            // V there, so the state warps never wait on a store.
-            auto store_out = [&](int c) {  // chunk c's staged output rows -> o
-                const int sc_ = c % NS;
-                if (!mbar_wait(&sm.o_staged[sc_], (c / NS) & 1, abort_flag)) {
-                    report(err, &sm.abort_flag, 8);
-                    return false;
-                }
-                const int nc = chunk_start(c);
-                tma_store_4d_hint(&tm_o, stage_v(sc_), 0, h, nc, b, pol);
-                tma_store_4d_hint(&tm_o, stage_v(sc_) + kHalf, 64, h, nc, b, pol);
-                bulk_commit_group();
-                return true;
-            };
-            for (int i = 0; i < nchunks; ++i) {
-                const int s = i % NS;
-                if (i >= NS && !mbar_wait(&sm.empty[s], ((i / NS) + 1) & 1, abort_flag)) {
-                    report(err, &sm.abort_flag, 1);
-                    break;
-                }
-                const int n0 = chunk_start(i);
-                mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
-                for (int half = 0; half < 2; ++half) {
-                    tma_load_4d_hint(stage_k(s) + half * kHalf, &tm_k, &sm.full[s], half * 64, h, n0, b, pol);
-                    tma_load_4d_hint(stage_q(s) + half * kHalf, &tm_q, &sm.full[s], half * 64, h, n0, b, pol);
-                }
-                if (i >= NS) {
-                    if (!store_out(i - NS)) break;
-                    bulk_wait_read_all();  // the slot has been read: V(i) may land in it
-                }
-                mbar_arrive_expect_tx(&sm.full_v[s], kTile);
-                for (int half = 0; half < 2; ++half)
-                    tma_load_4d_hint(stage_v(s) + half * kHalf, &tm_v, &sm.full_v[s], half * 64, h, n0, b, pol);
-            }
-            // leave no copy in flight: wait for the last loads of each stage
-            for (int i = max(0, nchunks - NS); i < nchunks; ++i) {
-                mbar_wait(&sm.full[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
-                mbar_wait(&sm.full_v[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
-            }
-            // the output rows of the last NS chunks, then every store complete before exit
-            for (int c = max(0, nchunks - NS); c < nchunks && !*abort_flag; ++c)
-                if (!store_out(c)) break;
-            bulk_wait_all();
-        }
-    } else if (warp == 9) {
-        // --------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t id_qk = idesc_bf16_f32(kC, kC, false, false);  // A=Q (K-major),    B=K (K-major)
-            const uint32_t id_pv = idesc_bf16_f32(kC, kD, false, true);   // A=P (TMEM),       B=V (N-major)
-            const uint32_t id_qs = idesc_bf16_f32(kC, kD, false, true);   // A=Q (K-major),    B=S (N-major)
-            const uint32_t id_kv = idesc_bf16_f32(kD, kD, true, true);    // A=K'^T (M-major), B=V (N-major)
-            bool ok = true;
-            for (int i = 0; i < nchunks && ok; ++i) {
-                const int s = i % NS, ob = i & 1;
-                const uint32_t q_a = smem_u32(stage_q(s)), k_a = smem_u32(stage_k(s)), v_a = smem_u32(stage_v(s));
-                if (!(ok = mbar_wait(&sm.full[s], (i / NS) & 1, abort_flag))) break;
-                // P of the previous chunk (TMEM columns of A) must have been consumed
-                if (i > 0 && !(ok = mbar_wait(&sm.p_free, (i - 1) & 1, abort_flag))) break;
-                tc_fence_after();
-                for (int kk = 0; kk < 8; ++kk) {  // MMA1: A = Q K^T
-                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    mma_ss(tmem + kColA, smem_desc_sw128(q_a + off, 16, 1024), smem_desc_sw128(k_a + off, 16, 1024),
-                           id_qk, kk > 0);
-                }
-                mma_commit(&sm.as_full);
-                // the decay warps publish the chunk's total decay first: it decides the order
-                if (!(ok = mbar_wait(&sm.bc_ready[i & 1], (i / 2) & 1, abort_flag))) break;
-                const bool factor = sm.bcr[i & 3] > kFactorMin;
-                if (i >= 2 && !(ok = mbar_wait(&sm.o_free[ob], ((i / 2) - 1) & 1, abort_flag))) break;
-                const uint32_t o_t = tmem + kColO + 128 * ob;
-                const uint32_t s_a = smem_u32(Sbuf);
-                auto mma3 = [&]() {  // O = Q S  (Q' = diag(e^b) Q in direct chunks)
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        mma_ss(o_t, smem_desc_sw128(q_a + off, 16, 1024),
-                               smem_desc_sw128(s_a + kk * 2048, kHalf, 1024), id_qs, kk > 0);
+    if (warp >= 8 && warp < 12) {
+        regs_dec<kRegsIssue>();
+        if (warp == 8) {
+            // ------------------------------------------------------ TMA producer
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_k);
+                tma_prefetch_desc(&tm_v);
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_o);
+                // every q, k, v line is read once per pass and every o line written once:
+                // all of them are marked first to leave L2 (measured: 0.235 -> 0.221 ms per
+                // 32K x 24 x 128 layer; keeping the segment-state pass's k, v tiles for this
+                // pass with evict-last was slower at every fraction of L2 tried)
+                const uint64_t pol = l2_policy_evict_first();
+                // Q and K complete `full`, V completes `full_v`.  The V slot doubles as the
+                // staging buffer of the output rows of the chunk NS back: this thread stores
+                // them (TMA) and waits for the store to read the slot before it loads the next
+                // V there, so the state warps never wait on a store.
+                auto store_out = [&](int c) {  // chunk c's staged output rows -> o
+                    const int sc_ = c % NS;
+                    if (!mbar_wait(&sm.o_staged[sc_], (c / NS) & 1, abort_flag)) {
+                        report(err, &sm.abort_flag, 8);
+                        return false;
                     }
+                    const int nc = chunk_start(c);
+                    tma_store_4d_hint(&tm_o, stage_v(sc_), 0, h, nc, b, pol);
+                    tma_store_4d_hint(&tm_o, stage_v(sc_) + kHalf, 64, h, nc, b, pol);
+                    bulk_commit_group();
+                    return true;
                 };
-                if (!factor) {  // Q is rescaled in place together with P
-                    if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
+                for (int i = 0; i < nchunks; ++i) {
+                    const int s = i % NS;
+                    if (i >= NS && !mbar_wait(&sm.empty[s], ((i / NS) + 1) & 1, abort_flag)) {
+                        report(err, &sm.abort_flag, 1);
+                        break;
+                    }
+                    const int n0 = chunk_start(i);
+                    mbar_arrive_expect_tx(&sm.full[s], 2 * kTile);
+                    for (int half = 0; half < 2; ++half) {
+                        tma_load_4d_hint(stage_k(s) + half * kHalf, &tm_k, &sm.full[s], half * 64, h, n0, b, pol);
+                        tma_load_4d_hint(stage_q(s) + half * kHalf, &tm_q, &sm.full[s], half * 64, h, n0, b, pol);
+                    }
+                    if (i >= NS) {
+                        if (!store_out(i - NS)) break;
+                        bulk_wait_read_all();  // the slot has been read: V(i) may land in it
+                    }
+                    mbar_arrive_expect_tx(&sm.full_v[s], kTile);
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_4d_hint(stage_v(s) + half * kHalf, &tm_v, &sm.full_v[s], half * 64, h, n0, b, pol);
                 }
-                // the cross term needs nothing else from the decay warps: it fills the P bubble
-                if (!(ok = mbar_wait(&sm.s_ready, i & 1, abort_flag))) break;
-                tc_fence_after();
-                mma3();
-                if (!(ok = mbar_wait(&sm.k_ready[s], (i / NS) & 1, abort_flag))) break;
-                if (!(ok = mbar_wait(&sm.full_v[s], (i / NS) & 1, abort_flag))) break;
-                if (i > 0 && !(ok = mbar_wait(&sm.u_free, (i - 1) & 1, abort_flag))) break;
-                tc_fence_after();
-                for (int kk = 0; kk < 8; ++kk)  // MMA4: U = K'^T V
-                    mma_ss(tmem + kColU, smem_desc_sw128(k_a + kk * 2048, kHalf, 1024),
-                           smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_kv, kk > 0);
-                mma_commit(&sm.u_full);
-                if (factor) {
-                    if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
-                    tc_fence_after();
+                // leave no copy in flight: wait for the last loads of each stage
+                for (int i = max(0, nchunks - NS); i < nchunks; ++i) {
+                    mbar_wait(&sm.full[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
+                    mbar_wait(&sm.full_v[i % NS], (i / NS) & 1, abort_flag, 200000000ull);
                 }
-                for (int kk = 0; kk < 8; ++kk)  // MMA2: O += P V
-                    mma_ts(o_t, tmem + kColA + kk * 8, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_pv, 1);
-                mma_commit(&sm.o_full[ob]);
-                mma_commit(&sm.p_free);
-                mma_commit(&sm.empty[s]);
+                // the output rows of the last NS chunks, then every store complete before exit
+                for (int c = max(0, nchunks - NS); c < nchunks && !*abort_flag; ++c)
+                    if (!store_out(c)) break;
+                bulk_wait_all();
             }
-            if (!ok) report(err, &sm.abort_flag, 2);
-            // drain: nothing of ours may still run when TMEM is released
-            mma_commit(&sm.drain);
-            mbar_wait(&sm.drain, 0, abort_flag, 200000000ull);
+        } else if (warp == 9) {
+            // --------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                const uint32_t id_qk = idesc_bf16_f32(kC, kC, false, false);  // A=Q (K-major),    B=K (K-major)
+                const uint32_t id_pv = idesc_bf16_f32(kC, kD, false, true);   // A=P (TMEM),       B=V (N-major)
+                const uint32_t id_qs = idesc_bf16_f32(kC, kD, false, true);   // A=Q (K-major),    B=S (N-major)
+                const uint32_t id_kv = idesc_bf16_f32(kD, kD, true, true);    // A=K'^T (M-major), B=V (N-major)
+                bool ok = true;
+                for (int i = 0; i < nchunks && ok; ++i) {
+                    const int s = i % NS, ob = i & 1;
+                    const uint32_t q_a = smem_u32(stage_q(s)), k_a = smem_u32(stage_k(s)), v_a = smem_u32(stage_v(s));
+                    if (!(ok = mbar_wait(&sm.full[s], (i / NS) & 1, abort_flag))) break;
+                    // P of the previous chunk (TMEM columns of A) must have been consumed
+                    if (i > 0 && !(ok = mbar_wait(&sm.p_free, (i - 1) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < 8; ++kk) {  // MMA1: A = Q K^T
+                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        mma_ss(tmem + kColA, smem_desc_sw128(q_a + off, 16, 1024), smem_desc_sw128(k_a + off, 16, 1024),
+                               id_qk, kk > 0);
+                    }
+                    mma_commit(&sm.as_full);
+                    // the decay warps publish the chunk's total decay first: it decides the order
+                    if (!(ok = mbar_wait(&sm.bc_ready[i & 1], (i / 2) & 1, abort_flag))) break;
+                    const bool factor = sm.bcr[i & 3] > kFactorMin;
+                    if (i >= 2 && !(ok = mbar_wait(&sm.o_free[ob], ((i / 2) - 1) & 1, abort_flag))) break;
+                    const uint32_t o_t = tmem + kColO + 128 * ob;
+                    const uint32_t s_a = smem_u32(Sbuf);
+                    auto mma3 = [&]() {  // O = Q S  (Q' = diag(e^b) Q in direct chunks)
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                            mma_ss(o_t, smem_desc_sw128(q_a + off, 16, 1024),
+                                   smem_desc_sw128(s_a + kk * 2048, kHalf, 1024), id_qs, kk > 0);
+                        }
+                    };
+                    if (!factor) {  // Q is rescaled in place together with P
+                        if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
+                    }
+                    // the cross term needs nothing else from the decay warps: it fills the P bubble
+                    if (!(ok = mbar_wait(&sm.s_ready, i & 1, abort_flag))) break;
+                    tc_fence_after();
+                    mma3();
+                    if (!(ok = mbar_wait(&sm.k_ready[s], (i / NS) & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait(&sm.full_v[s], (i / NS) & 1, abort_flag))) break;
+                    if (i > 0 && !(ok = mbar_wait(&sm.u_free, (i - 1) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < 8; ++kk)  // MMA4: U = K'^T V
+                        mma_ss(tmem + kColU, smem_desc_sw128(k_a + kk * 2048, kHalf, 1024),
+                               smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_kv, kk > 0);
+                    mma_commit(&sm.u_full);
+                    if (factor) {
+                        if (!(ok = mbar_wait(&sm.pq_ready[s], (i / NS) & 1, abort_flag))) break;
+                        tc_fence_after();
+                    }
+                    for (int kk = 0; kk < 8; ++kk)  // MMA2: O += P V
+                        mma_ts(o_t, tmem + kColA + kk * 8, smem_desc_sw128(v_a + kk * 2048, kHalf, 1024), id_pv, 1);
+                    mma_commit(&sm.o_full[ob]);
+                    mma_commit(&sm.p_free);
+                    mma_commit(&sm.empty[s]);
+                }
+                if (!ok) report(err, &sm.abort_flag, 2);
+                // drain: nothing of ours may still run when TMEM is released
+                mma_commit(&sm.drain);
+                mbar_wait(&sm.drain, 0, abort_flag, 200000000ull);
+            }
+        }
+    } else if (warp >= 12) {
+        // ----------------------------------------------------- epilogue warps
+        // Output rows o_j = e^{b_j} O_j (or O_j in direct chunks), staged as bf16 in
+        // the chunk's V slot (free once MMA2 is done); the TMA producer thread stores
+        // them.  With kGN, Eq. 7's output instead: z_j = swish(g_j) (.)
+        // (w (.) (o_j - mean_j) / sqrt(var_j + eps) + b), the moments over the head's
+        // 128 channels of the fp32 row; the gate row is requested before the wait for
+        // O, so it lands meanwhile.  Thread j = TMEM lane j = query row j.
+        const int j = tid - 384;
+        const int wq = warp - 12;
+        const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        if (kGN) {  // this head's affine, identity when absent
+            sm.gnw[j] = gn_w ? gn_w[(size_t)h * kD + j] : 1.f;
+            sm.gnb[j] = gn_b ? gn_b[(size_t)h * kD + j] : 0.f;
+            named_bar(3, 128);
+        }
+        float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), j) : 0.f;
+        for (int i = 0; i < nchunks; ++i) {
+            const int s = i % NS;
+            float bC;
+            const float bj = group_scan(lg_next, sm.wsum2, lane, wq, 3, bC);
+            if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), j);
+            const float sc = (bC > kFactorMin) ? __expf(bj) : 1.f;  // output row scale
+            uint4 g[kGN ? kD / 8 : 1];
+            if (kGN) {
+                const int n = chunk_start(i) + j;
+                const uint4 *src = reinterpret_cast<const uint4 *>(gate + (((size_t)b * N + n) * H + h) * kD);
+#pragma unroll
+                for (int c = 0; c < kD / 8; ++c) g[c] = (n < N) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (j == 0) {
+                const bool ok = mbar_wait(&sm.o_full[i & 1], (i / 2) & 1, abort_flag);
+                if (!ok) report(err, &sm.abort_flag, 6);
+                sm.go2 = ok && !*abort_flag;
+            }
+            named_bar(3, 128);
+            if (!sm.go2) break;
+            tc_fence_after();
+            uint8_t *stage_o = stage_v(s);
+            const uint32_t o_t = tmem + kColO + 128 * (i & 1) + lane_base;
+            if (!kGN) {
+                const uint64_t sc2 = f2_pack(sc, sc);
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(o_t + cb * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {  // two columns per packed multiply
+                            float y0, y1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[8 * q4 + 2 * e]),
+                                                     __uint_as_float(r[8 * q4 + 2 * e + 1])), sc2), y0, y1);
+                            w[e] = pack_bf16x2(y0, y1);
+                        }
+                        *reinterpret_cast<uint4 *>(stage_o + tile_chunk(j, cb * 4 + q4)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            } else {
+                // the row's mean, then its variance about the mean, then the output:
+                // three passes over O in tensor memory, nothing kept but two numbers
+                float sum = 0.f;
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(o_t + cb * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sum += __uint_as_float(r[e]);
+                }
+                const float mean = sc * sum * (1.f / kD);
+                float ss = 0.f;
+#pragma unroll 1
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(o_t + cb * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float dv = fmaf(sc, __uint_as_float(r[e]), -mean);
+                        ss = fmaf(dv, dv, ss);
+                    }
+                }
+                const float rstd = rsqrtf(ss * (1.f / kD) + gn_eps);
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    uint32_t r[32];
+                    tmem_ld32(o_t + cb * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const uint4 gq = g[cb * 4 + q4];  // gate columns cb*32 + 8 q4 .. + 7
+                        const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c0 = cb * 32 + 8 * q4 + 2 * e;
+                            const float x0 = fmaf(fmaf(sc, __uint_as_float(r[8 * q4 + 2 * e]), -mean) * rstd,
+                                                  sm.gnw[c0], sm.gnb[c0]);
+                            const float x1 = fmaf(fmaf(sc, __uint_as_float(r[8 * q4 + 2 * e + 1]), -mean) * rstd,
+                                                  sm.gnw[c0 + 1], sm.gnb[c0 + 1]);
+                            const float g0 = __uint_as_float(gw[e] << 16), g1 = __uint_as_float(gw[e] & 0xFFFF0000u);
+                            w[e] = pack_bf16x2(x0 * __fdividef(g0, 1.f + __expf(-g0)),
+                                               x1 * __fdividef(g1, 1.f + __expf(-g1)));
+                        }
+                        *reinterpret_cast<uint4 *>(stage_o + tile_chunk(j, cb * 4 + q4)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            named_bar(3, 128);
+            if (j == 0) {
+                mbar_arrive(&sm.o_free[i & 1]);
+                mbar_arrive(&sm.o_staged[s]);  // the TMA producer stores the rows
+            }
         }
     } else if (warp >= 4) {
-        // ------------------ decay, P, in-place scaling of K (Q) and the output rows
+        regs_dec<kRegsDecay>();
+        // ------------------------------ decay, P, in-place scaling of K (and Q)
         const int j = tid - 128;  // token row of the chunk = TMEM lane
         const int wq = warp - 4;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
@@ -491,6 +631,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (j == 0) mbar_arrive(&sm.pq_ready[s]);
         }
     } else {
+        regs_inc<kRegsState>();
         // ------------------------------------------------------- state warps
         const int t = tid;  // TMEM lane: d_k row t of S and U
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -547,13 +688,10 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), t) : 0.f;
         for (int i = 0; i < nchunks; ++i) {
-            const int s = i % NS;
             // the chunk's decay, computed here too (cheap) so no ring is shared with the decay warps
             float bC;
-            const float bt = group_scan(lg_next, sm.wsum0, lane, warp, 2, bC);
+            (void)group_scan(lg_next, sm.wsum0, lane, warp, 2, bC);
             if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), t);
-            const float sc = (bC > kFactorMin) ? __expf(bt) : 1.f;  // output row scale
-            const uint64_t sc2 = f2_pack(sc, sc);
             bool ok = true;
             if (t == 0) {
                 ok = mbar_wait(&sm.u_full, i & 1, abort_flag);
@@ -583,46 +721,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mbar_arrive(&sm.u_free);
                 if (i + 1 < nchunks) mbar_arrive(&sm.s_ready);
             }
-            // output rows o_t = e^{b_t} O_t (or O_t), staged as bf16 in this chunk's
-            // V slot (free once MMA2 is done); the TMA producer thread stores them
-            if (t == 0) {
-                ok = mbar_wait(&sm.o_full[i & 1], (i / 2) & 1, abort_flag);
-                if (!ok) report(err, &sm.abort_flag, 6);
-                sm.go0 = ok && !*abort_flag;
-            }
-            named_bar(2, 128);
-            if (!sm.go0) break;
-            tc_fence_after();
-            {
-                uint8_t *stage_o = stage_v(s);
-                const uint32_t o_t = tmem + kColO + 128 * (i & 1) + lane_base;
-#pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(o_t + cb * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {  // two columns per packed multiply
-                            float y0, y1;
-                            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[8 * q4 + 2 * e]),
-                                                     __uint_as_float(r[8 * q4 + 2 * e + 1])), sc2), y0, y1);
-                            w[e] = pack_bf16x2(y0, y1);
-                        }
-                        *reinterpret_cast<uint4 *>(stage_o + tile_chunk(t, cb * 4 + q4)) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                }
-                tc_fence_before();
-                fence_proxy_async_smem();
-                named_bar(2, 128);
-                if (t == 0) {
-                    mbar_arrive(&sm.o_free[i & 1]);
-                    mbar_arrive(&sm.o_staged[s]);  // the TMA producer stores the rows
-                }
-            }
         }
         named_bar(2, 128);
         if (t == 0) sm.go0 = !*abort_flag;
@@ -650,7 +748,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
         }
     }
-
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -992,7 +1089,9 @@ size_t gret_tc_workspace(int B, int N, int H, int dk, int dv) {
     return ws;
 }
 
-cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
+// The chunkwise prefill on the tensor cores.  gn == nullptr: o = the retention
+// output; else o = Eq. 7's z = swish(gate) (.) GroupNorm_h(retention output).
+cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaStream_t st) {
     CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, a.q, a.B, a.N, a.H) || !make_map(&mk, a.k, a.B, a.N, a.H) || !make_map(&mv, a.v, a.B, a.N, a.H) ||
         !make_map(&mo, a.o, a.B, a.N, a.H))
@@ -1005,15 +1104,20 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     float *G = E + (size_t)a.B * a.H * (P + 1) * kD * kD;
     int *hand = reinterpret_cast<int *>(G + (size_t)a.B * a.H * P);
     const float inv_tau = 1.0f / a.tau;
+    auto out_kernel = gn ? gret_tc_kernel<true> : gret_tc_kernel<false>;
+    const bf16_t *gate = gn ? (const bf16_t *)gn->gate : nullptr;
+    const float *gn_w = gn ? gn->w : nullptr, *gn_b = gn ? gn->b : nullptr;
+    const float gn_eps = gn ? gn->eps : 0.f;
     cudaError_t e;
-    e = cudaFuncSetAttribute(gret_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
+    e = cudaFuncSetAttribute(out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(gret_seg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSegSmemBytes);
     if (e != cudaSuccess) return e;
     if (P == 1) {
         count_launches(1);
-        gret_tc_kernel<<<dim3(a.B * a.H), kTcThreads, kTcSmemBytes, st>>>(
-            mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err, (uint64_t)0);
+        out_kernel<<<dim3(a.B * a.H), kTcThreads, kTcSmemBytes, st>>>(
+            mq, mk, mv, mo, a.logits, inv_tau, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err, (uint64_t)0, gate,
+            gn_w, gn_b, gn_eps);
         return cudaGetLastError();
     }
     // end states of segments 0 .. P-2 (the last segment's is computed by the OUTPUT pass)
@@ -1022,26 +1126,26 @@ cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = kTcSmemBytes;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // segment states: the prologue overlaps the previous kernel's tail; it waits for it
     // before reading anything
     cfg.gridDim = dim3(P - 1, a.H, a.B);
+    cfg.blockDim = dim3(kSegThreads);
     cfg.dynamicSmemBytes = kSegSmemBytes;
     e = cudaLaunchKernelEx(&cfg, gret_seg_kernel, mk, mv, a.logits, inv_tau, (const float *)a.state, E, G, hand,
                            a.N, a.H, seg_len, P, err);
     if (e != cudaSuccess) return e;
-    cfg.dynamicSmemBytes = kTcSmemBytes;
     // the output grid starts on the SMs the segment-state grid leaves free: its segment-0 CTAs (first in
     // the grid) run the whole segment meanwhile; the others begin loading and wait
     // for the segment states before touching E, G and `state`
     cfg.gridDim = dim3(P * a.B * a.H);
-    return cudaLaunchKernelEx(&cfg, gret_tc_kernel, mq, mk, mv, mo, a.logits, inv_tau, (bf16_t *)a.o,
-                              a.state, E, G, hand, a.N, a.H, seg_len, P, err,
-                              (uint64_t)test_hook_value(kHookGretSeg0DelayNs));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kTcSmemBytes;
+    return cudaLaunchKernelEx(&cfg, out_kernel, mq, mk, mv, mo, a.logits, inv_tau, a.state, E, G, hand, a.N, a.H,
+                              seg_len, P, err, (uint64_t)test_hook_value(kHookGretSeg0DelayNs), gate, gn_w, gn_b,
+                              gn_eps);
 }
 
 }  // namespace yoco_host

@@ -47,9 +47,14 @@ cudaError_t gret_decode_gn(const void *q, const void *k, const void *v, const fl
                            int B, int H, int dk, int dv, yoco_dtype dt, cudaStream_t st);
 
 // gret_tc.cu (bf16, d = 128, tensor cores)
+struct GnArgs {  // Eq. 7 output: z = swish(gate) (.) GroupNorm_h(o)
+    const void *gate;
+    const float *w, *b;  // per-channel affine [H * d] or NULL
+    float eps;
+};
 bool gret_tc_eligible(int B, int N, int H, int dk, int dv, yoco_dtype dt);
 size_t gret_tc_workspace(int B, int N, int H, int dk, int dv);
-cudaError_t gret_prefill_tc(const GretArgs &a, void *ws, cudaStream_t st);
+cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaStream_t st);
 
 // kv_proj.cu
 struct KvProjArgs {

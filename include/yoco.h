@@ -275,6 +275,29 @@ YOCO_API yoco_status yoco_gret_decode_step_gn_gate(const void *q, const void *k,
                                                    float eps, void *z, int B, int H, int dk, int dv, yoco_dtype dt,
                                                    void *stream);
 
+/*
+ * Chunkwise gated-retention prefill with the paper's Eq. 7 output for every
+ * token, fused (Section 3.1 Eq. 7; Appendix F ChunkwiseRetention applies the
+ * group norm to the chunk output):
+ *     z = swish(gate) (.) GroupNorm_h(o),   o = yoco_gret_prefill_chunkwise's output
+ * GroupNorm as in yoco_gret_group_norm_gate: one group per head, biased
+ * variance over the head's d channels, eps > 0, gn_weight / gn_bias fp32
+ * [H * d] or NULL (1 / 0).  With bf16 and d = 128 (the tensor-core kernel) o is
+ * never rounded or stored: each output row is normalised (moments of its fp32
+ * values) and gated as it leaves tensor memory.  Otherwise the CUDA-core kernel
+ * writes o into z and Eq. 7 is applied to z in place (two launches).
+ *   q, k, v, gate, z [B, N, H, d] of dtype dt (gate = X W_G, the caller's);
+ *   gate_logits [B, N, H] fp32; state as in yoco_gret_prefill_chunkwise.
+ *   workspace: yoco_gret_prefill_workspace_size(B, N, H, d, d, 0, dt) bytes.
+ * Supported: dk = dv in {64, 128}.
+ */
+YOCO_API yoco_status yoco_gret_prefill_chunkwise_gn_gate(const void *q, const void *k, const void *v,
+                                                         const float *gate_logits, float tau, const void *gate,
+                                                         const float *gn_weight, const float *gn_bias, float eps,
+                                                         void *z, float *state, int B, int N, int H, int dk, int dv,
+                                                         yoco_dtype dt, void *workspace, size_t ws_bytes,
+                                                         void *stream);
+
 /* ------------------------- gated-retention input projections in one GEMM */
 
 /*

@@ -88,6 +88,40 @@ def test_gret_layer_32k_x24_whole_heads(Y):
     _gret_layer(Y, 2, 1, 32768, 24, 128, heads=(0, 13, 23))
 
 
+def test_gret_gn_gate_fused_32k_x24_heads(Y):
+    """The 32K-token, 24 x 128 gRet layer with Eq. 7's output fused (GroupNorm per
+    head and the swish gate as rows leave the kernel): three whole heads of z,
+    chunk by chunk, against the oracle's recurrent form followed by its
+    group_norm_gate, and their final states."""
+    import torch
+    B, N, H, D, cfg = 1, 32768, 24, 128, 2
+    q = dev_normal((B, N, H, D), torch.bfloat16, SID(cfg, 0, synth.T_Q), std=D ** -0.5)
+    k = dev_normal((B, N, H, D), torch.bfloat16, SID(cfg, 0, synth.T_K), std=D ** -0.5)
+    v = dev_normal((B, N, H, D), torch.bfloat16, SID(cfg, 0, synth.T_V))
+    lg = dev_normal((B, N, H), torch.float32, SID(cfg, 0, synth.T_LOGIT), mean=2.0)
+    g = dev_normal((B, N, H, D), torch.bfloat16, SID(cfg, 0, synth.T_QX))
+    z = torch.empty_like(v)
+    S = torch.zeros(B, H, D, D, device="cuda")
+    ws = torch.empty(max(256, Y.yoco_gret_prefill_workspace_size(B, N, H, D, D, 0, Y.YOCO_BF16)),
+                     dtype=torch.uint8, device="cuda")
+    Y.yoco_gret_prefill_chunkwise_gn_gate(q, k, v, lg, 16.0, g, z, S, eps=1e-5, workspace=ws)
+    Y.yoco_workspace_status(ws)
+    for h in (0, 13, 23):
+        hq = host_head(SID(cfg, 0, synth.T_Q), B, N, H, D, 0, h, 0, N, std=D ** -0.5)
+        hk = host_head(SID(cfg, 0, synth.T_K), B, N, H, D, 0, h, 0, N, std=D ** -0.5)
+        hv = host_head(SID(cfg, 0, synth.T_V), B, N, H, D, 0, h, 0, N)
+        hl = host_logits(SID(cfg, 0, synth.T_LOGIT), B, N, H, 0, h, 0, N, 2.0)
+        hg = host_head(SID(cfg, 0, synth.T_QX), B, N, H, D, 0, h, 0, N)
+        o_ref, S_ref = oracle.gret_recurrent(hq[None, :, None], hk[None, :, None], hv[None, :, None],
+                                             hl[None, :, None], 16.0)
+        z_ref = oracle.group_norm_gate(o_ref, hg[None, :, None], 1e-5)[0, :, 0]
+        z_gpu = host_f64(z[0, :, h])
+        assert rel_l2(z_gpu, z_ref) <= BF16_REL_L2, (h, rel_l2(z_gpu, z_ref))
+        worst = worst_block_rel_l2(z_gpu, z_ref, 128)
+        assert worst <= BLOCK_REL_L2, (h, worst)
+        assert rel_l2(S[0, h].cpu().numpy(), S_ref[0, 0]) <= BF16_REL_L2
+
+
 def test_gret_layer_512k_x24_whole_head(Y):
     """One gRet layer of the 512K-token prefill (six segments of 87424 tokens):
     all 524288 outputs of head 7, chunk by chunk, and its final state."""

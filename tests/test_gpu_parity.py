@@ -815,6 +815,55 @@ def test_group_norm_gate(Y, dtype, d, affine, inplace):
         assert rel_l2(host_f64(z), z_ref) <= BF16_REL_L2
 
 
+@pytest.mark.parametrize("B,N,H,d,dtype,affine,with_state", [
+    (1, 8192 + 77, 24, 128, "bf16", True, True),    # tensor cores, 6 segments per head
+    (2, 300, 8, 128, "bf16", False, False),          # tensor cores, 3 one-chunk segments
+    (3, 200, 80, 128, "bf16", True, False),          # tensor cores, one segment (B*H >= SMs)
+    (1, 1000, 3, 64, "f32", True, True),             # CUDA cores, then Eq. 7 in place
+])
+def test_gret_prefill_gn_gate_fused(Y, B, N, H, d, dtype, affine, with_state):
+    """The chunkwise prefill with Eq. 7's output fused (z = swish(gate) (.)
+    GroupNorm_h(o)) against the oracle's recurrent form followed by its
+    group_norm_gate, and the final state; the bf16 result also against the two
+    separate calls."""
+    import torch
+    host, dev = gret_inputs(46, B, N, H, d, dtype, logit_mean=2.0)
+    gh, gd = gen(SEED, sid(46, 1, synth.T_QX), (B, N, H, d), dtype)
+    w = b = wd = bd = None
+    if affine:
+        w = 1.0 + 0.25 * synth.normal(SEED, sid(46, 2, synth.T_QX), (H * d,), "f32").astype(np.float64)
+        b = 0.1 * synth.normal(SEED, sid(46, 3, synth.T_QX), (H * d,), "f32").astype(np.float64)
+        wd, bd = dev_f32(w), dev_f32(b)
+    S0 = None
+    if with_state:
+        S0 = synth.normal(SEED, sid(46, 4, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
+    qd, kd, vd, lgd = dev
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    z = torch.full((B, N, H, d), float("nan"), dtype=tdt, device="cuda")
+    S = torch.zeros(B, H, d, d, device="cuda") if S0 is None else dev_f32(S0)
+    Y.yoco_gret_prefill_chunkwise_gn_gate(qd, kd, vd, lgd, 16.0, gd, z, S, eps=1e-5, gn_weight=wd, gn_bias=bd)
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0, S0=S0)
+    z_ref = oracle.group_norm_gate(o_ref, gh, 1e-5, w, b)
+    zg = host_f64(z)
+    if dtype == "f32":
+        assert max_abs(zg, z_ref) <= FP32_MAX_ABS
+        assert max_abs(S.cpu().numpy(), S_ref) <= FP32_MAX_ABS
+        return
+    assert rel_l2(zg, z_ref) <= BF16_REL_L2
+    for h in (0, H - 1):
+        assert worst_block_rel_l2(zg[0, :, h], z_ref[0, :, h], 128) <= BLOCK_REL_L2, h
+    assert rel_l2(S.cpu().numpy(), S_ref) <= BF16_REL_L2
+    # the two separate calls (o rounded to bf16 between them) agree to bf16 rounding
+    o2 = torch.empty_like(vd)
+    S2 = torch.zeros(B, H, d, d, device="cuda") if S0 is None else dev_f32(S0)
+    Y.yoco_gret_prefill_chunkwise(qd, kd, vd, lgd, 16.0, o2, S2)
+    z2 = torch.empty_like(o2)
+    Y.yoco_gret_group_norm_gate(o2, gd, z2, eps=1e-5, gn_weight=wd, gn_bias=bd)
+    torch.cuda.synchronize()
+    assert rel_l2(zg, host_f64(z2)) <= BF16_REL_L2
+
+
 def test_group_norm_gate_decode_row(Y):
     """A decode step's output [B, H, d] goes through the same call (N = 1)."""
     import torch
