@@ -17,7 +17,9 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libyoco.so")
+# YOCO_LIB_PATH selects another build of the same library (the debug-checks build
+# in _build_debug/, for its tests); the default is the release build
+LIB_PATH = os.environ.get("YOCO_LIB_PATH") or os.path.join(_HERE, "_build", "libyoco.so")
 
 YOCO_OK, YOCO_ERR_INVALID_ARG, YOCO_ERR_UNSUPPORTED, YOCO_ERR_CAPACITY, YOCO_ERR_CUDA, YOCO_ERR_TIMEOUT, \
     YOCO_ERR_WORKSPACE = range(7)
@@ -79,6 +81,7 @@ def _load():
         "yoco_gret_prefill_chunkwise_gn_gate": (i, [vp, vp, vp, vp, f, vp, vp, vp, f, vp, vp, i, i, i, i, i, i, vp, sz,
                                                     vp]),
         "yoco_selftest_occupy_sms": (i, [i, ctypes.c_uint64, vp]),
+        "yoco_debug_checks": (i, [i, ctypes.POINTER(ctypes.c_uint32)]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -96,7 +99,7 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_swa_prefill", "yoco_swa_decode", "yoco_swa_workspace_size", "yoco_gret_group_norm_gate",
             "yoco_rope_apply", "yoco_gret_qkvg_project", "yoco_gret_qkvg_workspace_size",
             "yoco_gret_decode_step_gn_gate", "yoco_cross_attn_decode_noalloc_status", "yoco_test_hook",
-            "yoco_selftest_occupy_sms", "yoco_gret_prefill_chunkwise_gn_gate")
+            "yoco_selftest_occupy_sms", "yoco_gret_prefill_chunkwise_gn_gate", "yoco_debug_checks")
 YOCO_HOOK_FAIL_NEXT_CALLS, YOCO_HOOK_GRET_SEG0_DELAY_NS = 1, 2
 
 

@@ -160,6 +160,30 @@ yoco_status yoco_selftest_occupy_sms(int ctas, uint64_t ns, void *stream) {
 
 uint64_t yoco_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+yoco_status yoco_debug_checks(int clear, uint32_t *word) {
+    if (!word) return fail(YOCO_ERR_INVALID_ARG, "word is NULL");
+    *word = 0;
+#ifdef YOCO_DEBUG_CHECKS
+    cudaError_t e = cudaDeviceSynchronize();
+    unsigned w = 0;
+#define YOCO_READ_DEBUG_WORD(tu)                                   \
+    if (e == cudaSuccess) {                                        \
+        unsigned x = 0;                                            \
+        e = debug_word_##tu(&x, clear);                            \
+        if (!w) w = x;                                             \
+    }
+    YOCO_DEBUG_TUS(YOCO_READ_DEBUG_WORD)
+#undef YOCO_READ_DEBUG_WORD
+    if (e != cudaSuccess) return cuda_status(e, "debug_checks");
+    *word = w;
+    g_last_error[0] = 0;
+    return YOCO_OK;
+#else
+    (void)clear;
+    return fail(YOCO_ERR_UNSUPPORTED, "libyoco was built without YOCO_DEBUG_CHECKS");
+#endif
+}
+
 yoco_status yoco_test_hook(int hook, int64_t value) {
     if (hook == YOCO_HOOK_FAIL_NEXT_CALLS) {
         if (value < 0 || value > 1000000) return fail(YOCO_ERR_INVALID_ARG, "failure count must be in [0, 1e6]");

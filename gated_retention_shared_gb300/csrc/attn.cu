@@ -88,6 +88,7 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
 
     const int64_t k_lo = (int64_t)split * keys_per_split;
     const int64_t k_hi = min(k_lo + keys_per_split, p0 + (int64_t)t1);  // last row reads up to p0+t1-1
+    if (!YOCO_DCHECK(k_lo >= 0 && p0 + (int64_t)t1 <= cap && b < (int)(gridDim.z / Hkv), 0x52)) return;
     const T *Kb = Kc + ((size_t)b * Hkv + hk) * (size_t)cap * D;
     const T *Vb = Vc + ((size_t)b * Hkv + hk) * (size_t)cap * D;
 
@@ -246,6 +247,7 @@ attn_split_kernel(const T *__restrict__ Q, T *__restrict__ O, const T *__restric
         }
         const int t = t0 + i / G, h = hk * G + i % G;
         const size_t qrow = ((size_t)b * T_rows + t) * Hq + h;
+        if (!YOCO_DCHECK(t < T_rows && h < Hq && split < splits, 0x53)) continue;
         if (splits == 1) {
             O[qrow * D + c] = from_f32<T>(A / L);
         } else {
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(const float *__restrict
         }
         M = mb;
     }
-    O[(size_t)w * D + c] = from_f32<T>(A / L);
+    if (YOCO_DCHECK(w < (int)gridDim.x, 0x54)) O[(size_t)w * D + c] = from_f32<T>(A / L);
 }
 
 }  // namespace yoco
@@ -417,3 +419,5 @@ cudaError_t attn_run(const AttnArgs &a, int splits, void *ws, cudaStream_t st) {
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(attn)

@@ -498,3 +498,5 @@ cudaError_t swa_fa_launch(const void *q, const void *k, const void *v, void *o, 
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(attn_fa)

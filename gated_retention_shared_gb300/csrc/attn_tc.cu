@@ -88,6 +88,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const int64_t k_lo = (int64_t)split * keys_per_split;
     const int64_t k_hi = min(k_lo + keys_per_split, p0 + (int64_t)t1);
     const int ntiles = (k_hi > k_lo) ? (int)((k_hi - k_lo + kAK - 1) / kAK) : 0;
+    (void)YOCO_DCHECK(k_lo >= 0 && t1 <= T_rows && split < splits, 0x50);
 
     if (tid == 0) {
         for (int s = 0; s < kAStages; ++s) {
@@ -371,6 +372,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             const float L = sm.wsum[0][n] + sm.wsum[1][n] + sm.wsum[2][n] + sm.wsum[3][n];
             const int t = t0 + n / G, h = hk * G + n % G;
             const size_t qrow = ((size_t)b * T_rows + t) * Hq + h;
+            if (!YOCO_DCHECK(t < T_rows && h < Hq && b < (int)(gridDim.z / Hkv) && split < splits, 0x51)) continue;
             if (splits == 1) {
                 O[qrow * kAD + d] = from_f32<bf16_t>(acc[n] / L);
             } else {
@@ -480,3 +482,5 @@ cudaError_t attn_tc_launch(const AttnArgs &a, int RB, int nq, int64_t kps, int s
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(attn_tc)

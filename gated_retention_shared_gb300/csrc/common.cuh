@@ -37,7 +37,50 @@ __device__ __forceinline__ float log_gate(float logit, float inv_tau) {
     return fmaxf(ls * inv_tau, kLogGateMin);
 }
 
+// Debug builds (-DYOCO_DEBUG_CHECKS, see build.py): kernels check the global indices
+// they form from runtime values before they use them.  A failed check records
+// kErrMagic | site in this translation unit's debug word (yoco_debug_checks reads
+// every unit's word) and the access is skipped: never a trap.  Release builds
+// compile every check to `true`.  Sites:
+//   0x40 gRet output: a segment's fold reads an E slot    0x41 gRet output: parked-state slot
+//   0x42 gRet output: hand-off word                        0x43 gRet segment state: E slot
+//   0x44 gRet segment state: G slot                        0x48 append (strip GEMV): cache slot
+//   0x49 append (split-K GEMV): cache slot                 0x4A append (CUDA-core GEMM): cache slot
+//   0x4B append (tensor-core GEMM): cache slot             0x50 decode attention (tensor cores): key range
+//   0x51 decode attention (tensor cores): partial row      0x52 attention (CUDA cores): key range
+//   0x53 attention (CUDA cores): output / partial row      0x54 split merge: output row
+//   0x58 gRet recurrent step: state element                0x5C GroupNorm + gate: row
+//   0x5D rotary encoding: row                              0x5E sliding-window ring: slot
+#ifdef YOCO_DEBUG_CHECKS
+static __device__ unsigned g_yoco_dbg_word;
+__device__ __forceinline__ bool dcheck(bool ok, unsigned site) {
+    if (!ok) atomicCAS(&g_yoco_dbg_word, 0u, kErrMagic | site);
+    return ok;
+}
+#define YOCO_DCHECK(cond, site) (::yoco::dcheck((cond), (site)))
+#else
+#define YOCO_DCHECK(cond, site) (true)
+#endif
+
 }  // namespace yoco
+
+// Host accessor of a translation unit's debug word (debug builds only): every .cu
+// file with kernels names itself once with YOCO_DEBUG_TU(name).
+#ifdef YOCO_DEBUG_CHECKS
+#define YOCO_DEBUG_TU(tu)                                                                      \
+    namespace yoco_host {                                                                      \
+    cudaError_t debug_word_##tu(unsigned *w, int clear) {                                      \
+        cudaError_t e = cudaMemcpyFromSymbol(w, ::yoco::g_yoco_dbg_word, sizeof(unsigned));    \
+        if (e == cudaSuccess && clear) {                                                       \
+            const unsigned zero = 0;                                                           \
+            e = cudaMemcpyToSymbol(::yoco::g_yoco_dbg_word, &zero, sizeof(unsigned));          \
+        }                                                                                      \
+        return e;                                                                              \
+    }                                                                                          \
+    }
+#else
+#define YOCO_DEBUG_TU(tu)
+#endif
 
 // Host-side status plumbing shared by the API translation units.
 namespace yoco_host {

@@ -60,6 +60,7 @@ group_norm_gate_kernel(const T *o, const T *__restrict__ gate, const float *__re
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
     for (int64_t row = blockIdx.x * (int64_t)(blockDim.x / 32) + threadIdx.x / 32; row < rows; row += warps) {
+        if (!YOCO_DCHECK(row < rows, 0x5C)) break;
         const size_t base = (size_t)row * D + (size_t)lane * V;
         float x[V], g[V];
         load_v<T, V>(o + base, x);
@@ -119,3 +120,5 @@ cudaError_t group_norm_gate(const void *o, const void *gate, const float *w, con
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(gn_gate)

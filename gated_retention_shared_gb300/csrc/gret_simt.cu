@@ -242,6 +242,7 @@ gret_decode_step_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, co
     const int tid = threadIdx.x;
     const int cg = tid % 8;   // columns c0 + 4 cg .. +3
     const int rg = tid / 8;   // rows rg, rg + 32, ...
+    (void)YOCO_DCHECK(c0 + 32 <= dv && dk <= 128 && bh < (int)gridDim.y, 0x58);
     // launched as a programmatic dependent of the previous kernel on the stream: let
     // the next one start its launch, then wait for this one's inputs
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -312,6 +313,7 @@ gret_decode_step_gn_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const int rg = tid / 8;
     const uint32_t rank = tc::cluster_ctarank();
     const uint32_t nrank = (uint32_t)(dv / 32);
+    (void)YOCO_DCHECK(c0 + 32 <= dv && dk <= 128, 0x58);
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     float *Sb = state + (size_t)bh * dk * dv;
@@ -516,3 +518,5 @@ cudaError_t gret_decode(const void *q, const void *k, const void *v, const float
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(gret_simt)

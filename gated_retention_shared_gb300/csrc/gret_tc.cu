@@ -170,6 +170,11 @@ __device__ __forceinline__ void seg_initial_row(float (&S)[kD], const float *E, 
     }
     const bool with_init = (q0 == 0) && (dec + __ldcg(g_bh) >= -kDropLog);
     const size_t slot0 = bh * (size_t)(P + 1);
+    if (!YOCO_DCHECK(slot0 + P < (size_t)(gridDim.x / P) * (P + 1), 0x40)) {
+#pragma unroll
+        for (int c = 0; c < kD; ++c) S[c] = 0.f;
+        return;
+    }
     if (with_init) {
         const float4 *src = reinterpret_cast<const float4 *>(E + (slot0 + P - 1) * kD * kD + (size_t)t * kD);
 #pragma unroll
@@ -670,7 +675,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         put_state();
         named_bar(2, 128);
         if (t == 0) mbar_arrive(&sm.s_ready);
-        if (p == 0 && P > 1) {
+        if (p == 0 && P > 1 && YOCO_DCHECK(bh < (size_t)(gridDim.x / P), 0x42)) {
             // the caller's state is in registers now, so the last segment may overwrite
             // it; if that segment has already parked the final state, copy it over
             if (t == 0) {
@@ -731,7 +736,8 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // segment 0 to copy (if segment 0 takes its copy in between, write it here too)
             if (P > 1 && t == 0) sm.hand_old = ld_acquire_gpu(hand + bh);
             named_bar(2, 128);
-            const bool parked = P > 1 && !(sm.hand_old & kHandInitRead);
+            const bool parked = P > 1 && !(sm.hand_old & kHandInitRead) &&
+                                YOCO_DCHECK(bh * (P + 1) + P < (size_t)(gridDim.x / P) * (P + 1), 0x41);
             float *row = parked ? E + (bh * (P + 1) + P) * kD * kD : state + bh * kD * kD;
             for (int pass = 0; pass < 2; ++pass) {
                 float4 *dst = reinterpret_cast<float4 *>(row + (size_t)t * kD);
@@ -799,6 +805,8 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const size_t bh = (size_t)b * H + h;
     const size_t bhp = bh * P + p;                 // G slot
     const size_t e_slot = bh * (size_t)(P + 1) + p;  // E slot
+    const size_t nbh = (size_t)gridDim.y * gridDim.z;
+    const bool slots_ok = YOCO_DCHECK(e_slot < nbh * (P + 1) && p < P - 1, 0x43) && YOCO_DCHECK(bhp < nbh * P, 0x44);
     auto stage_k = [&](int s) { return tiles + (size_t)s * 2 * kTile; };
     auto stage_v = [&](int s) { return tiles + (size_t)s * 2 * kTile + kTile; };
     auto chunk_at = [&](int i) { return t_begin + (nch - 1 - i) * kC; };  // backwards
@@ -994,7 +1002,7 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             named_bar(1, kSegScale);
             if (tid == 0) mbar_arrive(&sm.scaled[s]);
         }
-        if (tid == 0) G[bhp] = suffix;
+        if (tid == 0 && slots_ok) G[bhp] = suffix;
         if (p == 0 && tid < kD) {  // keep the caller's initial state: the OUTPUT pass overwrites `state`
             const float4 *src = reinterpret_cast<const float4 *>(state + bh * kD * kD + (size_t)tid * kD);
             float4 *dst = reinterpret_cast<float4 *>(E + (bh * (P + 1) + P - 1) * kD * kD + (size_t)tid * kD);
@@ -1007,7 +1015,7 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             sm.go = ok && !*abort_flag;
         }
         named_bar(1, kSegScale);
-        if (sm.go && alive && tid < kD) {
+        if (sm.go && alive && slots_ok && tid < kD) {
             // E^T row tid (lane = d_v column tid) -> E[d_k][d_v]
             tc_fence_after();
             const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -1149,3 +1157,5 @@ cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaS
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(gret_tc)

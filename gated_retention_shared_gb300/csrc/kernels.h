@@ -119,6 +119,12 @@ cudaError_t rope_table(float2 *tab, int64_t pos0, int T, int d, float base, cuda
 cudaError_t qkvg_project(const void *X, const void *W, int B, int N, int dm, int H, int d, void *q, void *k, void *v,
                          float *logits, const float2 *rope_cs, int *err, cudaStream_t st);
 
+// debug builds: each kernel file's debug word (see YOCO_DEBUG_TU in common.cuh)
+#define YOCO_DEBUG_TUS(X) X(attn) X(attn_fa) X(attn_tc) X(gn_gate) X(gret_simt) X(gret_tc) X(kv_proj) \
+    X(kv_proj_tc) X(qkvg_tc) X(rope) X(swa)
+#define YOCO_DECLARE_DEBUG_WORD(tu) cudaError_t debug_word_##tu(unsigned *w, int clear);
+YOCO_DEBUG_TUS(YOCO_DECLARE_DEBUG_WORD)
+
 // selftest.cu
 cudaError_t selftest_wait(void *ws, uint64_t limit_ns, cudaStream_t st);
 cudaError_t selftest_occupy(int ctas, uint64_t ns, cudaStream_t st);

@@ -156,7 +156,8 @@ proj_append_simt(const T *__restrict__ M, const T *__restrict__ g, const T *__re
             if (col >= 2 * n) continue;
             int cn = col % n, h = cn / d, c = cn % d;
             T *dst = (col < n) ? kc : vc;
-            dst[(((size_t)b * Hkv + h) * cap + len + t) * d + c] = from_f32<T>(val[j]);
+            if (YOCO_DCHECK(len + t < cap && h < Hkv, 0x4A))
+                dst[(((size_t)b * Hkv + h) * cap + len + t) * d + c] = from_f32<T>(val[j]);
         }
     }
     finish_append(len_dev, len + T_rows);
@@ -368,6 +369,7 @@ proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__re
             for (int q0 = first ? kTailBatch : 0; q0 < nkc; q0 += kTailBatch) add_batch(q0);
             // the 8 columns lie in one head of Wk or of Wv (n % 8 == 0, d % 8 == 0)
             const int cn = c % n, h = cn / d, cc = cn % d;
+            if (!YOCO_DCHECK(len + t < cap && h < Hkv && cc + 8 <= d, 0x49)) continue;
             T *dst = ((c < n) ? kc : vc) + (((size_t)b * Hkv + h) * cap + len + t) * d + cc;
 #pragma unroll
             for (int e = 0; e < 8; ++e) sum[e] *= rms_r;
@@ -493,8 +495,10 @@ proj_gemv_strip(const bf16_t *__restrict__ M, const bf16_t *__restrict__ g, cons
                     rope_turn(x0, x1, cs, sn);
                 }
                 bf16_t *dst = ((c < n) ? kc : vc) + (((size_t)b * Hkv + h) * cap + len + t) * d + cc;
-                dst[0] = from_f32<bf16_t>(x0);
-                dst[1] = from_f32<bf16_t>(x1);
+                if (YOCO_DCHECK(len + t < cap && h < Hkv && c + 2 <= 2 * n, 0x48)) {
+                    dst[0] = from_f32<bf16_t>(x0);
+                    dst[1] = from_f32<bf16_t>(x1);
+                }
             }
         }
         __syncthreads();  // red and fin are rewritten by the next rows
@@ -621,3 +625,5 @@ cudaError_t kv_project_append(const KvProjArgs &a, void *ws, cudaStream_t st) {
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(kv_proj)

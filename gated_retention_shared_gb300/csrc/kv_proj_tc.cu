@@ -53,6 +53,7 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tm_m, const __grid_constant__
                 r[2 * e2 + 1] = __float_as_uint(x1);
             }
         }
+        if (!YOCO_DCHECK(len + t < cap && row < R && cg < 2 * n, 0x4B)) return;
         uint4 *p = reinterpret_cast<uint4 *>(dst + (((size_t)bb * Hkv + h) * cap + len + t) * d + c);
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4) {
@@ -144,3 +145,5 @@ cudaError_t kv_project_append_tc(const KvProjArgs &a, const float *rrow, const f
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(kv_proj_tc)

@@ -135,3 +135,5 @@ cudaError_t qkvg_project(const void *X, const void *W, int B, int N, int dm, int
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(qkvg_tc)

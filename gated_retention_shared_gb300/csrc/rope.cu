@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(256) rope_apply_kernel(T *x, int N, int H, int
     }
     const int rows = min(kRopeRows, N - n0);
     const int items = rows * H;
+    if (!YOCO_DCHECK(n0 < N && b < (int)gridDim.y, 0x5D)) return;
     T *xb = x + ((size_t)b * N + n0) * H * D + ch * EV;
     for (int it = threadIdx.x / CH; it < items; it += STEP) {
         const int j = it / H;  // row offset inside the block (item = j * H + h)
@@ -115,3 +116,5 @@ cudaError_t rope_table(float2 *tab, int64_t pos0, int T, int d, float base, cuda
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(rope)

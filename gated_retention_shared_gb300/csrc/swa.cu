@@ -28,6 +28,7 @@ __global__ void swa_ring_write_kernel(const uint8_t *__restrict__ k, const uint8
         const int which = (int)(r / n);  // 0: k, 1: v
         const int64_t tok = tok0 + i;
         const int64_t slot = (pos0 + i) % window;
+        if (!YOCO_DCHECK(tok < N && slot >= 0 && slot < window, 0x5E)) continue;
         const uint8_t *src = (which ? v : k) + (((size_t)b * N + tok) * Hkv + hk) * (size_t)row_bytes;
         uint8_t *dst = (which ? rv : rk) + (((size_t)b * Hkv + hk) * window + slot) * (size_t)row_bytes;
         reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(src)[c];
@@ -52,3 +53,5 @@ cudaError_t swa_ring_write(const void *k, const void *v, void *rk, void *rv, int
 }
 
 }  // namespace yoco_host
+
+YOCO_DEBUG_TU(swa)

@@ -434,6 +434,16 @@ YOCO_API uint64_t yoco_launch_count(void);
  *       final state goes through the hand-off's parked path.  Results are
  *       unchanged; only timing moves.
  */
+/*
+ * Index checks of a debug build.  Built with YOCO_DEBUG_CHECKS (build.py with
+ * debug=True writes _build_debug/libyoco.so), every kernel checks the global
+ * indices it forms from runtime values before using them; a failed check skips
+ * the access and records 0x59434F00 | site, never a trap.  This call waits for
+ * the device, stores the first recorded word (0: every check passed) in *word
+ * and with clear != 0 resets it.  A release build returns YOCO_ERR_UNSUPPORTED.
+ */
+YOCO_API yoco_status yoco_debug_checks(int clear, uint32_t *word);
+
 #define YOCO_HOOK_FAIL_NEXT_CALLS 1
 #define YOCO_HOOK_GRET_SEG0_DELAY_NS 2
 YOCO_API yoco_status yoco_test_hook(int hook, int64_t value);

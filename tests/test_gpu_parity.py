@@ -1168,7 +1168,7 @@ def test_bounded_wait_times_out_and_context_survives(Y):
 
 
 def test_calls_make_progress_with_most_sms_taken(Y):
-    """A self-test kernel holds all but 40 SMs (one CTA on each, most of its shared
+    """A self-test kernel holds all but 30 SMs (one CTA on each, most of its shared
     memory) for 300 ms on another stream.  Meanwhile a segmented gRet prefill
     (24 heads x 6 segments: 264 CTAs of its two kernels, one per SM, far more than
     the free SMs hold at once) and a split-KV decode run on this stream: both
@@ -1192,9 +1192,14 @@ def test_calls_make_progress_with_most_sms_taken(Y):
     Od = torch.empty_like(Qd)
     wsa = torch.zeros(max(256, Y.lib.yoco_cross_attn_workspace_size(1, 6, 1, ctypes.byref(cache.c), 0)),
                       dtype=torch.uint8, device="cuda")
+    # The same calls once beforehand: with CUDA's lazy module loading, the first launch
+    # of a kernel in a process waits for work already running on the device (here the
+    # occupying kernel), which is not what this test is about.
+    Y.yoco_gret_prefill_chunkwise(qd, kd, vd, lgd, 16.0, o, dev_f32(S0), workspace=ws)
+    Y.yoco_cross_attn_decode(Qd, cache, Od, workspace=wsa)
     torch.cuda.synchronize()
     other = torch.cuda.Stream()
-    assert Y.lib.yoco_selftest_occupy_sms(n_sm - 40, 300_000_000, ctypes.c_void_p(other.cuda_stream)) == Y.YOCO_OK
+    assert Y.lib.yoco_selftest_occupy_sms(n_sm - 30, 300_000_000, ctypes.c_void_p(other.cuda_stream)) == Y.YOCO_OK
     Y.yoco_gret_prefill_chunkwise(qd, kd, vd, lgd, 16.0, o, S, workspace=ws)
     Y.yoco_cross_attn_decode(Qd, cache, Od, workspace=wsa)
     done = torch.cuda.Event()
