@@ -100,6 +100,14 @@ __device__ __forceinline__ void report(int *err, int *abort_flag, int code) {
     if (err) atomicExch(err, (int)(kErrMagic | (uint32_t)code));
 }
 
+// tanh on the special-function unit (the PTX approximate instruction, max relative
+// error about 2^-11)
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
@@ -150,15 +158,18 @@ __device__ __forceinline__ float group_scan(float x, float *wsum, int lane, int 
     return x + pre;
 }
 
-// Initial state of segment p >= 1 of one (b, h), row t (into S):
+// Initial state of segment p >= 1 of one (b, h): columns [OFF, OFF + 64) of row t
+// (into S[OFF .. OFF + 63]):
 //     S_start(p) = sum_{q<p} e^{dec(q)} E_q + e^{dec(-1)} S_init,  dec(q) = sum_{q<r<p} G_r,
 // evaluated as the fold S <- e^{G_q} S + E_q in order of q, starting at the earliest
 // segment q0 whose decay up to segment p is still >= e^-kDropLog (from S_init when
 // even the caller's state is that close, else from zero).  E slots per (b, h):
-// 0 .. P-2 the segments' end states, P-1 a copy of the caller's state.  Every thread
-// of the calling group reads the same G values, so the loop bounds are uniform.
-__device__ __forceinline__ void seg_initial_row(float (&S)[kD], const float *E, const float *G, size_t bh, int P,
-                                                int p, int t) {
+// 0 .. P-2 the segments' end states, P-1 a copy of the caller's state.  The state
+// warps fold columns 0-63 and the decay warps 64-127 of the same rows; every thread
+// reads the same G values, so the loop bounds are uniform.
+template <int OFF>
+__device__ __forceinline__ void seg_initial_half(float (&S)[kD], const float *E, const float *G, size_t bh, int P,
+                                                 int p, int t) {
     const float *g_bh = G + bh * P;
     float dec = 0.f;  // dec(q0)
     int q0 = p - 1;
@@ -170,40 +181,28 @@ __device__ __forceinline__ void seg_initial_row(float (&S)[kD], const float *E, 
     }
     const bool with_init = (q0 == 0) && (dec + __ldcg(g_bh) >= -kDropLog);
     const size_t slot0 = bh * (size_t)(P + 1);
-    if (!YOCO_DCHECK(slot0 + P < (size_t)(gridDim.x / P) * (P + 1), 0x40)) {
 #pragma unroll
-        for (int c = 0; c < kD; ++c) S[c] = 0.f;
-        return;
-    }
-    if (with_init) {
-        const float4 *src = reinterpret_cast<const float4 *>(E + (slot0 + P - 1) * kD * kD + (size_t)t * kD);
+    for (int c = 0; c < 64; ++c) S[OFF + c] = 0.f;
+    if (!YOCO_DCHECK(slot0 + P < (size_t)(gridDim.x / P) * (P + 1), 0x40)) return;
+    auto fold = [&](size_t slot, float gq) {  // S <- gq S + E_slot, 32 columns per round of loads
+        const float4 *src = reinterpret_cast<const float4 *>(E + slot * kD * kD + (size_t)t * kD + OFF);
 #pragma unroll
-        for (int c4 = 0; c4 < kD / 4; ++c4) {
-            const float4 x = __ldcg(src + c4);
-            S[4 * c4] = x.x; S[4 * c4 + 1] = x.y; S[4 * c4 + 2] = x.z; S[4 * c4 + 3] = x.w;
-        }
-    } else {
+        for (int cb = 0; cb < 2; ++cb) {
+            float4 x[8];
 #pragma unroll
-        for (int c = 0; c < kD; ++c) S[c] = 0.f;
-    }
-    for (int q = q0; q < p; ++q) {
-        const float gq = __expf(__ldcg(g_bh + q));
-        const float4 *src = reinterpret_cast<const float4 *>(E + (slot0 + q) * kD * kD + (size_t)t * kD);
+            for (int u = 0; u < 8; ++u) x[u] = __ldcg(src + cb * 8 + u);
 #pragma unroll
-        for (int cb = 0; cb < 8; ++cb) {  // 16 columns at a time: 4 loads in flight
-            float4 x[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) x[u] = __ldcg(src + cb * 4 + u);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float *s4 = &S[cb * 16 + 4 * u];
+            for (int u = 0; u < 8; ++u) {
+                float *s4 = &S[OFF + cb * 32 + 4 * u];
                 s4[0] = fmaf(gq, s4[0], x[u].x);
                 s4[1] = fmaf(gq, s4[1], x[u].y);
                 s4[2] = fmaf(gq, s4[2], x[u].z);
                 s4[3] = fmaf(gq, s4[3], x[u].w);
             }
         }
-    }
+    };
+    if (with_init) fold(slot0 + P - 1, 0.f);
+    for (int q = q0; q < p; ++q) fold(slot0 + q, __expf(__ldcg(g_bh + q)));
 }
 
 template <int R>
@@ -444,12 +443,23 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const float bj = group_scan(lg_next, sm.wsum2, lane, wq, 3, bC);
             if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), j);
             const float sc = (bC > kFactorMin) ? __expf(bj) : 1.f;  // output row scale
-            uint4 g[kGN ? kD / 8 : 1];
+            // kGN: swish(g) = g sigmoid(g) of this row's gate, as bf16 pairs, worked out
+            // before O is ready (sigmoid(x) = (1 + tanh(x / 2)) / 2)
+            uint32_t sw[kGN ? kD / 2 : 1];
             if (kGN) {
                 const int n = chunk_start(i) + j;
                 const uint4 *src = reinterpret_cast<const uint4 *>(gate + (((size_t)b * N + n) * H + h) * kD);
 #pragma unroll
-                for (int c = 0; c < kD / 8; ++c) g[c] = (n < N) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                for (int c = 0; c < kD / 8; ++c) {
+                    const uint4 u = (n < N) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                    sw[4 * c] = u.x; sw[4 * c + 1] = u.y; sw[4 * c + 2] = u.z; sw[4 * c + 3] = u.w;
+                }
+#pragma unroll
+                for (int c2 = 0; c2 < kD / 2; ++c2) {
+                    const float h0 = 0.5f * __uint_as_float(sw[c2] << 16);
+                    const float h1 = 0.5f * __uint_as_float(sw[c2] & 0xFFFF0000u);
+                    sw[c2] = pack_bf16x2(fmaf(h0, tanh_approx(h0), h0), fmaf(h1, tanh_approx(h1), h1));
+                }
             }
             if (j == 0) {
                 const bool ok = mbar_wait(&sm.o_full[i & 1], (i / 2) & 1, abort_flag);
@@ -483,31 +493,40 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                 }
             } else {
-                // the row's mean, then its variance about the mean, then the output:
-                // three passes over O in tensor memory, nothing kept but two numbers
-                float sum = 0.f;
-#pragma unroll 1
-                for (int cb = 0; cb < 4; ++cb) {
-                    uint32_t r[32];
-                    tmem_ld32(o_t + cb * 32, r);
+                // moments of the fp32 row x = sc O about its first element (one pass
+                // over O in tensor memory, packed pairs), then the output pass:
+                //   z = swish(g) (w ((x - mean) / sqrt(var + eps)) + b)
+                //     = swish(g) (w (O a + c) + b),  a = sc / sqrt(var + eps), c = -mean / sqrt(var + eps)
+                float o0;
+                {
+                    uint32_t r0[1];
+                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n" : "=r"(r0[0]) : "r"(o_t));
                     tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) sum += __uint_as_float(r[e]);
+                    o0 = __uint_as_float(r0[0]);
                 }
-                const float mean = sc * sum * (1.f / kD);
-                float ss = 0.f;
+                const uint64_t shift2 = f2_pack(-o0, -o0), one2 = f2_pack(1.f, 1.f);
+                uint64_t sum2 = 0, sq2 = 0;  // (0.f, 0.f)
 #pragma unroll 1
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t r[32];
                     tmem_ld32(o_t + cb * 32, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const float dv = fmaf(sc, __uint_as_float(r[e]), -mean);
-                        ss = fmaf(dv, dv, ss);
+                    for (int e = 0; e < 32; e += 2) {
+                        const uint64_t dv = f2_add(f2_pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), shift2);
+                        sum2 = f2_fma(dv, one2, sum2);
+                        sq2 = f2_fma(dv, dv, sq2);
                     }
                 }
-                const float rstd = rsqrtf(ss * (1.f / kD) + gn_eps);
+                float s0, s1, q0, q1;
+                f2_unpack(sum2, s0, s1);
+                f2_unpack(sq2, q0, q1);
+                const float md = (s0 + s1) * (1.f / kD);                    // mean of O - o0
+                const float var = sc * sc * fmaxf((q0 + q1) * (1.f / kD) - md * md, 0.f);
+                const float rstd = rsqrtf(var + gn_eps);
+                const float a = sc * rstd, c = -(sc * (o0 + md)) * rstd;
+                const uint64_t a2 = f2_pack(a, a), c2 = f2_pack(c, c);
+                const bool affine = (gn_w != nullptr) || (gn_b != nullptr);
 #pragma unroll
                 for (int cb = 0; cb < 4; ++cb) {
                     uint32_t r[32];
@@ -515,19 +534,19 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tmem_wait_ld();
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
-                        const uint4 gq = g[cb * 4 + q4];  // gate columns cb*32 + 8 q4 .. + 7
-                        const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
                         uint32_t w[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int c0 = cb * 32 + 8 * q4 + 2 * e;
-                            const float x0 = fmaf(fmaf(sc, __uint_as_float(r[8 * q4 + 2 * e]), -mean) * rstd,
-                                                  sm.gnw[c0], sm.gnb[c0]);
-                            const float x1 = fmaf(fmaf(sc, __uint_as_float(r[8 * q4 + 2 * e + 1]), -mean) * rstd,
-                                                  sm.gnw[c0 + 1], sm.gnb[c0 + 1]);
-                            const float g0 = __uint_as_float(gw[e] << 16), g1 = __uint_as_float(gw[e] & 0xFFFF0000u);
-                            w[e] = pack_bf16x2(x0 * __fdividef(g0, 1.f + __expf(-g0)),
-                                               x1 * __fdividef(g1, 1.f + __expf(-g1)));
+                            const int col = cb * 32 + 8 * q4 + 2 * e;
+                            uint64_t y = f2_fma(f2_pack(__uint_as_float(r[8 * q4 + 2 * e]),
+                                                        __uint_as_float(r[8 * q4 + 2 * e + 1])), a2, c2);
+                            if (affine)
+                                y = f2_fma(y, f2_pack(sm.gnw[col], sm.gnw[col + 1]), f2_pack(sm.gnb[col], sm.gnb[col + 1]));
+                            const uint32_t s2 = sw[col / 2];
+                            float z0, z1;
+                            f2_unpack(f2_mul(y, f2_pack(__uint_as_float(s2 << 16), __uint_as_float(s2 & 0xFFFF0000u))),
+                                      z0, z1);
+                            w[e] = pack_bf16x2(z0, z1);
                         }
                         *reinterpret_cast<uint4 *>(stage_o + tile_chunk(j, cb * 4 + q4)) =
                             make_uint4(w[0], w[1], w[2], w[3]);
@@ -548,6 +567,16 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int j = tid - 128;  // token row of the chunk = TMEM lane
         const int wq = warp - 4;
         const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+        if (p > 0) {  // columns 64-127 of row j of this segment's initial state, for the state warps
+            float Sh[kD];
+            asm volatile("griddepcontrol.wait;\n" ::: "memory");
+            seg_initial_half<64>(Sh, E, G, bh, P, p, j);
+            float4 *hi = reinterpret_cast<float4 *>(Sbuf + (size_t)j * 256);
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4)
+                hi[c4] = make_float4(Sh[64 + 4 * c4], Sh[64 + 4 * c4 + 1], Sh[64 + 4 * c4 + 2], Sh[64 + 4 * c4 + 3]);
+            named_bar(4, 256);
+        }
         float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), j) : 0.f;
         bool alive = true;
         for (int i = 0; i < nchunks && alive; ++i) {
@@ -660,8 +689,18 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 S[4 * c4] = x.x; S[4 * c4 + 1] = x.y; S[4 * c4 + 2] = x.z; S[4 * c4 + 3] = x.w;
             }
         } else {
+            // columns 0-63 here, 64-127 from the decay warps through Sbuf (fp32, row t
+            // at byte 256 t), which MMA3 does not read before the first put_state
             asm volatile("griddepcontrol.wait;\n" ::: "memory");
-            seg_initial_row(S, E, G, bh, P, p, t);
+            seg_initial_half<0>(S, E, G, bh, P, p, t);
+            named_bar(4, 256);
+            const float4 *hi = reinterpret_cast<const float4 *>(Sbuf + (size_t)t * 256);
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4) {
+                const float4 x = hi[c4];
+                S[64 + 4 * c4] = x.x; S[64 + 4 * c4 + 1] = x.y; S[64 + 4 * c4 + 2] = x.z; S[64 + 4 * c4 + 3] = x.w;
+            }
+            named_bar(2, 128);  // every row read before put_state overwrites Sbuf
         }
         auto put_state = [&]() {  // bf16 row t of S into the N-major B tile
 #pragma unroll
@@ -770,11 +809,12 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // the eight scale warps rescale K in place (thread = one row-half) and announce it;
 // the MMA E^T += V^T (w . K) into TMEM (lane = d_v) then frees the slot.
 // The walk stops at the first chunk whose newest token weighs below e^-kDropLog
-// (found from the gate logits in a short prologue, 16 chunks per round), and
+// (found from the gate logits in a short prologue, 64 chunks per round), and
 // G_p is then the decay of the walked chunks, itself below e^-kDropLog.
 constexpr int kSegStages = 3;
 constexpr int kSegThreads = 320;              // warps 0-7 scale, 8 TMA, 9 MMA
 constexpr int kSegScale = 256;
+constexpr int kSegScanChunks = 64;            // chunks per round of the walk-length prologue
 
 struct SegSmem {
     uint64_t full[kSegStages], empty[kSegStages], scaled[kSegStages], e_full, decided;
@@ -783,7 +823,7 @@ struct SegSmem {
     int go;
     int nuse;         // chunks the walk takes (decided by the scale warps' prologue)
     float wsum[2][8];
-    float csum[16];   // prologue: total log decay of 16 chunks
+    float csum[64];   // prologue: total log decay of 64 chunks
 };
 
 constexpr size_t kSegSmemBytes = (size_t)kSegStages * 2 * kTile + sizeof(SegSmem) + 1024;
@@ -805,7 +845,7 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     const size_t bh = (size_t)b * H + h;
     const size_t bhp = bh * P + p;                 // G slot
     const size_t e_slot = bh * (size_t)(P + 1) + p;  // E slot
-    const size_t nbh = (size_t)gridDim.y * gridDim.z;
+    [[maybe_unused]] const size_t nbh = (size_t)gridDim.y * gridDim.z;
     const bool slots_ok = YOCO_DCHECK(e_slot < nbh * (P + 1) && p < P - 1, 0x43) && YOCO_DCHECK(bhp < nbh * P, 0x44);
     auto stage_k = [&](int s) { return tiles + (size_t)s * 2 * kTile; };
     auto stage_v = [&](int s) { return tiles + (size_t)s * 2 * kTile + kTile; };
@@ -908,38 +948,41 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             return (n < N) ? log_gate(logits[((size_t)b * N + n) * H + h], inv_tau) : 0.f;
         };
         // prologue: how many chunks, walking back from the segment end, to take.  Round
-        // by round, warp w sums the log decay of chunks c0 + 2w and c0 + 2w + 1 (eight
-        // logits in flight per lane); every thread then scans the 16 totals the same way
-        // and stops before the first chunk that starts below e^-kDropLog.
+        // by round, warp w sums the log decay of chunks c0 + 8w .. c0 + 8w + 7 (32
+        // logits in flight per lane); every thread then scans the 64 totals the same
+        // way and stops before the first chunk that starts below e^-kDropLog.
         int nuse = nch;
         {
             float run = 0.f;  // log decay of the chunks already taken
-            for (int c0 = 0; c0 < nch; c0 += 16) {
-                float part[2] = {0.f, 0.f};
+            for (int c0 = 0; c0 < nch; c0 += kSegScanChunks) {
+                float part[8];
 #pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int c = c0 + 2 * wr + 8 * hf + k2;  // warp (hf, wr) = warp 4 hf + wr
+                for (int k8 = 0; k8 < 8; ++k8) {
+                    part[k8] = 0.f;
+                    const int c = c0 + 8 * warp + k8;
                     if (c < nch) {
                         const int n0 = chunk_at(c);
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             const int n = n0 + lane + 32 * m;
-                            if (n < N) part[k2] += log_gate(__ldg(logits + ((size_t)b * N + n) * H + h), inv_tau);
+                            if (n < N) part[k8] += log_gate(__ldg(logits + ((size_t)b * N + n) * H + h), inv_tau);
                         }
                     }
                 }
 #pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
+                for (int k8 = 0; k8 < 8; ++k8) {
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) part[k2] += __shfl_xor_sync(0xffffffffu, part[k2], off);
+                    for (int off = 16; off > 0; off >>= 1) part[k8] += __shfl_xor_sync(0xffffffffu, part[k8], off);
                 }
-                if (lane == 0) {
-                    sm.csum[2 * wr + 8 * hf] = part[0];
-                    sm.csum[2 * wr + 8 * hf + 1] = part[1];
+                if (lane < 8) {
+                    float pv = part[0];
+#pragma unroll
+                    for (int k8 = 1; k8 < 8; ++k8) pv = (lane == k8) ? part[k8] : pv;
+                    sm.csum[8 * warp + lane] = pv;
                 }
                 named_bar(1, kSegScale);
                 bool stop = false;
-                for (int k2 = 0; k2 < 16 && c0 + k2 < nch; ++k2) {
+                for (int k2 = 0; k2 < kSegScanChunks && c0 + k2 < nch; ++k2) {
                     if (run < -kDropLog) {
                         nuse = c0 + k2;
                         stop = true;
