@@ -62,6 +62,8 @@ def parse():
                                       "gret_decode_gn"], default=None,
                    help="time one call kind on its own (for profiling)")
     p.add_argument("--n", type=int, default=0, help="--only gret: tokens (default 32768)")
+    p.add_argument("--segments", type=int, default=0,
+                   help="--only gret: segments per head (test hook; 0 = one CTA per SM over the heads)")
     p.add_argument("--no-decay", action="store_true",
                    help="--only gret: logits +inf (gamma = 1), the case where nothing is left out")
     p.add_argument("--cache-len", type=int, default=0,
@@ -627,6 +629,8 @@ def run_only(args):
     P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
     stp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     N = args.n or N_LAYER      # tokens of the call's shape (the single 32K-token gRet layer by default)
+    if args.segments:
+        assert L.yoco_test_hook(3, args.segments) == 0, L.yoco_last_error()
     CFG = CFG_LAYER if N == N_LAYER else 4
     if args.only in ("gret", "gret_gn", "gret_gn_unfused"):
         q = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_Q), std=D ** -0.5)
@@ -799,7 +803,7 @@ def run_only(args):
         # the fused call also reads the gate (bf16, the size of q)
         nbytes = (4 + (args.only == "gret_gn")) * B * N * H * D * 2 + B * N * H * 4 + 2 * B * H * D * D * 4
         line.update({"bytes_per_call": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
-                     "no_decay": bool(args.no_decay)})
+                     "no_decay": bool(args.no_decay), "segments": args.segments or "auto"})
     if args.only == "qkvg":
         flops = 2.0 * B * N * DM * (3 * H * D + H)
         line.update({"flops_per_call": flops, "achieved_tflops": round(flops / (ms / 1e3) / 1e12, 1)})

@@ -100,7 +100,7 @@ EXPORTED = ("yoco_gret_prefill_chunkwise", "yoco_gret_prefill_workspace_size", "
             "yoco_rope_apply", "yoco_gret_qkvg_project", "yoco_gret_qkvg_workspace_size",
             "yoco_gret_decode_step_gn_gate", "yoco_cross_attn_decode_noalloc_status", "yoco_test_hook",
             "yoco_selftest_occupy_sms", "yoco_gret_prefill_chunkwise_gn_gate", "yoco_debug_checks")
-YOCO_HOOK_FAIL_NEXT_CALLS, YOCO_HOOK_GRET_SEG0_DELAY_NS = 1, 2
+YOCO_HOOK_FAIL_NEXT_CALLS, YOCO_HOOK_GRET_SEG0_DELAY_NS, YOCO_HOOK_GRET_SEGMENTS = 1, 2, 3
 
 
 def _check(status: int, where: str):

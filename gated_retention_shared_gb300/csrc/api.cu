@@ -189,6 +189,8 @@ yoco_status yoco_test_hook(int hook, int64_t value) {
         if (value < 0 || value > 1000000) return fail(YOCO_ERR_INVALID_ARG, "failure count must be in [0, 1e6]");
     } else if (hook == YOCO_HOOK_GRET_SEG0_DELAY_NS) {
         if (value < 0 || value > 1000000000) return fail(YOCO_ERR_INVALID_ARG, "delay must be in [0, 1e9] ns");
+    } else if (hook == YOCO_HOOK_GRET_SEGMENTS) {
+        if (value < 0 || value > 4096) return fail(YOCO_ERR_INVALID_ARG, "segment count must be in [0, 4096]");
     } else {
         return fail(YOCO_ERR_INVALID_ARG, "unknown test hook %d", hook);
     }

@@ -17,7 +17,7 @@ int device_sm_count();
 
 // Test hooks (yoco_test_hook): process-wide values that tests set to reach paths
 // ordinary inputs cannot force; all are 0 (off) unless a test sets them.
-enum { kHookFailNextCalls = 1, kHookGretSeg0DelayNs = 2, kHookCount = 3 };
+enum { kHookFailNextCalls = 1, kHookGretSeg0DelayNs = 2, kHookGretSegments = 3, kHookCount = 4 };
 int64_t test_hook_value(int hook);
 // true (and the call must return YOCO_ERR_CUDA before launching anything) while an
 // injected launch failure is pending; consumes one

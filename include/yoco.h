@@ -433,6 +433,11 @@ YOCO_API uint64_t yoco_launch_count(void);
  *       `value` ns (<= 1e9) late, so the last segment finishes first and its
  *       final state goes through the hand-off's parked path.  Results are
  *       unchanged; only timing moves.
+ *   YOCO_HOOK_GRET_SEGMENTS  the tensor-core gRet prefill cuts each head into
+ *       `value` (<= 4096, at most one per chunk) segments instead of about one
+ *       CTA per SM; 0 restores the default.  Set it before querying the
+ *       workspace size.  Results are unchanged up to rounding; for measuring
+ *       the sequence-parallel split.
  */
 /*
  * Index checks of a debug build.  Built with YOCO_DEBUG_CHECKS (build.py with
@@ -446,6 +451,7 @@ YOCO_API yoco_status yoco_debug_checks(int clear, uint32_t *word);
 
 #define YOCO_HOOK_FAIL_NEXT_CALLS 1
 #define YOCO_HOOK_GRET_SEG0_DELAY_NS 2
+#define YOCO_HOOK_GRET_SEGMENTS 3
 YOCO_API yoco_status yoco_test_hook(int hook, int64_t value);
 
 #ifdef __cplusplus

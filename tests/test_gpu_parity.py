@@ -1214,3 +1214,22 @@ def test_calls_make_progress_with_most_sms_taken(Y):
     assert rel_l2(S.cpu().numpy().astype(np.float64), S_ref) <= BF16_REL_L2
     O_ref = oracle.cross_attn(Qh[:, None], Kh, Vh, 4999, d ** -0.5)[:, 0]
     assert rel_l2(host_f64(Od), O_ref) <= BF16_REL_L2
+
+
+@pytest.mark.parametrize("segments", [1, 3, 40])
+def test_gret_prefill_forced_segment_counts(Y, segments):
+    """The tensor-core prefill with its sequence split forced (test hook) to one
+    segment per head, three, or 40 (one per chunk here): the same result."""
+    import torch
+    B, N, H, d = 1, 128 * 40 - 5, 4, 128
+    host, dev = gret_inputs(47, B, N, H, d, "bf16", logit_mean=2.0)
+    S0 = synth.normal(SEED, sid(47, 1, synth.T_S0), (B, H, d, d), "f32", std=0.05).astype(np.float64)
+    assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_GRET_SEGMENTS, segments) == Y.YOCO_OK
+    try:
+        o, S = run_prefill(Y, dev, B, N, H, d, "bf16", S0=S0)
+    finally:
+        assert Y.lib.yoco_test_hook(Y.YOCO_HOOK_GRET_SEGMENTS, 0) == Y.YOCO_OK
+    o_ref, S_ref = oracle.gret_recurrent(*host, 16.0, S0=S0)
+    assert rel_l2(o, o_ref) <= BF16_REL_L2
+    assert worst_block_rel_l2(o[0, :, 0], o_ref[0, :, 0], 128) <= BLOCK_REL_L2
+    assert rel_l2(S, S_ref) <= BF16_REL_L2
