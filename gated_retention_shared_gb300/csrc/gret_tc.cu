@@ -220,7 +220,7 @@ template <bool kGN>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-               const __grid_constant__ CUtensorMap tm_g, const float *__restrict__ logits, float inv_tau,
+               const float *__restrict__ logits, float inv_tau,
                float *__restrict__ state, float *__restrict__ E, float *__restrict__ G,
                int *__restrict__ hand, int N, int H, int seg_len, int P, int *err, uint64_t seg0_delay_ns,
                const bf16_t *__restrict__ gate, const float *__restrict__ gn_w, const float *__restrict__ gn_b,
@@ -437,26 +437,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             named_bar(3, 128);
         }
         float lg_next = (nchunks > 0) ? chunk_log_gate(chunk_start(0), j) : 0.f;
-        uint32_t sw[kGN ? kD / 2 : 1];  // kGN: this row's gate (raw bf16 pairs), then swish(gate)
-        auto load_gate = [&](int i) {  // row j of chunk i's gate into sw (zeros past N)
-            const int n = chunk_start(i) + j;
-            const uint4 *src = reinterpret_cast<const uint4 *>(gate + (((size_t)b * N + n) * H + h) * kD);
-#pragma unroll
-            for (int c = 0; c < kD / 8; ++c) {
-                const uint4 u = (n < N) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                sw[4 * c] = u.x; sw[4 * c + 1] = u.y; sw[4 * c + 2] = u.z; sw[4 * c + 3] = u.w;
-            }
-        };
-        if (kGN && nchunks > 0) {
-            if (j == 0) {
-                tma_prefetch_desc(&tm_g);
-                if (nchunks > 1) {
-                    tma_prefetch_l2_4d(&tm_g, 0, h, chunk_start(1), b);
-                    tma_prefetch_l2_4d(&tm_g, 64, h, chunk_start(1), b);
-                }
-            }
-            load_gate(0);
-        }
         for (int i = 0; i < nchunks; ++i) {
             const int s = i % NS;
             float bC;
@@ -464,13 +444,15 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (i + 1 < nchunks) lg_next = chunk_log_gate(chunk_start(i + 1), j);
             const float sc = (bC > kFactorMin) ? __expf(bj) : 1.f;  // output row scale
             // kGN: swish(g) = g sigmoid(g) of this row's gate, as bf16 pairs, worked out
-            // before O is ready (sigmoid(x) = (1 + tanh(x / 2)) / 2).  The gate rows
-            // were requested at the end of the previous chunk (from L2: the tile is
-            // prefetched two chunks ahead)
+            // before O is ready (sigmoid(x) = (1 + tanh(x / 2)) / 2)
+            uint32_t sw[kGN ? kD / 2 : 1];
             if (kGN) {
-                if (j == 0 && i + 2 < nchunks) {
-                    tma_prefetch_l2_4d(&tm_g, 0, h, chunk_start(i + 2), b);
-                    tma_prefetch_l2_4d(&tm_g, 64, h, chunk_start(i + 2), b);
+                const int n = chunk_start(i) + j;
+                const uint4 *src = reinterpret_cast<const uint4 *>(gate + (((size_t)b * N + n) * H + h) * kD);
+#pragma unroll
+                for (int c = 0; c < kD / 8; ++c) {
+                    const uint4 u = (n < N) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                    sw[4 * c] = u.x; sw[4 * c + 1] = u.y; sw[4 * c + 2] = u.z; sw[4 * c + 3] = u.w;
                 }
 #pragma unroll
                 for (int c2 = 0; c2 < kD / 2; ++c2) {
@@ -578,7 +560,6 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mbar_arrive(&sm.o_free[i & 1]);
                 mbar_arrive(&sm.o_staged[s]);  // the TMA producer stores the rows
             }
-            if (kGN && i + 1 < nchunks) load_gate(i + 1);  // lands while the next O is computed
         }
     } else if (warp >= 4) {
         regs_dec<kRegsDecay>();
@@ -1175,8 +1156,6 @@ cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaS
     float *G = E + (size_t)a.B * a.H * (P + 1) * kD * kD;
     int *hand = reinterpret_cast<int *>(G + (size_t)a.B * a.H * P);
     const float inv_tau = 1.0f / a.tau;
-    CUtensorMap mg = mq;  // the gate's map (Eq. 7 output only; the call's q otherwise, unused)
-    if (gn && !make_map(&mg, gn->gate, a.B, a.N, a.H)) return cudaErrorInvalidValue;
     auto out_kernel = gn ? gret_tc_kernel<true> : gret_tc_kernel<false>;
     const bf16_t *gate = gn ? (const bf16_t *)gn->gate : nullptr;
     const float *gn_w = gn ? gn->w : nullptr, *gn_b = gn ? gn->b : nullptr;
@@ -1189,7 +1168,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaS
     if (P == 1) {
         count_launches(1);
         out_kernel<<<dim3(a.B * a.H), kTcThreads, kTcSmemBytes, st>>>(
-            mq, mk, mv, mo, mg, a.logits, inv_tau, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err, (uint64_t)0, gate,
+            mq, mk, mv, mo, a.logits, inv_tau, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err, (uint64_t)0, gate,
             gn_w, gn_b, gn_eps);
         return cudaGetLastError();
     }
@@ -1216,7 +1195,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaS
     cfg.gridDim = dim3(P * a.B * a.H);
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = kTcSmemBytes;
-    return cudaLaunchKernelEx(&cfg, out_kernel, mq, mk, mv, mo, mg, a.logits, inv_tau, a.state, E, G, hand, a.N, a.H,
+    return cudaLaunchKernelEx(&cfg, out_kernel, mq, mk, mv, mo, a.logits, inv_tau, a.state, E, G, hand, a.N, a.H,
                               seg_len, P, err, (uint64_t)test_hook_value(kHookGretSeg0DelayNs), gate, gn_w, gn_b,
                               gn_eps);
 }
