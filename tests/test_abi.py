@@ -287,3 +287,14 @@ def test_selftest_occupy_rejects_bad_arguments(Y):
     assert Y.lib.yoco_selftest_occupy_sms(0, 1000, None) == Y.YOCO_ERR_INVALID_ARG
     assert Y.lib.yoco_selftest_occupy_sms(10, 0, None) == Y.YOCO_ERR_INVALID_ARG
     assert Y.lib.yoco_selftest_occupy_sms(10, 2 * 10 ** 9, None) == Y.YOCO_ERR_INVALID_ARG
+
+
+def test_release_build_reports_no_debug_checks(Y):
+    """yoco_debug_checks answers without touching a device: a release build
+    has no index checks compiled in."""
+    if os.environ.get("YOCO_LIB_PATH"):
+        pytest.skip("this process runs another build")
+    w = ctypes.c_uint32(7)
+    assert Y.lib.yoco_debug_checks(0, ctypes.byref(w)) == Y.YOCO_ERR_UNSUPPORTED
+    assert w.value == 0
+    assert Y.lib.yoco_debug_checks(0, None) == Y.YOCO_ERR_INVALID_ARG
