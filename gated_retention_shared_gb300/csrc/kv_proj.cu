@@ -394,15 +394,18 @@ proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__re
 }
 
 // Few rows, bf16 (decode): column strips.  CTA = 16 output columns of [W_K | W_V]
-// over the whole of d_model, 512 threads: thread t holds rows t, t + 512, ... of the
-// strip (32 bytes = one sector of W each), so every W byte is read once, by one
-// CTA, in one round of loads issued before the wait on the previous kernel (the
-// weights are not written by it; the input rows M may be).  The products, and each
-// input row's sum of squares for the RMS factor, are reduced inside the CTA by warp
-// shuffles and one pass through shared memory: no partial sums leave the CTA and
-// no CTA waits for another.
+// over the whole of d_model, 512 threads.  Lanes 2r and 2r + 1 of a warp read the
+// two 16-byte halves of one W row's 32-byte strip (one sector), so a warp's load
+// takes 16 whole sectors and every W byte is read once, by one CTA, in one round
+// of loads issued before the wait on the previous kernel (the weights are not
+// written by it; the input rows M may be).  Thread t covers rows t / 2, t / 2 + 256,
+// ... and columns 8 (t % 2) .. + 7 of the strip.  The products, and each input row's
+// sum of squares for the RMS factor, are reduced inside the CTA by warp shuffles
+// and one pass through shared memory: no partial sums leave the CTA and no CTA
+// waits for another.
 constexpr int kStripThreads = 512;
 constexpr int kStripCols = 16;
+constexpr int kStripRowsPerPass = kStripThreads / 2;  // W rows one round of loads covers
 
 template <int KR, int RG>
 __global__ void __launch_bounds__(kStripThreads, 1)
@@ -413,38 +416,32 @@ proj_gemv_strip(const bf16_t *__restrict__ M, const bf16_t *__restrict__ g, cons
     __shared__ float red[kStripThreads / 32][RG][kStripCols + 1];  // per warp: 16 column sums, sum of squares
     __shared__ float fin[RG][kStripCols + 1];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int half = tid & 1;                              // columns 8 half .. 8 half + 7 of the strip
     const int c0 = blockIdx.x * kStripCols;               // first column of the strip in [0, 2n)
-    const bf16_t *W = (c0 < n) ? Wk + c0 : Wv + (c0 - n);  // n % 16 == 0: a strip lies in W_K or in W_V
-    uint4 wr[KR][2];
+    const bf16_t *W = ((c0 < n) ? Wk + c0 : Wv + (c0 - n)) + 8 * half;  // n % 16 == 0: the strip lies in one
+    uint4 wr[KR];
 #pragma unroll
     for (int i = 0; i < KR; ++i) {
-        const int k = tid + i * kStripThreads;
-        if (k < dm) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(W + (size_t)k * n);
-            wr[i][0] = __ldg(src);
-            wr[i][1] = __ldg(src + 1);
-        } else {
-            wr[i][0] = wr[i][1] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        const int k = (tid >> 1) + i * kStripRowsPerPass;
+        wr[i] = (k < dm) ? __ldg(reinterpret_cast<const uint4 *>(W + (size_t)k * n)) : make_uint4(0u, 0u, 0u, 0u);
     }
     asm volatile("griddepcontrol.wait;\n" ::: "memory");  // M (and the cache) after the previous kernel
     for (int r0 = 0; r0 < R; r0 += RG) {
-        float acc[RG][kStripCols], ss[RG];
+        float acc[RG][8], ss[RG];
 #pragma unroll
         for (int rr = 0; rr < RG; ++rr) {
             ss[rr] = 0.f;
 #pragma unroll
-            for (int e = 0; e < kStripCols; ++e) acc[rr][e] = 0.f;
+            for (int e = 0; e < 8; ++e) acc[rr][e] = 0.f;
         }
 #pragma unroll
         for (int i = 0; i < KR; ++i) {
-            const int k = tid + i * kStripThreads;
+            const int k = (tid >> 1) + i * kStripRowsPerPass;
             if (k >= dm) continue;
-            float w[kStripCols];
-            const uint32_t x[8] = {wr[i][0].x, wr[i][0].y, wr[i][0].z, wr[i][0].w,
-                                   wr[i][1].x, wr[i][1].y, wr[i][1].z, wr[i][1].w};
+            float w[8];
+            const uint32_t x[4] = {wr[i].x, wr[i].y, wr[i].z, wr[i].w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
+            for (int e = 0; e < 4; ++e) {
                 w[2 * e] = __uint_as_float(x[e] << 16);
                 w[2 * e + 1] = __uint_as_float(x[e] & 0xFFFF0000u);
             }
@@ -453,24 +450,25 @@ proj_gemv_strip(const bf16_t *__restrict__ M, const bf16_t *__restrict__ g, cons
             for (int rr = 0; rr < RG; ++rr) {
                 if (r0 + rr >= R) break;
                 const float m = to_f32(M[(size_t)(r0 + rr) * dm + k]);
-                ss[rr] = fmaf(m, m, ss[rr]);
+                if (half == 0) ss[rr] = fmaf(m, m, ss[rr]);  // each row's squares once
                 const float mg = m * gk;
 #pragma unroll
-                for (int e = 0; e < kStripCols; ++e) acc[rr][e] = fmaf(mg, w[e], acc[rr][e]);
+                for (int e = 0; e < 8; ++e) acc[rr][e] = fmaf(mg, w[e], acc[rr][e]);
             }
         }
+        // lanes of one half hold the same 8 columns: add over lanes 2 apart and more
 #pragma unroll
         for (int rr = 0; rr < RG; ++rr) {
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
+            for (int off = 16; off > 1; off >>= 1) {
 #pragma unroll
-                for (int e = 0; e < kStripCols; ++e) acc[rr][e] += __shfl_xor_sync(0xffffffffu, acc[rr][e], off);
+                for (int e = 0; e < 8; ++e) acc[rr][e] += __shfl_xor_sync(0xffffffffu, acc[rr][e], off);
                 ss[rr] += __shfl_xor_sync(0xffffffffu, ss[rr], off);
             }
-            if (lane == 0) {
+            if (lane < 2) {  // lane = half
 #pragma unroll
-                for (int e = 0; e < kStripCols; ++e) red[warp][rr][e] = acc[rr][e];
-                red[warp][rr][kStripCols] = ss[rr];
+                for (int e = 0; e < 8; ++e) red[warp][rr][8 * lane + e] = acc[rr][e];
+                if (lane == 0) red[warp][rr][kStripCols] = ss[rr];
             }
         }
         __syncthreads();
@@ -530,7 +528,7 @@ static int gemv_chunks(int n, int dm) {
 constexpr int kStripMaxRows = 4;
 
 static bool strip_eligible(int R, int n, int dm, yoco_dtype dt) {
-    return dt == YOCO_BF16 && R <= kStripMaxRows && n % kStripCols == 0 && dm % 8 == 0 && dm <= 6 * kStripThreads;
+    return dt == YOCO_BF16 && R <= kStripMaxRows && n % kStripCols == 0 && dm % 8 == 0 && dm <= 12 * kStripRowsPerPass;
 }
 
 // workspace: [0, 256) status word of the tensor-core kernel, one fp32 RMS factor
@@ -578,10 +576,10 @@ static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
     float *r = (float *)((char *)ws + 256);
     cudaError_t e;
     if (strip_eligible(R, n, a.dm, a.dt)) {
-        const int kr = (a.dm + kStripThreads - 1) / kStripThreads;  // W rows per thread
-        if (kr <= 2) return launch_strip<2>(a, R, n, st);
+        const int kr = (a.dm + kStripRowsPerPass - 1) / kStripRowsPerPass;  // W rows per thread
         if (kr <= 4) return launch_strip<4>(a, R, n, st);
-        return launch_strip<6>(a, R, n, st);
+        if (kr <= 8) return launch_strip<8>(a, R, n, st);
+        return launch_strip<12>(a, R, n, st);
     }
     if (gemv_eligible(R, n, a.dm) && !(std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a))) {
         const int kch = gemv_chunks(n, a.dm);
