@@ -59,7 +59,7 @@ def parse():
     p.add_argument("--chunk", type=int, default=0)
     p.add_argument("--only", choices=["gret", "gret_gn", "gret_gn_unfused", "proj", "append", "cross_decode", "cross_prefill", "swa_prefill",
                                       "swa_decode", "gn_gate", "rope", "qkvg", "gret_decode_unfused",
-                                      "gret_decode_gn"], default=None,
+                                      "gret_decode_gn", "gret_steps", "gret_steps_append"], default=None,
                    help="time one call kind on its own (for profiling)")
     p.add_argument("--n", type=int, default=0, help="--only gret: tokens (default 32768)")
     p.add_argument("--segments", type=int, default=0,
@@ -748,6 +748,54 @@ def run_only(args):
             def call():
                 return L.yoco_gret_decode_step_gn_gate(P(q1), P(k1), P(v1), P(lg1), TAU, P(S1), P(g1), None, None,
                                                        1e-5, P(z1), B, H, D, D, 1, stp)
+    elif args.only in ("gret_steps", "gret_steps_append"):
+        # a generated token's 13 recurrent gRet steps (one CUDA graph), alone or followed
+        # by the one-slot append of its K^/V^: the difference is what the append adds
+        # inside a token, where it starts while the steps finish (W is cold in L2 each
+        # call: a 200 MB buffer is written between calls, as the cross layers' cache
+        # reads would evict it)
+        q1 = [normal((B, H, D), bf, sid(CFG, l, synth.T_Q, 1), std=D ** -0.5) for l in range(L_SELF)]
+        k1 = [normal((B, H, D), bf, sid(CFG, l, synth.T_K, 1), std=D ** -0.5) for l in range(L_SELF)]
+        v1 = [normal((B, H, D), bf, sid(CFG, l, synth.T_V, 1)) for l in range(L_SELF)]
+        lg1 = [normal((B, H), f32, sid(CFG, l, synth.T_LOGIT, 1), mean=2.0) for l in range(L_SELF)]
+        S1 = [normal((B, H, D, D), f32, sid(CFG, l, synth.T_S0), std=0.05) for l in range(L_SELF)]
+        o1 = [torch.empty(B, H, D, dtype=bf, device=dev) for _ in range(L_SELF)]
+        M1 = normal((B, 1, DM), bf, sid(CFG, 0, synth.T_M, 1))
+        Wk = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WK), std=0.02)
+        Wv = normal((DM, HKV * D), bf, sid(CFG, 0, synth.T_WV), std=0.02)
+        cache = Y.KVCache(B, HKV, D, 16 + args.warmup + args.steps, device=dev)
+        wsa = torch.empty(max(256, L.yoco_shared_kv_workspace_size(B, 1, DM, ctypes.byref(cache.c))),
+                          dtype=torch.uint8, device=dev)
+        flush = torch.empty(200 << 20, dtype=torch.uint8, device=dev)
+        sp = torch.cuda.current_stream(dev)
+
+        def steps(st_):
+            for l in range(L_SELF):
+                assert L.yoco_gret_decode_step(P(q1[l]), P(k1[l]), P(v1[l]), P(lg1[l]), TAU, P(S1[l]), P(o1[l]), B, H,
+                                               D, D, 1, 1, st_) == 0
+        steps(stp)
+        torch.cuda.synchronize()
+        cap_s = torch.cuda.Stream(dev)
+        cap_s.wait_stream(sp)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap_s):
+            steps(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+        sp.wait_stream(cap_s)
+        torch.cuda.synchronize()
+        timed_ms = []
+
+        def call():
+            flush.fill_(1)  # evicts W from L2, untimed
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(sp)
+            graph.replay()
+            st_ = 0
+            if args.only == "gret_steps_append":
+                st_ = L.yoco_shared_kv_project_append(P(M1), None, EPS, P(Wk), P(Wv), 1, DM, ctypes.byref(cache.c),
+                                                      P(wsa), wsa.numel(), stp)
+            e1.record(sp)
+            timed_ms.append((e0, e1))
+            return st_
     elif args.only == "rope":  # rotary encoding of one gRet layer's q in place
         qr = normal((B, N, H, D), bf, sid(CFG, 0, synth.T_Q))
 
@@ -798,6 +846,8 @@ def run_only(args):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
+    if args.only in ("gret_steps", "gret_steps_append"):  # events around each call only (the flush is untimed)
+        ms = statistics.mean(a.elapsed_time(b) for a, b in timed_ms[args.warmup:])
     line = {"only": args.only, "ms_per_call": ms, "steps": args.steps, "N": N}
     if args.only in ("gret", "gret_gn"):
         # the fused call also reads the gate (bf16, the size of q)
