@@ -15,7 +15,6 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "rope.cuh"
-#include "tc.cuh"
 
 namespace yoco {
 
@@ -394,43 +393,37 @@ proj_gemv_splitk(const T *__restrict__ M, const T *__restrict__ g, const T *__re
     }
 }
 
-// Few rows, bf16 (decode): clusters split over d_model.  A cluster of 8 CTAs covers
-// 128 output columns of [W_K | W_V]; CTA rank r takes W rows [r dm/8, (r+1) dm/8).
-// 512 threads: 16 lanes read one row's 256 contiguous bytes, so a warp load takes
-// two rows' worth of whole 128-byte lines and DRAM is read in 256-byte pieces; W is
-// read once, in one round of loads issued before the wait on the previous kernel
-// (the weights are not written by it; the input rows M may be).  Each CTA reduces its
-// rows' products (shuffles, one pass through shared memory), then the cluster
-// reduce-scatters them through distributed shared memory: rank r adds columns
-// 16 r .. 16 r + 15 over the 8 ranks.  Every CTA forms the RMS factor of each input
-// row from the whole row itself (d_model values from L2), so nothing else is summed
-// across CTAs and no partial leaves the cluster.
-constexpr int kGemvCl = 8;                          // CTAs per cluster = d_model chunks
-constexpr int kGemvClCols = 128;                    // output columns per cluster
-constexpr int kGemvClThreads = 512;
-constexpr int kGemvClRowsPerPass = kGemvClThreads / 16;  // W rows one round of loads covers
+// Few rows, bf16 (decode): column strips.  CTA = 16 output columns of [W_K | W_V]
+// over the whole of d_model, 512 threads.  Lanes 2r and 2r + 1 of a warp read the
+// two 16-byte halves of one W row's 32-byte strip (one sector), so a warp's load
+// takes 16 whole sectors and every W byte is read once, by one CTA, in one round
+// of loads issued before the wait on the previous kernel (the weights are not
+// written by it; the input rows M may be).  Thread t covers rows t / 2, t / 2 + 256,
+// ... and columns 8 (t % 2) .. + 7 of the strip.  The products, and each input row's
+// sum of squares for the RMS factor, are reduced inside the CTA by warp shuffles
+// and one pass through shared memory: no partial sums leave the CTA and no CTA
+// waits for another.
+constexpr int kStripThreads = 512;
+constexpr int kStripCols = 16;
+constexpr int kStripRowsPerPass = kStripThreads / 2;  // W rows one round of loads covers
 
 template <int KR, int RG>
-__global__ void __launch_bounds__(kGemvClThreads, 1)
-proj_gemv_cluster(const bf16_t *__restrict__ M, const bf16_t *__restrict__ g, const bf16_t *__restrict__ Wk,
-                  const bf16_t *__restrict__ Wv, bf16_t *__restrict__ kc, bf16_t *__restrict__ vc, int R, int T_rows,
-                  int dm, int n, int Hkv, int d, int64_t cap, int64_t len, float eps, int32_t *len_dev,
-                  float rope_base, const RopeFreq rf) {
-    __shared__ float red[RG][kGemvClThreads / 32][kGemvClCols];  // per warp: the 128 column sums
-    __shared__ float ssw[RG][kGemvClThreads / 32];                 // per warp: sums of squares
-    __shared__ float slot[kGemvCl][RG][kGemvClCols / kGemvCl];     // this rank's columns, from every rank
+__global__ void __launch_bounds__(kStripThreads, 1)
+proj_gemv_strip(const bf16_t *__restrict__ M, const bf16_t *__restrict__ g, const bf16_t *__restrict__ Wk,
+                const bf16_t *__restrict__ Wv, bf16_t *__restrict__ kc, bf16_t *__restrict__ vc, int R, int T_rows,
+                int dm, int n, int Hkv, int d, int64_t cap, int64_t len, float eps, int32_t *len_dev,
+                float rope_base, const RopeFreq rf) {
+    __shared__ float red[kStripThreads / 32][RG][kStripCols + 1];  // per warp: 16 column sums, sum of squares
+    __shared__ float fin[RG][kStripCols + 1];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = tc::cluster_ctarank();
-    const int c0 = (blockIdx.x / kGemvCl) * kGemvClCols;  // first column of the cluster in [0, 2n)
-    const int kchunk = (dm + kGemvCl - 1) / kGemvCl;
-    const int k0 = (int)rank * kchunk, k1 = min(dm, k0 + kchunk);
-    const int seg = lane & 15;  // columns c0 + 8 seg .. + 7
-    const bf16_t *W = ((c0 < n) ? Wk + c0 : Wv + (c0 - n)) + 8 * seg;  // n % 128 == 0: one matrix
+    const int half = tid & 1;                              // columns 8 half .. 8 half + 7 of the strip
+    const int c0 = blockIdx.x * kStripCols;               // first column of the strip in [0, 2n)
+    const bf16_t *W = ((c0 < n) ? Wk + c0 : Wv + (c0 - n)) + 8 * half;  // n % 16 == 0: the strip lies in one
     uint4 wr[KR];
 #pragma unroll
     for (int i = 0; i < KR; ++i) {
-        const int k = k0 + (tid >> 4) + i * kGemvClRowsPerPass;
-        wr[i] = (k < k1) ? __ldg(reinterpret_cast<const uint4 *>(W + (size_t)k * n)) : make_uint4(0u, 0u, 0u, 0u);
+        const int k = (tid >> 1) + i * kStripRowsPerPass;
+        wr[i] = (k < dm) ? __ldg(reinterpret_cast<const uint4 *>(W + (size_t)k * n)) : make_uint4(0u, 0u, 0u, 0u);
     }
     asm volatile("griddepcontrol.wait;\n" ::: "memory");  // M (and the cache) after the previous kernel
     for (int r0 = 0; r0 < R; r0 += RG) {
@@ -443,8 +436,8 @@ proj_gemv_cluster(const bf16_t *__restrict__ M, const bf16_t *__restrict__ g, co
         }
 #pragma unroll
         for (int i = 0; i < KR; ++i) {
-            const int k = k0 + (tid >> 4) + i * kGemvClRowsPerPass;
-            if (k >= k1) continue;
+            const int k = (tid >> 1) + i * kStripRowsPerPass;
+            if (k >= dm) continue;
             float w[8];
             const uint32_t x[4] = {wr[i].x, wr[i].y, wr[i].z, wr[i].w};
 #pragma unroll
@@ -456,58 +449,44 @@ proj_gemv_cluster(const bf16_t *__restrict__ M, const bf16_t *__restrict__ g, co
 #pragma unroll
             for (int rr = 0; rr < RG; ++rr) {
                 if (r0 + rr >= R) break;
-                const float mg = to_f32(M[(size_t)(r0 + rr) * dm + k]) * gk;
+                const float m = to_f32(M[(size_t)(r0 + rr) * dm + k]);
+                if (half == 0) ss[rr] = fmaf(m, m, ss[rr]);  // each row's squares once
+                const float mg = m * gk;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[rr][e] = fmaf(mg, w[e], acc[rr][e]);
             }
         }
-#pragma unroll
-        for (int rr = 0; rr < RG; ++rr) {  // the whole input row's squares, for the RMS factor
-            if (r0 + rr >= R) break;
-            for (int kk = tid; kk < dm; kk += kGemvClThreads) {
-                const float m = to_f32(M[(size_t)(r0 + rr) * dm + kk]);
-                ss[rr] = fmaf(m, m, ss[rr]);
-            }
-        }
+        // lanes of one half hold the same 8 columns: add over lanes 2 apart and more
 #pragma unroll
         for (int rr = 0; rr < RG; ++rr) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[rr][e] += __shfl_xor_sync(0xffffffffu, acc[rr][e], 16);
+            for (int off = 16; off > 1; off >>= 1) {
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss[rr] += __shfl_xor_sync(0xffffffffu, ss[rr], off);
-            if (lane < 16) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) red[rr][warp][8 * seg + e] = acc[rr][e];
+                for (int e = 0; e < 8; ++e) acc[rr][e] += __shfl_xor_sync(0xffffffffu, acc[rr][e], off);
+                ss[rr] += __shfl_xor_sync(0xffffffffu, ss[rr], off);
             }
-            if (lane == 0) ssw[rr][warp] = ss[rr];
+            if (lane < 2) {  // lane = half
+#pragma unroll
+                for (int e = 0; e < 8; ++e) red[warp][rr][8 * lane + e] = acc[rr][e];
+                if (lane == 0) red[warp][rr][kStripCols] = ss[rr];
+            }
         }
         __syncthreads();
-        if (tid < RG * kGemvClCols) {  // this CTA's sum for one (row, column), to the rank that owns it
-            const int rr = tid / kGemvClCols, c = tid % kGemvClCols;
+        if (tid < RG * (kStripCols + 1)) {  // (row, column or sum of squares): add the 16 warps in order
+            const int rr = tid / (kStripCols + 1), e = tid % (kStripCols + 1);
             float sum = 0.f;
 #pragma unroll
-            for (int w = 0; w < kGemvClThreads / 32; ++w) sum += red[rr][w][c];
-            const uint32_t owner = (uint32_t)(c / (kGemvClCols / kGemvCl));
-            tc::st_cluster_u32(tc::mapa_shared(&slot[rank][rr][c % (kGemvClCols / kGemvCl)], owner),
-                               __float_as_uint(sum));
+            for (int w = 0; w < kStripThreads / 32; ++w) sum += red[w][rr][e];
+            fin[rr][e] = sum;
         }
-        tc::cluster_sync();  // every rank's sums have landed
-        if (tid < RG * (kGemvClCols / kGemvCl / 2)) {  // one channel pair of one row: add, scale, rotate, store
-            const int rr = tid / (kGemvClCols / kGemvCl / 2), j = tid % (kGemvClCols / kGemvCl / 2), row = r0 + rr;
+        __syncthreads();
+        if (tid < RG * (kStripCols / 2)) {  // one channel pair of one row: scale, rotate (K^), round, store
+            const int rr = tid / (kStripCols / 2), j = tid % (kStripCols / 2), row = r0 + rr;
             if (row < R) {
-                float x0 = 0.f, x1 = 0.f, sq = 0.f;
-#pragma unroll
-                for (int q = 0; q < kGemvCl; ++q) {
-                    x0 += slot[q][rr][2 * j];
-                    x1 += slot[q][rr][2 * j + 1];
-                }
-#pragma unroll
-                for (int w = 0; w < kGemvClThreads / 32; ++w) sq += ssw[rr][w];
-                const float rms = rsqrtf(sq / (float)dm + eps);
-                x0 *= rms;
-                x1 *= rms;
                 const int b = row / T_rows, t = row % T_rows;
-                const int c = c0 + (int)rank * (kGemvClCols / kGemvCl) + 2 * j, cn = c % n, h = cn / d, cc = cn % d;
+                const float rms = rsqrtf(fin[rr][kStripCols] / (float)dm + eps);
+                float x0 = fin[rr][2 * j] * rms, x1 = fin[rr][2 * j + 1] * rms;
+                const int c = c0 + 2 * j, cn = c % n, h = cn / d, cc = cn % d;
                 if (rope_base > 0.f && c < n) {  // rotary encoding of K^ at slot position len + t
                     float cs, sn;
                     rope_cs_exact(len + t, rf.theta[cc / 2], cs, sn);
@@ -520,7 +499,7 @@ proj_gemv_cluster(const bf16_t *__restrict__ M, const bf16_t *__restrict__ g, co
                 }
             }
         }
-        tc::cluster_sync();  // slot, red and ssw are rewritten by the next rows
+        __syncthreads();  // red and fin are rewritten by the next rows
     }
     // No kernel reads the length on the device, and this grid releases no dependent
     // early, so whatever runs next on the stream sees every slot and the new length:
@@ -546,13 +525,10 @@ static int gemv_chunks(int n, int dm) {
     return (dm + kr - 1) / kr;
 }
 
-constexpr int kGemvClMaxRows = 4;
+constexpr int kStripMaxRows = 4;
 
-// bf16, at most 4 input rows (decode for up to 4 sequences), 128-column groups
-// (Hkv d a multiple of 128) and d_model <= 8 x 384 (twelve W rows per thread)
-static bool cluster_gemv_eligible(int R, int n, int dm, yoco_dtype dt) {
-    return dt == YOCO_BF16 && R <= kGemvClMaxRows && n % kGemvClCols == 0 && dm % 8 == 0 &&
-           dm <= kGemvCl * 12 * kGemvClRowsPerPass;
+static bool strip_eligible(int R, int n, int dm, yoco_dtype dt) {
+    return dt == YOCO_BF16 && R <= kStripMaxRows && n % kStripCols == 0 && dm % 8 == 0 && dm <= 12 * kStripRowsPerPass;
 }
 
 // workspace: [0, 256) status word of the tensor-core kernel, one fp32 RMS factor
@@ -565,34 +541,30 @@ size_t kv_proj_workspace(int B, int T, int dm, int Hkv, int d, yoco_dtype dt, fl
     size_t ws = 256 + ((rows * sizeof(float) + 255) / 256) * 256;
     const int n = Hkv * d;
     size_t extra = 0;
-    if (cluster_gemv_eligible((int)rows, n, dm, dt)) extra = 0;
+    if (strip_eligible((int)rows, n, dm, dt)) extra = 0;
     else if (gemv_eligible((int)rows, n, dm)) extra = (size_t)gemv_chunks(n, dm) * rows * 2 * n * sizeof(float);
     else if (rope_base > 0.f) extra = (size_t)T * (d / 2) * sizeof(float2);
     return ws + extra;
 }
 
 template <int KR>
-static cudaError_t launch_cluster_gemv(const KvProjArgs &a, int R, int n, cudaStream_t st) {
+static cudaError_t launch_strip(const KvProjArgs &a, int R, int n, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * n / kGemvClCols * kGemvCl);
-    cfg.blockDim = dim3(kGemvClThreads);
+    cfg.gridDim = dim3(2 * n / kStripCols);
+    cfg.blockDim = dim3(kStripThreads);
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = kGemvCl;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     count_launches(1);
     const RopeFreq rf = make_rope_freq(a.rope_base, a.d);
     if (R == 1)
-        return cudaLaunchKernelEx(&cfg, proj_gemv_cluster<KR, 1>, (const bf16_t *)a.M, (const bf16_t *)a.rms_w,
+        return cudaLaunchKernelEx(&cfg, proj_gemv_strip<KR, 1>, (const bf16_t *)a.M, (const bf16_t *)a.rms_w,
                                   (const bf16_t *)a.Wk, (const bf16_t *)a.Wv, (bf16_t *)a.kc, (bf16_t *)a.vc, R, a.T,
                                   a.dm, n, a.Hkv, a.d, a.cap, a.len, a.eps, a.len_dev, a.rope_base, rf);
-    return cudaLaunchKernelEx(&cfg, proj_gemv_cluster<KR, 2>, (const bf16_t *)a.M, (const bf16_t *)a.rms_w,
+    return cudaLaunchKernelEx(&cfg, proj_gemv_strip<KR, 2>, (const bf16_t *)a.M, (const bf16_t *)a.rms_w,
                               (const bf16_t *)a.Wk, (const bf16_t *)a.Wv, (bf16_t *)a.kc, (bf16_t *)a.vc, R, a.T, a.dm,
                               n, a.Hkv, a.d, a.cap, a.len, a.eps, a.len_dev, a.rope_base, rf);
 }
@@ -603,12 +575,11 @@ static cudaError_t run(const KvProjArgs &a, void *ws, cudaStream_t st) {
     const int n = a.Hkv * a.d;
     float *r = (float *)((char *)ws + 256);
     cudaError_t e;
-    if (cluster_gemv_eligible(R, n, a.dm, a.dt)) {
-        const int kchunk = (a.dm + kGemvCl - 1) / kGemvCl;
-        const int kr = (kchunk + kGemvClRowsPerPass - 1) / kGemvClRowsPerPass;  // W rows per thread
-        if (kr <= 4) return launch_cluster_gemv<4>(a, R, n, st);
-        if (kr <= 8) return launch_cluster_gemv<8>(a, R, n, st);
-        return launch_cluster_gemv<12>(a, R, n, st);
+    if (strip_eligible(R, n, a.dm, a.dt)) {
+        const int kr = (a.dm + kStripRowsPerPass - 1) / kStripRowsPerPass;  // W rows per thread
+        if (kr <= 4) return launch_strip<4>(a, R, n, st);
+        if (kr <= 8) return launch_strip<8>(a, R, n, st);
+        return launch_strip<12>(a, R, n, st);
     }
     if (gemv_eligible(R, n, a.dm) && !(std::is_same<T, bf16_t>::value && kv_proj_tc_eligible(a))) {
         const int kch = gemv_chunks(n, a.dm);

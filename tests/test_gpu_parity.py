@@ -408,9 +408,8 @@ def test_kv_append_bit_exact(Y):
                                                 (3, 1, 3072, 8, 128, False), (1, 3, 256, 1, 64, False),
                                                 (4, 1, 1000, 2, 128, True)])
 def test_kv_append_decode_rows_bit_exact(Y, B, T, dm, Hkv, d, gain):
-    """The few-row (decode) projection: at most four input rows, clusters of 8
-    CTAs splitting d_model over 128 columns of [W_K | W_V] (the split-K kernel
-    where Hkv d is not a multiple of 128).  +-1 rows, eps 0, dyadic
+    """The few-row (decode) projection: at most four input rows, each CTA one
+    16-column strip of [W_K | W_V] over all of d_model.  +-1 rows, eps 0, dyadic
     weights (and a gain of powers of two) make every sum exact, so the slots
     must equal the oracle's bit for bit, twice in a row, and nothing else in the
     cache may change."""
