@@ -61,7 +61,11 @@ constexpr size_t kFTileBytes = (size_t)2 * kFTile + (size_t)kFStages * 2 * kFTil
 constexpr size_t kFSmem = kFTileBytes + sizeof(FaSmem) + 1024;
 static_assert(kFSmem <= 232448, "flash-attention tiles must fit shared memory");
 
-__device__ __forceinline__ void fbar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
+// named barrier (aligned form: the warp is reconverged first, see gret_tc.cu)
+__device__ __forceinline__ void fbar(int id, int n) {
+    __syncwarp();
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
 
 __device__ __forceinline__ uint32_t fa_tile_chunk(int r, int c) {  // 16-B chunk c (0..15) of row r, SW128
     return (uint32_t)(c >> 3) * kFHalf + (uint32_t)r * 128u + (uint32_t)(((c & 7) ^ (r & 7)) * 16);

@@ -56,7 +56,11 @@ constexpr size_t kATileBytes = (size_t)kAStages * 2 * kATile + kAQBytes + 2 * kA
 constexpr size_t kASmem = kATileBytes + sizeof(AttnSmem) + 1024;
 static_assert(kASmem <= 232448, "attention tiles must fit shared memory");
 
-__device__ __forceinline__ void abar(int n) { asm volatile("bar.sync 1, %0;\n" ::"r"(n) : "memory"); }
+// named barrier 1 (aligned form: the warp is reconverged first, see gret_tc.cu)
+__device__ __forceinline__ void abar(int n) {
+    __syncwarp();
+    asm volatile("bar.sync 1, %0;\n" ::"r"(n) : "memory");
+}
 
 // Byte offset of element (row r, col c) in a K-major SW128 tile of `rows` rows
 // made of 64-column blocks.

@@ -93,7 +93,14 @@ constexpr size_t kTileBytes = (size_t)kStages * 3 * kTile + kTile;  // Q,K,V per
 constexpr size_t kTcSmemBytes = 232448;                            // the sm_100 per-block maximum
 static_assert(kTileBytes + sizeof(TcSmem) + 1024 <= kTcSmemBytes, "tiles + control block + alignment slack must fit");
 
-__device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
+// Named barrier of n threads.  bar.sync is the aligned form: all 32 lanes of a warp
+// must execute it together, and nothing else makes a warp reconverge after one lane
+// has waited alone (the `if (t == 0) { bounded wait }` pattern), so the warp is
+// synchronised first.
+__device__ __forceinline__ void named_bar(int id, int n) {
+    __syncwarp();
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
 
 __device__ __forceinline__ void report(int *err, int *abort_flag, int code) {
     *(volatile int *)abort_flag = 1;

@@ -176,6 +176,7 @@ __device__ __forceinline__ void run(const CUtensorMap *tm_x, WLoad wload, int R,
                 if (!ok) fail(code0 + 3);
                 sm.go = ok;
             }
+            __syncwarp();  // aligned barrier: reconverge the warp first
             asm volatile("bar.sync 1, 128;\n" ::: "memory");
             if (!sm.go) break;
             tc_fence_after();
@@ -192,6 +193,7 @@ __device__ __forceinline__ void run(const CUtensorMap *tm_x, WLoad wload, int R,
                 if (live) epi(r, row, c0);
             }
             tc_fence_before();
+            __syncwarp();  // aligned barrier: reconverge the warp first
             asm volatile("bar.sync 1, 128;\n" ::: "memory");
             if (rloc == 0) mbar_arrive_cluster(acc_empty0 + 8u * (uint32_t)a);
         }
