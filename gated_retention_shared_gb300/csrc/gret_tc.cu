@@ -46,7 +46,6 @@
 // and write the output rows (thread j = query row j), warp 8 issues TMA loads,
 // warp 9 issues the MMAs: per chunk MMA1, then (factored chunks) MMA3 while P is
 // being computed, then MMA4 so the state warps can start, then MMA2.
-#include <algorithm>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -230,7 +229,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                const float *__restrict__ logits, float inv_tau,
                float *__restrict__ state, float *__restrict__ E, float *__restrict__ G,
-               int *__restrict__ hand, int N, int H, int seg_len0, int seg_len, int P, int *err, uint64_t seg0_delay_ns,
+               int *__restrict__ hand, int N, int H, int seg_len, int P, int *err, uint64_t seg0_delay_ns,
                const bf16_t *__restrict__ gate, const float *__restrict__ gn_w, const float *__restrict__ gn_b,
                float gn_eps) {
     extern __shared__ uint8_t smem_raw[];
@@ -248,10 +247,8 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // segment-state grid, are dispatched first
     const int BH = (int)gridDim.x / P, r_bh = (int)blockIdx.x % BH;
     const int p = (int)blockIdx.x / BH, h = r_bh % H, b = r_bh / H;
-    // segment 0 is seg_len0 tokens (it starts at once, the others after the
-    // segment-state grid), every later one seg_len
-    const int t_begin = (p == 0) ? 0 : seg_len0 + (p - 1) * seg_len;
-    const int t_end = min(N, (p == 0) ? seg_len0 : t_begin + seg_len);
+    const int t_begin = p * seg_len;
+    const int t_end = min(N, t_begin + seg_len);
     const int nchunks = (t_end - t_begin + kC - 1) / kC;
     const size_t bh = (size_t)b * H + h;  // E slots: bh * (P + 1) + q; G: bh * P + q
     // each stage holds Q, K, V of one chunk
@@ -842,7 +839,7 @@ static_assert(kSegSmemBytes <= kTcSmemBytes, "segment-state ring + control block
 __global__ void __launch_bounds__(kSegThreads, 1)
 gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                 const float *__restrict__ logits, float inv_tau, const float *__restrict__ state,
-                float *__restrict__ E, float *__restrict__ G, int *__restrict__ hand, int N, int H, int seg_len0, int seg_len,
+                float *__restrict__ E, float *__restrict__ G, int *__restrict__ hand, int N, int H, int seg_len,
                 int P, int *err) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -850,8 +847,8 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
     SegSmem &sm = *reinterpret_cast<SegSmem *>(tiles + (size_t)kSegStages * 2 * kTile);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int p = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int t_begin = (p == 0) ? 0 : seg_len0 + (p - 1) * seg_len;
-    const int nch = (min(N, (p == 0) ? seg_len0 : t_begin + seg_len) - t_begin + kC - 1) / kC;
+    const int t_begin = p * seg_len;
+    const int nch = (min(N, t_begin + seg_len) - t_begin + kC - 1) / kC;
     const size_t bh = (size_t)b * H + h;
     const size_t bhp = bh * P + p;                 // G slot
     const size_t e_slot = bh * (size_t)(P + 1) + p;  // E slot
@@ -1136,31 +1133,9 @@ static int tc_segments(int B, int N, int H) {
     return P;
 }
 
-// Segment lengths for P segments over N tokens: segment 0 starts while the
-// segment-state grid runs and the others wait for it, so segment 0 takes up to
-// kSeg0Extra chunks more (a measured-time heuristic: the state grid takes about as
-// long as 16-20 output chunks with decaying gates) and the rest share what is left.
-// Returns the segment count actually used (<= P); len0 and len are in tokens.
-constexpr int kSeg0Extra = 16;
-
-static int tc_seg_plan(int N, int P, bool balance, int &len0, int &len) {
+static int tc_seg_len(int N, int P) {
     const int chunks = (N + kC - 1) / kC;
-    if (P <= 1) {
-        len0 = len = chunks * kC;
-        return 1;
-    }
-    const int base = (chunks + P - 1) / P;
-    const int extra = balance ? std::min(base / 2, kSeg0Extra) : 0;
-    const int c0 = std::min(chunks, base + extra);
-    const int rest = chunks - c0;
-    if (rest <= 0) {
-        len0 = len = chunks * kC;
-        return 1;
-    }
-    const int c = (rest + P - 2) / (P - 1);
-    len0 = c0 * kC;
-    len = c * kC;
-    return 1 + (rest + c - 1) / c;
+    return ((chunks + P - 1) / P) * kC;
 }
 
 size_t gret_tc_workspace(int B, int N, int H, int dk, int dv) {
@@ -1180,8 +1155,9 @@ cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaS
     if (!make_map(&mq, a.q, a.B, a.N, a.H) || !make_map(&mk, a.k, a.B, a.N, a.H) || !make_map(&mv, a.v, a.B, a.N, a.H) ||
         !make_map(&mo, a.o, a.B, a.N, a.H))
         return cudaErrorInvalidValue;
-    int seg_len0 = 0, seg_len = 0;
-    int P = tc_seg_plan(a.N, tc_segments(a.B, a.N, a.H), test_hook_value(kHookGretSegments) == 0, seg_len0, seg_len);
+    int P = tc_segments(a.B, a.N, a.H);
+    const int seg_len = tc_seg_len(a.N, P);
+    P = (a.N + seg_len - 1) / seg_len;
     int *err = (int *)ws;
     float *E = (float *)((char *)ws + 256);
     float *G = E + (size_t)a.B * a.H * (P + 1) * kD * kD;
@@ -1199,7 +1175,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaS
     if (P == 1) {
         count_launches(1);
         out_kernel<<<dim3(a.B * a.H), kTcThreads, kTcSmemBytes, st>>>(
-            mq, mk, mv, mo, a.logits, inv_tau, a.state, E, G, nullptr, a.N, a.H, seg_len0, seg_len, 1, err, (uint64_t)0, gate,
+            mq, mk, mv, mo, a.logits, inv_tau, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err, (uint64_t)0, gate,
             gn_w, gn_b, gn_eps);
         return cudaGetLastError();
     }
@@ -1218,7 +1194,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaS
     cfg.blockDim = dim3(kSegThreads);
     cfg.dynamicSmemBytes = kSegSmemBytes;
     e = cudaLaunchKernelEx(&cfg, gret_seg_kernel, mk, mv, a.logits, inv_tau, (const float *)a.state, E, G, hand,
-                           a.N, a.H, seg_len0, seg_len, P, err);
+                           a.N, a.H, seg_len, P, err);
     if (e != cudaSuccess) return e;
     // the output grid starts on the SMs the segment-state grid leaves free: its segment-0 CTAs (first in
     // the grid) run the whole segment meanwhile; the others begin loading and wait
@@ -1227,7 +1203,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaS
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = kTcSmemBytes;
     return cudaLaunchKernelEx(&cfg, out_kernel, mq, mk, mv, mo, a.logits, inv_tau, a.state, E, G, hand, a.N, a.H,
-                              seg_len0, seg_len, P, err, (uint64_t)test_hook_value(kHookGretSeg0DelayNs), gate, gn_w, gn_b,
+                              seg_len, P, err, (uint64_t)test_hook_value(kHookGretSeg0DelayNs), gate, gn_w, gn_b,
                               gn_eps);
 }
 

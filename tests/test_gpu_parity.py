@@ -176,7 +176,7 @@ def test_gret_prefill_bf16_mixed_decay_across_segments(Y):
     """Segments that decay strongly (the backward walk stops after a couple of
     chunks and later segments leave the older states out) next to segments
     with no decay at all (the walk and the fold reach back through them), from
-    an initial state: 24 heads, 61 chunks in 6 segments (segment 0 the longest)."""
+    an initial state: 24 heads, 6 segments of 11 chunks."""
     B, N, H, d = 1, 128 * 60 + 50, 24, 128
     host, dev = gret_inputs(42, B, N, H, d, "bf16", logit_mean=2.0)
     lg = host[3].copy()
