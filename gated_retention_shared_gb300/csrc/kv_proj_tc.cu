@@ -11,8 +11,9 @@
 // and [n, 2n) from W_V (n % 256 == 0, so a 64-column block never straddles the
 // two).  Tiles run row-block major so a block of M is reused from L2 across its
 // column tiles and the 12.6 MB of weights stay L2-resident.  The RMS factors come
-// from the kernel before this one (a programmatic dependency): only the epilogue
-// waits for it, while the loads and MMAs are already running.
+// from the kernel before this one (a programmatic dependency, so this grid is
+// launched while that pass runs); only the epilogue waits for the pass, but the
+// CTAs start as the pass's CTAs leave their SMs, so little runs alongside it.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"

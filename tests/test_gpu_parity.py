@@ -478,6 +478,36 @@ def test_kv_append_tensor_core_3b_width(Y):
     assert rel_l2(host_f64(cache.v), vref) <= BF16_REL_L2
 
 
+def test_kv_append_tensor_core_many_tiles_per_pair(Y):
+    """12040 rows at the 3B width: 48 row blocks x 8 column tiles, so each CTA pair
+    runs about five tiles and both factor buffers of the in-GEMM row norm, and
+    both parities of their barriers, are used several times; the last row block
+    holds 8 rows (its odd CTA none).  Against the oracle on every 7th row and the
+    last 40 (both CTAs of every row block), per tensor and per row block of each
+    kv head."""
+    import torch
+    B, T, dm, Hkv, d = 1, 12040, 3072, 8, 128
+    M, Md = gen(SEED, sid(23, 0, synth.T_M), (B, T, dm), "bf16")
+    Wk, Wkd = gen(SEED, sid(23, 0, synth.T_WK), (dm, Hkv * d), "bf16", std=0.02)
+    Wv, Wvd = gen(SEED, sid(23, 0, synth.T_WV), (dm, Hkv * d), "bf16", std=0.02)
+    cache = Y.KVCache(B, Hkv, d, T)
+    ws = torch.empty(Y.lib.yoco_shared_kv_workspace_size(B, T, dm, ctypes.byref(cache.c)), dtype=torch.uint8,
+                     device="cuda")
+    Y.yoco_shared_kv_project_append(Md, Wkd, Wvd, cache, eps=1e-6, workspace=ws)
+    Y.yoco_workspace_status(ws)
+    assert cache.length == T and int(cache.len_dev[0]) == T and int(cache.len_dev[1]) == 0
+    rows = np.array(sorted(set(range(0, T, 7)) | set(range(T - 40, T))))
+    blocks = rows // 256
+    for W, got in ((Wk, cache.k), (Wv, cache.v)):
+        ref = oracle.rmsnorm_proj(M[0, rows], W, 1e-6).reshape(len(rows), Hkv, d)
+        g = host_f64(got)[0][:, rows].transpose(1, 0, 2)  # [rows, Hkv, d]
+        assert rel_l2(g, ref) <= BF16_REL_L2
+        for blk in np.unique(blocks):
+            sel = blocks == blk
+            for h in range(Hkv):
+                assert rel_l2(g[sel, h], ref[sel, h]) <= BLOCK_REL_L2, (blk, h)
+
+
 def test_kv_append_fp32_and_gain(Y):
     """fp32 cache (tiny config: dm 128 -> one 64-wide head), with an RMSNorm gain."""
     import torch
