@@ -217,9 +217,12 @@ __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.a
 template <int R>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R)); }
 // Registers per thread by warpgroup (launched with 128 each, 512 threads = the whole
-// register file): state 216, decay 120, TMA + MMA 48, epilogue 128; 216 + 120 + 48 +
+// register file): state 216, decay 112, TMA + MMA 56, epilogue 128; 216 + 112 + 56 +
 // 128 = 4 x 128, so the state warpgroup's increase is exactly what the others free.
-constexpr int kRegsState = 216, kRegsDecay = 120, kRegsIssue = 48;
+// With 48 for the TMA producer and the MMA issuer, values of their per-chunk loops
+// lived in local memory, which misses L1 here (shared memory takes nearly all of it),
+// and each reload cost an L2 round trip on the pipeline's critical path.
+constexpr int kRegsState = 216, kRegsDecay = 112, kRegsIssue = 56;
 
 // kGN: the epilogue applies the paper's Eq. 7 output (GroupNorm per head, then the
 // swish gate) and writes z instead of the raw retention output o.
