@@ -217,12 +217,14 @@ __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.a
 template <int R>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R)); }
 // Registers per thread by warpgroup (launched with 128 each, 512 threads = the whole
-// register file): state 216, decay 112, TMA + MMA 56, epilogue 128; 216 + 112 + 56 +
-// 128 = 4 x 128, so the state warpgroup's increase is exactly what the others free.
-// With 48 for the TMA producer and the MMA issuer, values of their per-chunk loops
-// lived in local memory, which misses L1 here (shared memory takes nearly all of it),
-// and each reload cost an L2 round trip on the pipeline's critical path.
-constexpr int kRegsState = 216, kRegsDecay = 112, kRegsIssue = 56;
+// register file): state 216, decay 112, TMA + MMA 64, epilogue 120; 216 + 112 + 64 +
+// 120 = 4 x 128, so the state warpgroup's increase is exactly what the others free
+// (each does its decrease first thing).  With fewer for the TMA producer and the MMA
+// issuer (48 or 56), values of their per-chunk loops lived in local memory, which
+// misses L1 here (shared memory takes nearly all of it), and each reload cost an L2
+// round trip on the pipeline's critical path; this split leaves no spill at all.
+constexpr int kRegsState = 216, kRegsDecay = 112, kRegsIssue = 64, kRegsEpi = 120;
+static_assert(kRegsState + kRegsDecay + kRegsIssue + kRegsEpi == 4 * 128, "the split must use the launch's registers");
 
 // kGN: the epilogue applies the paper's Eq. 7 output (GroupNorm per head, then the
 // swish gate) and writes z instead of the raw retention output o.
@@ -431,6 +433,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
         }
     } else if (warp >= 12) {
+        regs_dec<kRegsEpi>();
         // ----------------------------------------------------- epilogue warps
         // Output rows o_j = e^{b_j} O_j (or O_j in direct chunks), staged as bf16 in
         // the chunk's V slot (free once MMA2 is done); the TMA producer thread stores
