@@ -837,6 +837,7 @@ struct SegSmem {
     int nuse;         // chunks the walk takes (decided by the scale warps' prologue)
     float wsum[2][8];
     float csum[64];   // prologue: total log decay of 64 chunks
+    float lgc[kSegScanChunks][kC];  // prologue's first round: each token's log gate, walk chunks 0-63
 };
 
 constexpr size_t kSegSmemBytes = (size_t)kSegStages * 2 * kTile + sizeof(SegSmem) + 1024;
@@ -978,7 +979,10 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             const int n = n0 + lane + 32 * m;
-                            if (n < N) part[k8] += log_gate(__ldg(logits + ((size_t)b * N + n) * H + h), inv_tau);
+                            const float lgv =
+                                (n < N) ? log_gate(__ldg(logits + ((size_t)b * N + n) * H + h), inv_tau) : 0.f;
+                            part[k8] += lgv;
+                            if (c0 == 0) sm.lgc[c][lane + 32 * m] = lgv;  // the walk reads them back
                         }
                     }
                 }
@@ -1012,12 +1016,15 @@ gret_seg_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant_
             }
         }
         float suffix = 0.f;  // log decay of the chunks after this one
-        float lg_next = (nuse > 0) ? log_gate_at(chunk_at(0)) : 0.f;
+        // walk chunk i's log gate of row r: the prologue kept those of chunks 0-63 (the
+        // whole walk unless the gates barely decay); later ones are read as it goes
+        auto lg_walk = [&](int i) { return i < kSegScanChunks ? sm.lgc[i][r] : log_gate_at(chunk_at(i)); };
+        float lg_next = (nuse > 0) ? lg_walk(0) : 0.f;
         bool alive = true;
         for (int i = 0; i < nuse && alive; ++i) {
             const int s = i % kSegStages;
             float x = lg_next;
-            if (i + 1 < nuse) lg_next = log_gate_at(chunk_at(i + 1));  // in flight during this chunk
+            if (i + 1 < nuse) lg_next = lg_walk(i + 1);  // from shared memory, or in flight during this chunk
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, x, off);
