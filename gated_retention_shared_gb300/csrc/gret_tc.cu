@@ -232,6 +232,7 @@ template <bool kGN>
 __global__ void __launch_bounds__(kTcThreads, 1)
 gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+               const __grid_constant__ CUtensorMap tm_g,
                const float *__restrict__ logits, float inv_tau,
                float *__restrict__ state, float *__restrict__ E, float *__restrict__ G,
                int *__restrict__ hand, int N, int H, int seg_len, int P, int *err, uint64_t seg0_delay_ns,
@@ -316,6 +317,7 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tma_prefetch_desc(&tm_v);
                 tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(&tm_o);
+                if (kGN) tma_prefetch_desc(&tm_g);
                 // every q, k, v line is read once per pass and every o line written once:
                 // all of them are marked first to leave L2 (measured: 0.235 -> 0.221 ms per
                 // 32K x 24 x 128 layer; keeping the segment-state pass's k, v tiles for this
@@ -348,6 +350,9 @@ gret_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     for (int half = 0; half < 2; ++half) {
                         tma_load_4d_hint(stage_k(s) + half * kHalf, &tm_k, &sm.full[s], half * 64, h, n0, b, pol);
                         tma_load_4d_hint(stage_q(s) + half * kHalf, &tm_q, &sm.full[s], half * 64, h, n0, b, pol);
+                        // Eq. 7: the chunk's gate rows into L2, where the epilogue's own row
+                        // loads find them about two chunks from now
+                        if (kGN) tma_prefetch_l2_4d(&tm_g, half * 64, h, n0, b);
                     }
                     if (i >= NS) {
                         if (!store_out(i - NS)) break;
@@ -1164,10 +1169,16 @@ size_t gret_tc_workspace(int B, int N, int H, int dk, int dv) {
 // The chunkwise prefill on the tensor cores.  gn == nullptr: o = the retention
 // output; else o = Eq. 7's z = swish(gate) (.) GroupNorm_h(retention output).
 cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaStream_t st) {
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv, mo, mg;
     if (!make_map(&mq, a.q, a.B, a.N, a.H) || !make_map(&mk, a.k, a.B, a.N, a.H) || !make_map(&mv, a.v, a.B, a.N, a.H) ||
         !make_map(&mo, a.o, a.B, a.N, a.H))
         return cudaErrorInvalidValue;
+    // the gate of Eq. 7 (same layout as q; without it the map is not used)
+    if (gn) {
+        if (!make_map(&mg, gn->gate, a.B, a.N, a.H)) return cudaErrorInvalidValue;
+    } else {
+        mg = mq;
+    }
     int P = tc_segments(a.B, a.N, a.H);
     const int seg_len = tc_seg_len(a.N, P);
     P = (a.N + seg_len - 1) / seg_len;
@@ -1188,7 +1199,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaS
     if (P == 1) {
         count_launches(1);
         out_kernel<<<dim3(a.B * a.H), kTcThreads, kTcSmemBytes, st>>>(
-            mq, mk, mv, mo, a.logits, inv_tau, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err, (uint64_t)0, gate,
+            mq, mk, mv, mo, mg, a.logits, inv_tau, a.state, E, G, nullptr, a.N, a.H, seg_len, 1, err, (uint64_t)0, gate,
             gn_w, gn_b, gn_eps);
         return cudaGetLastError();
     }
@@ -1215,7 +1226,7 @@ cudaError_t gret_prefill_tc(const GretArgs &a, const GnArgs *gn, void *ws, cudaS
     cfg.gridDim = dim3(P * a.B * a.H);
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = kTcSmemBytes;
-    return cudaLaunchKernelEx(&cfg, out_kernel, mq, mk, mv, mo, a.logits, inv_tau, a.state, E, G, hand, a.N, a.H,
+    return cudaLaunchKernelEx(&cfg, out_kernel, mq, mk, mv, mo, mg, a.logits, inv_tau, a.state, E, G, hand, a.N, a.H,
                               seg_len, P, err, (uint64_t)test_hook_value(kHookGretSeg0DelayNs), gate, gn_w, gn_b,
                               gn_eps);
 }
