@@ -429,12 +429,23 @@ def run_gpu(args):
                     + L_CROSS * cross_bytes / (hbm_peak * 1e9)) * 1e3
 
     # ---- end to end: inputs from pinned host memory, results back to host
+    barrier()
     e2e = e2e_measure(args, torch, stream, step, q, k, v, lg, [M] + Qx, Ox)
+    if e2e is not None:  # whole job: every rank's prompts over the slowest rank's time
+        e2e_s = e2e["ms_per_step"] / 1e3 * e2e["steps"]
+        e2e["value"], e2e_s = aggregate_over_ranks(e2e_s, B * N * e2e["steps"], dist, dev)
+        e2e["ms_per_step"] = e2e_s / e2e["steps"] * 1e3
     del q, k, v, lg, M, o
     torch.cuda.empty_cache()
 
     # ---- generation at a 1M-token context
+    barrier()
     decode = decode_1m(args, torch, Y, dev, seed, hbm_peak)
+    if decode is not None:  # whole job: every rank's generated tokens over the slowest rank's time
+        dec_s = decode["ms_per_token"] / 1e3 * decode["tokens"]
+        dec_value, dec_s = aggregate_over_ranks(dec_s, decode["tokens"], dist, dev)
+        decode["value"] = round(dec_value, 2)
+        decode["ms_per_token"] = round(dec_s / decode["tokens"] * 1e3, 4)
 
     clocks = clk.summary(t_lo - 0.1, t_hi + 0.1)
     clocks["window_ms"] = round((t_hi - t_lo) * 1e3, 1)
