@@ -19,9 +19,9 @@
 // a window W > 0, p - W < m.  Only tiles that cross a row's boundary are masked
 // element by element; key tiles outside the CTA's range are skipped.
 //
-// Warps: 0 TMA producer (Q_A, Q_B once, then K/V tiles through a 2-stage ring),
-// 1 MMA issuer, 2-5 softmax + epilogue of set A, 6-9 of set B (thread = TMEM lane
-// = query row).  Tensor-core order per tile: S_A(j), P_B V(j-1), S_B(j), P_A V(j),
+// Warps: 0 TMA producer (Q_A, Q_B once, then K and V tiles through 2-stage rings
+// with barriers of their own), 1 MMA issuer, 2-5 softmax + epilogue of set A, 6-9
+// of set B (thread = TMEM lane = query row).  Tensor-core order per tile: S_A(j), P_B V(j-1), S_B(j), P_A V(j),
 // so softmax A(j) overlaps the B-side MMAs and softmax B(j) the A-side ones.
 // TMEM: S_A 0, O_A 128, S_B 256, O_B 384.  The GQA group's heads are adjacent in
 // the grid, so their K/V tiles are shared through L2.
@@ -47,7 +47,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleGap2 = 8.f * kLog2e;  // reference moves only when passed by more than e^8
 
 struct FaSmem {
-    uint64_t q_full, full[kFStages], empty[kFStages];
+    uint64_t q_full;
+    uint64_t kfull[kFStages], kempty[kFStages], vfull[kFStages], vempty[kFStages];  // K and V slots apart
     uint64_t s_full[2], p_ready[2], pv_done[2];  // per set
     int walive[2][4];                              // per set and softmax warp, after the tile loop
     uint64_t q_rot[2];                           // per set: Q tile turned (rotary encoding) or as loaded
@@ -109,8 +110,10 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (tid == 0) {
         mbar_init(&sm.q_full, 1);
         for (int s = 0; s < kFStages; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], 1);
+            mbar_init(&sm.kfull[s], 1);
+            mbar_init(&sm.kempty[s], 1);
+            mbar_init(&sm.vfull[s], 1);
+            mbar_init(&sm.vempty[s], 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&sm.s_full[x], 1);
@@ -148,27 +151,39 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int x = 0; x < 2; ++x)
                 for (int half = 0; half < 2; ++half)
                     tma_load_4d(sQ + x * kFTile + half * kFHalf, &tm_q, &sm.q_full, half * 64, h, q0 + x * kFK, b);
-            int i = 0;
-            for (; i < ntiles; ++i) {
+            // K(i) reuses the slot of K(i - 2) once both S MMAs of tile i - 2 are done, V(i)
+            // that of V(i - 2) once both P V MMAs are: K is freed a softmax earlier than V
+            int nk = 0, nv = 0;  // tiles whose K / V copy was issued
+            for (int i = 0; i < ntiles; ++i) {
                 const int s = i % kFStages;
-                if (i >= kFStages && !mbar_wait(&sm.empty[s], ((i / kFStages) + 1) & 1, abort_flag)) {
+                const uint32_t par = ((i / kFStages) + 1) & 1;
+                const int key0 = (j_lo + i) * kFK;
+                uint8_t *st = ring + (size_t)s * 2 * kFTile;
+                // K/V as {d, key, kv head, b} (a cache) or {d, kv head, key, b} (token-major)
+                const int c1 = kv_token_major ? hk : key0, c2 = kv_token_major ? key0 : hk;
+                if (i >= kFStages && !mbar_wait(&sm.kempty[s], par, abort_flag)) {
                     fail(31);
                     break;
                 }
-                const int key0 = (j_lo + i) * kFK;
-                uint8_t *st = ring + (size_t)s * 2 * kFTile;
-                mbar_arrive_expect_tx(&sm.full[s], 2 * kFTile);
-                // K/V as {d, key, kv head, b} (a cache) or {d, kv head, key, b} (token-major)
-                const int c1 = kv_token_major ? hk : key0, c2 = kv_token_major ? key0 : hk;
-                for (int half = 0; half < 2; ++half) {
-                    tma_load_4d(st + half * kFHalf, &tm_k, &sm.full[s], half * 64, c1, c2, b);
-                    tma_load_4d(st + kFTile + half * kFHalf, &tm_v, &sm.full[s], half * 64, c1, c2, b);
+                mbar_arrive_expect_tx(&sm.kfull[s], kFTile);
+                for (int half = 0; half < 2; ++half)
+                    tma_load_4d(st + half * kFHalf, &tm_k, &sm.kfull[s], half * 64, c1, c2, b);
+                ++nk;
+                if (i >= kFStages && !mbar_wait(&sm.vempty[s], par, abort_flag)) {
+                    fail(31);
+                    break;
                 }
+                mbar_arrive_expect_tx(&sm.vfull[s], kFTile);
+                for (int half = 0; half < 2; ++half)
+                    tma_load_4d(st + kFTile + half * kFHalf, &tm_v, &sm.vfull[s], half * 64, c1, c2, b);
+                ++nv;
             }
-            // leave no copy in flight
+            // leave no copy in flight (only the last two of each kind can be)
             mbar_wait(&sm.q_full, 0, abort_flag, 200000000ull);
-            for (int k = max(0, i - kFStages); k < i; ++k)
-                mbar_wait(&sm.full[k % kFStages], (k / kFStages) & 1, abort_flag, 200000000ull);
+            for (int k = max(0, nk - kFStages); k < nk; ++k)
+                mbar_wait(&sm.kfull[k % kFStages], (k / kFStages) & 1, abort_flag, 200000000ull);
+            for (int k = max(0, nv - kFStages); k < nv; ++k)
+                mbar_wait(&sm.vfull[k % kFStages], (k / kFStages) & 1, abort_flag, 200000000ull);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------------- MMA
@@ -191,6 +206,8 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 return true;
             };
             auto issue_pv = [&](int x, int i) -> bool {  // O_X += P_X(i) V(i)
+                // set A's P V is the first use of V(i)
+                if (x == 0 && !mbar_wait(&sm.vfull[i % kFStages], (i / kFStages) & 1, abort_flag)) return false;
                 if (!mbar_wait(&sm.p_ready[x], i & 1, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t v_a = smem_u32(ring + (size_t)(i % kFStages) * 2 * kFTile + kFTile);
@@ -202,18 +219,19 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             };
             for (int i = 0; i < ntiles && ok; ++i) {
                 const int s = i % kFStages;
-                if (!(ok = mbar_wait(&sm.full[s], (i / kFStages) & 1, abort_flag))) break;
+                if (!(ok = mbar_wait(&sm.kfull[s], (i / kFStages) & 1, abort_flag))) break;
                 if (!(ok = issue_s(0, i))) break;
                 if (i > 0) {
                     if (!(ok = issue_pv(1, i - 1))) break;
-                    mma_commit(&sm.empty[(i - 1) % kFStages]);  // tile i-1 fully used
+                    mma_commit(&sm.vempty[(i - 1) % kFStages]);  // V(i-1) fully used
                 }
                 if (!(ok = issue_s(1, i))) break;
+                mma_commit(&sm.kempty[s]);  // K(i) fully used
                 if (!(ok = issue_pv(0, i))) break;
             }
             if (ok && ntiles > 0) {
                 ok = issue_pv(1, ntiles - 1);
-                mma_commit(&sm.empty[(ntiles - 1) % kFStages]);
+                mma_commit(&sm.vempty[(ntiles - 1) % kFStages]);
             }
             if (!ok) fail(32);
         }
@@ -292,23 +310,35 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // every row of the set sees every key of this tile: no per-element mask
             const bool full = (key0 + kFK - 1 <= set_lo) && (window <= 0 || key0 >= set_lo + kFK - 1 - window + 1);
             // maximum of the raw scores (the scale is positive: it is applied once, to the
-            // maximum, and folded into each exponent's argument below)
-            float mt = -INFINITY;
+            // maximum, and folded into each exponent's argument below), in four chains
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (full) {
 #pragma unroll
-                for (int c = 0; c < kFK; c += 2) mt = fmax3(mt, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+                for (int c = 0; c < kFK; c += 2)
+                    mq[(c >> 1) & 3] = fmax3(mq[(c >> 1) & 3], __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
             } else {
+                // the keys this row sees form one run [lo_c, hi_c) of the tile, held as 4 x 32 bits
                 const int64_t first = (window > 0) ? pos - window + 1 : 0;
                 const int lo_c = (int)max((int64_t)0, min((int64_t)kFK, first - key0));
                 const int hi_c = (int)max((int64_t)0, min((int64_t)kFK, pos + 1 - key0));
+                uint32_t bits[4];
 #pragma unroll
-                for (int c = 0; c < kFK; ++c) {
-                    const float v = (c >= lo_c && c < hi_c) ? __uint_as_float(sv[c]) : -INFINITY;
-                    sv[c] = __float_as_uint(v);
-                    mt = fmaxf(mt, v);
+                for (int w = 0; w < 4; ++w) {
+                    const int lo = min(max(lo_c - 32 * w, 0), 32), hi = min(max(hi_c - 32 * w, 0), 32);
+                    const uint32_t below_hi = (hi >= 32) ? 0xffffffffu : ((1u << hi) - 1u);
+                    const uint32_t below_lo = (lo >= 32) ? 0xffffffffu : ((1u << lo) - 1u);
+                    bits[w] = below_hi & ~below_lo;
+                }
+#pragma unroll
+                for (int c = 0; c < kFK; c += 2) {
+                    const float v0 = (bits[c >> 5] & (1u << (c & 31))) ? __uint_as_float(sv[c]) : -INFINITY;
+                    const float v1 = (bits[c >> 5] & (2u << (c & 31))) ? __uint_as_float(sv[c + 1]) : -INFINITY;
+                    sv[c] = __float_as_uint(v0);
+                    sv[c + 1] = __float_as_uint(v1);
+                    mq[(c >> 1) & 3] = fmax3(mq[(c >> 1) & 3], v0, v1);
                 }
             }
-            mt *= c2;  // -inf stays -inf
+            const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * c2;  // -inf stays -inf
             // move the reference maximum only when this tile passes it by more than the gap
             float alpha = 1.f;
             const bool move = (mt > m_ref + kRescaleGap2) || (m_ref == -INFINITY && mt > -INFINITY);
