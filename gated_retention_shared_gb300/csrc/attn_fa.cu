@@ -195,12 +195,14 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (i > 0 && !mbar_wait(&sm.pv_done[x], (i - 1) & 1, abort_flag)) return false;
                 if (i == 0 && !mbar_wait(&sm.q_rot[x], 0, abort_flag)) return false;  // Q_X as the MMA reads it
                 tc_fence_after();
-                const uint32_t q_a = smem_u32(sQ + x * kFTile);
-                const uint32_t k_a = smem_u32(ring + (size_t)(i % kFStages) * 2 * kFTile);
+                // descriptors built once and stepped: the address field (bytes / 16, 14 bits)
+                // cannot carry out below 256 KB of shared memory
+                const uint64_t dq = smem_desc_sw128(smem_u32(sQ + x * kFTile), 16, 1024);
+                const uint64_t dk = smem_desc_sw128(smem_u32(ring + (size_t)(i % kFStages) * 2 * kFTile), 16, 1024);
+#pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kFHalf + (kk & 3) * 32;
-                    mma_ss(tmem + 256 * x, smem_desc_sw128(q_a + off, 16, 1024), smem_desc_sw128(k_a + off, 16, 1024),
-                           id_s, kk > 0);
+                    const uint64_t off = ((kk >> 2) * kFHalf + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + 256 * x, dq + off, dk + off, id_s, kk > 0);
                 }
                 mma_commit(&sm.s_full[x]);
                 return true;
@@ -210,10 +212,11 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (x == 0 && !mbar_wait(&sm.vfull[i % kFStages], (i / kFStages) & 1, abort_flag)) return false;
                 if (!mbar_wait(&sm.p_ready[x], i & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t v_a = smem_u32(ring + (size_t)(i % kFStages) * 2 * kFTile + kFTile);
+                const uint64_t dv = smem_desc_sw128(smem_u32(ring + (size_t)(i % kFStages) * 2 * kFTile + kFTile), kFHalf, 1024);
+#pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + 256 * x + 128, tmem + 256 * x + kk * 8, smem_desc_sw128(v_a + kk * 2048, kFHalf, 1024),
-                           id_o, (i > 0 || kk > 0));
+                    mma_ts(tmem + 256 * x + 128, tmem + 256 * x + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), id_o,
+                           (i > 0 || kk > 0));
                 mma_commit(&sm.pv_done[x]);
                 return true;
             };
