@@ -8,8 +8,8 @@
 // tensor cores work on one set while the other set's softmax runs.  Per 128-key
 // tile j and set X:
 //     S_X   = Q_X K_j^T                     (tcgen05, M 128 rows, N 128 keys, TMEM)
-//     P_X   = 2^(c S_X - m)  masked         (softmax warps, bf16 written over S_X)
-//     O_X  += P_X V_j                       (tcgen05, A = P_X from TMEM)
+//     P_X   = 2^(c S_X - m)  masked         (softmax warps, bf16 into shared memory)
+//     O_X  += P_X V_j                       (tcgen05, A = P_X from shared memory)
 // with c = scale * log2(e) and m a per-row reference maximum (base-2 units) that
 // only moves when a tile's maximum passes it by more than 8 / ln 2 (so by e^8);
 // O_X is then rescaled in TMEM once.  Every P value stays below e^8 and the final
@@ -21,9 +21,13 @@
 //
 // Warps: 0 TMA producer (Q_A, Q_B once, then K and V tiles through 2-stage rings
 // with barriers of their own), 1 MMA issuer, 2-5 softmax + epilogue of set A, 6-9
-// of set B (thread = TMEM lane = query row).  Tensor-core order per tile: S_A(j), P_B V(j-1), S_B(j), P_A V(j),
-// so softmax A(j) overlaps the B-side MMAs and softmax B(j) the A-side ones.
-// TMEM: S_A 0, O_A 128, S_B 256, O_B 384.  The GQA group's heads are adjacent in
+// of set B (thread = TMEM lane = query row).  A set's softmax warps read S_X(j)
+// out of TMEM and free it at once, so S_X(j + 1) is computed while they work;
+// the two sets write P in turn into one shared-memory buffer (B's P(j) after
+// P_A V(j), A's P(j + 1) after P_B V(j)).  Tensor-core order per tile:
+// S_A(j + 1), P_A V(j), S_B(j + 1), P_B V(j): each S sits between the P V MMAs.
+// TMEM: S_A 0, O_A 128, S_B 256, O_B 384.  Shared memory: Q_A, Q_B, P, and the
+// K and V rings (224 KB).  The GQA group's heads are adjacent in
 // the grid, so their K/V tiles are shared through L2.
 #include <cudaTypedefs.h>
 
@@ -49,7 +53,7 @@ constexpr float kRescaleGap2 = 8.f * kLog2e;  // reference moves only when passe
 struct FaSmem {
     uint64_t q_full;
     uint64_t kfull[kFStages], kempty[kFStages], vfull[kFStages], vempty[kFStages];  // K and V slots apart
-    uint64_t s_full[2], p_ready[2], pv_done[2];  // per set
+    uint64_t s_full[2], s_free[2], p_ready[2], pv_done[2];  // per set
     int walive[2][4];                              // per set and softmax warp, after the tile loop
     uint64_t q_rot[2];                           // per set: Q tile turned (rotary encoding) or as loaded
     float rope_c[2][64], rope_s[2][64], rope_th[2][64];
@@ -58,7 +62,7 @@ struct FaSmem {
     int go[2];
 };
 
-constexpr size_t kFTileBytes = (size_t)2 * kFTile + (size_t)kFStages * 2 * kFTile;  // Q_A, Q_B + K/V ring
+constexpr size_t kFTileBytes = (size_t)3 * kFTile + (size_t)kFStages * 2 * kFTile;  // Q_A, Q_B, P + K/V rings
 constexpr size_t kFSmem = kFTileBytes + sizeof(FaSmem) + 1024;
 static_assert(kFSmem <= 232448, "flash-attention tiles must fit shared memory");
 
@@ -92,7 +96,8 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *tiles = smem_raw + pad;
     uint8_t *sQ = tiles;                      // Q_A, Q_B (later the output staging tiles)
-    uint8_t *ring = tiles + 2 * kFTile;       // stage s: K at ring + 2 s kFTile, V after it
+    uint8_t *sP = tiles + 2 * kFTile;         // P of one set at a time (A(i), B(i), A(i + 1), ...)
+    uint8_t *ring = tiles + 3 * kFTile;       // stage s: K at ring + 2 s kFTile, V after it
     FaSmem &sm = *reinterpret_cast<FaSmem *>(tiles + kFTileBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x % Hq;
@@ -117,6 +122,7 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&sm.s_full[x], 1);
+            mbar_init(&sm.s_free[x], 4);   // one arrival per softmax warp of the set: S read out
             mbar_init(&sm.p_ready[x], 4);  // one arrival per softmax warp of the set
             mbar_init(&sm.pv_done[x], 1);
             mbar_init(&sm.q_rot[x], 1);
@@ -189,10 +195,12 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // -------------------------------------------------------------- MMA
         if (lane == 0) {
             const uint32_t id_s = idesc_bf16_f32(kFK, kFK, false, false);  // A = Q (K-major), B = K (K-major)
-            const uint32_t id_o = idesc_bf16_f32(kFK, kFD, false, true);   // A = P (TMEM),   B = V (N-major)
+            const uint32_t id_o = idesc_bf16_f32(kFK, kFD, false, true);   // A = P (K-major), B = V (N-major)
             bool ok = mbar_wait(&sm.q_full, 0, abort_flag);
-            auto issue_s = [&](int x, int i) -> bool {  // S_X = Q_X K(i)^T; S_X's TMEM held P_X(i-1)
-                if (i > 0 && !mbar_wait(&sm.pv_done[x], (i - 1) & 1, abort_flag)) return false;
+            // S_X(i) = Q_X K(i)^T into the set's S columns, once the set's softmax warps have
+            // read S_X(i - 1) out of them
+            auto issue_s = [&](int x, int i) -> bool {
+                if (i > 0 && !mbar_wait(&sm.s_free[x], (i - 1) & 1, abort_flag)) return false;
                 if (i == 0 && !mbar_wait(&sm.q_rot[x], 0, abort_flag)) return false;  // Q_X as the MMA reads it
                 tc_fence_after();
                 // descriptors built once and stepped: the address field (bytes / 16, 14 bits)
@@ -207,34 +215,39 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mma_commit(&sm.s_full[x]);
                 return true;
             };
-            auto issue_pv = [&](int x, int i) -> bool {  // O_X += P_X(i) V(i)
+            auto issue_pv = [&](int x, int i) -> bool {  // O_X += P_X(i) V(i), P from shared memory
                 // set A's P V is the first use of V(i)
                 if (x == 0 && !mbar_wait(&sm.vfull[i % kFStages], (i / kFStages) & 1, abort_flag)) return false;
                 if (!mbar_wait(&sm.p_ready[x], i & 1, abort_flag)) return false;
                 tc_fence_after();
+                const uint64_t dp = smem_desc_sw128(smem_u32(sP), 16, 1024);
                 const uint64_t dv = smem_desc_sw128(smem_u32(ring + (size_t)(i % kFStages) * 2 * kFTile + kFTile), kFHalf, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + 256 * x + 128, tmem + 256 * x + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), id_o,
-                           (i > 0 || kk > 0));
+                    mma_ss(tmem + 256 * x + 128, dp + (uint64_t)(((kk >> 2) * kFHalf + (kk & 3) * 32) >> 4),
+                           dv + (uint64_t)((kk * 2048) >> 4), id_o, (i > 0 || kk > 0));
                 mma_commit(&sm.pv_done[x]);
                 return true;
             };
-            for (int i = 0; i < ntiles && ok; ++i) {
-                const int s = i % kFStages;
-                if (!(ok = mbar_wait(&sm.kfull[s], (i / kFStages) & 1, abort_flag))) break;
-                if (!(ok = issue_s(0, i))) break;
-                if (i > 0) {
-                    if (!(ok = issue_pv(1, i - 1))) break;
-                    mma_commit(&sm.vempty[(i - 1) % kFStages]);  // V(i-1) fully used
-                }
-                if (!(ok = issue_s(1, i))) break;
-                mma_commit(&sm.kempty[s]);  // K(i) fully used
-                if (!(ok = issue_pv(0, i))) break;
-            }
+            // S_A(0), S_B(0), then per tile i: S_A(i + 1), P_A V(i), S_B(i + 1), P_B V(i).  Set B
+            // writes P(i) once P_A V(i) is done and set A writes P(i + 1) once P_B V(i) is, so the
+            // two P V MMAs alternate on one buffer, and each S sits between them.
             if (ok && ntiles > 0) {
-                ok = issue_pv(1, ntiles - 1);
-                mma_commit(&sm.vempty[(ntiles - 1) % kFStages]);
+                ok = mbar_wait(&sm.kfull[0], 0, abort_flag) && issue_s(0, 0) && issue_s(1, 0);
+                if (ok) mma_commit(&sm.kempty[0]);  // K(0) fully used
+            }
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const bool next = i + 1 < ntiles;
+                const int s1 = (i + 1) % kFStages;
+                if (next && !(ok = mbar_wait(&sm.kfull[s1], ((i + 1) / kFStages) & 1, abort_flag))) break;
+                if (next && !(ok = issue_s(0, i + 1))) break;
+                if (!(ok = issue_pv(0, i))) break;
+                if (next) {
+                    if (!(ok = issue_s(1, i + 1))) break;
+                    mma_commit(&sm.kempty[s1]);  // K(i + 1) fully used
+                }
+                if (!(ok = issue_pv(1, i))) break;
+                mma_commit(&sm.vempty[i % kFStages]);  // V(i) fully used
             }
             if (!ok) fail(32);
         }
@@ -309,6 +322,10 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) tmem_ld32(s_t + cb * 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * cb));
             tmem_wait_ld();
+            // S is in registers: the MMA may write S(i + 1) over it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.s_free[x]);
             const int64_t key0 = (int64_t)(j_lo + i) * kFK;
             // every row of the set sees every key of this tile: no per-element mask
             const bool full = (key0 + kFK - 1 <= set_lo) && (window <= 0 || key0 >= set_lo + kFK - 1 - window + 1);
@@ -350,31 +367,25 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 m_ref = mt;
             }
             const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;  // a row with nothing seen yet: every p is 0
-            // P as packed bf16 over the first 64 columns of S (keys 2c, 2c+1 in column c; every
-            // S value is already in registers), 32 keys at a time
-            // per key pair: both exponent arguments s c2 - mu in one packed FMA, the row sum
-            // in a packed accumulator (masked scores are -inf and give exactly 0)
+            // P as packed bf16 in registers (keys 2c, 2c+1 in word c): per key pair both exponent
+            // arguments s c2 - mu in one packed FMA, the row sum in a packed accumulator
+            // (masked scores are -inf and give exactly 0)
             const uint64_t c2x2 = f2_pack(c2, c2), nmu2 = f2_pack(-mu, -mu);
             uint64_t acc2 = f2_pack(0.f, 0.f);
+            uint32_t pk[kFK / 2];
 #pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int c2i = 0; c2i < 16; ++c2i) {
-                    float x0, x1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[32 * cb + 2 * c2i]),
-                                             __uint_as_float(sv[32 * cb + 2 * c2i + 1])), c2x2, nmu2), x0, x1);
-                    const float e0 = fa_ex2(x0), e1 = fa_ex2(x1);
-                    acc2 = f2_add(acc2, f2_pack(e0, e1));
-                    pk[c2i] = fa_pack_bf16x2(e0, e1);
-                }
-                tmem_st16(s_t + cb * 16, pk);
+            for (int c = 0; c < kFK / 2; ++c) {
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), c2x2, nmu2),
+                          x0, x1);
+                const float e0 = fa_ex2(x0), e1 = fa_ex2(x1);
+                acc2 = f2_add(acc2, f2_pack(e0, e1));
+                pk[c] = fa_pack_bf16x2(e0, e1);
             }
             float ls0, ls1;
             f2_unpack(acc2, ls0, ls1);
             const float ls = ls0 + ls1;
             l = fmaf(l, alpha, ls);
-            tmem_wait_st();
             // O_X holds tiles < i; rows whose reference moved rescale it before P V of tile i
             // (the whole warp takes part: TMEM loads and stores are warp-wide)
             if (i > 0 && __any_sync(0xffffffffu, move)) {
@@ -398,8 +409,24 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tmem_wait_st();
                 }
             }
+            // the P buffer is free once the other set's last P V has read it: set A's P(i) follows
+            // P_B V(i - 1), set B's P(i) follows P_A V(i)
+            if (x == 1 || i > 0) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(&sm.pv_done[1 - x], (x == 0 ? i - 1 : i) & 1, abort_flag);
+                if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) {
+                    if (lane == 0) fail(37);
+                    alive = false;
+                    break;
+                }
+            }
+#pragma unroll
+            for (int ch = 0; ch < kFK / 8; ++ch)  // 16-byte chunk ch = keys 8 ch .. 8 ch + 7
+                *reinterpret_cast<uint4 *>(sP + fa_tile_chunk(r, ch)) =
+                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            fence_proxy_async_smem();  // P as the tensor cores read it
             tc_fence_before();
-            __syncwarp();  // this warp's rows of P (and rescaled O) are in TMEM
+            __syncwarp();  // this warp's rows of P (and rescaled O) are written
             if (lane == 0) mbar_arrive(&sm.p_ready[x]);
         }
         // the set agrees on going on: a warp that gave up stops the epilogue for all four
