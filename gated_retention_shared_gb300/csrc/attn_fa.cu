@@ -158,31 +158,32 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int half = 0; half < 2; ++half)
                     tma_load_4d(sQ + x * kFTile + half * kFHalf, &tm_q, &sm.q_full, half * 64, h, q0 + x * kFK, b);
             // K(i) reuses the slot of K(i - 2) once both S MMAs of tile i - 2 are done, V(i)
-            // that of V(i - 2) once both P V MMAs are: K is freed a softmax earlier than V
+            // that of V(i - 2) once both P V MMAs are.  The MMAs free K(i - 1)'s slot before
+            // V(i - 2)'s (S_B(i - 1) precedes P_B V(i - 2)), so K runs one tile ahead: K(0),
+            // K(1), V(0), K(2), V(1), ...
             int nk = 0, nv = 0;  // tiles whose K / V copy was issued
-            for (int i = 0; i < ntiles; ++i) {
+            auto load = [&](int i, bool is_v) -> bool {
                 const int s = i % kFStages;
-                const uint32_t par = ((i / kFStages) + 1) & 1;
                 const int key0 = (j_lo + i) * kFK;
-                uint8_t *st = ring + (size_t)s * 2 * kFTile;
+                uint8_t *st = ring + (size_t)s * 2 * kFTile + (is_v ? kFTile : 0);
+                uint64_t *full = is_v ? &sm.vfull[s] : &sm.kfull[s];
                 // K/V as {d, key, kv head, b} (a cache) or {d, kv head, key, b} (token-major)
                 const int c1 = kv_token_major ? hk : key0, c2 = kv_token_major ? key0 : hk;
-                if (i >= kFStages && !mbar_wait(&sm.kempty[s], par, abort_flag)) {
+                if (i >= kFStages &&
+                    !mbar_wait(is_v ? &sm.vempty[s] : &sm.kempty[s], ((i / kFStages) + 1) & 1, abort_flag)) {
                     fail(31);
-                    break;
+                    return false;
                 }
-                mbar_arrive_expect_tx(&sm.kfull[s], kFTile);
+                mbar_arrive_expect_tx(full, kFTile);
                 for (int half = 0; half < 2; ++half)
-                    tma_load_4d(st + half * kFHalf, &tm_k, &sm.kfull[s], half * 64, c1, c2, b);
-                ++nk;
-                if (i >= kFStages && !mbar_wait(&sm.vempty[s], par, abort_flag)) {
-                    fail(31);
-                    break;
-                }
-                mbar_arrive_expect_tx(&sm.vfull[s], kFTile);
-                for (int half = 0; half < 2; ++half)
-                    tma_load_4d(st + kFTile + half * kFHalf, &tm_v, &sm.vfull[s], half * 64, c1, c2, b);
-                ++nv;
+                    tma_load_4d(st + half * kFHalf, is_v ? &tm_v : &tm_k, full, half * 64, c1, c2, b);
+                ++(is_v ? nv : nk);
+                return true;
+            };
+            bool okp = ntiles <= 0 || load(0, false);
+            for (int i = 0; i < ntiles && okp; ++i) {
+                if (i + 1 < ntiles && !(okp = load(i + 1, false))) break;
+                okp = load(i, true);
             }
             // leave no copy in flight (only the last two of each kind can be)
             mbar_wait(&sm.q_full, 0, abort_flag, 200000000ull);
