@@ -53,7 +53,8 @@ constexpr float kRescaleGap2 = 8.f * kLog2e;  // reference moves only when passe
 struct FaSmem {
     uint64_t q_full;
     uint64_t kfull[kFStages], kempty[kFStages], vfull[kFStages], vempty[kFStages];  // K and V slots apart
-    uint64_t s_full[2], s_free[2], p_ready[2], pv_done[2];  // per set
+    uint64_t s_full[2], s_free[2];          // per set
+    uint64_t p_ready[2][2], pv_done[2][2];  // per set and 64-key half of P
     int walive[2][4];                              // per set and softmax warp, after the tile loop
     uint64_t q_rot[2];                           // per set: Q tile turned (rotary encoding) or as loaded
     float rope_c[2][64], rope_s[2][64], rope_th[2][64];
@@ -123,8 +124,10 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int x = 0; x < 2; ++x) {
             mbar_init(&sm.s_full[x], 1);
             mbar_init(&sm.s_free[x], 4);   // one arrival per softmax warp of the set: S read out
-            mbar_init(&sm.p_ready[x], 4);  // one arrival per softmax warp of the set
-            mbar_init(&sm.pv_done[x], 1);
+            for (int hh = 0; hh < 2; ++hh) {
+                mbar_init(&sm.p_ready[x][hh], 4);  // one arrival per softmax warp of the set
+                mbar_init(&sm.pv_done[x][hh], 1);
+            }
             mbar_init(&sm.q_rot[x], 1);
         }
         sm.abort_flag = 0;
@@ -219,15 +222,21 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             auto issue_pv = [&](int x, int i) -> bool {  // O_X += P_X(i) V(i), P from shared memory
                 // set A's P V is the first use of V(i)
                 if (x == 0 && !mbar_wait(&sm.vfull[i % kFStages], (i / kFStages) & 1, abort_flag)) return false;
-                if (!mbar_wait(&sm.p_ready[x], i & 1, abort_flag)) return false;
-                tc_fence_after();
                 const uint64_t dp = smem_desc_sw128(smem_u32(sP), 16, 1024);
                 const uint64_t dv = smem_desc_sw128(smem_u32(ring + (size_t)(i % kFStages) * 2 * kFTile + kFTile), kFHalf, 1024);
+                // by 64-key halves of P: each half's MMAs go as soon as the set has written it,
+                // and its barrier tells the other set when that half of the buffer is free
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!mbar_wait(&sm.p_ready[x][hh], i & 1, abort_flag)) return false;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + 256 * x + 128, dp + (uint64_t)(((kk >> 2) * kFHalf + (kk & 3) * 32) >> 4),
-                           dv + (uint64_t)((kk * 2048) >> 4), id_o, (i > 0 || kk > 0));
-                mma_commit(&sm.pv_done[x]);
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const int kk = 4 * hh + k4;
+                        mma_ss(tmem + 256 * x + 128, dp + (uint64_t)((hh * kFHalf + k4 * 32) >> 4),
+                               dv + (uint64_t)((kk * 2048) >> 4), id_o, (i > 0 || kk > 0));
+                    }
+                    mma_commit(&sm.pv_done[x][hh]);
+                }
                 return true;
             };
             // S_A(0), S_B(0), then per tile i: S_A(i + 1), P_A V(i), S_B(i + 1), P_B V(i).  Set B
@@ -391,7 +400,7 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // (the whole warp takes part: TMEM loads and stores are warp-wide)
             if (i > 0 && __any_sync(0xffffffffu, move)) {
                 bool ok = true;
-                if (lane == 0) ok = mbar_wait(&sm.pv_done[x], (i - 1) & 1, abort_flag);
+                if (lane == 0) ok = mbar_wait(&sm.pv_done[x][1], (i - 1) & 1, abort_flag);  // all of P V(i - 1)
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) {
                     if (lane == 0) fail(34);
@@ -410,25 +419,35 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tmem_wait_st();
                 }
             }
-            // the P buffer is free once the other set's last P V has read it: set A's P(i) follows
-            // P_B V(i - 1), set B's P(i) follows P_A V(i)
-            if (x == 1 || i > 0) {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait(&sm.pv_done[1 - x], (x == 0 ? i - 1 : i) & 1, abort_flag);
-                if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) {
-                    if (lane == 0) fail(37);
-                    alive = false;
-                    break;
-                }
-            }
+            // each 64-key half of the P buffer is free once the other set's P V has read that
+            // half: set A's P(i) follows P_B V(i - 1), set B's P(i) follows P_A V(i)
+            bool okb = true;
 #pragma unroll
-            for (int ch = 0; ch < kFK / 8; ++ch)  // 16-byte chunk ch = keys 8 ch .. 8 ch + 7
-                *reinterpret_cast<uint4 *>(sP + fa_tile_chunk(r, ch)) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            fence_proxy_async_smem();  // P as the tensor cores read it
-            tc_fence_before();
-            __syncwarp();  // this warp's rows of P (and rescaled O) are written
-            if (lane == 0) mbar_arrive(&sm.p_ready[x]);
+            for (int hh = 0; hh < 2; ++hh) {
+                if (x == 1 || i > 0) {
+                    bool ok = true;
+                    if (lane == 0) ok = mbar_wait(&sm.pv_done[1 - x][hh], (x == 0 ? i - 1 : i) & 1, abort_flag);
+                    if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) {
+                        okb = false;
+                        break;
+                    }
+                }
+#pragma unroll
+                for (int c8 = 0; c8 < kFK / 16; ++c8) {  // 16-byte chunk ch = keys 8 ch .. 8 ch + 7
+                    const int ch = hh * (kFK / 16) + c8;
+                    *reinterpret_cast<uint4 *>(sP + fa_tile_chunk(r, ch)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                }
+                fence_proxy_async_smem();  // P as the tensor cores read it
+                tc_fence_before();
+                __syncwarp();  // this warp's rows of this half of P (and rescaled O) are written
+                if (lane == 0) mbar_arrive(&sm.p_ready[x][hh]);
+            }
+            if (!okb) {
+                if (lane == 0) fail(37);
+                alive = false;
+                break;
+            }
         }
         // the set agrees on going on: a warp that gave up stops the epilogue for all four
         if (lane == 0) sm.walive[x][q4] = alive ? 1 : 0;
@@ -437,7 +456,7 @@ attn_fa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // epilogue: o = O / l as bf16, staged in this set's Q tile (free: every S MMA is done)
         if (alive && ntiles > 0) {
             if (r == 0) {
-                const bool ok = mbar_wait(&sm.pv_done[x], (ntiles - 1) & 1, abort_flag);
+                const bool ok = mbar_wait(&sm.pv_done[x][1], (ntiles - 1) & 1, abort_flag);
                 if (!ok) fail(35);
                 sm.go[x] = ok && !*abort_flag;
             }
