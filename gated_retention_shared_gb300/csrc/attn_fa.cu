@@ -24,7 +24,8 @@
 // of set B (thread = TMEM lane = query row).  A set's softmax warps read S_X(j)
 // out of TMEM and free it at once, so S_X(j + 1) is computed while they work;
 // the two sets write P in turn into one shared-memory buffer (B's P(j) after
-// P_A V(j), A's P(j + 1) after P_B V(j)).  Tensor-core order per tile:
+// P_A V(j), A's P(j + 1) after P_B V(j)), each 64-key half as soon as the other
+// set's MMAs have read that half.  Tensor-core order per tile:
 // S_A(j + 1), P_A V(j), S_B(j + 1), P_B V(j): each S sits between the P V MMAs.
 // TMEM: S_A 0, O_A 128, S_B 256, O_B 384.  Shared memory: Q_A, Q_B, P, and the
 // K and V rings (224 KB).  The GQA group's heads are adjacent in
