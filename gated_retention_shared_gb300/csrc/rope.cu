@@ -15,8 +15,8 @@
 namespace yoco {
 
 // Thread = one 16-byte chunk position of a head row (fixed pairs i), looping over
-// the block's rows and heads with 32-bit indices: the chunk's base angles and
-// frequencies stay in registers.
+// the block's rows and heads with 32-bit indices, four items' loads issued before
+// their arithmetic: the chunk's base angles and frequencies stay in registers.
 constexpr int kRopeRows = 32;  // rows per CTA of rope_apply_kernel
 
 template <typename T, int D>
@@ -37,34 +37,45 @@ __global__ void __launch_bounds__(256) rope_apply_kernel(T *x, int N, int H, int
     const int items = rows * H;
     if (!YOCO_DCHECK(n0 < N && b < (int)gridDim.y, 0x5D)) return;
     T *xb = x + ((size_t)b * N + n0) * H * D + ch * EV;
-    for (int it = threadIdx.x / CH; it < items; it += STEP) {
-        const int j = it / H;  // row offset inside the block (item = j * H + h)
-        uint4 *p = reinterpret_cast<uint4 *>(xb + (size_t)it * D);
-        uint4 u = *p;
-        float c[PC], s[PC];
+    constexpr int U = 4;  // items of a thread in flight at once, loads first
+    for (int it0 = threadIdx.x / CH; it0 < items; it0 += U * STEP) {
+        uint4 uu[U];
 #pragma unroll
-        for (int q = 0; q < PC; ++q) {
-            float cj, sj;
-            rope_cs_offset(j, th[q], cj, sj);
-            rope_cs_add(bc[q], bs[q], cj, sj, c[q], s[q]);
+        for (int k = 0; k < U; ++k) {
+            const int it = it0 + k * STEP;
+            if (it < items) uu[k] = *reinterpret_cast<const uint4 *>(xb + (size_t)it * D);
         }
-        if constexpr (sizeof(T) == 2) {
-            uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float x0 = __uint_as_float(w[q] << 16), x1 = __uint_as_float(w[q] & 0xFFFF0000u);
-                rope_turn(x0, x1, c[q], s[q]);
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
-                w[q] = *reinterpret_cast<uint32_t *>(&h2);
+        for (int k = 0; k < U; ++k) {
+            const int it = it0 + k * STEP;
+            if (it >= items) break;
+            const int j = it / H;  // row offset inside the block (item = j * H + h)
+            uint4 u = uu[k];
+            float c[PC], s[PC];
+#pragma unroll
+            for (int q = 0; q < PC; ++q) {
+                float cj, sj;
+                rope_cs_offset(j, th[q], cj, sj);
+                rope_cs_add(bc[q], bs[q], cj, sj, c[q], s[q]);
             }
-            u = make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
-            float f[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
+            if constexpr (sizeof(T) == 2) {
+                uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int q = 0; q < 2; ++q) rope_turn(f[2 * q], f[2 * q + 1], c[q], s[q]);
-            u = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+                for (int q = 0; q < 4; ++q) {
+                    float x0 = __uint_as_float(w[q] << 16), x1 = __uint_as_float(w[q] & 0xFFFF0000u);
+                    rope_turn(x0, x1, c[q], s[q]);
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+                    w[q] = *reinterpret_cast<uint32_t *>(&h2);
+                }
+                u = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+                float f[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
+#pragma unroll
+                for (int q = 0; q < 2; ++q) rope_turn(f[2 * q], f[2 * q + 1], c[q], s[q]);
+                u = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+            }
+            *reinterpret_cast<uint4 *>(xb + (size_t)it * D) = u;
         }
-        *p = u;
     }
 }
 
